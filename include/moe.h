@@ -1,0 +1,210 @@
+/*
+ * libmoe — routed-expert MLP (grouped GEMM over ragged per-expert token
+ * groups), forward and backward, for one NVIDIA GB300 (sm_103a).
+ *
+ * Sources, cited by page title and section:
+ *   [FK] "Improving MoE training throughput with advanced fused kernels"
+ *        (高度な融合カーネルによる MoE 学習スループットの向上):
+ *        "Overcoming training bottlenecks in the MoE block",
+ *        "Optimizing GLU activations with fused GEMM epilogues" (Figure 2),
+ *        "Eliminating host-device synchronisation and CPU launch overhead",
+ *        "Reducing exposed memory overhead by fusing MXFP8 and NVFP4
+ *        quantization", "From kernel-level gains to end-to-end pretraining
+ *        speedups".
+ *   [DL] "Accelerating dropless MoE training with JAX and NVIDIA Transformer
+ *        Engine", "Claims and evidence" (grouped GEMM over ragged tensors).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Notation: T tokens, E experts, k experts per token, d model width, F GLU
+ * half width (FC1: d -> 2F, FC2: F -> d), R = T*k routed rows.
+ *
+ * Row layout ("ragged tensor", [DL]): routed rows are stored expert after
+ * expert.  Expert e's group starts at padded_offsets[e], a multiple of
+ * desc->align (128), and holds counts[e] rows in ascending token order; the
+ * rows up to padded_offsets[e+1] are padding and every per-row tensor the
+ * library writes is zero there.  Per-row buffers hold `capacity` rows, with
+ * capacity >= T*k + E*(align-1) (any routing fits; no overflow is possible).
+ *
+ * FC1 weights are used "repacked" ([FK] GLU section, Figure 2): logical
+ * w1 [E,2F,d] (rows 0..F-1 gate, F..2F-1 linear) becomes w1p [E,2F_pad,d]
+ * whose row block b (256 rows) holds gate rows 128b..128b+127 then linear
+ * rows 128b..128b+127; F_pad = F rounded up to 128, padding rows zero.  So
+ * one 256-column output tile carries both halves of 128 GLU features.
+ * b1p and every FC1-shaped output (h, dh, dw1p, db1p) use the same packed
+ * column order.
+ *
+ * All tensors are row-major, bf16 unless stated.  All pointers are DEVICE
+ * pointers (the caller allocates and owns every buffer; the library never
+ * allocates, frees or synchronises, and reads no device data on the host),
+ * so every call can be captured in a CUDA graph.  Calls are asynchronous on
+ * `stream`.
+ *
+ * Errors: host-detectable problems (null pointer, bad shape, unsupported
+ * option, workspace too small, device not sm_103) return a non-zero status
+ * and enqueue nothing.  Problems only visible on the device (inconsistent
+ * offsets, expert index out of range, an internal wait that ran out) set a
+ * sticky device status word and the affected work is skipped; read it with
+ * moe_read_device_status() outside any graph.  CUDA launch failures return
+ * MOE_ERR_CUDA.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_NULL = 1,         /* a required pointer is NULL */
+  MOE_ERR_SHAPE = 2,        /* sizes out of the supported range */
+  MOE_ERR_UNSUPPORTED = 3,  /* option not implemented */
+  MOE_ERR_WORKSPACE = 4,    /* workspace smaller than moe_workspace_size() */
+  MOE_ERR_ARCH = 5,         /* current device is not sm_103 */
+  MOE_ERR_CUDA = 6,         /* a CUDA runtime/driver call failed */
+  MOE_ERR_DEVICE = 7        /* sticky device status word is set */
+} moe_status_t;
+
+/* Device status bits (OR-ed into the sticky word). */
+#define MOE_DEV_BAD_OFFSETS 0x1   /* offsets not monotone or past capacity */
+#define MOE_DEV_BAD_EXPERT  0x2   /* expert index outside [0,E) */
+#define MOE_DEV_TIMEOUT     0x4   /* an in-kernel wait ran past its limit */
+
+typedef enum { MOE_DTYPE_BF16 = 1 } moe_dtype_t;
+
+/* GLU activations ([FK] "Overcoming training bottlenecks": SwiGLU, GeGLU,
+ * sReLU with optional clamp and scaling).  With g the gate half, l the
+ * linear half, g' = min(g, limit), l' = clamp(l, -limit, limit):
+ *   SWIGLU: A = s * g' * sigmoid(alpha*g') * (l' + linear_offset)
+ *   GEGLU:  A = s * 0.5*g'*(1+erf(g'/sqrt2)) * (l' + linear_offset)
+ *   SREGLU: A = s * max(g',0)^2 * (l' + linear_offset)   (gated squared ReLU)
+ * where s = out_scale.  alpha applies to SWIGLU only. */
+typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU = 1, MOE_ACT_SREGLU = 3 } moe_act_t;
+
+typedef struct {
+  int32_t T;            /* tokens (routing calls; 0 when groups come directly) */
+  int32_t E;            /* experts, 1..256 */
+  int32_t k;            /* experts per token, 1..min(E,32) */
+  int32_t d;            /* model width, multiple of 64 */
+  int32_t F;            /* GLU half width, multiple of 32 */
+  int32_t dtype;        /* MOE_DTYPE_BF16 */
+  int32_t act;          /* moe_act_t */
+  float alpha;          /* SwiGLU gate scale (1 = plain SiLU) */
+  float limit;          /* clamp limit; +inf disables */
+  float linear_offset;  /* added to the linear half (0 = plain GLU) */
+  float out_scale;      /* scales the activation output */
+  int32_t has_b1;       /* FC1 bias present */
+  int32_t has_b2;       /* FC2 bias present */
+  int32_t align;        /* group alignment in rows: must be 128 */
+  int32_t sm_margin;    /* SMs left free for concurrent kernels ([FK] "From
+                           kernel-level gains...": configurable margin) */
+  int32_t capacity;     /* rows allocated in every per-row buffer */
+} moe_mlp_desc_t;
+
+/* F_pad = F rounded up to 128 (packed FC1 width is 2*F_pad). */
+int32_t moe_fc1_padded_width(int32_t F);
+
+/* Bytes of scratch `ws` the calls below need for this descriptor. */
+moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes);
+
+/* FC1 weight repack ([FK] GLU section, Figure 2: input and gate columns
+ * interleaved so one thread block owns half a tile of each; done once, e.g.
+ * at checkpoint load).  w1 [E,2F,d], b1 [E,2F] or NULL -> w1p [E,2F_pad,d],
+ * b1p [E,2F_pad] (NULL allowed iff b1 is NULL).  Bit-exact permutation. */
+moe_status_t moe_repack_fc1(const moe_mlp_desc_t* desc, const void* w1, const void* b1,
+                            void* w1p, void* b1p, cudaStream_t stream);
+/* Inverse of moe_repack_fc1 for a packed [E,2F_pad,d] tensor (e.g. dW1p);
+ * also for a packed [E,2F_pad] bias when d is given as 1 in `rows_width`. */
+moe_status_t moe_unpack_fc1(const moe_mlp_desc_t* desc, const void* w1p, void* w1,
+                            int32_t rows_width, cudaStream_t stream);
+
+/* Routing and permutation ([FK] "Overcoming training bottlenecks": tokens
+ * per expert are computed at run time; "Eliminating host-device
+ * synchronisation": the group sizes stay in GPU memory; [DL]: ragged groups).
+ *   logits fp32 [T,E]; bias fp32 [E] or NULL (selection only);  x [T,d].
+ * Selection: the k largest of logits+bias (fp32), equal scores to the lower
+ * expert, slots in descending score.  Weights: softmax of the selected raw
+ * logits.  Outputs: topk_idx i32 [T,k], topk_w fp32 [T,k], counts i32 [E],
+ * offsets i32 [E+1], padded_offsets i32 [E+1], tile_prefix i32 [E+1]
+ * (prefix of ceil(counts/128)), row_src i32 [capacity] (token of each row,
+ * -1 on padding), row_of i32 [T,k], x_perm [capacity,d].
+ * ws: moe_workspace_size() bytes. */
+moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
+                               const float* bias, const void* x, int32_t* topk_idx,
+                               float* topk_w, int32_t* counts, int32_t* offsets,
+                               int32_t* padded_offsets, int32_t* tile_prefix,
+                               int32_t* row_src, int32_t* row_of, void* x_perm,
+                               void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Offsets for groups whose sizes are given directly (no router): counts i32
+ * [E] -> offsets, padded_offsets, tile_prefix i32 [E+1]. */
+moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts,
+                               int32_t* offsets, int32_t* padded_offsets,
+                               int32_t* tile_prefix, cudaStream_t stream);
+
+/* Expert MLP forward: FC1 grouped GEMM with the GLU epilogue (bias, clamp,
+ * scale fused; [FK] GLU section) then FC2 grouped GEMM (+b2).
+ *   x_perm [capacity,d]; counts [E]; padded_offsets [E+1];
+ *   w1p [E,2F_pad,d]; b1p [E,2F_pad] or NULL; w2 [E,d,F]; b2 [E,d] or NULL.
+ * Outputs: h [capacity,2F_pad] (FC1 output incl. bias, packed; saved for the
+ * backward), a [capacity,F] (GLU output), y [capacity,d].
+ * Persistent tcgen05 kernels read the group sizes from device memory. */
+moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
+                         const int32_t* counts, const int32_t* padded_offsets,
+                         const void* w1p, const void* b1p, const void* w2, const void* b2,
+                         void* h, void* a, void* y, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
+
+/* Weighted combine: out[t] = sum_s topk_w[t,s] * y[row_of[t,s]] (fp32 sum in
+ * slot order, then bf16).  out [T,d]. */
+moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
+                                   const int32_t* row_of, const float* topk_w, void* out,
+                                   cudaStream_t stream);
+
+/* Backward of the combine: dy[row_of[t,s]] = topk_w[t,s]*dout[t] (bf16,
+ * padding rows zero) and dw[t,s] = <dout[t], y[row_of[t,s]]> (fp32).
+ * row_src/padded_offsets locate the padding rows. */
+moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* dout,
+                                       const void* y, const int32_t* row_of,
+                                       const float* topk_w, const int32_t* row_src,
+                                       const int32_t* padded_offsets, void* dy, float* dw,
+                                       cudaStream_t stream);
+
+/* Expert MLP backward: FC2 dgrad with the dGLU epilogue ([FK] GLU section:
+ * the epilogue reads the GEMM output and computes dSwiGLU) -> dh
+ * [capacity,2F_pad] packed; FC2 wgrad dw2 [E,d,F] = sum over the group's
+ * rows of dy^T a; FC1 dgrad dx_perm [capacity,d] = dh w1p; FC1 wgrad
+ * dw1p [E,2F_pad,d] = dh^T x_perm (packed); db1p [E,2F_pad] and db2 [E,d]
+ * (NULL when the bias is absent).  Experts with no rows get zero gradients. */
+moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
+                         const void* h, const void* a, const int32_t* counts,
+                         const int32_t* padded_offsets, const void* w1p, const void* w2,
+                         void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
+                         void* db2, void* ws, size_t ws_bytes, cudaStream_t stream);
+
+/* Backward of the permutation: dx[t] = sum_s dx_perm[row_of[t,s]] (fp32 in
+ * slot order, then bf16).  dx [T,d]. */
+moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
+                             const int32_t* row_of, void* dx, cudaStream_t stream);
+
+/* Backward of the routing softmax: dlogits fp32 [T,E] with
+ * dlogits[t,idx[t,s]] = w[t,s]*(dw[t,s] - sum_s' w[t,s']*dw[t,s']), 0 elsewhere. */
+moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const float* topk_w,
+                           const int32_t* topk_idx, float* dlogits, cudaStream_t stream);
+
+/* Read (and optionally clear) the sticky device status word of the current
+ * device.  Synchronises the device; call outside stream capture. */
+moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear);
+
+/* Static description of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_H_ */

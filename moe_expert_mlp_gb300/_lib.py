@@ -1,0 +1,183 @@
+"""ctypes binding of libmoe (include/moe.h).
+
+Argument marshalling only: every function here has the name of the C entry
+point it calls, turns torch tensors into device pointers and the current
+torch stream into a cudaStream_t, and raises on a non-zero status.  All
+computation happens in the library's CUDA kernels.  There is no fallback:
+if libmoe.so is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libmoe.so")
+
+MOE_DTYPE_BF16 = 1
+ACTS = {"swiglu": 0, "geglu": 1, "sreglu": 3}
+
+EXPORTS = (
+    "moe_fc1_padded_width", "moe_workspace_size", "moe_repack_fc1", "moe_unpack_fc1",
+    "moe_route_permute", "moe_group_offsets", "moe_mlp_fwd", "moe_unpermute_combine",
+    "moe_unpermute_combine_bwd", "moe_mlp_bwd", "moe_permute_bwd", "moe_route_bwd",
+    "moe_read_device_status", "moe_status_string",
+)
+
+
+class MoeError(RuntimeError):
+    pass
+
+
+class moe_mlp_desc_t(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int32), ("E", ctypes.c_int32), ("k", ctypes.c_int32),
+        ("d", ctypes.c_int32), ("F", ctypes.c_int32), ("dtype", ctypes.c_int32),
+        ("act", ctypes.c_int32), ("alpha", ctypes.c_float), ("limit", ctypes.c_float),
+        ("linear_offset", ctypes.c_float), ("out_scale", ctypes.c_float),
+        ("has_b1", ctypes.c_int32), ("has_b2", ctypes.c_int32), ("align", ctypes.c_int32),
+        ("sm_margin", ctypes.c_int32), ("capacity", ctypes.c_int32),
+    ]
+
+
+def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_offset=0.0,
+              out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0, capacity=None):
+    if capacity is None:
+        capacity = T * k + E * 127
+        capacity = (capacity + 127) // 128 * 128
+    return moe_mlp_desc_t(T, E, k, d, F, MOE_DTYPE_BF16, ACTS[act], alpha, limit, linear_offset,
+                          out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity)
+
+
+_lib = None
+
+
+def lib():
+    """Load libmoe.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise MoeError(f"{LIB_PATH} is not built; run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        D = ctypes.POINTER(moe_mlp_desc_t)
+        sig = {
+            "moe_fc1_padded_width": (ctypes.c_int32, [ctypes.c_int32]),
+            "moe_workspace_size": (ctypes.c_int, [D, ctypes.POINTER(ctypes.c_size_t)]),
+            "moe_repack_fc1": (ctypes.c_int, [D, P, P, P, P, P]),
+            "moe_unpack_fc1": (ctypes.c_int, [D, P, P, ctypes.c_int32, P]),
+            "moe_route_permute": (ctypes.c_int, [D] + [P] * 13 + [ctypes.c_size_t, P]),
+            "moe_group_offsets": (ctypes.c_int, [D, P, P, P, P, P]),
+            "moe_mlp_fwd": (ctypes.c_int, [D] + [P] * 11 + [ctypes.c_size_t, P]),
+            "moe_unpermute_combine": (ctypes.c_int, [D, P, P, P, P, P]),
+            "moe_unpermute_combine_bwd": (ctypes.c_int, [D] + [P] * 8 + [P]),
+            "moe_mlp_bwd": (ctypes.c_int, [D] + [P] * 15 + [ctypes.c_size_t, P]),
+            "moe_permute_bwd": (ctypes.c_int, [D, P, P, P, P]),
+            "moe_route_bwd": (ctypes.c_int, [D, P, P, P, P, P]),
+            "moe_read_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]),
+            "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("expected a torch tensor")
+    if not t.is_cuda or not t.is_contiguous():
+        raise ValueError("tensors passed to libmoe must be contiguous CUDA tensors")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(st):
+    if st != 0:
+        msg = lib().moe_status_string(st).decode()
+        raise MoeError(f"libmoe status {st}: {msg}")
+
+
+def moe_fc1_padded_width(F):
+    return int(lib().moe_fc1_padded_width(F))
+
+
+def moe_workspace_size(desc):
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_workspace_size(ctypes.byref(desc), ctypes.byref(n)))
+    return int(n.value)
+
+
+def moe_repack_fc1(desc, w1, b1, w1p, b1p, stream=None):
+    _check(lib().moe_repack_fc1(ctypes.byref(desc), _p(w1), _p(b1), _p(w1p), _p(b1p), _stream(stream)))
+
+
+def moe_unpack_fc1(desc, w1p, w1, rows_width, stream=None):
+    _check(lib().moe_unpack_fc1(ctypes.byref(desc), _p(w1p), _p(w1), rows_width, _stream(stream)))
+
+
+def moe_route_permute(desc, logits, bias, x, topk_idx, topk_w, counts, offsets, padded_offsets,
+                      tile_prefix, row_src, row_of, x_perm, ws, stream=None):
+    _check(lib().moe_route_permute(
+        ctypes.byref(desc), _p(logits), _p(bias), _p(x), _p(topk_idx), _p(topk_w), _p(counts),
+        _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of), _p(x_perm),
+        _p(ws), ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def moe_group_offsets(desc, counts, offsets, padded_offsets, tile_prefix, stream=None):
+    _check(lib().moe_group_offsets(ctypes.byref(desc), _p(counts), _p(offsets), _p(padded_offsets),
+                                   _p(tile_prefix), _stream(stream)))
+
+
+def moe_mlp_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, w2, b2, h, a, y, ws=None,
+                stream=None):
+    _check(lib().moe_mlp_fwd(
+        ctypes.byref(desc), _p(x_perm), _p(counts), _p(padded_offsets), _p(w1p), _p(b1p), _p(w2),
+        _p(b2), _p(h), _p(a), _p(y), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        _stream(stream)))
+
+
+def moe_unpermute_combine(desc, y, row_of, topk_w, out, stream=None):
+    _check(lib().moe_unpermute_combine(ctypes.byref(desc), _p(y), _p(row_of), _p(topk_w), _p(out),
+                                       _stream(stream)))
+
+
+def moe_unpermute_combine_bwd(desc, dout, y, row_of, topk_w, row_src, padded_offsets, dy, dw,
+                              stream=None):
+    _check(lib().moe_unpermute_combine_bwd(
+        ctypes.byref(desc), _p(dout), _p(y), _p(row_of), _p(topk_w), _p(row_src),
+        _p(padded_offsets), _p(dy), _p(dw), _stream(stream)))
+
+
+def moe_mlp_bwd(desc, dy, x_perm, h, a, counts, padded_offsets, w1p, w2, dh, dx_perm, dw1p, db1p,
+                dw2, db2, ws=None, stream=None):
+    _check(lib().moe_mlp_bwd(
+        ctypes.byref(desc), _p(dy), _p(x_perm), _p(h), _p(a), _p(counts), _p(padded_offsets),
+        _p(w1p), _p(w2), _p(dh), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2), _p(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def moe_permute_bwd(desc, dx_perm, row_of, dx, stream=None):
+    _check(lib().moe_permute_bwd(ctypes.byref(desc), _p(dx_perm), _p(row_of), _p(dx), _stream(stream)))
+
+
+def moe_route_bwd(desc, dw, topk_w, topk_idx, dlogits, stream=None):
+    _check(lib().moe_route_bwd(ctypes.byref(desc), _p(dw), _p(topk_w), _p(topk_idx), _p(dlogits),
+                               _stream(stream)))
+
+
+def moe_read_device_status(clear=True):
+    v = ctypes.c_int32(0)
+    _check(lib().moe_read_device_status(ctypes.byref(v), int(clear)))
+    return int(v.value)

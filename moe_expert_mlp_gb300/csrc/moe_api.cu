@@ -1,0 +1,438 @@
+// C-ABI entry points of libmoe: argument checks, TMA tensor-map encoding
+// and kernel launches.  See include/moe.h for the contract of each call.
+//
+// Nothing here allocates device memory, synchronises, or reads device data
+// on the host (except moe_read_device_status, which exists to do exactly
+// that outside any graph), so every call can be captured in a CUDA graph
+// ("Improving MoE training throughput with advanced fused kernels",
+// "Eliminating host-device synchronisation and CPU launch overhead").
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+// Sticky device status word (one per device that loaded the library).
+__device__ int g_status_word;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+  bool ready = false;
+  int sms = 0;
+  int major = 0, minor = 0;
+  int* status = nullptr;
+};
+
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+moe_status_t device_info(DeviceInfo** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  DeviceInfo& di = g_dev[dev];
+  if (!di.ready) {
+    if (cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&di.minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) return MOE_ERR_CUDA;
+    di.status = static_cast<int*>(p);
+    if (!g_encode) {
+      cudaDriverEntryPointQueryResult q;
+      void* fn = nullptr;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return MOE_ERR_CUDA;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    di.ready = true;
+  }
+  if (di.major != 10 || di.minor != 3) return MOE_ERR_ARCH;
+  *out = &di;
+  return MOE_OK;
+}
+
+// 3-D bf16 tensor map with 128-byte swizzle.  dims innermost first; the
+// innermost dimension is contiguous; row_bytes / plane_bytes are the strides
+// of dims 1 and 2.  Out-of-range box elements read as zero.
+bool encode_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1) {
+  if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes & 15) || (plane_bytes & 15))
+    return false;
+  cuuint64_t dims[3] = {d0, d1, d2};
+  cuuint64_t strides[2] = {row_bytes, plane_bytes};
+  cuuint32_t box[3] = {box0, box1, 1};
+  cuuint32_t estride[3] = {1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
+  if (!d) return MOE_ERR_NULL;
+  if (d->E < 1 || d->E > kMaxExperts) return MOE_ERR_SHAPE;
+  if (d->d < 64 || d->d % 64 != 0) return MOE_ERR_SHAPE;
+  if (d->F < 32 || d->F % 32 != 0) return MOE_ERR_SHAPE;
+  if (d->align != kAlign) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU)
+    return MOE_ERR_UNSUPPORTED;
+  if (d->capacity < kAlign || d->capacity % kAlign != 0) return MOE_ERR_SHAPE;
+  if (d->sm_margin < 0) return MOE_ERR_SHAPE;
+  if (need_tokens) {
+    if (d->T < 0 || d->k < 1 || d->k > kMaxTopK || d->k > d->E) return MOE_ERR_SHAPE;
+    const long long need = static_cast<long long>(d->T) * d->k +
+                           static_cast<long long>(d->E) * (kAlign - 1);
+    if (d->capacity < need) return MOE_ERR_SHAPE;
+  }
+  return MOE_OK;
+}
+
+int grid_for(const DeviceInfo* di, const moe_mlp_desc_t* d) {
+  int g = di->sms - d->sm_margin;
+  return g < 1 ? 1 : g;
+}
+
+size_t route_ws_bytes(const moe_mlp_desc_t* d) {
+  const size_t nchunks = (static_cast<size_t>(d->T) + kTokensPerChunk - 1) / kTokensPerChunk;
+  return (nchunks * d->E * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+void fill_common(GemmArgs& a, const moe_mlp_desc_t* d, const DeviceInfo* di,
+                 const int32_t* counts, const int32_t* padded_offsets) {
+  memset(&a, 0, sizeof(a));
+  a.padded_offsets = padded_offsets;
+  a.counts = counts;
+  a.status = di->status;
+  a.E = d->E;
+  a.f_real = d->F;
+  a.f_pad = fc1_pad(d->F);
+  a.capacity = d->capacity;
+  a.act = d->act;
+  a.alpha = d->alpha;
+  a.limit = d->limit;
+  a.lin_off = d->linear_offset;
+  a.out_scale = d->out_scale;
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int32_t moe_fc1_padded_width(int32_t F) { return fc1_pad(F); }
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_NULL: return "required pointer is NULL";
+    case MOE_ERR_SHAPE: return "sizes out of the supported range";
+    case MOE_ERR_UNSUPPORTED: return "option not supported";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_ARCH: return "current device is not sm_103";
+    case MOE_ERR_CUDA: return "CUDA call failed";
+    case MOE_ERR_DEVICE: return "device status word is set";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes) {
+  if (!desc || !bytes) return MOE_ERR_NULL;
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  *bytes = route_ws_bytes(desc) + 256;
+  return MOE_OK;
+}
+
+moe_status_t moe_repack_fc1(const moe_mlp_desc_t* desc, const void* w1, const void* b1,
+                            void* w1p, void* b1p, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!w1 || !w1p) return MOE_ERR_NULL;
+  if ((b1 == nullptr) != (b1p == nullptr)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaError_t e = launch_repack_fc1(w1, w1p, desc->E, desc->F, desc->d, stream);
+  if (e == cudaSuccess && b1) e = launch_repack_fc1(b1, b1p, desc->E, desc->F, 1, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_unpack_fc1(const moe_mlp_desc_t* desc, const void* w1p, void* w1,
+                            int32_t rows_width, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!w1p || !w1) return MOE_ERR_NULL;
+  if (rows_width < 1) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_unpack_fc1(w1p, w1, desc->E, desc->F, rows_width, stream));
+}
+
+moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
+                               const float* bias, const void* x, int32_t* topk_idx,
+                               float* topk_w, int32_t* counts, int32_t* offsets,
+                               int32_t* padded_offsets, int32_t* tile_prefix,
+                               int32_t* row_src, int32_t* row_of, void* x_perm, void* ws,
+                               size_t ws_bytes, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!logits || !x || !topk_idx || !topk_w || !counts || !offsets || !padded_offsets ||
+      !tile_prefix || !row_src || !row_of || !x_perm)
+    return MOE_ERR_NULL;
+  if (desc->T > 0 && !ws) return MOE_ERR_NULL;
+  if (ws_bytes < route_ws_bytes(desc)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const int T = desc->T, E = desc->E, k = desc->k;
+  const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
+  int32_t* chunk = static_cast<int32_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(row_src, 0xFF, sizeof(int32_t) * desc->capacity, stream);
+  if (e == cudaSuccess && T > 0)
+    e = launch_topk(logits, bias, T, E, k, topk_idx, topk_w, chunk, di->status, stream);
+  if (e == cudaSuccess) {
+    if (T > 0)
+      e = launch_scan(chunk, nchunks, E, desc->capacity, counts, offsets, padded_offsets,
+                      tile_prefix, di->status, stream);
+    else
+      e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
+    if (e == cudaSuccess && T == 0)
+      e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
+                                     tile_prefix, di->status, stream);
+  }
+  if (e == cudaSuccess && T > 0)
+    e = launch_assign(topk_idx, T, E, k, chunk, padded_offsets, row_src, row_of, di->status,
+                      stream);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
+                           di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts,
+                               int32_t* offsets, int32_t* padded_offsets,
+                               int32_t* tile_prefix, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!counts || !offsets || !padded_offsets || !tile_prefix) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_offsets_from_counts(counts, desc->E, desc->capacity, offsets,
+                                                padded_offsets, tile_prefix, di->status, stream));
+}
+
+moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
+                         const int32_t* counts, const int32_t* padded_offsets,
+                         const void* w1p, const void* b1p, const void* w2, const void* b2,
+                         void* h, void* a, void* y, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !w2 || !h || !a || !y)
+    return MOE_ERR_NULL;
+  if ((desc->has_b1 && !b1p) || (desc->has_b2 && !b2)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  const int grid = grid_for(di, desc);
+
+  GemmArgs g1;
+  fill_common(g1, desc, di, counts, padded_offsets);
+  if (!encode_map(&g1.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g1.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256))
+    return MOE_ERR_SHAPE;
+  g1.K = desc->d;
+  g1.n_ext = static_cast<int>(2 * Fp);
+  g1.b_ext = g1.n_ext;
+  g1.out0 = h;
+  g1.ld0 = 2 * Fp;
+  g1.out1 = a;
+  g1.ld1 = F;
+  g1.bias = desc->has_b1 ? b1p : nullptr;
+  g1.bias_ld = 2 * Fp;
+  cudaError_t e = launch_grouped_gemm(kFc1Glu, g1, grid, stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  GemmArgs g2;
+  fill_common(g2, desc, di, counts, padded_offsets);
+  if (!encode_map(&g2.tma_a, a, F, cap, 1, F * 2, cap * F * 2, 64, 128) ||
+      !encode_map(&g2.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256))
+    return MOE_ERR_SHAPE;
+  g2.K = desc->F;
+  g2.n_ext = desc->d;
+  g2.b_ext = desc->d;
+  g2.out0 = y;
+  g2.ld0 = d;
+  g2.bias = desc->has_b2 ? b2 : nullptr;
+  g2.bias_ld = d;
+  return cuda_status(launch_grouped_gemm(kFc2, g2, grid, stream));
+}
+
+moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
+                                   const int32_t* row_of, const float* topk_w, void* out,
+                                   cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!y || !row_of || !topk_w || !out) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_combine(y, row_of, topk_w, desc->T, desc->k, desc->d, out, stream));
+}
+
+moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* dout,
+                                       const void* y, const int32_t* row_of,
+                                       const float* topk_w, const int32_t* row_src,
+                                       const int32_t* padded_offsets, void* dy, float* dw,
+                                       cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!dout || !y || !row_of || !topk_w || !row_src || !padded_offsets || !dy || !dw)
+    return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaError_t e = launch_zero_pad_rows(row_src, padded_offsets, desc->E, desc->d,
+                                       desc->capacity, dy, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_combine_bwd(dout, y, row_of, topk_w, desc->T, desc->k, desc->d, dy, dw, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
+                         const void* h, const void* a, const int32_t* counts,
+                         const int32_t* padded_offsets, const void* w1p, const void* w2,
+                         void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
+                         void* db2, void* ws, size_t ws_bytes, cudaStream_t stream) {
+  (void)ws;
+  (void)ws_bytes;
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dy || !x_perm || !h || !a || !counts || !padded_offsets || !w1p || !w2 || !dh ||
+      !dx_perm || !dw1p || !dw2)
+    return MOE_ERR_NULL;
+  if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  const int grid = grid_for(di, desc);
+  cudaError_t e;
+
+  // FC2 dgrad + dGLU: dA = dY W2 (B = W2 read MN-major), dH from H
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(Fp);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = 2 * Fp;
+  g.aux = h;
+  g.ld_aux = 2 * Fp;
+  if ((e = launch_grouped_gemm(kDgradDglu, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // FC2 wgrad: dW2[e] (d x F) = sum_rows dY^T A
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
+      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.m_ext = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = dw2;
+  g.ld0 = F;
+  if ((e = launch_grouped_gemm(kWgrad, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // FC1 dgrad: dX = dH W1p (B = W1p read MN-major)
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dx_perm;
+  g.ld0 = d;
+  if ((e = launch_grouped_gemm(kDgradFc1, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // FC1 wgrad: dW1p[e] (2F_pad x d) = sum_rows dH^T X
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64) ||
+      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.m_ext = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dw1p;
+  g.ld0 = d;
+  if ((e = launch_grouped_gemm(kWgrad, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
+
+  if (desc->has_b2 &&
+      (e = launch_group_colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream)) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (desc->has_b1 &&
+      (e = launch_group_colsum(dh, counts, padded_offsets, desc->E, static_cast<int>(2 * Fp),
+                               db1p, stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
+                             const int32_t* row_of, void* dx, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!dx_perm || !row_of || !dx) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_permute_bwd(dx_perm, row_of, desc->T, desc->k, desc->d, dx, stream));
+}
+
+moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const float* topk_w,
+                           const int32_t* topk_idx, float* dlogits, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!dw || !topk_w || !topk_idx || !dlogits) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(
+      launch_route_bwd(dw, topk_w, topk_idx, desc->T, desc->E, desc->k, dlogits, stream));
+}
+
+moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear) {
+  if (!host_status) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, di->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (clear && cudaMemset(di->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  *host_status = v;
+  return MOE_OK;
+}
+
+}  // extern "C"

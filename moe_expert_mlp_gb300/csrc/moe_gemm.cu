@@ -1,0 +1,494 @@
+// Persistent grouped GEMM on the 5th-generation tensor cores (tcgen05) for
+// the routed-expert MLP, forward and backward, with the fused epilogues.
+//
+// Sources: "Improving MoE training throughput with advanced fused kernels":
+//   - "Overcoming training bottlenecks in the MoE block": the GroupGemm
+//     kernel families (GroupGemm + Activation, GroupGemm + dActivation).
+//   - "Optimizing GLU activations with fused GEMM epilogues" (Figure 2): with
+//     the FC1 weight repacked, one CTA's accumulator tile holds 128 gate and
+//     the matching 128 linear features, so the GLU (with bias, clamp and
+//     scaling) is applied in the epilogue; the backward epilogue reads the
+//     GEMM output and computes dSwiGLU.
+//   - "Eliminating host-device synchronisation and CPU launch overhead": the
+//     per-group token counts are read from GPU memory by the kernel; the grid
+//     is sized from the SM count, never from the routing result.
+//   - "From kernel-level gains to end-to-end pretraining speedups": the grid
+//     leaves `sm_margin` SMs free.
+// "Accelerating dropless MoE training with JAX and NVIDIA Transformer
+// Engine", "Claims and evidence": one grouped GEMM call over ragged groups.
+//
+// Design (one CTA per SM, 6 warps):
+//   warp 0   TMA producer: 128B-swizzled operand tiles into a 4-stage ring.
+//   warp 1   TMEM owner and single-thread MMA issuer (M=128, N=256, K=16).
+//   warps 2-5 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
+//            bf16 stores.  Two 256-column accumulators in TMEM let the
+//            epilogue of one tile overlap the MMAs of the next.
+// Tiles are 128 rows x 256 columns.  Every expert group starts at a
+// multiple of 128 rows, so an M tile never straddles two experts; rows past
+// the group's count are padding and are written as zeros.  Weight-gradient
+// tiles (ragged K) run the K loop over the group's rows only; groups are
+// visited largest first for balance.
+#include <cuda_bf16.h>
+#include <math.h>
+
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;                       // 64 bf16 = one 128-byte swizzle row
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
+constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
+constexpr int NUM_THREADS = 192;
+constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES;
+
+struct Tile {
+  int e;        // expert
+  int m0;       // first output row (ragged M: routed row; ragged K: weight row)
+  int n0;       // first output column
+  int k_row0;   // ragged K: first routed row of the group
+  int num_kb;   // K blocks of 64
+};
+
+struct ActP {
+  int act;
+  float alpha, limit, lin_off, out_scale;
+};
+
+__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
+
+__device__ __forceinline__ float glu_fwd(float g, float l, const ActP& p) {
+  const float gc = fminf(g, p.limit);
+  const float lc = fminf(fmaxf(l, -p.limit), p.limit);
+  float phi;
+  if (p.act == MOE_ACT_SWIGLU) {
+    phi = gc * sigmoid_f(p.alpha * gc);
+  } else if (p.act == MOE_ACT_GEGLU) {
+    phi = 0.5f * gc * (1.0f + erff(gc * 0.70710678118654752f));
+  } else {
+    const float r = fmaxf(gc, 0.0f);
+    phi = r * r;
+  }
+  return p.out_scale * phi * (lc + p.lin_off);
+}
+
+__device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& p, float& dg,
+                                        float& dl) {
+  const float gc = fminf(g, p.limit);
+  const float lc = fminf(fmaxf(l, -p.limit), p.limit);
+  float phi, dphi;
+  if (p.act == MOE_ACT_SWIGLU) {
+    const float s = sigmoid_f(p.alpha * gc);
+    phi = gc * s;
+    dphi = s + p.alpha * gc * s * (1.0f - s);
+  } else if (p.act == MOE_ACT_GEGLU) {
+    const float cdf = 0.5f * (1.0f + erff(gc * 0.70710678118654752f));
+    const float pdf = 0.39894228040143268f * __expf(-0.5f * gc * gc);
+    phi = gc * cdf;
+    dphi = cdf + gc * pdf;
+  } else {
+    const float r = fmaxf(gc, 0.0f);
+    phi = r * r;
+    dphi = 2.0f * r;
+  }
+  const float das = p.out_scale * da;
+  dg = (g <= p.limit) ? das * (lc + p.lin_off) * dphi : 0.0f;
+  dl = (l >= -p.limit && l <= p.limit) ? das * phi : 0.0f;
+}
+
+template <int MODE>
+struct Traits {
+  static constexpr bool kRaggedK = (MODE == kWgrad);
+  static constexpr bool kAmn = (MODE == kWgrad);
+  static constexpr bool kBmn = (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad);
+  static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
+};
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, const int* s_off,
+                                            const int* s_cnt, const int* s_order, int E) {
+  Tile ti;
+  if (Traits<MODE>::kRaggedK) {
+    const int per_e = m_tiles * n_tiles;
+    const int slot = t / per_e;
+    const int rem = t - slot * per_e;
+    const int mb = rem / n_tiles;
+    const int nb = rem - mb * n_tiles;
+    ti.e = s_order[slot];
+    ti.m0 = mb * BM;
+    ti.n0 = nb * BN;
+    ti.k_row0 = s_off[ti.e];
+    ti.num_kb = (s_cnt[ti.e] + BK - 1) / BK;
+  } else {
+    const int mb = t / n_tiles;
+    const int nb = t - mb * n_tiles;
+    const int row = mb * BM;
+    // last expert whose group starts at or before `row`
+    int lo = 0, hi = E;  // answer in [lo, hi)
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (s_off[mid] <= row) lo = mid; else hi = mid;
+    }
+    ti.e = lo;
+    ti.m0 = row;
+    ti.n0 = nb * BN;
+    ti.k_row0 = 0;
+    ti.num_kb = 0;  // filled by caller from K
+  }
+  return ti;
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
+  using Tr = Traits<MODE>;
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_total;
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_order[kMaxExperts];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int E = args.E;
+
+  // ---- group tables (sizes live in device memory; no host round trip)
+  for (int i = threadIdx.x; i <= E; i += NUM_THREADS) s_off[i] = args.padded_offsets[i];
+  for (int i = threadIdx.x; i < E; i += NUM_THREADS) s_cnt[i] = args.counts[i];
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem_base, TMEM_COLS);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+
+  const int n_tiles = (args.n_ext + BN - 1) / BN;
+  const int m_tiles = Tr::kRaggedK ? (args.m_ext + BM - 1) / BM : 0;
+  if (threadIdx.x == 0) {
+    // validate the offsets read from device memory; skip all work if bad
+    bool ok = s_off[0] == 0 && s_off[E] <= args.capacity;
+    for (int e = 0; e < E && ok; ++e) {
+      const int span = s_off[e + 1] - s_off[e];
+      ok = span >= 0 && (span % BM) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= span;
+    }
+    if (!ok) {
+      set_status(args.status, MOE_DEV_BAD_OFFSETS);
+      s_total = 0;
+    } else if (Tr::kRaggedK) {
+      s_total = E * m_tiles * n_tiles;
+    } else {
+      s_total = (s_off[E] / BM) * n_tiles;
+    }
+  }
+  if (Tr::kRaggedK) {
+    // largest group first; equal sizes keep expert order
+    for (int e = threadIdx.x; e < E; e += NUM_THREADS) {
+      int rank = 0;
+      for (int j = 0; j < E; ++j)
+        rank += (s_cnt[j] > s_cnt[e]) || (s_cnt[j] == s_cnt[e] && j < e);
+      s_order[rank] = e;
+    }
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int total = s_total;
+  const int kb_fixed = Tr::kRaggedK ? 0 : (args.K + BK - 1) / BK;
+  volatile int* abort_flag = &s_abort;
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&args.tma_a);
+      tma_prefetch_desc(&args.tma_b);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
+        Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+        const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
+        // boxes that hold at least one in-range column (skip fully-outside boxes)
+        const int b_boxes = Tr::kBmn ? min(4, (args.b_ext - ti.n0 + 63) / 64) : 1;
+        const int a_boxes = Tr::kAmn ? min(2, (args.m_ext - ti.m0 + 63) / 64) : 1;
+        const uint32_t tx = (Tr::kAmn ? a_boxes * MN_BOX_BYTES : A_BYTES) +
+                            (Tr::kBmn ? b_boxes * MN_BOX_BYTES : B_BYTES);
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, args.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * STAGE_BYTES;
+          uint8_t* sb = sa + A_BYTES;
+          uint64_t* fb = &full_bar[stage];
+          mbar_arrive_expect_tx(fb, tx);
+          const int kk = kb * BK;
+          // ---- A operand
+          if (Tr::kAmn) {
+            for (int i = 0; i < a_boxes; ++i)
+              tma_load_3d(sa + i * MN_BOX_BYTES, &args.tma_a, fb, ti.m0 + 64 * i, ti.k_row0 + kk, 0);
+          } else {
+            tma_load_3d(sa, &args.tma_a, fb, kk, ti.m0, 0);
+          }
+          // ---- B operand
+          if (MODE == kFc1Glu || MODE == kFc2) {
+            tma_load_3d(sb, &args.tma_b, fb, kk, ti.n0, ti.e);
+          } else if (MODE == kDgradDglu || MODE == kDgradFc1) {
+            for (int i = 0; i < b_boxes; ++i)
+              tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, kk, ti.e);
+          } else {
+            for (int i = 0; i < b_boxes; ++i)
+              tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, ti.k_row0 + kk, 0);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==============================
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
+        Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+        const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_par ^ 1u, args.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, args.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
+          const uint32_t b_base = a_base + A_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            // K-major: +32 B per K=16 step inside the 128-B swizzle row.
+            // MN-major: +16 K-rows of 128 B = 2048 B; atoms 8 KB apart along MN.
+            const uint64_t ad = Tr::kAmn ? sdesc_sw128(a_base + k * 2048, MN_BOX_BYTES, 1024)
+                                         : sdesc_sw128(a_base + k * 32, 16, 1024);
+            const uint64_t bd = Tr::kBmn ? sdesc_sw128(b_base + k * 2048, MN_BOX_BYTES, 1024)
+                                         : sdesc_sw128(b_base + k * 32, 16, 1024);
+            umma_bf16(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit(&empty_bar[stage]);
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull_bar[acc]);
+      }
+    }
+  } else {
+    // ============================ epilogue ================================
+    const int quarter = warp & 3;             // TMEM lanes this warp may read
+    const int row_local = quarter * 32 + lane;
+    const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
+    int it = 0;
+    for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+      Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+
+      if (MODE == kWgrad) {
+        const int row = ti.m0 + row_local;
+        const bool row_ok = row < args.m_ext;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out0) +
+                             (static_cast<long long>(ti.e) * args.m_ext + (row_ok ? row : 0)) * args.ld0;
+        for (int j = 0; j < BN / 32; ++j) {
+          const int c0 = ti.n0 + 32 * j;
+          if (c0 >= args.n_ext) break;
+          float v[32];
+          if (ti.num_kb > 0) {
+            uint32_t r[32];
+            tmem_ld32(tbase + 32 * j, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          }
+          if (row_ok) store_bf16x32(dst + c0, v);
+        }
+      } else {
+        const long long gr = ti.m0 + row_local;
+        const bool valid = (gr - s_off[ti.e]) < s_cnt[ti.e];
+        if (MODE == kFc1Glu) {
+          __nv_bfloat16* H = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0 + ti.n0;
+          __nv_bfloat16* A = static_cast<__nv_bfloat16*>(args.out1) + gr * args.ld1;
+          const __nv_bfloat16* b1 =
+              args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0
+                        : nullptr;
+          for (int j = 0; j < kGluHalf / 32; ++j) {
+            uint32_t rg[32], rl[32];
+            tmem_ld32(tbase + 32 * j, rg);
+            tmem_ld32(tbase + kGluHalf + 32 * j, rl);
+            tmem_ld_wait();
+            float g[32], l[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] = __uint_as_float(rg[i]);
+              l[i] = __uint_as_float(rl[i]);
+            }
+            if (b1) {
+              float bg[32], bl[32];
+              load_bf16x32(b1 + 32 * j, bg);
+              load_bf16x32(b1 + kGluHalf + 32 * j, bl);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) {
+                g[i] += bg[i];
+                l[i] += bl[i];
+              }
+            }
+            const int f0 = ti.n0 / 2 + 32 * j;
+            if (valid) {
+              store_bf16x32(H + 32 * j, g);
+              store_bf16x32(H + kGluHalf + 32 * j, l);
+              if (f0 < args.f_real) {
+                float a[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) a[i] = glu_fwd(g[i], l[i], ap);
+                store_bf16x32(A + f0, a);
+              }
+            } else {
+              store_zero_x32(H + 32 * j);
+              store_zero_x32(H + kGluHalf + 32 * j);
+              if (f0 < args.f_real) store_zero_x32(A + f0);
+            }
+          }
+        } else if (MODE == kDgradDglu) {
+          // tile columns are GLU features n0 .. n0+255; dH in packed layout
+          __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
+          const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
+          for (int j = 0; j < BN / 32; ++j) {
+            const int f0 = ti.n0 + 32 * j;
+            if (f0 >= args.f_pad) break;
+            uint32_t r[32];
+            tmem_ld32(tbase + 32 * j, r);
+            tmem_ld_wait();
+            const long long cg = static_cast<long long>(f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
+            const long long cl = cg + kGluHalf;
+            if (valid && f0 < args.f_real) {
+              float g[32], l[32], dg[32], dl[32];
+              load_bf16x32(H + cg, g);
+              load_bf16x32(H + cl, l);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) glu_bwd(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
+              store_bf16x32(dH + cg, dg);
+              store_bf16x32(dH + cl, dl);
+            } else {
+              store_zero_x32(dH + cg);
+              store_zero_x32(dH + cl);
+            }
+          }
+        } else {
+          // kFc2 (+b2) and kDgradFc1: plain row-major bf16 output
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
+          const __nv_bfloat16* bias =
+              (MODE == kFc2 && args.bias)
+                  ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
+                  : nullptr;
+          for (int j = 0; j < BN / 32; ++j) {
+            const int c0 = ti.n0 + 32 * j;
+            if (c0 >= args.n_ext) break;
+            uint32_t r[32];
+            tmem_ld32(tbase + 32 * j, r);
+            tmem_ld_wait();
+            if (valid) {
+              float v[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+              if (bias) {
+                float b[32];
+                load_bf16x32(bias + c0, b);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] += b[i];
+              }
+              store_bf16x32(dst + c0, v);
+            } else {
+              store_zero_x32(dst + c0);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+template <int MODE>
+cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(SMEM_BYTES));
+  if (err != cudaSuccess) return err;
+  k_grouped_gemm<MODE><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(args);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
+
+cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
+  switch (mode) {
+    case kFc1Glu: return launch_mode<kFc1Glu>(args, grid, s);
+    case kFc2: return launch_mode<kFc2>(args, grid, s);
+    case kDgradDglu: return launch_mode<kDgradDglu>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1>(args, grid, s);
+    case kWgrad: return launch_mode<kWgrad>(args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace moe

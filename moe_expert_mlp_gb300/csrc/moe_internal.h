@@ -1,0 +1,95 @@
+// Internal interface between the C-ABI entry points and the kernel
+// translation units.  Not installed; not part of the public boundary.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+constexpr int kTokensPerChunk = 256;   // routing: tokens per histogram chunk
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 32;
+constexpr int kAlign = 128;            // group alignment = GEMM tile rows
+constexpr int kGluHalf = 128;          // packed FC1 block: 128 gate + 128 linear rows
+
+inline int fc1_pad(int F) { return (F + kGluHalf - 1) / kGluHalf * kGluHalf; }
+
+// ------------------------------------------------ memory-bound kernels
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
+                        int32_t* topk_idx, float* topk_w, int32_t* chunk_counts, int* status,
+                        cudaStream_t s);
+cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int capacity,
+                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                        int32_t* tile_prefix, int* status, cudaStream_t s);
+cudaError_t launch_offsets_from_counts(const int32_t* counts, int E, int capacity,
+                                       int32_t* offsets, int32_t* padded_offsets,
+                                       int32_t* tile_prefix, int* status, cudaStream_t s);
+cudaError_t launch_assign(const int32_t* topk_idx, int T, int E, int k,
+                          const int32_t* chunk_base, const int32_t* padded_offsets,
+                          int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s);
+cudaError_t launch_gather_rows(const void* x, const int32_t* row_src,
+                               const int32_t* padded_offsets, int E, int d, int T, int capacity,
+                               void* x_perm, int num_sms, cudaStream_t s);
+cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* w, int T, int k,
+                           int d, void* out, cudaStream_t s);
+cudaError_t launch_combine_bwd(const void* dout, const void* y, const int32_t* row_of,
+                               const float* w, int T, int k, int d, void* dy, float* dw,
+                               cudaStream_t s);
+cudaError_t launch_zero_pad_rows(const int32_t* row_src, const int32_t* padded_offsets, int E,
+                                 int width, int capacity, void* rows, int num_sms,
+                                 cudaStream_t s);
+cudaError_t launch_permute_bwd(const void* dx_perm, const int32_t* row_of, int T, int k, int d,
+                               void* dx, cudaStream_t s);
+cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* idx, int T, int E,
+                             int k, float* dlogits, cudaStream_t s);
+cudaError_t launch_repack_fc1(const void* w1, void* w1p, int E, int F, int width,
+                              cudaStream_t s);
+cudaError_t launch_unpack_fc1(const void* w1p, void* w1, int E, int F, int width,
+                              cudaStream_t s);
+cudaError_t launch_group_colsum(const void* g, const int32_t* counts,
+                                const int32_t* padded_offsets, int E, int width, void* out,
+                                cudaStream_t s);
+
+// ------------------------------------------------ grouped GEMM (tcgen05)
+enum GemmMode : int {
+  kFc1Glu = 0,     // H = X W1p^T (+b1), A = GLU(H)             ragged M
+  kFc2 = 1,        // Y = A W2^T (+b2)                          ragged M
+  kDgradDglu = 2,  // dA = dY W2, dH = dGLU(dA, H)              ragged M
+  kDgradFc1 = 3,   // dX = dH W1p                               ragged M
+  kWgrad = 4       // dW[e] = sum over group rows of P^T Q      ragged K
+};
+
+struct GemmArgs {
+  CUtensorMap tma_a;
+  CUtensorMap tma_b;
+  const int32_t* padded_offsets;
+  const int32_t* counts;
+  int* status;
+  int E;
+  int K;            // contraction length (ragged-M modes)
+  int n_ext;        // output columns covered by tiles
+  int b_ext;        // real extent of B's N dimension (MN-major box count)
+  int m_ext;        // ragged-K mode: output rows
+  int f_real;       // F
+  int f_pad;        // F_pad
+  int capacity;
+  int act;
+  float alpha, limit, lin_off, out_scale;
+  void* out0;
+  long long ld0;
+  void* out1;
+  long long ld1;
+  const void* aux;
+  long long ld_aux;
+  const void* bias;
+  long long bias_ld;
+};
+
+cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);
+size_t grouped_gemm_smem_bytes();
+
+}  // namespace moe

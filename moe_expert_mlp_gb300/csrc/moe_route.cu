@@ -1,0 +1,510 @@
+// Memory-bound steps of the routed-expert MLP: top-k routing, group offsets,
+// the stable permutation into expert-contiguous ragged groups, the weighted
+// combine, their backward passes, the FC1 weight repack and the per-group
+// bias-gradient column sums.
+//
+// Sources: "Improving MoE training throughput with advanced fused kernels",
+// "Overcoming training bottlenecks in the MoE block" (tokens per expert are
+// computed at run time) and "Eliminating host-device synchronisation and CPU
+// launch overhead" (group sizes are kept in GPU memory so nothing here reads
+// device data on the host); "Accelerating dropless MoE training with JAX and
+// NVIDIA Transformer Engine", "Claims and evidence" (ragged tensors; the
+// combine step).
+//
+// All kernels are deterministic: no floating-point atomics, fixed reduction
+// trees, and the permutation is a stable counting sort.
+#include <cuda_bf16.h>
+#include <float.h>
+#include <math.h>
+
+#include "moe_internal.h"
+#include "moe_ptx.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarps = kTokensPerChunk / 32;   // 8 warps per routing block
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+  return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// ------------------------------------------------------------ top-k
+// One warp per token.  Lane l holds the scores of experts l, l+32, ...
+// k rounds of a warp arg-max (larger score wins, equal scores go to the
+// lower expert index) give the slots in descending score.  The weights are
+// the softmax of the selected raw logits.  Each block also histograms its
+// chunk of kTokensPerChunk tokens per expert (counts are exact integers).
+__global__ void __launch_bounds__(kTokensPerChunk) k_topk(
+    const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
+    int32_t* __restrict__ chunk_counts, int* status) {
+  __shared__ int s_cnt[kMaxExperts];
+  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int tt = warp; tt < kTokensPerChunk; tt += kWarps) {
+    const int t = blockIdx.x * kTokensPerChunk + tt;
+    if (t >= T) break;
+    const float* lrow = logits + static_cast<size_t>(t) * E;
+    float sc[kMaxExperts / 32];
+#pragma unroll
+    for (int q = 0; q < kMaxExperts / 32; ++q) {
+      const int e = lane + 32 * q;
+      sc[q] = -INFINITY;
+      if (e < E) sc[q] = lrow[e] + (bias ? bias[e] : 0.0f);
+    }
+    uint32_t taken = 0;
+    int my_idx = 0;
+    for (int s = 0; s < k; ++s) {
+      float best = -INFINITY;
+      int bi = E;                         // sentinel: nothing selectable
+#pragma unroll
+      for (int q = 0; q < kMaxExperts / 32; ++q) {
+        const int e = lane + 32 * q;
+        if (e < E && !((taken >> q) & 1u)) {
+          if (sc[q] > best || (sc[q] == best && e < bi)) {
+            best = sc[q];
+            bi = e;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+        if (ob > best || (ob == best && oi < bi)) {
+          best = ob;
+          bi = oi;
+        }
+      }
+      if (bi >= E) {                      // non-finite scores left nothing to pick
+        if (lane == 0) set_status(status, MOE_DEV_BAD_EXPERT);
+        bi = s;
+      }
+      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+      if (lane == s) my_idx = bi;
+    }
+    const float z = (lane < k) ? lrow[my_idx] : -INFINITY;
+    const float m = warp_max(z);
+    const float ex = (lane < k) ? expf(z - m) : 0.0f;
+    const float sum = warp_sum(ex);
+    if (lane < k) {
+      topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+      topk_w[static_cast<size_t>(t) * k + lane] = ex / sum;
+      atomicAdd(&s_cnt[my_idx], 1);
+    }
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = s_cnt[i];
+}
+
+// ------------------------------------------------------------- scans
+// Serial scans of at most 256 experts by one thread: offsets, padded
+// offsets (groups start at multiples of kAlign) and the tile prefix.
+__device__ void scan_experts(const int32_t* cnt, int E, int capacity, int32_t* offsets,
+                             int32_t* padded_offsets, int32_t* tile_prefix, int* status) {
+  int o = 0, p = 0, tp = 0;
+  for (int e = 0; e < E; ++e) {
+    offsets[e] = o;
+    padded_offsets[e] = p;
+    tile_prefix[e] = tp;
+    const int c = cnt[e];
+    if (c < 0) set_status(status, MOE_DEV_BAD_OFFSETS);
+    o += c;
+    p += (c + kAlign - 1) / kAlign * kAlign;
+    tp += (c + kAlign - 1) / kAlign;
+  }
+  offsets[E] = o;
+  padded_offsets[E] = p;
+  tile_prefix[E] = tp;
+  if (p > capacity) set_status(status, MOE_DEV_BAD_OFFSETS);
+}
+
+// chunk_counts [nchunks][E] -> exclusive per-expert bases over chunks (in
+// place), counts and the three expert prefixes.
+__global__ void k_scan(int32_t* __restrict__ chunk_counts, int nchunks, int E, int capacity,
+                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                       int32_t* __restrict__ padded_offsets, int32_t* __restrict__ tile_prefix,
+                       int* status) {
+  __shared__ int32_t s_tot[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[static_cast<size_t>(c) * E + e];
+      chunk_counts[static_cast<size_t>(c) * E + e] = run;
+      run += v;
+    }
+    s_tot[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    scan_experts(s_tot, E, capacity, offsets, padded_offsets, tile_prefix, status);
+}
+
+__global__ void k_offsets_from_counts(const int32_t* __restrict__ counts, int E, int capacity,
+                                      int32_t* offsets, int32_t* padded_offsets,
+                                      int32_t* tile_prefix, int* status) {
+  __shared__ int32_t s_c[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) s_c[e] = counts[e];
+  __syncthreads();
+  if (threadIdx.x == 0) scan_experts(s_c, E, capacity, offsets, padded_offsets, tile_prefix, status);
+}
+
+// ----------------------------------------------------- stable assignment
+// One thread per token, one block per chunk.  The row of (token t, expert e)
+// is padded_offsets[e] + (tokens of earlier chunks choosing e) + (earlier
+// tokens of this chunk choosing e), so rows inside a group ascend by token.
+// Ranks inside a warp come from ballots, across warps from a shared prefix.
+__global__ void __launch_bounds__(kTokensPerChunk) k_assign(
+    const int32_t* __restrict__ topk_idx, int T, int E, int k,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ padded_offsets,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_of, int* status) {
+  __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kTokensPerChunk + threadIdx.x;
+  const bool live = t < T;
+  uint64_t sel[kMaxExperts / 64] = {0, 0, 0, 0};
+  if (live) {
+    for (int s = 0; s < k; ++s) {
+      const int e = topk_idx[static_cast<size_t>(t) * k + s];
+      if (e < 0 || e >= E) {
+        set_status(status, MOE_DEV_BAD_EXPERT);
+        continue;
+      }
+      sel[e >> 6] |= 1ull << (e & 63);
+    }
+  }
+  const uint32_t lt_mask = (1u << lane) - 1u;
+  for (int e = 0; e < E; ++e) {
+    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
+    if (lane == 0) s_wcnt[warp][e] = __popc(b);
+  }
+  __syncthreads();
+  // exclusive prefix over warps, per expert
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = s_wcnt[w][e];
+      s_wcnt[w][e] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  for (int e = 0; e < E; ++e) {
+    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
+    const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
+    if (has) {
+      const int rank = s_wcnt[warp][e] + __popc(b & lt_mask);
+      const int row = padded_offsets[e] + chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+      row_src[row] = t;
+      for (int s = 0; s < k; ++s)
+        if (topk_idx[static_cast<size_t>(t) * k + s] == e) row_of[static_cast<size_t>(t) * k + s] = row;
+    }
+  }
+}
+
+// ---------------------------------------------------------- row gather
+// x_perm[j] = x[row_src[j]] (zero on padding), one warp per row, 16-byte
+// vectors.  The grid strides over the rows up to padded_offsets[E], which is
+// read on the device.
+__global__ void __launch_bounds__(256) k_gather_rows(
+    const uint4* __restrict__ x, const int32_t* __restrict__ row_src,
+    const int32_t* __restrict__ padded_offsets, int E, int vec_per_row, int T, int capacity,
+    uint4* __restrict__ x_perm) {
+  const int rows = min(padded_offsets[E], capacity);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
+    const int t = row_src[j];
+    uint4* dst = x_perm + static_cast<size_t>(j) * vec_per_row;
+    if (t >= 0 && t < T) {
+      const uint4* src = x + static_cast<size_t>(t) * vec_per_row;
+      for (int c = lane; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
+    } else {
+      for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_zero_pad_rows(
+    const int32_t* __restrict__ row_src, const int32_t* __restrict__ padded_offsets, int E,
+    int vec_per_row, int capacity, uint4* __restrict__ rows_out) {
+  const int rows = min(padded_offsets[E], capacity);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
+    if (row_src[j] >= 0) continue;
+    uint4* dst = rows_out + static_cast<size_t>(j) * vec_per_row;
+    for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+  }
+}
+
+__device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
+  v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+  v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+  v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+  v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  uint4 w;
+  w.x = pack_bf16x2(v[0], v[1]);
+  w.y = pack_bf16x2(v[2], v[3]);
+  w.z = pack_bf16x2(v[4], v[5]);
+  w.w = pack_bf16x2(v[6], v[7]);
+  return w;
+}
+
+// ------------------------------------------------------------- combine
+// out[t] = sum_s w[t,s] * y[row_of[t,s]]: one block per token, fp32 sums in
+// slot order.  With w == nullptr the weights are 1 (permute backward).
+__global__ void __launch_bounds__(128) k_combine(
+    const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
+    const float* __restrict__ w, int k, int vec_per_row, uint4* __restrict__ out) {
+  const int t = blockIdx.x;
+  for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
+    float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    for (int s = 0; s < k; ++s) {
+      const int r = row_of[static_cast<size_t>(t) * k + s];
+      const float ws = w ? w[static_cast<size_t>(t) * k + s] : 1.0f;
+      float v[8];
+      unpack8(__ldg(y + static_cast<size_t>(r) * vec_per_row + c), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(ws, v[i], acc[i]);
+    }
+    out[static_cast<size_t>(t) * vec_per_row + c] = pack8(acc);
+  }
+}
+
+// dy[row_of[t,s]] = bf16(w[t,s] * dout[t]); dw[t,s] = <dout[t], y[row_of[t,s]]>
+// with a fixed-shape block reduction (deterministic).
+__global__ void __launch_bounds__(128) k_combine_bwd(
+    const uint4* __restrict__ dout, const uint4* __restrict__ y,
+    const int32_t* __restrict__ row_of, const float* __restrict__ w, int k, int vec_per_row,
+    uint4* __restrict__ dy, float* __restrict__ dw) {
+  __shared__ float s_part[4];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int s = 0; s < k; ++s) {
+    const int r = row_of[static_cast<size_t>(t) * k + s];
+    const float ws = w[static_cast<size_t>(t) * k + s];
+    float dot = 0.0f;
+    for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
+      float g[8], v[8], o[8];
+      unpack8(__ldg(dout + static_cast<size_t>(t) * vec_per_row + c), g);
+      unpack8(__ldg(y + static_cast<size_t>(r) * vec_per_row + c), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dot = fmaf(g[i], v[i], dot);
+        o[i] = ws * g[i];
+      }
+      dy[static_cast<size_t>(r) * vec_per_row + c] = pack8(o);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) s_part[warp] = dot;
+    __syncthreads();
+    if (threadIdx.x == 0)
+      dw[static_cast<size_t>(t) * k + s] = (s_part[0] + s_part[1]) + (s_part[2] + s_part[3]);
+    __syncthreads();
+  }
+}
+
+// dlogits[t, idx[t,s]] = w_s * (dw_s - sum_s' w_s' dw_s'), zero elsewhere.
+__global__ void __launch_bounds__(256) k_route_bwd(
+    const float* __restrict__ dw, const float* __restrict__ w, const int32_t* __restrict__ idx,
+    int T, int E, int k, float* __restrict__ dlogits) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  float ws = 0.0f, dws = 0.0f;
+  int e = -1;
+  if (lane < k) {
+    ws = w[static_cast<size_t>(t) * k + lane];
+    dws = dw[static_cast<size_t>(t) * k + lane];
+    e = idx[static_cast<size_t>(t) * k + lane];
+  }
+  const float inner = warp_sum(ws * dws);
+  float* row = dlogits + static_cast<size_t>(t) * E;
+  for (int c = lane; c < E; c += 32) row[c] = 0.0f;
+  __syncwarp();
+  if (lane < k && e >= 0 && e < E) row[e] = ws * (dws - inner);
+}
+
+// --------------------------------------------------------- FC1 repack
+// Packed row p of an expert: block b = p / 256, j = p % 256; j < 128 is gate
+// feature 128b+j (logical row f), else linear feature 128b+j-128 (logical
+// row F+f); features >= F are zero rows.
+__device__ __forceinline__ int packed_to_logical(int p, int F) {
+  const int b = p / (2 * kGluHalf), j = p % (2 * kGluHalf);
+  const int f = b * kGluHalf + (j % kGluHalf);
+  if (f >= F) return -1;
+  return j < kGluHalf ? f : F + f;
+}
+
+// Copy with 2-byte elements; `width` elements per row (d for weights, 1 for
+// biases).  One block per packed row.
+__global__ void k_repack_fc1(const uint16_t* __restrict__ w1, uint16_t* __restrict__ w1p, int F,
+                             int F_pad, int width) {
+  const int e = blockIdx.y;
+  const int p = blockIdx.x;
+  const int src = packed_to_logical(p, F);
+  uint16_t* dst = w1p + (static_cast<size_t>(e) * 2 * F_pad + p) * width;
+  const uint16_t* s = w1 + (static_cast<size_t>(e) * 2 * F + (src < 0 ? 0 : src)) * width;
+  for (int c = threadIdx.x; c < width; c += blockDim.x) dst[c] = src < 0 ? 0 : s[c];
+}
+
+__global__ void k_unpack_fc1(const uint16_t* __restrict__ w1p, uint16_t* __restrict__ w1, int F,
+                             int F_pad, int width) {
+  const int e = blockIdx.y;
+  const int r = blockIdx.x;                    // logical row in [0, 2F)
+  const int f = r < F ? r : r - F;
+  const int p = (f / kGluHalf) * 2 * kGluHalf + (r < F ? 0 : kGluHalf) + f % kGluHalf;
+  const uint16_t* s = w1p + (static_cast<size_t>(e) * 2 * F_pad + p) * width;
+  uint16_t* dst = w1 + (static_cast<size_t>(e) * 2 * F + r) * width;
+  for (int c = threadIdx.x; c < width; c += blockDim.x) dst[c] = s[c];
+}
+
+// db[e, c] = sum over the group's rows of g[r, c]: one thread per column
+// pair, rows summed in order in fp32.
+__global__ void __launch_bounds__(256) k_group_colsum(
+    const uint32_t* __restrict__ g, const int32_t* __restrict__ counts,
+    const int32_t* __restrict__ padded_offsets, int pairs_per_row, uint32_t* __restrict__ out) {
+  const int e = blockIdx.y;
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= pairs_per_row) return;
+  const int r0 = padded_offsets[e], m = counts[e];
+  float a0 = 0.0f, a1 = 0.0f;
+  for (int r = 0; r < m; ++r) {
+    const uint32_t v = __ldg(g + static_cast<size_t>(r0 + r) * pairs_per_row + c);
+    a0 += bf16_lo(v);
+    a1 += bf16_hi(v);
+  }
+  out[static_cast<size_t>(e) * pairs_per_row + c] = pack_bf16x2(a0, a1);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
+                        int32_t* topk_idx, float* topk_w, int32_t* chunk_counts, int* status,
+                        cudaStream_t s) {
+  const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
+  if (nchunks == 0) return cudaSuccess;
+  k_topk<<<nchunks, kTokensPerChunk, 0, s>>>(logits, bias, T, E, k, topk_idx, topk_w,
+                                             chunk_counts, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int capacity,
+                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
+                        int32_t* tile_prefix, int* status, cudaStream_t s) {
+  k_scan<<<1, 256, 0, s>>>(chunk_counts, nchunks, E, capacity, counts, offsets, padded_offsets,
+                           tile_prefix, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offsets_from_counts(const int32_t* counts, int E, int capacity,
+                                       int32_t* offsets, int32_t* padded_offsets,
+                                       int32_t* tile_prefix, int* status, cudaStream_t s) {
+  k_offsets_from_counts<<<1, 256, 0, s>>>(counts, E, capacity, offsets, padded_offsets,
+                                          tile_prefix, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_assign(const int32_t* topk_idx, int T, int E, int k,
+                          const int32_t* chunk_base, const int32_t* padded_offsets,
+                          int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s) {
+  const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
+  if (nchunks == 0) return cudaSuccess;
+  k_assign<<<nchunks, kTokensPerChunk, 0, s>>>(topk_idx, T, E, k, chunk_base, padded_offsets,
+                                               row_src, row_of, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows(const void* x, const int32_t* row_src,
+                               const int32_t* padded_offsets, int E, int d, int T, int capacity,
+                               void* x_perm, int num_sms, cudaStream_t s) {
+  k_gather_rows<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(x), row_src, padded_offsets,
+                                            E, d / 8, T, capacity, static_cast<uint4*>(x_perm));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_zero_pad_rows(const int32_t* row_src, const int32_t* padded_offsets, int E,
+                                 int width, int capacity, void* rows, int num_sms,
+                                 cudaStream_t s) {
+  k_zero_pad_rows<<<num_sms * 4, 256, 0, s>>>(row_src, padded_offsets, E, width / 8, capacity,
+                                              static_cast<uint4*>(rows));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* w, int T, int k,
+                           int d, void* out, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  k_combine<<<T, 128, 0, s>>>(static_cast<const uint4*>(y), row_of, w, k, d / 8,
+                              static_cast<uint4*>(out));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const void* dout, const void* y, const int32_t* row_of,
+                               const float* w, int T, int k, int d, void* dy, float* dw,
+                               cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  k_combine_bwd<<<T, 128, 0, s>>>(static_cast<const uint4*>(dout), static_cast<const uint4*>(y),
+                                  row_of, w, k, d / 8, static_cast<uint4*>(dy), dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_bwd(const void* dx_perm, const int32_t* row_of, int T, int k, int d,
+                               void* dx, cudaStream_t s) {
+  return launch_combine(dx_perm, row_of, nullptr, T, k, d, dx, s);
+}
+
+cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* idx, int T, int E,
+                             int k, float* dlogits, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  k_route_bwd<<<(T + 7) / 8, 256, 0, s>>>(dw, w, idx, T, E, k, dlogits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_repack_fc1(const void* w1, void* w1p, int E, int F, int width,
+                              cudaStream_t s) {
+  const int F_pad = fc1_pad(F);
+  dim3 grid(2 * F_pad, E);
+  k_repack_fc1<<<grid, width >= 256 ? 256 : 32, 0, s>>>(static_cast<const uint16_t*>(w1),
+                                                       static_cast<uint16_t*>(w1p), F, F_pad,
+                                                       width);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_fc1(const void* w1p, void* w1, int E, int F, int width,
+                              cudaStream_t s) {
+  const int F_pad = fc1_pad(F);
+  dim3 grid(2 * F, E);
+  k_unpack_fc1<<<grid, width >= 256 ? 256 : 32, 0, s>>>(static_cast<const uint16_t*>(w1p),
+                                                       static_cast<uint16_t*>(w1), F, F_pad,
+                                                       width);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group_colsum(const void* g, const int32_t* counts,
+                                const int32_t* padded_offsets, int E, int width, void* out,
+                                cudaStream_t s) {
+  const int pairs = width / 2;
+  dim3 grid((pairs + 255) / 256, E);
+  k_group_colsum<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(g), counts, padded_offsets,
+                                      pairs, static_cast<uint32_t*>(out));
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,124 @@
+"""One routed-expert MLP layer on one GPU: device buffers plus the sequence
+of C-ABI calls that makes a forward and a backward pass.
+
+Torch is used only to allocate device memory and to name the stream; every
+step of the path runs in libmoe's kernels.  All buffers are allocated once
+for the worst case (capacity = T*k + E*127 rows), so a whole step can be
+captured in one CUDA graph and replayed with no host synchronisation.
+"""
+from __future__ import annotations
+
+import math
+
+import torch
+
+from . import _lib as L
+
+
+class MoEExpertMLP:
+    def __init__(self, E, d, F, T=0, k=1, act="swiglu", alpha=1.0, limit=math.inf,
+                 linear_offset=0.0, out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0,
+                 capacity=None, device="cuda"):
+        self.desc = L.make_desc(T, E, k, d, F, act=act, alpha=alpha, limit=limit,
+                                linear_offset=linear_offset, out_scale=out_scale,
+                                has_b1=has_b1, has_b2=has_b2, sm_margin=sm_margin,
+                                capacity=capacity)
+        self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
+        self.Fp = L.moe_fc1_padded_width(F)
+        self.has_b1, self.has_b2 = has_b1, has_b2
+        cap = self.desc.capacity
+        self.capacity = cap
+        dev = torch.device(device)
+        bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+
+        def z(*shape, dtype=bf):
+            return torch.zeros(shape, dtype=dtype, device=dev)
+
+        # weights (FC1 kept repacked) and their gradients
+        self.w1p = z(E, 2 * self.Fp, d)
+        self.b1p = z(E, 2 * self.Fp) if has_b1 else None
+        self.w2 = z(E, d, F)
+        self.b2 = z(E, d) if has_b2 else None
+        self.dw1p = z(E, 2 * self.Fp, d)
+        self.db1p = z(E, 2 * self.Fp) if has_b1 else None
+        self.dw2 = z(E, d, F)
+        self.db2 = z(E, d) if has_b2 else None
+        # routing state (device resident)
+        self.topk_idx = z(max(T, 1), k, dtype=i32)
+        self.topk_w = z(max(T, 1), k, dtype=f32)
+        self.counts = z(E, dtype=i32)
+        self.offsets = z(E + 1, dtype=i32)
+        self.padded_offsets = z(E + 1, dtype=i32)
+        self.tile_prefix = z(E + 1, dtype=i32)
+        self.row_src = z(cap, dtype=i32)
+        self.row_of = z(max(T, 1), k, dtype=i32)
+        # per-row activations and gradients (padded row layout)
+        self.x_perm = z(cap, d)
+        self.h = z(cap, 2 * self.Fp)
+        self.a = z(cap, F)
+        self.y = z(cap, d)
+        self.dy = z(cap, d)
+        self.dh = z(cap, 2 * self.Fp)
+        self.dx_perm = z(cap, d)
+        # per-token outputs
+        self.out = z(max(T, 1), d)
+        self.dw = z(max(T, 1), k, dtype=f32)
+        self.dx = z(max(T, 1), d)
+        self.dlogits = z(max(T, 1), E, dtype=f32)
+        self.ws = torch.zeros(max(L.moe_workspace_size(self.desc), 256), dtype=torch.uint8, device=dev)
+
+    # ------------------------------------------------------------ weights
+    def load_weights(self, w1, b1, w2, b2, stream=None):
+        """w1 [E,2F,d] logical (gate rows then linear rows), b1 [E,2F], w2
+        [E,d,F], b2 [E,d]; bf16 device tensors.  FC1 is repacked on device."""
+        L.moe_repack_fc1(self.desc, w1, b1 if self.has_b1 else None, self.w1p,
+                         self.b1p if self.has_b1 else None, stream)
+        self.w2.copy_(w2)
+        if self.has_b2:
+            self.b2.copy_(b2)
+
+    def unpack_fc1(self, packed, width, stream=None):
+        """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p)."""
+        out = torch.empty((self.E, 2 * self.F, width), dtype=torch.bfloat16, device=packed.device)
+        L.moe_unpack_fc1(self.desc, packed, out, width, stream)
+        return out
+
+    # ------------------------------------------------------------ passes
+    def route(self, x, logits, bias=None, stream=None):
+        L.moe_route_permute(self.desc, logits, bias, x, self.topk_idx, self.topk_w, self.counts,
+                            self.offsets, self.padded_offsets, self.tile_prefix, self.row_src,
+                            self.row_of, self.x_perm, self.ws, stream)
+
+    def set_groups(self, counts, stream=None):
+        """Groups given directly (no router): counts int32 [E] on device."""
+        self.counts.copy_(counts)
+        L.moe_group_offsets(self.desc, self.counts, self.offsets, self.padded_offsets,
+                            self.tile_prefix, stream)
+
+    def mlp_forward(self, stream=None):
+        L.moe_mlp_fwd(self.desc, self.x_perm, self.counts, self.padded_offsets, self.w1p, self.b1p,
+                      self.w2, self.b2, self.h, self.a, self.y, self.ws, stream)
+
+    def mlp_backward(self, stream=None):
+        L.moe_mlp_bwd(self.desc, self.dy, self.x_perm, self.h, self.a, self.counts,
+                      self.padded_offsets, self.w1p, self.w2, self.dh, self.dx_perm, self.dw1p,
+                      self.db1p, self.dw2, self.db2, self.ws, stream)
+
+    def forward(self, x, logits, bias=None, stream=None):
+        self.route(x, logits, bias, stream)
+        self.mlp_forward(stream)
+        L.moe_unpermute_combine(self.desc, self.y, self.row_of, self.topk_w, self.out, stream)
+        return self.out
+
+    def backward(self, dout, stream=None):
+        L.moe_unpermute_combine_bwd(self.desc, dout, self.y, self.row_of, self.topk_w, self.row_src,
+                                    self.padded_offsets, self.dy, self.dw, stream)
+        self.mlp_backward(stream)
+        L.moe_permute_bwd(self.desc, self.dx_perm, self.row_of, self.dx, stream)
+        L.moe_route_bwd(self.desc, self.dw, self.topk_w, self.topk_idx, self.dlogits, stream)
+        return self.dx
+
+    def step(self, x, logits, bias, dout, stream=None):
+        """One whole forward + backward pass of the layer."""
+        self.forward(x, logits, bias, stream)
+        self.backward(dout, stream)

@@ -1,0 +1,136 @@
+"""Runs one synthetic layer through the CUDA library and through the oracle
+on the same seeded inputs, and compares the results.
+
+The CUDA side goes through the C-ABI (via the thin binding); the oracle side
+is the fp64 CPU oracle.  The two share only the input generator.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from workloads import bf16_bits_to_f64
+
+TOL_REL = 1e-2      # max|gpu - ref| <= 1e-2 * max|ref| + 1e-3 (bf16 path)
+TOL_ABS = 1e-3
+
+
+def bits_to_dev(bits, device="cuda"):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def to_np(t):
+    if t.dtype == torch.bfloat16:
+        return t.float().cpu().numpy().astype(np.float64)
+    return t.cpu().numpy()
+
+
+def assert_close(name, got, ref, rel=TOL_REL, abs_=TOL_ABS):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    assert np.all(np.isfinite(got)), f"{name}: non-finite values"
+    err = float(np.max(np.abs(got - ref))) if got.size else 0.0
+    bound = rel * (float(np.max(np.abs(ref))) if ref.size else 0.0) + abs_
+    assert err <= bound, f"{name}: max err {err:.3e} > bound {bound:.3e}"
+    return err, bound
+
+
+def glu_params(wl):
+    return oracle.GluParams(wl.act, wl.alpha, wl.limit, wl.linear_offset, wl.out_scale)
+
+
+def oracle_weights(inp):
+    W1 = bf16_bits_to_f64(inp["w1"])
+    W2 = bf16_bits_to_f64(inp["w2"])
+    b1 = bf16_bits_to_f64(inp["b1"]) if inp["b1"] is not None else None
+    b2 = bf16_bits_to_f64(inp["b2"]) if inp["b2"] is not None else None
+    return W1, b1, W2, b2
+
+
+def run_oracle_routed(wl, inp):
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    x = bf16_bits_to_f64(inp["x"])
+    fwd = oracle.moe_forward(x, inp["logits"], inp["bias"], W1, b1, W2, b2, wl.k, p, align=128)
+    bwd = oracle.moe_backward(fwd, bf16_bits_to_f64(inp["dout"]), W1, W2, p)
+    return fwd, bwd
+
+
+def make_layer(wl, **kw):
+    from moe_expert_mlp_gb300 import MoEExpertMLP
+    return MoEExpertMLP(wl.E, wl.d, wl.F, T=wl.T, k=wl.k, act=wl.act, alpha=wl.alpha,
+                        limit=wl.limit, linear_offset=wl.linear_offset, out_scale=wl.out_scale,
+                        has_b1=wl.has_b1, has_b2=wl.has_b2, **kw)
+
+
+def load_layer_weights(layer, inp):
+    w1 = bits_to_dev(inp["w1"])
+    w2 = bits_to_dev(inp["w2"])
+    b1 = bits_to_dev(inp["b1"]) if inp["b1"] is not None else None
+    b2 = bits_to_dev(inp["b2"]) if inp["b2"] is not None else None
+    layer.load_weights(w1, b1, w2, b2)
+
+
+def run_gpu_routed(wl, inp, layer=None, **kw):
+    layer = layer or make_layer(wl, **kw)
+    load_layer_weights(layer, inp)
+    x = bits_to_dev(inp["x"])
+    logits = torch.from_numpy(inp["logits"]).cuda()
+    bias = torch.from_numpy(inp["bias"]).cuda() if inp["bias"] is not None else None
+    dout = bits_to_dev(inp["dout"])
+    layer.step(x, logits, bias, dout)
+    torch.cuda.synchronize()
+    return layer
+
+
+def padded_rows(rows_bits, sizes, padded_offsets, width):
+    """Place rows given in expert order into the padded layout (input prep
+    for workloads whose groups are given directly)."""
+    R_pad = int(padded_offsets[-1])
+    out = np.zeros((R_pad, width), dtype=np.uint16)
+    src = 0
+    for e, m in enumerate(sizes):
+        lo = int(padded_offsets[e])
+        out[lo:lo + m] = rows_bits[src:src + m]
+        src += m
+    return out
+
+
+def run_both_direct(wl, inp):
+    """Groups given directly: x rows and dY rows in expert order."""
+    sizes = inp["group_sizes"]
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    offsets, padded, tiles = oracle.group_offsets(sizes, align=128)
+    xp_bits = padded_rows(inp["x"], sizes, padded, wl.d)
+    dy_bits = padded_rows(inp["dout"], sizes, padded, wl.d)
+    xp = bf16_bits_to_f64(xp_bits)
+    dyp = bf16_bits_to_f64(dy_bits)
+    H, A, Y = oracle.grouped_forward(xp, padded, sizes, W1, b1, W2, b2, p)
+    dX, dH, dW1, db1, dW2, db2 = oracle.grouped_backward(xp, H, A, dyp, padded, sizes, W1, W2, p)
+    ref = dict(H=H, A=A, Y=Y, dX_perm=dX, dH=dH, dW1=dW1, db1=db1, dW2=dW2, db2=db2,
+               padded_offsets=padded, offsets=offsets, tile_prefix=tiles, counts=sizes)
+
+    cap = max(128, int(padded[-1]))
+    layer = make_layer(wl, capacity=cap)
+    load_layer_weights(layer, inp)
+    layer.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
+    R_pad = int(padded[-1])
+    layer.x_perm[:R_pad].copy_(bits_to_dev(xp_bits))
+    layer.dy[:R_pad].copy_(bits_to_dev(dy_bits))
+    layer.mlp_forward()
+    layer.mlp_backward()
+    torch.cuda.synchronize()
+    return layer, ref
+
+
+def packed_to_logical_cols(t_np, F):
+    """GPU packed FC1-shaped columns -> logical (gate then linear) columns;
+    also returns the packed padding columns for a zero check."""
+    src = oracle.fc1_packed_columns(F)
+    out = np.zeros(t_np.shape[:-1] + (2 * F,))
+    ok = src >= 0
+    out[..., src[ok]] = t_np[..., ok]
+    return out, t_np[..., ~ok]

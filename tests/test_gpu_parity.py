@@ -1,0 +1,138 @@
+"""GPU parity: the CUDA path (through the C-ABI) against the fp64 oracle on
+the same seeded inputs.
+
+Bit-exact: routing indices, counts, offsets, padded offsets, tile prefix,
+row_src, row_of, x_perm bytes, repacked weight bytes.  Floats: max|gpu-ref|
+<= 1e-2*max|ref| + 1e-3 per tensor (bf16 storage, fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import harness as H
+from workloads import WORKLOADS, make_inputs, scaled
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+BASE = WORKLOADS["bf16_t4096_e64"]
+
+# parity cases the oracle finishes in seconds; several tiles and ragged tails
+CASES = {
+    "e8_k2": scaled(BASE, T=512, E=8, k=2, d=256, F=256),
+    "e16_k6_bias_raggedF": scaled(BASE, T=600, E=16, k=6, d=320, F=352),
+    "gptoss_small": scaled(WORKLOADS["gptoss_t16384_e32"], T=300, E=8, k=4, d=192, F=224),
+    "geglu": scaled(BASE, T=256, E=4, k=2, d=128, F=384, act="geglu", router_bias=False),
+    "sreglu_scaled": scaled(BASE, T=256, E=4, k=1, d=256, F=128, act="sreglu", out_scale=0.5,
+                            router_bias=False),
+}
+
+
+def _check_routing(layer, fwd, wl):
+    T, k, E = wl.T, wl.k, wl.E
+    assert np.array_equal(H.to_np(layer.topk_idx)[:T], fwd["topk_idx"])
+    assert np.array_equal(H.to_np(layer.counts), fwd["counts"])
+    assert np.array_equal(H.to_np(layer.offsets), fwd["offsets"])
+    assert np.array_equal(H.to_np(layer.padded_offsets), fwd["padded_offsets"])
+    assert np.array_equal(H.to_np(layer.tile_prefix), fwd["tile_prefix"])
+    R_pad = int(fwd["padded_offsets"][-1])
+    assert np.array_equal(H.to_np(layer.row_src)[:R_pad], fwd["row_src"])
+    assert np.array_equal(H.to_np(layer.row_of)[:T], fwd["row_of"])
+    # permuted rows are copies of bf16 input rows: exact
+    assert np.array_equal(H.to_np(layer.x_perm)[:R_pad], fwd["x_perm"])
+    H.assert_close("topk_w", H.to_np(layer.topk_w)[:T], fwd["topk_w"], rel=1e-5, abs_=1e-6)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_fwd_bwd_parity(name):
+    wl = CASES[name]
+    inp = make_inputs(wl)
+    fwd, bwd = H.run_oracle_routed(wl, inp)
+    layer = H.run_gpu_routed(wl, inp)
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    _check_routing(layer, fwd, wl)
+    R_pad = int(fwd["padded_offsets"][-1])
+    T = wl.T
+    h_log, h_pad = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
+    assert np.all(h_pad == 0)
+    H.assert_close("H", h_log, fwd["H"])
+    H.assert_close("A", H.to_np(layer.a)[:R_pad], fwd["A"])
+    H.assert_close("Y", H.to_np(layer.y)[:R_pad], fwd["Y"])
+    H.assert_close("out", H.to_np(layer.out)[:T], fwd["out"])
+    H.assert_close("dY", H.to_np(layer.dy)[:R_pad], bwd["dY"])
+    H.assert_close("dw", H.to_np(layer.dw)[:T], bwd["dw"])
+    dh_log, dh_pad = H.packed_to_logical_cols(H.to_np(layer.dh)[:R_pad], wl.F)
+    assert np.all(dh_pad == 0)
+    H.assert_close("dH", dh_log, bwd["dH"])
+    H.assert_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], bwd["dX_perm"])
+    H.assert_close("dW2", H.to_np(layer.dw2), bwd["dW2"])
+    dw1 = H.to_np(layer.unpack_fc1(layer.dw1p, wl.d))
+    H.assert_close("dW1", dw1, bwd["dW1"])
+    if wl.has_b1:
+        db1 = H.to_np(layer.unpack_fc1(layer.db1p.reshape(wl.E, -1, 1).contiguous(), 1))[..., 0]
+        H.assert_close("db1", db1, bwd["db1"])
+    if wl.has_b2:
+        H.assert_close("db2", H.to_np(layer.db2), bwd["db2"])
+    H.assert_close("dx", H.to_np(layer.dx)[:T], bwd["dx"])
+    H.assert_close("dlogits", H.to_np(layer.dlogits)[:T], bwd["dlogits"])
+
+
+def test_repack_is_bit_exact():
+    wl = CASES["e16_k6_bias_raggedF"]
+    inp = make_inputs(scaled(wl, has_b1=True, b_std=0.01))
+    layer = H.make_layer(scaled(wl, has_b1=True))
+    H.load_layer_weights(layer, inp)
+    torch.cuda.synchronize()
+    w1p_ref, b1p_ref = oracle.repack_fc1(inp["w1"], inp["b1"])
+    got = layer.w1p.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(got, w1p_ref)
+    assert np.array_equal(layer.b1p.view(torch.int16).cpu().numpy().view(np.uint16), b1p_ref)
+    back = layer.unpack_fc1(layer.w1p, wl.d).view(torch.int16).cpu().numpy().view(np.uint16)
+    assert np.array_equal(back, inp["w1"])
+
+
+def test_direct_groups_with_empty_experts():
+    """Groups given directly, Zipf sizes with empty experts and a group of 1."""
+    wl = scaled(WORKLOADS["dsv3_r16384_e32"], R=700, E=9, d=256, F=192, zipf_empty=3)
+    inp = make_inputs(wl)
+    inp["group_sizes"][np.argmax(inp["group_sizes"])] -= 1
+    small = int(np.flatnonzero(inp["group_sizes"] == 0)[0])
+    inp["group_sizes"][small] = 1
+    layer, ref = H.run_both_direct(wl, inp)
+    R_pad = int(ref["padded_offsets"][-1])
+    h_log, _ = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
+    H.assert_close("H", h_log, ref["H"])
+    H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
+    H.assert_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
+    H.assert_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
+    H.assert_close("dW2", H.to_np(layer.dw2), ref["dW2"])
+    H.assert_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    # experts with no rows get exactly zero weight gradients
+    for e in np.flatnonzero(ref["counts"] == 0):
+        assert torch.count_nonzero(layer.dw2[e]) == 0
+        assert torch.count_nonzero(layer.dw1p[e]) == 0
+
+
+def test_dense_single_group():
+    """One group (E=1): the grouped GEMM is a dense MLP."""
+    wl = scaled(WORKLOADS["dense_m16384"], R=389, d=384, F=640)
+    inp = make_inputs(wl)
+    layer, ref = H.run_both_direct(wl, inp)
+    R_pad = int(ref["padded_offsets"][-1])
+    H.assert_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
+    H.assert_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
+    H.assert_close("dW2", H.to_np(layer.dw2), ref["dW2"])
+    H.assert_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+
+
+def test_deterministic_bitwise():
+    wl = CASES["e16_k6_bias_raggedF"]
+    inp = make_inputs(wl)
+    layer = H.run_gpu_routed(wl, inp)
+    snap = {n: getattr(layer, n).clone() for n in ("out", "dx", "dw1p", "dw2", "dlogits", "h")}
+    H.run_gpu_routed(wl, inp, layer=layer)
+    for n, t in snap.items():
+        assert torch.equal(getattr(layer, n).view(torch.uint8) if t.dtype != torch.float32 else getattr(layer, n),
+                           t.view(torch.uint8) if t.dtype != torch.float32 else t), n

@@ -1,0 +1,60 @@
+"""The C-ABI library builds, loads without a GPU, and exports every entry
+point that include/moe.h declares; the binding refuses to run without it."""
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_entry_points():
+    names = []
+    for fn in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if not fn.endswith(".h"):
+            continue
+        src = open(os.path.join(ROOT, "include", fn)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*(moe_[a-z0-9_]+)\s*\(",
+                            src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def libmoe():
+    from moe_expert_mlp_gb300.build import build_library
+    build_library()
+    import moe_expert_mlp_gb300 as m
+    return m.lib()
+
+
+def test_header_declares_the_boundary():
+    names = declared_entry_points()
+    for required in ("moe_repack_fc1", "moe_route_permute", "moe_mlp_fwd", "moe_mlp_bwd",
+                     "moe_unpermute_combine", "moe_unpermute_combine_bwd", "moe_permute_bwd",
+                     "moe_route_bwd", "moe_workspace_size", "moe_read_device_status"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(libmoe):
+    for name in declared_entry_points():
+        assert hasattr(libmoe, name), name
+    import moe_expert_mlp_gb300 as m
+    assert sorted(m.EXPORTS) == declared_entry_points()
+
+
+def test_host_side_errors_without_gpu(libmoe):
+    import ctypes
+    import moe_expert_mlp_gb300 as m
+    desc = m.make_desc(T=64, E=4, k=2, d=128, F=64)
+    n = ctypes.c_size_t(0)
+    assert libmoe.moe_workspace_size(ctypes.byref(desc), ctypes.byref(n)) == 0
+    assert n.value >= 256
+    assert libmoe.moe_workspace_size(None, ctypes.byref(n)) == 1            # MOE_ERR_NULL
+    bad = m.make_desc(T=64, E=4, k=2, d=100, F=64)
+    assert libmoe.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 2  # MOE_ERR_SHAPE
+    bad = m.make_desc(T=64, E=4, k=2, d=128, F=64)
+    bad.align = 32
+    assert libmoe.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 3  # unsupported
+    assert m.moe_fc1_padded_width(2880) == 2944 and m.moe_fc1_padded_width(1408) == 1408
+    assert libmoe.moe_status_string(2) == b"sizes out of the supported range"
