@@ -1,0 +1,549 @@
+#!/usr/bin/env python3
+"""Benchmark: one routed-expert MLP layer, forward + backward, on GB300.
+
+A step is one whole pass of the hot path over one batch of synthetic input:
+routing + permute -> FC1 grouped GEMM with the GLU epilogue -> FC2 grouped
+GEMM -> weighted combine -> combine backward -> FC2 dgrad with the dGLU
+epilogue -> FC2 wgrad -> FC1 dgrad -> FC1 wgrad -> permute backward ->
+router backward.  Default workload: T=4096 tokens, E=64 experts, top-6,
+d=2048, F=1408 (SwiGLU, bf16), logits ~N(0,1) plus a per-expert bias.
+
+The K timed steps are captured in one CUDA graph (no host synchronisation
+inside) with timing events around every library call, replayed once between
+a barrier + synchronize on both sides.  value = algorithmic TFLOPS
+(18*d*F per routed row, padding not counted) of the whole job.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload NAME]
+
+--impl reference times the CPU fp64 oracle (the method written out plainly)
+on a bounded sample of the same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+from workloads import WORKLOADS, bf16_bits_to_f64, make_inputs  # noqa: E402
+
+METRIC = "MoE expert-MLP fwd+bwd TFLOPS & tokens/s on 1 GB300; % of tensor-core peak"
+DEFAULT_WORKLOAD = "bf16_t4096_e64"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch from one ncu capture, with the hash of
+# the GEMM source the counters were taken on; a changed kernel reports null.
+NCU_TRAFFIC = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def gemm_source_hash():
+    h = hashlib.sha256()
+    for fn in ("moe_gemm.cu", "moe_ptx.cuh", "moe_internal.h"):
+        with open(os.path.join(ROOT, "moe_expert_mlp_gb300", "csrc", fn), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# --------------------------------------------------------------- per-call work
+def call_work(wl, name, R):
+    """Algorithmic FLOPs or bytes of one library call over R real routed rows.
+    GEMMs: 2*M*N*K with M = routed rows.  Memory-bound calls: bytes of the
+    tensors they must read and write once (bf16 rows, index arrays ignored)."""
+    d, F, T, k = wl.d, wl.F, wl.T, wl.k
+    gemm = {
+        "fc1_glu_fwd": 2.0 * R * d * 2 * F,
+        "fc2_fwd": 2.0 * R * F * d,
+        "fc2_dgrad_dglu": 2.0 * R * d * F,
+        "fc2_wgrad": 2.0 * R * d * F,
+        "fc1_dgrad": 2.0 * R * 2 * F * d,
+        "fc1_wgrad": 2.0 * R * 2 * F * d,
+    }
+    if name in gemm:
+        return "flop", gemm[name]
+    mem = {
+        "route_permute": T * wl.E * 4 + T * d * 2 + R * d * 2,
+        "combine": R * d * 2 + T * d * 2,
+        "combine_bwd": T * d * 2 + R * d * 2 + R * d * 2,
+        "permute_bwd": R * d * 2 + T * d * 2,
+        "route_bwd": T * k * 12 + T * wl.E * 4,
+        "bias_grads": R * d * 2 * int(wl.has_b2) + R * 2 * F * 2 * int(wl.has_b1),
+    }
+    return "byte", float(mem.get(name, 0.0))
+
+
+# ------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock / throttle sampling while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id):
+        self.path = tempfile.mktemp(prefix="moe_clocks_", suffix=".csv")
+        cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if gpu_id is not None:
+            cmd += ["-i", gpu_id]
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                    power.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power) if power else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def gpu_uuid(torch, dev):
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+# ------------------------------------------------------------ oracle timing
+def oracle_sample_run(wl, inp, n_tokens):
+    """Time the CPU oracle on the first n_tokens tokens (routed workloads) or
+    on the first experts holding about n_tokens rows (direct workloads).
+    Returns (seconds, flops of the sample, description)."""
+    import oracle
+    p = oracle.GluParams(wl.act, wl.alpha, wl.limit, wl.linear_offset, wl.out_scale)
+    W1 = bf16_bits_to_f64(inp["w1"])
+    W2 = bf16_bits_to_f64(inp["w2"])
+    b1 = bf16_bits_to_f64(inp["b1"]) if inp["b1"] is not None else None
+    b2 = bf16_bits_to_f64(inp["b2"]) if inp["b2"] is not None else None
+    if wl.router != "direct":
+        n = min(n_tokens, wl.T)
+        x = bf16_bits_to_f64(inp["x"][:n])
+        dout = bf16_bits_to_f64(inp["dout"][:n])
+        t0 = time.perf_counter()
+        fwd = oracle.moe_forward(x, inp["logits"][:n], inp["bias"], W1, b1, W2, b2, wl.k, p)
+        oracle.moe_backward(fwd, dout, W1, W2, p)
+        dt = time.perf_counter() - t0
+        rows = n * wl.k
+        desc = f"first {n} of {wl.T} tokens ({rows} routed rows), full fwd+bwd"
+    else:
+        sizes = inp["group_sizes"]
+        keep = np.zeros_like(sizes)
+        acc = 0
+        for e in np.argsort(sizes):
+            if sizes[e] == 0:
+                continue
+            if acc + sizes[e] > max(n_tokens, 1) and acc > 0:
+                break
+            keep[e] = sizes[e]
+            acc += sizes[e]
+        offsets, padded, _ = oracle.group_offsets(keep, align=128)
+        xr = np.zeros((int(padded[-1]), wl.d))
+        dyr = np.zeros((int(padded[-1]), wl.d))
+        src_off = np.concatenate([[0], np.cumsum(sizes)])
+        for e in range(wl.E):
+            if keep[e]:
+                lo = int(padded[e])
+                xr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["x"][src_off[e]:src_off[e] + keep[e]])
+                dyr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["dout"][src_off[e]:src_off[e] + keep[e]])
+        t0 = time.perf_counter()
+        Hh, A, Y = oracle.grouped_forward(xr, padded, keep, W1, b1, W2, b2, p)
+        oracle.grouped_backward(xr, Hh, A, dyr, padded, keep, W1, W2, p)
+        dt = time.perf_counter() - t0
+        rows = int(acc)
+        desc = f"{int((keep > 0).sum())} smallest experts ({rows} of {wl.R} rows), fwd+bwd"
+    flops = (18 if wl.gated else 12) * wl.d * wl.F * rows
+    return dt, float(flops), desc
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    inp = make_inputs(wl)
+    n_tok = args.ref_sample_tokens
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample_run(wl, inp, n_tok)
+    times = []
+    flops = 0.0
+    desc = ""
+    for _ in range(args.steps):
+        dt, flops, desc = oracle_sample_run(wl, inp, n_tok)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOPS",
+        "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
+                         "sample": "each step: " + desc},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def workload_config(wl):
+    cfg = {"workload": wl.name, "E": wl.E, "d": wl.d, "F": wl.F, "act": wl.act,
+           "routed_rows": wl.routed_rows}
+    if wl.router != "direct":
+        cfg.update({"T": wl.T, "k": wl.k, "router_bias": wl.router_bias})
+    else:
+        cfg.update({"groups": "zipf s=%.1f, %d empty" % (wl.zipf_s, wl.zipf_empty)
+                    if wl.E > 1 else "one group"})
+    if wl.limit != float("inf"):
+        cfg.update({"limit": wl.limit, "alpha": wl.alpha, "linear_offset": wl.linear_offset})
+    cfg["bias"] = bool(wl.has_b1 or wl.has_b2)
+    cfg["l2"] = "no flush: working set (weights + activations) far above the 129 MB L2"
+    return cfg
+
+
+# --------------------------------------------------------------- GPU bench
+def run_ours(args, wl):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import __graft_entry__
+    __graft_entry__.build()
+    from moe_expert_mlp_gb300 import MoEExpertMLP, moe_read_device_status
+
+    def bits_to_dev(bits, device):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+    inp = make_inputs(wl)
+    routed = wl.router != "direct"
+    cap = None
+    if not routed:
+        sizes = inp["group_sizes"]
+        cap = int(sum((int(m) + 127) // 128 * 128 for m in sizes))
+        cap = max(cap, 128)
+    layer = MoEExpertMLP(wl.E, wl.d, wl.F, T=wl.T if routed else 0, k=wl.k, act=wl.act,
+                         alpha=wl.alpha, limit=wl.limit, linear_offset=wl.linear_offset,
+                         out_scale=wl.out_scale, has_b1=wl.has_b1, has_b2=wl.has_b2,
+                         capacity=cap, device=dev)
+    w1 = bits_to_dev(inp["w1"], dev)
+    w2 = bits_to_dev(inp["w2"], dev)
+    b1 = bits_to_dev(inp["b1"], dev) if inp["b1"] is not None else None
+    b2 = bits_to_dev(inp["b2"], dev) if inp["b2"] is not None else None
+    layer.load_weights(w1, b1, w2, b2)
+    del w1, w2
+    if routed:
+        x = bits_to_dev(inp["x"], dev)
+        logits = torch.from_numpy(inp["logits"]).to(dev)
+        bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+        dout = bits_to_dev(inp["dout"], dev)
+
+        def step(timer=None):
+            layer.step(x, logits, bias, dout, timer=timer)
+    else:
+        layer.set_groups(torch.from_numpy(inp["group_sizes"].astype(np.int32)).to(dev))
+        po = layer.padded_offsets.cpu().numpy()          # set-up only, outside timing
+        xs, dys = bits_to_dev(inp["x"], dev), bits_to_dev(inp["dout"], dev)
+        src = 0
+        for e, m in enumerate(inp["group_sizes"]):
+            m = int(m)
+            layer.x_perm[po[e]:po[e] + m].copy_(xs[src:src + m])
+            layer.dy[po[e]:po[e] + m].copy_(dys[src:src + m])
+            src += m
+        del xs, dys
+
+        def step(timer=None):
+            layer.grouped_step(timer=timer)
+
+    R = wl.routed_rows
+    flops_step = wl.flops_fwd_bwd()
+    K, W = args.steps, max(args.warmup, 3)
+    stream = torch.cuda.current_stream()
+
+    # timing events inside the graph: one pair per library call per step
+    names = []
+    step(timer=lambda n: (names.append(n), _Null())[1])
+    torch.cuda.synchronize()
+    try:
+        torch.cuda.Event(enable_timing=True, external=True)
+        ext = True
+    except TypeError:
+        ext = False
+
+    class Timer:
+        def __init__(self):
+            self.ev = []
+
+        def __call__(self, name):
+            a = torch.cuda.Event(enable_timing=True, external=ext)
+            b = torch.cuda.Event(enable_timing=True, external=ext)
+            self.ev.append((name, a, b))
+            return _Rec(a, b)
+
+    timer = Timer()
+    use_graph = ext and not args.no_graph
+    graph = None
+    if use_graph:
+        warm = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(warm):
+            step()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(K):
+                step(timer=timer)
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(torch, local))
+    # warm-up: W steps, then more until about a second of work has run so
+    # that the clock samples describe the loaded GPU
+    t_w = time.perf_counter()
+    i = 0
+    while i < W or time.perf_counter() - t_w < 1.0:
+        if use_graph:
+            warm.replay()
+        else:
+            step()
+        i += 1
+        if i % 8 == 0:
+            torch.cuda.synchronize()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    if use_graph:
+        graph.replay()
+    else:
+        for _ in range(K):
+            step(timer=timer)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms_total = t0.elapsed_time(t1)
+    status = moe_read_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status word {status:#x} set during the timed region")
+
+    # per-call durations inside the timed region
+    per = {}
+    for name, a, b in timer.ev:
+        per.setdefault(name, []).append(a.elapsed_time(b))
+    ms_max = ms_total
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_max = float(tt.item())
+
+    # end-to-end: host buffers in pinned memory, copies inside the timed region
+    e2e = None
+    if not args.no_e2e and routed:
+        e2e = run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peak_src = load_peaks()
+    ms_step = ms_max / K
+    value = flops_step * K * world / (ms_max * 1e-3) / 1e12
+    kernels = {}
+    dominant, dom_ms = None, -1.0
+    for name, ts in per.items():
+        kind, work = call_work(wl, name, R)
+        avg = sum(ts) / len(ts)
+        ent = {"ms": round(avg, 5)}
+        if kind == "flop":
+            ent["tflops"] = round(work / (avg * 1e-3) / 1e12, 2)
+            if sum(ts) > dom_ms:
+                dominant, dom_ms = name, sum(ts)
+        elif work > 0:
+            ent["gbs"] = round(work / (avg * 1e-3) / 1e9, 1)
+        kernels[name] = ent
+    kind, work = call_work(wl, dominant, R)
+    dom_avg = sum(per[dominant]) / len(per[dominant])
+    achieved = work / (dom_avg * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    tr = NCU_TRAFFIC.get((dominant, wl.name))
+    traffic = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
+        "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(wl), parallelism=f"replicas x{world}",
+                       graph=bool(use_graph)),
+        "tokens_per_s": round((wl.T if routed else R) * K * world / (ms_max * 1e-3), 1),
+        "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
+                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_source": f"{peak_src} bf16 burst (cuBLAS)"},
+        "kernels": kernels,
+        "gpu_launches": layer.kernels_per_step(routed) * K,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline:
+        dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens)
+        line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": host_cores(),
+                                "kind": "oracle", "sample": desc}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
+    """The same step through the public API with host-resident inputs and
+    results: pinned host -> device copies of x, logits, dout before each
+    step and device -> host copies of out, dx, dlogits after it."""
+    xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    lh = torch.from_numpy(inp["logits"]).pin_memory()
+    dh = torch.from_numpy(inp["dout"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
+    xd, ld, dd = (torch.empty_like(t, device=dev) for t in (xh, lh, dh))
+    outs = [torch.empty(t.shape, dtype=t.dtype).pin_memory()
+            for t in (layer.out, layer.dx, layer.dlogits)]
+
+    def one():
+        xd.copy_(xh, non_blocking=True)
+        ld.copy_(lh, non_blocking=True)
+        dd.copy_(dh, non_blocking=True)
+        layer.step(xd, ld, bias, dd)
+        for o, t in zip(outs, (layer.out, layer.dx, layer.dlogits)):
+            o.copy_(t, non_blocking=True)
+
+    for _ in range(W):
+        one()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(K):
+        one()
+    b.record()
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    h2d = sum(t.numel() * t.element_size() for t in (xh, lh, dh))
+    d2h = sum(t.numel() * t.element_size() for t in outs)
+    return {"value": round(flops_step * K * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / K, 5)}
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *a):
+        return False
+
+
+class _Rec:
+    def __init__(self, a, b):
+        self.a, self.b = a, b
+
+    def __enter__(self):
+        self.a.record()
+        return self
+
+    def __exit__(self, *exc):
+        self.b.record()
+        return False
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-sample-tokens", type=int, default=1024,
+                    help="tokens (or rows) of the oracle sample in the cpu_baseline leg")
+    ap.add_argument("--ref-sample-tokens", type=int, default=256,
+                    help="tokens (or rows) per step of --impl reference")
+    ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, wl)
+    return run_ours(args, wl)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

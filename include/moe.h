@@ -160,6 +160,39 @@ moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          void* h, void* a, void* y, void* ws, size_t ws_bytes,
                          cudaStream_t stream);
 
+/* The grouped GEMMs one at a time (moe_mlp_fwd / moe_mlp_bwd call exactly
+ * these, in this order).  Buffers and layouts as in those two calls.
+ *   moe_fc1_glu_fwd    h, a  <- x_perm, w1p, b1p      (FC1 + GLU epilogue)
+ *   moe_fc2_fwd        y     <- a, w2, b2             (FC2, "GroupGemm")
+ *   moe_fc2_dgrad_dglu dh    <- dy, w2, h             (dGLU epilogue)
+ *   moe_fc2_wgrad      dw2   <- dy, a                 (K = group rows)
+ *   moe_fc1_dgrad      dx_perm <- dh, w1p
+ *   moe_fc1_wgrad      dw1p  <- dh, x_perm            (K = group rows)
+ *   moe_bias_grads     db1p, db2 <- dh, dy            (per-group column sums;
+ *                      either output may be NULL to skip it) */
+moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
+                             const int32_t* counts, const int32_t* padded_offsets,
+                             const void* w1p, const void* b1p, void* h, void* a,
+                             cudaStream_t stream);
+moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
+                         const int32_t* padded_offsets, const void* w2, const void* b2, void* y,
+                         cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, const void* h,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const void* w2, void* dh, cudaStream_t stream);
+moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
+                           const int32_t* counts, const int32_t* padded_offsets, void* dw2,
+                           cudaStream_t stream);
+moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int32_t* counts,
+                           const int32_t* padded_offsets, const void* w1p, void* dx_perm,
+                           cudaStream_t stream);
+moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const void* x_perm,
+                           const int32_t* counts, const int32_t* padded_offsets, void* dw1p,
+                           cudaStream_t stream);
+moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const void* dh,
+                            const int32_t* counts, const int32_t* padded_offsets, void* db1p,
+                            void* db2, cudaStream_t stream);
+
 /* Weighted combine: out[t] = sum_s topk_w[t,s] * y[row_of[t,s]] (fp32 sum in
  * slot order, then bf16).  out [T,d]. */
 moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,

@@ -24,7 +24,8 @@ EXPORTS = (
     "moe_fc1_padded_width", "moe_workspace_size", "moe_repack_fc1", "moe_unpack_fc1",
     "moe_route_permute", "moe_group_offsets", "moe_mlp_fwd", "moe_unpermute_combine",
     "moe_unpermute_combine_bwd", "moe_mlp_bwd", "moe_permute_bwd", "moe_route_bwd",
-    "moe_read_device_status", "moe_status_string",
+    "moe_read_device_status", "moe_status_string", "moe_fc1_glu_fwd", "moe_fc2_fwd",
+    "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
 )
 
 
@@ -79,6 +80,13 @@ def lib():
             "moe_route_bwd": (ctypes.c_int, [D, P, P, P, P, P]),
             "moe_read_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+            "moe_fc1_glu_fwd": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_fwd": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc2_dgrad_dglu": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc2_wgrad": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_dgrad": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_wgrad": (ctypes.c_int, [D] + [P] * 6),
+            "moe_bias_grads": (ctypes.c_int, [D] + [P] * 7),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -181,3 +189,38 @@ def moe_read_device_status(clear=True):
     v = ctypes.c_int32(0)
     _check(lib().moe_read_device_status(ctypes.byref(v), int(clear)))
     return int(v.value)
+
+
+def moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream=None):
+    _check(lib().moe_fc1_glu_fwd(ctypes.byref(desc), _p(x_perm), _p(counts), _p(padded_offsets),
+                                 _p(w1p), _p(b1p), _p(h), _p(a), _stream(stream)))
+
+
+def moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, stream=None):
+    _check(lib().moe_fc2_fwd(ctypes.byref(desc), _p(a), _p(counts), _p(padded_offsets), _p(w2),
+                             _p(b2), _p(y), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, stream=None):
+    _check(lib().moe_fc2_dgrad_dglu(ctypes.byref(desc), _p(dy), _p(h), _p(counts),
+                                    _p(padded_offsets), _p(w2), _p(dh), _stream(stream)))
+
+
+def moe_fc2_wgrad(desc, dy, a, counts, padded_offsets, dw2, stream=None):
+    _check(lib().moe_fc2_wgrad(ctypes.byref(desc), _p(dy), _p(a), _p(counts), _p(padded_offsets),
+                               _p(dw2), _stream(stream)))
+
+
+def moe_fc1_dgrad(desc, dh, counts, padded_offsets, w1p, dx_perm, stream=None):
+    _check(lib().moe_fc1_dgrad(ctypes.byref(desc), _p(dh), _p(counts), _p(padded_offsets), _p(w1p),
+                               _p(dx_perm), _stream(stream)))
+
+
+def moe_fc1_wgrad(desc, dh, x_perm, counts, padded_offsets, dw1p, stream=None):
+    _check(lib().moe_fc1_wgrad(ctypes.byref(desc), _p(dh), _p(x_perm), _p(counts),
+                               _p(padded_offsets), _p(dw1p), _stream(stream)))
+
+
+def moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream=None):
+    _check(lib().moe_bias_grads(ctypes.byref(desc), _p(dy), _p(dh), _p(counts),
+                                _p(padded_offsets), _p(db1p), _p(db2), _stream(stream)))

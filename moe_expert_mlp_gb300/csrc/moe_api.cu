@@ -239,6 +239,61 @@ moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts
                                                 padded_offsets, tile_prefix, di->status, stream));
 }
 
+moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
+                             const int32_t* counts, const int32_t* padded_offsets,
+                             const void* w1p, const void* b1p, void* h, void* a,
+                             cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(2 * Fp);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = 2 * Fp;
+  g.out1 = a;
+  g.ld1 = F;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = 2 * Fp;
+  return cuda_status(launch_grouped_gemm(kFc1Glu, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
+                         const int32_t* padded_offsets, const void* w2, const void* b2, void* y,
+                         cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!a || !counts || !padded_offsets || !w2 || !y) return MOE_ERR_NULL;
+  if (desc->has_b2 && !b2) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, a, F, cap, 1, F * 2, cap * F * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256))
+    return MOE_ERR_SHAPE;
+  g.K = desc->F;
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = y;
+  g.ld0 = d;
+  g.bias = desc->has_b2 ? b2 : nullptr;
+  g.bias_ld = d;
+  return cuda_status(launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream));
+}
+
 moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          const int32_t* counts, const int32_t* padded_offsets,
                          const void* w1p, const void* b1p, const void* w2, const void* b2,
@@ -246,47 +301,10 @@ moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          cudaStream_t stream) {
   (void)ws;
   (void)ws_bytes;
-  moe_status_t st = check_desc(desc, false);
+  if (!w2 || !y || (desc && desc->has_b2 && !b2)) return MOE_ERR_NULL;
+  moe_status_t st = moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream);
   if (st != MOE_OK) return st;
-  if (!x_perm || !counts || !padded_offsets || !w1p || !w2 || !h || !a || !y)
-    return MOE_ERR_NULL;
-  if ((desc->has_b1 && !b1p) || (desc->has_b2 && !b2)) return MOE_ERR_NULL;
-  DeviceInfo* di;
-  if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
-  const uint64_t cap = desc->capacity;
-  const int grid = grid_for(di, desc);
-
-  GemmArgs g1;
-  fill_common(g1, desc, di, counts, padded_offsets);
-  if (!encode_map(&g1.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g1.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256))
-    return MOE_ERR_SHAPE;
-  g1.K = desc->d;
-  g1.n_ext = static_cast<int>(2 * Fp);
-  g1.b_ext = g1.n_ext;
-  g1.out0 = h;
-  g1.ld0 = 2 * Fp;
-  g1.out1 = a;
-  g1.ld1 = F;
-  g1.bias = desc->has_b1 ? b1p : nullptr;
-  g1.bias_ld = 2 * Fp;
-  cudaError_t e = launch_grouped_gemm(kFc1Glu, g1, grid, stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-
-  GemmArgs g2;
-  fill_common(g2, desc, di, counts, padded_offsets);
-  if (!encode_map(&g2.tma_a, a, F, cap, 1, F * 2, cap * F * 2, 64, 128) ||
-      !encode_map(&g2.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256))
-    return MOE_ERR_SHAPE;
-  g2.K = desc->F;
-  g2.n_ext = desc->d;
-  g2.b_ext = desc->d;
-  g2.out0 = y;
-  g2.ld0 = d;
-  g2.bias = desc->has_b2 ? b2 : nullptr;
-  g2.bias_ld = d;
-  return cuda_status(launch_grouped_gemm(kFc2, g2, grid, stream));
+  return moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, stream);
 }
 
 moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
@@ -318,6 +336,120 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
   return cuda_status(e);
 }
 
+moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, const void* h,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const void* w2, void* dh, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dy || !h || !counts || !padded_offsets || !w2 || !dh) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dA = dY W2 with W2 [d,F] read MN-major (F contiguous); dH from H
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(Fp);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = 2 * Fp;
+  g.aux = h;
+  g.ld_aux = 2 * Fp;
+  return cuda_status(launch_grouped_gemm(kDgradDglu, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
+                           const int32_t* counts, const int32_t* padded_offsets, void* dw2,
+                           cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dy || !a || !counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  // dW2[e] (d x F) = sum over the group's rows of dY^T A (both read MN-major)
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
+      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.m_ext = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = dw2;
+  g.ld0 = F;
+  return cuda_status(launch_grouped_gemm(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int32_t* counts,
+                           const int32_t* padded_offsets, const void* w1p, void* dx_perm,
+                           cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dh || !counts || !padded_offsets || !w1p || !dx_perm) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dX = dH W1p with W1p [2F_pad,d] read MN-major (d contiguous)
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dx_perm;
+  g.ld0 = d;
+  return cuda_status(launch_grouped_gemm(kDgradFc1, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const void* x_perm,
+                           const int32_t* counts, const int32_t* padded_offsets, void* dw1p,
+                           cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dh || !x_perm || !counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dW1p[e] (2F_pad x d) = sum over the group's rows of dH^T X
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64) ||
+      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.m_ext = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dw1p;
+  g.ld0 = d;
+  return cuda_status(launch_grouped_gemm(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const void* dh,
+                            const int32_t* counts, const int32_t* padded_offsets, void* db1p,
+                            void* db2, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || (db2 && !dy) || (db1p && !dh)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaError_t e = cudaSuccess;
+  if (db2) e = launch_group_colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream);
+  if (e == cudaSuccess && db1p)
+    e = launch_group_colsum(dh, counts, padded_offsets, desc->E, 2 * fc1_pad(desc->F), db1p,
+                            stream);
+  return cuda_status(e);
+}
+
 moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
                          const void* h, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w1p, const void* w2,
@@ -331,73 +463,17 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
       !dx_perm || !dw1p || !dw2)
     return MOE_ERR_NULL;
   if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
-  DeviceInfo* di;
-  if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
-  const uint64_t cap = desc->capacity;
-  const int grid = grid_for(di, desc);
-  cudaError_t e;
-
-  // FC2 dgrad + dGLU: dA = dY W2 (B = W2 read MN-major), dH from H
-  GemmArgs g;
-  fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
-    return MOE_ERR_SHAPE;
-  g.K = desc->d;
-  g.n_ext = static_cast<int>(Fp);
-  g.b_ext = desc->F;
-  g.out0 = dh;
-  g.ld0 = 2 * Fp;
-  g.aux = h;
-  g.ld_aux = 2 * Fp;
-  if ((e = launch_grouped_gemm(kDgradDglu, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
-
-  // FC2 wgrad: dW2[e] (d x F) = sum_rows dY^T A
-  fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
-      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64))
-    return MOE_ERR_SHAPE;
-  g.m_ext = desc->d;
-  g.n_ext = desc->F;
-  g.b_ext = desc->F;
-  g.out0 = dw2;
-  g.ld0 = F;
-  if ((e = launch_grouped_gemm(kWgrad, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
-
-  // FC1 dgrad: dX = dH W1p (B = W1p read MN-major)
-  fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
-    return MOE_ERR_SHAPE;
-  g.K = static_cast<int>(2 * Fp);
-  g.n_ext = desc->d;
-  g.b_ext = desc->d;
-  g.out0 = dx_perm;
-  g.ld0 = d;
-  if ((e = launch_grouped_gemm(kDgradFc1, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
-
-  // FC1 wgrad: dW1p[e] (2F_pad x d) = sum_rows dH^T X
-  fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64) ||
-      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
-    return MOE_ERR_SHAPE;
-  g.m_ext = static_cast<int>(2 * Fp);
-  g.n_ext = desc->d;
-  g.b_ext = desc->d;
-  g.out0 = dw1p;
-  g.ld0 = d;
-  if ((e = launch_grouped_gemm(kWgrad, g, grid, stream)) != cudaSuccess) return MOE_ERR_CUDA;
-
-  if (desc->has_b2 &&
-      (e = launch_group_colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream)) !=
-          cudaSuccess)
-    return MOE_ERR_CUDA;
-  if (desc->has_b1 &&
-      (e = launch_group_colsum(dh, counts, padded_offsets, desc->E, static_cast<int>(2 * Fp),
-                               db1p, stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  return MOE_OK;
+  if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, stream)) != MOE_OK)
+    return st;
+  if ((st = moe_fc2_wgrad(desc, dy, a, counts, padded_offsets, dw2, stream)) != MOE_OK) return st;
+  if ((st = moe_fc1_dgrad(desc, dh, counts, padded_offsets, w1p, dx_perm, stream)) != MOE_OK)
+    return st;
+  if ((st = moe_fc1_wgrad(desc, dh, x_perm, counts, padded_offsets, dw1p, stream)) != MOE_OK)
+    return st;
+  if (desc->has_b1 || desc->has_b2)
+    st = moe_bias_grads(desc, dy, dh, counts, padded_offsets, desc->has_b1 ? db1p : nullptr,
+                        desc->has_b2 ? db2 : nullptr, stream);
+  return st;
 }
 
 moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,

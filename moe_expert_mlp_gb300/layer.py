@@ -8,6 +8,7 @@ captured in one CUDA graph and replayed with no host synchronisation.
 """
 from __future__ import annotations
 
+import contextlib
 import math
 
 import torch
@@ -84,10 +85,18 @@ class MoEExpertMLP:
         return out
 
     # ------------------------------------------------------------ passes
-    def route(self, x, logits, bias=None, stream=None):
-        L.moe_route_permute(self.desc, logits, bias, x, self.topk_idx, self.topk_w, self.counts,
-                            self.offsets, self.padded_offsets, self.tile_prefix, self.row_src,
-                            self.row_of, self.x_perm, self.ws, stream)
+    # Each pass below is a fixed sequence of C-ABI calls.  `timer`, if given,
+    # is a callable name -> context manager wrapped around each call (used by
+    # the benchmark to time individual kernels); it does no work itself.
+    @staticmethod
+    def _t(timer, name):
+        return timer(name) if timer is not None else contextlib.nullcontext()
+
+    def route(self, x, logits, bias=None, stream=None, timer=None):
+        with self._t(timer, "route_permute"):
+            L.moe_route_permute(self.desc, logits, bias, x, self.topk_idx, self.topk_w,
+                                self.counts, self.offsets, self.padded_offsets, self.tile_prefix,
+                                self.row_src, self.row_of, self.x_perm, self.ws, stream)
 
     def set_groups(self, counts, stream=None):
         """Groups given directly (no router): counts int32 [E] on device."""
@@ -95,30 +104,62 @@ class MoEExpertMLP:
         L.moe_group_offsets(self.desc, self.counts, self.offsets, self.padded_offsets,
                             self.tile_prefix, stream)
 
-    def mlp_forward(self, stream=None):
-        L.moe_mlp_fwd(self.desc, self.x_perm, self.counts, self.padded_offsets, self.w1p, self.b1p,
-                      self.w2, self.b2, self.h, self.a, self.y, self.ws, stream)
+    def mlp_forward(self, stream=None, timer=None):
+        c, po = self.counts, self.padded_offsets
+        with self._t(timer, "fc1_glu_fwd"):
+            L.moe_fc1_glu_fwd(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h, self.a,
+                              stream)
+        with self._t(timer, "fc2_fwd"):
+            L.moe_fc2_fwd(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream)
 
-    def mlp_backward(self, stream=None):
-        L.moe_mlp_bwd(self.desc, self.dy, self.x_perm, self.h, self.a, self.counts,
-                      self.padded_offsets, self.w1p, self.w2, self.dh, self.dx_perm, self.dw1p,
-                      self.db1p, self.dw2, self.db2, self.ws, stream)
+    def mlp_backward(self, stream=None, timer=None):
+        c, po = self.counts, self.padded_offsets
+        with self._t(timer, "fc2_dgrad_dglu"):
+            L.moe_fc2_dgrad_dglu(self.desc, self.dy, self.h, c, po, self.w2, self.dh, stream)
+        with self._t(timer, "fc2_wgrad"):
+            L.moe_fc2_wgrad(self.desc, self.dy, self.a, c, po, self.dw2, stream)
+        with self._t(timer, "fc1_dgrad"):
+            L.moe_fc1_dgrad(self.desc, self.dh, c, po, self.w1p, self.dx_perm, stream)
+        with self._t(timer, "fc1_wgrad"):
+            L.moe_fc1_wgrad(self.desc, self.dh, self.x_perm, c, po, self.dw1p, stream)
+        if self.has_b1 or self.has_b2:
+            with self._t(timer, "bias_grads"):
+                L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2, stream)
 
-    def forward(self, x, logits, bias=None, stream=None):
-        self.route(x, logits, bias, stream)
-        self.mlp_forward(stream)
-        L.moe_unpermute_combine(self.desc, self.y, self.row_of, self.topk_w, self.out, stream)
+    def forward(self, x, logits, bias=None, stream=None, timer=None):
+        self.route(x, logits, bias, stream, timer)
+        self.mlp_forward(stream, timer)
+        with self._t(timer, "combine"):
+            L.moe_unpermute_combine(self.desc, self.y, self.row_of, self.topk_w, self.out, stream)
         return self.out
 
-    def backward(self, dout, stream=None):
-        L.moe_unpermute_combine_bwd(self.desc, dout, self.y, self.row_of, self.topk_w, self.row_src,
-                                    self.padded_offsets, self.dy, self.dw, stream)
-        self.mlp_backward(stream)
-        L.moe_permute_bwd(self.desc, self.dx_perm, self.row_of, self.dx, stream)
-        L.moe_route_bwd(self.desc, self.dw, self.topk_w, self.topk_idx, self.dlogits, stream)
+    def backward(self, dout, stream=None, timer=None):
+        with self._t(timer, "combine_bwd"):
+            L.moe_unpermute_combine_bwd(self.desc, dout, self.y, self.row_of, self.topk_w,
+                                        self.row_src, self.padded_offsets, self.dy, self.dw,
+                                        stream)
+        self.mlp_backward(stream, timer)
+        with self._t(timer, "permute_bwd"):
+            L.moe_permute_bwd(self.desc, self.dx_perm, self.row_of, self.dx, stream)
+        with self._t(timer, "route_bwd"):
+            L.moe_route_bwd(self.desc, self.dw, self.topk_w, self.topk_idx, self.dlogits, stream)
         return self.dx
 
-    def step(self, x, logits, bias, dout, stream=None):
+    def step(self, x, logits, bias, dout, stream=None, timer=None):
         """One whole forward + backward pass of the layer."""
-        self.forward(x, logits, bias, stream)
-        self.backward(dout, stream)
+        self.forward(x, logits, bias, stream, timer)
+        self.backward(dout, stream, timer)
+
+    def grouped_step(self, stream=None, timer=None):
+        """Forward + backward of the expert MLP alone, for groups given
+        directly (x_perm and dy already in place)."""
+        self.mlp_forward(stream, timer)
+        self.mlp_backward(stream, timer)
+
+    def kernels_per_step(self, routed=True):
+        """Kernels of this library launched by one step() (routed) or
+        grouped_step(): six grouped GEMMs, one column-sum per bias, and for
+        the routed layer top-k, scan, assign, gather, combine, pad-row zeroing,
+        combine backward, permute backward and router backward."""
+        n = 6 + int(self.has_b1) + int(self.has_b2)
+        return n + (9 if routed else 0)
