@@ -63,15 +63,18 @@ struct ActP {
   float alpha, limit, lin_off, out_scale;
 };
 
-__device__ __forceinline__ float sigmoid_f(float x) { return 1.0f / (1.0f + __expf(-x)); }
+// sigmoid(x) = 1 / (1 + e^-x); the approximate reciprocal is within a few
+// ulp and returns 0 when e^-x overflows to +inf.
+__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
 
+template <int ACT>
 __device__ __forceinline__ float glu_fwd(float g, float l, const ActP& p) {
   const float gc = fminf(g, p.limit);
   const float lc = fminf(fmaxf(l, -p.limit), p.limit);
   float phi;
-  if (p.act == MOE_ACT_SWIGLU) {
+  if (ACT == MOE_ACT_SWIGLU) {
     phi = gc * sigmoid_f(p.alpha * gc);
-  } else if (p.act == MOE_ACT_GEGLU) {
+  } else if (ACT == MOE_ACT_GEGLU) {
     phi = 0.5f * gc * (1.0f + erff(gc * 0.70710678118654752f));
   } else {
     const float r = fmaxf(gc, 0.0f);
@@ -80,16 +83,17 @@ __device__ __forceinline__ float glu_fwd(float g, float l, const ActP& p) {
   return p.out_scale * phi * (lc + p.lin_off);
 }
 
+template <int ACT>
 __device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& p, float& dg,
                                         float& dl) {
   const float gc = fminf(g, p.limit);
   const float lc = fminf(fmaxf(l, -p.limit), p.limit);
   float phi, dphi;
-  if (p.act == MOE_ACT_SWIGLU) {
+  if (ACT == MOE_ACT_SWIGLU) {
     const float s = sigmoid_f(p.alpha * gc);
     phi = gc * s;
     dphi = s + p.alpha * gc * s * (1.0f - s);
-  } else if (p.act == MOE_ACT_GEGLU) {
+  } else if (ACT == MOE_ACT_GEGLU) {
     const float cdf = 0.5f * (1.0f + erff(gc * 0.70710678118654752f));
     const float pdf = 0.39894228040143268f * __expf(-0.5f * gc * gc);
     phi = gc * cdf;
@@ -102,6 +106,26 @@ __device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& 
   const float das = p.out_scale * da;
   dg = (g <= p.limit) ? das * (lc + p.lin_off) * dphi : 0.0f;
   dl = (l >= -p.limit && l <= p.limit) ? das * phi : 0.0f;
+}
+
+// One 32-feature chunk of the dGLU epilogue: dA (fp32, from TMEM) and the
+// saved gate/linear values (bf16, prefetched into registers) -> dG, dL.
+template <int ACT>
+__device__ __forceinline__ void dglu_chunk(const uint32_t (&r)[32], const uint4 (&hg)[4],
+                                           const uint4 (&hl)[4], bool live, const ActP& ap,
+                                           __nv_bfloat16* dg_dst, __nv_bfloat16* dl_dst) {
+  if (live) {
+    float g[32], l[32], dg[32], dl[32];
+    unpack_bf16x32(hg, g);
+    unpack_bf16x32(hl, l);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
+    store_bf16x32(dg_dst, dg);
+    store_bf16x32(dl_dst, dl);
+  } else {
+    store_zero_x32(dg_dst);
+    store_zero_x32(dl_dst);
+  }
 }
 
 template <int MODE>
@@ -146,7 +170,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
   return ti;
 }
 
-template <int MODE>
+template <int MODE, int ACT>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
   using Tr = Traits<MODE>;
   extern __shared__ uint8_t dyn_smem[];
@@ -323,6 +347,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
+      const long long gr = ti.m0 + row_local;
+      const bool valid = !Tr::kRaggedK && (gr - s_off[ti.e]) < s_cnt[ti.e];
+
+      // dGLU: the saved FC1 output H does not depend on the accumulator, so
+      // its first chunk is fetched before waiting for the MMAs.
+      uint4 hg[2][4], hl[2][4];
+      const __nv_bfloat16* Hrow = nullptr;
+      if (MODE == kDgradDglu) {
+        Hrow = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
+        if (valid && ti.n0 < args.f_real) {
+          const long long cg = static_cast<long long>(ti.n0 / kGluHalf) * 2 * kGluHalf + (ti.n0 % kGluHalf);
+          load_raw64(Hrow + cg, hg[0]);
+          load_raw64(Hrow + cg + kGluHalf, hl[0]);
+        }
+      }
+
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -330,125 +370,138 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
-      if (MODE == kWgrad) {
-        const int row = ti.m0 + row_local;
-        const bool row_ok = row < args.m_ext;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out0) +
-                             (static_cast<long long>(ti.e) * args.m_ext + (row_ok ? row : 0)) * args.ld0;
-        for (int j = 0; j < BN / 32; ++j) {
+      if (MODE == kFc1Glu) {
+        __nv_bfloat16* Hd = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0 + ti.n0;
+        __nv_bfloat16* A = static_cast<__nv_bfloat16*>(args.out1) + gr * args.ld1;
+        const __nv_bfloat16* b1 =
+            args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0
+                      : nullptr;
+        uint32_t rg[32], rl[32];
+        tmem_ld32(tbase, rg);
+        tmem_ld32(tbase + kGluHalf, rl);
+#pragma unroll 1
+        for (int j = 0; j < kGluHalf / 32; ++j) {
+          tmem_ld_wait(rg);
+          reg_fence(rl);
+          float g[32], l[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            g[i] = __uint_as_float(rg[i]);
+            l[i] = __uint_as_float(rl[i]);
+          }
+          if (j + 1 < kGluHalf / 32) {        // next chunk's accumulator in flight
+            tmem_ld32(tbase + 32 * (j + 1), rg);
+            tmem_ld32(tbase + kGluHalf + 32 * (j + 1), rl);
+          }
+          if (b1) {
+            float bg[32], bl[32];
+            load_bf16x32(b1 + 32 * j, bg);
+            load_bf16x32(b1 + kGluHalf + 32 * j, bl);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              g[i] += bg[i];
+              l[i] += bl[i];
+            }
+          }
+          const int f0 = ti.n0 / 2 + 32 * j;
+          if (valid) {
+            store_bf16x32(Hd + 32 * j, g);
+            store_bf16x32(Hd + kGluHalf + 32 * j, l);
+            if (f0 < args.f_real) {
+              float a[32];
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
+              store_bf16x32(A + f0, a);
+            }
+          } else {
+            store_zero_x32(Hd + 32 * j);
+            store_zero_x32(Hd + kGluHalf + 32 * j);
+            if (f0 < args.f_real) store_zero_x32(A + f0);
+          }
+        }
+      } else if (MODE == kDgradDglu) {
+        // tile columns are GLU features n0 .. n0+255; dH in packed layout.
+        // Chunks go in pairs so the two H prefetch buffers stay static.
+        __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
+        const int nch = min(BN / 32, (args.f_pad - ti.n0) / 32);   // 4 or 8
+        uint32_t r[32];
+        tmem_ld32(tbase, r);
+#pragma unroll 1
+        for (int j = 0; j < nch; j += 2) {
+          const int f0 = ti.n0 + 32 * j, f1 = f0 + 32, f2 = f0 + 64;
+          const long long c0 = static_cast<long long>(f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
+          const long long c1 = static_cast<long long>(f1 / kGluHalf) * 2 * kGluHalf + (f1 % kGluHalf);
+          const long long c2 = static_cast<long long>(f2 / kGluHalf) * 2 * kGluHalf + (f2 % kGluHalf);
+          // chunk j (buffer 0); prefetch chunk j+1 into buffer 1
+          if (valid && f1 < args.f_real) {
+            load_raw64(Hrow + c1, hg[1]);
+            load_raw64(Hrow + c1 + kGluHalf, hl[1]);
+          }
+          tmem_ld_wait(r);
+          uint32_t ra[32];
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ra[i] = r[i];
+          tmem_ld32(tbase + 32 * (j + 1), r);
+          dglu_chunk<ACT>(ra, hg[0], hl[0], valid && f0 < args.f_real, ap, dH + c0,
+                          dH + c0 + kGluHalf);
+          // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
+          if (j + 2 < nch && valid && f2 < args.f_real) {
+            load_raw64(Hrow + c2, hg[0]);
+            load_raw64(Hrow + c2 + kGluHalf, hl[0]);
+          }
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) ra[i] = r[i];
+          if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
+          dglu_chunk<ACT>(ra, hg[1], hl[1], valid && f1 < args.f_real, ap, dH + c1,
+                          dH + c1 + kGluHalf);
+        }
+      } else {
+        // kFc2 (+b2), kDgradFc1 and kWgrad: plain row-major bf16 output
+        const bool has_acc = !Tr::kRaggedK || ti.num_kb > 0;
+        bool row_ok;
+        __nv_bfloat16* dst;
+        if (Tr::kRaggedK) {
+          const int row = ti.m0 + row_local;
+          row_ok = row < args.m_ext;
+          dst = static_cast<__nv_bfloat16*>(args.out0) +
+                (static_cast<long long>(ti.e) * args.m_ext + (row_ok ? row : 0)) * args.ld0;
+        } else {
+          row_ok = true;
+          dst = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
+        }
+        const __nv_bfloat16* bias =
+            (MODE == kFc2 && args.bias)
+                ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
+                : nullptr;
+        const int nch = min(BN / 32, (args.n_ext - ti.n0 + 31) / 32);
+        uint32_t r[32];
+        if (has_acc) tmem_ld32(tbase, r);
+#pragma unroll 1
+        for (int j = 0; j < nch; ++j) {
           const int c0 = ti.n0 + 32 * j;
-          if (c0 >= args.n_ext) break;
           float v[32];
-          if (ti.num_kb > 0) {
-            uint32_t r[32];
-            tmem_ld32(tbase + 32 * j, r);
-            tmem_ld_wait();
+          if (has_acc) {
+            tmem_ld_wait(r);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+            if (j + 1 < nch) tmem_ld32(tbase + 32 * (j + 1), r);
           } else {
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
-          if (row_ok) store_bf16x32(dst + c0, v);
-        }
-      } else {
-        const long long gr = ti.m0 + row_local;
-        const bool valid = (gr - s_off[ti.e]) < s_cnt[ti.e];
-        if (MODE == kFc1Glu) {
-          __nv_bfloat16* H = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0 + ti.n0;
-          __nv_bfloat16* A = static_cast<__nv_bfloat16*>(args.out1) + gr * args.ld1;
-          const __nv_bfloat16* b1 =
-              args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0
-                        : nullptr;
-          for (int j = 0; j < kGluHalf / 32; ++j) {
-            uint32_t rg[32], rl[32];
-            tmem_ld32(tbase + 32 * j, rg);
-            tmem_ld32(tbase + kGluHalf + 32 * j, rl);
-            tmem_ld_wait();
-            float g[32], l[32];
+          if (Tr::kRaggedK) {
+            if (row_ok) store_bf16x32(dst + c0, v);
+          } else if (valid) {
+            if (bias) {
+              float b[32];
+              load_bf16x32(bias + c0, b);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              g[i] = __uint_as_float(rg[i]);
-              l[i] = __uint_as_float(rl[i]);
+              for (int i = 0; i < 32; ++i) v[i] += b[i];
             }
-            if (b1) {
-              float bg[32], bl[32];
-              load_bf16x32(b1 + 32 * j, bg);
-              load_bf16x32(b1 + kGluHalf + 32 * j, bl);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                g[i] += bg[i];
-                l[i] += bl[i];
-              }
-            }
-            const int f0 = ti.n0 / 2 + 32 * j;
-            if (valid) {
-              store_bf16x32(H + 32 * j, g);
-              store_bf16x32(H + kGluHalf + 32 * j, l);
-              if (f0 < args.f_real) {
-                float a[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = glu_fwd(g[i], l[i], ap);
-                store_bf16x32(A + f0, a);
-              }
-            } else {
-              store_zero_x32(H + 32 * j);
-              store_zero_x32(H + kGluHalf + 32 * j);
-              if (f0 < args.f_real) store_zero_x32(A + f0);
-            }
-          }
-        } else if (MODE == kDgradDglu) {
-          // tile columns are GLU features n0 .. n0+255; dH in packed layout
-          __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
-          const __nv_bfloat16* H = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
-          for (int j = 0; j < BN / 32; ++j) {
-            const int f0 = ti.n0 + 32 * j;
-            if (f0 >= args.f_pad) break;
-            uint32_t r[32];
-            tmem_ld32(tbase + 32 * j, r);
-            tmem_ld_wait();
-            const long long cg = static_cast<long long>(f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
-            const long long cl = cg + kGluHalf;
-            if (valid && f0 < args.f_real) {
-              float g[32], l[32], dg[32], dl[32];
-              load_bf16x32(H + cg, g);
-              load_bf16x32(H + cl, l);
-#pragma unroll
-              for (int i = 0; i < 32; ++i) glu_bwd(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
-              store_bf16x32(dH + cg, dg);
-              store_bf16x32(dH + cl, dl);
-            } else {
-              store_zero_x32(dH + cg);
-              store_zero_x32(dH + cl);
-            }
-          }
-        } else {
-          // kFc2 (+b2) and kDgradFc1: plain row-major bf16 output
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
-          const __nv_bfloat16* bias =
-              (MODE == kFc2 && args.bias)
-                  ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
-                  : nullptr;
-          for (int j = 0; j < BN / 32; ++j) {
-            const int c0 = ti.n0 + 32 * j;
-            if (c0 >= args.n_ext) break;
-            uint32_t r[32];
-            tmem_ld32(tbase + 32 * j, r);
-            tmem_ld_wait();
-            if (valid) {
-              float v[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-              if (bias) {
-                float b[32];
-                load_bf16x32(bias + c0, b);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] += b[i];
-              }
-              store_bf16x32(dst + c0, v);
-            } else {
-              store_zero_x32(dst + c0);
-            }
+            store_bf16x32(dst + c0, v);
+          } else {
+            store_zero_x32(dst + c0);
           }
         }
       }
@@ -466,14 +519,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
   }
 }
 
-template <int MODE>
+template <int MODE, int ACT>
 cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE>,
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(SMEM_BYTES));
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<MODE><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(args);
+  k_grouped_gemm<MODE, ACT><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(args);
   return cudaGetLastError();
+}
+
+template <int MODE>
+cudaError_t launch_act(const GemmArgs& args, int grid, cudaStream_t s) {
+  switch (args.act) {
+    case MOE_ACT_SWIGLU: return launch_mode<MODE, MOE_ACT_SWIGLU>(args, grid, s);
+    case MOE_ACT_GEGLU: return launch_mode<MODE, MOE_ACT_GEGLU>(args, grid, s);
+    case MOE_ACT_SREGLU: return launch_mode<MODE, MOE_ACT_SREGLU>(args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -482,11 +545,11 @@ size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
   switch (mode) {
-    case kFc1Glu: return launch_mode<kFc1Glu>(args, grid, s);
-    case kFc2: return launch_mode<kFc2>(args, grid, s);
-    case kDgradDglu: return launch_mode<kDgradDglu>(args, grid, s);
-    case kDgradFc1: return launch_mode<kDgradFc1>(args, grid, s);
-    case kWgrad: return launch_mode<kWgrad>(args, grid, s);
+    case kFc1Glu: return launch_act<kFc1Glu>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0>(args, grid, s);
+    case kWgrad: return launch_mode<kWgrad, 0>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

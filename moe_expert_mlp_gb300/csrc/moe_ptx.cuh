@@ -194,6 +194,29 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Wait for outstanding TMEM loads and tie `r` to the wait, so that no use
+// of the loaded registers can be scheduled before the data has arrived.
+__device__ __forceinline__ void tmem_ld_wait(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]),
+                 "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]),
+                 "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]),
+                 "+r"(r[30]), "+r"(r[31]));
+}
+
 // ------------------------------------------------------------- bf16 I/O
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -221,6 +244,27 @@ __device__ __forceinline__ void store_zero_x32(void* dst) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) p[q] = make_uint4(0, 0, 0, 0);
+}
+
+// Raw 64-byte load (32 bf16, 16-byte aligned) into four 16-byte vectors.
+__device__ __forceinline__ void load_raw64(const void* src, uint4 (&w)[4]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) w[q] = __ldg(p + q);
+}
+
+__device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&v)[32]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    v[8 * q + 0] = bf16_lo(w[q].x);
+    v[8 * q + 1] = bf16_hi(w[q].x);
+    v[8 * q + 2] = bf16_lo(w[q].y);
+    v[8 * q + 3] = bf16_hi(w[q].y);
+    v[8 * q + 4] = bf16_lo(w[q].z);
+    v[8 * q + 5] = bf16_hi(w[q].z);
+    v[8 * q + 6] = bf16_lo(w[q].w);
+    v[8 * q + 7] = bf16_hi(w[q].w);
+  }
 }
 
 // Load 32 bf16 (64 contiguous bytes, 16-byte aligned) as fp32.

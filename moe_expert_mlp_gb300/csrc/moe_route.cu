@@ -39,74 +39,68 @@ __device__ __forceinline__ float warp_sum(float v) {
 }
 
 // ------------------------------------------------------------ top-k
-// One warp per token.  Lane l holds the scores of experts l, l+32, ...
-// k rounds of a warp arg-max (larger score wins, equal scores go to the
-// lower expert index) give the slots in descending score.  The weights are
-// the softmax of the selected raw logits.  Each block also histograms its
-// chunk of kTokensPerChunk tokens per expert (counts are exact integers).
-__global__ void __launch_bounds__(kTokensPerChunk) k_topk(
+// One warp per token, 8 tokens per block.  Lane l holds the scores of
+// experts l, l+32, ...; k rounds of a warp arg-max (larger score wins, equal
+// scores go to the lower expert index) give the slots in descending score.
+// The weights are the softmax of the selected raw logits.  The per-expert
+// histogram of each chunk of kTokensPerChunk tokens is accumulated with
+// integer atomics into chunk_counts (zeroed beforehand); integer sums do
+// not depend on the order, so the counts are exact and reproducible.
+__global__ void __launch_bounds__(256) k_topk(
     const float* __restrict__ logits, const float* __restrict__ bias, int T, int E, int k,
     int32_t* __restrict__ topk_idx, float* __restrict__ topk_w,
     int32_t* __restrict__ chunk_counts, int* status) {
-  __shared__ int s_cnt[kMaxExperts];
-  for (int i = threadIdx.x; i < E; i += blockDim.x) s_cnt[i] = 0;
-  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int tt = warp; tt < kTokensPerChunk; tt += kWarps) {
-    const int t = blockIdx.x * kTokensPerChunk + tt;
-    if (t >= T) break;
-    const float* lrow = logits + static_cast<size_t>(t) * E;
-    float sc[kMaxExperts / 32];
+  const int t = blockIdx.x * 8 + warp;
+  if (t >= T) return;
+  const float* lrow = logits + static_cast<size_t>(t) * E;
+  float sc[kMaxExperts / 32];
+#pragma unroll
+  for (int q = 0; q < kMaxExperts / 32; ++q) {
+    const int e = lane + 32 * q;
+    sc[q] = -INFINITY;
+    if (e < E) sc[q] = lrow[e] + (bias ? bias[e] : 0.0f);
+  }
+  uint32_t taken = 0;
+  int my_idx = 0;
+  for (int s = 0; s < k; ++s) {
+    float best = -INFINITY;
+    int bi = E;                           // sentinel: nothing selectable
 #pragma unroll
     for (int q = 0; q < kMaxExperts / 32; ++q) {
       const int e = lane + 32 * q;
-      sc[q] = -INFINITY;
-      if (e < E) sc[q] = lrow[e] + (bias ? bias[e] : 0.0f);
-    }
-    uint32_t taken = 0;
-    int my_idx = 0;
-    for (int s = 0; s < k; ++s) {
-      float best = -INFINITY;
-      int bi = E;                         // sentinel: nothing selectable
-#pragma unroll
-      for (int q = 0; q < kMaxExperts / 32; ++q) {
-        const int e = lane + 32 * q;
-        if (e < E && !((taken >> q) & 1u)) {
-          if (sc[q] > best || (sc[q] == best && e < bi)) {
-            best = sc[q];
-            bi = e;
-          }
+      if (e < E && !((taken >> q) & 1u)) {
+        if (sc[q] > best || (sc[q] == best && e < bi)) {
+          best = sc[q];
+          bi = e;
         }
       }
+    }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-        if (ob > best || (ob == best && oi < bi)) {
-          best = ob;
-          bi = oi;
-        }
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+      const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+      if (ob > best || (ob == best && oi < bi)) {
+        best = ob;
+        bi = oi;
       }
-      if (bi >= E) {                      // non-finite scores left nothing to pick
-        if (lane == 0) set_status(status, MOE_DEV_BAD_EXPERT);
-        bi = s;
-      }
-      if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-      if (lane == s) my_idx = bi;
     }
-    const float z = (lane < k) ? lrow[my_idx] : -INFINITY;
-    const float m = warp_max(z);
-    const float ex = (lane < k) ? expf(z - m) : 0.0f;
-    const float sum = warp_sum(ex);
-    if (lane < k) {
-      topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
-      topk_w[static_cast<size_t>(t) * k + lane] = ex / sum;
-      atomicAdd(&s_cnt[my_idx], 1);
+    if (bi >= E) {                        // non-finite scores left nothing to pick
+      if (lane == 0) set_status(status, MOE_DEV_BAD_EXPERT);
+      bi = s;
     }
+    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    if (lane == s) my_idx = bi;
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    chunk_counts[static_cast<size_t>(blockIdx.x) * E + i] = s_cnt[i];
+  const float z = (lane < k) ? lrow[my_idx] : -INFINITY;
+  const float m = warp_max(z);
+  const float ex = (lane < k) ? expf(z - m) : 0.0f;
+  const float sum = warp_sum(ex);
+  if (lane < k) {
+    topk_idx[static_cast<size_t>(t) * k + lane] = my_idx;
+    topk_w[static_cast<size_t>(t) * k + lane] = ex / sum;
+    atomicAdd(&chunk_counts[static_cast<size_t>(t / kTokensPerChunk) * E + my_idx], 1);
+  }
 }
 
 // ------------------------------------------------------------- scans
@@ -401,8 +395,10 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
                         cudaStream_t s) {
   const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
   if (nchunks == 0) return cudaSuccess;
-  k_topk<<<nchunks, kTokensPerChunk, 0, s>>>(logits, bias, T, E, k, topk_idx, topk_w,
-                                             chunk_counts, status);
+  cudaError_t e = cudaMemsetAsync(chunk_counts, 0, sizeof(int32_t) * nchunks * E, s);
+  if (e != cudaSuccess) return e;
+  k_topk<<<(T + 7) / 8, 256, 0, s>>>(logits, bias, T, E, k, topk_idx, topk_w, chunk_counts,
+                                     status);
   return cudaGetLastError();
 }
 
