@@ -69,7 +69,8 @@ moe_status_t device_info(DeviceInfo** out) {
 // innermost dimension is contiguous; row_bytes / plane_bytes are the strides
 // of dims 1 and 2.  Out-of-range box elements read as zero.
 bool encode_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
-                uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1) {
+                uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1,
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes & 15) || (plane_bytes & 15))
     return false;
   cuuint64_t dims[3] = {d0, d1, d2};
@@ -77,8 +78,8 @@ bool encode_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, ui
   cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t estride[3] = {1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
-                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -111,6 +112,12 @@ int grid_for(const DeviceInfo* di, const moe_mlp_desc_t* d) {
 size_t route_ws_bytes(const moe_mlp_desc_t* d) {
   const size_t nchunks = (static_cast<size_t>(d->T) + kTokensPerChunk - 1) / kTokensPerChunk;
   return (nchunks * d->E * sizeof(int32_t) + 255) / 256 * 256;
+}
+
+// Output map: 32x32 boxes with 64-byte swizzle (the epilogue staging layout).
+bool encode_out(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
+  return encode_map(map, base, d0, d1, d2, d0 * 2, d1 * d0 * 2, 32, 32,
+                    CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -254,7 +261,8 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256))
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out(&g.tma_out1, a, F, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = static_cast<int>(2 * Fp);
@@ -282,7 +290,8 @@ moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, a, F, cap, 1, F * 2, cap * F * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256))
+      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, y, d, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->F;
   g.n_ext = desc->d;
@@ -350,7 +359,8 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
+      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64) ||
+      !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = static_cast<int>(Fp);
@@ -370,13 +380,14 @@ moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const voi
   if (!dy || !a || !counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t d = desc->d, F = desc->F;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
   const uint64_t cap = desc->capacity;
   // dW2[e] (d x F) = sum over the group's rows of dY^T A (both read MN-major)
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
-      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64))
+      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64) ||
+      !encode_out(&g.tma_out0, dw2, F, d, E))
     return MOE_ERR_SHAPE;
   g.m_ext = desc->d;
   g.n_ext = desc->F;
@@ -400,7 +411,8 @@ moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64) ||
+      !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = static_cast<int>(2 * Fp);
   g.n_ext = desc->d;
@@ -418,13 +430,14 @@ moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const voi
   if (!dh || !x_perm || !counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
   const uint64_t cap = desc->capacity;
   // dW1p[e] (2F_pad x d) = sum over the group's rows of dH^T X
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64) ||
-      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
+      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
+      !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
     return MOE_ERR_SHAPE;
   g.m_ext = static_cast<int>(2 * Fp);
   g.n_ext = desc->d;

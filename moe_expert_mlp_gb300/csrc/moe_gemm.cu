@@ -48,7 +48,10 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
 constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
 constexpr int NUM_THREADS = 192;
-constexpr size_t SMEM_BYTES = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES;
+constexpr int kRing = 3;                     // output staging boxes per epilogue warp
+constexpr int BOX_BYTES = 32 * 32 * 2;       // one 32x32 bf16 output box
+constexpr size_t SMEM_BYTES =
+    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 4 * kRing * BOX_BYTES;
 
 struct Tile {
   int e;        // expert
@@ -111,21 +114,50 @@ __device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& 
 // One 32-feature chunk of the dGLU epilogue: dA (fp32, from TMEM) and the
 // saved gate/linear values (bf16, prefetched into registers) -> dG, dL.
 template <int ACT>
-__device__ __forceinline__ void dglu_chunk(const uint32_t (&r)[32], const uint4 (&hg)[4],
-                                           const uint4 (&hl)[4], bool live, const ActP& ap,
-                                           __nv_bfloat16* dg_dst, __nv_bfloat16* dl_dst) {
-  if (live) {
-    float g[32], l[32], dg[32], dl[32];
-    unpack_bf16x32(hg, g);
-    unpack_bf16x32(hl, l);
+__device__ __forceinline__ void dglu_compute(const uint32_t (&r)[32], const uint4 (&hg)[4],
+                                             const uint4 (&hl)[4], const ActP& ap,
+                                             float (&dg)[32], float (&dl)[32]) {
+  float g[32], l[32];
+  unpack_bf16x32(hg, g);
+  unpack_bf16x32(hl, l);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
-    store_bf16x32(dg_dst, dg);
-    store_bf16x32(dl_dst, dl);
-  } else {
-    store_zero_x32(dg_dst);
-    store_zero_x32(dl_dst);
+  for (int i = 0; i < 32; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
+}
+
+// Output staging: each epilogue warp owns kRing boxes of 32 rows x 32 bf16
+// (64-byte rows, 64-byte swizzle as in the output tensor maps).  Lane i
+// writes row i; lane 0 then issues one TMA bulk tensor store per box.
+struct StoreRing {
+  uint32_t base;   // shared address of this warp's first box
+  int slot;
+};
+
+__device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32], bool live,
+                                           const CUtensorMap* map, int x, int y, int z,
+                                           int lane) {
+  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;
+  if (lane == 0) bulk_wait_read<kRing - 1>();   // the box's previous store has read it
+  __syncwarp();
+  const uint32_t row = buf + lane * 64;
+  const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (live) {
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    }
+    st_shared_v4(row + ((q ^ sw) << 4), w);
   }
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(map, buf, x, y, z);
+    bulk_commit();
+  }
+  ring.slot = ring.slot == kRing - 1 ? 0 : ring.slot + 1;
 }
 
 template <int MODE>
@@ -342,6 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
+    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES + (warp - 2) * kRing * BOX_BYTES), 0};
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
@@ -349,6 +382,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       const uint32_t acc_par = (it >> 1) & 1;
       const long long gr = ti.m0 + row_local;
       const bool valid = !Tr::kRaggedK && (gr - s_off[ti.e]) < s_cnt[ti.e];
+      const int y0 = ti.m0 + quarter * 32;     // first output row of this warp's boxes
 
       // dGLU: the saved FC1 output H does not depend on the accumulator, so
       // its first chunk is fetched before waiting for the MMAs.
@@ -371,8 +405,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
       if (MODE == kFc1Glu) {
-        __nv_bfloat16* Hd = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0 + ti.n0;
-        __nv_bfloat16* A = static_cast<__nv_bfloat16*>(args.out1) + gr * args.ld1;
         const __nv_bfloat16* b1 =
             args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0
                       : nullptr;
@@ -403,35 +435,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
               l[i] += bl[i];
             }
           }
+          ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, lane);
+          ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, lane);
           const int f0 = ti.n0 / 2 + 32 * j;
-          if (valid) {
-            store_bf16x32(Hd + 32 * j, g);
-            store_bf16x32(Hd + kGluHalf + 32 * j, l);
-            if (f0 < args.f_real) {
-              float a[32];
+          if (f0 < args.f_real) {
+            float a[32];
 #pragma unroll
-              for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
-              store_bf16x32(A + f0, a);
-            }
-          } else {
-            store_zero_x32(Hd + 32 * j);
-            store_zero_x32(Hd + kGluHalf + 32 * j);
-            if (f0 < args.f_real) store_zero_x32(A + f0);
+            for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
+            ring_store(ring, a, valid, &args.tma_out1, f0, y0, 0, lane);
           }
         }
       } else if (MODE == kDgradDglu) {
         // tile columns are GLU features n0 .. n0+255; dH in packed layout.
         // Chunks go in pairs so the two H prefetch buffers stay static.
-        __nv_bfloat16* dH = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
         const int nch = min(BN / 32, (args.f_pad - ti.n0) / 32);   // 4 or 8
         uint32_t r[32];
         tmem_ld32(tbase, r);
 #pragma unroll 1
         for (int j = 0; j < nch; j += 2) {
           const int f0 = ti.n0 + 32 * j, f1 = f0 + 32, f2 = f0 + 64;
-          const long long c0 = static_cast<long long>(f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
-          const long long c1 = static_cast<long long>(f1 / kGluHalf) * 2 * kGluHalf + (f1 % kGluHalf);
-          const long long c2 = static_cast<long long>(f2 / kGluHalf) * 2 * kGluHalf + (f2 % kGluHalf);
+          const int c0 = (f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
+          const int c1 = (f1 / kGluHalf) * 2 * kGluHalf + (f1 % kGluHalf);
+          const int c2 = (f2 / kGluHalf) * 2 * kGluHalf + (f2 % kGluHalf);
+          float dg[32], dl[32];
           // chunk j (buffer 0); prefetch chunk j+1 into buffer 1
           if (valid && f1 < args.f_real) {
             load_raw64(Hrow + c1, hg[1]);
@@ -442,8 +468,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 #pragma unroll
           for (int i = 0; i < 32; ++i) ra[i] = r[i];
           tmem_ld32(tbase + 32 * (j + 1), r);
-          dglu_chunk<ACT>(ra, hg[0], hl[0], valid && f0 < args.f_real, ap, dH + c0,
-                          dH + c0 + kGluHalf);
+          const bool live0 = valid && f0 < args.f_real;
+          if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
+          ring_store(ring, dg, live0, &args.tma_out0, c0, y0, 0, lane);
+          ring_store(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, lane);
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
             load_raw64(Hrow + c2, hg[0]);
@@ -453,23 +481,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 #pragma unroll
           for (int i = 0; i < 32; ++i) ra[i] = r[i];
           if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
-          dglu_chunk<ACT>(ra, hg[1], hl[1], valid && f1 < args.f_real, ap, dH + c1,
-                          dH + c1 + kGluHalf);
+          const bool live1 = valid && f1 < args.f_real;
+          if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
+          ring_store(ring, dg, live1, &args.tma_out0, c1, y0, 0, lane);
+          ring_store(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, lane);
         }
       } else {
         // kFc2 (+b2), kDgradFc1 and kWgrad: plain row-major bf16 output
         const bool has_acc = !Tr::kRaggedK || ti.num_kb > 0;
-        bool row_ok;
-        __nv_bfloat16* dst;
-        if (Tr::kRaggedK) {
-          const int row = ti.m0 + row_local;
-          row_ok = row < args.m_ext;
-          dst = static_cast<__nv_bfloat16*>(args.out0) +
-                (static_cast<long long>(ti.e) * args.m_ext + (row_ok ? row : 0)) * args.ld0;
-        } else {
-          row_ok = true;
-          dst = static_cast<__nv_bfloat16*>(args.out0) + gr * args.ld0;
-        }
+        const bool write = !Tr::kRaggedK || y0 < args.m_ext;   // warp-uniform
         const __nv_bfloat16* bias =
             (MODE == kFc2 && args.bias)
                 ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
@@ -490,25 +510,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = 0.0f;
           }
-          if (Tr::kRaggedK) {
-            if (row_ok) store_bf16x32(dst + c0, v);
-          } else if (valid) {
-            if (bias) {
-              float b[32];
-              load_bf16x32(bias + c0, b);
+          if (bias && valid) {
+            float b[32];
+            load_bf16x32(bias + c0, b);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] += b[i];
-            }
-            store_bf16x32(dst + c0, v);
-          } else {
-            store_zero_x32(dst + c0);
+            for (int i = 0; i < 32; ++i) v[i] += b[i];
           }
+          if (write)
+            ring_store(ring, v, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
+                       Tr::kRaggedK ? ti.e : 0, lane);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
+    if (lane == 0) bulk_wait_all();           // stores done before the CTA exits
   }
 
   __syncthreads();

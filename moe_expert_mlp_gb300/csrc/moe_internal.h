@@ -66,6 +66,8 @@ enum GemmMode : int {
 struct GemmArgs {
   CUtensorMap tma_a;
   CUtensorMap tma_b;
+  CUtensorMap tma_out0;   // primary output, 32x32 boxes, 64-byte swizzle
+  CUtensorMap tma_out1;   // GLU output A (FC1 mode only)
   const int32_t* padded_offsets;
   const int32_t* counts;
   int* status;
