@@ -114,9 +114,10 @@ size_t route_ws_bytes(const moe_mlp_desc_t* d) {
   return (nchunks * d->E * sizeof(int32_t) + 255) / 256 * 256;
 }
 
-// Output map: 32x32 boxes with 64-byte swizzle (the epilogue staging layout).
+// Output map: 32-column x 128-row boxes with 64-byte swizzle (the epilogue
+// staging layout).
 bool encode_out(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
-  return encode_map(map, base, d0, d1, d2, d0 * 2, d1 * d0 * 2, 32, 32,
+  return encode_map(map, base, d0, d1, d2, d0 * 2, d1 * d0 * 2, 32, 128,
                     CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
@@ -394,7 +395,7 @@ moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const voi
   g.b_ext = desc->F;
   g.out0 = dw2;
   g.ld0 = F;
-  return cuda_status(launch_grouped_gemm(kWgrad, g, grid_for(di, desc), stream));
+  return cuda_status(launch_grouped_gemm(kWgradPair, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int32_t* counts,
@@ -444,7 +445,7 @@ moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const voi
   g.b_ext = desc->d;
   g.out0 = dw1p;
   g.ld0 = d;
-  return cuda_status(launch_grouped_gemm(kWgrad, g, grid_for(di, desc), stream));
+  return cuda_status(launch_grouped_gemm(kWgradPair, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const void* dh,

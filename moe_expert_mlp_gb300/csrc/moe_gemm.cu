@@ -48,10 +48,12 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
 constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
 constexpr int NUM_THREADS = 192;
-constexpr int kRing = 3;                     // output staging boxes per epilogue warp
-constexpr int BOX_BYTES = 32 * 32 * 2;       // one 32x32 bf16 output box
+constexpr int kRing = 3;                     // output staging boxes (shared by the epilogue)
+constexpr int BOX_BYTES = 128 * 32 * 2;      // one 128-row x 32-column bf16 output box
+constexpr int kEpiThreads = 128;             // 4 epilogue warps
+constexpr int kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr size_t SMEM_BYTES =
-    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + 4 * kRing * BOX_BYTES;
+    1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + kRing * BOX_BYTES;
 
 struct Tile {
   int e;        // expert
@@ -124,22 +126,24 @@ __device__ __forceinline__ void dglu_compute(const uint32_t (&r)[32], const uint
   for (int i = 0; i < 32; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
 }
 
-// Output staging: each epilogue warp owns kRing boxes of 32 rows x 32 bf16
-// (64-byte rows, 64-byte swizzle as in the output tensor maps).  Lane i
-// writes row i; lane 0 then issues one TMA bulk tensor store per box.
+// Output staging: the four epilogue warps share kRing boxes of 128 rows x
+// 32 bf16 (64-byte rows, 64-byte swizzle as in the output tensor maps).
+// Thread row (= its TMEM lane) writes its 64 bytes; after a named barrier one
+// thread issues a single TMA bulk tensor store for the whole box and waits
+// until the box issued kRing-1 stores earlier has been read, so the buffer
+// the next box uses is free by the time the other threads pass the next
+// barrier.  All epilogue threads must call ring_store in the same sequence.
 struct StoreRing {
-  uint32_t base;   // shared address of this warp's first box
+  uint32_t base;   // shared address of the first box
   int slot;
 };
 
 __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32], bool live,
                                            const CUtensorMap* map, int x, int y, int z,
-                                           int lane) {
+                                           int row, bool issuer) {
   const uint32_t buf = ring.base + ring.slot * BOX_BYTES;
-  if (lane == 0) bulk_wait_read<kRing - 1>();   // the box's previous store has read it
-  __syncwarp();
-  const uint32_t row = buf + lane * 64;
-  const uint32_t sw = (lane >> 1) & 3;
+  const uint32_t raddr = buf + row * 64;
+  const uint32_t sw = (row >> 1) & 3;
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     uint4 w = make_uint4(0, 0, 0, 0);
@@ -149,13 +153,14 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
       w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
       w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     }
-    st_shared_v4(row + ((q ^ sw) << 4), w);
+    st_shared_v4(raddr + ((q ^ sw) << 4), w);
   }
   fence_proxy_async_smem();
-  __syncwarp();
-  if (lane == 0) {
+  named_bar_sync(kEpiBar, kEpiThreads);
+  if (issuer) {
     tma_store_3d(map, buf, x, y, z);
     bulk_commit();
+    bulk_wait_read<kRing - 2>();
   }
   ring.slot = ring.slot == kRing - 1 ? 0 : ring.slot + 1;
 }
@@ -374,7 +379,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
-    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES + (warp - 2) * kRing * BOX_BYTES), 0};
+    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES), 0};
+    const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       const uint32_t acc_par = (it >> 1) & 1;
       const long long gr = ti.m0 + row_local;
       const bool valid = !Tr::kRaggedK && (gr - s_off[ti.e]) < s_cnt[ti.e];
-      const int y0 = ti.m0 + quarter * 32;     // first output row of this warp's boxes
+      const int y0 = ti.m0;                     // first output row of the tile's boxes
 
       // dGLU: the saved FC1 output H does not depend on the accumulator, so
       // its first chunk is fetched before waiting for the MMAs.
@@ -400,7 +406,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
+      // leave together: the store barriers below need all epilogue warps
+      if (named_bar_any(kEpiBar, kEpiThreads, !ok)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
 
@@ -435,14 +442,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
               l[i] += bl[i];
             }
           }
-          ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, lane);
-          ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, lane);
+          ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
+          ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
+                     issuer);
           const int f0 = ti.n0 / 2 + 32 * j;
           if (f0 < args.f_real) {
             float a[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
-            ring_store(ring, a, valid, &args.tma_out1, f0, y0, 0, lane);
+            ring_store(ring, a, valid, &args.tma_out1, f0, y0, 0, row_local, issuer);
           }
         }
       } else if (MODE == kDgradDglu) {
@@ -470,8 +478,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           tmem_ld32(tbase + 32 * (j + 1), r);
           const bool live0 = valid && f0 < args.f_real;
           if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
-          ring_store(ring, dg, live0, &args.tma_out0, c0, y0, 0, lane);
-          ring_store(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, lane);
+          ring_store(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
+          ring_store(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local, issuer);
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
             load_raw64(Hrow + c2, hg[0]);
@@ -483,13 +491,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
           const bool live1 = valid && f1 < args.f_real;
           if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
-          ring_store(ring, dg, live1, &args.tma_out0, c1, y0, 0, lane);
-          ring_store(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, lane);
+          ring_store(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
+          ring_store(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local, issuer);
         }
       } else {
         // kFc2 (+b2), kDgradFc1 and kWgrad: plain row-major bf16 output
         const bool has_acc = !Tr::kRaggedK || ti.num_kb > 0;
-        const bool write = !Tr::kRaggedK || y0 < args.m_ext;   // warp-uniform
+        const bool write = !Tr::kRaggedK || y0 < args.m_ext;   // CTA-uniform
         const __nv_bfloat16* bias =
             (MODE == kFc2 && args.bias)
                 ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
@@ -518,14 +526,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           }
           if (write)
             ring_store(ring, v, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
-                       Tr::kRaggedK ? ti.e : 0, lane);
+                       Tr::kRaggedK ? ti.e : 0, row_local, issuer);
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
-    if (lane == 0) bulk_wait_all();           // stores done before the CTA exits
+    if (issuer) bulk_wait_all();              // stores done before the CTA exits
   }
 
   __syncthreads();
@@ -534,6 +542,234 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Weight gradients on CTA pairs (2-SM MMA).  dW[e] (m_ext x n_ext) = sum over
+// the rows of group e of P^T Q, with P [rows, m_ext] and Q [rows, n_ext] both
+// read MN-major.  A pair owns a 256 x 256 output tile: CTA r stages rows
+// m0+128r.. of P and columns n0+128r.. of Q (16 KB + 16 KB per 64-row K step,
+// 6 stages) and keeps output rows m0+128r.. in its TMEM.  The lead CTA issues
+// the MMAs (M=256, N=256) and its commits arrive on both CTAs' barriers;
+// both CTAs' TMA loads complete on the lead CTA's "full" barriers.  Per SM
+// this halves the operand bytes per MMA relative to the single-CTA tile.
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_HALF = 128 * BK * 2;               // 16 KB
+constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF;       // A half + B half
+constexpr size_t PAIR_SMEM_BYTES =
+    1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES + kRing * BOX_BYTES;
+constexpr uint32_t kPairIdesc = idesc_bf16(256, BN, true, true);
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+    k_wgrad_pair(const __grid_constant__ GemmArgs args) {
+  extern __shared__ uint8_t dyn_smem[];
+  __shared__ __align__(8) uint64_t full_bar[PAIR_STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[PAIR_STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ uint32_t s_tmem_base;
+  __shared__ int s_abort;
+  __shared__ int s_total;
+  __shared__ int s_off[kMaxExperts + 1];
+  __shared__ int s_cnt[kMaxExperts];
+  __shared__ int s_order[kMaxExperts];
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int E = args.E;
+
+  for (int i = threadIdx.x; i <= E; i += NUM_THREADS) s_off[i] = args.padded_offsets[i];
+  for (int i = threadIdx.x; i < E; i += NUM_THREADS) s_cnt[i] = args.counts[i];
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 8);         // 4 epilogue warps x 2 CTAs
+    }
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(&s_tmem_base, TMEM_COLS);
+    tmem_relinquish_pair();
+    tc_fence_before();
+  }
+  __syncthreads();
+  const int m_tiles = (args.m_ext + 255) / 256;
+  const int n_tiles = (args.n_ext + BN - 1) / BN;
+  if (threadIdx.x == 0) {
+    bool ok = s_off[0] == 0 && s_off[E] <= args.capacity;
+    for (int e = 0; e < E && ok; ++e) {
+      const int span = s_off[e + 1] - s_off[e];
+      ok = span >= 0 && (span % BM) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= span;
+    }
+    if (!ok) set_status(args.status, MOE_DEV_BAD_OFFSETS);
+    s_total = ok ? E * m_tiles * n_tiles : 0;
+  }
+  for (int e = threadIdx.x; e < E; e += NUM_THREADS) {
+    int r = 0;
+    for (int j = 0; j < E; ++j) r += (s_cnt[j] > s_cnt[e]) || (s_cnt[j] == s_cnt[e] && j < e);
+    s_order[r] = e;
+  }
+  __syncthreads();
+  cluster_sync();                            // peer barriers initialised before any remote use
+  tc_fence_after();
+  const uint32_t tmem_base = s_tmem_base;
+  const int total = s_total;
+  volatile int* abort_flag = &s_abort;
+  const int per_e = m_tiles * n_tiles;
+
+  if (warp == 0) {
+    // ====================== TMA producer (both CTAs) ======================
+    if (lane == 0) {
+      tma_prefetch_desc(&args.tma_a);
+      tma_prefetch_desc(&args.tma_b);
+      uint32_t stage = 0, phase = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs) {
+        const int slot = t / per_e, rem = t - slot * per_e;
+        const int mb = rem / n_tiles, nb = rem - mb * n_tiles;
+        const int e = s_order[slot];
+        const int m0 = mb * 256, n0 = nb * BN;
+        const int k_row0 = s_off[e];
+        const int num_kb = (s_cnt[e] + BK - 1) / BK;
+        int nbox[2][2];                      // [cta][A,B] boxes holding in-range data
+        for (int r = 0; r < 2; ++r) {
+          nbox[r][0] = max(0, min(2, (args.m_ext - (m0 + 128 * r) + 63) / 64));
+          nbox[r][1] = max(0, min(2, (args.b_ext - (n0 + 128 * r) + 63) / 64));
+        }
+        const uint32_t tx = (nbox[0][0] + nbox[0][1] + nbox[1][0] + nbox[1][1]) * MN_BOX_BYTES;
+        const int my_a = nbox[rank][0], my_b = nbox[rank][1];
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&empty_bar[stage], phase ^ 1u, args.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * PAIR_STAGE_BYTES;
+          uint8_t* sb = sa + PAIR_HALF;
+          const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], tx);
+          const int kr = k_row0 + kb * BK;
+          for (int i = 0; i < my_a; ++i)
+            tma_load_3d_pair(sa + i * MN_BOX_BYTES, &args.tma_a, fb, m0 + 128 * rank + 64 * i, kr, 0);
+          for (int i = 0; i < my_b; ++i)
+            tma_load_3d_pair(sb + i * MN_BOX_BYTES, &args.tma_b, fb, n0 + 128 * rank + 64 * i, kr, 0);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ====================== MMA issuer (lead CTA only) ====================
+    if (lane == 0 && rank == 0) {
+      uint32_t stage = 0, phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = pair; t < total && ok; t += npairs, ++it) {
+        const int slot = t / per_e;
+        const int e = s_order[slot];
+        const int num_kb = (s_cnt[e] + BK - 1) / BK;
+        const int acc = it & 1;
+        const uint32_t acc_par = (it >> 1) & 1;
+        if (!mbar_wait(&tempty_bar[acc], acc_par ^ 1u, args.status, abort_flag)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          if (!mbar_wait(&full_bar[stage], phase, args.status, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(smem + stage * PAIR_STAGE_BYTES);
+          const uint32_t b_base = a_base + PAIR_HALF;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t ad = sdesc_sw128(a_base + k * 2048, MN_BOX_BYTES, 1024);
+            const uint64_t bd = sdesc_sw128(b_base + k * 2048, MN_BOX_BYTES, 1024);
+            umma_bf16_pair(d_tmem, ad, bd, kPairIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          umma_commit_pair(&empty_bar[stage]);
+          if (++stage == PAIR_STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(&tfull_bar[acc]);
+      }
+    }
+  } else {
+    // ====================== epilogue (both CTAs) ==========================
+    const int quarter = warp & 3;
+    StoreRing ring{smem_u32(smem + PAIR_STAGES * PAIR_STAGE_BYTES), 0};
+    const bool issuer = threadIdx.x == 64;
+    const int row_local = quarter * 32 + lane;
+    int it = 0;
+    for (int t = pair; t < total; t += npairs, ++it) {
+      const int slot = t / per_e, rem = t - slot * per_e;
+      const int mb = rem / n_tiles, nb = rem - mb * n_tiles;
+      const int e = s_order[slot];
+      const int n0 = nb * BN;
+      const int y0 = mb * 256 + 128 * static_cast<int>(rank);
+      const bool has_acc = s_cnt[e] > 0;
+      const int acc = it & 1;
+      const uint32_t acc_par = (it >> 1) & 1;
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      // leave together: the store barriers below need all epilogue warps
+      if (named_bar_any(kEpiBar, kEpiThreads, !ok)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const bool write = y0 < args.m_ext;
+      const int nch = min(BN / 32, (args.n_ext - n0 + 31) / 32);
+      uint32_t r[32];
+      if (has_acc) tmem_ld32(tbase, r);
+#pragma unroll 1
+      for (int j = 0; j < nch; ++j) {
+        float v[32];
+        if (has_acc) {
+          tmem_ld_wait(r);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+          if (j + 1 < nch) tmem_ld32(tbase + 32 * (j + 1), r);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        if (write) ring_store(ring, v, true, &args.tma_out0, n0 + 32 * j, y0, e, row_local, issuer);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+    }
+    if (issuer) bulk_wait_all();
+  }
+
+  __syncthreads();
+  cluster_sync();                            // no remote arrivals after this point
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
+  }
+}
+
+cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(k_wgrad_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(PAIR_SMEM_BYTES));
+  if (err != cudaSuccess) return err;
+  const int g = grid & ~1;
+  k_wgrad_pair<<<g < 2 ? 2 : g, NUM_THREADS, PAIR_SMEM_BYTES, s>>>(args);
+  return cudaGetLastError();
 }
 
 template <int MODE, int ACT>
@@ -567,6 +803,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
     case kDgradDglu: return launch_act<kDgradDglu>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0>(args, grid, s);
     case kWgrad: return launch_mode<kWgrad, 0>(args, grid, s);
+    case kWgradPair: return launch_wgrad_pair(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

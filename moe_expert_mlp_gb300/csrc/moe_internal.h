@@ -6,7 +6,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -60,7 +60,8 @@ enum GemmMode : int {
   kFc2 = 1,        // Y = A W2^T (+b2)                          ragged M
   kDgradDglu = 2,  // dA = dY W2, dH = dGLU(dA, H)              ragged M
   kDgradFc1 = 3,   // dX = dH W1p                               ragged M
-  kWgrad = 4       // dW[e] = sum over group rows of P^T Q      ragged K
+  kWgrad = 4,      // dW[e] = sum over group rows of P^T Q      ragged K
+  kWgradPair = 5   // same on CTA pairs (2-SM MMA, 256x256 tiles)
 };
 
 struct GemmArgs {
