@@ -230,6 +230,27 @@ moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
 moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const float* topk_w,
                            const int32_t* topk_idx, float* dlogits, cudaStream_t stream);
 
+/* moe_route_permute for callers that cannot allocate device memory (for
+ * example a host program whose device memory is all handed to its own fixed
+ * pool, or a runtime that allows no allocation after start-up).  The pages
+ * have no counterpart to this call; it exists only for such callers.
+ * Same arguments and results as moe_route_permute minus ws/ws_bytes: the
+ * scratch histogram lives in a static device array of this library
+ * (256 KiB, reserved on every GPU that loads the library until the process
+ * exits).  Requires ceil(T/256)*E*4 <= 262144 bytes, else returns
+ * MOE_ERR_WORKSPACE and enqueues nothing.  It allocates nothing.  The first
+ * call on a device looks up the array's device address (with that device
+ * current) and should happen before any stream capture.  All calls share
+ * the array: calls whose GPU work may overlap (unordered streams) race;
+ * calls ordered on one stream are safe because each call zeroes the
+ * histogram before use. */
+moe_status_t moe_route_permute_noalloc(const moe_mlp_desc_t* desc, const float* logits,
+                                       const float* bias, const void* x, int32_t* topk_idx,
+                                       float* topk_w, int32_t* counts, int32_t* offsets,
+                                       int32_t* padded_offsets, int32_t* tile_prefix,
+                                       int32_t* row_src, int32_t* row_of, void* x_perm,
+                                       cudaStream_t stream);
+
 /* Read (and optionally clear) the sticky device status word of the current
  * device.  Synchronises the device; call outside stream capture. */
 moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear);

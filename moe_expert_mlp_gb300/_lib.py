@@ -26,6 +26,7 @@ EXPORTS = (
     "moe_unpermute_combine_bwd", "moe_mlp_bwd", "moe_permute_bwd", "moe_route_bwd",
     "moe_read_device_status", "moe_status_string", "moe_fc1_glu_fwd", "moe_fc2_fwd",
     "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
+    "moe_route_permute_noalloc",
 )
 
 
@@ -87,6 +88,7 @@ def lib():
             "moe_fc1_dgrad": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_wgrad": (ctypes.c_int, [D] + [P] * 6),
             "moe_bias_grads": (ctypes.c_int, [D] + [P] * 7),
+            "moe_route_permute_noalloc": (ctypes.c_int, [D] + [P] * 12 + [P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -224,3 +226,12 @@ def moe_fc1_wgrad(desc, dh, x_perm, counts, padded_offsets, dw1p, stream=None):
 def moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream=None):
     _check(lib().moe_bias_grads(ctypes.byref(desc), _p(dy), _p(dh), _p(counts),
                                 _p(padded_offsets), _p(db1p), _p(db2), _stream(stream)))
+
+
+def moe_route_permute_noalloc(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,
+                              padded_offsets, tile_prefix, row_src, row_of, x_perm, stream=None):
+    """moe_route_permute without a caller-provided workspace (see include/moe.h)."""
+    _check(lib().moe_route_permute_noalloc(
+        ctypes.byref(desc), _p(logits), _p(bias), _p(x), _p(topk_idx), _p(topk_w), _p(counts),
+        _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of), _p(x_perm),
+        _stream(stream)))
