@@ -99,6 +99,20 @@ def call_work(wl, name, R):
     return "byte", float(mem.get(name, 0.0))
 
 
+# ------------------------------------------------------------ multi-rank
+def max_over_ranks(value, dist, device):
+    """Largest value over all ranks (the slowest replica sets the job time)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(work_per_step, steps, world, ms_max):
+    """Whole-job rate: the work of every rank's steps over the slowest time."""
+    return work_per_step * steps * world / (ms_max * 1e-3)
+
+
 # ------------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi clock / throttle sampling while the GPU works."""
@@ -395,11 +409,7 @@ def run_ours(args, wl):
     per = {}
     for name, a, b in timer.ev:
         per.setdefault(name, []).append(a.elapsed_time(b))
-    ms_max = ms_total
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_max = float(tt.item())
+    ms_max = max_over_ranks(ms_total, dist, dev) if world > 1 else ms_total
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
     e2e = None
@@ -413,7 +423,7 @@ def run_ours(args, wl):
 
     peaks, peak_src = load_peaks()
     ms_step = ms_max / K
-    value = flops_step * K * world / (ms_max * 1e-3) / 1e12
+    value = job_rate(flops_step, K, world, ms_max) / 1e12
     kernels = {}
     dominant, dom_ms = None, -1.0
     for name, ts in per.items():
@@ -439,7 +449,7 @@ def run_ours(args, wl):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(wl), parallelism=f"replicas x{world}",
                        graph=bool(use_graph)),
-        "tokens_per_s": round((wl.T if routed else R) * K * world / (ms_max * 1e-3), 1),
+        "tokens_per_s": round(job_rate(wl.T if routed else R, K, world, ms_max), 1),
         "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
@@ -493,12 +503,10 @@ def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
     if world > 1:
-        tt = torch.tensor([ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+        ms = max_over_ranks(ms, dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in (xh, lh, dh))
     d2h = sum(t.numel() * t.element_size() for t in outs)
-    return {"value": round(flops_step * K * world / (ms * 1e-3) / 1e12, 2), "unit": "TFLOPS",
+    return {"value": round(job_rate(flops_step, K, world, ms) / 1e12, 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / K, 5)}
 

@@ -106,6 +106,30 @@ typedef struct {
   int32_t capacity;     /* rows allocated in every per-row buffer */
 } moe_mlp_desc_t;
 
+/* Optional MXFP8 and NVFP4-preparation outputs of a GEMM epilogue ([FK]
+ * "Reducing exposed memory overhead by fusing MXFP8 and NVFP4
+ * quantization": the BF16 output is also written as MXFP8 rowwise and as a
+ * transposed MXFP8 copy for the backward, and per-tensor amax values are
+ * produced in the same pass).  The quantized values are those of the stored
+ * bf16 tensor X [capacity, width]; padding rows are zero.  Any member may be
+ * NULL to skip that output.
+ *   q       rowwise E4M3 codes [capacity, width], blocks of 32 along a row
+ *   scale   rowwise E8M0 scales [capacity, width/32]             (with q)
+ *   qt      columnwise codes written transposed [width, capacity]; blocks of
+ *           32 consecutive rows (never across expert groups)
+ *   scale_t columnwise scales [width, capacity/32]               (with qt)
+ *   amax    float[2]: max|X| over real rows, and max|H16·s/4| over every
+ *           16-row segment s of every column inside each group (the transposed
+ *           16x16 Hadamard rotation; segments completed with zeros).  The
+ *           call zeroes it first. */
+typedef struct {
+  uint8_t* q;
+  uint8_t* scale;
+  uint8_t* qt;
+  uint8_t* scale_t;
+  float* amax;
+} moe_mx_out_t;
+
 /* F_pad = F rounded up to 128 (packed FC1 width is 2*F_pad). */
 int32_t moe_fc1_padded_width(int32_t F);
 
@@ -152,19 +176,21 @@ moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts
  *   x_perm [capacity,d]; counts [E]; padded_offsets [E+1];
  *   w1p [E,2F_pad,d]; b1p [E,2F_pad] or NULL; w2 [E,d,F]; b2 [E,d] or NULL.
  * Outputs: h [capacity,2F_pad] (FC1 output incl. bias, packed; saved for the
- * backward), a [capacity,F] (GLU output), y [capacity,d].
+ * backward), a [capacity,F] (GLU output), y [capacity,d].  a_mx / y_mx
+ * (NULL = none): MXFP8 / amax outputs of A (width F) and Y (width d).
  * Persistent tcgen05 kernels read the group sizes from device memory. */
 moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          const int32_t* counts, const int32_t* padded_offsets,
                          const void* w1p, const void* b1p, const void* w2, const void* b2,
-                         void* h, void* a, void* y, void* ws, size_t ws_bytes,
+                         void* h, void* a, void* y, const moe_mx_out_t* a_mx,
+                         const moe_mx_out_t* y_mx, void* ws, size_t ws_bytes,
                          cudaStream_t stream);
 
 /* The grouped GEMMs one at a time (moe_mlp_fwd / moe_mlp_bwd call exactly
  * these, in this order).  Buffers and layouts as in those two calls.
- *   moe_fc1_glu_fwd    h, a  <- x_perm, w1p, b1p      (FC1 + GLU epilogue)
- *   moe_fc2_fwd        y     <- a, w2, b2             (FC2, "GroupGemm")
- *   moe_fc2_dgrad_dglu dh    <- dy, w2, h             (dGLU epilogue)
+ *   moe_fc1_glu_fwd    h, a  <- x_perm, w1p, b1p      (FC1 + GLU epilogue [+ MX of A])
+ *   moe_fc2_fwd        y     <- a, w2, b2             (FC2 "GroupGemm" [+ MX of Y])
+ *   moe_fc2_dgrad_dglu dh    <- dy, w2, h             (dGLU epilogue [+ MX of dH])
  *   moe_fc2_wgrad      dw2   <- dy, a                 (K = group rows)
  *   moe_fc1_dgrad      dx_perm <- dh, w1p
  *   moe_fc1_wgrad      dw1p  <- dh, x_perm            (K = group rows)
@@ -173,13 +199,14 @@ moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
 moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                              const int32_t* counts, const int32_t* padded_offsets,
                              const void* w1p, const void* b1p, void* h, void* a,
-                             cudaStream_t stream);
+                             const moe_mx_out_t* a_mx, cudaStream_t stream);
 moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w2, const void* b2, void* y,
-                         cudaStream_t stream);
+                         const moe_mx_out_t* y_mx, cudaStream_t stream);
 moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, const void* h,
                                 const int32_t* counts, const int32_t* padded_offsets,
-                                const void* w2, void* dh, cudaStream_t stream);
+                                const void* w2, void* dh, const moe_mx_out_t* dh_mx,
+                                cudaStream_t stream);
 moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
                            const int32_t* counts, const int32_t* padded_offsets, void* dw2,
                            cudaStream_t stream);
@@ -213,12 +240,14 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
  * [capacity,2F_pad] packed; FC2 wgrad dw2 [E,d,F] = sum over the group's
  * rows of dy^T a; FC1 dgrad dx_perm [capacity,d] = dh w1p; FC1 wgrad
  * dw1p [E,2F_pad,d] = dh^T x_perm (packed); db1p [E,2F_pad] and db2 [E,d]
- * (NULL when the bias is absent).  Experts with no rows get zero gradients. */
+ * (NULL when the bias is absent).  Experts with no rows get zero gradients.
+ * dh_mx (NULL = none): MXFP8 / amax outputs of dH (width 2*F_pad, packed). */
 moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
                          const void* h, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w1p, const void* w2,
                          void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
-                         void* db2, void* ws, size_t ws_bytes, cudaStream_t stream);
+                         void* db2, const moe_mx_out_t* dh_mx, void* ws, size_t ws_bytes,
+                         cudaStream_t stream);
 
 /* Backward of the permutation: dx[t] = sum_s dx_perm[row_of[t,s]] (fp32 in
  * slot order, then bf16).  dx [T,d]. */
@@ -229,6 +258,19 @@ moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
  * dlogits[t,idx[t,s]] = w[t,s]*(dw[t,s] - sum_s' w[t,s']*dw[t,s']), 0 elsewhere. */
 moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const float* topk_w,
                            const int32_t* topk_idx, float* dlogits, cudaStream_t stream);
+
+/* MXFP8 quantization of fp32 values in [rows, cols] (row-major), with the
+ * device quantizer the fused epilogues use ([FK] "Reducing exposed memory
+ * overhead by fusing MXFP8 and NVFP4 quantization"; format: OCP MX E4M3
+ * payload, one E8M0 scale per 32 elements, scale 2^(floor(log2 amax)-8),
+ * round-to-nearest-even with saturation to +-448).
+ *   colwise = 0: blocks run along each row; q [rows, cols], scales
+ *                [rows, cols/32]; cols % 32 == 0.
+ *   colwise = 1: blocks run down each column; q is written transposed
+ *                [cols, rows], scales [cols, rows/32]; rows % 32 == 0.
+ * in and q 16-byte aligned. */
+moe_status_t moe_quantize_mx(const float* in, int32_t rows, int32_t cols, int32_t colwise,
+                             uint8_t* q, uint8_t* scales, cudaStream_t stream);
 
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed
@@ -250,6 +292,13 @@ moe_status_t moe_route_permute_noalloc(const moe_mlp_desc_t* desc, const float* 
                                        int32_t* padded_offsets, int32_t* tile_prefix,
                                        int32_t* row_src, int32_t* row_of, void* x_perm,
                                        cudaStream_t stream);
+
+/* Failure-detection self test (the pages have no counterpart): one CTA waits,
+ * through the bounded mbarrier wait the GEMM pipelines use, on a phase that
+ * nothing completes; after limit_us microseconds (1..5e6) the wait gives up,
+ * sets MOE_DEV_TIMEOUT in the status word and the kernel returns, leaving
+ * the context usable. */
+moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
 /* Read (and optionally clear) the sticky device status word of the current
  * device.  Synchronises the device; call outside stream capture. */

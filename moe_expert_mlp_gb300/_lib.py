@@ -26,7 +26,7 @@ EXPORTS = (
     "moe_unpermute_combine_bwd", "moe_mlp_bwd", "moe_permute_bwd", "moe_route_bwd",
     "moe_read_device_status", "moe_status_string", "moe_fc1_glu_fwd", "moe_fc2_fwd",
     "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
-    "moe_route_permute_noalloc",
+    "moe_route_permute_noalloc", "moe_quantize_mx", "moe_selftest_wait_timeout",
 )
 
 
@@ -43,6 +43,20 @@ class moe_mlp_desc_t(ctypes.Structure):
         ("has_b1", ctypes.c_int32), ("has_b2", ctypes.c_int32), ("align", ctypes.c_int32),
         ("sm_margin", ctypes.c_int32), ("capacity", ctypes.c_int32),
     ]
+
+
+class moe_mx_out_t(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("qt", ctypes.c_void_p),
+                ("scale_t", ctypes.c_void_p), ("amax", ctypes.c_void_p)]
+
+
+def _mx(mx):
+    """dict of optional tensors {q, scale, qt, scale_t, amax} -> struct pointer."""
+    if mx is None:
+        return None
+    st = moe_mx_out_t(*[(_p(mx[k]).value if mx.get(k) is not None else None)
+                        for k in ("q", "scale", "qt", "scale_t", "amax")])
+    return ctypes.byref(st)
 
 
 def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_offset=0.0,
@@ -73,22 +87,25 @@ def lib():
             "moe_unpack_fc1": (ctypes.c_int, [D, P, P, ctypes.c_int32, P]),
             "moe_route_permute": (ctypes.c_int, [D] + [P] * 13 + [ctypes.c_size_t, P]),
             "moe_group_offsets": (ctypes.c_int, [D, P, P, P, P, P]),
-            "moe_mlp_fwd": (ctypes.c_int, [D] + [P] * 11 + [ctypes.c_size_t, P]),
+            "moe_mlp_fwd": (ctypes.c_int, [D] + [P] * 13 + [ctypes.c_size_t, P]),
             "moe_unpermute_combine": (ctypes.c_int, [D, P, P, P, P, P]),
             "moe_unpermute_combine_bwd": (ctypes.c_int, [D] + [P] * 8 + [P]),
-            "moe_mlp_bwd": (ctypes.c_int, [D] + [P] * 15 + [ctypes.c_size_t, P]),
+            "moe_mlp_bwd": (ctypes.c_int, [D] + [P] * 16 + [ctypes.c_size_t, P]),
             "moe_permute_bwd": (ctypes.c_int, [D, P, P, P, P]),
             "moe_route_bwd": (ctypes.c_int, [D, P, P, P, P, P]),
             "moe_read_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]),
             "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
-            "moe_fc1_glu_fwd": (ctypes.c_int, [D] + [P] * 8),
-            "moe_fc2_fwd": (ctypes.c_int, [D] + [P] * 7),
-            "moe_fc2_dgrad_dglu": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc1_glu_fwd": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_fwd": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_dgrad_dglu": (ctypes.c_int, [D] + [P] * 8),
             "moe_fc2_wgrad": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_dgrad": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_wgrad": (ctypes.c_int, [D] + [P] * 6),
             "moe_bias_grads": (ctypes.c_int, [D] + [P] * 7),
             "moe_route_permute_noalloc": (ctypes.c_int, [D] + [P] * 12 + [P]),
+            "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
+            "moe_quantize_mx": (ctypes.c_int, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                               P, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -151,11 +168,11 @@ def moe_group_offsets(desc, counts, offsets, padded_offsets, tile_prefix, stream
 
 
 def moe_mlp_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, w2, b2, h, a, y, ws=None,
-                stream=None):
+                stream=None, a_mx=None, y_mx=None):
     _check(lib().moe_mlp_fwd(
         ctypes.byref(desc), _p(x_perm), _p(counts), _p(padded_offsets), _p(w1p), _p(b1p), _p(w2),
-        _p(b2), _p(h), _p(a), _p(y), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
-        _stream(stream)))
+        _p(b2), _p(h), _p(a), _p(y), _mx(a_mx), _mx(y_mx), _p(ws),
+        ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
 
 
 def moe_unpermute_combine(desc, y, row_of, topk_w, out, stream=None):
@@ -171,11 +188,11 @@ def moe_unpermute_combine_bwd(desc, dout, y, row_of, topk_w, row_src, padded_off
 
 
 def moe_mlp_bwd(desc, dy, x_perm, h, a, counts, padded_offsets, w1p, w2, dh, dx_perm, dw1p, db1p,
-                dw2, db2, ws=None, stream=None):
+                dw2, db2, ws=None, stream=None, dh_mx=None):
     _check(lib().moe_mlp_bwd(
         ctypes.byref(desc), _p(dy), _p(x_perm), _p(h), _p(a), _p(counts), _p(padded_offsets),
-        _p(w1p), _p(w2), _p(dh), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2), _p(ws),
-        ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+        _p(w1p), _p(w2), _p(dh), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2), _mx(dh_mx),
+        _p(ws), ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
 
 
 def moe_permute_bwd(desc, dx_perm, row_of, dx, stream=None):
@@ -193,19 +210,19 @@ def moe_read_device_status(clear=True):
     return int(v.value)
 
 
-def moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream=None):
+def moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream=None, mx=None):
     _check(lib().moe_fc1_glu_fwd(ctypes.byref(desc), _p(x_perm), _p(counts), _p(padded_offsets),
-                                 _p(w1p), _p(b1p), _p(h), _p(a), _stream(stream)))
+                                 _p(w1p), _p(b1p), _p(h), _p(a), _mx(mx), _stream(stream)))
 
 
-def moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, stream=None):
+def moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, stream=None, mx=None):
     _check(lib().moe_fc2_fwd(ctypes.byref(desc), _p(a), _p(counts), _p(padded_offsets), _p(w2),
-                             _p(b2), _p(y), _stream(stream)))
+                             _p(b2), _p(y), _mx(mx), _stream(stream)))
 
 
-def moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, stream=None):
+def moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, stream=None, mx=None):
     _check(lib().moe_fc2_dgrad_dglu(ctypes.byref(desc), _p(dy), _p(h), _p(counts),
-                                    _p(padded_offsets), _p(w2), _p(dh), _stream(stream)))
+                                    _p(padded_offsets), _p(w2), _p(dh), _mx(mx), _stream(stream)))
 
 
 def moe_fc2_wgrad(desc, dy, a, counts, padded_offsets, dw2, stream=None):
@@ -226,6 +243,18 @@ def moe_fc1_wgrad(desc, dh, x_perm, counts, padded_offsets, dw1p, stream=None):
 def moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream=None):
     _check(lib().moe_bias_grads(ctypes.byref(desc), _p(dy), _p(dh), _p(counts),
                                 _p(padded_offsets), _p(db1p), _p(db2), _stream(stream)))
+
+
+def moe_selftest_wait_timeout(limit_us, stream=None):
+    _check(lib().moe_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def moe_quantize_mx(x, colwise, q, scales, stream=None):
+    """MXFP8-quantize fp32 x [rows, cols] rowwise (colwise=False) or
+    columnwise into the transposed q (colwise=True)."""
+    rows, cols = x.shape
+    _check(lib().moe_quantize_mx(_p(x), rows, cols, int(bool(colwise)), _p(q), _p(scales),
+                                 _stream(stream)))
 
 
 def moe_route_permute_noalloc(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "moe_internal.h"
+#include "moe_ptx.cuh"
 
 namespace moe {
 
@@ -22,6 +23,20 @@ namespace moe {
 __device__ int g_status_word;
 
 namespace {
+
+// One CTA waits, with the pipelines' bounded wait, on an mbarrier phase that
+// nothing completes; the wait gives up after limit_ns and records a timeout.
+__global__ void k_wait_selftest(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) mbar_wait(&bar, 0, status, &abort_flag, limit_ns);
+}
 
 constexpr int kMaxDevices = 64;
 
@@ -119,6 +134,22 @@ size_t route_ws_bytes(const moe_mlp_desc_t* d) {
 bool encode_out(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
   return encode_map(map, base, d0, d1, d2, d0 * 2, d1 * d0 * 2, 32, 128,
                     CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+// Copy the optional MX outputs into the kernel arguments; zero the amax.
+moe_status_t set_mx(GemmArgs& g, const moe_mx_out_t* mx, long long width, cudaStream_t stream) {
+  if (!mx) return MOE_OK;
+  if ((mx->q && !mx->scale) || (mx->qt && !mx->scale_t)) return MOE_ERR_NULL;
+  if ((reinterpret_cast<uintptr_t>(mx->q) & 15) || width % 32 != 0) return MOE_ERR_SHAPE;
+  g.mx_q = mx->q;
+  g.mx_s = mx->scale;
+  g.mx_qt = mx->qt;
+  g.mx_st = mx->scale_t;
+  g.mx_amax = mx->amax;
+  g.mx_width = width;
+  if (mx->amax && cudaMemsetAsync(mx->amax, 0, 2 * sizeof(float), stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -250,7 +281,7 @@ moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts
 moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                              const int32_t* counts, const int32_t* padded_offsets,
                              const void* w1p, const void* b1p, void* h, void* a,
-                             cudaStream_t stream) {
+                             const moe_mx_out_t* a_mx, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
@@ -274,12 +305,13 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
   g.ld1 = F;
   g.bias = desc->has_b1 ? b1p : nullptr;
   g.bias_ld = 2 * Fp;
+  if ((st = set_mx(g, a_mx, desc->F, stream)) != MOE_OK) return st;
   return cuda_status(launch_grouped_gemm(kFc1Glu, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w2, const void* b2, void* y,
-                         cudaStream_t stream) {
+                         const moe_mx_out_t* y_mx, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   if (!a || !counts || !padded_offsets || !w2 || !y) return MOE_ERR_NULL;
@@ -301,20 +333,23 @@ moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_
   g.ld0 = d;
   g.bias = desc->has_b2 ? b2 : nullptr;
   g.bias_ld = d;
+  if ((st = set_mx(g, y_mx, desc->d, stream)) != MOE_OK) return st;
   return cuda_status(launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          const int32_t* counts, const int32_t* padded_offsets,
                          const void* w1p, const void* b1p, const void* w2, const void* b2,
-                         void* h, void* a, void* y, void* ws, size_t ws_bytes,
+                         void* h, void* a, void* y, const moe_mx_out_t* a_mx,
+                         const moe_mx_out_t* y_mx, void* ws, size_t ws_bytes,
                          cudaStream_t stream) {
   (void)ws;
   (void)ws_bytes;
   if (!w2 || !y || (desc && desc->has_b2 && !b2)) return MOE_ERR_NULL;
-  moe_status_t st = moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream);
+  moe_status_t st =
+      moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, a_mx, stream);
   if (st != MOE_OK) return st;
-  return moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, stream);
+  return moe_fc2_fwd(desc, a, counts, padded_offsets, w2, b2, y, y_mx, stream);
 }
 
 moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
@@ -348,7 +383,8 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
 
 moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, const void* h,
                                 const int32_t* counts, const int32_t* padded_offsets,
-                                const void* w2, void* dh, cudaStream_t stream) {
+                                const void* w2, void* dh, const moe_mx_out_t* dh_mx,
+                                cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   if (!dy || !h || !counts || !padded_offsets || !w2 || !dh) return MOE_ERR_NULL;
@@ -370,6 +406,7 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
   g.ld0 = 2 * Fp;
   g.aux = h;
   g.ld_aux = 2 * Fp;
+  if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
   return cuda_status(launch_grouped_gemm(kDgradDglu, g, grid_for(di, desc), stream));
 }
 
@@ -468,7 +505,8 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
                          const void* h, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w1p, const void* w2,
                          void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
-                         void* db2, void* ws, size_t ws_bytes, cudaStream_t stream) {
+                         void* db2, const moe_mx_out_t* dh_mx, void* ws, size_t ws_bytes,
+                         cudaStream_t stream) {
   (void)ws;
   (void)ws_bytes;
   moe_status_t st = check_desc(desc, false);
@@ -477,7 +515,8 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
       !dx_perm || !dw1p || !dw2)
     return MOE_ERR_NULL;
   if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
-  if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, stream)) != MOE_OK)
+  if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, dh_mx, stream)) !=
+      MOE_OK)
     return st;
   if ((st = moe_fc2_wgrad(desc, dy, a, counts, padded_offsets, dw2, stream)) != MOE_OK) return st;
   if ((st = moe_fc1_dgrad(desc, dh, counts, padded_offsets, w1p, dx_perm, stream)) != MOE_OK)
@@ -509,6 +548,15 @@ moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const fl
   if ((st = device_info(&di)) != MOE_OK) return st;
   return cuda_status(
       launch_route_bwd(dw, topk_w, topk_idx, desc->T, desc->E, desc->k, dlogits, stream));
+}
+
+moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 5000000) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  k_wait_selftest<<<1, 32, 0, stream>>>(di->status, 1000ull * limit_us);
+  return cuda_status(cudaGetLastError());
 }
 
 moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear) {

@@ -32,6 +32,7 @@
 #include <math.h>
 
 #include "moe_internal.h"
+#include "moe_mx.cuh"
 #include "moe_ptx.cuh"
 
 namespace moe {
@@ -381,6 +382,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
     StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES), 0};
     const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
+    const MxOut mx{args.mx_q, args.mx_s, args.mx_qt, args.mx_st, args.mx_amax, args.mx_width,
+                   args.capacity};
+    const bool want_mx = mx.q != nullptr || mx.qt != nullptr || mx.amax != nullptr;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
@@ -451,6 +455,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
             ring_store(ring, a, valid, &args.tma_out1, f0, y0, 0, row_local, issuer);
+            if (want_mx) {                      // MXFP8 / amax of the stored bf16 A
+#pragma unroll
+              for (int i = 0; i < 32; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
+              mx_epilogue_block(mx, a, y0 + quarter * 32, f0, lane);
+            }
           }
         }
       } else if (MODE == kDgradDglu) {
@@ -480,6 +489,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
           ring_store(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
           ring_store(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local, issuer);
+          if (want_mx) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              dg[i] = live0 ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live0 ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_epilogue_block(mx, dg, y0 + quarter * 32, c0, lane);
+            mx_epilogue_block(mx, dl, y0 + quarter * 32, c0 + kGluHalf, lane);
+          }
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
             load_raw64(Hrow + c2, hg[0]);
@@ -493,6 +511,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
           ring_store(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
           ring_store(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local, issuer);
+          if (want_mx) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_epilogue_block(mx, dg, y0 + quarter * 32, c1, lane);
+            mx_epilogue_block(mx, dl, y0 + quarter * 32, c1 + kGluHalf, lane);
+          }
         }
       } else {
         // kFc2 (+b2), kDgradFc1 and kWgrad: plain row-major bf16 output
@@ -527,6 +554,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (write)
             ring_store(ring, v, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
                        Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+          if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the stored bf16 Y
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = valid ? bf16_round(v[i]) : 0.0f;
+            mx_epilogue_block(mx, v, y0 + quarter * 32, c0, lane);
+          }
         }
       }
       tc_fence_before();

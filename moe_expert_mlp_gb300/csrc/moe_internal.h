@@ -90,6 +90,13 @@ struct GemmArgs {
   long long ld_aux;
   const void* bias;
   long long bias_ld;
+  // optional MXFP8 / amax outputs of the epilogue's bf16 result
+  uint8_t* mx_q;
+  uint8_t* mx_s;
+  uint8_t* mx_qt;
+  uint8_t* mx_st;
+  float* mx_amax;
+  long long mx_width;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);

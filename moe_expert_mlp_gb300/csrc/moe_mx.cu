@@ -1,0 +1,72 @@
+// Standalone MXFP8 quantization (rowwise, or columnwise written transposed),
+// using the same device quantizer as the fused GEMM epilogues.  It exists so
+// that codes and scales can be checked bit for bit against the oracle on
+// identical fp32 inputs.
+#include <cuda_runtime.h>
+
+#include "moe_internal.h"
+#include "moe_mx.cuh"
+
+namespace moe {
+namespace {
+
+// Rowwise: one thread per 32-element block of a row.
+__global__ void __launch_bounds__(256) k_quant_rows(const float* __restrict__ in, int rows,
+                                                    int cols, uint8_t* __restrict__ q,
+                                                    uint8_t* __restrict__ scales) {
+  const int bpr = cols / 32;
+  const long long nblk = static_cast<long long>(rows) * bpr;
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblk;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long r = b / bpr, c = (b - r * bpr) * 32;
+    const float4* src = reinterpret_cast<const float4*>(in + r * cols + c);
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float4 f = __ldg(src + i);
+      v[4 * i] = f.x;
+      v[4 * i + 1] = f.y;
+      v[4 * i + 2] = f.z;
+      v[4 * i + 3] = f.w;
+    }
+    scales[b] = mx_quant32(v, q + r * cols + c);
+  }
+}
+
+// Columnwise: one thread per (column, 32-row block); codes go to the
+// transposed tensor qT [cols, rows], scales to [cols, rows/32].
+__global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in, int rows,
+                                                    int cols, uint8_t* __restrict__ qt,
+                                                    uint8_t* __restrict__ scales) {
+  const int rb_n = rows / 32;
+  const long long nblk = static_cast<long long>(cols) * rb_n;
+  for (long long b = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; b < nblk;
+       b += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long rb = b / cols, c = b - rb * cols;     // adjacent threads: adjacent columns
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __ldg(in + (rb * 32 + i) * cols + c);
+    scales[c * rb_n + rb] = mx_quant32(v, qt + c * rows + rb * 32);
+  }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_quantize_mx(const float* in, int32_t rows, int32_t cols,
+                                        int32_t colwise, uint8_t* q, uint8_t* scales,
+                                        cudaStream_t stream) {
+  if (!in || !q || !scales) return MOE_ERR_NULL;
+  if (rows < 0 || cols < 0) return MOE_ERR_SHAPE;
+  if (colwise ? (rows % 32 != 0) : (cols % 32 != 0)) return MOE_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(q) & 15))
+    return MOE_ERR_SHAPE;
+  if (rows == 0 || cols == 0) return MOE_OK;
+  const long long nblk = static_cast<long long>(rows) * cols / 32;
+  const int grid = static_cast<int>((nblk + 255) / 256 < 65535 ? (nblk + 255) / 256 : 65535);
+  if (colwise)
+    moe::k_quant_cols<<<grid, 256, 0, stream>>>(in, rows, cols, q, scales);
+  else
+    moe::k_quant_rows<<<grid, 256, 0, stream>>>(in, rows, cols, q, scales);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}

@@ -1,0 +1,144 @@
+// MXFP8 (OCP Microscaling: E4M3 payload, one E8M0 scale per 32 elements)
+// and NVFP4-preparation amax helpers shared by the quantize kernel and the
+// GEMM epilogues.
+//
+// "Improving MoE training throughput with advanced fused kernels", "Reducing
+// exposed memory overhead by fusing MXFP8 and NVFP4 quantization": the
+// activation output (BF16) is written in MXFP8 together with a transposed
+// MXFP8 copy for the backward; for NVFP4 a per-tensor amax of the output and
+// of its transposed Hadamard-rotated form is produced in the same pass.
+//
+// Scale rule: X = 2^(floor(log2 amax) - 8), exponent clamped to [-127, 127],
+// E8M0 code = exponent + 127 (code 0 for an all-zero block).  Payload: v / X
+// rounded to nearest-even E4M3 with saturation to +-448 (the hardware
+// cvt.rn.satfinite conversion); dividing by X is an exact power-of-two scale.
+#pragma once
+
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+namespace moe {
+
+// floor(log2(a)) of a finite a > 0, exact (handles fp32 subnormals).
+__device__ __forceinline__ int floor_log2_f32(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int e = static_cast<int>((b >> 23) & 0xFFu);
+  if (e != 0) return e - 127;
+  return (31 - __clz(static_cast<int>(b & 0x7FFFFFu))) - 149;
+}
+
+// Unbiased E8M0 exponent of the block scale for block abs-max `amax`.
+__device__ __forceinline__ int mx_scale_exponent(float amax) {
+  if (!(amax > 0.0f)) return -127;
+  const int s = floor_log2_f32(amax) - 8;
+  return s < -127 ? -127 : (s > 127 ? 127 : s);
+}
+
+// 2^-s as fp32 (s in [-127, 119] for finite fp32 amax, so 2^-s is normal).
+__device__ __forceinline__ float mx_inv_scale(int s) {
+  return __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+}
+
+// Two fp32 values -> two E4M3 codes (a in the low byte).
+__device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
+  const __nv_fp8x2_storage_t r =
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  return static_cast<uint32_t>(r);
+}
+
+// Quantize one block of 32 values: writes 32 codes (16-byte aligned
+// destination) and returns the E8M0 scale code.
+__device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* q) {
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  const int s = mx_scale_exponent(amax);
+  const float inv = mx_inv_scale(s);
+  uint32_t w[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t lo = e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv);
+    const uint32_t hi = e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv);
+    w[j] = lo | (hi << 16);
+  }
+  uint4* d = reinterpret_cast<uint4*>(q);
+  d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+  d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+  return static_cast<uint8_t>(s + 127);
+}
+
+// Non-negative float max into a global word (bit patterns of non-negative
+// floats order like the floats, so an integer max is exact and order-free).
+__device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
+  atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
+}
+
+// Optional MXFP8 / amax outputs of a GEMM epilogue (all-null = none).
+struct MxOut {
+  uint8_t* q;        // rowwise codes [cap, width]
+  uint8_t* s;        // rowwise scales [cap, width/32]
+  uint8_t* qt;       // columnwise codes, transposed [width, cap]
+  uint8_t* st;       // columnwise scales [width, cap/32]
+  float* amax;       // [2]: max |x|, max |H16 x^T / 4|
+  long long width;
+  long long cap;
+};
+
+// One warp holds a 32 x 32 block: lane l owns row r0 + l, columns
+// col0 .. col0+31 in v (already rounded to the stored bf16 values; zero on
+// padding rows).  Writes the rowwise block of this lane, the columnwise
+// blocks (32 rows = the warp) of the 32 columns, and folds the plain and
+// Hadamard amax into mx.amax.  Whole warp must call.
+__device__ __forceinline__ void mx_epilogue_block(const MxOut& mx, const float (&v)[32],
+                                                  long long r0, int col0, int lane) {
+  const long long row = r0 + lane;
+  if (mx.q) {
+    const uint8_t sc = mx_quant32(v, mx.q + row * mx.width + col0);
+    mx.s[row * (mx.width / 32) + col0 / 32] = sc;
+  }
+  if (mx.qt) {
+    uint8_t my_sc = 0;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      float a = fabsf(v[i]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
+      const int sx = mx_scale_exponent(a);
+      const uint32_t code = e4m3x2(v[i] * mx_inv_scale(sx), 0.0f) & 0xFFu;
+      mx.qt[static_cast<long long>(col0 + i) * mx.cap + row] = static_cast<uint8_t>(code);
+      if (lane == i) my_sc = static_cast<uint8_t>(sx + 127);
+    }
+    mx.st[static_cast<long long>(col0 + lane) * (mx.cap / 32) + r0 / 32] = my_sc;
+  }
+  if (mx.amax) {
+    float m = 0.0f, h = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      m = fmaxf(m, fabsf(v[i]));
+      // Walsh-Hadamard butterflies across the 16 rows of each half warp
+      // (rows r0..r0+15 and r0+16..r0+31 are 16-row segments of one group)
+      float x = v[i];
+#pragma unroll
+      for (int b = 1; b < 16; b <<= 1) {
+        const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
+        x = (lane & b) ? (p - x) : (x + p);
+      }
+      h = fmaxf(h, fabsf(x) * 0.25f);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+      h = fmaxf(h, __shfl_xor_sync(0xFFFFFFFFu, h, o));
+    }
+    if (lane == 0) {
+      atomic_max_nonneg(mx.amax, m);
+      atomic_max_nonneg(mx.amax + 1, h);
+    }
+  }
+}
+
+__device__ __forceinline__ float bf16_round(float x) {
+  return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+}  // namespace moe

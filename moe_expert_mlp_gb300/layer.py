@@ -104,18 +104,29 @@ class MoEExpertMLP:
         L.moe_group_offsets(self.desc, self.counts, self.offsets, self.padded_offsets,
                             self.tile_prefix, stream)
 
-    def mlp_forward(self, stream=None, timer=None):
+    def mx_buffers(self, width):
+        """Device buffers for the optional MXFP8 / amax outputs of a tensor
+        [capacity, width] (see moe_mx_out_t in include/moe.h)."""
+        cap, dev, u8 = self.capacity, self.w2.device, torch.uint8
+        return dict(q=torch.zeros((cap, width), dtype=u8, device=dev),
+                    scale=torch.zeros((cap, width // 32), dtype=u8, device=dev),
+                    qt=torch.zeros((width, cap), dtype=u8, device=dev),
+                    scale_t=torch.zeros((width, cap // 32), dtype=u8, device=dev),
+                    amax=torch.zeros(2, dtype=torch.float32, device=dev))
+
+    def mlp_forward(self, stream=None, timer=None, a_mx=None, y_mx=None):
         c, po = self.counts, self.padded_offsets
         with self._t(timer, "fc1_glu_fwd"):
             L.moe_fc1_glu_fwd(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h, self.a,
-                              stream)
+                              stream, mx=a_mx)
         with self._t(timer, "fc2_fwd"):
-            L.moe_fc2_fwd(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream)
+            L.moe_fc2_fwd(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream, mx=y_mx)
 
-    def mlp_backward(self, stream=None, timer=None):
+    def mlp_backward(self, stream=None, timer=None, dh_mx=None):
         c, po = self.counts, self.padded_offsets
         with self._t(timer, "fc2_dgrad_dglu"):
-            L.moe_fc2_dgrad_dglu(self.desc, self.dy, self.h, c, po, self.w2, self.dh, stream)
+            L.moe_fc2_dgrad_dglu(self.desc, self.dy, self.h, c, po, self.w2, self.dh, stream,
+                                 mx=dh_mx)
         with self._t(timer, "fc2_wgrad"):
             L.moe_fc2_wgrad(self.desc, self.dy, self.a, c, po, self.dw2, stream)
         with self._t(timer, "fc1_dgrad"):
