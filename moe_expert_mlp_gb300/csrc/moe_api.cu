@@ -129,6 +129,38 @@ size_t route_ws_bytes(const moe_mlp_desc_t* d) {
   return (nchunks * d->E * sizeof(int32_t) + 255) / 256 * 256;
 }
 
+// MN-major operand [E][K rows][W] (W contiguous, W % 64 == 0) viewed as
+// [E][W/64 atoms][K][64] so that one box {64, 64 rows, atoms, 1} fetches
+// several 64-column atoms; the atom stride (128 B) is smaller than the row
+// stride.  Returns false if the driver does not accept the view.
+bool encode_mn_atoms(CUtensorMap* map, const void* base, uint64_t W, uint64_t K, uint64_t E,
+                     uint64_t row_bytes, uint64_t plane_bytes, uint32_t atoms) {
+  if (W % 64 != 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[4] = {64, K, W / 64, E};
+  cuuint64_t strides[3] = {row_bytes, 128, plane_bytes};
+  cuuint32_t box[4] = {64, 64, atoms, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims,
+                        strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Output [E][rows][W] viewed as [E][W/32][rows][32]: box {32, 128, 2, 1}
+// stores two adjacent 32-column chunks staged back to back.
+bool encode_out2(CUtensorMap* map, const void* base, uint64_t W, uint64_t rows, uint64_t E) {
+  if (W % 32 != 0 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[4] = {32, rows, W / 32, E};
+  cuuint64_t strides[3] = {W * 2, 64, rows * W * 2};
+  cuuint32_t box[4] = {32, 128, 2, 1};
+  cuuint32_t estride[4] = {1, 1, 1, 1};
+  return g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+                  box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Output map: 32-column x 128-row boxes with 64-byte swizzle (the epilogue
 // staging layout).
 bool encode_out(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2) {
@@ -324,7 +356,7 @@ moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, a, F, cap, 1, F * 2, cap * F * 2, 64, 128) ||
       !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 256) ||
-      !encode_out(&g.tma_out0, y, d, cap, 1))
+      !encode_out(&g.tma_out0, y, d, cap, 1) || !encode_out2(&g.tma_out2, y, d, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->F;
   g.n_ext = desc->d;
@@ -396,8 +428,10 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64) ||
       !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 4);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = static_cast<int>(Fp);
@@ -423,9 +457,13 @@ moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const voi
   // dW2[e] (d x F) = sum over the group's rows of dY^T A (both read MN-major)
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
-      !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64) ||
-      !encode_out(&g.tma_out0, dw2, F, d, E))
+  if (!encode_out(&g.tma_out0, dw2, F, d, E) || !encode_out2(&g.tma_out2, dw2, F, d, E))
+    return MOE_ERR_SHAPE;
+  g.a_atoms4d = encode_mn_atoms(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 2);
+  if (!g.a_atoms4d && !encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 2);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, a, F, cap, 1, F * 2, cap * F * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.m_ext = desc->d;
   g.n_ext = desc->F;
@@ -449,8 +487,11 @@ moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64) ||
-      !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
+      !encode_out(&g.tma_out0, dx_perm, d, cap, 1) ||
+      !encode_out2(&g.tma_out2, dx_perm, d, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 4);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.K = static_cast<int>(2 * Fp);
   g.n_ext = desc->d;
@@ -473,9 +514,15 @@ moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const voi
   // dW1p[e] (2F_pad x d) = sum over the group's rows of dH^T X
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64) ||
-      !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64) ||
-      !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
+  if (!encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E) ||
+      !encode_out2(&g.tma_out2, dw1p, d, 2 * Fp, E))
+    return MOE_ERR_SHAPE;
+  g.a_atoms4d = encode_mn_atoms(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 2);
+  if (!g.a_atoms4d &&
+      !encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 2);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.m_ext = static_cast<int>(2 * Fp);
   g.n_ext = desc->d;

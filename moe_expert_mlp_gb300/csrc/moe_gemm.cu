@@ -49,7 +49,7 @@ constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
 constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
 constexpr int NUM_THREADS = 192;
-constexpr int kRing = 3;                     // output staging boxes (shared by the epilogue)
+constexpr int kRing = 4;                     // output staging boxes (shared by the epilogue)
 constexpr int BOX_BYTES = 128 * 32 * 2;      // one 128-row x 32-column bf16 output box
 constexpr int kEpiThreads = 128;             // 4 epilogue warps
 constexpr int kEpiBar = 1;                   // named barrier of the epilogue warps
@@ -166,6 +166,45 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
   ring.slot = ring.slot == kRing - 1 ? 0 : ring.slot + 1;
 }
 
+// Two adjacent 32-column chunks per round, one TMA store for both.  Rounds
+// alternate between slot pairs {0,1} and {2,3}; the issuer waits for every
+// earlier store to finish reading before the round's barrier, so the pair
+// the next round writes (last stored two rounds ago) is free.  map2 views the
+// output as [E][W/32][rows][32]; the second chunk of a single-chunk round lies
+// past the tensor's end and is clipped.
+__device__ __forceinline__ void stage_box(uint32_t buf, const float (&v)[32], bool live, int row) {
+  const uint32_t raddr = buf + row * 64;
+  const uint32_t sw = (row >> 1) & 3;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (live) {
+      w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
+      w.y = pack_bf16x2(v[8 * q + 2], v[8 * q + 3]);
+      w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
+      w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
+    }
+    st_shared_v4(raddr + ((q ^ sw) << 4), w);
+  }
+}
+
+__device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v0)[32],
+                                                const float (&v1)[32], bool two, bool live,
+                                                const CUtensorMap* map2, int c0, int y, int z,
+                                                int row, bool issuer) {
+  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;   // slot is 0 or 2
+  stage_box(buf, v0, live, row);
+  if (two) stage_box(buf + BOX_BYTES, v1, live, row);
+  fence_proxy_async_smem();
+  if (issuer) bulk_wait_read<0>();
+  named_bar_sync(kEpiBar, kEpiThreads);
+  if (issuer) {
+    tma_store_4d(map2, buf, 0, y, c0 / 32, z);
+    bulk_commit();
+  }
+  ring.slot ^= 2;
+}
+
 template <int MODE>
 struct Traits {
   static constexpr bool kRaggedK = (MODE == kWgrad);
@@ -220,7 +259,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
   __shared__ int s_abort;
   __shared__ int s_total;
   __shared__ int s_off[kMaxExperts + 1];
-  __shared__ int s_cnt[kMaxExperts];
   __shared__ int s_order[kMaxExperts];
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dyn_smem) + 1023) &
@@ -230,7 +268,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 
   // ---- group tables (sizes live in device memory; no host round trip)
   for (int i = threadIdx.x; i <= E; i += NUM_THREADS) s_off[i] = args.padded_offsets[i];
-  for (int i = threadIdx.x; i < E; i += NUM_THREADS) s_cnt[i] = args.counts[i];
+  const int* __restrict__ s_cnt = args.counts;   // group sizes read through L1
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < STAGES; ++s) {
@@ -295,7 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
         const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
         // boxes that hold at least one in-range column (skip fully-outside boxes)
-        const int b_boxes = Tr::kBmn ? min(4, (args.b_ext - ti.n0 + 63) / 64) : 1;
+        const int b_boxes = Tr::kBmn ? (args.b_atoms4d ? 4 : min(4, (args.b_ext - ti.n0 + 63) / 64)) : 1;
         const int a_boxes = Tr::kAmn ? min(2, (args.m_ext - ti.m0 + 63) / 64) : 1;
         const uint32_t tx = (Tr::kAmn ? a_boxes * MN_BOX_BYTES : A_BYTES) +
                             (Tr::kBmn ? b_boxes * MN_BOX_BYTES : B_BYTES);
@@ -320,8 +358,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (MODE == kFc1Glu || MODE == kFc2) {
             tma_load_3d(sb, &args.tma_b, fb, kk, ti.n0, ti.e);
           } else if (MODE == kDgradDglu || MODE == kDgradFc1) {
-            for (int i = 0; i < b_boxes; ++i)
-              tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, kk, ti.e);
+            if (args.b_atoms4d)
+              tma_load_4d(sb, &args.tma_b, fb, 0, kk, ti.n0 / 64, ti.e);
+            else
+              for (int i = 0; i < b_boxes; ++i)
+                tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, kk, ti.e);
           } else {
             for (int i = 0; i < b_boxes; ++i)
               tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, ti.k_row0 + kk, 0);
@@ -530,34 +571,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
                 ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
                 : nullptr;
         const int nch = min(BN / 32, (args.n_ext - ti.n0 + 31) / 32);
-        uint32_t r[32];
-        if (has_acc) tmem_ld32(tbase, r);
+        // TMEM is read two 32-column chunks per wait; the next pair is in
+        // flight while the current one is staged and stored.
+        uint32_t ra[32], rb[32];
+        if (has_acc) {
+          tmem_ld32(tbase, ra);
+          if (nch > 1) tmem_ld32(tbase + 32, rb);
+        }
 #pragma unroll 1
-        for (int j = 0; j < nch; ++j) {
+        for (int j = 0; j < nch; j += 2) {
+          const bool two = j + 1 < nch;
           const int c0 = ti.n0 + 32 * j;
-          float v[32];
+          float v0[32], v1[32];
           if (has_acc) {
-            tmem_ld_wait(r);
+            tmem_ld_wait(ra);
+            reg_fence(rb);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-            if (j + 1 < nch) tmem_ld32(tbase + 32 * (j + 1), r);
+            for (int i = 0; i < 32; ++i) {
+              v0[i] = __uint_as_float(ra[i]);
+              v1[i] = __uint_as_float(rb[i]);
+            }
+            if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), ra);
+            if (j + 3 < nch) tmem_ld32(tbase + 32 * (j + 3), rb);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
           }
           if (bias && valid) {
             float b[32];
             load_bf16x32(bias + c0, b);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] += b[i];
+            for (int i = 0; i < 32; ++i) v0[i] += b[i];
+            if (two) {
+              load_bf16x32(bias + c0 + 32, b);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v1[i] += b[i];
+            }
           }
           if (write)
-            ring_store(ring, v, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
-                       Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+            ring_store_pair(ring, v0, v1, two, Tr::kRaggedK || valid, &args.tma_out2, c0, y0,
+                            Tr::kRaggedK ? ti.e : 0, row_local, issuer);
           if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the stored bf16 Y
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = valid ? bf16_round(v[i]) : 0.0f;
-            mx_epilogue_block(mx, v, y0 + quarter * 32, c0, lane);
+            for (int i = 0; i < 32; ++i) v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
+            mx_epilogue_block(mx, v0, y0 + quarter * 32, c0, lane);
+            if (two) {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) v1[i] = valid ? bf16_round(v1[i]) : 0.0f;
+              mx_epilogue_block(mx, v1, y0 + quarter * 32, c0 + 32, lane);
+            }
           }
         }
       }
@@ -585,7 +647,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 // the MMAs (M=256, N=256) and its commits arrive on both CTAs' barriers;
 // both CTAs' TMA loads complete on the lead CTA's "full" barriers.  Per SM
 // this halves the operand bytes per MMA relative to the single-CTA tile.
-constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_STAGES = 5;
 constexpr int PAIR_HALF = 128 * BK * 2;               // 16 KB
 constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF;       // A half + B half
 constexpr size_t PAIR_SMEM_BYTES =
@@ -675,6 +737,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
         for (int r = 0; r < 2; ++r) {
           nbox[r][0] = max(0, min(2, (args.m_ext - (m0 + 128 * r) + 63) / 64));
           nbox[r][1] = max(0, min(2, (args.b_ext - (n0 + 128 * r) + 63) / 64));
+          // a 4-D atom load always moves both atoms (out-of-range ones zero-filled)
+          if (args.a_atoms4d && nbox[r][0] > 0) nbox[r][0] = 2;
+          if (args.b_atoms4d && nbox[r][1] > 0) nbox[r][1] = 2;
         }
         const uint32_t tx = (nbox[0][0] + nbox[0][1] + nbox[1][0] + nbox[1][1]) * MN_BOX_BYTES;
         const int my_a = nbox[rank][0], my_b = nbox[rank][1];
@@ -688,10 +753,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);
           if (rank == 0) mbar_arrive_expect_tx(&full_bar[stage], tx);
           const int kr = k_row0 + kb * BK;
-          for (int i = 0; i < my_a; ++i)
-            tma_load_3d_pair(sa + i * MN_BOX_BYTES, &args.tma_a, fb, m0 + 128 * rank + 64 * i, kr, 0);
-          for (int i = 0; i < my_b; ++i)
-            tma_load_3d_pair(sb + i * MN_BOX_BYTES, &args.tma_b, fb, n0 + 128 * rank + 64 * i, kr, 0);
+          if (args.a_atoms4d) {
+            if (my_a) tma_load_4d_pair(sa, &args.tma_a, fb, 0, kr, (m0 + 128 * rank) / 64, 0);
+          } else {
+            for (int i = 0; i < my_a; ++i)
+              tma_load_3d_pair(sa + i * MN_BOX_BYTES, &args.tma_a, fb, m0 + 128 * rank + 64 * i, kr, 0);
+          }
+          if (args.b_atoms4d) {
+            if (my_b) tma_load_4d_pair(sb, &args.tma_b, fb, 0, kr, (n0 + 128 * rank) / 64, 0);
+          } else {
+            for (int i = 0; i < my_b; ++i)
+              tma_load_3d_pair(sb + i * MN_BOX_BYTES, &args.tma_b, fb, n0 + 128 * rank + 64 * i, kr, 0);
+          }
           if (++stage == PAIR_STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -763,21 +836,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
       const bool write = y0 < args.m_ext;
       const int nch = min(BN / 32, (args.n_ext - n0 + 31) / 32);
-      uint32_t r[32];
-      if (has_acc) tmem_ld32(tbase, r);
+      uint32_t ra[32], rb[32];
+      if (has_acc) {
+        tmem_ld32(tbase, ra);
+        if (nch > 1) tmem_ld32(tbase + 32, rb);
+      }
 #pragma unroll 1
-      for (int j = 0; j < nch; ++j) {
-        float v[32];
+      for (int j = 0; j < nch; j += 2) {
+        const bool two = j + 1 < nch;
+        float v0[32], v1[32];
         if (has_acc) {
-          tmem_ld_wait(r);
+          tmem_ld_wait(ra);
+          reg_fence(rb);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-          if (j + 1 < nch) tmem_ld32(tbase + 32 * (j + 1), r);
+          for (int i = 0; i < 32; ++i) {
+            v0[i] = __uint_as_float(ra[i]);
+            v1[i] = __uint_as_float(rb[i]);
+          }
+          if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), ra);
+          if (j + 3 < nch) tmem_ld32(tbase + 32 * (j + 3), rb);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+          for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
         }
-        if (write) ring_store(ring, v, true, &args.tma_out0, n0 + 32 * j, y0, e, row_local, issuer);
+        if (write)
+          ring_store_pair(ring, v0, v1, two, true, &args.tma_out2, n0 + 32 * j, y0, e, row_local,
+                          issuer);
       }
       tc_fence_before();
       __syncwarp();
@@ -834,7 +918,6 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
     case kFc2: return launch_mode<kFc2, 0>(args, grid, s);
     case kDgradDglu: return launch_act<kDgradDglu>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0>(args, grid, s);
-    case kWgrad: return launch_mode<kWgrad, 0>(args, grid, s);
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
     default: return cudaErrorInvalidValue;
   }

@@ -69,6 +69,7 @@ struct GemmArgs {
   CUtensorMap tma_b;
   CUtensorMap tma_out0;   // primary output, 32x32 boxes, 64-byte swizzle
   CUtensorMap tma_out1;   // GLU output A (FC1 mode only)
+  CUtensorMap tma_out2;   // primary output as [E][W/32][rows][32]: two-chunk boxes
   const int32_t* padded_offsets;
   const int32_t* counts;
   int* status;
@@ -97,6 +98,10 @@ struct GemmArgs {
   uint8_t* mx_st;
   float* mx_amax;
   long long mx_width;
+  // MN-major operands given as [E][atom][K][64] views (one TMA per stage
+  // fetches all atoms) instead of one 64x64 box per atom: 1 = yes.
+  int a_atoms4d;
+  int b_atoms4d;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);
