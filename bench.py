@@ -42,9 +42,17 @@ METRIC = "MoE expert-MLP fwd+bwd TFLOPS & tokens/s on 1 GB300; % of tensor-core 
 DEFAULT_WORKLOAD = "bf16_t4096_e64"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per launch from one ncu capture, with the hash of
-# the GEMM source the counters were taken on; a changed kernel reports null.
-NCU_TRAFFIC = {}
+# DRAM bytes (read + write) per launch from one ncu capture of the default
+# workload (profiles/grouped_gemm_bf16_t4096_e64.md), with the hash of the
+# GEMM sources the counters were taken on; a changed kernel reports null.
+_NCU_SRC = "dd05950cd75c1d2f"
+NCU_TRAFFIC = {
+    ("fc1_glu_fwd", "bf16_t4096_e64"): {"bytes": 785.678592e6 + 216.864768e6, "src": _NCU_SRC},
+    ("fc2_fwd", "bf16_t4096_e64"): {"bytes": 409.688064e6 + 101.865728e6, "src": _NCU_SRC},
+    ("fc2_dgrad_dglu", "bf16_t4096_e64"): {"bytes": 613.943040e6 + 134.005504e6, "src": _NCU_SRC},
+    ("fc2_wgrad", "bf16_t4096_e64"): {"bytes": 185.114112e6 + 313.563392e6, "src": _NCU_SRC},
+    ("fc1_wgrad", "bf16_t4096_e64"): {"bytes": 258.164736e6 + 682.315008e6, "src": _NCU_SRC},
+}
 
 
 def load_peaks():
@@ -59,7 +67,7 @@ def load_peaks():
 
 def gemm_source_hash():
     h = hashlib.sha256()
-    for fn in ("moe_gemm.cu", "moe_ptx.cuh", "moe_internal.h"):
+    for fn in ("moe_gemm.cu", "moe_ptx.cuh", "moe_internal.h", "moe_mx.cuh"):
         with open(os.path.join(ROOT, "moe_expert_mlp_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
