@@ -27,6 +27,7 @@ EXPORTS = (
     "moe_read_device_status", "moe_status_string", "moe_fc1_glu_fwd", "moe_fc2_fwd",
     "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
     "moe_route_permute_noalloc", "moe_quantize_mx", "moe_selftest_wait_timeout",
+    "moe_fc1_glu_fwd_unfused", "moe_fc2_dgrad_dglu_unfused",
 )
 
 
@@ -104,6 +105,8 @@ def lib():
             "moe_bias_grads": (ctypes.c_int, [D] + [P] * 7),
             "moe_route_permute_noalloc": (ctypes.c_int, [D] + [P] * 12 + [P]),
             "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
+            "moe_fc1_glu_fwd_unfused": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_dgrad_dglu_unfused": (ctypes.c_int, [D] + [P] * 8),
             "moe_quantize_mx": (ctypes.c_int, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                P, P, P]),
         }
@@ -264,3 +267,15 @@ def moe_route_permute_noalloc(desc, logits, bias, x, topk_idx, topk_w, counts, o
         ctypes.byref(desc), _p(logits), _p(bias), _p(x), _p(topk_idx), _p(topk_w), _p(counts),
         _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of), _p(x_perm),
         _stream(stream)))
+
+
+def moe_fc1_glu_fwd_unfused(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, stream=None):
+    _check(lib().moe_fc1_glu_fwd_unfused(ctypes.byref(desc), _p(x_perm), _p(counts),
+                                         _p(padded_offsets), _p(w1p), _p(b1p), _p(h), _p(a),
+                                         _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_unfused(desc, dy, h, counts, padded_offsets, w2, da, dh, stream=None):
+    _check(lib().moe_fc2_dgrad_dglu_unfused(ctypes.byref(desc), _p(dy), _p(h), _p(counts),
+                                            _p(padded_offsets), _p(w2), _p(da), _p(dh),
+                                            _stream(stream)))

@@ -576,6 +576,73 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
   return st;
 }
 
+moe_status_t moe_fc1_glu_fwd_unfused(const moe_mlp_desc_t* desc, const void* x_perm,
+                                     const int32_t* counts, const int32_t* padded_offsets,
+                                     const void* w1p, const void* b1p, void* h, void* a,
+                                     cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // plain grouped GEMM H = X W1p^T (+b1): the FC2-shaped kernel with W1p as B
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out2(&g.tma_out2, h, 2 * Fp, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(2 * Fp);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = 2 * Fp;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = 2 * Fp;
+  cudaError_t e = launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream);
+  if (e == cudaSuccess)
+    e = launch_glu_rows(h, counts, padded_offsets, desc->E, desc->F, static_cast<int>(Fp), a,
+                        desc->act, desc->alpha, desc->limit, desc->linear_offset,
+                        desc->out_scale, di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_fc2_dgrad_dglu_unfused(const moe_mlp_desc_t* desc, const void* dy,
+                                        const void* h, const int32_t* counts,
+                                        const int32_t* padded_offsets, const void* w2, void* da,
+                                        void* dh, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!dy || !h || !counts || !padded_offsets || !w2 || !da || !dh) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // plain grouped GEMM dA = dY W2: the FC1-dgrad-shaped kernel with W2 as B
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_out(&g.tma_out0, da, F, cap, 1) || !encode_out2(&g.tma_out2, da, F, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 4);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = da;
+  g.ld0 = F;
+  cudaError_t e = launch_grouped_gemm(kDgradFc1, g, grid_for(di, desc), stream);
+  if (e == cudaSuccess)
+    e = launch_dglu_rows(da, h, counts, padded_offsets, desc->E, desc->F, static_cast<int>(Fp),
+                         dh, desc->act, desc->alpha, desc->limit, desc->linear_offset,
+                         desc->out_scale, di->sms, stream);
+  return cuda_status(e);
+}
+
 moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
                              const int32_t* row_of, void* dx, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, true);

@@ -54,6 +54,14 @@ cudaError_t launch_group_colsum(const void* g, const int32_t* counts,
                                 const int32_t* padded_offsets, int E, int width, void* out,
                                 cudaStream_t s);
 
+cudaError_t launch_glu_rows(const void* h, const int32_t* counts, const int32_t* padded_offsets,
+                            int E, int F, int F_pad, void* a, int act, float alpha, float limit,
+                            float lin_off, float out_scale, int num_sms, cudaStream_t s);
+cudaError_t launch_dglu_rows(const void* da, const void* h, const int32_t* counts,
+                             const int32_t* padded_offsets, int E, int F, int F_pad, void* dh,
+                             int act, float alpha, float limit, float lin_off, float out_scale,
+                             int num_sms, cudaStream_t s);
+
 // ------------------------------------------------ grouped GEMM (tcgen05)
 enum GemmMode : int {
   kFc1Glu = 0,     // H = X W1p^T (+b1), A = GLU(H)             ragged M

@@ -137,6 +137,36 @@ class MoEExpertMLP:
             with self._t(timer, "bias_grads"):
                 L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2, stream)
 
+    # ---------------------------------------------------- unfused comparison
+    def mlp_forward_unfused(self, stream=None, timer=None):
+        """FC1 plain GEMM + separate GLU pass, then FC2 (the unfused path the
+        fused epilogue replaces)."""
+        c, po = self.counts, self.padded_offsets
+        with self._t(timer, "fc1_glu_fwd"):
+            L.moe_fc1_glu_fwd_unfused(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h,
+                                      self.a, stream)
+        with self._t(timer, "fc2_fwd"):
+            L.moe_fc2_fwd(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream)
+
+    def mlp_backward_unfused(self, stream=None, timer=None):
+        """FC2 dgrad plain GEMM + separate dGLU pass, then the rest as fused."""
+        if getattr(self, "da", None) is None:
+            self.da = torch.zeros((self.capacity, self.F), dtype=torch.bfloat16,
+                                  device=self.w2.device)
+        c, po = self.counts, self.padded_offsets
+        with self._t(timer, "fc2_dgrad_dglu"):
+            L.moe_fc2_dgrad_dglu_unfused(self.desc, self.dy, self.h, c, po, self.w2, self.da,
+                                         self.dh, stream)
+        with self._t(timer, "fc2_wgrad"):
+            L.moe_fc2_wgrad(self.desc, self.dy, self.a, c, po, self.dw2, stream)
+        with self._t(timer, "fc1_dgrad"):
+            L.moe_fc1_dgrad(self.desc, self.dh, c, po, self.w1p, self.dx_perm, stream)
+        with self._t(timer, "fc1_wgrad"):
+            L.moe_fc1_wgrad(self.desc, self.dh, self.x_perm, c, po, self.dw1p, stream)
+        if self.has_b1 or self.has_b2:
+            with self._t(timer, "bias_grads"):
+                L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2, stream)
+
     def forward(self, x, logits, bias=None, stream=None, timer=None):
         self.route(x, logits, bias, stream, timer)
         self.mlp_forward(stream, timer)
