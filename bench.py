@@ -504,11 +504,22 @@ def measure_fusion(torch, layer, K):
     f_unf = timed(layer.mlp_forward_unfused)
     b_fused = timed(layer.mlp_backward)
     b_unf = timed(layer.mlp_backward_unfused)
+    # activation recompute: the backward regenerates H in its workspace
+    from moe_expert_mlp_gb300 import _lib as L
+    desc_r = type(layer.desc).from_buffer_copy(layer.desc)
+    desc_r.recompute_h = 1
+    ws_r = torch.zeros(L.moe_workspace_size(desc_r), dtype=torch.uint8, device=layer.ws.device)
+    b_rec = timed(lambda: L.moe_mlp_bwd(
+        desc_r, layer.dy, layer.x_perm, None, layer.a, layer.counts, layer.padded_offsets,
+        layer.w1p, layer.w2, layer.dh, layer.dx_perm, layer.dw1p, layer.db1p, layer.dw2,
+        layer.db2, ws_r, b1p=layer.b1p))
+    del ws_r
     layer.mlp_forward()                      # leave the fused results in place
     layer.mlp_backward()
     return {"fwd_fused_ms": round(f_fused, 4), "fwd_unfused_ms": round(f_unf, 4),
             "fwd_speedup": round(f_unf / f_fused, 3), "bwd_fused_ms": round(b_fused, 4),
             "bwd_unfused_ms": round(b_unf, 4), "bwd_speedup": round(b_unf / b_fused, 3),
+            "bwd_recompute_h_ms": round(b_rec, 4),
             "unfused": "same grouped GEMMs with plain epilogues; GLU / dGLU as separate passes"}
 
 

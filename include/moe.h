@@ -104,6 +104,10 @@ typedef struct {
   int32_t sm_margin;    /* SMs left free for concurrent kernels ([FK] "From
                            kernel-level gains...": configurable margin) */
   int32_t capacity;     /* rows allocated in every per-row buffer */
+  int32_t recompute_h;  /* 1: the forward may skip storing H (h = NULL) and
+                           moe_mlp_bwd regenerates it in the workspace ([FK]
+                           "Next steps": activation recompute); the workspace
+                           then includes capacity*2*F_pad bf16 */
 } moe_mlp_desc_t;
 
 /* Optional MXFP8 and NVFP4-preparation outputs of a GEMM epilogue ([FK]
@@ -176,7 +180,8 @@ moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts
  *   x_perm [capacity,d]; counts [E]; padded_offsets [E+1];
  *   w1p [E,2F_pad,d]; b1p [E,2F_pad] or NULL; w2 [E,d,F]; b2 [E,d] or NULL.
  * Outputs: h [capacity,2F_pad] (FC1 output incl. bias, packed; saved for the
- * backward), a [capacity,F] (GLU output), y [capacity,d].  a_mx / y_mx
+ * backward; NULL = not stored, to be recomputed), a [capacity,F] (GLU
+ * output), y [capacity,d].  a_mx / y_mx
  * (NULL = none): MXFP8 / amax outputs of A (width F) and Y (width d).
  * Persistent tcgen05 kernels read the group sizes from device memory. */
 moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
@@ -238,6 +243,13 @@ moe_status_t moe_fc2_dgrad_dglu_unfused(const moe_mlp_desc_t* desc, const void* 
                                         const int32_t* padded_offsets, const void* w2, void* da,
                                         void* dh, cudaStream_t stream);
 
+/* Activation recompute ([FK] "Next steps" lists it): H = X W1p^T (+b1) as a
+ * plain grouped GEMM, the FC1 output the backward needs when the forward did
+ * not keep it.  h [capacity, 2F_pad] packed, padding rows zero. */
+moe_status_t moe_fc1_recompute_h(const moe_mlp_desc_t* desc, const void* x_perm,
+                                 const int32_t* counts, const int32_t* padded_offsets,
+                                 const void* w1p, const void* b1p, void* h, cudaStream_t stream);
+
 /* Weighted combine: out[t] = sum_s topk_w[t,s] * y[row_of[t,s]] (fp32 sum in
  * slot order, then bf16).  out [T,d]. */
 moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
@@ -259,13 +271,16 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
  * rows of dy^T a; FC1 dgrad dx_perm [capacity,d] = dh w1p; FC1 wgrad
  * dw1p [E,2F_pad,d] = dh^T x_perm (packed); db1p [E,2F_pad] and db2 [E,d]
  * (NULL when the bias is absent).  Experts with no rows get zero gradients.
- * dh_mx (NULL = none): MXFP8 / amax outputs of dH (width 2*F_pad, packed). */
+ * dh_mx (NULL = none): MXFP8 / amax outputs of dH (width 2*F_pad, packed).
+ * h = NULL: H is recomputed from x_perm, w1p and b1p (plain FC1 grouped GEMM
+ * + bias; b1p is used only then) into the workspace first; needs desc->recompute_h = 1 and a
+ * workspace of moe_workspace_size() bytes. */
 moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
                          const void* h, const void* a, const int32_t* counts,
-                         const int32_t* padded_offsets, const void* w1p, const void* w2,
-                         void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
-                         void* db2, const moe_mx_out_t* dh_mx, void* ws, size_t ws_bytes,
-                         cudaStream_t stream);
+                         const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                         const void* w2, void* dh, void* dx_perm, void* dw1p, void* db1p,
+                         void* dw2, void* db2, const moe_mx_out_t* dh_mx, void* ws,
+                         size_t ws_bytes, cudaStream_t stream);
 
 /* Backward of the permutation: dx[t] = sum_s dx_perm[row_of[t,s]] (fp32 in
  * slot order, then bf16).  dx [T,d]. */

@@ -27,7 +27,7 @@ EXPORTS = (
     "moe_read_device_status", "moe_status_string", "moe_fc1_glu_fwd", "moe_fc2_fwd",
     "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
     "moe_route_permute_noalloc", "moe_quantize_mx", "moe_selftest_wait_timeout",
-    "moe_fc1_glu_fwd_unfused", "moe_fc2_dgrad_dglu_unfused",
+    "moe_fc1_glu_fwd_unfused", "moe_fc2_dgrad_dglu_unfused", "moe_fc1_recompute_h",
 )
 
 
@@ -43,6 +43,7 @@ class moe_mlp_desc_t(ctypes.Structure):
         ("linear_offset", ctypes.c_float), ("out_scale", ctypes.c_float),
         ("has_b1", ctypes.c_int32), ("has_b2", ctypes.c_int32), ("align", ctypes.c_int32),
         ("sm_margin", ctypes.c_int32), ("capacity", ctypes.c_int32),
+        ("recompute_h", ctypes.c_int32),
     ]
 
 
@@ -61,12 +62,14 @@ def _mx(mx):
 
 
 def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_offset=0.0,
-              out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0, capacity=None):
+              out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0, capacity=None,
+              recompute_h=False):
     if capacity is None:
         capacity = T * k + E * 127
         capacity = (capacity + 127) // 128 * 128
     return moe_mlp_desc_t(T, E, k, d, F, MOE_DTYPE_BF16, ACTS[act], alpha, limit, linear_offset,
-                          out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity)
+                          out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity,
+                          int(recompute_h))
 
 
 _lib = None
@@ -91,7 +94,7 @@ def lib():
             "moe_mlp_fwd": (ctypes.c_int, [D] + [P] * 13 + [ctypes.c_size_t, P]),
             "moe_unpermute_combine": (ctypes.c_int, [D, P, P, P, P, P]),
             "moe_unpermute_combine_bwd": (ctypes.c_int, [D] + [P] * 8 + [P]),
-            "moe_mlp_bwd": (ctypes.c_int, [D] + [P] * 16 + [ctypes.c_size_t, P]),
+            "moe_mlp_bwd": (ctypes.c_int, [D] + [P] * 17 + [ctypes.c_size_t, P]),
             "moe_permute_bwd": (ctypes.c_int, [D, P, P, P, P]),
             "moe_route_bwd": (ctypes.c_int, [D, P, P, P, P, P]),
             "moe_read_device_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_int32), ctypes.c_int32]),
@@ -106,6 +109,7 @@ def lib():
             "moe_route_permute_noalloc": (ctypes.c_int, [D] + [P] * 12 + [P]),
             "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
             "moe_fc1_glu_fwd_unfused": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc1_recompute_h": (ctypes.c_int, [D] + [P] * 7),
             "moe_fc2_dgrad_dglu_unfused": (ctypes.c_int, [D] + [P] * 8),
             "moe_quantize_mx": (ctypes.c_int, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                P, P, P]),
@@ -191,11 +195,12 @@ def moe_unpermute_combine_bwd(desc, dout, y, row_of, topk_w, row_src, padded_off
 
 
 def moe_mlp_bwd(desc, dy, x_perm, h, a, counts, padded_offsets, w1p, w2, dh, dx_perm, dw1p, db1p,
-                dw2, db2, ws=None, stream=None, dh_mx=None):
+                dw2, db2, ws=None, stream=None, dh_mx=None, b1p=None):
     _check(lib().moe_mlp_bwd(
         ctypes.byref(desc), _p(dy), _p(x_perm), _p(h), _p(a), _p(counts), _p(padded_offsets),
-        _p(w1p), _p(w2), _p(dh), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2), _mx(dh_mx),
-        _p(ws), ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+        _p(w1p), _p(b1p), _p(w2), _p(dh), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2),
+        _mx(dh_mx), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        _stream(stream)))
 
 
 def moe_permute_bwd(desc, dx_perm, row_of, dx, stream=None):
@@ -279,3 +284,8 @@ def moe_fc2_dgrad_dglu_unfused(desc, dy, h, counts, padded_offsets, w2, da, dh, 
     _check(lib().moe_fc2_dgrad_dglu_unfused(ctypes.byref(desc), _p(dy), _p(h), _p(counts),
                                             _p(padded_offsets), _p(w2), _p(da), _p(dh),
                                             _stream(stream)))
+
+
+def moe_fc1_recompute_h(desc, x_perm, counts, padded_offsets, w1p, b1p, h, stream=None):
+    _check(lib().moe_fc1_recompute_h(ctypes.byref(desc), _p(x_perm), _p(counts),
+                                     _p(padded_offsets), _p(w1p), _p(b1p), _p(h), _stream(stream)))

@@ -231,6 +231,8 @@ moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   *bytes = route_ws_bytes(desc) + 256;
+  if (desc->recompute_h)
+    *bytes += static_cast<size_t>(desc->capacity) * 2 * fc1_pad(desc->F) * 2 + 256;
   return MOE_OK;
 }
 
@@ -316,7 +318,8 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                              const moe_mx_out_t* a_mx, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
-  if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !a) return MOE_ERR_NULL;
+  if (!h && !desc->recompute_h) return MOE_ERR_NULL;
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
@@ -326,7 +329,8 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
       !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
-      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out(&g.tma_out1, a, F, cap, 1))
+      (h && !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1)) ||
+      !encode_out(&g.tma_out1, a, F, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = static_cast<int>(2 * Fp);
@@ -550,18 +554,29 @@ moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const vo
 
 moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
                          const void* h, const void* a, const int32_t* counts,
-                         const int32_t* padded_offsets, const void* w1p, const void* w2,
-                         void* dh, void* dx_perm, void* dw1p, void* db1p, void* dw2,
-                         void* db2, const moe_mx_out_t* dh_mx, void* ws, size_t ws_bytes,
-                         cudaStream_t stream) {
-  (void)ws;
-  (void)ws_bytes;
+                         const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                         const void* w2, void* dh, void* dx_perm, void* dw1p, void* db1p,
+                         void* dw2, void* db2, const moe_mx_out_t* dh_mx, void* ws,
+                         size_t ws_bytes, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
-  if (!dy || !x_perm || !h || !a || !counts || !padded_offsets || !w1p || !w2 || !dh ||
+  if (!dy || !x_perm || !a || !counts || !padded_offsets || !w1p || !w2 || !dh ||
       !dx_perm || !dw1p || !dw2)
     return MOE_ERR_NULL;
   if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
+  if (!h) {
+    // activation recompute: regenerate H in the workspace
+    size_t need = 0;
+    if (!desc->recompute_h) return MOE_ERR_NULL;
+    if ((st = moe_workspace_size(desc, &need)) != MOE_OK) return st;
+    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+    const size_t off = (route_ws_bytes(desc) + 256 + 255) / 256 * 256;
+    void* h_ws = static_cast<uint8_t*>(ws) + off;
+    if ((st = moe_fc1_recompute_h(desc, x_perm, counts, padded_offsets, w1p, b1p, h_ws,
+                                  stream)) != MOE_OK)
+      return st;
+    h = h_ws;
+  }
   if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, dh_mx, stream)) !=
       MOE_OK)
     return st;
@@ -608,6 +623,33 @@ moe_status_t moe_fc1_glu_fwd_unfused(const moe_mlp_desc_t* desc, const void* x_p
                         desc->act, desc->alpha, desc->limit, desc->linear_offset,
                         desc->out_scale, di->sms, stream);
   return cuda_status(e);
+}
+
+moe_status_t moe_fc1_recompute_h(const moe_mlp_desc_t* desc, const void* x_perm,
+                                 const int32_t* counts, const int32_t* padded_offsets,
+                                 const void* w1p, const void* b1p, void* h, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !h) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  GemmArgs g;   // the FC2-shaped plain kernel with W1p as B
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out2(&g.tma_out2, h, 2 * Fp, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(2 * Fp);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = 2 * Fp;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = 2 * Fp;
+  return cuda_status(launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_dgrad_dglu_unfused(const moe_mlp_desc_t* desc, const void* dy,

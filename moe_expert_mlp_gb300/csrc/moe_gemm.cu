@@ -188,21 +188,27 @@ __device__ __forceinline__ void stage_box(uint32_t buf, const float (&v)[32], bo
   }
 }
 
+template <int NPAIRS>
 __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v0)[32],
                                                 const float (&v1)[32], bool two, bool live,
                                                 const CUtensorMap* map2, int c0, int y, int z,
                                                 int row, bool issuer) {
-  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;   // slot is 0 or 2
+  // Round r stages into pair r % NPAIRS.  With 3 pairs the issuer only waits
+  // (after issuing) for the store one round older, so a store overlaps the
+  // next round's staging; the pair a round writes was stored 3 rounds ago
+  // and that store was waited for before the previous round's barrier.
+  static_assert(NPAIRS == 3, "three slot pairs");
+  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;   // slot 0, 2 or 4
   stage_box(buf, v0, live, row);
   if (two) stage_box(buf + BOX_BYTES, v1, live, row);
   fence_proxy_async_smem();
-  if (issuer) bulk_wait_read<0>();
   named_bar_sync(kEpiBar, kEpiThreads);
   if (issuer) {
     tma_store_4d(map2, buf, 0, y, c0 / 32, z);
     bulk_commit();
+    bulk_wait_read<1>();
   }
-  ring.slot ^= 2;
+  ring.slot = ring.slot == 2 * (NPAIRS - 1) ? 0 : ring.slot + 2;
 }
 
 template <int MODE>
@@ -487,9 +493,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
               l[i] += bl[i];
             }
           }
-          ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
-          ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
-                     issuer);
+          if (args.out0 != nullptr) {           // H kept for the backward (else recomputed)
+            ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
+            ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
+                       issuer);
+          }
           const int f0 = ti.n0 / 2 + 32 * j;
           if (f0 < args.f_real) {
             float a[32];
@@ -608,9 +616,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
               for (int i = 0; i < 32; ++i) v1[i] += b[i];
             }
           }
-          if (write)
-            ring_store_pair(ring, v0, v1, two, Tr::kRaggedK || valid, &args.tma_out2, c0, y0,
-                            Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+          if (write) {
+            ring_store(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
+                       Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+            if (two)
+              ring_store(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32, y0,
+                         Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+          }
           if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the stored bf16 Y
 #pragma unroll
             for (int i = 0; i < 32; ++i) v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
@@ -650,8 +662,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
 constexpr int PAIR_STAGES = 5;
 constexpr int PAIR_HALF = 128 * BK * 2;               // 16 KB
 constexpr int PAIR_STAGE_BYTES = 2 * PAIR_HALF;       // A half + B half
+constexpr int kPairRing = 6;                          // three pairs of output boxes
 constexpr size_t PAIR_SMEM_BYTES =
-    1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES + kRing * BOX_BYTES;
+    1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES + kPairRing * BOX_BYTES;
 constexpr uint32_t kPairIdesc = idesc_bf16(256, BN, true, true);
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
@@ -860,8 +873,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
           for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
         }
         if (write)
-          ring_store_pair(ring, v0, v1, two, true, &args.tma_out2, n0 + 32 * j, y0, e, row_local,
-                          issuer);
+          ring_store_pair<3>(ring, v0, v1, two, true, &args.tma_out2, n0 + 32 * j, y0, e,
+                             row_local, issuer);
       }
       tc_fence_before();
       __syncwarp();

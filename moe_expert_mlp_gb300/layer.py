@@ -19,11 +19,14 @@ from . import _lib as L
 class MoEExpertMLP:
     def __init__(self, E, d, F, T=0, k=1, act="swiglu", alpha=1.0, limit=math.inf,
                  linear_offset=0.0, out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0,
-                 capacity=None, device="cuda"):
+                 capacity=None, device="cuda", recompute_h=False):
         self.desc = L.make_desc(T, E, k, d, F, act=act, alpha=alpha, limit=limit,
                                 linear_offset=linear_offset, out_scale=out_scale,
                                 has_b1=has_b1, has_b2=has_b2, sm_margin=sm_margin,
-                                capacity=capacity)
+                                capacity=capacity, recompute_h=recompute_h)
+        # recompute_h: the forward keeps no H; the backward regenerates it in
+        # the library workspace (activation recompute)
+        self.recompute_h = recompute_h
         self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
         self.Fp = L.moe_fc1_padded_width(F)
         self.has_b1, self.has_b2 = has_b1, has_b2
@@ -55,7 +58,7 @@ class MoEExpertMLP:
         self.row_of = z(max(T, 1), k, dtype=i32)
         # per-row activations and gradients (padded row layout)
         self.x_perm = z(cap, d)
-        self.h = z(cap, 2 * self.Fp)
+        self.h = None if recompute_h else z(cap, 2 * self.Fp)
         self.a = z(cap, F)
         self.y = z(cap, d)
         self.dy = z(cap, d)
@@ -124,6 +127,12 @@ class MoEExpertMLP:
 
     def mlp_backward(self, stream=None, timer=None, dh_mx=None):
         c, po = self.counts, self.padded_offsets
+        if self.recompute_h:
+            with self._t(timer, "mlp_bwd_recompute"):
+                L.moe_mlp_bwd(self.desc, self.dy, self.x_perm, None, self.a, c, po, self.w1p,
+                              self.w2, self.dh, self.dx_perm, self.dw1p, self.db1p, self.dw2,
+                              self.db2, self.ws, stream, dh_mx=dh_mx, b1p=self.b1p)
+            return
         with self._t(timer, "fc2_dgrad_dglu"):
             L.moe_fc2_dgrad_dglu(self.desc, self.dy, self.h, c, po, self.w2, self.dh, stream,
                                  mx=dh_mx)
