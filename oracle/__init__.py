@@ -27,3 +27,4 @@ differences, the MX format's own code table).  No function is unpinned.
 """
 from .moe_oracle import *  # noqa: F401,F403
 from .mx_oracle import *  # noqa: F401,F403
+from .mx_mlp_oracle import *  # noqa: F401,F403
