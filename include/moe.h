@@ -75,7 +75,13 @@ typedef enum {
 #define MOE_DEV_BAD_EXPERT  0x2   /* expert index outside [0,E) */
 #define MOE_DEV_TIMEOUT     0x4   /* an in-kernel wait ran past its limit */
 
-typedef enum { MOE_DTYPE_BF16 = 1 } moe_dtype_t;
+/* Operand type of the grouped GEMMs.  BF16: bf16 operands.  MXFP8: the
+ * *_mx calls, with E4M3 operands and one E8M0 scale per 32 elements along
+ * each GEMM's contraction dimension ([FK] "Reducing exposed memory overhead
+ * by fusing MXFP8 and NVFP4 quantization"); requires d and F multiples of 32
+ * and recompute_h = 0.  Routing, combine and their backward are bf16 in
+ * both. */
+typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2 } moe_dtype_t;
 
 /* GLU activations ([FK] "Overcoming training bottlenecks": SwiGLU, GeGLU,
  * sReLU with optional clamp and scaling).  With g the gate half, l the
@@ -92,7 +98,7 @@ typedef struct {
   int32_t k;            /* experts per token, 1..min(E,32) */
   int32_t d;            /* model width, multiple of 64 */
   int32_t F;            /* GLU half width, multiple of 32 */
-  int32_t dtype;        /* MOE_DTYPE_BF16 */
+  int32_t dtype;        /* moe_dtype_t */
   int32_t act;          /* moe_act_t */
   float alpha;          /* SwiGLU gate scale (1 = plain SiLU) */
   float limit;          /* clamp limit; +inf disables */
@@ -125,14 +131,50 @@ typedef struct {
  *   amax    float[2]: max|X| over real rows, and max|H16·s/4| over every
  *           16-row segment s of every column inside each group (the transposed
  *           16x16 Hadamard rotation; segments completed with zeros).  The
- *           call zeroes it first. */
+ *           call zeroes it first.
+ *   layout  where the scales go (moe_mx_layout_t).
+ * The same struct describes the MXFP8 inputs of the *_mx GEMM calls, which
+ * need the MOE_MX_SCALES_MMA layout. */
+typedef enum {
+  /* scale of row r, block j at r * (cols/32) + j */
+  MOE_MX_SCALES_ROWMAJOR = 0,
+  /* the layout the block-scaled tensor-core MMA reads: for a tensor of
+   * `rows` rows and `cols` columns (blocks along a row), atoms of 128 rows
+   * x 4 blocks, 512 bytes each; the scale of row r, block j is at byte
+   *   ((j/4)*RA + r/128)*512 + (r%32)*16 + ((r/32)%4)*4 + j%4,
+   * RA = 2*ceil(rows/256).  The buffer holds moe_mx_scale_bytes(rows, cols)
+   * bytes; entries past the tensor are read by the GEMMs but never written,
+   * so the buffer must be zeroed once when allocated.  For the transposed
+   * copy qt [width, capacity], rows = width and cols = capacity. */
+  MOE_MX_SCALES_MMA = 1
+} moe_mx_layout_t;
+
 typedef struct {
   uint8_t* q;
   uint8_t* scale;
   uint8_t* qt;
   uint8_t* scale_t;
   float* amax;
+  int32_t layout;
 } moe_mx_out_t;
+
+/* MXFP8 copies of the expert weights for the *_mx calls (each with its
+ * MOE_MX_SCALES_MMA scales, per expert moe_mx_scale_bytes(rows, cols) bytes
+ * where rows x cols is the per-expert code matrix):
+ *   w1  [E, 2F_pad, d]  packed FC1 weight, blocks along d     (FC1)
+ *   w1t [E, d, 2F_pad]  its transpose, blocks along 2F_pad   (FC1 dgrad)
+ *   w2  [E, d, F]       FC2 weight, blocks along F           (FC2)
+ *   w2t [E, F, d]       its transpose, blocks along d        (FC2 dgrad) */
+typedef struct {
+  uint8_t* w1;
+  uint8_t* w1_s;
+  uint8_t* w1t;
+  uint8_t* w1t_s;
+  uint8_t* w2;
+  uint8_t* w2_s;
+  uint8_t* w2t;
+  uint8_t* w2t_s;
+} moe_mx_weights_t;
 
 /* F_pad = F rounded up to 128 (packed FC1 width is 2*F_pad). */
 int32_t moe_fc1_padded_width(int32_t F);
@@ -304,6 +346,67 @@ moe_status_t moe_route_bwd(const moe_mlp_desc_t* desc, const float* dw, const fl
  * in and q 16-byte aligned. */
 moe_status_t moe_quantize_mx(const float* in, int32_t rows, int32_t cols, int32_t colwise,
                              uint8_t* q, uint8_t* scales, cudaStream_t stream);
+
+/* ------------------------------------------------------------- MXFP8 path
+ * [FK] "Reducing exposed memory overhead by fusing MXFP8 and NVFP4
+ * quantization": the MoE GEMMs read MXFP8 operands; the FC1 epilogue writes
+ * the activation both rowwise (next GEMM) and transposed (its weight
+ * gradient); the dSwiGLU epilogue does the same for dH.  Every GEMM operand
+ * is quantized along that GEMM's contraction dimension; weight gradients
+ * contract over an expert group's rows, in 32-row blocks from the group's
+ * start.  Accumulation is fp32; H, A, Y, dH, dX_perm and dW are stored bf16. */
+
+/* Bytes of a MOE_MX_SCALES_MMA scale buffer of a [rows, cols] tensor (0 for
+ * an empty one). */
+size_t moe_mx_scale_bytes(int64_t rows, int64_t cols);
+
+/* bf16 in [batch, rows, cols] -> MXFP8 (rows, cols multiples of 32): q
+ * [batch, rows, cols] with blocks along a row and/or qt [batch, cols, rows]
+ * with blocks down a column; scales in out->layout, per batch entry
+ * moe_mx_scale_bytes(rows, cols) resp. (cols, rows) bytes in the MMA layout.
+ * out->amax must be NULL.  Same quantizer as the fused epilogues. */
+moe_status_t moe_quantize_mx_bf16(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                                  const moe_mx_out_t* out, cudaStream_t stream);
+
+/* An activation [capacity, width] (x_perm or dY) in MXFP8, rowwise and/or
+ * transposed, MOE_MX_SCALES_MMA; only rows below padded_offsets[E] (read on
+ * the device) are converted. */
+moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                 const int32_t* padded_offsets, const moe_mx_out_t* out,
+                                 cudaStream_t stream);
+
+/* Weight preparation, once per optimizer step: w1p [E,2F_pad,d] and w2
+ * [E,d,F] (bf16) -> the four MXFP8 copies of moe_mx_weights_t. */
+moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p,
+                                     const void* w2, const moe_mx_weights_t* out,
+                                     cudaStream_t stream);
+
+/* MXFP8 forward (desc->dtype = MOE_DTYPE_MXFP8):
+ *   x_mx  x_perm rowwise (q, scale)                      [input]
+ *   h     H bf16 [capacity, 2F_pad] (kept for the dGLU)  [output]
+ *   a     A bf16 [capacity, F] or NULL to skip it        [output]
+ *   a_mx  A rowwise (q, scale: FC2's operand) and, when qt is given, the
+ *         transposed copy (qt, scale_t: FC2 weight gradient); amax optional
+ *   y     Y bf16 [capacity, d]
+ * Biases as in moe_mlp_fwd.  Same groups, padding and errors as moe_mlp_fwd. */
+moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,
+                            void* a, const moe_mx_out_t* a_mx, void* y, cudaStream_t stream);
+
+/* MXFP8 backward:
+ *   dy     dY bf16 [capacity, d] (bias gradient)   dy_mx  its rowwise and
+ *          transposed MXFP8 copies                  x_mx   x_perm transposed
+ *          (qt, scale_t)                            a_mx   A transposed
+ *   h      the forward's H;  dh: dH bf16 [capacity, 2F_pad] (output)
+ *   dh_mx  receives dH rowwise and transposed (q, scale, qt, scale_t)
+ *   dx_perm, dw1p, db1p, dw2, db2 as in moe_mlp_bwd (db1p / db2 NULL to skip). */
+moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
+                            const moe_mx_out_t* dy_mx, const moe_mx_out_t* x_mx, const void* h,
+                            const moe_mx_out_t* a_mx, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_mx_weights_t* w, void* dh,
+                            const moe_mx_out_t* dh_mx, void* dx_perm, void* dw1p, void* db1p,
+                            void* dw2, void* db2, cudaStream_t stream);
 
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed

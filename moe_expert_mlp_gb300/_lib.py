@@ -18,6 +18,9 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_DTYPE_BF16 = 1
+MOE_DTYPE_MXFP8 = 2
+MOE_MX_SCALES_ROWMAJOR = 0
+MOE_MX_SCALES_MMA = 1
 ACTS = {"swiglu": 0, "geglu": 1, "sreglu": 3}
 
 EXPORTS = (
@@ -28,6 +31,8 @@ EXPORTS = (
     "moe_fc2_dgrad_dglu", "moe_fc2_wgrad", "moe_fc1_dgrad", "moe_fc1_wgrad", "moe_bias_grads",
     "moe_route_permute_noalloc", "moe_quantize_mx", "moe_selftest_wait_timeout",
     "moe_fc1_glu_fwd_unfused", "moe_fc2_dgrad_dglu_unfused", "moe_fc1_recompute_h",
+    "moe_mx_scale_bytes", "moe_quantize_mx_bf16", "moe_quantize_act_mx",
+    "moe_quantize_weights_mx", "moe_mlp_fwd_mx", "moe_mlp_bwd_mx",
 )
 
 
@@ -49,25 +54,41 @@ class moe_mlp_desc_t(ctypes.Structure):
 
 class moe_mx_out_t(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("scale", ctypes.c_void_p), ("qt", ctypes.c_void_p),
-                ("scale_t", ctypes.c_void_p), ("amax", ctypes.c_void_p)]
+                ("scale_t", ctypes.c_void_p), ("amax", ctypes.c_void_p),
+                ("layout", ctypes.c_int32)]
+
+
+class moe_mx_weights_t(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("w1", "w1_s", "w1t", "w1t_s", "w2", "w2_s", "w2t", "w2t_s")]
 
 
 def _mx(mx):
-    """dict of optional tensors {q, scale, qt, scale_t, amax} -> struct pointer."""
+    """dict of optional tensors {q, scale, qt, scale_t, amax} (+ "layout":
+    "mma" for the MMA scale layout) -> struct pointer."""
     if mx is None:
         return None
     st = moe_mx_out_t(*[(_p(mx[k]).value if mx.get(k) is not None else None)
-                        for k in ("q", "scale", "qt", "scale_t", "amax")])
+                        for k in ("q", "scale", "qt", "scale_t", "amax")],
+                      MOE_MX_SCALES_MMA if mx.get("layout") == "mma" else MOE_MX_SCALES_ROWMAJOR)
+    return ctypes.byref(st)
+
+
+def _mxw(w):
+    """dict of the eight MXFP8 weight tensors -> moe_mx_weights_t pointer."""
+    st = moe_mx_weights_t(*[_p(w[k]).value for k in
+                            ("w1", "w1_s", "w1t", "w1t_s", "w2", "w2_s", "w2t", "w2t_s")])
     return ctypes.byref(st)
 
 
 def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_offset=0.0,
               out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0, capacity=None,
-              recompute_h=False):
+              recompute_h=False, dtype="bf16"):
     if capacity is None:
         capacity = T * k + E * 127
         capacity = (capacity + 127) // 128 * 128
-    return moe_mlp_desc_t(T, E, k, d, F, MOE_DTYPE_BF16, ACTS[act], alpha, limit, linear_offset,
+    dt = {"bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8}[dtype]
+    return moe_mlp_desc_t(T, E, k, d, F, dt, ACTS[act], alpha, limit, linear_offset,
                           out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity,
                           int(recompute_h))
 
@@ -113,6 +134,13 @@ def lib():
             "moe_fc2_dgrad_dglu_unfused": (ctypes.c_int, [D] + [P] * 8),
             "moe_quantize_mx": (ctypes.c_int, [P, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                                                P, P, P]),
+            "moe_mx_scale_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+            "moe_quantize_mx_bf16": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64,
+                                                    ctypes.c_int64, P, P]),
+            "moe_quantize_act_mx": (ctypes.c_int, [D, P, ctypes.c_int32, P, P, P]),
+            "moe_quantize_weights_mx": (ctypes.c_int, [D, P, P, P, P]),
+            "moe_mlp_fwd_mx": (ctypes.c_int, [D] + [P] * 11),
+            "moe_mlp_bwd_mx": (ctypes.c_int, [D] + [P] * 16),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -289,3 +317,37 @@ def moe_fc2_dgrad_dglu_unfused(desc, dy, h, counts, padded_offsets, w2, da, dh, 
 def moe_fc1_recompute_h(desc, x_perm, counts, padded_offsets, w1p, b1p, h, stream=None):
     _check(lib().moe_fc1_recompute_h(ctypes.byref(desc), _p(x_perm), _p(counts),
                                      _p(padded_offsets), _p(w1p), _p(b1p), _p(h), _stream(stream)))
+
+
+# ------------------------------------------------------------------ MXFP8
+def moe_mx_scale_bytes(rows, cols):
+    return int(lib().moe_mx_scale_bytes(rows, cols))
+
+
+def moe_quantize_mx_bf16(inp, batch, rows, cols, out, stream=None):
+    _check(lib().moe_quantize_mx_bf16(_p(inp), batch, rows, cols, _mx(out), _stream(stream)))
+
+
+def moe_quantize_act_mx(desc, inp, width, padded_offsets, out, stream=None):
+    _check(lib().moe_quantize_act_mx(ctypes.byref(desc), _p(inp), width, _p(padded_offsets),
+                                     _mx(out), _stream(stream)))
+
+
+def moe_quantize_weights_mx(desc, w1p, w2, out, stream=None):
+    _check(lib().moe_quantize_weights_mx(ctypes.byref(desc), _p(w1p), _p(w2), _mxw(out),
+                                         _stream(stream)))
+
+
+def moe_mlp_fwd_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, b2, h, a, a_mx, y,
+                   stream=None):
+    _check(lib().moe_mlp_fwd_mx(ctypes.byref(desc), _mx(x_mx), _p(counts), _p(padded_offsets),
+                                _mxw(w_mx), _p(b1p), _p(b2), _p(h), _p(a), _mx(a_mx), _p(y),
+                                _stream(stream)))
+
+
+def moe_mlp_bwd_mx(desc, dy, dy_mx, x_mx, h, a_mx, counts, padded_offsets, w_mx, dh, dh_mx,
+                   dx_perm, dw1p, db1p, dw2, db2, stream=None):
+    _check(lib().moe_mlp_bwd_mx(ctypes.byref(desc), _p(dy), _mx(dy_mx), _mx(x_mx), _p(h),
+                                _mx(a_mx), _p(counts), _p(padded_offsets), _mxw(w_mx), _p(dh),
+                                _mx(dh_mx), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2),
+                                _stream(stream)))

@@ -15,6 +15,7 @@
 #include <mutex>
 
 #include "moe_internal.h"
+#include "moe_mx.cuh"
 #include "moe_ptx.cuh"
 
 namespace moe {
@@ -85,14 +86,15 @@ moe_status_t device_info(DeviceInfo** out) {
 // of dims 1 and 2.  Out-of-range box elements read as zero.
 bool encode_map(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                 uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1,
-                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   if ((reinterpret_cast<uintptr_t>(base) & 15) || (row_bytes & 15) || (plane_bytes & 15))
     return false;
   cuuint64_t dims[3] = {d0, d1, d2};
   cuuint64_t strides[2] = {row_bytes, plane_bytes};
   cuuint32_t box[3] = {box0, box1, 1};
   cuuint32_t estride[3] = {1, 1, 1};
-  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims,
+  CUresult r = g_encode(map, dtype, 3, const_cast<void*>(base), dims,
                         strides, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -105,7 +107,7 @@ moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
   if (d->d < 64 || d->d % 64 != 0) return MOE_ERR_SHAPE;
   if (d->F < 32 || d->F % 32 != 0) return MOE_ERR_SHAPE;
   if (d->align != kAlign) return MOE_ERR_UNSUPPORTED;
-  if (d->dtype != MOE_DTYPE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8) return MOE_ERR_UNSUPPORTED;
   if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU)
     return MOE_ERR_UNSUPPORTED;
   if (d->capacity < kAlign || d->capacity % kAlign != 0) return MOE_ERR_SHAPE;
@@ -173,6 +175,9 @@ moe_status_t set_mx(GemmArgs& g, const moe_mx_out_t* mx, long long width, cudaSt
   if (!mx) return MOE_OK;
   if ((mx->q && !mx->scale) || (mx->qt && !mx->scale_t)) return MOE_ERR_NULL;
   if ((reinterpret_cast<uintptr_t>(mx->q) & 15) || width % 32 != 0) return MOE_ERR_SHAPE;
+  if (mx->layout != MOE_MX_SCALES_ROWMAJOR && mx->layout != MOE_MX_SCALES_MMA)
+    return MOE_ERR_UNSUPPORTED;
+  g.mx_mma_layout = mx->layout == MOE_MX_SCALES_MMA;
   g.mx_q = mx->q;
   g.mx_s = mx->scale;
   g.mx_qt = mx->qt;
@@ -726,6 +731,263 @@ moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear) {
     return MOE_ERR_CUDA;
   if (clear && cudaMemset(di->status, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
   *host_status = v;
+  return MOE_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// MXFP8 path: the same grouped-GEMM modes with E4M3 operands (K-major, the
+// transposed operands of the backward come from transposed MXFP8 copies) and
+// E8M0 scales in the MMA layout.
+namespace moe {
+namespace {
+
+long long sf_bytes(long long rows, long long cols) {
+  return (cols + 127) / 128 * sf_row_atoms(rows) * 512;
+}
+
+// MXFP8 tensor described by `m`: the rowwise and/or transposed parts the
+// caller needs, in the MMA layout, codes 16-byte aligned.
+bool mx_ok(const moe_mx_out_t* m, bool row, bool col) {
+  if (!m || m->layout != MOE_MX_SCALES_MMA) return false;
+  if (row && (!m->q || !m->scale || (reinterpret_cast<uintptr_t>(m->q) & 15))) return false;
+  if (col && (!m->qt || !m->scale_t || (reinterpret_cast<uintptr_t>(m->qt) & 15))) return false;
+  return true;
+}
+
+bool mx_weights_ok(const moe_mx_weights_t* w) {
+  return w && w->w1 && w->w1_s && w->w1t && w->w1t_s && w->w2 && w->w2_s && w->w2t && w->w2t_s;
+}
+
+// E4M3 operand [E][rows][K] (K contiguous), boxes of 128 K x box_rows rows.
+bool encode_u8(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint64_t E,
+               uint32_t box_rows) {
+  return encode_map(map, base, K, rows, E, K, rows * K, 128, box_rows,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_UINT8);
+}
+
+void set_scales(GemmArgs& g, const uint8_t* sfa, long long a_rows, const uint8_t* sfb,
+                long long b_rows, long long b_expert_bytes) {
+  g.sfa = sfa;
+  g.sfa_atoms = sf_row_atoms(a_rows);
+  g.sfb = sfb;
+  g.sfb_atoms = sf_row_atoms(b_rows);
+  g.sfb_expert_bytes = b_expert_bytes;
+}
+
+moe_status_t check_mx_desc(const moe_mlp_desc_t* d) {
+  moe_status_t st = check_desc(d, false);
+  if (st != MOE_OK) return st;
+  if (d->dtype != MOE_DTYPE_MXFP8 || d->recompute_h) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_mx_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return static_cast<size_t>(sf_bytes(rows, cols));
+}
+
+moe_status_t moe_quantize_mx_bf16(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                                  const moe_mx_out_t* out, cudaStream_t stream) {
+  if (!in || !out) return MOE_ERR_NULL;
+  if ((out->q && !out->scale) || (out->qt && !out->scale_t) || (!out->q && !out->qt))
+    return MOE_ERR_NULL;
+  if (out->amax) return MOE_ERR_UNSUPPORTED;
+  if (out->layout != MOE_MX_SCALES_ROWMAJOR && out->layout != MOE_MX_SCALES_MMA)
+    return MOE_ERR_UNSUPPORTED;
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 32 != 0 || cols % 32 != 0)
+    return MOE_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out->q) & 15) ||
+      (reinterpret_cast<uintptr_t>(out->qt) & 15))
+    return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_quant_bf16_mx(in, batch, rows, cols, out->q, out->scale, out->qt,
+                                          out->scale_t, out->layout == MOE_MX_SCALES_MMA,
+                                          nullptr, di->sms, stream));
+}
+
+moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                 const int32_t* padded_offsets, const moe_mx_out_t* out,
+                                 cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!in || !padded_offsets || !out) return MOE_ERR_NULL;
+  if ((out->q && !out->scale) || (out->qt && !out->scale_t) || (!out->q && !out->qt))
+    return MOE_ERR_NULL;
+  if (out->amax) return MOE_ERR_UNSUPPORTED;
+  if (out->layout != MOE_MX_SCALES_MMA) return MOE_ERR_UNSUPPORTED;
+  if (width < 32 || width % 32 != 0) return MOE_ERR_SHAPE;
+  if ((reinterpret_cast<uintptr_t>(in) & 15) || (reinterpret_cast<uintptr_t>(out->q) & 15) ||
+      (reinterpret_cast<uintptr_t>(out->qt) & 15))
+    return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_quant_bf16_mx(in, 1, desc->capacity, width, out->q, out->scale,
+                                          out->qt, out->scale_t, 1, padded_offsets + desc->E,
+                                          di->sms, stream));
+}
+
+moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p,
+                                     const void* w2, const moe_mx_weights_t* out,
+                                     cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!w1p || !w2 || !mx_weights_ok(out)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const long long E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  cudaError_t e = launch_quant_bf16_mx(w1p, E, 2 * Fp, d, out->w1, out->w1_s, out->w1t,
+                                       out->w1t_s, 1, nullptr, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_quant_bf16_mx(w2, E, d, F, out->w2, out->w2_s, out->w2t, out->w2t_s, 1, nullptr,
+                             di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,
+                            void* a, const moe_mx_out_t* a_mx, void* y, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h || !y) return MOE_ERR_NULL;
+  if ((desc->has_b1 && !b1p) || (desc->has_b2 && !b2)) return MOE_ERR_NULL;
+  if (!mx_ok(x_mx, true, false) || !mx_ok(a_mx, true, a_mx && a_mx->qt)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // FC1 + GLU: x_perm (codes [cap, d]) x W1p (codes [E, 2F_pad, d])
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w1, d, 2 * Fp, E, 256) ||
+      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) ||
+      (a && !encode_out(&g.tma_out1, a, F, cap, 1)))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(2 * Fp);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = 2 * Fp;
+  g.out1 = a;
+  g.ld1 = F;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = 2 * Fp;
+  set_scales(g, x_mx->scale, cap, w->w1_s, 2 * Fp, sf_bytes(2 * Fp, d));
+  if ((st = set_mx(g, a_mx, desc->F, stream)) != MOE_OK) return st;
+  cudaError_t e = launch_grouped_gemm_mx(kFc1Glu, g, grid_for(di, desc), stream);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // FC2: A (codes [cap, F]) x W2 (codes [E, d, F])
+  GemmArgs g2;
+  fill_common(g2, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g2.tma_a, a_mx->q, F, cap, 1, 128) ||
+      !encode_u8(&g2.tma_b, w->w2, F, d, E, 256) || !encode_out(&g2.tma_out0, y, d, cap, 1))
+    return MOE_ERR_SHAPE;
+  g2.K = desc->F;
+  g2.n_ext = desc->d;
+  g2.b_ext = desc->d;
+  g2.out0 = y;
+  g2.ld0 = d;
+  g2.bias = desc->has_b2 ? b2 : nullptr;
+  g2.bias_ld = d;
+  set_scales(g2, a_mx->scale, cap, w->w2_s, d, sf_bytes(d, F));
+  return cuda_status(launch_grouped_gemm_mx(kFc2, g2, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
+                            const moe_mx_out_t* dy_mx, const moe_mx_out_t* x_mx, const void* h,
+                            const moe_mx_out_t* a_mx, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_mx_weights_t* w, void* dh,
+                            const moe_mx_out_t* dh_mx, void* dx_perm, void* dw1p, void* db1p,
+                            void* dw2, void* db2, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dy || !h || !counts || !padded_offsets || !mx_weights_ok(w) || !dh || !dx_perm ||
+      !dw1p || !dw2)
+    return MOE_ERR_NULL;
+  if (!mx_ok(dy_mx, true, true) || !mx_ok(x_mx, false, true) || !mx_ok(a_mx, false, true) ||
+      !mx_ok(dh_mx, true, true))
+    return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  const int grid = grid_for(di, desc);
+  {  // FC2 dgrad + dGLU: dY (codes [cap, d]) x W2^T (codes [E, F, d]); dH from H
+    GemmArgs g;
+    fill_common(g, desc, di, counts, padded_offsets);
+    if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
+        !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) ||
+        !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
+      return MOE_ERR_SHAPE;
+    g.K = desc->d;
+    g.n_ext = static_cast<int>(Fp);
+    g.b_ext = desc->F;
+    g.out0 = dh;
+    g.ld0 = 2 * Fp;
+    g.aux = h;
+    g.ld_aux = 2 * Fp;
+    set_scales(g, dy_mx->scale, cap, w->w2t_s, F, sf_bytes(F, d));
+    if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
+    if (launch_grouped_gemm_mx(kDgradDglu, g, grid, stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  {  // FC2 wgrad: dW2[e] = dY^T A over the group's rows (codes [d, cap] and [F, cap])
+    GemmArgs g;
+    fill_common(g, desc, di, counts, padded_offsets);
+    if (!encode_u8(&g.tma_a, dy_mx->qt, cap, d, 1, 128) ||
+        !encode_u8(&g.tma_b, a_mx->qt, cap, F, 1, 256) ||
+        !encode_out(&g.tma_out0, dw2, F, d, E))
+      return MOE_ERR_SHAPE;
+    g.m_ext = desc->d;
+    g.n_ext = desc->F;
+    g.b_ext = desc->F;
+    g.out0 = dw2;
+    g.ld0 = F;
+    set_scales(g, dy_mx->scale_t, d, a_mx->scale_t, F, 0);
+    if (launch_grouped_gemm_mx(kWgrad, g, grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  {  // FC1 dgrad: dH (codes [cap, 2F_pad]) x W1p^T (codes [E, d, 2F_pad])
+    GemmArgs g;
+    fill_common(g, desc, di, counts, padded_offsets);
+    if (!encode_u8(&g.tma_a, dh_mx->q, 2 * Fp, cap, 1, 128) ||
+        !encode_u8(&g.tma_b, w->w1t, 2 * Fp, d, E, 256) ||
+        !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
+      return MOE_ERR_SHAPE;
+    g.K = static_cast<int>(2 * Fp);
+    g.n_ext = desc->d;
+    g.b_ext = desc->d;
+    g.out0 = dx_perm;
+    g.ld0 = d;
+    set_scales(g, dh_mx->scale, cap, w->w1t_s, d, sf_bytes(d, 2 * Fp));
+    if (launch_grouped_gemm_mx(kDgradFc1, g, grid, stream) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  {  // FC1 wgrad: dW1p[e] = dH^T X over the group's rows (codes [2F_pad, cap], [d, cap])
+    GemmArgs g;
+    fill_common(g, desc, di, counts, padded_offsets);
+    if (!encode_u8(&g.tma_a, dh_mx->qt, cap, 2 * Fp, 1, 128) ||
+        !encode_u8(&g.tma_b, x_mx->qt, cap, d, 1, 256) ||
+        !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
+      return MOE_ERR_SHAPE;
+    g.m_ext = static_cast<int>(2 * Fp);
+    g.n_ext = desc->d;
+    g.b_ext = desc->d;
+    g.out0 = dw1p;
+    g.ld0 = d;
+    set_scales(g, dh_mx->scale_t, 2 * Fp, x_mx->scale_t, d, 0);
+    if (launch_grouped_gemm_mx(kWgrad, g, grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (db1p || db2) return moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream);
   return MOE_OK;
 }
 

@@ -55,13 +55,27 @@ constexpr int kEpiThreads = 128;             // 4 epilogue warps
 constexpr int kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr size_t SMEM_BYTES =
     1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + kRing * BOX_BYTES;
+// MXFP8 operands: the same 128-byte rows hold 128 E4M3 values, so a stage
+// covers K = 128; its scales (A: one 512-byte atom, B: two) follow the
+// operand stages, and the output ring shrinks to 3 boxes to make room.
+constexpr int BK_MX = 128;
+constexpr int SF_STAGE_BYTES = 1536;
+constexpr int kRingMx = 3;
+constexpr size_t SMEM_BYTES_MX = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTES +
+                                 static_cast<size_t>(STAGES) * SF_STAGE_BYTES +
+                                 kRingMx * BOX_BYTES;
+// TMEM columns (from the start of the accumulator NOT in use by the current
+// tile) that receive one stage's scales: A at +0 (4 columns), B at +32 (8),
+// both 32-column aligned.  The epilogue releases them once it has read the
+// accumulator's first 64 columns.
+constexpr uint32_t kSfaCol = 0, kSfbCol = 32;
 
 struct Tile {
   int e;        // expert
   int m0;       // first output row (ragged M: routed row; ragged K: weight row)
   int n0;       // first output column
   int k_row0;   // ragged K: first routed row of the group
-  int num_kb;   // K blocks of 64
+  int num_kb;   // K blocks (64 bf16 or 128 E4M3 per block)
 };
 
 struct ActP {
@@ -139,6 +153,7 @@ struct StoreRing {
   int slot;
 };
 
+template <int NR>
 __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32], bool live,
                                            const CUtensorMap* map, int x, int y, int z,
                                            int row, bool issuer) {
@@ -161,9 +176,9 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
   if (issuer) {
     tma_store_3d(map, buf, x, y, z);
     bulk_commit();
-    bulk_wait_read<kRing - 2>();
+    bulk_wait_read<NR - 2>();
   }
-  ring.slot = ring.slot == kRing - 1 ? 0 : ring.slot + 1;
+  ring.slot = ring.slot == NR - 1 ? 0 : ring.slot + 1;
 }
 
 // Two adjacent 32-column chunks per round, one TMA store for both.  Rounds
@@ -211,19 +226,24 @@ __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v
   ring.slot = ring.slot == 2 * (NPAIRS - 1) ? 0 : ring.slot + 2;
 }
 
-template <int MODE>
+// bf16: the backward reads transposed operands MN-major from the forward's
+// buffers.  MXFP8: every operand is K-major (the transposed copies are
+// quantized along the contraction dimension).
+template <int MODE, bool MX>
 struct Traits {
   static constexpr bool kRaggedK = (MODE == kWgrad);
-  static constexpr bool kAmn = (MODE == kWgrad);
-  static constexpr bool kBmn = (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad);
+  static constexpr bool kAmn = !MX && (MODE == kWgrad);
+  static constexpr bool kBmn = !MX && (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad);
   static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
+  static constexpr int kBK = MX ? BK_MX : BK;
+  static constexpr int kNR = MX ? kRingMx : kRing;
 };
 
-template <int MODE>
+template <int MODE, int KB>
 __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, const int* s_off,
                                             const int* s_cnt, const int* s_order, int E) {
   Tile ti;
-  if (Traits<MODE>::kRaggedK) {
+  if (MODE == kWgrad) {
     const int per_e = m_tiles * n_tiles;
     const int slot = t / per_e;
     const int rem = t - slot * per_e;
@@ -233,7 +253,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
     ti.m0 = mb * BM;
     ti.n0 = nb * BN;
     ti.k_row0 = s_off[ti.e];
-    ti.num_kb = (s_cnt[ti.e] + BK - 1) / BK;
+    ti.num_kb = (s_cnt[ti.e] + KB - 1) / KB;
   } else {
     const int mb = t / n_tiles;
     const int nb = t - mb * n_tiles;
@@ -253,14 +273,15 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
   return ti;
 }
 
-template <int MODE, int ACT>
+template <int MODE, int ACT, bool MX>
 __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
-  using Tr = Traits<MODE>;
+  using Tr = Traits<MODE, MX>;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ __align__(8) uint64_t empty_bar[STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t tearly_bar[2];   // MX: first chunk of an accumulator read
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
   __shared__ int s_total;
@@ -284,6 +305,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
       mbar_init(&tempty_bar[a], 4);
+      mbar_init(&tearly_bar[a], 4);
     }
     fence_mbar_init();
   }
@@ -325,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int total = s_total;
-  const int kb_fixed = Tr::kRaggedK ? 0 : (args.K + BK - 1) / BK;
+  const int kb_fixed = Tr::kRaggedK ? 0 : (args.K + Tr::kBK - 1) / Tr::kBK;
   volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
@@ -336,7 +358,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       uint32_t stage = 0, phase = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-        Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+        Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
         const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
         // boxes that hold at least one in-range column (skip fully-outside boxes)
         const int b_boxes = Tr::kBmn ? (args.b_atoms4d ? 4 : min(4, (args.b_ext - ti.n0 + 63) / 64)) : 1;
@@ -351,6 +373,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           uint8_t* sa = smem + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           uint64_t* fb = &full_bar[stage];
+          if constexpr (MX) {
+            // E4M3 tiles (K-major, 128 K per row) and their scale atoms
+            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SF_STAGE_BYTES);
+            const int kx = (Tr::kRaggedK ? ti.k_row0 : 0) + kb * BK_MX;
+            const long long kt = kx / BK_MX;
+            uint8_t* ssf = smem + STAGES * STAGE_BYTES + stage * SF_STAGE_BYTES;
+            tma_load_3d(sa, &args.tma_a, fb, kx, ti.m0, 0);
+            tma_load_3d(sb, &args.tma_b, fb, kx, ti.n0, Tr::kRaggedK ? 0 : ti.e);
+            bulk_load(ssf, args.sfa + (kt * args.sfa_atoms + (ti.m0 >> 7)) * 512, 512, fb);
+            bulk_load(ssf + 512,
+                      args.sfb + (Tr::kRaggedK ? 0 : ti.e * args.sfb_expert_bytes) +
+                          (kt * args.sfb_atoms + (ti.n0 >> 7)) * 512,
+                      1024, fb);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           mbar_arrive_expect_tx(fb, tx);
           const int kk = kb * BK;
           // ---- A operand
@@ -387,13 +428,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       int it = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
-        Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+        Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
         const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
         const int acc = it & 1;
         const uint32_t acc_par = (it >> 1) & 1;
         if (!mbar_wait(&tempty_bar[acc], acc_par ^ 1u, args.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        // MX: this tile's scales go to the first columns of the other
+        // accumulator, which the previous tile's epilogue must have read.
+        const uint32_t sf_tmem = tmem_base + (acc ^ 1) * BN;
+        if constexpr (MX) {
+          if (it > 0) {
+            if (!mbar_wait(&tearly_bar[acc ^ 1], ((it - 1) >> 1) & 1, args.status, abort_flag))
+              break;
+            tc_fence_after();
+          }
+        }
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&full_bar[stage], phase, args.status, abort_flag)) {
             ok = false;
@@ -402,6 +453,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_BYTES;
+          if constexpr (MX) {
+            // scales smem -> TMEM, then 4 MMAs of K = 32 (32 bytes apart in
+            // the swizzled rows); MMA k takes byte k of each scale column.
+            // tcgen05.cp and tcgen05.mma from this thread run in issue order.
+            const uint32_t sf = smem_u32(smem + STAGES * STAGE_BYTES + stage * SF_STAGE_BYTES);
+            tmem_cp_32x128_x4(sf_tmem + kSfaCol, sdesc_noswz(sf, 128, 128));
+            tmem_cp_32x128_x4(sf_tmem + kSfbCol, sdesc_noswz(sf + 512, 128, 128));
+            tmem_cp_32x128_x4(sf_tmem + kSfbCol + 4, sdesc_noswz(sf + 1024, 128, 128));
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              umma_mx(d_tmem, sdesc_sw128(a_base + k * 32, 16, 1024),
+                      sdesc_sw128(b_base + k * 32, 16, 1024), idesc_mx(BM, BN, k, k),
+                      sf_tmem + kSfaCol, sf_tmem + kSfbCol, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
             // K-major: +32 B per K=16 step inside the 128-B swizzle row.
@@ -427,14 +498,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
-    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES), 0};
+    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES + (MX ? STAGES * SF_STAGE_BYTES : 0)), 0};
     const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
     const MxOut mx{args.mx_q, args.mx_s, args.mx_qt, args.mx_st, args.mx_amax, args.mx_width,
-                   args.capacity};
+                   args.capacity, args.mx_mma_layout};
+    // MX: tell the MMA warp that the accumulator's first 64 columns have
+    // been read (the next tile stages its scales there).  Once per tile.
+    auto early_release = [&](int acc_id) {
+      if constexpr (MX) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tearly_bar[acc_id]);
+      }
+    };
     const bool want_mx = mx.q != nullptr || mx.qt != nullptr || mx.amax != nullptr;
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-      Tile ti = decode_tile<MODE>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
+      Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
       const int acc = it & 1;
       const uint32_t acc_par = (it >> 1) & 1;
       const long long gr = ti.m0 + row_local;
@@ -473,6 +553,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         for (int j = 0; j < kGluHalf / 32; ++j) {
           tmem_ld_wait(rg);
           reg_fence(rl);
+          if (j == 1) early_release(acc);             // columns 0-63 read
           float g[32], l[32];
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -494,8 +575,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
             }
           }
           if (args.out0 != nullptr) {           // H kept for the backward (else recomputed)
-            ring_store(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
-            ring_store(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
+            ring_store<Tr::kNR>(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
+            ring_store<Tr::kNR>(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
                        issuer);
           }
           const int f0 = ti.n0 / 2 + 32 * j;
@@ -503,7 +584,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
             float a[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
-            ring_store(ring, a, valid, &args.tma_out1, f0, y0, 0, row_local, issuer);
+            if (args.out1 != nullptr)
+              ring_store<Tr::kNR>(ring, a, valid, &args.tma_out1, f0, y0, 0, row_local, issuer);
             if (want_mx) {                      // MXFP8 / amax of the stored bf16 A
 #pragma unroll
               for (int i = 0; i < 32; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
@@ -536,8 +618,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           tmem_ld32(tbase + 32 * (j + 1), r);
           const bool live0 = valid && f0 < args.f_real;
           if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
-          ring_store(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
-          ring_store(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local, issuer);
+          ring_store<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
+          ring_store<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local, issuer);
           if (want_mx) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -553,13 +635,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
             load_raw64(Hrow + c2 + kGluHalf, hl[0]);
           }
           tmem_ld_wait(r);
+          if (j == 0) early_release(acc);             // columns 0-63 read
 #pragma unroll
           for (int i = 0; i < 32; ++i) ra[i] = r[i];
           if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
           const bool live1 = valid && f1 < args.f_real;
           if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
-          ring_store(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
-          ring_store(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local, issuer);
+          ring_store<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
+          ring_store<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local, issuer);
           if (want_mx) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
@@ -585,6 +668,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         if (has_acc) {
           tmem_ld32(tbase, ra);
           if (nch > 1) tmem_ld32(tbase + 32, rb);
+        } else {
+          early_release(acc);
         }
 #pragma unroll 1
         for (int j = 0; j < nch; j += 2) {
@@ -594,6 +679,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (has_acc) {
             tmem_ld_wait(ra);
             reg_fence(rb);
+            if (j == 0) early_release(acc);           // columns 0-63 read (or all there are)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               v0[i] = __uint_as_float(ra[i]);
@@ -617,10 +703,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
             }
           }
           if (write) {
-            ring_store(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
+            ring_store<Tr::kNR>(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
                        Tr::kRaggedK ? ti.e : 0, row_local, issuer);
             if (two)
-              ring_store(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32, y0,
+              ring_store<Tr::kNR>(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32, y0,
                          Tr::kRaggedK ? ti.e : 0, row_local, issuer);
           }
           if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the stored bf16 Y
@@ -901,22 +987,23 @@ cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int MODE, int ACT>
+template <int MODE, int ACT, bool MX>
 cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT>,
+  constexpr size_t smem = MX ? SMEM_BYTES_MX : SMEM_BYTES;
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT, MX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(SMEM_BYTES));
+                                         static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<MODE, ACT><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(args);
+  k_grouped_gemm<MODE, ACT, MX><<<grid, NUM_THREADS, smem, s>>>(args);
   return cudaGetLastError();
 }
 
-template <int MODE>
+template <int MODE, bool MX>
 cudaError_t launch_act(const GemmArgs& args, int grid, cudaStream_t s) {
   switch (args.act) {
-    case MOE_ACT_SWIGLU: return launch_mode<MODE, MOE_ACT_SWIGLU>(args, grid, s);
-    case MOE_ACT_GEGLU: return launch_mode<MODE, MOE_ACT_GEGLU>(args, grid, s);
-    case MOE_ACT_SREGLU: return launch_mode<MODE, MOE_ACT_SREGLU>(args, grid, s);
+    case MOE_ACT_SWIGLU: return launch_mode<MODE, MOE_ACT_SWIGLU, MX>(args, grid, s);
+    case MOE_ACT_GEGLU: return launch_mode<MODE, MOE_ACT_GEGLU, MX>(args, grid, s);
+    case MOE_ACT_SREGLU: return launch_mode<MODE, MOE_ACT_SREGLU, MX>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -927,11 +1014,22 @@ size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
   switch (mode) {
-    case kFc1Glu: return launch_act<kFc1Glu>(args, grid, s);
-    case kFc2: return launch_mode<kFc2, 0>(args, grid, s);
-    case kDgradDglu: return launch_act<kDgradDglu>(args, grid, s);
-    case kDgradFc1: return launch_mode<kDgradFc1, 0>(args, grid, s);
+    case kFc1Glu: return launch_act<kFc1Glu, false>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0, false>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu, false>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0, false>(args, grid, s);
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
+  switch (mode) {
+    case kFc1Glu: return launch_act<kFc1Glu, true>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0, true>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu, true>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0, true>(args, grid, s);
+    case kWgrad: return launch_mode<kWgrad, 0, true>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

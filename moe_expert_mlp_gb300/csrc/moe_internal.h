@@ -110,9 +110,25 @@ struct GemmArgs {
   // fetches all atoms) instead of one 64x64 box per atom: 1 = yes.
   int a_atoms4d;
   int b_atoms4d;
+  int mx_mma_layout;      // epilogue MX scales in the MMA layout
+  // MXFP8 operands (launch_grouped_gemm_mx): E4M3 codes through tma_a /
+  // tma_b (K-major, 128-element boxes), scales in the MMA layout.  A's scale
+  // tensor has sfa_atoms row groups; B's has sfb_atoms, and sfb_expert_bytes
+  // between experts (ragged-M modes; 0 for weight gradients).
+  const uint8_t* sfa;
+  const uint8_t* sfb;
+  long long sfa_atoms;
+  long long sfb_atoms;
+  long long sfb_expert_bytes;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);
+// The same modes with block-scaled MXFP8 operands (kWgrad: 1-CTA tiles).
+cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cudaStream_t s);
+cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows, long long cols,
+                                 uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
+                                 int mma_layout, const int32_t* row_limit, int num_sms,
+                                 cudaStream_t stream);
 size_t grouped_gemm_smem_bytes();
 
 }  // namespace moe

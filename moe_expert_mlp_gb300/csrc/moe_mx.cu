@@ -2,10 +2,12 @@
 // using the same device quantizer as the fused GEMM epilogues.  It exists so
 // that codes and scales can be checked bit for bit against the oracle on
 // identical fp32 inputs.
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "moe_internal.h"
 #include "moe_mx.cuh"
+#include "moe_ptx.cuh"
 
 namespace moe {
 namespace {
@@ -50,7 +52,56 @@ __global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in
   }
 }
 
+// bf16 [batch][rows][cols] -> MXFP8, one warp per 32 x 32 block (lane =
+// row), consecutive warps on consecutive column blocks of the same rows.
+// Rowwise codes [batch][rows][cols]; columnwise codes written transposed
+// [batch][cols][rows]; scales row-major or in the MMA layout.
+__global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restrict__ in,
+                                                    long long batch, long long rows,
+                                                    long long cols, uint8_t* q, uint8_t* s,
+                                                    uint8_t* qt, uint8_t* st, int mma_layout,
+                                                    const int32_t* row_limit) {
+  const int lane = threadIdx.x & 31;
+  const long long rbn = rows / 32, cbn = cols / 32;
+  const long long per_batch = rbn * cbn;
+  const long long nblk = batch * per_batch;
+  const long long s_bytes = mma_layout ? (cols + 127) / 128 * sf_row_atoms(rows) * 512
+                                       : rows * cols / 32;
+  const long long st_bytes = mma_layout ? (rows + 127) / 128 * sf_row_atoms(cols) * 512
+                                        : rows * cols / 32;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
+  const long long rlim = row_limit ? __ldg(row_limit) : rows;   // rows past it are skipped
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x / 32) + threadIdx.x / 32;
+       w < nblk; w += warps) {
+    const long long b = w / per_batch;
+    const long long rem = w - b * per_batch;
+    const long long rb = rem / cbn, cb = rem - rb * cbn;
+    if (rb * 32 >= rlim) continue;
+    float v[32];
+    load_bf16x32(in + (b * rows + rb * 32 + lane) * cols + cb * 32, v);
+    const MxOut mx{q ? q + b * rows * cols : nullptr, s ? s + b * s_bytes : nullptr,
+                   qt ? qt + b * rows * cols : nullptr, st ? st + b * st_bytes : nullptr,
+                   nullptr, cols, rows, mma_layout};
+    mx_epilogue_block(mx, v, rb * 32, static_cast<int>(cb * 32), lane);
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows, long long cols,
+                                 uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
+                                 int mma_layout, const int32_t* row_limit, int num_sms,
+                                 cudaStream_t stream) {
+  const long long nblk = batch * (rows / 32) * (cols / 32);
+  if (nblk == 0) return cudaSuccess;
+  long long grid = (nblk + 7) / 8;
+  if (grid > static_cast<long long>(num_sms) * 16) grid = static_cast<long long>(num_sms) * 16;
+  k_quant_bf16<<<static_cast<int>(grid), 256, 0, stream>>>(
+      static_cast<const __nv_bfloat16*>(in), batch, rows, cols, q, s, qt, st, mma_layout,
+      row_limit);
+  return cudaGetLastError();
+}
+
 }  // namespace moe
 
 extern "C" moe_status_t moe_quantize_mx(const float* in, int32_t rows, int32_t cols,

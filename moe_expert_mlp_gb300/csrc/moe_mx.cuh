@@ -73,15 +73,31 @@ __device__ __forceinline__ void atomic_max_nonneg(float* addr, float v) {
   atomicMax(reinterpret_cast<unsigned int*>(addr), __float_as_uint(v));
 }
 
+// Byte offset of the scale of row r, K block j (32 elements) in the layout
+// the block-scaled MMA consumes: atoms of 128 rows x 4 K blocks (512 bytes,
+// row r at (r % 32) * 16 + ((r / 32) % 4) * 4 + j % 4), atoms ordered by K
+// group (j / 4) and then by row group (r / 128); `row_atoms` is the number
+// of row groups, rounded up to even so that a 256-row operand tile reads
+// two adjacent atoms.
+__host__ __device__ __forceinline__ long long sf_mma_offset(long long r, long long j,
+                                                            long long row_atoms) {
+  return ((j >> 2) * row_atoms + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
+}
+
+__host__ __device__ __forceinline__ long long sf_row_atoms(long long rows) {
+  return 2 * ((rows + 255) / 256);
+}
+
 // Optional MXFP8 / amax outputs of a GEMM epilogue (all-null = none).
 struct MxOut {
   uint8_t* q;        // rowwise codes [cap, width]
-  uint8_t* s;        // rowwise scales [cap, width/32]
+  uint8_t* s;        // rowwise scales [cap, width/32] or MMA layout
   uint8_t* qt;       // columnwise codes, transposed [width, cap]
-  uint8_t* st;       // columnwise scales [width, cap/32]
+  uint8_t* st;       // columnwise scales [width, cap/32] or MMA layout
   float* amax;       // [2]: max |x|, max |H16 x^T / 4|
   long long width;
   long long cap;
+  int mma_layout;    // scales in the block-scaled MMA layout (sf_mma_offset)
 };
 
 // One warp holds a 32 x 32 block: lane l owns row r0 + l, columns
@@ -94,7 +110,8 @@ __device__ __forceinline__ void mx_epilogue_block(const MxOut& mx, const float (
   const long long row = r0 + lane;
   if (mx.q) {
     const uint8_t sc = mx_quant32(v, mx.q + row * mx.width + col0);
-    mx.s[row * (mx.width / 32) + col0 / 32] = sc;
+    mx.s[mx.mma_layout ? sf_mma_offset(row, col0 / 32, sf_row_atoms(mx.cap))
+                       : row * (mx.width / 32) + col0 / 32] = sc;
   }
   if (mx.qt) {
     uint8_t my_sc = 0;
@@ -108,7 +125,9 @@ __device__ __forceinline__ void mx_epilogue_block(const MxOut& mx, const float (
       mx.qt[static_cast<long long>(col0 + i) * mx.cap + row] = static_cast<uint8_t>(code);
       if (lane == i) my_sc = static_cast<uint8_t>(sx + 127);
     }
-    mx.st[static_cast<long long>(col0 + lane) * (mx.cap / 32) + r0 / 32] = my_sc;
+    const long long c = col0 + lane;
+    mx.st[mx.mma_layout ? sf_mma_offset(c, r0 / 32, sf_row_atoms(mx.width))
+                        : c * (mx.cap / 32) + r0 / 32] = my_sc;
   }
   if (mx.amax) {
     float m = 0.0f, h = 0.0f;

@@ -241,6 +241,65 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// ------------------------------------------ MXFP8 block-scaled MMA
+// Shared-memory descriptor of an unswizzled K-major matrix (layout code 0):
+// 8-row core matrices of 16-byte rows; lbo / sbo are the strides between
+// core matrices along K and along M/N.
+__device__ __forceinline__ uint64_t sdesc_noswz(uint32_t saddr, uint32_t lbo_bytes,
+                                                uint32_t sbo_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  return d;
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with E4M3 A/B (K-major), fp32
+// accumulate and UE8M0 scales (bit 23).  a_sf / b_sf pick the byte of each
+// 32-bit scale column that holds this MMA's 32-element K block.
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int a_sf, int b_sf) {
+  return (static_cast<uint32_t>(b_sf) << 4)            // B scale byte
+         | (static_cast<uint32_t>(N >> 3) << 17)       // A/B format 0 = E4M3
+         | (1u << 23)                                  // scale type UE8M0
+         | (static_cast<uint32_t>(M >> 4) << 24)
+         | (static_cast<uint32_t>(a_sf) << 29);        // A scale byte
+}
+
+// D[tmem] (+)= (A * sA)[smem] * (B * sB)[smem]^T, one K=32 step; the
+// scales sit in TMEM: scale of row r at lane r % 32 (every lane quadrant),
+// column (r / 32) from the given address, byte chosen by the descriptor.
+__device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                        uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Shared memory -> TMEM: 32 rows x 16 bytes, written to the same 32 lanes
+// of every lane quadrant, 4 columns wide.  Executes in issue order with
+// this thread's tcgen05.mma.
+__device__ __forceinline__ void tmem_cp_32x128_x4(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Untiled bulk copy global -> shared (16-byte aligned, size % 16 == 0),
+// completing on `bar` with a transaction-count decrement.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread
 // has completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {

@@ -19,11 +19,14 @@ from . import _lib as L
 class MoEExpertMLP:
     def __init__(self, E, d, F, T=0, k=1, act="swiglu", alpha=1.0, limit=math.inf,
                  linear_offset=0.0, out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0,
-                 capacity=None, device="cuda", recompute_h=False):
+                 capacity=None, device="cuda", recompute_h=False, dtype="bf16"):
         self.desc = L.make_desc(T, E, k, d, F, act=act, alpha=alpha, limit=limit,
                                 linear_offset=linear_offset, out_scale=out_scale,
                                 has_b1=has_b1, has_b2=has_b2, sm_margin=sm_margin,
-                                capacity=capacity, recompute_h=recompute_h)
+                                capacity=capacity, recompute_h=recompute_h, dtype=dtype)
+        # dtype "mxfp8": the grouped GEMMs read MXFP8 operands (E4M3 codes,
+        # E8M0 scales per 32 elements); routing and combine stay bf16
+        self.mx = dtype == "mxfp8"
         # recompute_h: the forward keeps no H; the backward regenerates it in
         # the library workspace (activation recompute)
         self.recompute_h = recompute_h
@@ -70,6 +73,35 @@ class MoEExpertMLP:
         self.dx = z(max(T, 1), d)
         self.dlogits = z(max(T, 1), E, dtype=f32)
         self.ws = torch.zeros(max(L.moe_workspace_size(self.desc), 256), dtype=torch.uint8, device=dev)
+        if self.mx:
+            Fp = self.Fp
+            # activations: rowwise for the GEMM that contracts over features,
+            # transposed for the weight gradient that contracts over rows
+            self.x_mx = self.mx_operand(d)
+            self.a_mx = self.mx_operand(F)
+            self.dy_mx = self.mx_operand(d)
+            self.dh_mx = self.mx_operand(2 * Fp)
+            u8 = torch.uint8
+
+            def sc(rows, cols):
+                return z(E * L.moe_mx_scale_bytes(rows, cols), dtype=u8)
+
+            self.w_mx = dict(w1=z(E, 2 * Fp, d, dtype=u8), w1_s=sc(2 * Fp, d),
+                             w1t=z(E, d, 2 * Fp, dtype=u8), w1t_s=sc(d, 2 * Fp),
+                             w2=z(E, d, F, dtype=u8), w2_s=sc(d, F),
+                             w2t=z(E, F, d, dtype=u8), w2t_s=sc(F, d))
+
+    def mx_operand(self, width):
+        """MXFP8 buffers of a per-row tensor [capacity, width] in the MMA scale
+        layout: rowwise codes + scales and the transposed copy.  Scale
+        buffers start zeroed (entries past the tensor are read, never
+        written)."""
+        cap, dev, u8 = self.capacity, self.w2.device, torch.uint8
+        return dict(q=torch.zeros((cap, width), dtype=u8, device=dev),
+                    scale=torch.zeros(L.moe_mx_scale_bytes(cap, width), dtype=u8, device=dev),
+                    qt=torch.zeros((width, cap), dtype=u8, device=dev),
+                    scale_t=torch.zeros(L.moe_mx_scale_bytes(width, cap), dtype=u8, device=dev),
+                    layout="mma")
 
     # ------------------------------------------------------------ weights
     def load_weights(self, w1, b1, w2, b2, stream=None):
@@ -80,6 +112,13 @@ class MoEExpertMLP:
         self.w2.copy_(w2)
         if self.has_b2:
             self.b2.copy_(b2)
+        if self.mx:
+            self.quantize_weights(stream)
+
+    def quantize_weights(self, stream=None):
+        """MXFP8 weight copies (rowwise and transposed) from the bf16 masters;
+        once per optimizer step."""
+        L.moe_quantize_weights_mx(self.desc, self.w1p, self.w2, self.w_mx, stream)
 
     def unpack_fc1(self, packed, width, stream=None):
         """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p)."""
@@ -119,6 +158,13 @@ class MoEExpertMLP:
 
     def mlp_forward(self, stream=None, timer=None, a_mx=None, y_mx=None):
         c, po = self.counts, self.padded_offsets
+        if self.mx:
+            with self._t(timer, "quant_x"):
+                L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
+            with self._t(timer, "mlp_fwd_mx"):
+                L.moe_mlp_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.b2,
+                                 self.h, self.a, self.a_mx, self.y, stream)
+            return
         with self._t(timer, "fc1_glu_fwd"):
             L.moe_fc1_glu_fwd(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h, self.a,
                               stream, mx=a_mx)
@@ -127,6 +173,14 @@ class MoEExpertMLP:
 
     def mlp_backward(self, stream=None, timer=None, dh_mx=None):
         c, po = self.counts, self.padded_offsets
+        if self.mx:
+            with self._t(timer, "quant_dy"):
+                L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
+            with self._t(timer, "mlp_bwd_mx"):
+                L.moe_mlp_bwd_mx(self.desc, self.dy, self.dy_mx, self.x_mx, self.h, self.a_mx, c,
+                                 po, self.w_mx, self.dh, self.dh_mx, self.dx_perm, self.dw1p,
+                                 self.db1p, self.dw2, self.db2, stream)
+            return
         if self.recompute_h:
             with self._t(timer, "mlp_bwd_recompute"):
                 L.moe_mlp_bwd(self.desc, self.dy, self.x_perm, None, self.a, c, po, self.w1p,
@@ -208,8 +262,9 @@ class MoEExpertMLP:
 
     def kernels_per_step(self, routed=True):
         """Kernels of this library launched by one step() (routed) or
-        grouped_step(): six grouped GEMMs, one column-sum per bias, and for
+        grouped_step(): six grouped GEMMs, one column-sum per bias, the two
+        activation quantizations of the MXFP8 layer, and for
         the routed layer top-k, scan, assign, gather, combine, pad-row zeroing,
         combine backward, permute backward and router backward."""
-        n = 6 + int(self.has_b1) + int(self.has_b2)
+        n = 6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0)
         return n + (9 if routed else 0)

@@ -134,3 +134,73 @@ def packed_to_logical_cols(t_np, F):
     ok = src >= 0
     out[..., src[ok]] = t_np[..., ok]
     return out, t_np[..., ~ok]
+
+
+# --------------------------------------------------------------------------
+# MXFP8 path
+# --------------------------------------------------------------------------
+TOL_MX = 6e-2       # max|gpu - ref| <= 6e-2 * max|ref| (MXFP8 path)
+
+
+def mma_scales_to_rowmajor(buf, rows, cols):
+    """Scales stored in the MMA layout (include/moe.h, MOE_MX_SCALES_MMA)
+    -> [rows, cols/32] row-major, by the layout's index formula."""
+    buf = np.asarray(buf).reshape(-1)
+    ra = 2 * ((rows + 255) // 256)
+    r = np.arange(rows)[:, None]
+    j = np.arange(cols // 32)[None, :]
+    off = ((j // 4) * ra + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4
+    return buf[off]
+
+
+def run_oracle_routed_mx(wl, inp):
+    """The routed layer with the MXFP8 expert MLP: routing, permute, combine
+    and their backward as in the bf16 oracle; dY rounded to bf16 (the stored
+    tensor the quantizer reads) before the MXFP8 backward."""
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    x = bf16_bits_to_f64(inp["x"])
+    topk_idx, topk_w, counts = oracle.route(inp["logits"], inp["bias"], wl.k)
+    offsets, padded, tiles = oracle.group_offsets(counts, 128)
+    row_src, row_of = oracle.permute_index(topk_idx, wl.E, padded)
+    xp = oracle.gather_rows(x, row_src)
+    H, A, Y = oracle.grouped_forward_mx(xp, padded, counts, W1, b1, W2, b2, p)
+    out = oracle.combine(Y, row_of, topk_w)
+    dY, dw = oracle.combine_backward(bf16_bits_to_f64(inp["dout"]), Y, row_of, topk_w,
+                                     xp.shape[0])
+    dY16 = oracle.bf16_round(dY)
+    dX, dH, dW1, db1, dW2, db2 = oracle.grouped_backward_mx(xp, H, A, dY16, padded, counts,
+                                                           W1, W2, p)
+    dx = oracle.permute_backward(dX, row_of)
+    dlogits = oracle.route_backward(dw, topk_w, topk_idx, wl.E)
+    return dict(topk_idx=topk_idx, counts=counts, padded_offsets=padded, x_perm=xp, H=H, A=A,
+                Y=Y, out=out, dY=dY16, dw=dw, dX_perm=dX, dH=dH, dW1=dW1, db1=db1, dW2=dW2,
+                db2=db2, dx=dx, dlogits=dlogits)
+
+
+def run_both_direct_mx(wl, inp):
+    """Groups given directly, MXFP8 expert MLP on both sides."""
+    sizes = inp["group_sizes"]
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    offsets, padded, tiles = oracle.group_offsets(sizes, align=128)
+    xp_bits = padded_rows(inp["x"], sizes, padded, wl.d)
+    dy_bits = padded_rows(inp["dout"], sizes, padded, wl.d)
+    xp = bf16_bits_to_f64(xp_bits)
+    dyp = bf16_bits_to_f64(dy_bits)
+    H, A, Y = oracle.grouped_forward_mx(xp, padded, sizes, W1, b1, W2, b2, p)
+    dX, dH, dW1, db1, dW2, db2 = oracle.grouped_backward_mx(xp, H, A, dyp, padded, sizes, W1,
+                                                           W2, p)
+    ref = dict(H=H, A=A, Y=Y, dX_perm=dX, dH=dH, dW1=dW1, db1=db1, dW2=dW2, db2=db2,
+               padded_offsets=padded, counts=sizes)
+    cap = max(128, int(padded[-1]))
+    layer = make_layer(wl, capacity=cap, dtype="mxfp8")
+    load_layer_weights(layer, inp)
+    layer.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
+    R_pad = int(padded[-1])
+    layer.x_perm[:R_pad].copy_(bits_to_dev(xp_bits))
+    layer.dy[:R_pad].copy_(bits_to_dev(dy_bits))
+    layer.mlp_forward()
+    layer.mlp_backward()
+    torch.cuda.synchronize()
+    return layer, ref

@@ -1,0 +1,146 @@
+"""GPU parity of the MXFP8 path (block-scaled tcgen05 GEMMs) against the
+fp64 MXFP8 oracle on the same seeded inputs.
+
+Bit-exact: routing, the quantizer in the MMA scale layout, and the fused
+MXFP8 outputs of the epilogues (given the GPU's own bf16 values, as for the
+bf16 path's fused outputs).  H and A come from identical quantized operands,
+so they meet the bf16 tolerance; everything downstream of a quantized
+intermediate meets max|gpu-ref| <= 6e-2 * max|ref|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from tests import harness as H
+from workloads import WORKLOADS, make_inputs, scaled
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+BASE = WORKLOADS["bf16_t4096_e64"]
+ROUTED = {
+    "e8_k2": scaled(BASE, T=512, E=8, k=2, d=256, F=256),
+    "gptoss_small": scaled(WORKLOADS["gptoss_t16384_e32"], T=300, E=8, k=4, d=192, F=224),
+    "geglu_raggedF": scaled(BASE, T=320, E=6, k=3, d=320, F=352, act="geglu",
+                            router_bias=False),
+}
+
+
+def _mx_close(name, got, ref):
+    return H.assert_close(name, got, ref, rel=H.TOL_MX, abs_=0.0)
+
+
+def test_quantizer_mma_layout_bit_exact():
+    """moe_quantize_mx_bf16 in the MMA scale layout == the oracle quantizer,
+    rowwise and transposed, on a batch of tensors whose sizes are not
+    multiples of 128 (partial scale atoms)."""
+    from moe_expert_mlp_gb300 import _lib as L
+    rng = np.random.default_rng(5)
+    batch, rows, cols = 3, 160, 224
+    v = (rng.standard_normal((batch, rows, cols)) *
+         np.exp2(rng.integers(-20, 20, (batch, rows, 1)))).astype(np.float32)
+    bits = torch.from_numpy(v).to(torch.bfloat16)
+    vals = bits.float().numpy()
+    x = bits.cuda()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    sb, stb = L.moe_mx_scale_bytes(rows, cols), L.moe_mx_scale_bytes(cols, rows)
+    out = dict(q=torch.zeros((batch, rows, cols), **u8), scale=torch.zeros(batch * sb, **u8),
+               qt=torch.zeros((batch, cols, rows), **u8), scale_t=torch.zeros(batch * stb, **u8),
+               layout="mma")
+    L.moe_quantize_mx_bf16(x, batch, rows, cols, out)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        q_ref, s_ref = oracle.mx_quantize_rows(vals[b])
+        qt_ref, st_ref = oracle.mx_quantize_cols(vals[b])
+        assert np.array_equal(out["q"][b].cpu().numpy(), q_ref)
+        assert np.array_equal(out["qt"][b].cpu().numpy(), qt_ref)
+        sbuf = out["scale"].cpu().numpy()[b * sb:(b + 1) * sb]
+        stbuf = out["scale_t"].cpu().numpy()[b * stb:(b + 1) * stb]
+        assert np.array_equal(H.mma_scales_to_rowmajor(sbuf, rows, cols), s_ref)
+        assert np.array_equal(H.mma_scales_to_rowmajor(stbuf, cols, rows), st_ref)
+        # entries outside the tensor stay zero (a finite scale for the MMA)
+        n_used = rows * cols // 32
+        assert np.count_nonzero(sbuf) <= n_used and np.count_nonzero(stbuf) <= n_used
+
+
+def _check_fused_mx(layer, name, x_bf16, mx, width):
+    """Fused epilogue MXFP8 outputs (MMA layout) == oracle quantizer applied
+    to the GPU's stored bf16 tensor."""
+    R_pad = int(H.to_np(layer.padded_offsets)[-1])
+    x = H.to_np(x_bf16)[:R_pad].astype(np.float32)
+    cap = layer.capacity
+    q_ref, s_ref = oracle.mx_quantize_rows(x)
+    assert np.array_equal(mx["q"].cpu().numpy()[:R_pad], q_ref), name + " rowwise codes"
+    s = H.mma_scales_to_rowmajor(mx["scale"].cpu().numpy(), cap, width)[:R_pad]
+    assert np.array_equal(s, s_ref), name + " rowwise scales"
+    qt_ref, st_ref = oracle.mx_quantize_cols(x)
+    assert np.array_equal(mx["qt"].cpu().numpy()[:, :R_pad], qt_ref), name + " columnwise codes"
+    st = H.mma_scales_to_rowmajor(mx["scale_t"].cpu().numpy(), width, cap)[:, :R_pad // 32]
+    assert np.array_equal(st, st_ref), name + " columnwise scales"
+
+
+@pytest.mark.parametrize("name", list(ROUTED))
+def test_routed_layer_mxfp8(name):
+    wl = ROUTED[name]
+    inp = make_inputs(wl)
+    ref = H.run_oracle_routed_mx(wl, inp)
+    layer = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8"))
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    T = wl.T
+    R_pad = int(ref["padded_offsets"][-1])
+    assert np.array_equal(H.to_np(layer.topk_idx)[:T], ref["topk_idx"])
+    assert np.array_equal(H.to_np(layer.padded_offsets), ref["padded_offsets"])
+    h_log, h_pad = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
+    assert np.all(h_pad == 0)
+    H.assert_close("H", h_log, ref["H"])
+    H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
+    _mx_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
+    _mx_close("out", H.to_np(layer.out)[:T], ref["out"])
+    dh_log, dh_pad = H.packed_to_logical_cols(H.to_np(layer.dh)[:R_pad], wl.F)
+    assert np.all(dh_pad == 0)
+    _mx_close("dH", dh_log, ref["dH"])
+    _mx_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
+    _mx_close("dW2", H.to_np(layer.dw2), ref["dW2"])
+    _mx_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    if wl.has_b1:
+        db1 = H.to_np(layer.unpack_fc1(layer.db1p.reshape(wl.E, -1, 1).contiguous(), 1))[..., 0]
+        _mx_close("db1", db1, ref["db1"])
+    if wl.has_b2:
+        _mx_close("db2", H.to_np(layer.db2), ref["db2"])
+    _mx_close("dx", H.to_np(layer.dx)[:T], ref["dx"])
+    _mx_close("dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"])
+    _check_fused_mx(layer, "A", layer.a, layer.a_mx, wl.F)
+    _check_fused_mx(layer, "dH", layer.dh, layer.dh_mx, 2 * layer.Fp)
+
+
+def test_direct_groups_mxfp8_with_empty_experts():
+    """Zipf group sizes with empty experts and a one-row group, as in the
+    DeepSeek-shaped workload."""
+    wl = scaled(WORKLOADS["dsv3_r16384_e32"], R=700, E=9, d=256, F=192, zipf_empty=3)
+    inp = make_inputs(wl)
+    inp["group_sizes"][np.argmax(inp["group_sizes"])] -= 1
+    inp["group_sizes"][int(np.flatnonzero(inp["group_sizes"] == 0)[0])] = 1
+    layer, ref = H.run_both_direct_mx(wl, inp)
+    R_pad = int(ref["padded_offsets"][-1])
+    h_log, _ = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
+    H.assert_close("H", h_log, ref["H"])
+    H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
+    _mx_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
+    _mx_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
+    _mx_close("dW2", H.to_np(layer.dw2), ref["dW2"])
+    _mx_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    for e in np.flatnonzero(ref["counts"] == 0):
+        assert torch.count_nonzero(layer.dw2[e]) == 0
+        assert torch.count_nonzero(layer.dw1p[e]) == 0
+
+
+def test_mxfp8_deterministic_bitwise():
+    wl = ROUTED["gptoss_small"]
+    inp = make_inputs(wl)
+    layer = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8"))
+    snap = {n: getattr(layer, n).clone() for n in ("out", "dx", "dw1p", "dw2", "dlogits", "h")}
+    H.run_gpu_routed(wl, inp, layer=layer)
+    for n, t in snap.items():
+        assert torch.equal(getattr(layer, n), t), n
