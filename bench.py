@@ -47,11 +47,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # GEMM sources the counters were taken on; a changed kernel reports null.
 _NCU_SRC = "dd05950cd75c1d2f"
 NCU_TRAFFIC = {
-    ("fc1_glu_fwd", "bf16_t4096_e64"): {"bytes": 785.678592e6 + 216.864768e6, "src": _NCU_SRC},
-    ("fc2_fwd", "bf16_t4096_e64"): {"bytes": 409.688064e6 + 101.865728e6, "src": _NCU_SRC},
-    ("fc2_dgrad_dglu", "bf16_t4096_e64"): {"bytes": 613.943040e6 + 134.005504e6, "src": _NCU_SRC},
-    ("fc2_wgrad", "bf16_t4096_e64"): {"bytes": 185.114112e6 + 313.563392e6, "src": _NCU_SRC},
-    ("fc1_wgrad", "bf16_t4096_e64"): {"bytes": 258.164736e6 + 682.315008e6, "src": _NCU_SRC},
+    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 785.678592e6 + 216.864768e6, "src": _NCU_SRC},
+    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.688064e6 + 101.865728e6, "src": _NCU_SRC},
+    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 613.943040e6 + 134.005504e6, "src": _NCU_SRC},
+    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.114112e6 + 313.563392e6, "src": _NCU_SRC},
+    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 258.164736e6 + 682.315008e6, "src": _NCU_SRC},
 }
 
 
@@ -103,6 +103,9 @@ def call_work(wl, name, R):
         "permute_bwd": R * d * 2 + T * d * 2,
         "route_bwd": T * k * 12 + T * wl.E * 4,
         "bias_grads": R * d * 2 * int(wl.has_b2) + R * 2 * F * 2 * int(wl.has_b1),
+        # bf16 rows in; rowwise and transposed E4M3 codes + one scale per 32 out
+        "quant_x": R * d * (2 + 2 + 2 / 32),
+        "quant_dy": R * d * (2 + 2 + 2 / 32),
     }
     return "byte", float(mem.get(name, 0.0))
 
@@ -183,10 +186,28 @@ def gpu_uuid(torch, dev):
 
 
 # ------------------------------------------------------------ oracle timing
-def oracle_sample_run(wl, inp, n_tokens):
-    """Time the CPU oracle on the first n_tokens tokens (routed workloads) or
-    on the first experts holding about n_tokens rows (direct workloads).
-    Returns (seconds, flops of the sample, description)."""
+def _oracle_routed_mx(oracle, x, logits, bias, dout, W1, b1, W2, b2, k, p):
+    """The routed layer with the MXFP8 expert MLP (routing, combine and their
+    backward as in the bf16 oracle; dY rounded to the stored bf16)."""
+    E = W1.shape[0]
+    topk_idx, topk_w, counts = oracle.route(logits, bias, k)
+    _, padded, _ = oracle.group_offsets(counts, 128)
+    row_src, row_of = oracle.permute_index(topk_idx, E, padded)
+    xp = oracle.gather_rows(x, row_src)
+    Hh, A, Y = oracle.grouped_forward_mx(xp, padded, counts, W1, b1, W2, b2, p)
+    oracle.combine(Y, row_of, topk_w)
+    dY, dw = oracle.combine_backward(dout, Y, row_of, topk_w, xp.shape[0])
+    dX = oracle.grouped_backward_mx(xp, Hh, A, oracle.bf16_round(dY), padded, counts, W1, W2,
+                                    p)[0]
+    oracle.permute_backward(dX, row_of)
+    oracle.route_backward(dw, topk_w, topk_idx, E)
+
+
+def oracle_sample_run(wl, inp, n_tokens, mx=False):
+    """Time the CPU oracle (its MXFP8 variant when mx) on the first n_tokens
+    tokens (routed workloads) or on the first experts holding about n_tokens
+    rows (direct workloads).  Returns (seconds, flops of the sample,
+    description)."""
     import oracle
     p = oracle.GluParams(wl.act, wl.alpha, wl.limit, wl.linear_offset, wl.out_scale)
     W1 = bf16_bits_to_f64(inp["w1"])
@@ -198,8 +219,12 @@ def oracle_sample_run(wl, inp, n_tokens):
         x = bf16_bits_to_f64(inp["x"][:n])
         dout = bf16_bits_to_f64(inp["dout"][:n])
         t0 = time.perf_counter()
-        fwd = oracle.moe_forward(x, inp["logits"][:n], inp["bias"], W1, b1, W2, b2, wl.k, p)
-        oracle.moe_backward(fwd, dout, W1, W2, p)
+        if mx:
+            _oracle_routed_mx(oracle, x, inp["logits"][:n], inp["bias"], dout, W1, b1, W2, b2,
+                              wl.k, p)
+        else:
+            fwd = oracle.moe_forward(x, inp["logits"][:n], inp["bias"], W1, b1, W2, b2, wl.k, p)
+            oracle.moe_backward(fwd, dout, W1, W2, p)
         dt = time.perf_counter() - t0
         rows = n * wl.k
         desc = f"first {n} of {wl.T} tokens ({rows} routed rows), full fwd+bwd"
@@ -224,8 +249,12 @@ def oracle_sample_run(wl, inp, n_tokens):
                 xr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["x"][src_off[e]:src_off[e] + keep[e]])
                 dyr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["dout"][src_off[e]:src_off[e] + keep[e]])
         t0 = time.perf_counter()
-        Hh, A, Y = oracle.grouped_forward(xr, padded, keep, W1, b1, W2, b2, p)
-        oracle.grouped_backward(xr, Hh, A, dyr, padded, keep, W1, W2, p)
+        if mx:
+            Hh, A, Y = oracle.grouped_forward_mx(xr, padded, keep, W1, b1, W2, b2, p)
+            oracle.grouped_backward_mx(xr, Hh, A, dyr, padded, keep, W1, W2, p)
+        else:
+            Hh, A, Y = oracle.grouped_forward(xr, padded, keep, W1, b1, W2, b2, p)
+            oracle.grouped_backward(xr, Hh, A, dyr, padded, keep, W1, W2, p)
         dt = time.perf_counter() - t0
         rows = int(acc)
         desc = f"{int((keep > 0).sum())} smallest experts ({rows} of {wl.R} rows), fwd+bwd"
@@ -239,13 +268,14 @@ def run_reference(args, wl):
         return 0
     inp = make_inputs(wl)
     n_tok = args.ref_sample_tokens
+    mx = args.dtype == "mxfp8"
     for _ in range(max(args.warmup, 0)):
-        oracle_sample_run(wl, inp, n_tok)
+        oracle_sample_run(wl, inp, n_tok, mx)
     times = []
     flops = 0.0
     desc = ""
     for _ in range(args.steps):
-        dt, flops, desc = oracle_sample_run(wl, inp, n_tok)
+        dt, flops, desc = oracle_sample_run(wl, inp, n_tok, mx)
         times.append(dt)
     total = sum(times)
     value = flops * args.steps / total / 1e12
@@ -255,7 +285,7 @@ def run_reference(args, wl):
         "n_gpus": 0, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(wl),
+        "config": workload_config(wl, args.dtype),
         "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cores, "kind": "oracle",
                          "sample": "each step: " + desc},
         "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0,
@@ -265,9 +295,9 @@ def run_reference(args, wl):
     return 0
 
 
-def workload_config(wl):
+def workload_config(wl, dtype="bf16"):
     cfg = {"workload": wl.name, "E": wl.E, "d": wl.d, "F": wl.F, "act": wl.act,
-           "routed_rows": wl.routed_rows}
+           "routed_rows": wl.routed_rows, "gemm_operands": dtype}
     if wl.router != "direct":
         cfg.update({"T": wl.T, "k": wl.k, "router_bias": wl.router_bias})
     else:
@@ -310,7 +340,8 @@ def run_ours(args, wl):
     layer = MoEExpertMLP(wl.E, wl.d, wl.F, T=wl.T if routed else 0, k=wl.k, act=wl.act,
                          alpha=wl.alpha, limit=wl.limit, linear_offset=wl.linear_offset,
                          out_scale=wl.out_scale, has_b1=wl.has_b1, has_b2=wl.has_b2,
-                         capacity=cap, device=dev)
+                         capacity=cap, device=dev, dtype=args.dtype)
+    mx = args.dtype == "mxfp8"
     w1 = bits_to_dev(inp["w1"], dev)
     w2 = bits_to_dev(inp["w2"], dev)
     b1 = bits_to_dev(inp["b1"], dev) if inp["b1"] is not None else None
@@ -421,7 +452,7 @@ def run_ours(args, wl):
 
     # fused vs unfused expert MLP (same kernels, activation as its own pass)
     fusion = None
-    if not args.no_fusion:
+    if not args.no_fusion and not mx:
         fusion = measure_fusion(torch, layer, K)
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
@@ -454,19 +485,23 @@ def run_ours(args, wl):
     dom_avg = sum(per[dominant]) / len(per[dominant])
     achieved = work / (dom_avg * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
-    tr = NCU_TRAFFIC.get((dominant, wl.name))
+    peak_note = f"{peak_src} bf16 burst (cuBLAS)"
+    if mx:   # no measured FP8 figure: bf16 measured x the nominal FP8/BF16 ratio (2)
+        peak *= 2.0
+        peak_note = f"{peak_src} bf16 burst (cuBLAS) x 2, the nominal FP8/BF16 dense ratio"
+    tr = NCU_TRAFFIC.get((dominant, wl.name, args.dtype))
     traffic = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(wl), parallelism=f"replicas x{world}",
+        "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
+        "config": dict(workload_config(wl, args.dtype), parallelism=f"replicas x{world}",
                        graph=bool(use_graph)),
         "tokens_per_s": round(job_rate(wl.T if routed else R, K, world, ms_max), 1),
         "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": f"{peak_src} bf16 burst (cuBLAS)"},
+                     "traffic": traffic, "peak_source": peak_note},
         "kernels": kernels,
         "gpu_launches": layer.kernels_per_step(routed) * K,
         "clocks": clocks,
@@ -474,7 +509,7 @@ def run_ours(args, wl):
         "fusion": fusion,
     }
     if not args.no_cpu_baseline:
-        dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens)
+        dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens, mx)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": host_cores(),
                                 "kind": "oracle", "sample": desc}
     print(json.dumps(line))
@@ -597,6 +632,8 @@ def main():
                     help="tokens (or rows) of the oracle sample in the cpu_baseline leg")
     ap.add_argument("--ref-sample-tokens", type=int, default=256,
                     help="tokens (or rows) per step of --impl reference")
+    ap.add_argument("--dtype", choices=["bf16", "mxfp8"], default="bf16",
+                    help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -394,6 +394,36 @@ moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx
                             const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,
                             void* a, const moe_mx_out_t* a_mx, void* y, cudaStream_t stream);
 
+/* The MXFP8 grouped GEMMs one at a time (moe_mlp_fwd_mx / moe_mlp_bwd_mx
+ * call exactly these, in this order); arguments as in those two calls.
+ *   moe_fc1_glu_fwd_mx    h, a, a_mx <- x_mx (rowwise), w1
+ *   moe_fc2_fwd_mx        y          <- a_mx (rowwise), w2
+ *   moe_fc2_dgrad_dglu_mx dh, dh_mx  <- dy_mx (rowwise), w2t, h
+ *   moe_fc2_wgrad_mx      dw2        <- dy_mx, a_mx (transposed copies)
+ *   moe_fc1_dgrad_mx      dx_perm    <- dh_mx (rowwise), w1t
+ *   moe_fc1_wgrad_mx      dw1p       <- dh_mx, x_mx (transposed copies) */
+moe_status_t moe_fc1_glu_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const moe_mx_weights_t* w, const void* b1p, void* h, void* a,
+                                const moe_mx_out_t* a_mx, cudaStream_t stream);
+moe_status_t moe_fc2_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_mx,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_mx_weights_t* w, const void* b2, void* y,
+                            cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_mx,
+                                   const void* h, const int32_t* counts,
+                                   const int32_t* padded_offsets, const moe_mx_weights_t* w,
+                                   void* dh, const moe_mx_out_t* dh_mx, cudaStream_t stream);
+moe_status_t moe_fc2_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_mx,
+                              const moe_mx_out_t* a_mx, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw2, cudaStream_t stream);
+moe_status_t moe_fc1_dgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_mx,
+                              const int32_t* counts, const int32_t* padded_offsets,
+                              const moe_mx_weights_t* w, void* dx_perm, cudaStream_t stream);
+moe_status_t moe_fc1_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_mx,
+                              const moe_mx_out_t* x_mx, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw1p, cudaStream_t stream);
+
 /* MXFP8 backward:
  *   dy     dY bf16 [capacity, d] (bias gradient)   dy_mx  its rowwise and
  *          transposed MXFP8 copies                  x_mx   x_perm transposed

@@ -32,7 +32,9 @@ EXPORTS = (
     "moe_route_permute_noalloc", "moe_quantize_mx", "moe_selftest_wait_timeout",
     "moe_fc1_glu_fwd_unfused", "moe_fc2_dgrad_dglu_unfused", "moe_fc1_recompute_h",
     "moe_mx_scale_bytes", "moe_quantize_mx_bf16", "moe_quantize_act_mx",
-    "moe_quantize_weights_mx", "moe_mlp_fwd_mx", "moe_mlp_bwd_mx",
+    "moe_quantize_weights_mx", "moe_mlp_fwd_mx", "moe_mlp_bwd_mx", "moe_fc1_glu_fwd_mx",
+    "moe_fc2_fwd_mx", "moe_fc2_dgrad_dglu_mx", "moe_fc2_wgrad_mx", "moe_fc1_dgrad_mx",
+    "moe_fc1_wgrad_mx",
 )
 
 
@@ -141,6 +143,12 @@ def lib():
             "moe_quantize_weights_mx": (ctypes.c_int, [D, P, P, P, P]),
             "moe_mlp_fwd_mx": (ctypes.c_int, [D] + [P] * 11),
             "moe_mlp_bwd_mx": (ctypes.c_int, [D] + [P] * 16),
+            "moe_fc1_glu_fwd_mx": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_fwd_mx": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc2_dgrad_dglu_mx": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_wgrad_mx": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_dgrad_mx": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_wgrad_mx": (ctypes.c_int, [D] + [P] * 6),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -351,3 +359,36 @@ def moe_mlp_bwd_mx(desc, dy, dy_mx, x_mx, h, a_mx, counts, padded_offsets, w_mx,
                                 _mx(a_mx), _p(counts), _p(padded_offsets), _mxw(w_mx), _p(dh),
                                 _mx(dh_mx), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2),
                                 _stream(stream)))
+
+
+def moe_fc1_glu_fwd_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, a, a_mx, stream=None):
+    _check(lib().moe_fc1_glu_fwd_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
+                                    _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h), _p(a),
+                                    _mx(a_mx), _stream(stream)))
+
+
+def moe_fc2_fwd_mx(desc, a_mx, counts, padded_offsets, w_mx, b2, y, stream=None):
+    _check(lib().moe_fc2_fwd_mx(ctypes.byref(desc), _mx(a_mx), _p(counts), _p(padded_offsets),
+                                _mxw(w_mx), _p(b2), _p(y), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_mx(desc, dy_mx, h, counts, padded_offsets, w_mx, dh, dh_mx,
+                          stream=None):
+    _check(lib().moe_fc2_dgrad_dglu_mx(ctypes.byref(desc), _mx(dy_mx), _p(h), _p(counts),
+                                       _p(padded_offsets), _mxw(w_mx), _p(dh), _mx(dh_mx),
+                                       _stream(stream)))
+
+
+def moe_fc2_wgrad_mx(desc, dy_mx, a_mx, counts, padded_offsets, dw2, stream=None):
+    _check(lib().moe_fc2_wgrad_mx(ctypes.byref(desc), _mx(dy_mx), _mx(a_mx), _p(counts),
+                                  _p(padded_offsets), _p(dw2), _stream(stream)))
+
+
+def moe_fc1_dgrad_mx(desc, dh_mx, counts, padded_offsets, w_mx, dx_perm, stream=None):
+    _check(lib().moe_fc1_dgrad_mx(ctypes.byref(desc), _mx(dh_mx), _p(counts),
+                                  _p(padded_offsets), _mxw(w_mx), _p(dx_perm), _stream(stream)))
+
+
+def moe_fc1_wgrad_mx(desc, dh_mx, x_mx, counts, padded_offsets, dw1p, stream=None):
+    _check(lib().moe_fc1_wgrad_mx(ctypes.byref(desc), _mx(dh_mx), _mx(x_mx), _p(counts),
+                                  _p(padded_offsets), _p(dw1p), _stream(stream)))

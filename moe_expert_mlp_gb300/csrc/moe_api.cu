@@ -852,20 +852,20 @@ moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p
   return cuda_status(e);
 }
 
-moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
-                            const int32_t* counts, const int32_t* padded_offsets,
-                            const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,
-                            void* a, const moe_mx_out_t* a_mx, void* y, cudaStream_t stream) {
+moe_status_t moe_fc1_glu_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const moe_mx_weights_t* w, const void* b1p, void* h, void* a,
+                                const moe_mx_out_t* a_mx, cudaStream_t stream) {
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
-  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h || !y) return MOE_ERR_NULL;
-  if ((desc->has_b1 && !b1p) || (desc->has_b2 && !b2)) return MOE_ERR_NULL;
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   if (!mx_ok(x_mx, true, false) || !mx_ok(a_mx, true, a_mx && a_mx->qt)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
   const uint64_t cap = desc->capacity;
-  // FC1 + GLU: x_perm (codes [cap, d]) x W1p (codes [E, 2F_pad, d])
+  // x_perm (codes [cap, d]) x W1p (codes [E, 2F_pad, d]); GLU epilogue
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
@@ -884,23 +884,159 @@ moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx
   g.bias_ld = 2 * Fp;
   set_scales(g, x_mx->scale, cap, w->w1_s, 2 * Fp, sf_bytes(2 * Fp, d));
   if ((st = set_mx(g, a_mx, desc->F, stream)) != MOE_OK) return st;
-  cudaError_t e = launch_grouped_gemm_mx(kFc1Glu, g, grid_for(di, desc), stream);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  // FC2: A (codes [cap, F]) x W2 (codes [E, d, F])
-  GemmArgs g2;
-  fill_common(g2, desc, di, counts, padded_offsets);
-  if (!encode_u8(&g2.tma_a, a_mx->q, F, cap, 1, 128) ||
-      !encode_u8(&g2.tma_b, w->w2, F, d, E, 256) || !encode_out(&g2.tma_out0, y, d, cap, 1))
+  return cuda_status(launch_grouped_gemm_mx(kFc1Glu, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_mx,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_mx_weights_t* w, const void* b2, void* y,
+                            cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !y) return MOE_ERR_NULL;
+  if (desc->has_b2 && !b2) return MOE_ERR_NULL;
+  if (!mx_ok(a_mx, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  // A (codes [cap, F]) x W2 (codes [E, d, F])
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, a_mx->q, F, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w2, F, d, E, 256) || !encode_out(&g.tma_out0, y, d, cap, 1))
     return MOE_ERR_SHAPE;
-  g2.K = desc->F;
-  g2.n_ext = desc->d;
-  g2.b_ext = desc->d;
-  g2.out0 = y;
-  g2.ld0 = d;
-  g2.bias = desc->has_b2 ? b2 : nullptr;
-  g2.bias_ld = d;
-  set_scales(g2, a_mx->scale, cap, w->w2_s, d, sf_bytes(d, F));
-  return cuda_status(launch_grouped_gemm_mx(kFc2, g2, grid_for(di, desc), stream));
+  g.K = desc->F;
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = y;
+  g.ld0 = d;
+  g.bias = desc->has_b2 ? b2 : nullptr;
+  g.bias_ld = d;
+  set_scales(g, a_mx->scale, cap, w->w2_s, d, sf_bytes(d, F));
+  return cuda_status(launch_grouped_gemm_mx(kFc2, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_dgrad_dglu_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_mx,
+                                   const void* h, const int32_t* counts,
+                                   const int32_t* padded_offsets, const moe_mx_weights_t* w,
+                                   void* dh, const moe_mx_out_t* dh_mx, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!h || !counts || !padded_offsets || !mx_weights_ok(w) || !dh) return MOE_ERR_NULL;
+  if (!mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dY (codes [cap, d]) x W2^T (codes [E, F, d]); dGLU epilogue reads H
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) ||
+      !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(Fp);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = 2 * Fp;
+  g.aux = h;
+  g.ld_aux = 2 * Fp;
+  set_scales(g, dy_mx->scale, cap, w->w2t_s, F, sf_bytes(F, d));
+  if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm_mx(kDgradDglu, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_mx,
+                              const moe_mx_out_t* a_mx, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw2, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
+  if (!mx_ok(dy_mx, false, true) || !mx_ok(a_mx, false, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  // dW2[e] = dY^T A over the group's rows: codes [d, cap] and [F, cap]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dy_mx->qt, cap, d, 1, 128) ||
+      !encode_u8(&g.tma_b, a_mx->qt, cap, F, 1, 256) || !encode_out(&g.tma_out0, dw2, F, d, E))
+    return MOE_ERR_SHAPE;
+  g.m_ext = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = dw2;
+  g.ld0 = F;
+  set_scales(g, dy_mx->scale_t, d, a_mx->scale_t, F, 0);
+  return cuda_status(launch_grouped_gemm_mx(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_dgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_mx,
+                              const int32_t* counts, const int32_t* padded_offsets,
+                              const moe_mx_weights_t* w, void* dx_perm, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !dx_perm) return MOE_ERR_NULL;
+  if (!mx_ok(dh_mx, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dH (codes [cap, 2F_pad]) x W1p^T (codes [E, d, 2F_pad])
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dh_mx->q, 2 * Fp, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w1t, 2 * Fp, d, E, 256) ||
+      !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dx_perm;
+  g.ld0 = d;
+  set_scales(g, dh_mx->scale, cap, w->w1t_s, d, sf_bytes(d, 2 * Fp));
+  return cuda_status(launch_grouped_gemm_mx(kDgradFc1, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_mx,
+                              const moe_mx_out_t* x_mx, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw1p, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
+  if (!mx_ok(dh_mx, false, true) || !mx_ok(x_mx, false, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t cap = desc->capacity;
+  // dW1p[e] = dH^T X over the group's rows: codes [2F_pad, cap] and [d, cap]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dh_mx->qt, cap, 2 * Fp, 1, 128) ||
+      !encode_u8(&g.tma_b, x_mx->qt, cap, d, 1, 256) ||
+      !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
+    return MOE_ERR_SHAPE;
+  g.m_ext = static_cast<int>(2 * Fp);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dw1p;
+  g.ld0 = d;
+  set_scales(g, dh_mx->scale_t, 2 * Fp, x_mx->scale_t, d, 0);
+  return cuda_status(launch_grouped_gemm_mx(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,
+                            void* a, const moe_mx_out_t* a_mx, void* y, cudaStream_t stream) {
+  if (!y) return MOE_ERR_NULL;
+  moe_status_t st =
+      moe_fc1_glu_fwd_mx(desc, x_mx, counts, padded_offsets, w, b1p, h, a, a_mx, stream);
+  if (st != MOE_OK) return st;
+  return moe_fc2_fwd_mx(desc, a_mx, counts, padded_offsets, w, b2, y, stream);
 }
 
 moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
@@ -911,82 +1047,17 @@ moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
                             void* dw2, void* db2, cudaStream_t stream) {
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
-  if (!dy || !h || !counts || !padded_offsets || !mx_weights_ok(w) || !dh || !dx_perm ||
-      !dw1p || !dw2)
-    return MOE_ERR_NULL;
+  if (!dy || !dx_perm || !dw1p || !dw2) return MOE_ERR_NULL;
   if (!mx_ok(dy_mx, true, true) || !mx_ok(x_mx, false, true) || !mx_ok(a_mx, false, true) ||
       !mx_ok(dh_mx, true, true))
     return MOE_ERR_NULL;
-  DeviceInfo* di;
-  if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
-  const uint64_t cap = desc->capacity;
-  const int grid = grid_for(di, desc);
-  {  // FC2 dgrad + dGLU: dY (codes [cap, d]) x W2^T (codes [E, F, d]); dH from H
-    GemmArgs g;
-    fill_common(g, desc, di, counts, padded_offsets);
-    if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
-        !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) ||
-        !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
-      return MOE_ERR_SHAPE;
-    g.K = desc->d;
-    g.n_ext = static_cast<int>(Fp);
-    g.b_ext = desc->F;
-    g.out0 = dh;
-    g.ld0 = 2 * Fp;
-    g.aux = h;
-    g.ld_aux = 2 * Fp;
-    set_scales(g, dy_mx->scale, cap, w->w2t_s, F, sf_bytes(F, d));
-    if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
-    if (launch_grouped_gemm_mx(kDgradDglu, g, grid, stream) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
-  {  // FC2 wgrad: dW2[e] = dY^T A over the group's rows (codes [d, cap] and [F, cap])
-    GemmArgs g;
-    fill_common(g, desc, di, counts, padded_offsets);
-    if (!encode_u8(&g.tma_a, dy_mx->qt, cap, d, 1, 128) ||
-        !encode_u8(&g.tma_b, a_mx->qt, cap, F, 1, 256) ||
-        !encode_out(&g.tma_out0, dw2, F, d, E))
-      return MOE_ERR_SHAPE;
-    g.m_ext = desc->d;
-    g.n_ext = desc->F;
-    g.b_ext = desc->F;
-    g.out0 = dw2;
-    g.ld0 = F;
-    set_scales(g, dy_mx->scale_t, d, a_mx->scale_t, F, 0);
-    if (launch_grouped_gemm_mx(kWgrad, g, grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  {  // FC1 dgrad: dH (codes [cap, 2F_pad]) x W1p^T (codes [E, d, 2F_pad])
-    GemmArgs g;
-    fill_common(g, desc, di, counts, padded_offsets);
-    if (!encode_u8(&g.tma_a, dh_mx->q, 2 * Fp, cap, 1, 128) ||
-        !encode_u8(&g.tma_b, w->w1t, 2 * Fp, d, E, 256) ||
-        !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
-      return MOE_ERR_SHAPE;
-    g.K = static_cast<int>(2 * Fp);
-    g.n_ext = desc->d;
-    g.b_ext = desc->d;
-    g.out0 = dx_perm;
-    g.ld0 = d;
-    set_scales(g, dh_mx->scale, cap, w->w1t_s, d, sf_bytes(d, 2 * Fp));
-    if (launch_grouped_gemm_mx(kDgradFc1, g, grid, stream) != cudaSuccess)
-      return MOE_ERR_CUDA;
-  }
-  {  // FC1 wgrad: dW1p[e] = dH^T X over the group's rows (codes [2F_pad, cap], [d, cap])
-    GemmArgs g;
-    fill_common(g, desc, di, counts, padded_offsets);
-    if (!encode_u8(&g.tma_a, dh_mx->qt, cap, 2 * Fp, 1, 128) ||
-        !encode_u8(&g.tma_b, x_mx->qt, cap, d, 1, 256) ||
-        !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
-      return MOE_ERR_SHAPE;
-    g.m_ext = static_cast<int>(2 * Fp);
-    g.n_ext = desc->d;
-    g.b_ext = desc->d;
-    g.out0 = dw1p;
-    g.ld0 = d;
-    set_scales(g, dh_mx->scale_t, 2 * Fp, x_mx->scale_t, d, 0);
-    if (launch_grouped_gemm_mx(kWgrad, g, grid, stream) != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  if ((st = moe_fc2_dgrad_dglu_mx(desc, dy_mx, h, counts, padded_offsets, w, dh, dh_mx,
+                                  stream)) != MOE_OK ||
+      (st = moe_fc2_wgrad_mx(desc, dy_mx, a_mx, counts, padded_offsets, dw2, stream)) != MOE_OK ||
+      (st = moe_fc1_dgrad_mx(desc, dh_mx, counts, padded_offsets, w, dx_perm, stream)) !=
+          MOE_OK ||
+      (st = moe_fc1_wgrad_mx(desc, dh_mx, x_mx, counts, padded_offsets, dw1p, stream)) != MOE_OK)
+    return st;
   if (db1p || db2) return moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream);
   return MOE_OK;
 }

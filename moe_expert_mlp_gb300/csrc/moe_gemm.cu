@@ -151,6 +151,7 @@ __device__ __forceinline__ void dglu_compute(const uint32_t (&r)[32], const uint
 struct StoreRing {
   uint32_t base;   // shared address of the first box
   int slot;
+  uint8_t* gbase;  // the same box as a generic pointer
 };
 
 template <int NR>
@@ -174,11 +175,20 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
   fence_proxy_async_smem();
   named_bar_sync(kEpiBar, kEpiThreads);
   if (issuer) {
-    tma_store_3d(map, buf, x, y, z);
-    bulk_commit();
-    bulk_wait_read<NR - 2>();
+    if (map != nullptr) {
+      tma_store_3d(map, buf, x, y, z);
+      bulk_commit();
+      bulk_wait_read<NR - 2>();
+    } else {
+      bulk_wait_read<0>();   // staged only: keep the slot-reuse distance without a new store
+    }
   }
   ring.slot = ring.slot == NR - 1 ? 0 : ring.slot + 1;
+}
+
+// The box the next ring_store stages into (generic pointer to shared memory).
+__device__ __forceinline__ const uint8_t* ring_next_box(const StoreRing& ring) {
+  return ring.gbase + ring.slot * BOX_BYTES;
 }
 
 // Two adjacent 32-column chunks per round, one TMA store for both.  Rounds
@@ -498,7 +508,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     const int quarter = warp & 3;             // TMEM lanes this warp may read
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
-    StoreRing ring{smem_u32(smem + STAGES * STAGE_BYTES + (MX ? STAGES * SF_STAGE_BYTES : 0)), 0};
+    uint8_t* const ring_mem = smem + STAGES * STAGE_BYTES + (MX ? STAGES * SF_STAGE_BYTES : 0);
+    StoreRing ring{smem_u32(ring_mem), 0, ring_mem};
     const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
     const MxOut mx{args.mx_q, args.mx_s, args.mx_qt, args.mx_st, args.mx_amax, args.mx_width,
                    args.capacity, args.mx_mma_layout};
@@ -584,12 +595,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
             float a[32];
 #pragma unroll
             for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
-            if (args.out1 != nullptr)
-              ring_store<Tr::kNR>(ring, a, valid, &args.tma_out1, f0, y0, 0, row_local, issuer);
-            if (want_mx) {                      // MXFP8 / amax of the stored bf16 A
+            const uint8_t* box = ring_next_box(ring);
+            if (args.out1 != nullptr || want_mx)
+              ring_store<Tr::kNR>(ring, a, valid, args.out1 ? &args.tma_out1 : nullptr, f0, y0, 0,
+                                  row_local, issuer);
+            if (want_mx) {                      // MXFP8 / amax of the staged bf16 A
+              mx_block_from_box(mx, box, quarter * 32, y0 + quarter * 32, f0, lane);
+              if (mx.amax) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
-              mx_epilogue_block(mx, a, y0 + quarter * 32, f0, lane);
+                for (int i = 0; i < 32; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
+                mx_amax_block(mx, a, lane);
+              }
             }
           }
         }
@@ -618,16 +634,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           tmem_ld32(tbase + 32 * (j + 1), r);
           const bool live0 = valid && f0 < args.f_real;
           if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
-          ring_store<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
-          ring_store<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local, issuer);
-          if (want_mx) {
+          {
+            const uint8_t* box_g = ring_next_box(ring);
+            ring_store<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
+            if (want_mx) mx_block_from_box(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane);
+            const uint8_t* box_l = ring_next_box(ring);
+            ring_store<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local,
+                                issuer);
+            if (want_mx)
+              mx_block_from_box(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane);
+          }
+          if (want_mx && mx.amax) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               dg[i] = live0 ? bf16_round(dg[i]) : 0.0f;
               dl[i] = live0 ? bf16_round(dl[i]) : 0.0f;
             }
-            mx_epilogue_block(mx, dg, y0 + quarter * 32, c0, lane);
-            mx_epilogue_block(mx, dl, y0 + quarter * 32, c0 + kGluHalf, lane);
+            mx_amax_block(mx, dg, lane);
+            mx_amax_block(mx, dl, lane);
           }
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
@@ -641,16 +665,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
           if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
           const bool live1 = valid && f1 < args.f_real;
           if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
-          ring_store<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
-          ring_store<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local, issuer);
-          if (want_mx) {
+          {
+            const uint8_t* box_g = ring_next_box(ring);
+            ring_store<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
+            if (want_mx) mx_block_from_box(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane);
+            const uint8_t* box_l = ring_next_box(ring);
+            ring_store<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local,
+                                issuer);
+            if (want_mx)
+              mx_block_from_box(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane);
+          }
+          if (want_mx && mx.amax) {
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
               dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
               dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
             }
-            mx_epilogue_block(mx, dg, y0 + quarter * 32, c1, lane);
-            mx_epilogue_block(mx, dl, y0 + quarter * 32, c1 + kGluHalf, lane);
+            mx_amax_block(mx, dg, lane);
+            mx_amax_block(mx, dl, lane);
           }
         }
       } else {
@@ -702,21 +734,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
               for (int i = 0; i < 32; ++i) v1[i] += b[i];
             }
           }
+          const uint8_t* box0 = ring_next_box(ring);
+          const uint8_t* box1 = box0;
           if (write) {
             ring_store<Tr::kNR>(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
                        Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+            box1 = ring_next_box(ring);
             if (two)
               ring_store<Tr::kNR>(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32, y0,
                          Tr::kRaggedK ? ti.e : 0, row_local, issuer);
           }
-          if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the stored bf16 Y
+          if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the staged bf16 Y
+            mx_block_from_box(mx, box0, quarter * 32, y0 + quarter * 32, c0, lane);
+            if (two) mx_block_from_box(mx, box1, quarter * 32, y0 + quarter * 32, c0 + 32, lane);
+            if (mx.amax) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
-            mx_epilogue_block(mx, v0, y0 + quarter * 32, c0, lane);
-            if (two) {
-#pragma unroll
-              for (int i = 0; i < 32; ++i) v1[i] = valid ? bf16_round(v1[i]) : 0.0f;
-              mx_epilogue_block(mx, v1, y0 + quarter * 32, c0 + 32, lane);
+              for (int i = 0; i < 32; ++i) {
+                v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
+                v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
+              }
+              mx_amax_block(mx, v0, lane);
+              if (two) mx_amax_block(mx, v1, lane);
             }
           }
         }

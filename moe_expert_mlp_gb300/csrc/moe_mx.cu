@@ -52,16 +52,21 @@ __global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in
   }
 }
 
-// bf16 [batch][rows][cols] -> MXFP8, one warp per 32 x 32 block (lane =
-// row), consecutive warps on consecutive column blocks of the same rows.
-// Rowwise codes [batch][rows][cols]; columnwise codes written transposed
-// [batch][cols][rows]; scales row-major or in the MMA layout.
+// bf16 [batch][rows][cols] -> MXFP8, one warp per 32 x 32 block,
+// consecutive warps on consecutive column blocks of the same rows.  The
+// block is read coalesced (lane l: 16-byte chunk l % 4 of rows l / 4 + 8k)
+// into the warp's shared box (64-byte rows, 64-byte swizzle), from which
+// lane l quantizes row l and column l.  Rowwise codes [batch][rows][cols];
+// columnwise codes written transposed [batch][cols][rows]; scales row-major
+// or in the MMA layout.
 __global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restrict__ in,
                                                     long long batch, long long rows,
                                                     long long cols, uint8_t* q, uint8_t* s,
                                                     uint8_t* qt, uint8_t* st, int mma_layout,
                                                     const int32_t* row_limit) {
-  const int lane = threadIdx.x & 31;
+  __shared__ __align__(128) uint8_t boxes[8][32 * 64];
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  uint8_t* const box = boxes[wid];
   const long long rbn = rows / 32, cbn = cols / 32;
   const long long per_batch = rbn * cbn;
   const long long nblk = batch * per_batch;
@@ -71,18 +76,25 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restr
                                         : rows * cols / 32;
   const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   const long long rlim = row_limit ? __ldg(row_limit) : rows;   // rows past it are skipped
-  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x / 32) + threadIdx.x / 32;
-       w < nblk; w += warps) {
+  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x / 32) + wid; w < nblk;
+       w += warps) {
     const long long b = w / per_batch;
     const long long rem = w - b * per_batch;
     const long long rb = rem / cbn, cb = rem - rb * cbn;
     if (rb * 32 >= rlim) continue;
-    float v[32];
-    load_bf16x32(in + (b * rows + rb * 32 + lane) * cols + cb * 32, v);
+    const __nv_bfloat16* src = in + (b * rows + rb * 32) * cols + cb * 32;
+    __syncwarp();                       // the previous block's reads are done
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int r = (lane >> 2) + 8 * k, ch = lane & 3;
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * cols) + ch);
+      *reinterpret_cast<uint4*>(box + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)) = v;
+    }
+    __syncwarp();
     const MxOut mx{q ? q + b * rows * cols : nullptr, s ? s + b * s_bytes : nullptr,
                    qt ? qt + b * rows * cols : nullptr, st ? st + b * st_bytes : nullptr,
                    nullptr, cols, rows, mma_layout};
-    mx_epilogue_block(mx, v, rb * 32, static_cast<int>(cb * 32), lane);
+    mx_block_from_box(mx, box, 0, rb * 32, static_cast<int>(cb * 32), lane);
   }
 }
 

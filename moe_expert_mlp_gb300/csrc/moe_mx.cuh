@@ -49,10 +49,14 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
 // Quantize one block of 32 values: writes 32 codes (16-byte aligned
 // destination) and returns the E8M0 scale code.
 __device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* q) {
-  float amax = 0.0f;
+  float m[16];                                   // block max as a tree (depth 5)
 #pragma unroll
-  for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
-  const int s = mx_scale_exponent(amax);
+  for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+  const int s = mx_scale_exponent(m[0]);
   const float inv = mx_inv_scale(s);
   uint32_t w[8];
 #pragma unroll
@@ -100,59 +104,79 @@ struct MxOut {
   int mma_layout;    // scales in the block-scaled MMA layout (sf_mma_offset)
 };
 
-// One warp holds a 32 x 32 block: lane l owns row r0 + l, columns
-// col0 .. col0+31 in v (already rounded to the stored bf16 values; zero on
-// padding rows).  Writes the rowwise block of this lane, the columnwise
-// blocks (32 rows = the warp) of the 32 columns, and folds the plain and
-// Hadamard amax into mx.amax.  Whole warp must call.
-__device__ __forceinline__ void mx_epilogue_block(const MxOut& mx, const float (&v)[32],
+// MXFP8 of one staged 32 x 32 bf16 block.  The block sits in a
+// shared-memory box of 64-byte rows with the 64-byte swizzle (16-byte chunk
+// q of row r at chunk q ^ ((r >> 1) & 3)) -- the GEMM epilogue's output
+// staging layout -- as the box's rows row0 .. row0+31; they are the
+// tensor's rows r0 .. r0+31, columns col0 .. col0+31.  Lane l quantizes row
+// r0+l (rowwise) and column col0+l (columnwise, written to the transposed
+// tensor), reading shared memory only: no cross-lane shuffles.  Whole warp
+// calls; the box must be visible to the warp.
+__device__ __forceinline__ void mx_block_from_box(const MxOut& mx, const uint8_t* box, int row0,
                                                   long long r0, int col0, int lane) {
-  const long long row = r0 + lane;
   if (mx.q) {
+    // the lane's own row: four 16-byte chunks (the swizzle spreads the 8
+    // rows of a quarter warp over distinct banks)
+    float v[32];
+    const int r = row0 + lane;
+    const uint4* rowp = reinterpret_cast<const uint4*>(box + r * 64);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const uint4 c4 = rowp[q ^ ((r >> 1) & 3)];
+      const uint32_t w[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        v[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
+        v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+      }
+    }
+    const long long row = r0 + lane;
     const uint8_t sc = mx_quant32(v, mx.q + row * mx.width + col0);
     mx.s[mx.mma_layout ? sf_mma_offset(row, col0 / 32, sf_row_atoms(mx.cap))
                        : row * (mx.width / 32) + col0 / 32] = sc;
   }
   if (mx.qt) {
-    uint8_t my_sc = 0;
+    // column `lane` down the 32 rows (consecutive lanes read consecutive
+    // bf16 of one 64-byte row: no bank conflicts)
+    float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
-      float a = fabsf(v[i]);
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, o));
-      const int sx = mx_scale_exponent(a);
-      const uint32_t code = e4m3x2(v[i] * mx_inv_scale(sx), 0.0f) & 0xFFu;
-      mx.qt[static_cast<long long>(col0 + i) * mx.cap + row] = static_cast<uint8_t>(code);
-      if (lane == i) my_sc = static_cast<uint8_t>(sx + 127);
+      const int r = row0 + i;
+      const uint16_t b = *reinterpret_cast<const uint16_t*>(
+          box + r * 64 + ((((lane >> 3) ^ ((r >> 1) & 3))) << 4) + (lane & 7) * 2);
+      v[i] = __uint_as_float(static_cast<uint32_t>(b) << 16);
     }
     const long long c = col0 + lane;
+    const uint8_t sc = mx_quant32(v, mx.qt + c * mx.cap + r0);
     mx.st[mx.mma_layout ? sf_mma_offset(c, r0 / 32, sf_row_atoms(mx.width))
-                        : c * (mx.cap / 32) + r0 / 32] = my_sc;
+                        : c * (mx.cap / 32) + r0 / 32] = sc;
   }
-  if (mx.amax) {
-    float m = 0.0f, h = 0.0f;
+}
+
+// The per-tensor amax outputs of a 32 x 32 block held one row per lane in v
+// (bf16-rounded values, zero on padding rows): plain amax and the amax of
+// the 16-row Walsh-Hadamard rotation (H16 / 4) of each column segment.
+__device__ __forceinline__ void mx_amax_block(const MxOut& mx, const float (&v)[32], int lane) {
+  float m = 0.0f, h = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      m = fmaxf(m, fabsf(v[i]));
-      // Walsh-Hadamard butterflies across the 16 rows of each half warp
-      // (rows r0..r0+15 and r0+16..r0+31 are 16-row segments of one group)
-      float x = v[i];
+  for (int i = 0; i < 32; ++i) {
+    m = fmaxf(m, fabsf(v[i]));
+    float x = v[i];
 #pragma unroll
-      for (int b = 1; b < 16; b <<= 1) {
-        const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
-        x = (lane & b) ? (p - x) : (x + p);
-      }
-      h = fmaxf(h, fabsf(x) * 0.25f);
+    for (int b = 1; b < 16; b <<= 1) {
+      const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
+      x = (lane & b) ? (p - x) : (x + p);
     }
+    h = fmaxf(h, fabsf(x) * 0.25f);
+  }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-      h = fmaxf(h, __shfl_xor_sync(0xFFFFFFFFu, h, o));
-    }
-    if (lane == 0) {
-      atomic_max_nonneg(mx.amax, m);
-      atomic_max_nonneg(mx.amax + 1, h);
-    }
+  for (int o = 16; o > 0; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    h = fmaxf(h, __shfl_xor_sync(0xFFFFFFFFu, h, o));
+  }
+  if (lane == 0) {
+    atomic_max_nonneg(mx.amax, m);
+    atomic_max_nonneg(mx.amax + 1, h);
   }
 }
 

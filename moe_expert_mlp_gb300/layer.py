@@ -161,9 +161,11 @@ class MoEExpertMLP:
         if self.mx:
             with self._t(timer, "quant_x"):
                 L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
-            with self._t(timer, "mlp_fwd_mx"):
-                L.moe_mlp_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.b2,
-                                 self.h, self.a, self.a_mx, self.y, stream)
+            with self._t(timer, "fc1_glu_fwd"):
+                L.moe_fc1_glu_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.h,
+                                     self.a, self.a_mx, stream)
+            with self._t(timer, "fc2_fwd"):
+                L.moe_fc2_fwd_mx(self.desc, self.a_mx, c, po, self.w_mx, self.b2, self.y, stream)
             return
         with self._t(timer, "fc1_glu_fwd"):
             L.moe_fc1_glu_fwd(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h, self.a,
@@ -176,10 +178,19 @@ class MoEExpertMLP:
         if self.mx:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
-            with self._t(timer, "mlp_bwd_mx"):
-                L.moe_mlp_bwd_mx(self.desc, self.dy, self.dy_mx, self.x_mx, self.h, self.a_mx, c,
-                                 po, self.w_mx, self.dh, self.dh_mx, self.dx_perm, self.dw1p,
-                                 self.db1p, self.dw2, self.db2, stream)
+            with self._t(timer, "fc2_dgrad_dglu"):
+                L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, self.h, c, po, self.w_mx,
+                                        self.dh, self.dh_mx, stream)
+            with self._t(timer, "fc2_wgrad"):
+                L.moe_fc2_wgrad_mx(self.desc, self.dy_mx, self.a_mx, c, po, self.dw2, stream)
+            with self._t(timer, "fc1_dgrad"):
+                L.moe_fc1_dgrad_mx(self.desc, self.dh_mx, c, po, self.w_mx, self.dx_perm, stream)
+            with self._t(timer, "fc1_wgrad"):
+                L.moe_fc1_wgrad_mx(self.desc, self.dh_mx, self.x_mx, c, po, self.dw1p, stream)
+            if self.has_b1 or self.has_b2:
+                with self._t(timer, "bias_grads"):
+                    L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2,
+                                     stream)
             return
         if self.recompute_h:
             with self._t(timer, "mlp_bwd_recompute"):

@@ -144,3 +144,25 @@ def test_mxfp8_deterministic_bitwise():
     H.run_gpu_routed(wl, inp, layer=layer)
     for n, t in snap.items():
         assert torch.equal(getattr(layer, n), t), n
+
+
+def test_combined_mx_calls_match_per_gemm_calls():
+    """moe_mlp_fwd_mx / moe_mlp_bwd_mx (one call each) == the six per-GEMM
+    calls the layer makes, bit for bit."""
+    from moe_expert_mlp_gb300 import _lib as L
+    wl = ROUTED["gptoss_small"]
+    inp = make_inputs(wl)
+    layer = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8"))
+    ref = {n: getattr(layer, n).clone() for n in ("h", "a", "y", "dh", "dx_perm", "dw1p",
+                                                   "dw2", "db1p", "db2")}
+    for n in ref:
+        getattr(layer, n).zero_()
+    c, po = layer.counts, layer.padded_offsets
+    L.moe_mlp_fwd_mx(layer.desc, layer.x_mx, c, po, layer.w_mx, layer.b1p, layer.b2, layer.h,
+                     layer.a, layer.a_mx, layer.y)
+    L.moe_mlp_bwd_mx(layer.desc, layer.dy, layer.dy_mx, layer.x_mx, layer.h, layer.a_mx, c, po,
+                     layer.w_mx, layer.dh, layer.dh_mx, layer.dx_perm, layer.dw1p, layer.db1p,
+                     layer.dw2, layer.db2)
+    torch.cuda.synchronize()
+    for n, t in ref.items():
+        assert torch.equal(getattr(layer, n), t), n
