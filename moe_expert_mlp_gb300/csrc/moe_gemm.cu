@@ -17,12 +17,15 @@
 // "Accelerating dropless MoE training with JAX and NVIDIA Transformer
 // Engine", "Claims and evidence": one grouped GEMM call over ragged groups.
 //
-// Design (one CTA per SM, 6 warps):
+// Design of the grouped GEMM (one CTA per SM, 10 warps):
 //   warp 0   TMA producer: 128B-swizzled operand tiles into a 4-stage ring.
-//   warp 1   TMEM owner and single-thread MMA issuer (M=128, N=256, K=16).
-//   warps 2-5 epilogue: tcgen05.ld of the fp32 accumulator, fused math,
-//            bf16 stores.  Two 256-column accumulators in TMEM let the
-//            epilogue of one tile overlap the MMAs of the next.
+//   warp 1   TMEM owner and single-thread MMA issuer (M=128, N=256; K=16
+//            per bf16 MMA, K=32 per block-scaled MXFP8 MMA).
+//   warps 2-9 epilogue, two warps per TMEM lane quarter, each taking 16 of
+//            every 32 accumulator columns: tcgen05.ld, fused math, bf16
+//            (and MXFP8) outputs.  Two 256-column accumulators in TMEM let
+//            the epilogue of one tile overlap the MMAs of the next.
+// The weight-gradient kernel on CTA pairs (bf16) keeps 6 warps.
 // Tiles are 128 rows x 256 columns.  Every expert group starts at a
 // multiple of 128 rows, so an M tile never straddles two experts; rows past
 // the group's count are padding and are written as zeros.  Weight-gradient
@@ -48,10 +51,12 @@ constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
 constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
-constexpr int NUM_THREADS = 192;
+constexpr int NUM_THREADS = 192;             // CTA-pair weight-gradient kernel
+constexpr int GEMM_THREADS = 320;            // grouped GEMM: producer, MMA, 8 epilogue warps
+constexpr int kGemmEpiThreads = 256;
 constexpr int kRing = 4;                     // output staging boxes (shared by the epilogue)
 constexpr int BOX_BYTES = 128 * 32 * 2;      // one 128-row x 32-column bf16 output box
-constexpr int kEpiThreads = 128;             // 4 epilogue warps
+constexpr int kEpiThreads = 128;             // 4 epilogue warps (CTA-pair kernel)
 constexpr int kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr size_t SMEM_BYTES =
     1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + kRing * BOX_BYTES;
@@ -128,41 +133,44 @@ __device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& 
   dl = (l >= -p.limit && l <= p.limit) ? das * phi : 0.0f;
 }
 
-// One 32-feature chunk of the dGLU epilogue: dA (fp32, from TMEM) and the
-// saved gate/linear values (bf16, prefetched into registers) -> dG, dL.
+// The 16-column share of one chunk (see the grouped GEMM's epilogue).
 template <int ACT>
-__device__ __forceinline__ void dglu_compute(const uint32_t (&r)[32], const uint4 (&hg)[4],
-                                             const uint4 (&hl)[4], const ActP& ap,
-                                             float (&dg)[32], float (&dl)[32]) {
-  float g[32], l[32];
-  unpack_bf16x32(hg, g);
-  unpack_bf16x32(hl, l);
+__device__ __forceinline__ void dglu_compute16(const uint32_t (&r)[16], const uint4 (&hg)[2],
+                                               const uint4 (&hl)[2], const ActP& ap,
+                                               float (&dg)[16], float (&dl)[16]) {
+  float g[16], l[16];
+  unpack_bf16x16(hg, g);
+  unpack_bf16x16(hl, l);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
+  for (int i = 0; i < 16; ++i) glu_bwd<ACT>(__uint_as_float(r[i]), g[i], l[i], ap, dg[i], dl[i]);
 }
 
-// Output staging: the four epilogue warps share kRing boxes of 128 rows x
+// Output staging: the epilogue warps share a ring of NR boxes of 128 rows x
 // 32 bf16 (64-byte rows, 64-byte swizzle as in the output tensor maps).
-// Thread row (= its TMEM lane) writes its 64 bytes; after a named barrier one
+// Each thread writes its row's share of a box; after a named barrier one
 // thread issues a single TMA bulk tensor store for the whole box and waits
-// until the box issued kRing-1 stores earlier has been read, so the buffer
-// the next box uses is free by the time the other threads pass the next
-// barrier.  All epilogue threads must call ring_store in the same sequence.
+// until at most NR-2 stores are still reading shared memory, so the box the
+// next round reuses is free by the time the other threads pass the next
+// barrier.  All epilogue threads must stage in the same sequence.
 struct StoreRing {
   uint32_t base;   // shared address of the first box
   int slot;
   uint8_t* gbase;  // the same box as a generic pointer
 };
 
+// Grouped-GEMM variant: eight epilogue warps, two per TMEM lane quarter;
+// the warp of `half` h writes columns 16h .. 16h+15 of its row into the box
+// (two 16-byte chunks), all 256 threads meet at the barrier, and one thread
+// stores the whole box.  `map` may be null: the box is then only staged.
 template <int NR>
-__device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32], bool live,
-                                           const CUtensorMap* map, int x, int y, int z,
-                                           int row, bool issuer) {
+__device__ __forceinline__ void ring_store_half(StoreRing& ring, const float (&v)[16], bool live,
+                                                const CUtensorMap* map, int x, int y, int z,
+                                                int row, int half, bool issuer) {
   const uint32_t buf = ring.base + ring.slot * BOX_BYTES;
   const uint32_t raddr = buf + row * 64;
   const uint32_t sw = (row >> 1) & 3;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     uint4 w = make_uint4(0, 0, 0, 0);
     if (live) {
       w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
@@ -170,10 +178,10 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
       w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
       w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     }
-    st_shared_v4(raddr + ((q ^ sw) << 4), w);
+    st_shared_v4(raddr + (((2 * half + q) ^ sw) << 4), w);
   }
   fence_proxy_async_smem();
-  named_bar_sync(kEpiBar, kEpiThreads);
+  named_bar_sync(kEpiBar, kGemmEpiThreads);
   if (issuer) {
     if (map != nullptr) {
       tma_store_3d(map, buf, x, y, z);
@@ -184,6 +192,40 @@ __device__ __forceinline__ void ring_store(StoreRing& ring, const float (&v)[32]
     }
   }
   ring.slot = ring.slot == NR - 1 ? 0 : ring.slot + 1;
+}
+
+// MXFP8 of a staged 32 x 32 block shared by the two warps of a lane quarter:
+// half 0 quantizes its rows, half 1 its columns.
+__device__ __forceinline__ void mx_block_half(const MxOut& mx, const uint8_t* box, int row0,
+                                              long long r0, int col0, int lane, int half) {
+  MxOut m = mx;
+  if (half == 0) m.qt = nullptr; else m.q = nullptr;
+  mx_block_from_box(m, box, row0, r0, col0, lane);
+}
+
+// amax outputs over one warp's 16 columns of a block (rows = lanes).
+__device__ __forceinline__ void mx_amax_block16(const MxOut& mx, const float (&v)[16], int lane) {
+  float m = 0.0f, h = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    m = fmaxf(m, fabsf(v[i]));
+    float x = v[i];
+#pragma unroll
+    for (int b = 1; b < 16; b <<= 1) {
+      const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
+      x = (lane & b) ? (p - x) : (x + p);
+    }
+    h = fmaxf(h, fabsf(x) * 0.25f);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    h = fmaxf(h, __shfl_xor_sync(0xFFFFFFFFu, h, o));
+  }
+  if (lane == 0) {
+    atomic_max_nonneg(mx.amax, m);
+    atomic_max_nonneg(mx.amax + 1, h);
+  }
 }
 
 // The box the next ring_store stages into (generic pointer to shared memory).
@@ -284,7 +326,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
 }
 
 template <int MODE, int ACT, bool MX>
-__global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
+__global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
   using Tr = Traits<MODE, MX>;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
@@ -304,7 +346,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
   const int E = args.E;
 
   // ---- group tables (sizes live in device memory; no host round trip)
-  for (int i = threadIdx.x; i <= E; i += NUM_THREADS) s_off[i] = args.padded_offsets[i];
+  for (int i = threadIdx.x; i <= E; i += GEMM_THREADS) s_off[i] = args.padded_offsets[i];
   const int* __restrict__ s_cnt = args.counts;   // group sizes read through L1
   if (threadIdx.x == 0) {
     s_abort = 0;
@@ -314,8 +356,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);
-      mbar_init(&tearly_bar[a], 4);
+      mbar_init(&tempty_bar[a], 8);
+      mbar_init(&tearly_bar[a], 8);
     }
     fence_mbar_init();
   }
@@ -346,7 +388,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
   }
   if (Tr::kRaggedK) {
     // largest group first; equal sizes keep expert order
-    for (int e = threadIdx.x; e < E; e += NUM_THREADS) {
+    for (int e = threadIdx.x; e < E; e += GEMM_THREADS) {
       int rank = 0;
       for (int j = 0; j < E; ++j)
         rank += (s_cnt[j] > s_cnt[e]) || (s_cnt[j] == s_cnt[e] && j < e);
@@ -505,7 +547,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
     }
   } else {
     // ============================ epilogue ================================
+    // Eight warps, two per TMEM lane quarter: the warp of `half` h owns
+    // columns 16h .. 16h+15 of every 32-column chunk of its 32 rows.  All
+    // eight stage each chunk into one shared box and meet at its barrier.
     const int quarter = warp & 3;             // TMEM lanes this warp may read
+    const int half = (warp - 2) >> 2;         // warps 2-5: 0, warps 6-9: 1
+    const int hc = 16 * half;                 // first column of this warp's share
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
     uint8_t* const ring_mem = smem + STAGES * STAGE_BYTES + (MX ? STAGES * SF_STAGE_BYTES : 0);
@@ -533,15 +580,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       const int y0 = ti.m0;                     // first output row of the tile's boxes
 
       // dGLU: the saved FC1 output H does not depend on the accumulator, so
-      // its first chunk is fetched before waiting for the MMAs.
-      uint4 hg[2][4], hl[2][4];
+      // the first chunk's share is fetched before waiting for the MMAs.
+      uint4 hg[2][2], hl[2][2];
       const __nv_bfloat16* Hrow = nullptr;
       if (MODE == kDgradDglu) {
         Hrow = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
         if (valid && ti.n0 < args.f_real) {
-          const long long cg = static_cast<long long>(ti.n0 / kGluHalf) * 2 * kGluHalf + (ti.n0 % kGluHalf);
-          load_raw64(Hrow + cg, hg[0]);
-          load_raw64(Hrow + cg + kGluHalf, hl[0]);
+          const long long cg = static_cast<long long>(ti.n0 / kGluHalf) * 2 * kGluHalf +
+                               (ti.n0 % kGluHalf) + hc;
+          load_raw32(Hrow + cg, hg[0]);
+          load_raw32(Hrow + cg + kGluHalf, hl[0]);
         }
       }
 
@@ -549,62 +597,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
       if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       // leave together: the store barriers below need all epilogue warps
-      if (named_bar_any(kEpiBar, kEpiThreads, !ok)) break;
+      if (named_bar_any(kEpiBar, kGemmEpiThreads, !ok)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + hc;
 
       if (MODE == kFc1Glu) {
         const __nv_bfloat16* b1 =
-            args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0
+            args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0 + hc
                       : nullptr;
-        uint32_t rg[32], rl[32];
-        tmem_ld32(tbase, rg);
-        tmem_ld32(tbase + kGluHalf, rl);
+        uint32_t rg[16], rl[16];
+        tmem_ld16(tbase, rg);
+        tmem_ld16(tbase + kGluHalf, rl);
 #pragma unroll 1
         for (int j = 0; j < kGluHalf / 32; ++j) {
-          tmem_ld_wait(rg);
-          reg_fence(rl);
+          tmem_ld_wait16(rg);
+          reg_fence16(rl);
           if (j == 1) early_release(acc);             // columns 0-63 read
-          float g[32], l[32];
+          float g[16], l[16];
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             g[i] = __uint_as_float(rg[i]);
             l[i] = __uint_as_float(rl[i]);
           }
           if (j + 1 < kGluHalf / 32) {        // next chunk's accumulator in flight
-            tmem_ld32(tbase + 32 * (j + 1), rg);
-            tmem_ld32(tbase + kGluHalf + 32 * (j + 1), rl);
+            tmem_ld16(tbase + 32 * (j + 1), rg);
+            tmem_ld16(tbase + kGluHalf + 32 * (j + 1), rl);
           }
           if (b1) {
-            float bg[32], bl[32];
-            load_bf16x32(b1 + 32 * j, bg);
-            load_bf16x32(b1 + kGluHalf + 32 * j, bl);
+            float bg[16], bl[16];
+            load_bf16x16(b1 + 32 * j, bg);
+            load_bf16x16(b1 + kGluHalf + 32 * j, bl);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               g[i] += bg[i];
               l[i] += bl[i];
             }
           }
           if (args.out0 != nullptr) {           // H kept for the backward (else recomputed)
-            ring_store<Tr::kNR>(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0, row_local, issuer);
-            ring_store<Tr::kNR>(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j, y0, 0, row_local,
-                       issuer);
+            ring_store_half<Tr::kNR>(ring, g, valid, &args.tma_out0, ti.n0 + 32 * j, y0, 0,
+                                     row_local, half, issuer);
+            ring_store_half<Tr::kNR>(ring, l, valid, &args.tma_out0, ti.n0 + kGluHalf + 32 * j,
+                                     y0, 0, row_local, half, issuer);
           }
           const int f0 = ti.n0 / 2 + 32 * j;
           if (f0 < args.f_real) {
-            float a[32];
+            float a[16];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
+            for (int i = 0; i < 16; ++i) a[i] = glu_fwd<ACT>(g[i], l[i], ap);
             const uint8_t* box = ring_next_box(ring);
             if (args.out1 != nullptr || want_mx)
-              ring_store<Tr::kNR>(ring, a, valid, args.out1 ? &args.tma_out1 : nullptr, f0, y0, 0,
-                                  row_local, issuer);
+              ring_store_half<Tr::kNR>(ring, a, valid, args.out1 ? &args.tma_out1 : nullptr, f0,
+                                       y0, 0, row_local, half, issuer);
             if (want_mx) {                      // MXFP8 / amax of the staged bf16 A
-              mx_block_from_box(mx, box, quarter * 32, y0 + quarter * 32, f0, lane);
+              mx_block_half(mx, box, quarter * 32, y0 + quarter * 32, f0, lane, half);
               if (mx.amax) {
 #pragma unroll
-                for (int i = 0; i < 32; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
-                mx_amax_block(mx, a, lane);
+                for (int i = 0; i < 16; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
+                mx_amax_block16(mx, a, lane);
               }
             }
           }
@@ -613,76 +663,78 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         // tile columns are GLU features n0 .. n0+255; dH in packed layout.
         // Chunks go in pairs so the two H prefetch buffers stay static.
         const int nch = min(BN / 32, (args.f_pad - ti.n0) / 32);   // 4 or 8
-        uint32_t r[32];
-        tmem_ld32(tbase, r);
+        uint32_t r[16];
+        tmem_ld16(tbase, r);
 #pragma unroll 1
         for (int j = 0; j < nch; j += 2) {
           const int f0 = ti.n0 + 32 * j, f1 = f0 + 32, f2 = f0 + 64;
           const int c0 = (f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
           const int c1 = (f1 / kGluHalf) * 2 * kGluHalf + (f1 % kGluHalf);
           const int c2 = (f2 / kGluHalf) * 2 * kGluHalf + (f2 % kGluHalf);
-          float dg[32], dl[32];
+          float dg[16], dl[16];
+          uint32_t ra[16];
           // chunk j (buffer 0); prefetch chunk j+1 into buffer 1
           if (valid && f1 < args.f_real) {
-            load_raw64(Hrow + c1, hg[1]);
-            load_raw64(Hrow + c1 + kGluHalf, hl[1]);
+            load_raw32(Hrow + c1 + hc, hg[1]);
+            load_raw32(Hrow + c1 + hc + kGluHalf, hl[1]);
           }
-          tmem_ld_wait(r);
-          uint32_t ra[32];
+          tmem_ld_wait16(r);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ra[i] = r[i];
-          tmem_ld32(tbase + 32 * (j + 1), r);
+          for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          tmem_ld16(tbase + 32 * (j + 1), r);
           const bool live0 = valid && f0 < args.f_real;
-          if (live0) dglu_compute<ACT>(ra, hg[0], hl[0], ap, dg, dl);
+          if (live0) dglu_compute16<ACT>(ra, hg[0], hl[0], ap, dg, dl);
           {
             const uint8_t* box_g = ring_next_box(ring);
-            ring_store<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, issuer);
-            if (want_mx) mx_block_from_box(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane);
+            ring_store_half<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, half,
+                                     issuer);
+            if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
             const uint8_t* box_l = ring_next_box(ring);
-            ring_store<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0, row_local,
-                                issuer);
+            ring_store_half<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0,
+                                     row_local, half, issuer);
             if (want_mx)
-              mx_block_from_box(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane);
+              mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
           }
           if (want_mx && mx.amax) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               dg[i] = live0 ? bf16_round(dg[i]) : 0.0f;
               dl[i] = live0 ? bf16_round(dl[i]) : 0.0f;
             }
-            mx_amax_block(mx, dg, lane);
-            mx_amax_block(mx, dl, lane);
+            mx_amax_block16(mx, dg, lane);
+            mx_amax_block16(mx, dl, lane);
           }
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
-            load_raw64(Hrow + c2, hg[0]);
-            load_raw64(Hrow + c2 + kGluHalf, hl[0]);
+            load_raw32(Hrow + c2 + hc, hg[0]);
+            load_raw32(Hrow + c2 + hc + kGluHalf, hl[0]);
           }
-          tmem_ld_wait(r);
+          tmem_ld_wait16(r);
           if (j == 0) early_release(acc);             // columns 0-63 read
 #pragma unroll
-          for (int i = 0; i < 32; ++i) ra[i] = r[i];
-          if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), r);
+          for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          if (j + 2 < nch) tmem_ld16(tbase + 32 * (j + 2), r);
           const bool live1 = valid && f1 < args.f_real;
-          if (live1) dglu_compute<ACT>(ra, hg[1], hl[1], ap, dg, dl);
+          if (live1) dglu_compute16<ACT>(ra, hg[1], hl[1], ap, dg, dl);
           {
             const uint8_t* box_g = ring_next_box(ring);
-            ring_store<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, issuer);
-            if (want_mx) mx_block_from_box(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane);
+            ring_store_half<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, half,
+                                     issuer);
+            if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane, half);
             const uint8_t* box_l = ring_next_box(ring);
-            ring_store<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0, row_local,
-                                issuer);
+            ring_store_half<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0,
+                                     row_local, half, issuer);
             if (want_mx)
-              mx_block_from_box(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane);
+              mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane, half);
           }
           if (want_mx && mx.amax) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
               dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
             }
-            mx_amax_block(mx, dg, lane);
-            mx_amax_block(mx, dl, lane);
+            mx_amax_block16(mx, dg, lane);
+            mx_amax_block16(mx, dl, lane);
           }
         }
       } else {
@@ -691,15 +743,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         const bool write = !Tr::kRaggedK || y0 < args.m_ext;   // CTA-uniform
         const __nv_bfloat16* bias =
             (MODE == kFc2 && args.bias)
-                ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld
+                ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + hc
                 : nullptr;
         const int nch = min(BN / 32, (args.n_ext - ti.n0 + 31) / 32);
         // TMEM is read two 32-column chunks per wait; the next pair is in
         // flight while the current one is staged and stored.
-        uint32_t ra[32], rb[32];
+        uint32_t ra[16], rb[16];
         if (has_acc) {
-          tmem_ld32(tbase, ra);
-          if (nch > 1) tmem_ld32(tbase + 32, rb);
+          tmem_ld16(tbase, ra);
+          if (nch > 1) tmem_ld16(tbase + 32, rb);
         } else {
           early_release(acc);
         }
@@ -707,54 +759,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1) k_grouped_gemm(const __grid_co
         for (int j = 0; j < nch; j += 2) {
           const bool two = j + 1 < nch;
           const int c0 = ti.n0 + 32 * j;
-          float v0[32], v1[32];
+          float v0[16], v1[16];
           if (has_acc) {
-            tmem_ld_wait(ra);
-            reg_fence(rb);
+            tmem_ld_wait16(ra);
+            reg_fence16(rb);
             if (j == 0) early_release(acc);           // columns 0-63 read (or all there are)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               v0[i] = __uint_as_float(ra[i]);
               v1[i] = __uint_as_float(rb[i]);
             }
-            if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), ra);
-            if (j + 3 < nch) tmem_ld32(tbase + 32 * (j + 3), rb);
+            if (j + 2 < nch) tmem_ld16(tbase + 32 * (j + 2), ra);
+            if (j + 3 < nch) tmem_ld16(tbase + 32 * (j + 3), rb);
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
+            for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.0f;
           }
           if (bias && valid) {
-            float b[32];
-            load_bf16x32(bias + c0, b);
+            float b[16];
+            load_bf16x16(bias + c0, b);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v0[i] += b[i];
+            for (int i = 0; i < 16; ++i) v0[i] += b[i];
             if (two) {
-              load_bf16x32(bias + c0 + 32, b);
+              load_bf16x16(bias + c0 + 32, b);
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v1[i] += b[i];
+              for (int i = 0; i < 16; ++i) v1[i] += b[i];
             }
           }
           const uint8_t* box0 = ring_next_box(ring);
           const uint8_t* box1 = box0;
           if (write) {
-            ring_store<Tr::kNR>(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
-                       Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+            ring_store_half<Tr::kNR>(ring, v0, Tr::kRaggedK || valid, &args.tma_out0, c0, y0,
+                                     Tr::kRaggedK ? ti.e : 0, row_local, half, issuer);
             box1 = ring_next_box(ring);
             if (two)
-              ring_store<Tr::kNR>(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32, y0,
-                         Tr::kRaggedK ? ti.e : 0, row_local, issuer);
+              ring_store_half<Tr::kNR>(ring, v1, Tr::kRaggedK || valid, &args.tma_out0, c0 + 32,
+                                       y0, Tr::kRaggedK ? ti.e : 0, row_local, half, issuer);
           }
           if (MODE == kFc2 && want_mx) {        // MXFP8 / amax of the staged bf16 Y
-            mx_block_from_box(mx, box0, quarter * 32, y0 + quarter * 32, c0, lane);
-            if (two) mx_block_from_box(mx, box1, quarter * 32, y0 + quarter * 32, c0 + 32, lane);
+            mx_block_half(mx, box0, quarter * 32, y0 + quarter * 32, c0, lane, half);
+            if (two) mx_block_half(mx, box1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
             if (mx.amax) {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
+              for (int i = 0; i < 16; ++i) {
                 v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
                 v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
               }
-              mx_amax_block(mx, v0, lane);
-              if (two) mx_amax_block(mx, v1, lane);
+              mx_amax_block16(mx, v0, lane);
+              if (two) mx_amax_block16(mx, v1, lane);
             }
           }
         }
@@ -1032,7 +1084,7 @@ cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<MODE, ACT, MX><<<grid, NUM_THREADS, smem, s>>>(args);
+  k_grouped_gemm<MODE, ACT, MX><<<grid, GEMM_THREADS, smem, s>>>(args);
   return cudaGetLastError();
 }
 

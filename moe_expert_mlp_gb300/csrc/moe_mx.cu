@@ -52,49 +52,134 @@ __global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in
   }
 }
 
-// bf16 [batch][rows][cols] -> MXFP8, one warp per 32 x 32 block,
-// consecutive warps on consecutive column blocks of the same rows.  The
-// block is read coalesced (lane l: 16-byte chunk l % 4 of rows l / 4 + 8k)
-// into the warp's shared box (64-byte rows, 64-byte swizzle), from which
-// lane l quantizes row l and column l.  Rowwise codes [batch][rows][cols];
-// columnwise codes written transposed [batch][cols][rows]; scales row-major
-// or in the MMA layout.
+// bf16 [batch][rows][cols] -> MXFP8 (rows, cols multiples of 32).  One CTA
+// (8 warps) per 128 x 128 tile: the tile is loaded coalesced into four
+// shared boxes of 128 rows x 32 columns (64-byte rows, 64-byte swizzle);
+// each warp quantizes 32 x 32 blocks rowwise (lane = row) or columnwise
+// (lane = column) into shared code tiles; the codes then leave as whole
+// 128-byte lines and, in the MMA scale layout, each tile's scales as one
+// 512-byte atom per direction.  Rowwise codes [batch][rows][cols];
+// columnwise codes transposed [batch][cols][rows].
+constexpr int kQT = 128;                       // tile edge
+constexpr int kQuantSmem = 4 * 8192 + 2 * kQT * kQT + 2 * 512;
+
+__device__ __forceinline__ void quant_block_to_smem(const float (&v)[32], uint8_t* code_row,
+                                                    int line, int c32, uint8_t& scale) {
+  // codes of one block row (32 bytes) into line `line` of a 128 x 128 code
+  // tile at column c32*32; 16-byte chunks swizzled by (line & 7)
+  uint32_t w[8];
+  scale = mx_quant32_words(v, w);
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int ch = (c32 * 2 + h) ^ (line & 7);
+    *reinterpret_cast<uint4*>(code_row + line * kQT + ch * 16) =
+        make_uint4(w[4 * h], w[4 * h + 1], w[4 * h + 2], w[4 * h + 3]);
+  }
+}
+
 __global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restrict__ in,
                                                     long long batch, long long rows,
                                                     long long cols, uint8_t* q, uint8_t* s,
                                                     uint8_t* qt, uint8_t* st, int mma_layout,
                                                     const int32_t* row_limit) {
-  __shared__ __align__(128) uint8_t boxes[8][32 * 64];
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  uint8_t* const box = boxes[wid];
-  const long long rbn = rows / 32, cbn = cols / 32;
-  const long long per_batch = rbn * cbn;
-  const long long nblk = batch * per_batch;
+  extern __shared__ __align__(1024) uint8_t qsm[];
+  uint8_t* boxes = qsm;                              // 4 x [128][64 B]
+  uint8_t* code_r = qsm + 4 * 8192;                  // [128 rows][128 B]
+  uint8_t* code_c = code_r + kQT * kQT;              // [128 cols][128 B]
+  uint8_t* atom_r = code_c + kQT * kQT;              // scale atoms (MMA layout)
+  uint8_t* atom_c = atom_r + 512;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  const long long rtn = (rows + kQT - 1) / kQT, ctn = (cols + kQT - 1) / kQT;
+  const long long ntiles = batch * rtn * ctn;
   const long long s_bytes = mma_layout ? (cols + 127) / 128 * sf_row_atoms(rows) * 512
                                        : rows * cols / 32;
   const long long st_bytes = mma_layout ? (rows + 127) / 128 * sf_row_atoms(cols) * 512
                                         : rows * cols / 32;
-  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x / 32);
   const long long rlim = row_limit ? __ldg(row_limit) : rows;   // rows past it are skipped
-  for (long long w = blockIdx.x * static_cast<long long>(blockDim.x / 32) + wid; w < nblk;
-       w += warps) {
-    const long long b = w / per_batch;
-    const long long rem = w - b * per_batch;
-    const long long rb = rem / cbn, cb = rem - rb * cbn;
-    if (rb * 32 >= rlim) continue;
-    const __nv_bfloat16* src = in + (b * rows + rb * 32) * cols + cb * 32;
-    __syncwarp();                       // the previous block's reads are done
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int r = (lane >> 2) + 8 * k, ch = lane & 3;
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(src + r * cols) + ch);
-      *reinterpret_cast<uint4*>(box + r * 64 + ((ch ^ ((r >> 1) & 3)) << 4)) = v;
+  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
+    const long long b = t / (rtn * ctn);
+    const long long rem = t - b * rtn * ctn;
+    const long long r0 = (rem / ctn) * kQT, c0 = (rem % ctn) * kQT;
+    if (r0 >= rlim) continue;                        // uniform across the CTA
+    const int nr = static_cast<int>(min(static_cast<long long>(kQT), rows - r0));   // multiples of 32
+    const int nc = static_cast<int>(min(static_cast<long long>(kQT), cols - c0));
+    __syncthreads();                                 // previous tile fully stored
+    // load: thread -> 16-byte chunk (row i / 16, chunk i % 16 of 256 bytes)
+    for (int i = tid; i < kQT * 16; i += 256) {
+      const int r = i >> 4, ch = i & 15;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < nr && ch * 8 < nc)
+        v = __ldg(reinterpret_cast<const uint4*>(in + (b * rows + r0 + r) * cols + c0) + ch);
+      *reinterpret_cast<uint4*>(boxes + (ch >> 2) * 8192 + r * 64 +
+                                (((ch & 3) ^ ((r >> 1) & 3)) << 4)) = v;
     }
-    __syncwarp();
-    const MxOut mx{q ? q + b * rows * cols : nullptr, s ? s + b * s_bytes : nullptr,
-                   qt ? qt + b * rows * cols : nullptr, st ? st + b * st_bytes : nullptr,
-                   nullptr, cols, rows, mma_layout};
-    mx_block_from_box(mx, box, 0, rb * 32, static_cast<int>(cb * 32), lane);
+    for (int i = tid; i < 1024; i += 256) atom_r[i] = 0;   // both atoms
+    __syncthreads();
+    // quantize: 16 blocks x {rowwise, columnwise}; warp w takes items w + 8k
+    for (int item = wid; item < 32; item += 8) {
+      const int colwise = item >> 4, blk = item & 15;
+      const int bi = blk >> 2, bj = blk & 3;         // block row / column in the tile
+      if (bi * 32 >= nr || bj * 32 >= nc) continue;  // warp-uniform
+      if ((colwise ? qt : q) == nullptr) continue;
+      const uint8_t* box = boxes + bj * 8192;
+      float v[32];
+      if (!colwise) {
+        const int r = bi * 32 + lane;
+        const uint4* rowp = reinterpret_cast<const uint4*>(box + r * 64);
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          const uint4 w4 = rowp[c4 ^ ((r >> 1) & 3)];
+          const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            v[8 * c4 + 2 * k] = __uint_as_float(w[k] << 16);
+            v[8 * c4 + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+          }
+        }
+        uint8_t sc;
+        quant_block_to_smem(v, code_r, r, bj, sc);
+        if (mma_layout)
+          atom_r[(r & 31) * 16 + (r >> 5) * 4 + bj] = sc;
+        else
+          s[b * s_bytes + (r0 + r) * (cols / 32) + c0 / 32 + bj] = sc;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int r = bi * 32 + i;
+          const uint16_t h = *reinterpret_cast<const uint16_t*>(
+              box + r * 64 + ((((lane >> 3) ^ ((r >> 1) & 3))) << 4) + (lane & 7) * 2);
+          v[i] = __uint_as_float(static_cast<uint32_t>(h) << 16);
+        }
+        const int c = bj * 32 + lane;                // column inside the tile
+        uint8_t sc;
+        quant_block_to_smem(v, code_c, c, bi, sc);
+        if (mma_layout)
+          atom_c[(c & 31) * 16 + (c >> 5) * 4 + bi] = sc;
+        else
+          st[b * st_bytes + (c0 + c) * (rows / 32) + r0 / 32 + bi] = sc;
+      }
+    }
+    __syncthreads();
+    // store codes as whole lines: thread -> 16-byte chunk (line i / 8)
+    for (int i = tid; i < kQT * 8; i += 256) {
+      const int line = i >> 3, ch = i & 7;
+      const int sch = ch ^ (line & 7);
+      if (q && line < nr && ch * 16 < nc)
+        *reinterpret_cast<uint4*>(q + (b * rows + r0 + line) * cols + c0 + ch * 16) =
+            *reinterpret_cast<const uint4*>(code_r + line * kQT + sch * 16);
+      if (qt && line < nc && ch * 16 < nr)
+        *reinterpret_cast<uint4*>(qt + (b * cols + c0 + line) * rows + r0 + ch * 16) =
+            *reinterpret_cast<const uint4*>(code_c + line * kQT + sch * 16);
+    }
+    if (mma_layout && tid < 64) {                    // one 512-byte atom per direction
+      const int h = tid >> 5, k = tid & 31;
+      if (h == 0 && q)
+        reinterpret_cast<uint4*>(s + b * s_bytes + sf_mma_offset(r0, c0 / 32, sf_row_atoms(rows)))[k] =
+            reinterpret_cast<const uint4*>(atom_r)[k];
+      if (h == 1 && qt)
+        reinterpret_cast<uint4*>(st + b * st_bytes + sf_mma_offset(c0, r0 / 32, sf_row_atoms(cols)))[k] =
+            reinterpret_cast<const uint4*>(atom_c)[k];
+    }
   }
 }
 
@@ -104,11 +189,14 @@ cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows
                                  uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
                                  int mma_layout, const int32_t* row_limit, int num_sms,
                                  cudaStream_t stream) {
-  const long long nblk = batch * (rows / 32) * (cols / 32);
-  if (nblk == 0) return cudaSuccess;
-  long long grid = (nblk + 7) / 8;
-  if (grid > static_cast<long long>(num_sms) * 16) grid = static_cast<long long>(num_sms) * 16;
-  k_quant_bf16<<<static_cast<int>(grid), 256, 0, stream>>>(
+  const long long ntiles = batch * ((rows + kQT - 1) / kQT) * ((cols + kQT - 1) / kQT);
+  if (ntiles == 0) return cudaSuccess;
+  cudaError_t err = cudaFuncSetAttribute(k_quant_bf16, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kQuantSmem);
+  if (err != cudaSuccess) return err;
+  long long grid = ntiles;
+  if (grid > static_cast<long long>(num_sms) * 3) grid = static_cast<long long>(num_sms) * 3;
+  k_quant_bf16<<<static_cast<int>(grid), 256, kQuantSmem, stream>>>(
       static_cast<const __nv_bfloat16*>(in), batch, rows, cols, q, s, qt, st, mma_layout,
       row_limit);
   return cudaGetLastError();

@@ -46,29 +46,36 @@ __device__ __forceinline__ uint32_t e4m3x2(float a, float b) {
   return static_cast<uint32_t>(r);
 }
 
-// Quantize one block of 32 values: writes 32 codes (16-byte aligned
-// destination) and returns the E8M0 scale code.
-__device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* q) {
+// Quantize one block of 32 values into eight 32-bit words of codes (code i
+// in byte i % 4 of word i / 4); returns the E8M0 scale code.
+__device__ __forceinline__ uint8_t mx_quant32_words(const float (&v)[32], uint32_t (&w)[8]) {
   float m[16];                                   // block max as a tree (depth 5)
 #pragma unroll
   for (int i = 0; i < 16; ++i) m[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1)
+  for (int k = 8; k >= 1; k >>= 1)
 #pragma unroll
-    for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    for (int i = 0; i < k; ++i) m[i] = fmaxf(m[i], m[i + k]);
   const int s = mx_scale_exponent(m[0]);
   const float inv = mx_inv_scale(s);
-  uint32_t w[8];
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     const uint32_t lo = e4m3x2(v[4 * j] * inv, v[4 * j + 1] * inv);
     const uint32_t hi = e4m3x2(v[4 * j + 2] * inv, v[4 * j + 3] * inv);
     w[j] = lo | (hi << 16);
   }
+  return static_cast<uint8_t>(s + 127);
+}
+
+// Quantize one block of 32 values: writes 32 codes (16-byte aligned
+// destination) and returns the E8M0 scale code.
+__device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* q) {
+  uint32_t w[8];
+  const uint8_t sc = mx_quant32_words(v, w);
   uint4* d = reinterpret_cast<uint4*>(q);
   d[0] = make_uint4(w[0], w[1], w[2], w[3]);
   d[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  return static_cast<uint8_t>(s + 127);
+  return sc;
 }
 
 // Non-negative float max into a global word (bit patterns of non-negative
@@ -150,33 +157,6 @@ __device__ __forceinline__ void mx_block_from_box(const MxOut& mx, const uint8_t
     const uint8_t sc = mx_quant32(v, mx.qt + c * mx.cap + r0);
     mx.st[mx.mma_layout ? sf_mma_offset(c, r0 / 32, sf_row_atoms(mx.width))
                         : c * (mx.cap / 32) + r0 / 32] = sc;
-  }
-}
-
-// The per-tensor amax outputs of a 32 x 32 block held one row per lane in v
-// (bf16-rounded values, zero on padding rows): plain amax and the amax of
-// the 16-row Walsh-Hadamard rotation (H16 / 4) of each column segment.
-__device__ __forceinline__ void mx_amax_block(const MxOut& mx, const float (&v)[32], int lane) {
-  float m = 0.0f, h = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 32; ++i) {
-    m = fmaxf(m, fabsf(v[i]));
-    float x = v[i];
-#pragma unroll
-    for (int b = 1; b < 16; b <<= 1) {
-      const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
-      x = (lane & b) ? (p - x) : (x + p);
-    }
-    h = fmaxf(h, fabsf(x) * 0.25f);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    h = fmaxf(h, __shfl_xor_sync(0xFFFFFFFFu, h, o));
-  }
-  if (lane == 0) {
-    atomic_max_nonneg(mx.amax, m);
-    atomic_max_nonneg(mx.amax + 1, h);
   }
 }
 

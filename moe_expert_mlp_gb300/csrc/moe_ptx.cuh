@@ -326,6 +326,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
       : "r"(taddr));
 }
 
+// 32 lanes x 16 consecutive 32-bit TMEM columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]),
+                 "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]),
+                 "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]));
+}
+
+// Wait for outstanding TMEM loads; `r` is tied to the wait.
+__device__ __forceinline__ void tmem_ld_wait16(uint32_t (&r)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  reg_fence16(r);
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -489,6 +513,30 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&v)[3
 }
 
 // Load 32 bf16 (64 contiguous bytes, 16-byte aligned) as fp32.
+__device__ __forceinline__ void load_raw32(const void* src, uint4 (&w)[2]) {
+  const uint4* p = reinterpret_cast<const uint4*>(src);
+  w[0] = __ldg(p);
+  w[1] = __ldg(p + 1);
+}
+
+__device__ __forceinline__ void unpack_bf16x16(const uint4 (&w)[2], float (&v)[16]) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t x[4] = {w[q].x, w[q].y, w[q].z, w[q].w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      v[8 * q + 2 * k] = bf16_lo(x[k]);
+      v[8 * q + 2 * k + 1] = bf16_hi(x[k]);
+    }
+  }
+}
+
+__device__ __forceinline__ void load_bf16x16(const void* src, float (&v)[16]) {
+  uint4 w[2];
+  load_raw32(src, w);
+  unpack_bf16x16(w, v);
+}
+
 __device__ __forceinline__ void load_bf16x32(const void* src, float (&v)[32]) {
   const uint4* p = reinterpret_cast<const uint4*>(src);
 #pragma unroll
