@@ -23,6 +23,8 @@ Engine" refer to):
   clamp 7.0, gate scale alpha=1.702, linear offset 1, biases ~N(0,0.01).
 * ``dense_m16384``      one group of 16384 rows, d=4096, F=14336 (a dense
   MLP); the activation is chosen per run.
+* ``dsv3_r4096_e8``     the DeepSeek-shaped layer cut to 8 experts / 4096
+  rows (one empty), for hardware-counter captures.
 
 Unstated scales are read as: x ~ N(0,1), expert weights ~ N(0,0.02),
 upstream gradient ~ N(0,1).
@@ -93,6 +95,12 @@ WORKLOADS = {
         b_std=0.01),
     "dense_m16384": Workload(
         name="dense_m16384", R=16384, E=1, d=4096, F=14336, router="direct"),
+    # the DeepSeek-shaped layer cut to 8 experts and 4096 rows (same d, F and
+    # group-size law, about 2 GB on the device in MXFP8): small enough for
+    # per-kernel hardware-counter captures
+    "dsv3_r4096_e8": Workload(
+        name="dsv3_r4096_e8", R=4096, E=8, d=7168, F=2048, router="direct",
+        zipf_s=1.2, zipf_empty=1, w_std=0.006),
 }
 
 
