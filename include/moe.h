@@ -90,7 +90,15 @@ typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2 } moe_dtype_t;
  *   GEGLU:  A = s * 0.5*g'*(1+erf(g'/sqrt2)) * (l' + linear_offset)
  *   SREGLU: A = s * max(g',0)^2 * (l' + linear_offset)   (gated squared ReLU)
  * where s = out_scale.  alpha applies to SWIGLU only. */
-typedef enum { MOE_ACT_SWIGLU = 0, MOE_ACT_GEGLU = 1, MOE_ACT_SREGLU = 3 } moe_act_t;
+typedef enum {
+  MOE_ACT_SWIGLU = 0,
+  MOE_ACT_GEGLU = 1,
+  /* non-gated squared ReLU: FC1 has F outputs (no linear half, no packing:
+   * the "packed" FC1 weight is the plain [E,F,d] one and every FC1-shaped
+   * tensor is F wide); A = s * max(min(h, limit), 0)^2 */
+  MOE_ACT_SRELU = 2,
+  MOE_ACT_SREGLU = 3
+} moe_act_t;
 
 typedef struct {
   int32_t T;            /* tokens (routing calls; 0 when groups come directly) */

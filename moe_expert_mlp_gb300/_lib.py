@@ -21,7 +21,7 @@ MOE_DTYPE_BF16 = 1
 MOE_DTYPE_MXFP8 = 2
 MOE_MX_SCALES_ROWMAJOR = 0
 MOE_MX_SCALES_MMA = 1
-ACTS = {"swiglu": 0, "geglu": 1, "sreglu": 3}
+ACTS = {"swiglu": 0, "geglu": 1, "srelu": 2, "sreglu": 3}
 
 EXPORTS = (
     "moe_fc1_padded_width", "moe_workspace_size", "moe_repack_fc1", "moe_unpack_fc1",

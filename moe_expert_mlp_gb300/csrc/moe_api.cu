@@ -108,7 +108,8 @@ moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
   if (d->F < 32 || d->F % 32 != 0) return MOE_ERR_SHAPE;
   if (d->align != kAlign) return MOE_ERR_UNSUPPORTED;
   if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8) return MOE_ERR_UNSUPPORTED;
-  if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU)
+  if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU &&
+      d->act != MOE_ACT_SRELU)
     return MOE_ERR_UNSUPPORTED;
   if (d->capacity < kAlign || d->capacity % kAlign != 0) return MOE_ERR_SHAPE;
   if (d->sm_margin < 0) return MOE_ERR_SHAPE;
@@ -237,7 +238,7 @@ moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes) {
   if (st != MOE_OK) return st;
   *bytes = route_ws_bytes(desc) + 256;
   if (desc->recompute_h)
-    *bytes += static_cast<size_t>(desc->capacity) * 2 * fc1_pad(desc->F) * 2 + 256;
+    *bytes += static_cast<size_t>(desc->capacity) * fc1_width(desc->act, desc->F) * 2 + 256;
   return MOE_OK;
 }
 
@@ -249,7 +250,14 @@ moe_status_t moe_repack_fc1(const moe_mlp_desc_t* desc, const void* w1, const vo
   if ((b1 == nullptr) != (b1p == nullptr)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  cudaError_t e = launch_repack_fc1(w1, w1p, desc->E, desc->F, desc->d, stream);
+  cudaError_t e;
+  if (desc->act == MOE_ACT_SRELU) {   // no halves to interleave: a plain copy
+    const size_t n = static_cast<size_t>(desc->E) * desc->F;
+    e = cudaMemcpyAsync(w1p, w1, n * desc->d * 2, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && b1) e = cudaMemcpyAsync(b1p, b1, n * 2, cudaMemcpyDeviceToDevice, stream);
+    return cuda_status(e);
+  }
+  e = launch_repack_fc1(w1, w1p, desc->E, desc->F, desc->d, stream);
   if (e == cudaSuccess && b1) e = launch_repack_fc1(b1, b1p, desc->E, desc->F, 1, stream);
   return cuda_status(e);
 }
@@ -262,6 +270,10 @@ moe_status_t moe_unpack_fc1(const moe_mlp_desc_t* desc, const void* w1p, void* w
   if (rows_width < 1) return MOE_ERR_SHAPE;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU)
+    return cuda_status(cudaMemcpyAsync(w1, w1p,
+                                       static_cast<size_t>(desc->E) * desc->F * rows_width * 2,
+                                       cudaMemcpyDeviceToDevice, stream));
   return cuda_status(launch_unpack_fc1(w1p, w1, desc->E, desc->F, rows_width, stream));
 }
 
@@ -328,26 +340,28 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
-      (h && !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1)) ||
+      !encode_map(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 64, 256) ||
+      (h && !encode_out(&g.tma_out0, h, W1, cap, 1)) ||
       !encode_out(&g.tma_out1, a, F, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(2 * Fp);
+  g.n_ext = static_cast<int>(W1);
   g.b_ext = g.n_ext;
   g.out0 = h;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.out1 = a;
   g.ld1 = F;
   g.bias = desc->has_b1 ? b1p : nullptr;
-  g.bias_ld = 2 * Fp;
+  g.bias_ld = W1;
   if ((st = set_mx(g, a_mx, desc->F, stream)) != MOE_OK) return st;
-  return cuda_status(launch_grouped_gemm(kFc1Glu, g, grid_for(di, desc), stream));
+  return cuda_status(launch_grouped_gemm(desc->act == MOE_ACT_SRELU ? kFc1Act : kFc1Glu, g,
+                                         grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
@@ -431,26 +445,28 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
   if (!dy || !h || !counts || !padded_offsets || !w2 || !dh) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dA = dY W2 with W2 [d,F] read MN-major (F contiguous); dH from H
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
+      !encode_out(&g.tma_out0, dh, W1, cap, 1))
     return MOE_ERR_SHAPE;
   g.b_atoms4d = encode_mn_atoms(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 4);
   if (!g.b_atoms4d && !encode_map(&g.tma_b, w2, F, d, E, F * 2, d * F * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(Fp);
+  g.n_ext = desc->act == MOE_ACT_SRELU ? desc->F : static_cast<int>(Fp);
   g.b_ext = desc->F;
   g.out0 = dh;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.aux = h;
-  g.ld_aux = 2 * Fp;
-  if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
-  return cuda_status(launch_grouped_gemm(kDgradDglu, g, grid_for(di, desc), stream));
+  g.ld_aux = W1;
+  if ((st = set_mx(g, dh_mx, W1, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm(desc->act == MOE_ACT_SRELU ? kDgradAct : kDgradDglu, g,
+                                         grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
@@ -490,19 +506,20 @@ moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int
   if (!dh || !counts || !padded_offsets || !w1p || !dx_perm) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dX = dH W1p with W1p [2F_pad,d] read MN-major (d contiguous)
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 128) ||
+  if (!encode_map(&g.tma_a, dh, W1, cap, 1, W1 * 2, cap * W1 * 2, 64, 128) ||
       !encode_out(&g.tma_out0, dx_perm, d, cap, 1) ||
       !encode_out2(&g.tma_out2, dx_perm, d, cap, 1))
     return MOE_ERR_SHAPE;
-  g.b_atoms4d = encode_mn_atoms(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 4);
-  if (!g.b_atoms4d && !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 64))
+  g.b_atoms4d = encode_mn_atoms(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 4);
+  if (!g.b_atoms4d && !encode_map(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 64, 64))
     return MOE_ERR_SHAPE;
-  g.K = static_cast<int>(2 * Fp);
+  g.K = static_cast<int>(W1);
   g.n_ext = desc->d;
   g.b_ext = desc->d;
   g.out0 = dx_perm;
@@ -518,22 +535,23 @@ moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const voi
   if (!dh || !x_perm || !counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dW1p[e] (2F_pad x d) = sum over the group's rows of dH^T X
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E) ||
-      !encode_out2(&g.tma_out2, dw1p, d, 2 * Fp, E))
+  if (!encode_out(&g.tma_out0, dw1p, d, W1, E) ||
+      !encode_out2(&g.tma_out2, dw1p, d, W1, E))
     return MOE_ERR_SHAPE;
-  g.a_atoms4d = encode_mn_atoms(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 2);
+  g.a_atoms4d = encode_mn_atoms(&g.tma_a, dh, W1, cap, 1, W1 * 2, cap * W1 * 2, 2);
   if (!g.a_atoms4d &&
-      !encode_map(&g.tma_a, dh, 2 * Fp, cap, 1, 2 * Fp * 2, cap * 2 * Fp * 2, 64, 64))
+      !encode_map(&g.tma_a, dh, W1, cap, 1, W1 * 2, cap * W1 * 2, 64, 64))
     return MOE_ERR_SHAPE;
   g.b_atoms4d = encode_mn_atoms(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 2);
   if (!g.b_atoms4d && !encode_map(&g.tma_b, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 64))
     return MOE_ERR_SHAPE;
-  g.m_ext = static_cast<int>(2 * Fp);
+  g.m_ext = static_cast<int>(W1);
   g.n_ext = desc->d;
   g.b_ext = desc->d;
   g.out0 = dw1p;
@@ -552,7 +570,7 @@ moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const vo
   cudaError_t e = cudaSuccess;
   if (db2) e = launch_group_colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream);
   if (e == cudaSuccess && db1p)
-    e = launch_group_colsum(dh, counts, padded_offsets, desc->E, 2 * fc1_pad(desc->F), db1p,
+    e = launch_group_colsum(dh, counts, padded_offsets, desc->E, fc1_width(desc->act, desc->F), db1p,
                             stream);
   return cuda_status(e);
 }
@@ -602,26 +620,28 @@ moe_status_t moe_fc1_glu_fwd_unfused(const moe_mlp_desc_t* desc, const void* x_p
                                      cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
   if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // plain grouped GEMM H = X W1p^T (+b1): the FC2-shaped kernel with W1p as B
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
-      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out2(&g.tma_out2, h, 2 * Fp, cap, 1))
+      !encode_map(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, h, W1, cap, 1) || !encode_out2(&g.tma_out2, h, W1, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(2 * Fp);
+  g.n_ext = static_cast<int>(W1);
   g.b_ext = g.n_ext;
   g.out0 = h;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.bias = desc->has_b1 ? b1p : nullptr;
-  g.bias_ld = 2 * Fp;
+  g.bias_ld = W1;
   cudaError_t e = launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream);
   if (e == cudaSuccess)
     e = launch_glu_rows(h, counts, padded_offsets, desc->E, desc->F, static_cast<int>(Fp), a,
@@ -639,21 +659,22 @@ moe_status_t moe_fc1_recompute_h(const moe_mlp_desc_t* desc, const void* x_perm,
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   GemmArgs g;   // the FC2-shaped plain kernel with W1p as B
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
-      !encode_map(&g.tma_b, w1p, d, 2 * Fp, E, d * 2, 2 * Fp * d * 2, 64, 256) ||
-      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) || !encode_out2(&g.tma_out2, h, 2 * Fp, cap, 1))
+      !encode_map(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 64, 256) ||
+      !encode_out(&g.tma_out0, h, W1, cap, 1) || !encode_out2(&g.tma_out2, h, W1, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(2 * Fp);
+  g.n_ext = static_cast<int>(W1);
   g.b_ext = g.n_ext;
   g.out0 = h;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.bias = desc->has_b1 ? b1p : nullptr;
-  g.bias_ld = 2 * Fp;
+  g.bias_ld = W1;
   return cuda_status(launch_grouped_gemm(kFc2, g, grid_for(di, desc), stream));
 }
 
@@ -663,10 +684,12 @@ moe_status_t moe_fc2_dgrad_dglu_unfused(const moe_mlp_desc_t* desc, const void* 
                                         void* dh, cudaStream_t stream) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
   if (!dy || !h || !counts || !padded_offsets || !w2 || !da || !dh) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // plain grouped GEMM dA = dY W2: the FC1-dgrad-shaped kernel with W2 as B
   GemmArgs g;
@@ -843,8 +866,9 @@ moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p
   if (!w1p || !w2 || !mx_weights_ok(out)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const long long E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
-  cudaError_t e = launch_quant_bf16_mx(w1p, E, 2 * Fp, d, out->w1, out->w1_s, out->w1t,
+  const long long E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
+  cudaError_t e = launch_quant_bf16_mx(w1p, E, W1, d, out->w1, out->w1_s, out->w1t,
                                        out->w1t_s, 1, nullptr, di->sms, stream);
   if (e == cudaSuccess)
     e = launch_quant_bf16_mx(w2, E, d, F, out->w2, out->w2_s, out->w2t, out->w2t_s, 1, nullptr,
@@ -863,28 +887,30 @@ moe_status_t moe_fc1_glu_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
   if (!mx_ok(x_mx, true, false) || !mx_ok(a_mx, true, a_mx && a_mx->qt)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // x_perm (codes [cap, d]) x W1p (codes [E, 2F_pad, d]); GLU epilogue
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
-      !encode_u8(&g.tma_b, w->w1, d, 2 * Fp, E, 256) ||
-      !encode_out(&g.tma_out0, h, 2 * Fp, cap, 1) ||
+      !encode_u8(&g.tma_b, w->w1, d, W1, E, 256) ||
+      !encode_out(&g.tma_out0, h, W1, cap, 1) ||
       (a && !encode_out(&g.tma_out1, a, F, cap, 1)))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(2 * Fp);
+  g.n_ext = static_cast<int>(W1);
   g.b_ext = g.n_ext;
   g.out0 = h;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.out1 = a;
   g.ld1 = F;
   g.bias = desc->has_b1 ? b1p : nullptr;
-  g.bias_ld = 2 * Fp;
-  set_scales(g, x_mx->scale, cap, w->w1_s, 2 * Fp, sf_bytes(2 * Fp, d));
+  g.bias_ld = W1;
+  set_scales(g, x_mx->scale, cap, w->w1_s, W1, sf_bytes(W1, d));
   if ((st = set_mx(g, a_mx, desc->F, stream)) != MOE_OK) return st;
-  return cuda_status(launch_grouped_gemm_mx(kFc1Glu, g, grid_for(di, desc), stream));
+  return cuda_status(launch_grouped_gemm_mx(desc->act == MOE_ACT_SRELU ? kFc1Act : kFc1Glu, g,
+                                            grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_mx,
@@ -927,25 +953,27 @@ moe_status_t moe_fc2_dgrad_dglu_mx(const moe_mlp_desc_t* desc, const moe_mx_out_
   if (!mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dY (codes [cap, d]) x W2^T (codes [E, F, d]); dGLU epilogue reads H
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
       !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) ||
-      !encode_out(&g.tma_out0, dh, 2 * Fp, cap, 1))
+      !encode_out(&g.tma_out0, dh, W1, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
-  g.n_ext = static_cast<int>(Fp);
+  g.n_ext = desc->act == MOE_ACT_SRELU ? desc->F : static_cast<int>(Fp);
   g.b_ext = desc->F;
   g.out0 = dh;
-  g.ld0 = 2 * Fp;
+  g.ld0 = W1;
   g.aux = h;
-  g.ld_aux = 2 * Fp;
+  g.ld_aux = W1;
   set_scales(g, dy_mx->scale, cap, w->w2t_s, F, sf_bytes(F, d));
-  if ((st = set_mx(g, dh_mx, 2 * Fp, stream)) != MOE_OK) return st;
-  return cuda_status(launch_grouped_gemm_mx(kDgradDglu, g, grid_for(di, desc), stream));
+  if ((st = set_mx(g, dh_mx, W1, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm_mx(desc->act == MOE_ACT_SRELU ? kDgradAct : kDgradDglu,
+                                            g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_mx,
@@ -983,21 +1011,22 @@ moe_status_t moe_fc1_dgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
   if (!mx_ok(dh_mx, true, false)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dH (codes [cap, 2F_pad]) x W1p^T (codes [E, d, 2F_pad])
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_u8(&g.tma_a, dh_mx->q, 2 * Fp, cap, 1, 128) ||
-      !encode_u8(&g.tma_b, w->w1t, 2 * Fp, d, E, 256) ||
+  if (!encode_u8(&g.tma_a, dh_mx->q, W1, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w1t, W1, d, E, 256) ||
       !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
     return MOE_ERR_SHAPE;
-  g.K = static_cast<int>(2 * Fp);
+  g.K = static_cast<int>(W1);
   g.n_ext = desc->d;
   g.b_ext = desc->d;
   g.out0 = dx_perm;
   g.ld0 = d;
-  set_scales(g, dh_mx->scale, cap, w->w1t_s, d, sf_bytes(d, 2 * Fp));
+  set_scales(g, dh_mx->scale, cap, w->w1t_s, d, sf_bytes(d, W1));
   return cuda_status(launch_grouped_gemm_mx(kDgradFc1, g, grid_for(di, desc), stream));
 }
 
@@ -1010,21 +1039,22 @@ moe_status_t moe_fc1_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
   if (!mx_ok(dh_mx, false, true) || !mx_ok(x_mx, false, true)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F);
+  const uint64_t E = desc->E, d = desc->d, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
   // dW1p[e] = dH^T X over the group's rows: codes [2F_pad, cap] and [d, cap]
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
-  if (!encode_u8(&g.tma_a, dh_mx->qt, cap, 2 * Fp, 1, 128) ||
+  if (!encode_u8(&g.tma_a, dh_mx->qt, cap, W1, 1, 128) ||
       !encode_u8(&g.tma_b, x_mx->qt, cap, d, 1, 256) ||
-      !encode_out(&g.tma_out0, dw1p, d, 2 * Fp, E))
+      !encode_out(&g.tma_out0, dw1p, d, W1, E))
     return MOE_ERR_SHAPE;
-  g.m_ext = static_cast<int>(2 * Fp);
+  g.m_ext = static_cast<int>(W1);
   g.n_ext = desc->d;
   g.b_ext = desc->d;
   g.out0 = dw1p;
   g.ld0 = d;
-  set_scales(g, dh_mx->scale_t, 2 * Fp, x_mx->scale_t, d, 0);
+  set_scales(g, dh_mx->scale_t, W1, x_mx->scale_t, d, 0);
   return cuda_status(launch_grouped_gemm_mx(kWgrad, g, grid_for(di, desc), stream));
 }
 

@@ -108,6 +108,18 @@ __device__ __forceinline__ float glu_fwd(float g, float l, const ActP& p) {
   return p.out_scale * phi * (lc + p.lin_off);
 }
 
+// Non-gated squared ReLU: A = s * max(min(h, limit), 0)^2 and its gradient
+// (the clamp passes the gradient where h <= limit).
+__device__ __forceinline__ float srelu_fwd(float h, const ActP& p) {
+  const float r = fmaxf(fminf(h, p.limit), 0.0f);
+  return p.out_scale * r * r;
+}
+
+__device__ __forceinline__ float srelu_bwd(float da, float h, const ActP& p) {
+  const float r = fmaxf(fminf(h, p.limit), 0.0f);
+  return h <= p.limit ? p.out_scale * da * 2.0f * r : 0.0f;
+}
+
 template <int ACT>
 __device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& p, float& dg,
                                         float& dl) {
@@ -285,7 +297,8 @@ template <int MODE, bool MX>
 struct Traits {
   static constexpr bool kRaggedK = (MODE == kWgrad);
   static constexpr bool kAmn = !MX && (MODE == kWgrad);
-  static constexpr bool kBmn = !MX && (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad);
+  static constexpr bool kBmn =
+      !MX && (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad || MODE == kDgradAct);
   static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
   static constexpr int kBK = MX ? BK_MX : BK;
   static constexpr int kNR = MX ? kRingMx : kRing;
@@ -454,9 +467,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             tma_load_3d(sa, &args.tma_a, fb, kk, ti.m0, 0);
           }
           // ---- B operand
-          if (MODE == kFc1Glu || MODE == kFc2) {
+          if (MODE == kFc1Glu || MODE == kFc2 || MODE == kFc1Act) {
             tma_load_3d(sb, &args.tma_b, fb, kk, ti.n0, ti.e);
-          } else if (MODE == kDgradDglu || MODE == kDgradFc1) {
+          } else if (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kDgradAct) {
             if (args.b_atoms4d)
               tma_load_4d(sb, &args.tma_b, fb, 0, kk, ti.n0 / 64, ti.e);
             else
@@ -742,7 +755,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         const bool has_acc = !Tr::kRaggedK || ti.num_kb > 0;
         const bool write = !Tr::kRaggedK || y0 < args.m_ext;   // CTA-uniform
         const __nv_bfloat16* bias =
-            (MODE == kFc2 && args.bias)
+            ((MODE == kFc2 || MODE == kFc1Act) && args.bias)
                 ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + hc
                 : nullptr;
         const int nch = min(BN / 32, (args.n_ext - ti.n0 + 31) / 32);
@@ -785,6 +798,63 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
 #pragma unroll
               for (int i = 0; i < 16; ++i) v1[i] += b[i];
             }
+          }
+          if constexpr (MODE == kFc1Act || MODE == kDgradAct) {
+            // non-gated activation: FC1 writes H and A = act(H); the dgrad
+            // turns dA into dH = act'(H) dA from the saved H
+            if (MODE == kDgradAct && valid) {
+              const __nv_bfloat16* Hrow =
+                  static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux + c0 + hc;
+              float h0[16], h1[16];
+              load_bf16x16(Hrow, h0);
+              if (two) load_bf16x16(Hrow + 32, h1);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                v0[i] = srelu_bwd(v0[i], h0[i], ap);
+                v1[i] = two ? srelu_bwd(v1[i], h1[i], ap) : 0.0f;
+              }
+            }
+            const uint8_t* bx0 = ring_next_box(ring);
+            const uint8_t* bx1 = bx0;
+            if (args.out0 != nullptr) {           // H (FC1; skipped when recomputed) / dH
+              ring_store_half<Tr::kNR>(ring, v0, valid, &args.tma_out0, c0, y0, 0, row_local,
+                                       half, issuer);
+              bx1 = ring_next_box(ring);
+              if (two)
+                ring_store_half<Tr::kNR>(ring, v1, valid, &args.tma_out0, c0 + 32, y0, 0,
+                                         row_local, half, issuer);
+            }
+            if (MODE == kFc1Act) {
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                v0[i] = srelu_fwd(v0[i], ap);
+                v1[i] = srelu_fwd(v1[i], ap);
+              }
+              bx0 = ring_next_box(ring);
+              bx1 = bx0;
+              if (args.out1 != nullptr || want_mx) {
+                ring_store_half<Tr::kNR>(ring, v0, valid, args.out1 ? &args.tma_out1 : nullptr,
+                                         c0, y0, 0, row_local, half, issuer);
+                bx1 = ring_next_box(ring);
+                if (two)
+                  ring_store_half<Tr::kNR>(ring, v1, valid, args.out1 ? &args.tma_out1 : nullptr,
+                                           c0 + 32, y0, 0, row_local, half, issuer);
+              }
+            }
+            if (want_mx) {                      // MXFP8 / amax of the staged A (FC1) or dH
+              mx_block_half(mx, bx0, quarter * 32, y0 + quarter * 32, c0, lane, half);
+              if (two) mx_block_half(mx, bx1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
+              if (mx.amax) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
+                  v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
+                }
+                mx_amax_block16(mx, v0, lane);
+                if (two) mx_amax_block16(mx, v1, lane);
+              }
+            }
+            continue;
           }
           const uint8_t* box0 = ring_next_box(ring);
           const uint8_t* box1 = box0;
@@ -1109,6 +1179,8 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
     case kDgradDglu: return launch_act<kDgradDglu, false>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0, false>(args, grid, s);
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
+    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, false>(args, grid, s);
+    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, false>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1120,6 +1192,8 @@ cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cud
     case kDgradDglu: return launch_act<kDgradDglu, true>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0, true>(args, grid, s);
     case kWgrad: return launch_mode<kWgrad, 0, true>(args, grid, s);
+    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, true>(args, grid, s);
+    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, true>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

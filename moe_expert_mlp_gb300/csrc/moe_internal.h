@@ -69,8 +69,14 @@ enum GemmMode : int {
   kDgradDglu = 2,  // dA = dY W2, dH = dGLU(dA, H)              ragged M
   kDgradFc1 = 3,   // dX = dH W1p                               ragged M
   kWgrad = 4,      // dW[e] = sum over group rows of P^T Q      ragged K
-  kWgradPair = 5   // same on CTA pairs (2-SM MMA, 256x256 tiles)
+  kWgradPair = 5,  // same on CTA pairs (2-SM MMA, 256x256 tiles)
+  kFc1Act = 6,     // non-gated: H = X W1^T (+b1), A = act(H)   ragged M
+  kDgradAct = 7    // non-gated: dA = dY W2, dH = act'(H) dA     ragged M
 };
+
+// FC1 output width: 2*F_pad (gate and linear halves, packed) for the GLU
+// activations, F for the non-gated squared ReLU.
+inline int fc1_width(int act, int F) { return act == MOE_ACT_SRELU ? F : 2 * fc1_pad(F); }
 
 struct GemmArgs {
   CUtensorMap tma_a;

@@ -32,6 +32,10 @@ class MoEExpertMLP:
         self.recompute_h = recompute_h
         self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
         self.Fp = L.moe_fc1_padded_width(F)
+        # FC1 output width: packed gate|linear halves (2*F_pad) for the GLU
+        # activations, F for the non-gated squared ReLU
+        self.W1 = F if act == "srelu" else 2 * self.Fp
+        self.gated = act != "srelu"
         self.has_b1, self.has_b2 = has_b1, has_b2
         cap = self.desc.capacity
         self.capacity = cap
@@ -42,12 +46,12 @@ class MoEExpertMLP:
             return torch.zeros(shape, dtype=dtype, device=dev)
 
         # weights (FC1 kept repacked) and their gradients
-        self.w1p = z(E, 2 * self.Fp, d)
-        self.b1p = z(E, 2 * self.Fp) if has_b1 else None
+        self.w1p = z(E, self.W1, d)
+        self.b1p = z(E, self.W1) if has_b1 else None
         self.w2 = z(E, d, F)
         self.b2 = z(E, d) if has_b2 else None
-        self.dw1p = z(E, 2 * self.Fp, d)
-        self.db1p = z(E, 2 * self.Fp) if has_b1 else None
+        self.dw1p = z(E, self.W1, d)
+        self.db1p = z(E, self.W1) if has_b1 else None
         self.dw2 = z(E, d, F)
         self.db2 = z(E, d) if has_b2 else None
         # routing state (device resident)
@@ -61,11 +65,11 @@ class MoEExpertMLP:
         self.row_of = z(max(T, 1), k, dtype=i32)
         # per-row activations and gradients (padded row layout)
         self.x_perm = z(cap, d)
-        self.h = None if recompute_h else z(cap, 2 * self.Fp)
+        self.h = None if recompute_h else z(cap, self.W1)
         self.a = z(cap, F)
         self.y = z(cap, d)
         self.dy = z(cap, d)
-        self.dh = z(cap, 2 * self.Fp)
+        self.dh = z(cap, self.W1)
         self.dx_perm = z(cap, d)
         # per-token outputs
         self.out = z(max(T, 1), d)
@@ -74,20 +78,20 @@ class MoEExpertMLP:
         self.dlogits = z(max(T, 1), E, dtype=f32)
         self.ws = torch.zeros(max(L.moe_workspace_size(self.desc), 256), dtype=torch.uint8, device=dev)
         if self.mx:
-            Fp = self.Fp
             # activations: rowwise for the GEMM that contracts over features,
             # transposed for the weight gradient that contracts over rows
             self.x_mx = self.mx_operand(d)
             self.a_mx = self.mx_operand(F)
             self.dy_mx = self.mx_operand(d)
-            self.dh_mx = self.mx_operand(2 * Fp)
+            self.dh_mx = self.mx_operand(self.W1)
             u8 = torch.uint8
 
             def sc(rows, cols):
                 return z(E * L.moe_mx_scale_bytes(rows, cols), dtype=u8)
 
-            self.w_mx = dict(w1=z(E, 2 * Fp, d, dtype=u8), w1_s=sc(2 * Fp, d),
-                             w1t=z(E, d, 2 * Fp, dtype=u8), w1t_s=sc(d, 2 * Fp),
+            W1 = self.W1
+            self.w_mx = dict(w1=z(E, W1, d, dtype=u8), w1_s=sc(W1, d),
+                             w1t=z(E, d, W1, dtype=u8), w1t_s=sc(d, W1),
                              w2=z(E, d, F, dtype=u8), w2_s=sc(d, F),
                              w2t=z(E, F, d, dtype=u8), w2t_s=sc(F, d))
 
@@ -121,8 +125,10 @@ class MoEExpertMLP:
         L.moe_quantize_weights_mx(self.desc, self.w1p, self.w2, self.w_mx, stream)
 
     def unpack_fc1(self, packed, width, stream=None):
-        """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p)."""
-        out = torch.empty((self.E, 2 * self.F, width), dtype=torch.bfloat16, device=packed.device)
+        """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p);
+        [E,F,width] unchanged for the non-gated activation."""
+        n1 = 2 * self.F if self.gated else self.F
+        out = torch.empty((self.E, n1, width), dtype=torch.bfloat16, device=packed.device)
         L.moe_unpack_fc1(self.desc, packed, out, width, stream)
         return out
 

@@ -71,13 +71,13 @@ def _pad_rows32(v):
 
 def expert_forward_mx(X, W1, b1, W2, b2, p):
     """One expert.  X [m,d] bf16 values; W1 [2F,d] (logical gate | linear
-    rows), W2 [d,F].  Returns H (bf16), A (bf16), Y (fp64, before the bf16
+    rows; [F,d] for the non-gated activation), W2 [d,F].  Returns H (bf16), A (bf16), Y (fp64, before the bf16
     store)."""
     F = W2.shape[1]
     H = mx_fake_rows(X) @ mx_fake_rows(W1).T
     if b1 is not None:
         H = H + b1[None, :]
-    A = glu_forward(H[:, :F], H[:, F:], p)
+    A = glu_forward(H[:, :F], H[:, F:], p) if p.gated else glu_forward(H, None, p)
     A16 = bf16_round(A)
     Y = mx_fake_rows(A16) @ mx_fake_rows(W2).T
     if b2 is not None:
@@ -91,8 +91,11 @@ def expert_backward_mx(X, H16, A16, dY, W1, W2, p):
     F = W2.shape[1]
     m = X.shape[0]
     dA = mx_fake_rows(dY) @ mx_fake_cols(W2)             # K = d
-    dG, dL = glu_backward(dA, H16[:, :F], H16[:, F:], p)
-    dH16 = bf16_round(np.concatenate([dG, dL], axis=1))
+    if p.gated:
+        dG, dL = glu_backward(dA, H16[:, :F], H16[:, F:], p)
+        dH16 = bf16_round(np.concatenate([dG, dL], axis=1))
+    else:
+        dH16 = bf16_round(glu_backward(dA, H16, None, p)[0])
     dX = mx_fake_rows(dH16) @ mx_fake_cols(W1)           # K = 2F
     # weight gradients: K = the group's tokens, 32-row blocks from its start
     dW2 = mx_fake_cols(_pad_rows32(dY)).T @ mx_fake_cols(_pad_rows32(A16))

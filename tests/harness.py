@@ -128,7 +128,10 @@ def run_both_direct(wl, inp):
 
 def packed_to_logical_cols(t_np, F):
     """GPU packed FC1-shaped columns -> logical (gate then linear) columns;
-    also returns the packed padding columns for a zero check."""
+    also returns the packed padding columns for a zero check.  A tensor F
+    wide is the non-gated activation's, which is not packed."""
+    if t_np.shape[-1] == F:
+        return t_np, t_np[..., :0]
     src = oracle.fc1_packed_columns(F)
     out = np.zeros(t_np.shape[:-1] + (2 * F,))
     ok = src >= 0

@@ -24,6 +24,8 @@ ROUTED = {
     "gptoss_small": scaled(WORKLOADS["gptoss_t16384_e32"], T=300, E=8, k=4, d=192, F=224),
     "geglu_raggedF": scaled(BASE, T=320, E=6, k=3, d=320, F=352, act="geglu",
                             router_bias=False),
+    "srelu_nongated": scaled(BASE, T=256, E=4, k=2, d=256, F=224, act="srelu",
+                             router_bias=False),
 }
 
 
@@ -112,7 +114,7 @@ def test_routed_layer_mxfp8(name):
     _mx_close("dx", H.to_np(layer.dx)[:T], ref["dx"])
     _mx_close("dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"])
     _check_fused_mx(layer, "A", layer.a, layer.a_mx, wl.F)
-    _check_fused_mx(layer, "dH", layer.dh, layer.dh_mx, 2 * layer.Fp)
+    _check_fused_mx(layer, "dH", layer.dh, layer.dh_mx, layer.W1)
 
 
 def test_direct_groups_mxfp8_with_empty_experts():

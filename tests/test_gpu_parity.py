@@ -26,6 +26,11 @@ CASES = {
     "geglu": scaled(BASE, T=256, E=4, k=2, d=128, F=384, act="geglu", router_bias=False),
     "sreglu_scaled": scaled(BASE, T=256, E=4, k=1, d=256, F=128, act="sreglu", out_scale=0.5,
                             router_bias=False),
+    # non-gated squared ReLU: FC1 is F wide, F not a multiple of the 256-column tile
+    "srelu_nongated": scaled(BASE, T=320, E=5, k=2, d=192, F=224, act="srelu",
+                             router_bias=False),
+    "srelu_clamp_bias": scaled(WORKLOADS["gptoss_t16384_e32"], T=200, E=4, k=2, d=128, F=160,
+                               act="srelu", linear_offset=0.0, out_scale=0.75, limit=1.5),
 }
 
 

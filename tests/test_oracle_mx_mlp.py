@@ -122,3 +122,23 @@ def test_close_to_unquantized_oracle(act):
             zip(["dX", "dH", "dW1", "db1", "dW2", "db2"], got_b, ref_b)):
         err = np.linalg.norm(g - r) / np.linalg.norm(r)
         assert err < 0.1, (name, err)
+
+
+def test_nongated_close_to_unquantized_oracle():
+    """Non-gated squared ReLU (FC1 F wide): the same wiring check."""
+    rng = np.random.default_rng(4)
+    m, d, F = 96, 128, 64
+    X = _bf(rng.standard_normal((m, d)))
+    W1 = _bf(rng.standard_normal((F, d)) * 0.1)
+    W2 = _bf(rng.standard_normal((d, F)) * 0.1)
+    dY = _bf(rng.standard_normal((m, d)))
+    p = _params(act="srelu")           # no clamp: its gradient jump is not noise
+    Hm, Am, Ym = oracle.expert_forward_mx(X, W1, None, W2, None, p)
+    H, A, Y = oracle.expert_forward(X, W1, None, W2, None, p)
+    assert Hm.shape == (m, F) and Am.shape == (m, F)
+    ref_b = oracle.expert_backward(X, H, A, dY, W1, W2, p)
+    got_b = oracle.expert_backward_mx(X, Hm, Am, dY, W1, W2, p)
+    for name, g, r in [("H", Hm, H), ("A", Am, A), ("Y", Ym, Y)] + list(
+            zip(["dX", "dH", "dW1", "db1", "dW2", "db2"], got_b, ref_b)):
+        err = np.linalg.norm(g - r) / np.linalg.norm(r)
+        assert err < 0.1, (name, err)
