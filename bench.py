@@ -22,6 +22,7 @@ on a bounded sample of the same workload on the host cores.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import os
@@ -87,13 +88,14 @@ def call_work(wl, name, R):
     GEMMs: 2*M*N*K with M = routed rows.  Memory-bound calls: bytes of the
     tensors they must read and write once (bf16 rows, index arrays ignored)."""
     d, F, T, k = wl.d, wl.F, wl.T, wl.k
+    n1 = 2 * F if wl.gated else F          # FC1 outputs (gate + linear halves when gated)
     gemm = {
-        "fc1_glu_fwd": 2.0 * R * d * 2 * F,
+        "fc1_glu_fwd": 2.0 * R * d * n1,
         "fc2_fwd": 2.0 * R * F * d,
         "fc2_dgrad_dglu": 2.0 * R * d * F,
         "fc2_wgrad": 2.0 * R * d * F,
-        "fc1_dgrad": 2.0 * R * 2 * F * d,
-        "fc1_wgrad": 2.0 * R * 2 * F * d,
+        "fc1_dgrad": 2.0 * R * n1 * d,
+        "fc1_wgrad": 2.0 * R * n1 * d,
     }
     if name in gemm:
         return "flop", gemm[name]
@@ -103,7 +105,7 @@ def call_work(wl, name, R):
         "combine_bwd": T * d * 2 + R * d * 2 + R * d * 2,
         "permute_bwd": R * d * 2 + T * d * 2,
         "route_bwd": T * k * 12 + T * wl.E * 4,
-        "bias_grads": R * d * 2 * int(wl.has_b2) + R * 2 * F * 2 * int(wl.has_b1),
+        "bias_grads": R * d * 2 * int(wl.has_b2) + R * n1 * 2 * int(wl.has_b1),
         # bf16 rows in; rowwise and transposed E4M3 codes + one scale per 32 out
         "quant_x": R * d * (2 + 2 + 2 / 32),
         "quant_dy": R * d * (2 + 2 + 2 / 32),
@@ -351,6 +353,9 @@ def run_ours(args, wl):
     # per optimizer step, timed on its own, outside the step
     for _ in range(2):
         layer.load_weights(w1, b1, w2, b2)
+    if args.amax:      # fused NVFP4-prep outputs inside the timed step
+        layer.amax_a = torch.zeros(2, dtype=torch.float32, device=dev)
+        layer.amax_dh = torch.zeros(2, dtype=torch.float32, device=dev)
     torch.cuda.synchronize()
     p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     p0.record()
@@ -507,7 +512,8 @@ def run_ours(args, wl):
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": args.dtype, "data": "synthetic",
-        "config": dict(workload_config(wl, args.dtype), parallelism=f"replicas x{world}",
+        "config": dict(workload_config(wl, args.dtype), amax_outputs=bool(args.amax),
+                       parallelism=f"replicas x{world}",
                        graph=bool(use_graph)),
         "tokens_per_s": round(job_rate(wl.T if routed else R, K, world, ms_max), 1),
         "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
@@ -647,6 +653,10 @@ def main():
                     help="tokens (or rows) per step of --impl reference")
     ap.add_argument("--dtype", choices=["bf16", "mxfp8"], default="bf16",
                     help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales)")
+    ap.add_argument("--act", choices=["swiglu", "geglu", "sreglu", "srelu"], default=None,
+                    help="override the workload's activation (the dense sweep)")
+    ap.add_argument("--amax", action="store_true",
+                    help="also produce the fused per-tensor amax of A and dH (NVFP4 prep)")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -654,6 +664,8 @@ def main():
                     help="skip the fused-vs-unfused expert MLP comparison")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
+    if args.act is not None:
+        wl = dataclasses.replace(wl, act=args.act)
     if args.impl == "reference":
         return run_reference(args, wl)
     return run_ours(args, wl)

@@ -215,20 +215,46 @@ __device__ __forceinline__ void mx_block_half(const MxOut& mx, const uint8_t* bo
   mx_block_from_box(m, box, row0, r0, col0, lane);
 }
 
-// amax outputs over one warp's 16 columns of a block (rows = lanes).
-__device__ __forceinline__ void mx_amax_block16(const MxOut& mx, const float (&v)[16], int lane) {
-  float m = 0.0f, h = 0.0f;
+// amax of one warp's 16 columns of a staged 32-row block (box rows row0 ..
+// row0+31, columns col .. col+15 of the box): lane l takes column col + l %
+// 16 and the 16-row segment l / 16, transforms it with the 16-point
+// Walsh-Hadamard butterflies in registers (H16 s / 4), and folds the plain
+// and rotated maxima into its running maxima m_acc / h_acc (published once
+// per warp by mx_amax_publish).
+__device__ __forceinline__ void mx_amax_from_box(const uint8_t* box, int row0, int col, int lane,
+                                                 float& m_acc, float& h_acc) {
+  const int c = col + (lane & 15);
+  const int r0 = row0 + 16 * (lane >> 4);
+  float x[16];
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    m = fmaxf(m, fabsf(v[i]));
-    float x = v[i];
-#pragma unroll
-    for (int b = 1; b < 16; b <<= 1) {
-      const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
-      x = (lane & b) ? (p - x) : (x + p);
-    }
-    h = fmaxf(h, fabsf(x) * 0.25f);
+    const int r = r0 + i;
+    const uint16_t b = *reinterpret_cast<const uint16_t*>(
+        box + r * 64 + ((((c >> 3) ^ ((r >> 1) & 3))) << 4) + (c & 7) * 2);
+    x[i] = __uint_as_float(static_cast<uint32_t>(b) << 16);
   }
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
+#pragma unroll
+  for (int st = 1; st < 16; st <<= 1)
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+      if ((i & st) == 0) {
+        const float a = x[i], b = x[i + st];
+        x[i] = a + b;
+        x[i + st] = a - b;
+      }
+  float h = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 16; ++i) h = fmaxf(h, fabsf(x[i]));
+  m_acc = fmaxf(m_acc, m);
+  h_acc = fmaxf(h_acc, h * 0.25f);
+}
+
+// Warp-reduce the running maxima and fold them into mx.amax (one atomic
+// pair per warp per kernel).  Whole warp calls.
+__device__ __forceinline__ void mx_amax_publish(const MxOut& mx, float m, float h, int lane) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
@@ -583,6 +609,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       }
     };
     const bool want_mx = mx.q != nullptr || mx.qt != nullptr || mx.amax != nullptr;
+    float am_m = 0.0f, am_h = 0.0f;           // running amax (plain, Hadamard) of this lane
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
@@ -664,11 +691,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                                        y0, 0, row_local, half, issuer);
             if (want_mx) {                      // MXFP8 / amax of the staged bf16 A
               mx_block_half(mx, box, quarter * 32, y0 + quarter * 32, f0, lane, half);
-              if (mx.amax) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
-                mx_amax_block16(mx, a, lane);
-              }
+              if (mx.amax) mx_amax_from_box(box, quarter * 32, hc, lane, am_m, am_h);
             }
           }
         }
@@ -702,20 +725,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             ring_store_half<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
+            if (want_mx && mx.amax) mx_amax_from_box(box_g, quarter * 32, hc, lane, am_m, am_h);
             const uint8_t* box_l = ring_next_box(ring);
             ring_store_half<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
-          }
-          if (want_mx && mx.amax) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              dg[i] = live0 ? bf16_round(dg[i]) : 0.0f;
-              dl[i] = live0 ? bf16_round(dl[i]) : 0.0f;
-            }
-            mx_amax_block16(mx, dg, lane);
-            mx_amax_block16(mx, dl, lane);
+            if (want_mx && mx.amax) mx_amax_from_box(box_l, quarter * 32, hc, lane, am_m, am_h);
           }
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
@@ -734,20 +750,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             ring_store_half<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane, half);
+            if (want_mx && mx.amax) mx_amax_from_box(box_g, quarter * 32, hc, lane, am_m, am_h);
             const uint8_t* box_l = ring_next_box(ring);
             ring_store_half<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane, half);
-          }
-          if (want_mx && mx.amax) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
-              dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
-            }
-            mx_amax_block16(mx, dg, lane);
-            mx_amax_block16(mx, dl, lane);
+            if (want_mx && mx.amax) mx_amax_from_box(box_l, quarter * 32, hc, lane, am_m, am_h);
           }
         }
       } else {
@@ -845,13 +854,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
               mx_block_half(mx, bx0, quarter * 32, y0 + quarter * 32, c0, lane, half);
               if (two) mx_block_half(mx, bx1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
               if (mx.amax) {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                  v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
-                  v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
-                }
-                mx_amax_block16(mx, v0, lane);
-                if (two) mx_amax_block16(mx, v1, lane);
+                mx_amax_from_box(bx0, quarter * 32, hc, lane, am_m, am_h);
+                if (two) mx_amax_from_box(bx1, quarter * 32, hc, lane, am_m, am_h);
               }
             }
             continue;
@@ -870,13 +874,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             mx_block_half(mx, box0, quarter * 32, y0 + quarter * 32, c0, lane, half);
             if (two) mx_block_half(mx, box1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
             if (mx.amax) {
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
-                v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
-              }
-              mx_amax_block16(mx, v0, lane);
-              if (two) mx_amax_block16(mx, v1, lane);
+              mx_amax_from_box(box0, quarter * 32, hc, lane, am_m, am_h);
+              if (two) mx_amax_from_box(box1, quarter * 32, hc, lane, am_m, am_h);
             }
           }
         }
@@ -885,6 +884,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
+    if (mx.amax) mx_amax_publish(mx, am_m, am_h, lane);
     if (issuer) bulk_wait_all();              // stores done before the CTA exits
   }
 

@@ -27,6 +27,10 @@ class MoEExpertMLP:
         # dtype "mxfp8": the grouped GEMMs read MXFP8 operands (E4M3 codes,
         # E8M0 scales per 32 elements); routing and combine stay bf16
         self.mx = dtype == "mxfp8"
+        # optional fused NVFP4-preparation outputs (per-tensor amax of A and
+        # of dH, plain and Hadamard-rotated): float[2] device tensors or None
+        self.amax_a = None
+        self.amax_dh = None
         # recompute_h: the forward keeps no H; the backward regenerates it in
         # the library workspace (activation recompute)
         self.recompute_h = recompute_h
@@ -164,12 +168,15 @@ class MoEExpertMLP:
 
     def mlp_forward(self, stream=None, timer=None, a_mx=None, y_mx=None):
         c, po = self.counts, self.padded_offsets
+        if a_mx is None and self.amax_a is not None and not self.mx:
+            a_mx = dict(amax=self.amax_a)
         if self.mx:
             with self._t(timer, "quant_x"):
                 L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
             with self._t(timer, "fc1_glu_fwd"):
+                a_out = self.a_mx if self.amax_a is None else dict(self.a_mx, amax=self.amax_a)
                 L.moe_fc1_glu_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.h,
-                                     self.a, self.a_mx, stream)
+                                     self.a, a_out, stream)
             with self._t(timer, "fc2_fwd"):
                 L.moe_fc2_fwd_mx(self.desc, self.a_mx, c, po, self.w_mx, self.b2, self.y, stream)
             return
@@ -181,12 +188,15 @@ class MoEExpertMLP:
 
     def mlp_backward(self, stream=None, timer=None, dh_mx=None):
         c, po = self.counts, self.padded_offsets
+        if dh_mx is None and self.amax_dh is not None and not self.mx:
+            dh_mx = dict(amax=self.amax_dh)
         if self.mx:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
             with self._t(timer, "fc2_dgrad_dglu"):
+                dh_out = self.dh_mx if self.amax_dh is None else dict(self.dh_mx, amax=self.amax_dh)
                 L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, self.h, c, po, self.w_mx,
-                                        self.dh, self.dh_mx, stream)
+                                        self.dh, dh_out, stream)
             with self._t(timer, "fc2_wgrad"):
                 L.moe_fc2_wgrad_mx(self.desc, self.dy_mx, self.a_mx, c, po, self.dw2, stream)
             with self._t(timer, "fc1_dgrad"):
