@@ -25,7 +25,7 @@
 //            every 32 accumulator columns: tcgen05.ld, fused math, bf16
 //            (and MXFP8) outputs.  Two 256-column accumulators in TMEM let
 //            the epilogue of one tile overlap the MMAs of the next.
-// The weight-gradient kernel on CTA pairs (bf16) keeps 6 warps.
+// The bf16 weight-gradient kernel on CTA pairs uses the same warp roles.
 // Tiles are 128 rows x 256 columns.  Every expert group starts at a
 // multiple of 128 rows, so an M tile never straddles two experts; rows past
 // the group's count are padding and are written as zeros.  Weight-gradient
@@ -51,12 +51,10 @@ constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int MN_BOX_BYTES = 64 * BK * 2;    // one 64(MN) x 64(K) box, 8 KB
 constexpr int TMEM_COLS = 2 * BN;            // two fp32 accumulators
-constexpr int NUM_THREADS = 192;             // CTA-pair weight-gradient kernel
-constexpr int GEMM_THREADS = 320;            // grouped GEMM: producer, MMA, 8 epilogue warps
+constexpr int GEMM_THREADS = 320;            // producer, MMA, 8 epilogue warps (both kernels)
 constexpr int kGemmEpiThreads = 256;
 constexpr int kRing = 4;                     // output staging boxes (shared by the epilogue)
 constexpr int BOX_BYTES = 128 * 32 * 2;      // one 128-row x 32-column bf16 output box
-constexpr int kEpiThreads = 128;             // 4 epilogue warps (CTA-pair kernel)
 constexpr int kEpiBar = 1;                   // named barrier of the epilogue warps
 constexpr size_t SMEM_BYTES =
     1024 + static_cast<size_t>(STAGES) * STAGE_BYTES + kRing * BOX_BYTES;
@@ -215,41 +213,24 @@ __device__ __forceinline__ void mx_block_half(const MxOut& mx, const uint8_t* bo
   mx_block_from_box(m, box, row0, r0, col0, lane);
 }
 
-// amax of one warp's 16 columns of a staged 32-row block (box rows row0 ..
-// row0+31, columns col .. col+15 of the box): lane l takes column col + l %
-// 16 and the 16-row segment l / 16, transforms it with the 16-point
-// Walsh-Hadamard butterflies in registers (H16 s / 4), and folds the plain
-// and rotated maxima into its running maxima m_acc / h_acc (published once
-// per warp by mx_amax_publish).
-__device__ __forceinline__ void mx_amax_from_box(const uint8_t* box, int row0, int col, int lane,
-                                                 float& m_acc, float& h_acc) {
-  const int c = col + (lane & 15);
-  const int r0 = row0 + 16 * (lane >> 4);
-  float x[16];
+// amax of one warp's 16 columns of a 32-row block held one row per lane in
+// v (bf16-rounded values, zero on padding rows): the plain maximum and the
+// maximum of the 16-row Walsh-Hadamard rotation (H16 s / 4) of each column
+// segment (half warps are the 16-row segments), folded into this lane's
+// running maxima m_acc / h_acc (published once per warp by mx_amax_publish).
+__device__ __forceinline__ void mx_amax_regs16(const float (&v)[16], int lane, float& m_acc,
+                                               float& h_acc) {
 #pragma unroll
   for (int i = 0; i < 16; ++i) {
-    const int r = r0 + i;
-    const uint16_t b = *reinterpret_cast<const uint16_t*>(
-        box + r * 64 + ((((c >> 3) ^ ((r >> 1) & 3))) << 4) + (c & 7) * 2);
-    x[i] = __uint_as_float(static_cast<uint32_t>(b) << 16);
+    m_acc = fmaxf(m_acc, fabsf(v[i]));
+    float x = v[i];
+#pragma unroll
+    for (int b = 1; b < 16; b <<= 1) {
+      const float p = __shfl_xor_sync(0xFFFFFFFFu, x, b);
+      x = (lane & b) ? (p - x) : (x + p);
+    }
+    h_acc = fmaxf(h_acc, fabsf(x) * 0.25f);
   }
-  float m = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(x[i]));
-#pragma unroll
-  for (int st = 1; st < 16; st <<= 1)
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-      if ((i & st) == 0) {
-        const float a = x[i], b = x[i + st];
-        x[i] = a + b;
-        x[i + st] = a - b;
-      }
-  float h = 0.0f;
-#pragma unroll
-  for (int i = 0; i < 16; ++i) h = fmaxf(h, fabsf(x[i]));
-  m_acc = fmaxf(m_acc, m);
-  h_acc = fmaxf(h_acc, h * 0.25f);
 }
 
 // Warp-reduce the running maxima and fold them into mx.amax (one atomic
@@ -271,17 +252,16 @@ __device__ __forceinline__ const uint8_t* ring_next_box(const StoreRing& ring) {
   return ring.gbase + ring.slot * BOX_BYTES;
 }
 
-// Two adjacent 32-column chunks per round, one TMA store for both.  Rounds
-// alternate between slot pairs {0,1} and {2,3}; the issuer waits for every
-// earlier store to finish reading before the round's barrier, so the pair
-// the next round writes (last stored two rounds ago) is free.  map2 views the
-// output as [E][W/32][rows][32]; the second chunk of a single-chunk round lies
-// past the tensor's end and is clipped.
-__device__ __forceinline__ void stage_box(uint32_t buf, const float (&v)[32], bool live, int row) {
+// Two adjacent 32-column chunks per round, one TMA store for both, through
+// a ring of three slot pairs (see ring_store_pair).  map2 views the output as
+// [E][W/32][rows][32]; the second chunk of a single-chunk round lies past the
+// tensor's end and is clipped.  Each thread stages the 16 columns of its half.
+__device__ __forceinline__ void stage_box_half(uint32_t buf, const float (&v)[16], bool live,
+                                               int row, int half) {
   const uint32_t raddr = buf + row * 64;
   const uint32_t sw = (row >> 1) & 3;
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < 2; ++q) {
     uint4 w = make_uint4(0, 0, 0, 0);
     if (live) {
       w.x = pack_bf16x2(v[8 * q + 0], v[8 * q + 1]);
@@ -289,25 +269,26 @@ __device__ __forceinline__ void stage_box(uint32_t buf, const float (&v)[32], bo
       w.z = pack_bf16x2(v[8 * q + 4], v[8 * q + 5]);
       w.w = pack_bf16x2(v[8 * q + 6], v[8 * q + 7]);
     }
-    st_shared_v4(raddr + ((q ^ sw) << 4), w);
+    st_shared_v4(raddr + (((2 * half + q) ^ sw) << 4), w);
   }
 }
 
 template <int NPAIRS>
-__device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v0)[32],
-                                                const float (&v1)[32], bool two, bool live,
+__device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v0)[16],
+                                                const float (&v1)[16], bool two, bool live,
                                                 const CUtensorMap* map2, int c0, int y, int z,
-                                                int row, bool issuer) {
-  // Round r stages into pair r % NPAIRS.  With 3 pairs the issuer only waits
-  // (after issuing) for the store one round older, so a store overlaps the
-  // next round's staging; the pair a round writes was stored 3 rounds ago
-  // and that store was waited for before the previous round's barrier.
+                                                int row, int half, bool issuer) {
+  // Round r stages into pair r % NPAIRS; each of the eight epilogue warps
+  // writes its 16 columns of both chunks.  With 3 pairs the issuer only
+  // waits (after issuing) for the store one round older, so a store overlaps
+  // the next round's staging; the pair a round writes was stored 3 rounds
+  // ago and that store was waited for before the previous round's barrier.
   static_assert(NPAIRS == 3, "three slot pairs");
   const uint32_t buf = ring.base + ring.slot * BOX_BYTES;   // slot 0, 2 or 4
-  stage_box(buf, v0, live, row);
-  if (two) stage_box(buf + BOX_BYTES, v1, live, row);
+  stage_box_half(buf, v0, live, row, half);
+  if (two) stage_box_half(buf + BOX_BYTES, v1, live, row, half);
   fence_proxy_async_smem();
-  named_bar_sync(kEpiBar, kEpiThreads);
+  named_bar_sync(kEpiBar, kGemmEpiThreads);
   if (issuer) {
     tma_store_4d(map2, buf, 0, y, c0 / 32, z);
     bulk_commit();
@@ -691,7 +672,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                                        y0, 0, row_local, half, issuer);
             if (want_mx) {                      // MXFP8 / amax of the staged bf16 A
               mx_block_half(mx, box, quarter * 32, y0 + quarter * 32, f0, lane, half);
-              if (mx.amax) mx_amax_from_box(box, quarter * 32, hc, lane, am_m, am_h);
+              if (mx.amax) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) a[i] = valid ? bf16_round(a[i]) : 0.0f;
+                mx_amax_regs16(a, lane, am_m, am_h);
+              }
             }
           }
         }
@@ -725,13 +710,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             ring_store_half<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
-            if (want_mx && mx.amax) mx_amax_from_box(box_g, quarter * 32, hc, lane, am_m, am_h);
             const uint8_t* box_l = ring_next_box(ring);
             ring_store_half<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
-            if (want_mx && mx.amax) mx_amax_from_box(box_l, quarter * 32, hc, lane, am_m, am_h);
+          }
+          if (want_mx && mx.amax) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dg[i] = live0 ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live0 ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_amax_regs16(dg, lane, am_m, am_h);
+            mx_amax_regs16(dl, lane, am_m, am_h);
           }
           // chunk j+1 (buffer 1); prefetch chunk j+2 into buffer 0
           if (j + 2 < nch && valid && f2 < args.f_real) {
@@ -750,13 +742,20 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             ring_store_half<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane, half);
-            if (want_mx && mx.amax) mx_amax_from_box(box_g, quarter * 32, hc, lane, am_m, am_h);
             const uint8_t* box_l = ring_next_box(ring);
             ring_store_half<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane, half);
-            if (want_mx && mx.amax) mx_amax_from_box(box_l, quarter * 32, hc, lane, am_m, am_h);
+          }
+          if (want_mx && mx.amax) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_amax_regs16(dg, lane, am_m, am_h);
+            mx_amax_regs16(dl, lane, am_m, am_h);
           }
         }
       } else {
@@ -854,8 +853,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
               mx_block_half(mx, bx0, quarter * 32, y0 + quarter * 32, c0, lane, half);
               if (two) mx_block_half(mx, bx1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
               if (mx.amax) {
-                mx_amax_from_box(bx0, quarter * 32, hc, lane, am_m, am_h);
-                if (two) mx_amax_from_box(bx1, quarter * 32, hc, lane, am_m, am_h);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
+                  v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
+                }
+                mx_amax_regs16(v0, lane, am_m, am_h);
+                if (two) mx_amax_regs16(v1, lane, am_m, am_h);
               }
             }
             continue;
@@ -874,8 +878,13 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             mx_block_half(mx, box0, quarter * 32, y0 + quarter * 32, c0, lane, half);
             if (two) mx_block_half(mx, box1, quarter * 32, y0 + quarter * 32, c0 + 32, lane, half);
             if (mx.amax) {
-              mx_amax_from_box(box0, quarter * 32, hc, lane, am_m, am_h);
-              if (two) mx_amax_from_box(box1, quarter * 32, hc, lane, am_m, am_h);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                v0[i] = valid ? bf16_round(v0[i]) : 0.0f;
+                v1[i] = valid && two ? bf16_round(v1[i]) : 0.0f;
+              }
+              mx_amax_regs16(v0, lane, am_m, am_h);
+              if (two) mx_amax_regs16(v1, lane, am_m, am_h);
             }
           }
         }
@@ -913,7 +922,7 @@ constexpr size_t PAIR_SMEM_BYTES =
     1024 + static_cast<size_t>(PAIR_STAGES) * PAIR_STAGE_BYTES + kPairRing * BOX_BYTES;
 constexpr uint32_t kPairIdesc = idesc_bf16(256, BN, true, true);
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
     k_wgrad_pair(const __grid_constant__ GemmArgs args) {
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[PAIR_STAGES];
@@ -934,8 +943,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int E = args.E;
 
-  for (int i = threadIdx.x; i <= E; i += NUM_THREADS) s_off[i] = args.padded_offsets[i];
-  for (int i = threadIdx.x; i < E; i += NUM_THREADS) s_cnt[i] = args.counts[i];
+  for (int i = threadIdx.x; i <= E; i += GEMM_THREADS) s_off[i] = args.padded_offsets[i];
+  for (int i = threadIdx.x; i < E; i += GEMM_THREADS) s_cnt[i] = args.counts[i];
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < PAIR_STAGES; ++s) {
@@ -944,7 +953,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 8);         // 4 epilogue warps x 2 CTAs
+      mbar_init(&tempty_bar[a], 16);        // 8 epilogue warps x 2 CTAs
     }
     fence_mbar_init();
   }
@@ -965,7 +974,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     if (!ok) set_status(args.status, MOE_DEV_BAD_OFFSETS);
     s_total = ok ? E * m_tiles * n_tiles : 0;
   }
-  for (int e = threadIdx.x; e < E; e += NUM_THREADS) {
+  for (int e = threadIdx.x; e < E; e += GEMM_THREADS) {
     int r = 0;
     for (int j = 0; j < E; ++j) r += (s_cnt[j] > s_cnt[e]) || (s_cnt[j] == s_cnt[e] && j < e);
     s_order[r] = e;
@@ -1072,8 +1081,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // ====================== epilogue (both CTAs) ==========================
+    // eight warps, two per TMEM lane quarter, 16 of every 32 columns each
     const int quarter = warp & 3;
-    StoreRing ring{smem_u32(smem + PAIR_STAGES * PAIR_STAGE_BYTES), 0};
+    const int half = (warp - 2) >> 2;
+    const int hc = 16 * half;
+    StoreRing ring{smem_u32(smem + PAIR_STAGES * PAIR_STAGE_BYTES), 0, nullptr};
     const bool issuer = threadIdx.x == 64;
     const int row_local = quarter * 32 + lane;
     int it = 0;
@@ -1090,37 +1102,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) ok = mbar_wait(&tfull_bar[acc], acc_par, args.status, abort_flag);
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       // leave together: the store barriers below need all epilogue warps
-      if (named_bar_any(kEpiBar, kEpiThreads, !ok)) break;
+      if (named_bar_any(kEpiBar, kGemmEpiThreads, !ok)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + hc;
       const bool write = y0 < args.m_ext;
       const int nch = min(BN / 32, (args.n_ext - n0 + 31) / 32);
-      uint32_t ra[32], rb[32];
+      uint32_t ra[16], rb[16];
       if (has_acc) {
-        tmem_ld32(tbase, ra);
-        if (nch > 1) tmem_ld32(tbase + 32, rb);
+        tmem_ld16(tbase, ra);
+        if (nch > 1) tmem_ld16(tbase + 32, rb);
       }
 #pragma unroll 1
       for (int j = 0; j < nch; j += 2) {
         const bool two = j + 1 < nch;
-        float v0[32], v1[32];
+        float v0[16], v1[16];
         if (has_acc) {
-          tmem_ld_wait(ra);
-          reg_fence(rb);
+          tmem_ld_wait16(ra);
+          reg_fence16(rb);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
+          for (int i = 0; i < 16; ++i) {
             v0[i] = __uint_as_float(ra[i]);
             v1[i] = __uint_as_float(rb[i]);
           }
-          if (j + 2 < nch) tmem_ld32(tbase + 32 * (j + 2), ra);
-          if (j + 3 < nch) tmem_ld32(tbase + 32 * (j + 3), rb);
+          if (j + 2 < nch) tmem_ld16(tbase + 32 * (j + 2), ra);
+          if (j + 3 < nch) tmem_ld16(tbase + 32 * (j + 3), rb);
         } else {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) v0[i] = v1[i] = 0.0f;
+          for (int i = 0; i < 16; ++i) v0[i] = v1[i] = 0.0f;
         }
         if (write)
           ring_store_pair<3>(ring, v0, v1, two, true, &args.tma_out2, n0 + 32 * j, y0, e,
-                             row_local, issuer);
+                             row_local, half, issuer);
       }
       tc_fence_before();
       __syncwarp();
@@ -1143,7 +1156,7 @@ cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
                                          static_cast<int>(PAIR_SMEM_BYTES));
   if (err != cudaSuccess) return err;
   const int g = grid & ~1;
-  k_wgrad_pair<<<g < 2 ? 2 : g, NUM_THREADS, PAIR_SMEM_BYTES, s>>>(args);
+  k_wgrad_pair<<<g < 2 ? 2 : g, GEMM_THREADS, PAIR_SMEM_BYTES, s>>>(args);
   return cudaGetLastError();
 }
 
