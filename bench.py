@@ -471,6 +471,9 @@ def run_ours(args, wl):
     fusion = None
     if not args.no_fusion and not mx:
         fusion = measure_fusion(torch, layer, K)
+    overlap = None
+    if args.overlap and not mx:
+        overlap = measure_overlap(torch, layer)
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
     e2e = None
@@ -526,6 +529,7 @@ def run_ours(args, wl):
         "clocks": clocks,
         "e2e": e2e,
         "fusion": fusion,
+        "overlap": overlap,
     }
     if not args.no_cpu_baseline:
         dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens, mx)
@@ -575,6 +579,74 @@ def measure_fusion(torch, layer, K):
             "bwd_unfused_ms": round(b_unf, 4), "bwd_speedup": round(b_unf / b_fused, 3),
             "bwd_recompute_h_ms": round(b_rec, 4),
             "unfused": "same grouped GEMMs with plain epilogues; GLU / dGLU as separate passes"}
+
+
+def measure_overlap(torch, layer, reps=10):
+    """sm_margin: the grouped GEMM leaves `sm_margin` SMs free so that a
+    concurrent kernel (in the pages, the expert-parallel communication
+    kernels) progresses beside it.  Stand-in concurrent kernel: a 512 MB
+    device copy (torch's elementwise copy, SM-bound memory streaming) on a
+    second stream.  For each margin: FC1+GLU alone, the copy alone, and both
+    launched together (time until both finish), CUDA events, medians."""
+    from moe_expert_mlp_gb300 import _lib as L
+    src = torch.empty(256 * 2**20, dtype=torch.bfloat16, device=layer.w2.device)
+    dst = torch.empty_like(src)
+    s_main = torch.cuda.current_stream()
+    s_side = torch.cuda.Stream()
+    c, po = layer.counts, layer.padded_offsets
+
+    def gemm(desc, stream):
+        L.moe_fc1_glu_fwd(desc, layer.x_perm, c, po, layer.w1p, layer.b1p, layer.h, layer.a,
+                          stream)
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(s_main)
+            fn()
+            b.record(s_main)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    def both(desc):
+        start = torch.cuda.Event()
+        start.record(s_main)
+        s_side.wait_event(start)
+        gemm(desc, s_main)
+        with torch.cuda.stream(s_side):
+            dst.copy_(src)
+        done = torch.cuda.Event()
+        done.record(s_side)
+        s_main.wait_event(done)
+
+    def side_only():
+        start = torch.cuda.Event()
+        start.record(s_main)
+        s_side.wait_event(start)
+        with torch.cuda.stream(s_side):
+            dst.copy_(src)
+        done = torch.cuda.Event()
+        done.record(s_side)
+        s_main.wait_event(done)
+
+    side = timed(side_only)
+    out = {"concurrent": "512 MB device copy on a second stream", "copy_alone_ms": round(side, 4)}
+    rows = []
+    for m in (0, 16, 32):
+        desc = type(layer.desc).from_buffer_copy(layer.desc)
+        desc.sm_margin = m
+        g = timed(lambda: gemm(desc, s_main))
+        bt = timed(lambda: both(desc))
+        rows.append({"sm_margin": m, "fc1_glu_alone_ms": round(g, 4), "both_ms": round(bt, 4),
+                     "serial_ms": round(g + side, 4)})
+    out["by_margin"] = rows
+    del src, dst
+    return out
 
 
 def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
@@ -657,6 +729,8 @@ def main():
                     help="override the workload's activation (the dense sweep)")
     ap.add_argument("--amax", action="store_true",
                     help="also produce the fused per-tensor amax of A and dH (NVFP4 prep)")
+    ap.add_argument("--overlap", action="store_true",
+                    help="also time FC1 beside a concurrent kernel for several sm_margin values")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
