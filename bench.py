@@ -474,6 +474,9 @@ def run_ours(args, wl):
     overlap = None
     if args.overlap and not mx:
         overlap = measure_overlap(torch, layer)
+    router = None
+    if routed and not args.no_router:
+        router = measure_router(torch, layer, x, logits, bias)
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
     e2e = None
@@ -530,6 +533,7 @@ def run_ours(args, wl):
         "e2e": e2e,
         "fusion": fusion,
         "overlap": overlap,
+        "router": router,
     }
     if not args.no_cpu_baseline:
         dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens, mx)
@@ -579,6 +583,37 @@ def measure_fusion(torch, layer, K):
             "bwd_unfused_ms": round(b_unf, 4), "bwd_speedup": round(b_unf / b_fused, 3),
             "bwd_recompute_h_ms": round(b_rec, 4),
             "unfused": "same grouped GEMMs with plain epilogues; GLU / dGLU as separate passes"}
+
+
+def measure_router(torch, layer, x, logits, bias, reps=20):
+    """Routing from given logits (the step's moe_route_permute) against the
+    fused router, which computes the logits itself (router GEMM x W_r^T,
+    W_r seeded bf16 [E,d]) and takes the top-k in the GEMM epilogue, both
+    followed by the same permutation; CUDA events, medians."""
+    g = torch.Generator(device="cpu").manual_seed(5)
+    w_r = (torch.randn((layer.E, layer.d), generator=g) / layer.d ** 0.5).to(torch.bfloat16)
+    w_r = w_r.to(x.device)
+
+    def timed(fn):
+        ts = []
+        for i in range(reps + 3):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize()
+            if i >= 3:
+                ts.append(a.elapsed_time(b))
+        return statistics.median(ts)
+
+    given = timed(lambda: layer.route(x, logits, bias))
+    fused = timed(lambda: layer.route_fused(x, w_r, bias))
+    layer.route(x, logits, bias)          # leave the step's routing in place
+    torch.cuda.synchronize()
+    return {"route_permute_ms": round(given, 4), "route_fused_ms": round(fused, 4),
+            "fused": "router GEMM x W_r^T + top-k/softmax/histogram epilogue, then the "
+                     "same scan/assign/gather"}
 
 
 def measure_overlap(torch, layer, reps=10):
@@ -731,6 +766,8 @@ def main():
                     help="also produce the fused per-tensor amax of A and dH (NVFP4 prep)")
     ap.add_argument("--overlap", action="store_true",
                     help="also time FC1 beside a concurrent kernel for several sm_margin values")
+    ap.add_argument("--no-router", action="store_true",
+                    help="skip timing the fused router against routing from given logits")
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -219,6 +219,25 @@ moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
                                int32_t* row_src, int32_t* row_of, void* x_perm,
                                void* ws, size_t ws_bytes, cudaStream_t stream);
 
+/* Fused router (the routing work stays on the device with no host step,
+ * [FK] "Overcoming training bottlenecks in the MoE block"; fusion of the
+ * dispatch side, "Mixture-of-Kittens: MoE Megakernel for NVL72s", Abstract;
+ * more fusion patterns, [FK] "Next steps"): logits = x W_r^T on the
+ * tensor cores (bf16 x [T,d], bf16 w_router [E,d], fp32 accumulation), and in
+ * the GEMM epilogue, per token, the top-k of logit + bias (fp32, ties to the
+ * lower expert, descending), the softmax of the selected raw logits and the
+ * expert histogram -- the logits never go through HBM unless `logits`
+ * (fp32 [T,E]) is given; then the scan, counting-sort assignment and gather
+ * of moe_route_permute.  Outputs and workspace as in moe_route_permute.  The
+ * selection is decided on the kernel's fp32 logits. */
+moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
+                                     const void* w_router, const float* bias, float* logits,
+                                     int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                     int32_t* offsets, int32_t* padded_offsets,
+                                     int32_t* tile_prefix, int32_t* row_src, int32_t* row_of,
+                                     void* x_perm, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream);
+
 /* Offsets for groups whose sizes are given directly (no router): counts i32
  * [E] -> offsets, padded_offsets, tile_prefix i32 [E+1]. */
 moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts,

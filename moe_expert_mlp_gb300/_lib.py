@@ -34,7 +34,7 @@ EXPORTS = (
     "moe_mx_scale_bytes", "moe_quantize_mx_bf16", "moe_quantize_act_mx",
     "moe_quantize_weights_mx", "moe_mlp_fwd_mx", "moe_mlp_bwd_mx", "moe_fc1_glu_fwd_mx",
     "moe_fc2_fwd_mx", "moe_fc2_dgrad_dglu_mx", "moe_fc2_wgrad_mx", "moe_fc1_dgrad_mx",
-    "moe_fc1_wgrad_mx",
+    "moe_fc1_wgrad_mx", "moe_route_permute_fused",
 )
 
 
@@ -144,6 +144,7 @@ def lib():
             "moe_mlp_fwd_mx": (ctypes.c_int, [D] + [P] * 11),
             "moe_mlp_bwd_mx": (ctypes.c_int, [D] + [P] * 16),
             "moe_fc1_glu_fwd_mx": (ctypes.c_int, [D] + [P] * 9),
+            "moe_route_permute_fused": (ctypes.c_int, [D] + [P] * 14 + [ctypes.c_size_t, P]),
             "moe_fc2_fwd_mx": (ctypes.c_int, [D] + [P] * 7),
             "moe_fc2_dgrad_dglu_mx": (ctypes.c_int, [D] + [P] * 8),
             "moe_fc2_wgrad_mx": (ctypes.c_int, [D] + [P] * 6),
@@ -203,6 +204,16 @@ def moe_route_permute(desc, logits, bias, x, topk_idx, topk_w, counts, offsets, 
         ctypes.byref(desc), _p(logits), _p(bias), _p(x), _p(topk_idx), _p(topk_w), _p(counts),
         _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of), _p(x_perm),
         _p(ws), ws.numel() * ws.element_size() if ws is not None else 0, _stream(stream)))
+
+
+def moe_route_permute_fused(desc, x, w_router, bias, logits, topk_idx, topk_w, counts, offsets,
+                            padded_offsets, tile_prefix, row_src, row_of, x_perm, ws,
+                            stream=None):
+    _check(lib().moe_route_permute_fused(
+        ctypes.byref(desc), _p(x), _p(w_router), _p(bias), _p(logits), _p(topk_idx), _p(topk_w),
+        _p(counts), _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of),
+        _p(x_perm), _p(ws), ws.numel() * ws.element_size() if ws is not None else 0,
+        _stream(stream)))
 
 
 def moe_group_offsets(desc, counts, offsets, padded_offsets, tile_prefix, stream=None):

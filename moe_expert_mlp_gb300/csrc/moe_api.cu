@@ -317,6 +317,70 @@ moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
   return cuda_status(e);
 }
 
+moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
+                                     const void* w_router, const float* bias, float* logits,
+                                     int32_t* topk_idx, float* topk_w, int32_t* counts,
+                                     int32_t* offsets, int32_t* padded_offsets,
+                                     int32_t* tile_prefix, int32_t* row_src, int32_t* row_of,
+                                     void* x_perm, void* ws, size_t ws_bytes,
+                                     cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!x || !w_router || !topk_idx || !topk_w || !counts || !offsets || !padded_offsets ||
+      !tile_prefix || !row_src || !row_of || !x_perm)
+    return MOE_ERR_NULL;
+  if (desc->T > 0 && !ws) return MOE_ERR_NULL;
+  if (ws_bytes < route_ws_bytes(desc)) return MOE_ERR_WORKSPACE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const int T = desc->T, E = desc->E, k = desc->k;
+  const uint64_t d = desc->d;
+  const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
+  int32_t* chunk = static_cast<int32_t*>(ws);
+  cudaError_t e = cudaMemsetAsync(row_src, 0xFF, sizeof(int32_t) * desc->capacity, stream);
+  if (e == cudaSuccess && T > 0) {
+    e = cudaMemsetAsync(chunk, 0, sizeof(int32_t) * nchunks * E, stream);
+    // logits = x W_r^T on the tensor cores, top-k + softmax + histogram in the epilogue
+    GemmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.status = di->status;
+    g.E = 1;
+    g.capacity = (T + kAlign - 1) / kAlign * kAlign;
+    g.dense_rows = T;
+    if (!encode_map(&g.tma_a, x, d, T, 1, d * 2, static_cast<uint64_t>(T) * d * 2, 64, 128) ||
+        !encode_map(&g.tma_b, w_router, d, E, 1, d * 2, static_cast<uint64_t>(E) * d * 2, 64,
+                    256))
+      return MOE_ERR_SHAPE;
+    g.K = desc->d;
+    g.n_ext = E;
+    g.b_ext = E;
+    g.topk = k;
+    g.r_bias = bias;
+    g.r_idx = topk_idx;
+    g.r_w = topk_w;
+    g.r_hist = chunk;
+    g.r_logits = logits;
+    if (e == cudaSuccess) e = launch_grouped_gemm(kRouter, g, grid_for(di, desc), stream);
+  }
+  if (e == cudaSuccess) {
+    if (T > 0)
+      e = launch_scan(chunk, nchunks, E, desc->capacity, counts, offsets, padded_offsets,
+                      tile_prefix, di->status, stream);
+    else
+      e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
+    if (e == cudaSuccess && T == 0)
+      e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
+                                     tile_prefix, di->status, stream);
+  }
+  if (e == cudaSuccess && T > 0)
+    e = launch_assign(topk_idx, T, E, k, chunk, padded_offsets, row_src, row_of, di->status,
+                      stream);
+  if (e == cudaSuccess)
+    e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
+                           di->sms, stream);
+  return cuda_status(e);
+}
+
 moe_status_t moe_group_offsets(const moe_mlp_desc_t* desc, const int32_t* counts,
                                int32_t* offsets, int32_t* padded_offsets,
                                int32_t* tile_prefix, cudaStream_t stream) {

@@ -366,8 +366,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   const int E = args.E;
 
   // ---- group tables (sizes live in device memory; no host round trip)
-  for (int i = threadIdx.x; i <= E; i += GEMM_THREADS) s_off[i] = args.padded_offsets[i];
+  __shared__ int s_dense_cnt;
   const int* __restrict__ s_cnt = args.counts;   // group sizes read through L1
+  if (args.dense_rows > 0) {                     // one dense group (router GEMM)
+    if (threadIdx.x == 0) {
+      s_off[0] = 0;
+      s_off[1] = (args.dense_rows + BM - 1) / BM * BM;
+      s_dense_cnt = args.dense_rows;
+    }
+    s_cnt = &s_dense_cnt;
+  } else {
+    for (int i = threadIdx.x; i <= E; i += GEMM_THREADS) s_off[i] = args.padded_offsets[i];
+  }
   if (threadIdx.x == 0) {
     s_abort = 0;
     for (int s = 0; s < STAGES; ++s) {
@@ -474,7 +484,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             tma_load_3d(sa, &args.tma_a, fb, kk, ti.m0, 0);
           }
           // ---- B operand
-          if (MODE == kFc1Glu || MODE == kFc2 || MODE == kFc1Act) {
+          if (MODE == kFc1Glu || MODE == kFc2 || MODE == kFc1Act || MODE == kRouter) {
             tma_load_3d(sb, &args.tma_b, fb, kk, ti.n0, ti.e);
           } else if (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kDgradAct) {
             if (args.b_atoms4d)
@@ -623,7 +633,56 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       const uint32_t tbase =
           tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * BN + hc;
 
-      if (MODE == kFc1Glu) {
+      if (MODE == kRouter) {
+        // one token per lane (rows of this quarter): top-k of logit + bias
+        // over the E accumulator columns, ties to the lower expert, read 32
+        // columns at a time; softmax of the selected raw logits
+        if (half == 0) {
+          const int Ec = args.n_ext, kk = args.topk;
+          float sv[kMaxTopK], lv[kMaxTopK];
+          int iv[kMaxTopK];
+          int cnt = 0;
+          const uint32_t trow = tbase - hc;
+#pragma unroll 1
+          for (int c0 = 0; c0 < Ec; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(trow + c0, r);
+            tmem_ld_wait(r);
+#pragma unroll 1
+            for (int i = 0; i < 32 && c0 + i < Ec; ++i) {
+              const int e = c0 + i;
+              const float l = __uint_as_float(r[i]);
+              if (valid && args.r_logits) args.r_logits[gr * Ec + e] = l;
+              const float sc = l + (args.r_bias ? args.r_bias[e] : 0.0f);
+              if (cnt == kk && !(sc > sv[kk - 1])) continue;
+              int pos = cnt < kk ? cnt : kk - 1;
+              while (pos > 0 && sc > sv[pos - 1]) {
+                sv[pos] = sv[pos - 1];
+                lv[pos] = lv[pos - 1];
+                iv[pos] = iv[pos - 1];
+                --pos;
+              }
+              sv[pos] = sc;
+              lv[pos] = l;
+              iv[pos] = e;
+              if (cnt < kk) ++cnt;
+            }
+          }
+          if (valid) {
+            if (cnt < kk) set_status(args.status, MOE_DEV_BAD_EXPERT);   // non-finite scores
+            float mx_l = -INFINITY;
+            for (int s_ = 0; s_ < cnt; ++s_) mx_l = fmaxf(mx_l, lv[s_]);
+            float sum = 0.0f;
+            for (int s_ = 0; s_ < cnt; ++s_) sum += expf(lv[s_] - mx_l);
+            for (int s_ = 0; s_ < kk; ++s_) {
+              const int e = s_ < cnt ? iv[s_] : s_;
+              args.r_idx[gr * kk + s_] = e;
+              args.r_w[gr * kk + s_] = s_ < cnt ? expf(lv[s_] - mx_l) / sum : 0.0f;
+              atomicAdd(&args.r_hist[(gr / kTokensPerChunk) * Ec + e], 1);
+            }
+          }
+        }
+      } else if (MODE == kFc1Glu) {
         const __nv_bfloat16* b1 =
             args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld + ti.n0 + hc
                       : nullptr;
@@ -1194,6 +1253,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
     case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, false>(args, grid, s);
     case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, false>(args, grid, s);
+    case kRouter: return launch_mode<kRouter, 0, false>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -71,7 +71,8 @@ enum GemmMode : int {
   kWgrad = 4,      // dW[e] = sum over group rows of P^T Q      ragged K
   kWgradPair = 5,  // same on CTA pairs (2-SM MMA, 256x256 tiles)
   kFc1Act = 6,     // non-gated: H = X W1^T (+b1), A = act(H)   ragged M
-  kDgradAct = 7    // non-gated: dA = dY W2, dH = act'(H) dA     ragged M
+  kDgradAct = 7,   // non-gated: dA = dY W2, dH = act'(H) dA     ragged M
+  kRouter = 8      // logits = x W_r^T, top-k in the epilogue    one dense group
 };
 
 // FC1 output width: 2*F_pad (gate and linear halves, packed) for the GLU
@@ -126,6 +127,17 @@ struct GemmArgs {
   long long sfa_atoms;
   long long sfb_atoms;
   long long sfb_expert_bytes;
+  // one dense group of `dense_rows` rows instead of device offsets (router)
+  int dense_rows;
+  // kRouter outputs: per token the top-`topk` experts by logit + bias
+  // (fp32), their softmax weights over the raw logits, the per-chunk expert
+  // histogram, and optionally the logits themselves
+  int topk;
+  const float* r_bias;
+  int32_t* r_idx;
+  float* r_w;
+  int32_t* r_hist;
+  float* r_logits;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);

@@ -150,6 +150,16 @@ class MoEExpertMLP:
                                 self.counts, self.offsets, self.padded_offsets, self.tile_prefix,
                                 self.row_src, self.row_of, self.x_perm, self.ws, stream)
 
+    def route_fused(self, x, w_router, bias=None, logits_out=None, stream=None, timer=None):
+        """Routing from the tokens themselves: router GEMM (x W_r^T) with the
+        top-k in its epilogue, then the same permutation as route();
+        w_router bf16 [E,d]; logits_out fp32 [T,E] or None."""
+        with self._t(timer, "route_fused"):
+            L.moe_route_permute_fused(self.desc, x, w_router, bias, logits_out, self.topk_idx,
+                                      self.topk_w, self.counts, self.offsets,
+                                      self.padded_offsets, self.tile_prefix, self.row_src,
+                                      self.row_of, self.x_perm, self.ws, stream)
+
     def set_groups(self, counts, stream=None):
         """Groups given directly (no router): counts int32 [E] on device."""
         self.counts.copy_(counts)
