@@ -589,18 +589,25 @@ def measure_router(torch, layer, x, logits, bias, reps=20):
     """Routing from given logits (the step's moe_route_permute) against the
     fused router, which computes the logits itself (router GEMM x W_r^T,
     W_r seeded bf16 [E,d]) and takes the top-k in the GEMM epilogue, both
-    followed by the same permutation; CUDA events, medians."""
+    followed by the same permutation; each captured in a CUDA graph, CUDA
+    events around the replays, medians."""
     g = torch.Generator(device="cpu").manual_seed(5)
     w_r = (torch.randn((layer.E, layer.d), generator=g) / layer.d ** 0.5).to(torch.bfloat16)
     w_r = w_r.to(x.device)
 
     def timed(fn):
+        # captured in a CUDA graph, as the step is: device time only
+        fn()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            fn()
         ts = []
         for i in range(reps + 3):
             a = torch.cuda.Event(enable_timing=True)
             b = torch.cuda.Event(enable_timing=True)
             a.record()
-            fn()
+            graph.replay()
             b.record()
             torch.cuda.synchronize()
             if i >= 3:

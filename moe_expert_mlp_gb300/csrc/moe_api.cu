@@ -349,7 +349,7 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
     g.dense_rows = T;
     if (!encode_map(&g.tma_a, x, d, T, 1, d * 2, static_cast<uint64_t>(T) * d * 2, 64, 128) ||
         !encode_map(&g.tma_b, w_router, d, E, 1, d * 2, static_cast<uint64_t>(E) * d * 2, 64,
-                    256))
+                    static_cast<uint32_t>((E + 15) / 16 * 16)))
       return MOE_ERR_SHAPE;
     g.K = desc->d;
     g.n_ext = E;

@@ -445,8 +445,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         // boxes that hold at least one in-range column (skip fully-outside boxes)
         const int b_boxes = Tr::kBmn ? (args.b_atoms4d ? 4 : min(4, (args.b_ext - ti.n0 + 63) / 64)) : 1;
         const int a_boxes = Tr::kAmn ? min(2, (args.m_ext - ti.m0 + 63) / 64) : 1;
+        // the router's B tile is only as tall as the expert count (rounded to 16)
+        const uint32_t b_rows = MODE == kRouter ? (args.n_ext + 15) / 16 * 16 : BN;
         const uint32_t tx = (Tr::kAmn ? a_boxes * MN_BOX_BYTES : A_BYTES) +
-                            (Tr::kBmn ? b_boxes * MN_BOX_BYTES : B_BYTES);
+                            (Tr::kBmn ? b_boxes * MN_BOX_BYTES : b_rows * BK * 2);
         for (int kb = 0; kb < num_kb; ++kb) {
           if (!mbar_wait(&empty_bar[stage], phase ^ 1u, args.status, abort_flag)) {
             ok = false;
@@ -517,6 +519,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         if (!mbar_wait(&tempty_bar[acc], acc_par ^ 1u, args.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
+        // MMA width: 256, or for the router the expert count rounded to 16
+        const uint32_t idesc =
+            MODE == kRouter ? idesc_bf16(BM, (args.n_ext + 15) / 16 * 16, false, false) : Tr::kIdesc;
         // MX: this tile's scales go to the first columns of the other
         // accumulator, which the previous tile's epilogue must have read.
         const uint32_t sf_tmem = tmem_base + (acc ^ 1) * BN;
@@ -563,7 +568,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                                          : sdesc_sw128(a_base + k * 32, 16, 1024);
             const uint64_t bd = Tr::kBmn ? sdesc_sw128(b_base + k * 2048, MN_BOX_BYTES, 1024)
                                          : sdesc_sw128(b_base + k * 32, 16, 1024);
-            umma_bf16(d_tmem, ad, bd, Tr::kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+            umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
           if (++stage == STAGES) {
