@@ -28,3 +28,4 @@ differences, the MX format's own code table).  No function is unpinned.
 from .moe_oracle import *  # noqa: F401,F403
 from .mx_oracle import *  # noqa: F401,F403
 from .mx_mlp_oracle import *  # noqa: F401,F403
+from .nvfp4_oracle import *  # noqa: F401,F403
