@@ -83,7 +83,7 @@ def host_cores():
 
 
 # --------------------------------------------------------------- per-call work
-def call_work(wl, name, R):
+def call_work(wl, name, R, dtype="bf16"):
     """Algorithmic FLOPs or bytes of one library call over R real routed rows.
     GEMMs: 2*M*N*K with M = routed rows.  Memory-bound calls: bytes of the
     tensors they must read and write once (bf16 rows, index arrays ignored)."""
@@ -110,6 +110,11 @@ def call_work(wl, name, R):
         "quant_x": R * d * (2 + 2 + 2 / 32),
         "quant_dy": R * d * (2 + 2 + 2 / 32),
     }
+    if dtype == "nvfp4":
+        # bf16 rows in; rowwise and rotated transposed E2M1 codes (half a
+        # byte each) + one scale per 16 out; x and dY also read once for amax
+        mem.update(quant_x=R * d * (2 + 2 + 1 + 2 / 16), quant_dy=R * d * (2 + 2 + 1 + 2 / 16),
+                   quant_a=R * F * (2 + 1 + 2 / 16), quant_dh=R * n1 * (2 + 1 + 2 / 16))
     return "byte", float(mem.get(name, 0.0))
 
 
@@ -206,8 +211,26 @@ def _oracle_routed_mx(oracle, x, logits, bias, dout, W1, b1, W2, b2, k, p):
     oracle.route_backward(dw, topk_w, topk_idx, E)
 
 
-def oracle_sample_run(wl, inp, n_tokens, mx=False):
-    """Time the CPU oracle (its MXFP8 variant when mx) on the first n_tokens
+def _oracle_routed_nv(oracle, x, logits, bias, dout, W1, b1, W2, b2, k, p):
+    """The routed layer with the NVFP4 expert MLP (routing and combine as in
+    the bf16 oracle; dY rounded to the stored bf16)."""
+    E = W1.shape[0]
+    topk_idx, topk_w, counts = oracle.route(logits, bias, k)
+    _, padded, _ = oracle.group_offsets(counts, 128)
+    row_src, row_of = oracle.permute_index(topk_idx, E, padded)
+    xp = oracle.gather_rows(x, row_src)
+    Hh, A, Y = oracle.grouped_forward_nv(xp, padded, counts, W1, b1, W2, b2, p)
+    oracle.combine(Y, row_of, topk_w)
+    dY, dw = oracle.combine_backward(dout, Y, row_of, topk_w, xp.shape[0])
+    dX = oracle.grouped_backward_nv(xp, Hh, A, oracle.bf16_round(dY), padded, counts, W1, W2,
+                                    p)[0]
+    oracle.permute_backward(dX, row_of)
+    oracle.route_backward(dw, topk_w, topk_idx, E)
+
+
+def oracle_sample_run(wl, inp, n_tokens, fmt="bf16"):
+    """Time the CPU oracle (its MXFP8 / NVFP4 variant for fmt "mxfp8" /
+    "nvfp4") on the first n_tokens
     tokens (routed workloads) or on the first experts holding about n_tokens
     rows (direct workloads).  Returns (seconds, flops of the sample,
     description)."""
@@ -222,9 +245,9 @@ def oracle_sample_run(wl, inp, n_tokens, mx=False):
         x = bf16_bits_to_f64(inp["x"][:n])
         dout = bf16_bits_to_f64(inp["dout"][:n])
         t0 = time.perf_counter()
-        if mx:
-            _oracle_routed_mx(oracle, x, inp["logits"][:n], inp["bias"], dout, W1, b1, W2, b2,
-                              wl.k, p)
+        if fmt in ("mxfp8", "nvfp4"):
+            run = _oracle_routed_mx if fmt == "mxfp8" else _oracle_routed_nv
+            run(oracle, x, inp["logits"][:n], inp["bias"], dout, W1, b1, W2, b2, wl.k, p)
         else:
             fwd = oracle.moe_forward(x, inp["logits"][:n], inp["bias"], W1, b1, W2, b2, wl.k, p)
             oracle.moe_backward(fwd, dout, W1, W2, p)
@@ -252,9 +275,12 @@ def oracle_sample_run(wl, inp, n_tokens, mx=False):
                 xr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["x"][src_off[e]:src_off[e] + keep[e]])
                 dyr[lo:lo + keep[e]] = bf16_bits_to_f64(inp["dout"][src_off[e]:src_off[e] + keep[e]])
         t0 = time.perf_counter()
-        if mx:
+        if fmt == "mxfp8":
             Hh, A, Y = oracle.grouped_forward_mx(xr, padded, keep, W1, b1, W2, b2, p)
             oracle.grouped_backward_mx(xr, Hh, A, dyr, padded, keep, W1, W2, p)
+        elif fmt == "nvfp4":
+            Hh, A, Y = oracle.grouped_forward_nv(xr, padded, keep, W1, b1, W2, b2, p)
+            oracle.grouped_backward_nv(xr, Hh, A, dyr, padded, keep, W1, W2, p)
         else:
             Hh, A, Y = oracle.grouped_forward(xr, padded, keep, W1, b1, W2, b2, p)
             oracle.grouped_backward(xr, Hh, A, dyr, padded, keep, W1, W2, p)
@@ -271,14 +297,13 @@ def run_reference(args, wl):
         return 0
     inp = make_inputs(wl)
     n_tok = args.ref_sample_tokens
-    mx = args.dtype == "mxfp8"
     for _ in range(max(args.warmup, 0)):
-        oracle_sample_run(wl, inp, n_tok, mx)
+        oracle_sample_run(wl, inp, n_tok, args.dtype)
     times = []
     flops = 0.0
     desc = ""
     for _ in range(args.steps):
-        dt, flops, desc = oracle_sample_run(wl, inp, n_tok, mx)
+        dt, flops, desc = oracle_sample_run(wl, inp, n_tok, args.dtype)
         times.append(dt)
     total = sum(times)
     value = flops * args.steps / total / 1e12
@@ -344,7 +369,7 @@ def run_ours(args, wl):
                          alpha=wl.alpha, limit=wl.limit, linear_offset=wl.linear_offset,
                          out_scale=wl.out_scale, has_b1=wl.has_b1, has_b2=wl.has_b2,
                          capacity=cap, device=dev, dtype=args.dtype)
-    mx = args.dtype == "mxfp8"
+    mx = args.dtype in ("mxfp8", "nvfp4")      # block-scaled operands
     w1 = bits_to_dev(inp["w1"], dev)
     w2 = bits_to_dev(inp["w2"], dev)
     b1 = bits_to_dev(inp["b1"], dev) if inp["b1"] is not None else None
@@ -494,7 +519,7 @@ def run_ours(args, wl):
     kernels = {}
     dominant, dom_ms = None, -1.0
     for name, ts in per.items():
-        kind, work = call_work(wl, name, R)
+        kind, work = call_work(wl, name, R, args.dtype)
         avg = sum(ts) / len(ts)
         ent = {"ms": round(avg, 5)}
         if kind == "flop":
@@ -504,14 +529,17 @@ def run_ours(args, wl):
         elif work > 0:
             ent["gbs"] = round(work / (avg * 1e-3) / 1e9, 1)
         kernels[name] = ent
-    kind, work = call_work(wl, dominant, R)
+    kind, work = call_work(wl, dominant, R, args.dtype)
     dom_avg = sum(per[dominant]) / len(per[dominant])
     achieved = work / (dom_avg * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
     peak_note = f"{peak_src} bf16 burst (cuBLAS)"
-    if mx:   # no measured FP8 figure: bf16 measured x the nominal FP8/BF16 ratio (2)
+    if args.dtype == "mxfp8":   # no measured FP8 figure: bf16 measured x nominal FP8/BF16 (2)
         peak *= 2.0
         peak_note = f"{peak_src} bf16 burst (cuBLAS) x 2, the nominal FP8/BF16 dense ratio"
+    elif args.dtype == "nvfp4":  # bf16 measured x the nominal FP4/BF16 dense ratio (13.5/2.25)
+        peak *= 6.0
+        peak_note = f"{peak_src} bf16 burst (cuBLAS) x 6, the nominal FP4/BF16 dense ratio"
     tr = NCU_TRAFFIC.get((dominant, wl.name, args.dtype))
     traffic = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
     line = {
@@ -536,7 +564,7 @@ def run_ours(args, wl):
         "router": router,
     }
     if not args.no_cpu_baseline:
-        dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens, mx)
+        dt, fl, desc = oracle_sample_run(wl, inp, args.cpu_sample_tokens, args.dtype)
         line["cpu_baseline"] = {"value": fl / dt / 1e12, "unit": "TFLOPS", "cores": host_cores(),
                                 "kind": "oracle", "sample": desc}
     print(json.dumps(line))
@@ -765,8 +793,9 @@ def main():
                     help="tokens (or rows) of the oracle sample in the cpu_baseline leg")
     ap.add_argument("--ref-sample-tokens", type=int, default=256,
                     help="tokens (or rows) per step of --impl reference")
-    ap.add_argument("--dtype", choices=["bf16", "mxfp8"], default="bf16",
-                    help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales)")
+    ap.add_argument("--dtype", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
+                    help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales; nvfp4: E2M1 + "
+                         "UE4M3 scales per 16 + per-tensor scales)")
     ap.add_argument("--act", choices=["swiglu", "geglu", "sreglu", "srelu"], default=None,
                     help="override the workload's activation (the dense sweep)")
     ap.add_argument("--amax", action="store_true",

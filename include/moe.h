@@ -81,7 +81,10 @@ typedef enum {
  * by fusing MXFP8 and NVFP4 quantization"); requires d and F multiples of 32
  * and recompute_h = 0.  Routing, combine and their backward are bf16 in
  * both. */
-typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2 } moe_dtype_t;
+typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2, MOE_DTYPE_NVFP4 = 3 } moe_dtype_t;
+/* NVFP4 (the *_nv calls): E2M1 operands, one UE4M3 scale per 16 elements
+ * along each GEMM's contraction dimension and one fp32 encode scale per
+ * tensor from its amax; requires d and F multiples of 64 and recompute_h = 0. */
 
 /* GLU activations ([FK] "Overcoming training bottlenecks": SwiGLU, GeGLU,
  * sReLU with optional clamp and scaling).  With g the gate half, l the
@@ -464,6 +467,105 @@ moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
                             const int32_t* padded_offsets, const moe_mx_weights_t* w, void* dh,
                             const moe_mx_out_t* dh_mx, void* dx_perm, void* dw1p, void* db1p,
                             void* dw2, void* db2, cudaStream_t stream);
+
+/* ------------------------------------------------------------- NVFP4 path
+ * [FK] "Reducing exposed memory overhead by fusing MXFP8 and NVFP4
+ * quantization": for NVFP4 the GEMM epilogues emit the BF16 output with its
+ * per-tensor amax and the amax of its transposed Hadamard rotation, and the
+ * tensor is then quantized for the next NVFP4 GEMMs with the per-tensor
+ * scale those amax values give.  Readings: E2M1 values (+-{0, .5, 1, 1.5, 2,
+ * 3, 4, 6}, round to nearest even, saturating) in blocks of 16 along the
+ * contraction axis; per block a UE4M3 scale s = E4M3((amax_block / 6) * g)
+ * (round to nearest even, saturating at 448); per tensor g = 2688 / amax
+ * (1 for amax 0); a value is code * s / g; every step in fp32.  The copies
+ * that the weight gradients contract over tokens are rotated first by H16/4
+ * (Sylvester Hadamard) in 16-row segments inside each group and use the
+ * rotated tensor's amax.
+ *
+ * NVFP4 tensors are described by moe_mx_out_t with layout MOE_MX_SCALES_MMA:
+ *   q       packed E2M1 [rows, cols/2] (two values per byte, element 2i in
+ *           the low nibble), 16-byte aligned; scale: UE4M3 codes in the MMA
+ *           layout of MXFP8 with 16-element blocks (moe_nvfp4_scale_bytes).
+ *   qt      the transposed copy [cols, rows/2], scale_t its scales.
+ *   amax    float[2]: [0] the amax that encodes q, [1] the one that encodes
+ *           qt (for activations the rotated tensor's amax; for weights
+ *           both are the tensor's amax).
+ * The GEMMs divide the encode scales out of the accumulator (factor
+ * 1 / (g_a g_b)) before bias, activation and output. */
+
+/* Bytes of the NVFP4 scale buffer of a [rows, cols] operand (0 for empty):
+ * ceil(cols/64) * 2*ceil(rows/256) atoms of 512 bytes. */
+size_t moe_nvfp4_scale_bytes(int64_t rows, int64_t cols);
+
+/* amax[0] = max |x|, amax[1] = max |H16 x / 4| (each column rotated along
+ * the rows in 16-row segments) of bf16 [batch, rows, cols], rows % 16 == 0,
+ * cols even, over the rows below *row_limit (device int; NULL = all rows).
+ * amax is overwritten. */
+moe_status_t moe_amax_nvfp4(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                            const int32_t* row_limit, float* amax, cudaStream_t stream);
+
+/* bf16 [batch, rows, cols] (rows, cols multiples of 32) -> NVFP4 with the
+ * encode amax values in out->amax (device float[2], read on the device):
+ * rowwise (out->q) and/or transposed (out->qt, rotated by H16/4 along the
+ * rows when rotate_t != 0).  Scales per batch entry: moe_nvfp4_scale_bytes
+ * (rows, cols) resp. (cols, rows). */
+moe_status_t moe_quantize_nvfp4_bf16(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                                     const moe_mx_out_t* out, int32_t rotate_t,
+                                     cudaStream_t stream);
+
+/* An activation [capacity, width] (x_perm, A, dY or dH) in NVFP4: rowwise
+ * and/or the rotated transposed copy, only rows below padded_offsets[E].
+ * compute_amax != 0: out->amax is first computed from the tensor (x_perm,
+ * dY); 0: out->amax already holds it (A, dH: written by the GEMM epilogue). */
+moe_status_t moe_quantize_act_nvfp4(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                    const int32_t* padded_offsets, const moe_mx_out_t* out,
+                                    int32_t compute_amax, cudaStream_t stream);
+
+/* NVFP4 copies of the expert weights: as moe_mx_weights_t (w1 [E, W1, d/2]
+ * rowwise along d, w1t [E, d, W1/2], w2 [E, d, F/2], w2t [E, F, d/2], scales
+ * per expert moe_nvfp4_scale_bytes) plus amax: device float[4], written by
+ * moe_quantize_weights_nvfp4: [0] = max|W1p| (encodes w1 and w1t), [2] =
+ * max|W2| (w2, w2t); [1] and [3] hold the rotated amax, which is unused. */
+typedef struct {
+  moe_mx_weights_t q;
+  float* amax;
+} moe_nv_weights_t;
+
+moe_status_t moe_quantize_weights_nvfp4(const moe_mlp_desc_t* desc, const void* w1p,
+                                        const void* w2, const moe_nv_weights_t* out,
+                                        cudaStream_t stream);
+
+/* The NVFP4 grouped GEMMs (desc->dtype = MOE_DTYPE_NVFP4), as the *_mx
+ * calls, with NVFP4 operands:
+ *   moe_fc1_glu_fwd_nv    h, a, a_amax  <- x_nv (q), w1      a_amax: float[2]
+ *   moe_fc2_fwd_nv        y             <- a_nv (q), w2
+ *   moe_fc2_dgrad_dglu_nv dh, dh_amax   <- dy_nv (q), w2t, h dh_amax: float[2]
+ *   moe_fc2_wgrad_nv      dw2           <- dy_nv, a_nv (qt: rotated copies)
+ *   moe_fc1_dgrad_nv      dx_perm       <- dh_nv (q), w1t
+ *   moe_fc1_wgrad_nv      dw1p          <- dh_nv, x_nv (qt: rotated copies)
+ * a_amax / dh_amax receive the plain and rotated amax of the bf16 A / dH
+ * (over real rows), which moe_quantize_act_nvfp4 then uses. */
+moe_status_t moe_fc1_glu_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_nv,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const moe_nv_weights_t* w, const void* b1p, void* h, void* a,
+                                float* a_amax, cudaStream_t stream);
+moe_status_t moe_fc2_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_nv,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_nv_weights_t* w, const void* b2, void* y,
+                            cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_nv,
+                                   const void* h, const int32_t* counts,
+                                   const int32_t* padded_offsets, const moe_nv_weights_t* w,
+                                   void* dh, float* dh_amax, cudaStream_t stream);
+moe_status_t moe_fc2_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_nv,
+                              const moe_mx_out_t* a_nv, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw2, cudaStream_t stream);
+moe_status_t moe_fc1_dgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_nv,
+                              const int32_t* counts, const int32_t* padded_offsets,
+                              const moe_nv_weights_t* w, void* dx_perm, cudaStream_t stream);
+moe_status_t moe_fc1_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_nv,
+                              const moe_mx_out_t* x_nv, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw1p, cudaStream_t stream);
 
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 
 MOE_DTYPE_BF16 = 1
 MOE_DTYPE_MXFP8 = 2
+MOE_DTYPE_NVFP4 = 3
 MOE_MX_SCALES_ROWMAJOR = 0
 MOE_MX_SCALES_MMA = 1
 ACTS = {"swiglu": 0, "geglu": 1, "srelu": 2, "sreglu": 3}
@@ -34,7 +35,10 @@ EXPORTS = (
     "moe_mx_scale_bytes", "moe_quantize_mx_bf16", "moe_quantize_act_mx",
     "moe_quantize_weights_mx", "moe_mlp_fwd_mx", "moe_mlp_bwd_mx", "moe_fc1_glu_fwd_mx",
     "moe_fc2_fwd_mx", "moe_fc2_dgrad_dglu_mx", "moe_fc2_wgrad_mx", "moe_fc1_dgrad_mx",
-    "moe_fc1_wgrad_mx", "moe_route_permute_fused",
+    "moe_fc1_wgrad_mx", "moe_route_permute_fused", "moe_nvfp4_scale_bytes", "moe_amax_nvfp4",
+    "moe_quantize_nvfp4_bf16", "moe_quantize_act_nvfp4", "moe_quantize_weights_nvfp4",
+    "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
+    "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv",
 )
 
 
@@ -65,6 +69,18 @@ class moe_mx_weights_t(ctypes.Structure):
                 ("w1", "w1_s", "w1t", "w1t_s", "w2", "w2_s", "w2t", "w2t_s")]
 
 
+class moe_nv_weights_t(ctypes.Structure):
+    _fields_ = [("q", moe_mx_weights_t), ("amax", ctypes.c_void_p)]
+
+
+def _nvw(w):
+    """dict of the eight NVFP4 weight tensors + "amax" (float[4]) ->
+    moe_nv_weights_t pointer."""
+    q = moe_mx_weights_t(*[_p(w[k]).value for k in
+                           ("w1", "w1_s", "w1t", "w1t_s", "w2", "w2_s", "w2t", "w2t_s")])
+    return ctypes.byref(moe_nv_weights_t(q, _p(w["amax"]).value))
+
+
 def _mx(mx):
     """dict of optional tensors {q, scale, qt, scale_t, amax} (+ "layout":
     "mma" for the MMA scale layout) -> struct pointer."""
@@ -89,7 +105,7 @@ def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_off
     if capacity is None:
         capacity = T * k + E * 127
         capacity = (capacity + 127) // 128 * 128
-    dt = {"bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8}[dtype]
+    dt = {"bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8, "nvfp4": MOE_DTYPE_NVFP4}[dtype]
     return moe_mlp_desc_t(T, E, k, d, F, dt, ACTS[act], alpha, limit, linear_offset,
                           out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity,
                           int(recompute_h))
@@ -150,6 +166,20 @@ def lib():
             "moe_fc2_wgrad_mx": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_dgrad_mx": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_wgrad_mx": (ctypes.c_int, [D] + [P] * 6),
+            "moe_nvfp4_scale_bytes": (ctypes.c_size_t, [ctypes.c_int64, ctypes.c_int64]),
+            "moe_amax_nvfp4": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                              P, P, P]),
+            "moe_quantize_nvfp4_bf16": (ctypes.c_int, [P, ctypes.c_int64, ctypes.c_int64,
+                                                       ctypes.c_int64, P, ctypes.c_int32, P]),
+            "moe_quantize_act_nvfp4": (ctypes.c_int, [D, P, ctypes.c_int32, P, P,
+                                                      ctypes.c_int32, P]),
+            "moe_quantize_weights_nvfp4": (ctypes.c_int, [D, P, P, P, P]),
+            "moe_fc1_glu_fwd_nv": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_fwd_nv": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc2_dgrad_dglu_nv": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_dgrad_nv": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -402,4 +432,62 @@ def moe_fc1_dgrad_mx(desc, dh_mx, counts, padded_offsets, w_mx, dx_perm, stream=
 
 def moe_fc1_wgrad_mx(desc, dh_mx, x_mx, counts, padded_offsets, dw1p, stream=None):
     _check(lib().moe_fc1_wgrad_mx(ctypes.byref(desc), _mx(dh_mx), _mx(x_mx), _p(counts),
+                                  _p(padded_offsets), _p(dw1p), _stream(stream)))
+
+
+# ------------------------------------------------------------------ NVFP4
+def moe_nvfp4_scale_bytes(rows, cols):
+    return int(lib().moe_nvfp4_scale_bytes(rows, cols))
+
+
+def moe_amax_nvfp4(inp, batch, rows, cols, amax, row_limit=None, stream=None):
+    _check(lib().moe_amax_nvfp4(_p(inp), batch, rows, cols, _p(row_limit), _p(amax),
+                                _stream(stream)))
+
+
+def moe_quantize_nvfp4_bf16(inp, batch, rows, cols, out, rotate_t=False, stream=None):
+    _check(lib().moe_quantize_nvfp4_bf16(_p(inp), batch, rows, cols, _mx(out),
+                                         int(bool(rotate_t)), _stream(stream)))
+
+
+def moe_quantize_act_nvfp4(desc, inp, width, padded_offsets, out, compute_amax, stream=None):
+    _check(lib().moe_quantize_act_nvfp4(ctypes.byref(desc), _p(inp), width, _p(padded_offsets),
+                                        _mx(out), int(bool(compute_amax)), _stream(stream)))
+
+
+def moe_quantize_weights_nvfp4(desc, w1p, w2, out, stream=None):
+    _check(lib().moe_quantize_weights_nvfp4(ctypes.byref(desc), _p(w1p), _p(w2), _nvw(out),
+                                            _stream(stream)))
+
+
+def moe_fc1_glu_fwd_nv(desc, x_nv, counts, padded_offsets, w_nv, b1p, h, a, a_amax, stream=None):
+    _check(lib().moe_fc1_glu_fwd_nv(ctypes.byref(desc), _mx(x_nv), _p(counts),
+                                    _p(padded_offsets), _nvw(w_nv), _p(b1p), _p(h), _p(a),
+                                    _p(a_amax), _stream(stream)))
+
+
+def moe_fc2_fwd_nv(desc, a_nv, counts, padded_offsets, w_nv, b2, y, stream=None):
+    _check(lib().moe_fc2_fwd_nv(ctypes.byref(desc), _mx(a_nv), _p(counts), _p(padded_offsets),
+                                _nvw(w_nv), _p(b2), _p(y), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_nv(desc, dy_nv, h, counts, padded_offsets, w_nv, dh, dh_amax,
+                          stream=None):
+    _check(lib().moe_fc2_dgrad_dglu_nv(ctypes.byref(desc), _mx(dy_nv), _p(h), _p(counts),
+                                       _p(padded_offsets), _nvw(w_nv), _p(dh), _p(dh_amax),
+                                       _stream(stream)))
+
+
+def moe_fc2_wgrad_nv(desc, dy_nv, a_nv, counts, padded_offsets, dw2, stream=None):
+    _check(lib().moe_fc2_wgrad_nv(ctypes.byref(desc), _mx(dy_nv), _mx(a_nv), _p(counts),
+                                  _p(padded_offsets), _p(dw2), _stream(stream)))
+
+
+def moe_fc1_dgrad_nv(desc, dh_nv, counts, padded_offsets, w_nv, dx_perm, stream=None):
+    _check(lib().moe_fc1_dgrad_nv(ctypes.byref(desc), _mx(dh_nv), _p(counts),
+                                  _p(padded_offsets), _nvw(w_nv), _p(dx_perm), _stream(stream)))
+
+
+def moe_fc1_wgrad_nv(desc, dh_nv, x_nv, counts, padded_offsets, dw1p, stream=None):
+    _check(lib().moe_fc1_wgrad_nv(ctypes.byref(desc), _mx(dh_nv), _mx(x_nv), _p(counts),
                                   _p(padded_offsets), _p(dw1p), _stream(stream)))

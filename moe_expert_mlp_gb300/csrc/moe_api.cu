@@ -107,7 +107,8 @@ moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
   if (d->d < 64 || d->d % 64 != 0) return MOE_ERR_SHAPE;
   if (d->F < 32 || d->F % 32 != 0) return MOE_ERR_SHAPE;
   if (d->align != kAlign) return MOE_ERR_UNSUPPORTED;
-  if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8 && d->dtype != MOE_DTYPE_NVFP4)
+    return MOE_ERR_UNSUPPORTED;
   if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU &&
       d->act != MOE_ACT_SRELU)
     return MOE_ERR_UNSUPPORTED;
@@ -1154,6 +1155,315 @@ moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
     return st;
   if (db1p || db2) return moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream);
   return MOE_OK;
+}
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// NVFP4 path: the same grouped-GEMM modes with packed E2M1 operands (K-major;
+// 128-byte boxes hold 256 values), UE4M3 scales per 16 values in the MMA
+// layout, and the operands' encode amax values for the epilogue's 1/(g_a g_b).
+namespace moe {
+namespace {
+
+moe_status_t check_nv_desc(const moe_mlp_desc_t* d) {
+  moe_status_t st = check_desc(d, false);
+  if (st != MOE_OK) return st;
+  if (d->dtype != MOE_DTYPE_NVFP4 || d->recompute_h) return MOE_ERR_UNSUPPORTED;
+  if (d->F % 64 != 0) return MOE_ERR_SHAPE;
+  return MOE_OK;
+}
+
+// NVFP4 tensor: the needed parts, the MMA layout, 16-byte aligned codes and
+// the encode amax pair.
+bool nv_ok(const moe_mx_out_t* m, bool row, bool col) {
+  return mx_ok(m, row, col) && m->amax != nullptr;
+}
+
+bool nv_weights_ok(const moe_nv_weights_t* w) { return w && mx_weights_ok(&w->q) && w->amax; }
+
+void set_nv_scales(GemmArgs& g, const uint8_t* sfa, long long a_rows, const uint8_t* sfb,
+                   long long b_rows, long long b_expert_bytes, const float* amax_a,
+                   const float* amax_b) {
+  set_scales(g, sfa, a_rows, sfb, b_rows, b_expert_bytes);
+  g.nv_amax_a = amax_a;
+  g.nv_amax_b = amax_b;
+}
+
+// epilogue amax outputs only (plain and rotated amax of the bf16 result)
+moe_status_t set_amax_out(GemmArgs& g, float* amax, long long width, cudaStream_t stream) {
+  moe_mx_out_t m;
+  memset(&m, 0, sizeof(m));
+  m.amax = amax;
+  m.layout = MOE_MX_SCALES_MMA;
+  return set_mx(g, &m, width, stream);
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+size_t moe_nvfp4_scale_bytes(int64_t rows, int64_t cols) {
+  if (rows <= 0 || cols <= 0) return 0;
+  return static_cast<size_t>(nv_sf_bytes(rows, cols));
+}
+
+moe_status_t moe_amax_nvfp4(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                            const int32_t* row_limit, float* amax, cudaStream_t stream) {
+  if (!in || !amax) return MOE_ERR_NULL;
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 16 != 0 || cols % 2 != 0) return MOE_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(in) & 3) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_amax_nv(in, batch, rows, cols, row_limit, amax, di->sms, stream));
+}
+
+moe_status_t moe_quantize_nvfp4_bf16(const void* in, int64_t batch, int64_t rows, int64_t cols,
+                                     const moe_mx_out_t* out, int32_t rotate_t,
+                                     cudaStream_t stream) {
+  if (!in || !out) return MOE_ERR_NULL;
+  if (!nv_ok(out, out->q != nullptr, out->qt != nullptr) || (!out->q && !out->qt))
+    return MOE_ERR_NULL;
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 32 != 0 || cols % 32 != 0)
+    return MOE_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(in) & 15) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  return cuda_status(launch_quant_nv(in, batch, rows, cols, static_cast<uint8_t*>(out->q),
+                                     static_cast<uint8_t*>(out->scale),
+                                     static_cast<uint8_t*>(out->qt),
+                                     static_cast<uint8_t*>(out->scale_t), out->amax,
+                                     out->amax + 1, rotate_t != 0, nullptr, di->sms, stream));
+}
+
+moe_status_t moe_quantize_act_nvfp4(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                    const int32_t* padded_offsets, const moe_mx_out_t* out,
+                                    int32_t compute_amax, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (!in || !padded_offsets || !out) return MOE_ERR_NULL;
+  if (!nv_ok(out, out->q != nullptr, out->qt != nullptr) || (!out->q && !out->qt))
+    return MOE_ERR_NULL;
+  if (width < 64 || width % 64 != 0) return MOE_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(in) & 15) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const int32_t* lim = padded_offsets + desc->E;
+  cudaError_t e = cudaSuccess;
+  if (compute_amax) e = launch_amax_nv(in, 1, desc->capacity, width, lim, out->amax, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_quant_nv(in, 1, desc->capacity, width, static_cast<uint8_t*>(out->q),
+                        static_cast<uint8_t*>(out->scale), static_cast<uint8_t*>(out->qt),
+                        static_cast<uint8_t*>(out->scale_t), out->amax, out->amax + 1, 1, lim,
+                        di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_quantize_weights_nvfp4(const moe_mlp_desc_t* desc, const void* w1p,
+                                        const void* w2, const moe_nv_weights_t* out,
+                                        cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!w1p || !w2 || !nv_weights_ok(out)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const long long E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const moe_mx_weights_t& q = out->q;
+  cudaError_t e = launch_amax_nv(w1p, 1, E * W1, d, nullptr, out->amax, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_amax_nv(w2, 1, E * d, F, nullptr, out->amax + 2, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_quant_nv(w1p, E, W1, d, static_cast<uint8_t*>(q.w1), static_cast<uint8_t*>(q.w1_s),
+                        static_cast<uint8_t*>(q.w1t), static_cast<uint8_t*>(q.w1t_s), out->amax,
+                        out->amax, 0, nullptr, di->sms, stream);
+  if (e == cudaSuccess)
+    e = launch_quant_nv(w2, E, d, F, static_cast<uint8_t*>(q.w2), static_cast<uint8_t*>(q.w2_s),
+                        static_cast<uint8_t*>(q.w2t), static_cast<uint8_t*>(q.w2t_s),
+                        out->amax + 2, out->amax + 2, 0, nullptr, di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_fc1_glu_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_nv,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const moe_nv_weights_t* w, const void* b1p, void* h, void* a,
+                                float* a_amax, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !nv_weights_ok(w) || !h || !a || !a_amax) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!nv_ok(x_nv, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // x_perm (codes [cap, d/2]) x W1p (codes [E, W1, d/2]); GLU epilogue
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, x_nv->q, d / 2, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->q.w1, d / 2, W1, E, 256) ||
+      !encode_out(&g.tma_out0, h, W1, cap, 1) || !encode_out(&g.tma_out1, a, F, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(W1);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = W1;
+  g.out1 = a;
+  g.ld1 = F;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  set_nv_scales(g, x_nv->scale, cap, w->q.w1_s, W1, nv_sf_bytes(W1, d), x_nv->amax, w->amax);
+  if ((st = set_amax_out(g, a_amax, desc->F, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm_nv(desc->act == MOE_ACT_SRELU ? kFc1Act : kFc1Glu, g,
+                                            grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_nv,
+                            const int32_t* counts, const int32_t* padded_offsets,
+                            const moe_nv_weights_t* w, const void* b2, void* y,
+                            cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !nv_weights_ok(w) || !y) return MOE_ERR_NULL;
+  if (desc->has_b2 && !b2) return MOE_ERR_NULL;
+  if (!nv_ok(a_nv, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  // A (codes [cap, F/2]) x W2 (codes [E, d, F/2])
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, a_nv->q, F / 2, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->q.w2, F / 2, d, E, 256) || !encode_out(&g.tma_out0, y, d, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->F;
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = y;
+  g.ld0 = d;
+  g.bias = desc->has_b2 ? b2 : nullptr;
+  g.bias_ld = d;
+  set_nv_scales(g, a_nv->scale, cap, w->q.w2_s, d, nv_sf_bytes(d, F), a_nv->amax, w->amax + 2);
+  return cuda_status(launch_grouped_gemm_nv(kFc2, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_dgrad_dglu_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_nv,
+                                   const void* h, const int32_t* counts,
+                                   const int32_t* padded_offsets, const moe_nv_weights_t* w,
+                                   void* dh, float* dh_amax, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!h || !counts || !padded_offsets || !nv_weights_ok(w) || !dh || !dh_amax)
+    return MOE_ERR_NULL;
+  if (!nv_ok(dy_nv, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
+                 W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // dY (codes [cap, d/2]) x W2^T (codes [E, F, d/2]); dGLU epilogue reads H
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dy_nv->q, d / 2, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->q.w2t, d / 2, F, E, 256) ||
+      !encode_out(&g.tma_out0, dh, W1, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = desc->act == MOE_ACT_SRELU ? desc->F : static_cast<int>(Fp);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = W1;
+  g.aux = h;
+  g.ld_aux = W1;
+  set_nv_scales(g, dy_nv->scale, cap, w->q.w2t_s, F, nv_sf_bytes(F, d), dy_nv->amax,
+                w->amax + 2);
+  if ((st = set_amax_out(g, dh_amax, W1, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm_nv(desc->act == MOE_ACT_SRELU ? kDgradAct : kDgradDglu,
+                                            g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dy_nv,
+                              const moe_mx_out_t* a_nv, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw2, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
+  if (!nv_ok(dy_nv, false, true) || !nv_ok(a_nv, false, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F;
+  const uint64_t cap = desc->capacity;
+  // dW2[e] = (H dY)^T (H A) over the group's rows: codes [d, cap/2], [F, cap/2]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dy_nv->qt, cap / 2, d, 1, 128) ||
+      !encode_u8(&g.tma_b, a_nv->qt, cap / 2, F, 1, 256) || !encode_out(&g.tma_out0, dw2, F, d, E))
+    return MOE_ERR_SHAPE;
+  g.m_ext = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = dw2;
+  g.ld0 = F;
+  set_nv_scales(g, dy_nv->scale_t, d, a_nv->scale_t, F, 0, dy_nv->amax + 1, a_nv->amax + 1);
+  return cuda_status(launch_grouped_gemm_nv(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_dgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_nv,
+                              const int32_t* counts, const int32_t* padded_offsets,
+                              const moe_nv_weights_t* w, void* dx_perm, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !nv_weights_ok(w) || !dx_perm) return MOE_ERR_NULL;
+  if (!nv_ok(dh_nv, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // dH (codes [cap, W1/2]) x W1p^T (codes [E, d, W1/2])
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dh_nv->q, W1 / 2, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->q.w1t, W1 / 2, d, E, 256) ||
+      !encode_out(&g.tma_out0, dx_perm, d, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = static_cast<int>(W1);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dx_perm;
+  g.ld0 = d;
+  set_nv_scales(g, dh_nv->scale, cap, w->q.w1t_s, d, nv_sf_bytes(d, W1), dh_nv->amax, w->amax);
+  return cuda_status(launch_grouped_gemm_nv(kDgradFc1, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_nv,
+                              const moe_mx_out_t* x_nv, const int32_t* counts,
+                              const int32_t* padded_offsets, void* dw1p, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
+  if (!nv_ok(dh_nv, false, true) || !nv_ok(x_nv, false, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // dW1p[e] = (H dH)^T (H X) over the group's rows: codes [W1, cap/2], [d, cap/2]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dh_nv->qt, cap / 2, W1, 1, 128) ||
+      !encode_u8(&g.tma_b, x_nv->qt, cap / 2, d, 1, 256) ||
+      !encode_out(&g.tma_out0, dw1p, d, W1, E))
+    return MOE_ERR_SHAPE;
+  g.m_ext = static_cast<int>(W1);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dw1p;
+  g.ld0 = d;
+  set_nv_scales(g, dh_nv->scale_t, W1, x_nv->scale_t, d, 0, dh_nv->amax + 1, x_nv->amax + 1);
+  return cuda_status(launch_grouped_gemm_nv(kWgrad, g, grid_for(di, desc), stream));
 }
 
 }  // extern "C"

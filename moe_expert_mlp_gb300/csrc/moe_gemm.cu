@@ -72,6 +72,18 @@ constexpr size_t SMEM_BYTES_MX = 1024 + static_cast<size_t>(STAGES) * STAGE_BYTE
 // both 32-column aligned.  The epilogue releases them once it has read the
 // accumulator's first 64 columns.
 constexpr uint32_t kSfaCol = 0, kSfbCol = 32;
+// NVFP4 operands: packed E2M1 (two per byte), so a 128-byte row holds 256
+// values and a stage covers K = 256, four MMAs of K = 64.  Every MMA takes
+// its own scale atoms (A: one 512-byte atom, B: two), 6 KB per stage; with
+// three stages the full output ring still fits.
+constexpr int BK_NV = 256;
+constexpr int STAGES_NV = 3;
+constexpr int SF_STAGE_BYTES_NV = 6144;
+constexpr size_t SMEM_BYTES_NV = 1024 + static_cast<size_t>(STAGES_NV) *
+                                            (STAGE_BYTES + SF_STAGE_BYTES_NV) +
+                                 kRing * BOX_BYTES;
+// operand formats of k_grouped_gemm
+constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2;
 
 struct Tile {
   int e;        // expert
@@ -298,18 +310,28 @@ __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v
 }
 
 // bf16: the backward reads transposed operands MN-major from the forward's
-// buffers.  MXFP8: every operand is K-major (the transposed copies are
-// quantized along the contraction dimension).
-template <int MODE, bool MX>
+// buffers.  MXFP8 / NVFP4: every operand is K-major (the transposed copies
+// are quantized along the contraction dimension).
+template <int MODE, int OP>
 struct Traits {
+  static constexpr bool kScaled = OP != kOpBf16;
   static constexpr bool kRaggedK = (MODE == kWgrad);
-  static constexpr bool kAmn = !MX && (MODE == kWgrad);
-  static constexpr bool kBmn =
-      !MX && (MODE == kDgradDglu || MODE == kDgradFc1 || MODE == kWgrad || MODE == kDgradAct);
+  static constexpr bool kAmn = !kScaled && (MODE == kWgrad);
+  static constexpr bool kBmn = !kScaled && (MODE == kDgradDglu || MODE == kDgradFc1 ||
+                                            MODE == kWgrad || MODE == kDgradAct);
   static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
-  static constexpr int kBK = MX ? BK_MX : BK;
-  static constexpr int kNR = MX ? kRingMx : kRing;
+  static constexpr int kBK = OP == kOpNv ? BK_NV : (OP == kOpMx ? BK_MX : BK);
+  static constexpr int kNR = OP == kOpMx ? kRingMx : kRing;
+  static constexpr int kStages = OP == kOpNv ? STAGES_NV : STAGES;
+  static constexpr int kSfStage =
+      OP == kOpNv ? SF_STAGE_BYTES_NV : (OP == kOpMx ? SF_STAGE_BYTES : 0);
 };
+
+// Accumulator factor of an NVFP4 GEMM: both operands were encoded with
+// g = 2688 / amax of their tensor, so the product carries g_a g_b.
+__device__ __forceinline__ float nv_encode_scale(float amax) {
+  return amax > 0.0f ? __fdiv_rn(2688.0f, amax) : 1.0f;
+}
 
 template <int MODE, int KB>
 __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, const int* s_off,
@@ -345,12 +367,14 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
   return ti;
 }
 
-template <int MODE, int ACT, bool MX>
+template <int MODE, int ACT, int OP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
-  using Tr = Traits<MODE, MX>;
+  using Tr = Traits<MODE, OP>;
+  constexpr bool MX = OP == kOpMx, NV = OP == kOpNv;
+  constexpr int NST = Tr::kStages;
   extern __shared__ uint8_t dyn_smem[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t full_bar[NST];
+  __shared__ __align__(8) uint64_t empty_bar[NST];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t tearly_bar[2];   // MX: first chunk of an accumulator read
@@ -380,7 +404,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   }
   if (threadIdx.x == 0) {
     s_abort = 0;
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < NST; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
@@ -457,12 +481,38 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           uint8_t* sa = smem + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           uint64_t* fb = &full_bar[stage];
+          if constexpr (NV) {
+            // packed E2M1 tiles (K-major, 256 K per 128-byte row; the TMA
+            // coordinate is in bytes) and the scale atoms of each K = 64
+            // step that lies inside K (the last stage of a group or of an
+            // odd K may hold fewer than four)
+            const int kx = (Tr::kRaggedK ? ti.k_row0 : 0) + kb * BK_NV;
+            const int krem = (Tr::kRaggedK ? s_cnt[ti.e] : args.K) - kb * BK_NV;
+            const int nk = min(4, (krem + 63) / 64);
+            mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + nk * 1536);
+            uint8_t* ssf = smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES_NV;
+            tma_load_3d(sa, &args.tma_a, fb, kx / 2, ti.m0, 0);
+            tma_load_3d(sb, &args.tma_b, fb, kx / 2, ti.n0, Tr::kRaggedK ? 0 : ti.e);
+            const uint8_t* sfb_e = args.sfb + (Tr::kRaggedK ? 0 : ti.e * args.sfb_expert_bytes);
+            for (int k = 0; k < nk; ++k) {
+              const long long kt = kx / 64 + k;        // atom column of this K = 64 step
+              bulk_load(ssf + k * 512, args.sfa + (kt * args.sfa_atoms + (ti.m0 >> 7)) * 512,
+                        512, fb);
+              bulk_load(ssf + 2048 + k * 1024,
+                        sfb_e + (kt * args.sfb_atoms + (ti.n0 >> 7)) * 512, 1024, fb);
+            }
+            if (++stage == NST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if constexpr (MX) {
             // E4M3 tiles (K-major, 128 K per row) and their scale atoms
             mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SF_STAGE_BYTES);
             const int kx = (Tr::kRaggedK ? ti.k_row0 : 0) + kb * BK_MX;
             const long long kt = kx / BK_MX;
-            uint8_t* ssf = smem + STAGES * STAGE_BYTES + stage * SF_STAGE_BYTES;
+            uint8_t* ssf = smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES;
             tma_load_3d(sa, &args.tma_a, fb, kx, ti.m0, 0);
             tma_load_3d(sb, &args.tma_b, fb, kx, ti.n0, Tr::kRaggedK ? 0 : ti.e);
             bulk_load(ssf, args.sfa + (kt * args.sfa_atoms + (ti.m0 >> 7)) * 512, 512, fb);
@@ -470,7 +520,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                       args.sfb + (Tr::kRaggedK ? 0 : ti.e * args.sfb_expert_bytes) +
                           (kt * args.sfb_atoms + (ti.n0 >> 7)) * 512,
                       1024, fb);
-            if (++stage == STAGES) {
+            if (++stage == NST) {
               stage = 0;
               phase ^= 1u;
             }
@@ -498,7 +548,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             for (int i = 0; i < b_boxes; ++i)
               tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b, fb, ti.n0 + 64 * i, ti.k_row0 + kk, 0);
           }
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -525,7 +575,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         // MX: this tile's scales go to the first columns of the other
         // accumulator, which the previous tile's epilogue must have read.
         const uint32_t sf_tmem = tmem_base + (acc ^ 1) * BN;
-        if constexpr (MX) {
+        if constexpr (MX || NV) {
           if (it > 0) {
             if (!mbar_wait(&tearly_bar[acc ^ 1], ((it - 1) >> 1) & 1, args.status, abort_flag))
               break;
@@ -540,11 +590,35 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_BYTES;
+          if constexpr (NV) {
+            // per K = 64 step (32 bytes along the swizzled rows): its scale
+            // atoms to TMEM -- one 32-bit cell per row holding the four
+            // 16-element block scales -- then its MMA.  tcgen05.cp and
+            // tcgen05.mma from this thread run in issue order.
+            const int krem = (Tr::kRaggedK ? s_cnt[ti.e] : args.K) - kb * BK_NV;
+            const int nk = min(4, (krem + 63) / 64);
+            const uint32_t sf = smem_u32(smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES_NV);
+            for (int k = 0; k < nk; ++k) {
+              tmem_cp_32x128_x4(sf_tmem + kSfaCol, sdesc_noswz(sf + k * 512, 128, 128));
+              tmem_cp_32x128_x4(sf_tmem + kSfbCol, sdesc_noswz(sf + 2048 + k * 1024, 128, 128));
+              tmem_cp_32x128_x4(sf_tmem + kSfbCol + 4,
+                                sdesc_noswz(sf + 2048 + k * 1024 + 512, 128, 128));
+              umma_nvf4(d_tmem, sdesc_sw128(a_base + k * 32, 16, 1024),
+                        sdesc_sw128(b_base + k * 32, 16, 1024), idesc_nvf4(BM, BN),
+                        sf_tmem + kSfaCol, sf_tmem + kSfbCol, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == NST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if constexpr (MX) {
             // scales smem -> TMEM, then 4 MMAs of K = 32 (32 bytes apart in
             // the swizzled rows); MMA k takes byte k of each scale column.
             // tcgen05.cp and tcgen05.mma from this thread run in issue order.
-            const uint32_t sf = smem_u32(smem + STAGES * STAGE_BYTES + stage * SF_STAGE_BYTES);
+            const uint32_t sf = smem_u32(smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES);
             tmem_cp_32x128_x4(sf_tmem + kSfaCol, sdesc_noswz(sf, 128, 128));
             tmem_cp_32x128_x4(sf_tmem + kSfbCol, sdesc_noswz(sf + 512, 128, 128));
             tmem_cp_32x128_x4(sf_tmem + kSfbCol + 4, sdesc_noswz(sf + 1024, 128, 128));
@@ -554,7 +628,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                       sdesc_sw128(b_base + k * 32, 16, 1024), idesc_mx(BM, BN, k, k),
                       sf_tmem + kSfaCol, sf_tmem + kSfbCol, (kb > 0 || k > 0) ? 1u : 0u);
             umma_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
+            if (++stage == NST) {
               stage = 0;
               phase ^= 1u;
             }
@@ -571,7 +645,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             umma_bf16(d_tmem, ad, bd, idesc, (kb > 0 || k > 0) ? 1u : 0u);
           }
           umma_commit(&empty_bar[stage]);
-          if (++stage == STAGES) {
+          if (++stage == NST) {
             stage = 0;
             phase ^= 1u;
           }
@@ -590,7 +664,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
     const int hc = 16 * half;                 // first column of this warp's share
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
-    uint8_t* const ring_mem = smem + STAGES * STAGE_BYTES + (MX ? STAGES * SF_STAGE_BYTES : 0);
+    uint8_t* const ring_mem = smem + NST * STAGE_BYTES + NST * Tr::kSfStage;
     StoreRing ring{smem_u32(ring_mem), 0, ring_mem};
     const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
     const MxOut mx{args.mx_q, args.mx_s, args.mx_qt, args.mx_st, args.mx_amax, args.mx_width,
@@ -598,13 +672,18 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
     // MX: tell the MMA warp that the accumulator's first 64 columns have
     // been read (the next tile stages its scales there).  Once per tile.
     auto early_release = [&](int acc_id) {
-      if constexpr (MX) {
+      if constexpr (MX || NV) {
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tearly_bar[acc_id]);
       }
     };
     const bool want_mx = mx.q != nullptr || mx.qt != nullptr || mx.amax != nullptr;
+    // NVFP4: undo the two operands' encode scales on the accumulator
+    float nv_alpha = 1.0f;
+    if constexpr (NV)
+      nv_alpha = __fdiv_rn(1.0f, __fmul_rn(nv_encode_scale(__ldg(args.nv_amax_a)),
+                                           nv_encode_scale(__ldg(args.nv_amax_b))));
     float am_m = 0.0f, am_h = 0.0f;           // running amax (plain, Hadamard) of this lane
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
@@ -704,6 +783,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           for (int i = 0; i < 16; ++i) {
             g[i] = __uint_as_float(rg[i]);
             l[i] = __uint_as_float(rl[i]);
+            if constexpr (NV) {
+              g[i] *= nv_alpha;
+              l[i] *= nv_alpha;
+            }
           }
           if (j + 1 < kGluHalf / 32) {        // next chunk's accumulator in flight
             tmem_ld16(tbase + 32 * (j + 1), rg);
@@ -765,7 +848,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           }
           tmem_ld_wait16(r);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          for (int i = 0; i < 16; ++i)
+            ra[i] = NV ? __float_as_uint(__uint_as_float(r[i]) * nv_alpha) : r[i];
           tmem_ld16(tbase + 32 * (j + 1), r);
           const bool live0 = valid && f0 < args.f_real;
           if (live0) dglu_compute16<ACT>(ra, hg[0], hl[0], ap, dg, dl);
@@ -797,7 +881,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           tmem_ld_wait16(r);
           if (j == 0) early_release(acc);             // columns 0-63 read
 #pragma unroll
-          for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          for (int i = 0; i < 16; ++i)
+            ra[i] = NV ? __float_as_uint(__uint_as_float(r[i]) * nv_alpha) : r[i];
           if (j + 2 < nch) tmem_ld16(tbase + 32 * (j + 2), r);
           const bool live1 = valid && f1 < args.f_real;
           if (live1) dglu_compute16<ACT>(ra, hg[1], hl[1], ap, dg, dl);
@@ -853,6 +938,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             for (int i = 0; i < 16; ++i) {
               v0[i] = __uint_as_float(ra[i]);
               v1[i] = __uint_as_float(rb[i]);
+              if constexpr (NV) {
+                v0[i] *= nv_alpha;
+                v1[i] *= nv_alpha;
+              }
             }
             if (j + 2 < nch) tmem_ld16(tbase + 32 * (j + 2), ra);
             if (j + 3 < nch) tmem_ld16(tbase + 32 * (j + 3), rb);
@@ -1224,23 +1313,25 @@ cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int MODE, int ACT, bool MX>
+template <int MODE, int ACT, int OP>
 cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
-  constexpr size_t smem = MX ? SMEM_BYTES_MX : SMEM_BYTES;
-  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT, MX>,
+  constexpr size_t smem =
+      OP == kOpNv ? SMEM_BYTES_NV : (OP == kOpMx ? SMEM_BYTES_MX : SMEM_BYTES);
+  static_assert(smem <= 232448, "shared memory per CTA");
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<MODE, ACT, MX><<<grid, GEMM_THREADS, smem, s>>>(args);
+  k_grouped_gemm<MODE, ACT, OP><<<grid, GEMM_THREADS, smem, s>>>(args);
   return cudaGetLastError();
 }
 
-template <int MODE, bool MX>
+template <int MODE, int OP>
 cudaError_t launch_act(const GemmArgs& args, int grid, cudaStream_t s) {
   switch (args.act) {
-    case MOE_ACT_SWIGLU: return launch_mode<MODE, MOE_ACT_SWIGLU, MX>(args, grid, s);
-    case MOE_ACT_GEGLU: return launch_mode<MODE, MOE_ACT_GEGLU, MX>(args, grid, s);
-    case MOE_ACT_SREGLU: return launch_mode<MODE, MOE_ACT_SREGLU, MX>(args, grid, s);
+    case MOE_ACT_SWIGLU: return launch_mode<MODE, MOE_ACT_SWIGLU, OP>(args, grid, s);
+    case MOE_ACT_GEGLU: return launch_mode<MODE, MOE_ACT_GEGLU, OP>(args, grid, s);
+    case MOE_ACT_SREGLU: return launch_mode<MODE, MOE_ACT_SREGLU, OP>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1251,27 +1342,40 @@ size_t grouped_gemm_smem_bytes() { return SMEM_BYTES; }
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
   switch (mode) {
-    case kFc1Glu: return launch_act<kFc1Glu, false>(args, grid, s);
-    case kFc2: return launch_mode<kFc2, 0, false>(args, grid, s);
-    case kDgradDglu: return launch_act<kDgradDglu, false>(args, grid, s);
-    case kDgradFc1: return launch_mode<kDgradFc1, 0, false>(args, grid, s);
+    case kFc1Glu: return launch_act<kFc1Glu, kOpBf16>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0, kOpBf16>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu, kOpBf16>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0, kOpBf16>(args, grid, s);
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
-    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, false>(args, grid, s);
-    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, false>(args, grid, s);
-    case kRouter: return launch_mode<kRouter, 0, false>(args, grid, s);
+    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpBf16>(args, grid, s);
+    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, kOpBf16>(args, grid, s);
+    case kRouter: return launch_mode<kRouter, 0, kOpBf16>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
 
 cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
   switch (mode) {
-    case kFc1Glu: return launch_act<kFc1Glu, true>(args, grid, s);
-    case kFc2: return launch_mode<kFc2, 0, true>(args, grid, s);
-    case kDgradDglu: return launch_act<kDgradDglu, true>(args, grid, s);
-    case kDgradFc1: return launch_mode<kDgradFc1, 0, true>(args, grid, s);
-    case kWgrad: return launch_mode<kWgrad, 0, true>(args, grid, s);
-    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, true>(args, grid, s);
-    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, true>(args, grid, s);
+    case kFc1Glu: return launch_act<kFc1Glu, kOpMx>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0, kOpMx>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu, kOpMx>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0, kOpMx>(args, grid, s);
+    case kWgrad: return launch_mode<kWgrad, 0, kOpMx>(args, grid, s);
+    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpMx>(args, grid, s);
+    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, kOpMx>(args, grid, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_grouped_gemm_nv(int mode, const GemmArgs& args, int grid, cudaStream_t s) {
+  switch (mode) {
+    case kFc1Glu: return launch_act<kFc1Glu, kOpNv>(args, grid, s);
+    case kFc2: return launch_mode<kFc2, 0, kOpNv>(args, grid, s);
+    case kDgradDglu: return launch_act<kDgradDglu, kOpNv>(args, grid, s);
+    case kDgradFc1: return launch_mode<kDgradFc1, 0, kOpNv>(args, grid, s);
+    case kWgrad: return launch_mode<kWgrad, 0, kOpNv>(args, grid, s);
+    case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpNv>(args, grid, s);
+    case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, kOpNv>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

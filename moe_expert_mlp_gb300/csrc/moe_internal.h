@@ -138,15 +138,35 @@ struct GemmArgs {
   float* r_w;
   int32_t* r_hist;
   float* r_logits;
+  // NVFP4 operands (launch_grouped_gemm_nv): per-tensor amax of the
+  // quantized A and B operands; the epilogue scales the accumulator by
+  // 1 / (g_a g_b), g = 2688 / amax (1 for amax 0)
+  const float* nv_amax_a;
+  const float* nv_amax_b;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);
 // The same modes with block-scaled MXFP8 operands (kWgrad: 1-CTA tiles).
 cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cudaStream_t s);
+// The ragged-M modes and kWgrad with NVFP4 operands: packed E2M1 codes
+// (K-major, 128-byte boxes = 256 values) and UE4M3 scales per 16 values in
+// the MMA layout (sf_mma_offset with 16-element blocks).
+cudaError_t launch_grouped_gemm_nv(int mode, const GemmArgs& args, int grid, cudaStream_t s);
 cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows, long long cols,
                                  uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
                                  int mma_layout, const int32_t* row_limit, int num_sms,
                                  cudaStream_t stream);
+// NVFP4 quantization (moe_nvfp4.cu): scale-buffer bytes of a [rows, cols]
+// operand; per-tensor plain and 16-row-Hadamard amax (zeroed first); the
+// rowwise / (rotated) transposed quantizer with encode amax pointers.
+long long nv_sf_bytes(long long rows, long long cols);
+cudaError_t launch_amax_nv(const void* in, long long batch, long long rows, long long cols,
+                           const int32_t* row_limit, float* amax, int num_sms,
+                           cudaStream_t stream);
+cudaError_t launch_quant_nv(const void* in, long long batch, long long rows, long long cols,
+                            uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
+                            const float* amax_row, const float* amax_col, int rotate,
+                            const int32_t* row_limit, int num_sms, cudaStream_t stream);
 size_t grouped_gemm_smem_bytes();
 
 }  // namespace moe

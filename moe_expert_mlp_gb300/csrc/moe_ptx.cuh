@@ -281,6 +281,32 @@ __device__ __forceinline__ void umma_mx(uint32_t d_tmem, uint64_t a_desc, uint64
       : "memory");
 }
 
+// Instruction descriptor for kind::mxf4nvf4 with 16-element UE4M3 block
+// scales (scale_vec::4X): A and B format E2M1 (code 1), scale type bit 23
+// clear (UE4M3), scale bytes 0 (each 32-bit scale cell holds the four
+// 16-element blocks of one K = 64 step).
+__host__ __device__ constexpr uint32_t idesc_nvf4(int M, int N) {
+  return (1u << 7)                                      // A format: E2M1
+         | (1u << 10)                                   // B format: E2M1
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= (A * sA)[smem] * (B * sB)[smem]^T, one K=64 step of packed
+// E2M1 operands (two values per byte, element 2i in the low nibble); the
+// scale cell of row r sits at lane r % 32, column r / 32 from the address.
+__device__ __forceinline__ void umma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X "
+      "[%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
 // Shared memory -> TMEM: 32 rows x 16 bytes, written to the same 32 lanes
 // of every lane quadrant, 4 columns wide.  Executes in issue order with
 // this thread's tcgen05.mma.

@@ -27,6 +27,9 @@ class MoEExpertMLP:
         # dtype "mxfp8": the grouped GEMMs read MXFP8 operands (E4M3 codes,
         # E8M0 scales per 32 elements); routing and combine stay bf16
         self.mx = dtype == "mxfp8"
+        # dtype "nvfp4": packed E2M1 operands with UE4M3 scales per 16
+        # elements and per-tensor encode scales from their amax
+        self.nv = dtype == "nvfp4"
         # optional fused NVFP4-preparation outputs (per-tensor amax of A and
         # of dH, plain and Hadamard-rotated): float[2] device tensors or None
         self.amax_a = None
@@ -99,6 +102,37 @@ class MoEExpertMLP:
                              w2=z(E, d, F, dtype=u8), w2_s=sc(d, F),
                              w2t=z(E, F, d, dtype=u8), w2t_s=sc(F, d))
 
+        if self.nv:
+            # activations: rowwise for the GEMM that contracts over features,
+            # the rotated transposed copy for the weight gradient
+            self.x_nv = self.nv_operand(d)
+            self.a_nv = self.nv_operand(F)
+            self.dy_nv = self.nv_operand(d)
+            self.dh_nv = self.nv_operand(self.W1)
+            u8 = torch.uint8
+
+            def scn(rows, cols):
+                return z(E * L.moe_nvfp4_scale_bytes(rows, cols), dtype=u8)
+
+            W1 = self.W1
+            self.w_nv = dict(w1=z(E, W1, d // 2, dtype=u8), w1_s=scn(W1, d),
+                             w1t=z(E, d, W1 // 2, dtype=u8), w1t_s=scn(d, W1),
+                             w2=z(E, d, F // 2, dtype=u8), w2_s=scn(d, F),
+                             w2t=z(E, F, d // 2, dtype=u8), w2t_s=scn(F, d),
+                             amax=z(4, dtype=f32))
+
+    def nv_operand(self, width):
+        """NVFP4 buffers of a per-row tensor [capacity, width]: packed rowwise
+        codes + scales, the rotated transposed copy, and its encode amax pair
+        (plain, rotated)."""
+        cap, dev, u8 = self.capacity, self.w2.device, torch.uint8
+        return dict(q=torch.zeros((cap, width // 2), dtype=u8, device=dev),
+                    scale=torch.zeros(L.moe_nvfp4_scale_bytes(cap, width), dtype=u8, device=dev),
+                    qt=torch.zeros((width, cap // 2), dtype=u8, device=dev),
+                    scale_t=torch.zeros(L.moe_nvfp4_scale_bytes(width, cap), dtype=u8,
+                                        device=dev),
+                    amax=torch.zeros(2, dtype=torch.float32, device=dev), layout="mma")
+
     def mx_operand(self, width):
         """MXFP8 buffers of a per-row tensor [capacity, width] in the MMA scale
         layout: rowwise codes + scales and the transposed copy.  Scale
@@ -120,13 +154,16 @@ class MoEExpertMLP:
         self.w2.copy_(w2)
         if self.has_b2:
             self.b2.copy_(b2)
-        if self.mx:
+        if self.mx or self.nv:
             self.quantize_weights(stream)
 
     def quantize_weights(self, stream=None):
-        """MXFP8 weight copies (rowwise and transposed) from the bf16 masters;
-        once per optimizer step."""
-        L.moe_quantize_weights_mx(self.desc, self.w1p, self.w2, self.w_mx, stream)
+        """MXFP8 / NVFP4 weight copies (rowwise and transposed) from the bf16
+        masters; once per optimizer step."""
+        if self.nv:
+            L.moe_quantize_weights_nvfp4(self.desc, self.w1p, self.w2, self.w_nv, stream)
+        else:
+            L.moe_quantize_weights_mx(self.desc, self.w1p, self.w2, self.w_mx, stream)
 
     def unpack_fc1(self, packed, width, stream=None):
         """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p);
@@ -180,6 +217,18 @@ class MoEExpertMLP:
         c, po = self.counts, self.padded_offsets
         if a_mx is None and self.amax_a is not None and not self.mx:
             a_mx = dict(amax=self.amax_a)
+        if self.nv:
+            with self._t(timer, "quant_x"):
+                L.moe_quantize_act_nvfp4(self.desc, self.x_perm, self.d, po, self.x_nv, True,
+                                         stream)
+            with self._t(timer, "fc1_glu_fwd"):
+                L.moe_fc1_glu_fwd_nv(self.desc, self.x_nv, c, po, self.w_nv, self.b1p, self.h,
+                                     self.a, self.a_nv["amax"], stream)
+            with self._t(timer, "quant_a"):
+                L.moe_quantize_act_nvfp4(self.desc, self.a, self.F, po, self.a_nv, False, stream)
+            with self._t(timer, "fc2_fwd"):
+                L.moe_fc2_fwd_nv(self.desc, self.a_nv, c, po, self.w_nv, self.b2, self.y, stream)
+            return
         if self.mx:
             with self._t(timer, "quant_x"):
                 L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
@@ -200,6 +249,26 @@ class MoEExpertMLP:
         c, po = self.counts, self.padded_offsets
         if dh_mx is None and self.amax_dh is not None and not self.mx:
             dh_mx = dict(amax=self.amax_dh)
+        if self.nv:
+            with self._t(timer, "quant_dy"):
+                L.moe_quantize_act_nvfp4(self.desc, self.dy, self.d, po, self.dy_nv, True, stream)
+            with self._t(timer, "fc2_dgrad_dglu"):
+                L.moe_fc2_dgrad_dglu_nv(self.desc, self.dy_nv, self.h, c, po, self.w_nv, self.dh,
+                                        self.dh_nv["amax"], stream)
+            with self._t(timer, "quant_dh"):
+                L.moe_quantize_act_nvfp4(self.desc, self.dh, self.W1, po, self.dh_nv, False,
+                                         stream)
+            with self._t(timer, "fc2_wgrad"):
+                L.moe_fc2_wgrad_nv(self.desc, self.dy_nv, self.a_nv, c, po, self.dw2, stream)
+            with self._t(timer, "fc1_dgrad"):
+                L.moe_fc1_dgrad_nv(self.desc, self.dh_nv, c, po, self.w_nv, self.dx_perm, stream)
+            with self._t(timer, "fc1_wgrad"):
+                L.moe_fc1_wgrad_nv(self.desc, self.dh_nv, self.x_nv, c, po, self.dw1p, stream)
+            if self.has_b1 or self.has_b2:
+                with self._t(timer, "bias_grads"):
+                    L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2,
+                                     stream)
+            return
         if self.mx:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
@@ -300,8 +369,9 @@ class MoEExpertMLP:
     def kernels_per_step(self, routed=True):
         """Kernels of this library launched by one step() (routed) or
         grouped_step(): six grouped GEMMs, one column-sum per bias, the two
-        activation quantizations of the MXFP8 layer, and for
+        activation quantizations of the MXFP8 layer (NVFP4: four quantizations
+        and two amax passes), and for
         the routed layer top-k, scan, assign, gather, combine, pad-row zeroing,
         combine backward, permute backward and router backward."""
-        n = 6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0)
+        n = 6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0) + (6 if self.nv else 0)
         return n + (9 if routed else 0)

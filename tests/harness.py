@@ -207,3 +207,68 @@ def run_both_direct_mx(wl, inp):
     layer.mlp_backward()
     torch.cuda.synchronize()
     return layer, ref
+
+
+# ------------------------------------------------------------------ NVFP4
+TOL_NV = 0.1        # max|gpu - ref| <= 0.1 * max|ref| downstream of a requantized intermediate
+TOL_NV_FRO = 2e-2   # and ||gpu - ref||_F <= 2e-2 ||ref||_F
+
+E2M1_SIGNED = np.array([0, .5, 1, 1.5, 2, 3, 4, 6, 0, -.5, -1, -1.5, -2, -3, -4, -6])
+
+
+def unpack_fp4_codes(q):
+    """Packed E2M1 bytes [..., n/2] -> 4-bit codes [..., n] (element 2i in
+    the low nibble)."""
+    q = np.asarray(q, dtype=np.uint8)
+    out = np.empty(q.shape[:-1] + (2 * q.shape[-1],), dtype=np.uint8)
+    out[..., 0::2] = q & 0xF
+    out[..., 1::2] = q >> 4
+    return out
+
+
+def nv_scales_to_rowmajor(buf, rows, cols):
+    """NVFP4 scales in the MMA layout (16-element blocks) -> [rows, cols/16]."""
+    buf = np.asarray(buf).reshape(-1)
+    ra = 2 * ((rows + 255) // 256)
+    r = np.arange(rows)[:, None]
+    j = np.arange(cols // 16)[None, :]
+    off = ((j // 4) * ra + r // 128) * 512 + (r % 32) * 16 + ((r // 32) % 4) * 4 + j % 4
+    return buf[off]
+
+
+def nv_dequant(q, scale_buf, amax, rows, cols):
+    """Values of an NVFP4 tensor [rows, cols] as the GPU encoded it (codes,
+    UE4M3 scales in the MMA layout, encode amax), decoded with the oracle's
+    formula value = code * s / g."""
+    codes = unpack_fp4_codes(np.asarray(q).reshape(rows, cols // 2))
+    s = oracle.e4m3_decode(nv_scales_to_rowmajor(scale_buf, rows, cols))
+    g = oracle.nvfp4_global_scale(float(amax))
+    return oracle.nvfp4_dequantize_rows(E2M1_SIGNED[codes], s, g)
+
+
+def run_both_direct_nv(wl, inp):
+    """Groups given directly, NVFP4 expert MLP on both sides."""
+    sizes = inp["group_sizes"]
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    offsets, padded, tiles = oracle.group_offsets(sizes, align=128)
+    xp_bits = padded_rows(inp["x"], sizes, padded, wl.d)
+    dy_bits = padded_rows(inp["dout"], sizes, padded, wl.d)
+    xp = bf16_bits_to_f64(xp_bits)
+    dyp = bf16_bits_to_f64(dy_bits)
+    H, A, Y = oracle.grouped_forward_nv(xp, padded, sizes, W1, b1, W2, b2, p)
+    dX, dH, dW1, db1, dW2, db2 = oracle.grouped_backward_nv(xp, H, A, dyp, padded, sizes, W1,
+                                                           W2, p)
+    ref = dict(H=H, A=A, Y=Y, dX_perm=dX, dH=dH, dW1=dW1, db1=db1, dW2=dW2, db2=db2,
+               padded_offsets=padded, counts=sizes)
+    cap = max(128, int(padded[-1]))
+    layer = make_layer(wl, capacity=cap, dtype="nvfp4")
+    load_layer_weights(layer, inp)
+    layer.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
+    R_pad = int(padded[-1])
+    layer.x_perm[:R_pad].copy_(bits_to_dev(xp_bits))
+    layer.dy[:R_pad].copy_(bits_to_dev(dy_bits))
+    layer.mlp_forward()
+    layer.mlp_backward()
+    torch.cuda.synchronize()
+    return layer, ref

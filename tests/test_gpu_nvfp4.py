@@ -1,0 +1,216 @@
+"""NVFP4 path against the oracle, through the C-ABI.
+
+* The amax and quantize kernels are checked bit for bit (E2M1 codes, UE4M3
+  scale codes, amax values) against the oracle on identical inputs; the
+  rotated transposed copy on inputs whose 16-row Hadamard sums are exact in
+  fp32 (integers times 2^-6), so both sides decide on the same values.
+  Signed zeros compare as zero.
+* Each grouped GEMM is checked against the fp64 product of its operands as
+  the GPU encoded them (decoded with the oracle's NVFP4 formula), with the
+  bf16 bound: this isolates the block-scaled MMA, the scale layout, the
+  per-tensor factor 1/(g_a g_b), ragged K tails and the epilogues.
+* The whole expert MLP is checked against the NVFP4 oracle
+  (grouped_forward_nv / grouped_backward_nv).  H and dH see identically
+  quantized operands (bf16 bound); outputs downstream of a requantized
+  intermediate (A, dH, or a rotated copy) may see single codes flip where
+  accumulation rounding moved a value across a decision boundary, so they
+  get max|gpu-ref| <= 0.1 max|ref| and a 2% Frobenius bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_mlp_gb300 import _lib as L
+from tests import harness as H
+from workloads import WORKLOADS, bf16_bits_to_f64, f32_to_bf16_bits, make_inputs, scaled
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+
+def _zero_signs(codes):
+    codes = np.asarray(codes, dtype=np.uint8)
+    return np.where((codes & 7) == 0, 0, codes)
+
+
+def _inputs(kind, rows, cols, seed):
+    rng = np.random.default_rng(seed)
+    if kind == "grid":
+        v = rng.integers(-127, 128, (rows, cols)).astype(np.float32) * np.float32(2.0 ** -6)
+        v[rng.random((rows, cols)) < 0.05] = 0.0
+    else:
+        v = (rng.standard_normal((rows, cols)) *
+             np.exp(rng.standard_normal((rows, 1)))).astype(np.float32)
+    bits = f32_to_bf16_bits(v)
+    return bits, bf16_bits_to_f64(bits)
+
+
+def _quantize_gpu(bits, rows, cols, rotate):
+    x = H.bits_to_dev(bits)
+    amax = torch.zeros(2, dtype=torch.float32, device="cuda")
+    L.moe_amax_nvfp4(x, 1, rows, cols, amax)
+    u8 = torch.uint8
+    out = dict(q=torch.zeros((rows, cols // 2), dtype=u8, device="cuda"),
+               scale=torch.zeros(L.moe_nvfp4_scale_bytes(rows, cols), dtype=u8, device="cuda"),
+               qt=torch.zeros((cols, rows // 2), dtype=u8, device="cuda"),
+               scale_t=torch.zeros(L.moe_nvfp4_scale_bytes(cols, rows), dtype=u8, device="cuda"),
+               amax=amax, layout="mma")
+    L.moe_quantize_nvfp4_bf16(x, 1, rows, cols, out, rotate_t=rotate)
+    torch.cuda.synchronize()
+    return {k: (H.to_np(v) if isinstance(v, torch.Tensor) else v) for k, v in out.items()}
+
+
+def _check_codes(name, q_gpu, sc_gpu_buf, rows, cols, vals, g):
+    q_ref, sc_ref, _ = oracle.nvfp4_quantize_rows(vals.astype(np.float32), g)
+    codes = H.unpack_fp4_codes(q_gpu)
+    assert np.array_equal(_zero_signs(codes), _zero_signs(oracle.e2m1_encode(q_ref))), name
+    assert np.array_equal(H.nv_scales_to_rowmajor(sc_gpu_buf, rows, cols), sc_ref), name
+
+
+@pytest.mark.parametrize("kind,rows,cols", [("grid", 256, 320), ("grid", 96, 128),
+                                             ("random", 256, 320), ("random", 384, 192)])
+def test_quantizer_bit_exact(kind, rows, cols):
+    bits, v = _inputs(kind, rows, cols, seed=rows + cols)
+    rotate = kind == "grid"
+    out = _quantize_gpu(bits, rows, cols, rotate)
+    amax = out["amax"]
+    assert amax[0] == np.float32(np.max(np.abs(v)))
+    vt = oracle.rht16_rows(v) if rotate else v
+    if rotate:                                       # exact sums on the grid inputs
+        assert amax[1] == np.float32(np.max(np.abs(vt)))
+    _check_codes("rowwise", out["q"], out["scale"], rows, cols, v,
+                 oracle.nvfp4_global_scale(amax[0]))
+    _check_codes("transposed", out["qt"], out["scale_t"], cols, rows, vt.T,
+                 oracle.nvfp4_global_scale(amax[1]))
+
+
+def test_quantizer_plain_transpose_random():
+    """The transposed copy without rotation, on non-grid values, encoded
+    with the tensor's amax: bit exact."""
+    rows, cols = 192, 256
+    bits, v = _inputs("random", rows, cols, seed=5)
+    x = H.bits_to_dev(bits)
+    a = float(np.max(np.abs(v)))
+    amax = torch.tensor([a, a], dtype=torch.float32, device="cuda")
+    u8 = torch.uint8
+    out = dict(qt=torch.zeros((cols, rows // 2), dtype=u8, device="cuda"),
+               scale_t=torch.zeros(L.moe_nvfp4_scale_bytes(cols, rows), dtype=u8, device="cuda"),
+               amax=amax, layout="mma")
+    L.moe_quantize_nvfp4_bf16(x, 1, rows, cols, out, rotate_t=False)
+    torch.cuda.synchronize()
+    _check_codes("transposed", H.to_np(out["qt"]), H.to_np(out["scale_t"]), cols, rows, v.T,
+                 oracle.nvfp4_global_scale(a))
+
+
+BASE = WORKLOADS["dsv3_r16384_e32"]
+CASES = {
+    # K tails: d = 320 is one full K stage plus one MMA; F = 192 three MMAs
+    "swiglu_d320": scaled(BASE, R=577, E=4, d=320, F=192, zipf_empty=1, w_std=0.05),
+    "gptoss_like": scaled(WORKLOADS["gptoss_t16384_e32"], router="direct", R=450, E=5, d=192,
+                          F=192, zipf_s=1.1, zipf_empty=1, w_std=0.05),
+    "srelu_nongated": scaled(BASE, R=300, E=3, d=256, F=128, act="srelu", zipf_empty=0,
+                             w_std=0.05),
+}
+
+
+def _groups(layer):
+    po = H.to_np(layer.padded_offsets)
+    cnt = H.to_np(layer.counts)
+    return [(e, int(po[e]), int(cnt[e])) for e in range(layer.E) if cnt[e] > 0]
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_gemms_on_gpu_codes(name):
+    """Every NVFP4 GEMM equals the fp64 product of its GPU-encoded operands."""
+    wl = CASES[name]
+    inp = make_inputs(wl)
+    layer, _ = H.run_both_direct_nv(wl, inp)
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    p = H.glu_params(wl)
+    E, d, F, W1, cap = layer.E, layer.d, layer.F, layer.W1, layer.capacity
+    g = {n: H.to_np(t) for n, t in layer.w_nv.items()}
+    wa = g["amax"]
+    w1q = [H.nv_dequant(g["w1"][e], g["w1_s"].reshape(E, -1)[e], wa[0], W1, d) for e in range(E)]
+    w1tq = [H.nv_dequant(g["w1t"][e], g["w1t_s"].reshape(E, -1)[e], wa[0], d, W1) for e in range(E)]
+    w2q = [H.nv_dequant(g["w2"][e], g["w2_s"].reshape(E, -1)[e], wa[2], d, F) for e in range(E)]
+    w2tq = [H.nv_dequant(g["w2t"][e], g["w2t_s"].reshape(E, -1)[e], wa[2], F, d) for e in range(E)]
+
+    def act(nv, width, rowwise=True):
+        t = {k: H.to_np(v) for k, v in nv.items() if isinstance(v, torch.Tensor)}
+        if rowwise:
+            return H.nv_dequant(t["q"], t["scale"], t["amax"][0], cap, width)
+        return H.nv_dequant(t["qt"], t["scale_t"], t["amax"][1], width, cap)
+
+    Xq, Aq, dYq, dHq = act(layer.x_nv, d), act(layer.a_nv, F), act(layer.dy_nv, d), act(layer.dh_nv, W1)
+    Xt, At, dYt, dHt = (act(layer.x_nv, d, False), act(layer.a_nv, F, False),
+                        act(layer.dy_nv, d, False), act(layer.dh_nv, W1, False))
+    h, a, y = H.to_np(layer.h), H.to_np(layer.a), H.to_np(layer.y)
+    dh, dx = H.to_np(layer.dh), H.to_np(layer.dx_perm)
+    dw1p, dw2 = H.to_np(layer.dw1p), H.to_np(layer.dw2)
+    b1p = H.to_np(layer.b1p) if layer.b1p is not None else None
+    b2 = H.to_np(layer.b2) if layer.b2 is not None else None
+    got = {k: [] for k in ("H", "Y", "dH", "dX", "dW1", "dW2")}
+    ref = {k: [] for k in got}
+    for e, lo, m in _groups(layer):
+        rows = slice(lo, lo + m)
+        hr = Xq[rows] @ w1q[e].T + (b1p[e] if b1p is not None else 0)
+        got["H"].append(h[rows]); ref["H"].append(hr)
+        yr = Aq[rows] @ w2q[e].T + (b2[e] if b2 is not None else 0)
+        got["Y"].append(y[rows]); ref["Y"].append(yr)
+        da = dYq[rows] @ w2tq[e].T                        # [m, F]
+        hl = H.packed_to_logical_cols(h[rows], F)[0]
+        if p.gated:
+            dg, dl = oracle.glu_backward(da, hl[:, :F], hl[:, F:], p)
+            dhr = np.concatenate([dg, dl], axis=1)
+        else:
+            dhr = oracle.glu_backward(da, hl, None, p)[0]
+        got["dH"].append(H.packed_to_logical_cols(dh[rows], F)[0]); ref["dH"].append(dhr)
+        got["dX"].append(dx[rows]); ref["dX"].append(dHq[rows] @ w1tq[e].T)
+        k_rows = slice(lo, lo + (m + 63) // 64 * 64)          # K runs to the 64-row step
+        got["dW2"].append(dw2[e]); ref["dW2"].append(dYt[:, k_rows] @ At[:, k_rows].T)
+        got["dW1"].append(dw1p[e]); ref["dW1"].append(dHt[:, k_rows] @ Xt[:, k_rows].T)
+    for k in got:
+        H.assert_close(f"{name}/{k}", np.concatenate([x.ravel() for x in got[k]]),
+                       np.concatenate([x.ravel() for x in ref[k]]))
+    # A = GLU(H) in the FC1 epilogue, and the encode amax values it emits
+    for e, lo, m in _groups(layer):
+        hl = H.packed_to_logical_cols(h[lo:lo + m], F)[0]
+        ar = oracle.glu_forward(hl[:, :F], hl[:, F:], p) if p.gated else oracle.glu_forward(hl, None, p)
+        H.assert_close(f"{name}/A", a[lo:lo + m], ar)
+    amax_a = H.to_np(layer.a_nv["amax"])
+    assert amax_a[0] == np.float32(np.max(np.abs(a)))
+    # the requantized A matches the oracle quantizer on the GPU's A, bit for bit
+    q_ref, sc_ref, _ = oracle.nvfp4_quantize_rows(
+        a[:int(H.to_np(layer.padded_offsets)[-1])].astype(np.float32),
+        oracle.nvfp4_global_scale(amax_a[0]))
+    R = q_ref.shape[0]
+    codes = H.unpack_fp4_codes(H.to_np(layer.a_nv["q"]))[:R]
+    assert np.array_equal(_zero_signs(codes), _zero_signs(oracle.e2m1_encode(q_ref)))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_mlp_vs_nvfp4_oracle(name):
+    wl = CASES[name]
+    inp = make_inputs(wl)
+    layer, ref = H.run_both_direct_nv(wl, inp)
+    F = wl.F
+    got = dict(H=H.packed_to_logical_cols(H.to_np(layer.h), F)[0], A=H.to_np(layer.a),
+               Y=H.to_np(layer.y), dH=H.packed_to_logical_cols(H.to_np(layer.dh), F)[0],
+               dX_perm=H.to_np(layer.dx_perm),
+               dW1=H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), dW2=H.to_np(layer.dw2))
+    if wl.has_b1:
+        got["db1"] = H.to_np(layer.unpack_fc1(layer.db1p.reshape(wl.E, -1, 1).contiguous(), 1))[..., 0]
+    if wl.has_b2:
+        got["db2"] = H.to_np(layer.db2)
+    R = int(ref["padded_offsets"][-1])
+    for k, g_ in got.items():
+        r = ref[k][:R] if k in ("H", "A", "Y", "dH", "dX_perm") else ref[k]
+        g_ = g_[:R] if k in ("H", "A", "Y", "dH", "dX_perm") else g_
+        if k in ("H", "A", "db2"):
+            H.assert_close(f"{name}/{k}", g_, r)
+        else:
+            H.assert_close(f"{name}/{k}", g_, r, rel=H.TOL_NV, abs_=0.0)
+            fro = np.linalg.norm(g_ - r) / max(np.linalg.norm(r), 1e-30)
+            assert fro <= H.TOL_NV_FRO, (name, k, fro)
