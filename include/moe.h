@@ -499,8 +499,8 @@ size_t moe_nvfp4_scale_bytes(int64_t rows, int64_t cols);
 
 /* amax[0] = max |x|, amax[1] = max |H16 x / 4| (each column rotated along
  * the rows in 16-row segments) of bf16 [batch, rows, cols], rows % 16 == 0,
- * cols even, over the rows below *row_limit (device int; NULL = all rows).
- * amax is overwritten. */
+ * cols % 8 == 0, in 16-byte aligned, over the rows below *row_limit (device
+ * int; NULL = all rows).  amax is overwritten. */
 moe_status_t moe_amax_nvfp4(const void* in, int64_t batch, int64_t rows, int64_t cols,
                             const int32_t* row_limit, float* amax, cudaStream_t stream);
 

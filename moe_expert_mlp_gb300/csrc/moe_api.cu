@@ -1212,8 +1212,8 @@ size_t moe_nvfp4_scale_bytes(int64_t rows, int64_t cols) {
 moe_status_t moe_amax_nvfp4(const void* in, int64_t batch, int64_t rows, int64_t cols,
                             const int32_t* row_limit, float* amax, cudaStream_t stream) {
   if (!in || !amax) return MOE_ERR_NULL;
-  if (batch < 0 || rows < 0 || cols < 0 || rows % 16 != 0 || cols % 2 != 0) return MOE_ERR_SHAPE;
-  if (reinterpret_cast<uintptr_t>(in) & 3) return MOE_ERR_SHAPE;
+  if (batch < 0 || rows < 0 || cols < 0 || rows % 16 != 0 || cols % 8 != 0) return MOE_ERR_SHAPE;
+  if (reinterpret_cast<uintptr_t>(in) & 15) return MOE_ERR_SHAPE;
   DeviceInfo* di;
   moe_status_t st = device_info(&di);
   if (st != MOE_OK) return st;

@@ -69,36 +69,40 @@ __device__ __forceinline__ uint8_t nv_quant16(const float (&v)[16], float g, uin
   return static_cast<uint8_t>(sc);
 }
 
-// Per-tensor amax of bf16 [batch, rows, cols] (rows % 16 == 0, cols even)
-// over rows below *row_limit: amax[0] = max |x|, amax[1] = max |H16 x / 4|
+// Per-tensor amax of bf16 [batch, rows, cols] (rows % 16 == 0, cols % 8 ==
+// 0) over rows below *row_limit: amax[0] = max |x|, amax[1] = max |H16 x / 4|
 // over 16-row segments (each column rotated along the rows).  One thread
-// per (segment, column pair); both outputs must be zero on entry.
+// per (segment, 8 columns): sixteen 16-byte row loads; both outputs must be
+// zero on entry.
 __global__ void __launch_bounds__(256) k_amax_nv(const __nv_bfloat16* __restrict__ in,
                                                  long long batch, long long rows, long long cols,
                                                  const int32_t* row_limit, float* amax) {
   const long long rlim = row_limit ? __ldg(row_limit) : rows;
   const long long segs = (rlim < rows ? rlim : rows) / 16;
-  const long long cp_n = cols / 2;
-  const long long n = batch * segs * cp_n;
+  const long long c8_n = cols / 8;
+  const long long n = batch * segs * c8_n;
   float m0 = 0.0f, m1 = 0.0f;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long cp = i % cp_n, rest = i / cp_n;
+    const long long c8 = i % c8_n, rest = i / c8_n;
     const long long sg = rest % segs, b = rest / segs;
-    const __nv_bfloat162* p =
-        reinterpret_cast<const __nv_bfloat162*>(in + (b * rows + sg * 16) * cols) + cp;
-    float v0[16], v1[16];
+    const uint4* p = reinterpret_cast<const uint4*>(in + (b * rows + sg * 16) * cols) + c8;
+    uint4 w[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) {
-      const float2 f = __bfloat1622float2(p[r * cp_n]);
-      v0[r] = f.x;
-      v1[r] = f.y;
-      m0 = fmaxf(m0, fmaxf(fabsf(f.x), fabsf(f.y)));
+    for (int r = 0; r < 16; ++r) w[r] = __ldg(p + r * c8_n);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      float v[16];
+#pragma unroll
+      for (int r = 0; r < 16; ++r) {
+        const uint32_t word = (c < 2) ? w[r].x : (c < 4) ? w[r].y : (c < 6) ? w[r].z : w[r].w;
+        v[r] = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
+        m0 = fmaxf(m0, fabsf(v[r]));
+      }
+      fwht16(v);
+#pragma unroll
+      for (int r = 0; r < 16; ++r) m1 = fmaxf(m1, fabsf(v[r]));
     }
-    fwht16(v0);
-    fwht16(v1);
-#pragma unroll
-    for (int r = 0; r < 16; ++r) m1 = fmaxf(m1, fmaxf(fabsf(v0[r]), fabsf(v1[r])));
   }
   m1 *= 0.25f;
 #pragma unroll
@@ -123,7 +127,7 @@ constexpr int kNT = 128;                       // tile edge
 constexpr int kTilePitch = 272;                // bytes per staged row (256 + 16 pad)
 constexpr int kNvQuantSmem = kNT * kTilePitch + 2 * kNT * 64 + 4 * 512;
 
-__global__ void __launch_bounds__(256) k_quant_nv(const __nv_bfloat16* __restrict__ in,
+__global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __restrict__ in,
                                                   long long batch, long long rows, long long cols,
                                                   uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
                                                   const float* amax_row, const float* amax_col,
@@ -143,21 +147,43 @@ __global__ void __launch_bounds__(256) k_quant_nv(const __nv_bfloat16* __restric
   const long long rlim = row_limit ? __ldg(row_limit) : rows;
   const float g_row = q ? nv_encode_scale_q(amax_row) : 1.0f;
   const float g_col = qt ? nv_encode_scale_q(amax_col) : 1.0f;
+  // the tile's 2048 16-byte chunks, eight per thread, are loaded one tile
+  // ahead into registers so that the loads overlap the previous tile's work
+  auto load_tile = [&](long long t, uint4 (&v)[8]) {
+    const long long b = t / (rtn * ctn);
+    const long long rem = t - b * rtn * ctn;
+    const long long r0 = (rem / ctn) * kNT, c0 = (rem % ctn) * kNT;
+    const int nr = static_cast<int>(min(static_cast<long long>(kNT), rows - r0));
+    const int nc = static_cast<int>(min(static_cast<long long>(kNT), cols - c0));
+    const bool live = t < ntiles && r0 < rlim;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = tid + 256 * k;
+      const int r = i >> 4, ch = i & 15;
+      v[k] = make_uint4(0, 0, 0, 0);
+      if (live && r < nr && ch * 8 < nc)
+        v[k] = __ldg(reinterpret_cast<const uint4*>(in + (b * rows + r0 + r) * cols + c0) + ch);
+    }
+  };
+  uint4 pre[8];
+  load_tile(blockIdx.x, pre);
   for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
     const long long b = t / (rtn * ctn);
     const long long rem = t - b * rtn * ctn;
     const long long r0 = (rem / ctn) * kNT, c0 = (rem % ctn) * kNT;
-    if (r0 >= rlim) continue;                        // uniform across the CTA
+    if (r0 >= rlim) {                                // uniform across the CTA
+      load_tile(t + gridDim.x, pre);
+      continue;
+    }
     const int nr = static_cast<int>(min(static_cast<long long>(kNT), rows - r0));
     const int nc = static_cast<int>(min(static_cast<long long>(kNT), cols - c0));
     __syncthreads();                                 // previous tile fully stored
-    for (int i = tid; i < kNT * 16; i += 256) {
-      const int r = i >> 4, ch = i & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < nr && ch * 8 < nc)
-        v = __ldg(reinterpret_cast<const uint4*>(in + (b * rows + r0 + r) * cols + c0) + ch);
-      *reinterpret_cast<uint4*>(tile + r * kTilePitch + ch * 16) = v;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const int i = tid + 256 * k;
+      *reinterpret_cast<uint4*>(tile + (i >> 4) * kTilePitch + (i & 15) * 16) = pre[k];
     }
+    load_tile(t + gridDim.x, pre);
     if (tid < 128) reinterpret_cast<uint4*>(atom_r)[tid] = make_uint4(0, 0, 0, 0);   // both
     __syncthreads();
     if (q) {
@@ -248,7 +274,7 @@ cudaError_t launch_amax_nv(const void* in, long long batch, long long rows, long
                            cudaStream_t stream) {
   cudaError_t err = cudaMemsetAsync(amax, 0, 2 * sizeof(float), stream);
   if (err != cudaSuccess) return err;
-  const long long n = batch * (rows / 16) * (cols / 2);
+  const long long n = batch * (rows / 16) * (cols / 8);
   if (n == 0) return cudaSuccess;
   long long grid = (n + 255) / 256;
   if (grid > static_cast<long long>(num_sms) * 8) grid = static_cast<long long>(num_sms) * 8;
