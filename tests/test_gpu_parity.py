@@ -31,6 +31,11 @@ CASES = {
                              router_bias=False),
     "srelu_clamp_bias": scaled(WORKLOADS["gptoss_t16384_e32"], T=200, E=4, k=2, d=128, F=160,
                                act="srelu", linear_offset=0.0, out_scale=0.75, limit=1.5),
+    # the largest expert count and top-k the library accepts (256, 32)
+    "max_e256_k32": scaled(BASE, T=64, E=256, k=32, d=128, F=64),
+    # degenerate routing: a single token; a single expert (softmax of one logit)
+    "one_token": scaled(BASE, T=1, E=4, k=2, d=128, F=64),
+    "one_expert": scaled(BASE, T=100, E=1, k=1, d=128, F=64, router_bias=False),
 }
 
 
