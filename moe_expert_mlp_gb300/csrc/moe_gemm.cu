@@ -82,8 +82,19 @@ constexpr int SF_STAGE_BYTES_NV = 6144;
 constexpr size_t SMEM_BYTES_NV = 1024 + static_cast<size_t>(STAGES_NV) *
                                             (STAGE_BYTES + SF_STAGE_BYTES_NV) +
                                  kRing * BOX_BYTES;
-// operand formats of k_grouped_gemm
-constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2;
+// operand formats of k_grouped_gemm; kOpBf16H is bf16 with the FC2 dgrad +
+// dGLU epilogue reading the saved H (gate and linear share of each
+// 32-feature chunk, 64 bytes per thread) through cp.async into a shared
+// buffer kHDepth chunks deep, so that several chunks' loads are in flight
+// without holding registers; the buffer takes one operand stage.  That pays
+// where the epilogue, not the operand feed, sets the pace: short K (measured:
+// K = 2048 10 % faster; K = 2880 9 % slower, K = 7168 15 % slower).
+constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2, kOpBf16H = 3;
+constexpr int kHAsyncMaxK = 2048;
+constexpr int kHDepth = 3;
+constexpr int H_BUF_BYTES = kHDepth * 4 * kGemmEpiThreads * 16;
+constexpr size_t SMEM_BYTES_HA = 1024 + static_cast<size_t>(STAGES - 1) * STAGE_BYTES +
+                                 kRing * BOX_BYTES + H_BUF_BYTES;
 
 struct Tile {
   int e;        // expert
@@ -314,7 +325,7 @@ __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v
 // are quantized along the contraction dimension).
 template <int MODE, int OP>
 struct Traits {
-  static constexpr bool kScaled = OP != kOpBf16;
+  static constexpr bool kScaled = OP == kOpMx || OP == kOpNv;
   static constexpr bool kRaggedK = (MODE == kWgrad);
   static constexpr bool kAmn = !kScaled && (MODE == kWgrad);
   static constexpr bool kBmn = !kScaled && (MODE == kDgradDglu || MODE == kDgradFc1 ||
@@ -322,7 +333,8 @@ struct Traits {
   static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
   static constexpr int kBK = OP == kOpNv ? BK_NV : (OP == kOpMx ? BK_MX : BK);
   static constexpr int kNR = OP == kOpMx ? kRingMx : kRing;
-  static constexpr int kStages = OP == kOpNv ? STAGES_NV : STAGES;
+  static constexpr bool kHAsync = MODE == kDgradDglu && OP == kOpBf16H;
+  static constexpr int kStages = OP == kOpNv ? STAGES_NV : (kHAsync ? STAGES - 1 : STAGES);
   static constexpr int kSfStage =
       OP == kOpNv ? SF_STAGE_BYTES_NV : (OP == kOpMx ? SF_STAGE_BYTES : 0);
 };
@@ -665,6 +677,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
     const int row_local = quarter * 32 + lane;
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
     uint8_t* const ring_mem = smem + NST * STAGE_BYTES + NST * Tr::kSfStage;
+    const uint32_t h_buf = smem_u32(ring_mem + Tr::kNR * BOX_BYTES);   // async H (bf16 dGLU)
+    const uint8_t* const h_gen = ring_mem + Tr::kNR * BOX_BYTES;
     StoreRing ring{smem_u32(ring_mem), 0, ring_mem};
     const bool issuer = threadIdx.x == 64;   // first epilogue thread issues the stores
     const MxOut mx{args.mx_q, args.mx_s, args.mx_qt, args.mx_st, args.mx_amax, args.mx_width,
@@ -698,7 +712,29 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       // the first chunk's share is fetched before waiting for the MMAs.
       uint4 hg[2][2], hl[2][2];
       const __nv_bfloat16* Hrow = nullptr;
-      if (MODE == kDgradDglu) {
+      // async H: chunk jn's share into buffer slot jn % kHDepth (an empty
+      // group past the tile's chunks keeps the group count uniform)
+      const int nch_h = MODE == kDgradDglu ? min(BN / 32, (args.f_pad - ti.n0) / 32) : 0;
+      auto h_issue = [&](int jn) {
+        if constexpr (Tr::kHAsync) {
+          const int f = ti.n0 + 32 * jn;
+          if (jn < nch_h && valid && f < args.f_real) {
+            const __nv_bfloat16* src =
+                Hrow + (f / kGluHalf) * 2 * kGluHalf + (f % kGluHalf) + hc;
+            const uint32_t dst =
+                h_buf + ((jn % kHDepth) * 4 * kGemmEpiThreads + (threadIdx.x - 64)) * 16;
+            cp_async16(dst, src);
+            cp_async16(dst + kGemmEpiThreads * 16, src + 8);
+            cp_async16(dst + 2 * kGemmEpiThreads * 16, src + kGluHalf);
+            cp_async16(dst + 3 * kGemmEpiThreads * 16, src + kGluHalf + 8);
+          }
+          cp_async_commit();
+        }
+      };
+      if (MODE == kDgradDglu && Tr::kHAsync) {
+        Hrow = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
+        for (int jn = 0; jn < kHDepth - 1; ++jn) h_issue(jn);
+      } else if (MODE == kDgradDglu) {
         Hrow = static_cast<const __nv_bfloat16*>(args.aux) + gr * args.ld_aux;
         if (valid && ti.n0 < args.f_real) {
           const long long cg = static_cast<long long>(ti.n0 / kGluHalf) * 2 * kGluHalf +
@@ -825,6 +861,50 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
                 mx_amax_regs16(a, lane, am_m, am_h);
               }
             }
+          }
+        }
+      } else if (MODE == kDgradDglu && Tr::kHAsync) {
+        // tile columns are GLU features n0 .. n0+255; dH in packed layout;
+        // H arrives kHDepth - 1 chunks ahead through the async buffer
+        uint32_t r[16];
+        tmem_ld16(tbase, r);
+#pragma unroll 1
+        for (int j = 0; j < nch_h; ++j) {
+          h_issue(j + kHDepth - 1);
+          cp_async_wait<kHDepth - 1>();             // this thread's chunk j landed
+          const uint8_t* hs =
+              h_gen + ((j % kHDepth) * 4 * kGemmEpiThreads + (threadIdx.x - 64)) * 16;
+          const uint4 hgv[2] = {*reinterpret_cast<const uint4*>(hs),
+                                *reinterpret_cast<const uint4*>(hs + kGemmEpiThreads * 16)};
+          const uint4 hlv[2] = {*reinterpret_cast<const uint4*>(hs + 2 * kGemmEpiThreads * 16),
+                                *reinterpret_cast<const uint4*>(hs + 3 * kGemmEpiThreads * 16)};
+          uint32_t ra[16];
+          tmem_ld_wait16(r);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          if (j + 1 < nch_h) tmem_ld16(tbase + 32 * (j + 1), r);
+          const int f0 = ti.n0 + 32 * j;
+          const int c0 = (f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
+          const bool live = valid && f0 < args.f_real;
+          float dg[16], dl[16];
+          if (live) dglu_compute16<ACT>(ra, hgv, hlv, ap, dg, dl);
+          const uint8_t* box_g = ring_next_box(ring);
+          ring_store_half<Tr::kNR>(ring, dg, live, &args.tma_out0, c0, y0, 0, row_local, half,
+                                   issuer);
+          if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
+          const uint8_t* box_l = ring_next_box(ring);
+          ring_store_half<Tr::kNR>(ring, dl, live, &args.tma_out0, c0 + kGluHalf, y0, 0,
+                                   row_local, half, issuer);
+          if (want_mx)
+            mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
+          if (want_mx && mx.amax) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dg[i] = live ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_amax_regs16(dg, lane, am_m, am_h);
+            mx_amax_regs16(dl, lane, am_m, am_h);
           }
         }
       } else if (MODE == kDgradDglu) {
@@ -1316,7 +1396,9 @@ cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
 template <int MODE, int ACT, int OP>
 cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
   constexpr size_t smem =
-      OP == kOpNv ? SMEM_BYTES_NV : (OP == kOpMx ? SMEM_BYTES_MX : SMEM_BYTES);
+      OP == kOpNv ? SMEM_BYTES_NV
+                  : (OP == kOpMx ? SMEM_BYTES_MX
+                                 : (Traits<MODE, OP>::kHAsync ? SMEM_BYTES_HA : SMEM_BYTES));
   static_assert(smem <= 232448, "shared memory per CTA");
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1344,7 +1426,9 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
   switch (mode) {
     case kFc1Glu: return launch_act<kFc1Glu, kOpBf16>(args, grid, s);
     case kFc2: return launch_mode<kFc2, 0, kOpBf16>(args, grid, s);
-    case kDgradDglu: return launch_act<kDgradDglu, kOpBf16>(args, grid, s);
+    case kDgradDglu:
+      return args.K <= kHAsyncMaxK ? launch_act<kDgradDglu, kOpBf16H>(args, grid, s)
+                                   : launch_act<kDgradDglu, kOpBf16>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0, kOpBf16>(args, grid, s);
     case kWgradPair: return launch_wgrad_pair(args, grid, s);
     case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpBf16>(args, grid, s);

@@ -539,6 +539,20 @@ __device__ __forceinline__ void unpack_bf16x32(const uint4 (&w)[4], float (&v)[3
 }
 
 // Load 32 bf16 (64 contiguous bytes, 16-byte aligned) as fp32.
+// 16-byte global -> shared copy that completes asynchronously (no register
+// staging); groups of them are committed and waited for by the issuing
+// thread, which then sees the data.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 __device__ __forceinline__ void load_raw32(const void* src, uint4 (&w)[2]) {
   const uint4* p = reinterpret_cast<const uint4*>(src);
   w[0] = __ldg(p);
