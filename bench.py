@@ -46,14 +46,14 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch from one ncu capture of the default
 # workload (profiles/grouped_gemm_bf16_t4096_e64.md), with the hash of the
 # GEMM sources the counters were taken on; a changed kernel reports null.
-_NCU_SRC = "759d68a17c155205"
+_NCU_SRC = "d7e31ef6a207c43d"
 NCU_TRAFFIC = {
-    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 786.830336e6 + 217.318144e6, "src": _NCU_SRC},
-    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.696512e6 + 101.440000e6, "src": _NCU_SRC},
-    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 615.273216e6 + 136.397568e6, "src": _NCU_SRC},
-    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 834.776320e6 + 103.280384e6, "src": _NCU_SRC},
-    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 184.817408e6 + 313.530368e6, "src": _NCU_SRC},
-    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 257.856768e6 + 682.106112e6, "src": _NCU_SRC},
+    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 788.546560e6 + 216.858112e6, "src": _NCU_SRC},
+    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.573632e6 + 101.975808e6, "src": _NCU_SRC},
+    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 595.847168e6 + 135.504640e6, "src": _NCU_SRC},
+    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 842.212864e6 + 104.080896e6, "src": _NCU_SRC},
+    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.303296e6 + 313.145856e6, "src": _NCU_SRC},
+    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 257.506304e6 + 682.261248e6, "src": _NCU_SRC},
 }
 
 
