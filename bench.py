@@ -118,6 +118,48 @@ def call_work(wl, name, R, dtype="bf16"):
     return "byte", float(mem.get(name, 0.0))
 
 
+def step_bytes(wl, dtype="bf16"):
+    """Algorithmic HBM bytes of one fwd+bwd step (the attainable-roofline
+    byte model): every weight read once per GEMM that uses it (the bf16
+    masters, or the quantized copies on the block-scaled paths, whose
+    preparation runs outside the step), every dW written once in bf16, every
+    per-row tensor written once and read once per consumer (x_perm by FC1 and
+    FC1 wgrad, H by the dGLU, A by FC2 and FC2 wgrad, Y by the combine, dY
+    by FC2 dgrad and FC2 wgrad, dH by FC1 dgrad and FC1 wgrad, dX_perm by the
+    permute backward); on the block-scaled paths each quantized operand copy
+    is written once and read by its GEMM, after one bf16 read of its source
+    (two for x_perm / dY on NVFP4: the amax pass); routed layers add the
+    token-side x, out, dOut, dx.  Padding rows and index arrays are ignored."""
+    d, F, E = wl.d, wl.F, wl.E
+    n1 = 2 * F if wl.gated else F
+    R = wl.routed_rows
+    w_el = E * (n1 * d + d * F)
+    q = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16}[dtype]
+    b = 2.0 * w_el * (2.0 if dtype == "bf16" else q)      # two GEMMs per weight
+    b += 2.0 * w_el                                       # dW in bf16
+    if dtype == "bf16":
+        per_row = 2 * (3 * d        # x_perm: written (permute or input), FC1, FC1 wgrad
+                       + 2 * n1     # H: FC1 writes, dGLU reads
+                       + 3 * F      # A: FC1 writes, FC2 and FC2 wgrad read
+                       + 2 * d      # Y: FC2 writes, combine reads
+                       + 3 * d      # dY: combine bwd writes, FC2 dgrad and wgrad read
+                       + 3 * n1     # dH: dGLU writes, FC1 dgrad and wgrad read
+                       + 2 * d)     # dX_perm: FC1 dgrad writes, permute bwd reads
+    else:
+        amax_reads = 2 if dtype == "nvfp4" else 1
+        per_row = (2 * d + 2 * d * amax_reads + 4 * d * q          # x_perm + its two copies
+                   + 2 * 2 * n1                                    # H written, read by dGLU
+                   + 2 * F + 2 * F + 4 * F * q                     # A (bf16) + its copies
+                   + 2 * 2 * d                                     # Y
+                   + 2 * d + 2 * d * amax_reads + 4 * d * q        # dY + its copies
+                   + 2 * n1 + 2 * n1 + 4 * n1 * q                  # dH + its copies
+                   + 2 * 2 * d)                                    # dX_perm
+    b += R * per_row
+    if wl.router != "direct":
+        b += wl.T * 4 * d * 2 + wl.T * wl.E * 4 * 2               # x, out, dOut, dx; logits
+    return float(b)
+
+
 # ------------------------------------------------------------ multi-rank
 def max_over_ranks(value, dist, device):
     """Largest value over all ranks (the slowest replica sets the job time)."""
@@ -540,6 +582,17 @@ def run_ours(args, wl):
     elif args.dtype == "nvfp4":  # bf16 measured x the nominal FP4/BF16 dense ratio (13.5/2.25)
         peak *= 6.0
         peak_note = f"{peak_src} bf16 burst (cuBLAS) x 6, the nominal FP4/BF16 dense ratio"
+    # attainable-roofline view of the whole step: max(FLOP / tensor peak,
+    # algorithmic bytes / measured HBM bandwidth), and the nominal peak
+    hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    nominal = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 13500.0}[args.dtype]
+    sb = step_bytes(wl, args.dtype)
+    t_tc, t_hbm = flops_step / (peak * 1e12) * 1e3, sb / (hbm * 1e9) * 1e3
+    attainable = {"bytes_per_step": round(sb), "t_tensor_ms": round(t_tc, 4),
+                  "t_hbm_ms": round(t_hbm, 4), "bound": "hbm" if t_hbm > t_tc else "tensor",
+                  "pct_of_attainable": round(100.0 * max(t_tc, t_hbm) / ms_step, 2),
+                  "pct_of_nominal_peak": round(100.0 * value / world / nominal, 2),
+                  "nominal_peak_tflops": nominal, "hbm_gbs": hbm}
     tr = NCU_TRAFFIC.get((dominant, wl.name, args.dtype))
     traffic = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
     line = {
@@ -551,6 +604,7 @@ def run_ours(args, wl):
                        graph=bool(use_graph)),
         "tokens_per_s": round(job_rate(wl.T if routed else R, K, world, ms_max), 1),
         "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
+        "attainable": attainable,
         "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
                      "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "peak_source": peak_note},
