@@ -82,19 +82,25 @@ constexpr int SF_STAGE_BYTES_NV = 6144;
 constexpr size_t SMEM_BYTES_NV = 1024 + static_cast<size_t>(STAGES_NV) *
                                             (STAGE_BYTES + SF_STAGE_BYTES_NV) +
                                  kRing * BOX_BYTES;
-// operand formats of k_grouped_gemm; kOpBf16H is bf16 with the FC2 dgrad +
-// dGLU epilogue reading the saved H (gate and linear share of each
-// 32-feature chunk, 64 bytes per thread) through cp.async into a shared
-// buffer kHDepth chunks deep, so that several chunks' loads are in flight
-// without holding registers; the buffer takes one operand stage.  That pays
-// where the epilogue, not the operand feed, sets the pace: short K (measured:
-// K = 2048 10 % faster; K = 2880 9 % slower, K = 7168 15 % slower).
-constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2, kOpBf16H = 3;
-constexpr int kHAsyncMaxK = 2048;
+// operand formats of k_grouped_gemm.  kOpBf16H / kOpMxH are bf16 / MXFP8
+// with the FC2 dgrad + dGLU epilogue reading the saved H (gate and linear
+// share of each 32-feature chunk, 64 bytes per thread) through cp.async into
+// a shared buffer kHDepth chunks deep, so that several chunks' loads are in
+// flight without holding registers; the buffer takes one operand stage.
+// That pays where the epilogue, not the operand feed, sets the pace: short K
+// (measured, bf16: K = 2048 10 % faster, K = 2880 9 % slower, K = 7168 15 %
+// slower; MXFP8, whose epilogue also quantizes dH both ways: K = 2880 14 %
+// faster, K = 7168 6 % slower).
+constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2, kOpBf16H = 3, kOpMxH = 4;
+constexpr int kHAsyncMaxK = 2048, kHAsyncMaxKMx = 4096;
+__host__ __device__ constexpr bool op_mx(int op) { return op == kOpMx || op == kOpMxH; }
 constexpr int kHDepth = 3;
 constexpr int H_BUF_BYTES = kHDepth * 4 * kGemmEpiThreads * 16;
 constexpr size_t SMEM_BYTES_HA = 1024 + static_cast<size_t>(STAGES - 1) * STAGE_BYTES +
                                  kRing * BOX_BYTES + H_BUF_BYTES;
+constexpr size_t SMEM_BYTES_MXH = 1024 + static_cast<size_t>(STAGES - 1) *
+                                             (STAGE_BYTES + SF_STAGE_BYTES) +
+                                  kRingMx * BOX_BYTES + H_BUF_BYTES;
 
 struct Tile {
   int e;        // expert
@@ -325,18 +331,18 @@ __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v
 // are quantized along the contraction dimension).
 template <int MODE, int OP>
 struct Traits {
-  static constexpr bool kScaled = OP == kOpMx || OP == kOpNv;
+  static constexpr bool kScaled = op_mx(OP) || OP == kOpNv;
   static constexpr bool kRaggedK = (MODE == kWgrad);
   static constexpr bool kAmn = !kScaled && (MODE == kWgrad);
   static constexpr bool kBmn = !kScaled && (MODE == kDgradDglu || MODE == kDgradFc1 ||
                                             MODE == kWgrad || MODE == kDgradAct);
   static constexpr uint32_t kIdesc = idesc_bf16(BM, BN, kAmn, kBmn);
-  static constexpr int kBK = OP == kOpNv ? BK_NV : (OP == kOpMx ? BK_MX : BK);
-  static constexpr int kNR = OP == kOpMx ? kRingMx : kRing;
-  static constexpr bool kHAsync = MODE == kDgradDglu && OP == kOpBf16H;
+  static constexpr int kBK = OP == kOpNv ? BK_NV : (op_mx(OP) ? BK_MX : BK);
+  static constexpr int kNR = op_mx(OP) ? kRingMx : kRing;
+  static constexpr bool kHAsync = MODE == kDgradDglu && (OP == kOpBf16H || OP == kOpMxH);
   static constexpr int kStages = OP == kOpNv ? STAGES_NV : (kHAsync ? STAGES - 1 : STAGES);
   static constexpr int kSfStage =
-      OP == kOpNv ? SF_STAGE_BYTES_NV : (OP == kOpMx ? SF_STAGE_BYTES : 0);
+      OP == kOpNv ? SF_STAGE_BYTES_NV : (op_mx(OP) ? SF_STAGE_BYTES : 0);
 };
 
 // Accumulator factor of an NVFP4 GEMM: both operands were encoded with
@@ -382,7 +388,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
 template <int MODE, int ACT, int OP>
 __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_constant__ GemmArgs args) {
   using Tr = Traits<MODE, OP>;
-  constexpr bool MX = OP == kOpMx, NV = OP == kOpNv;
+  constexpr bool MX = op_mx(OP), NV = OP == kOpNv;
   constexpr int NST = Tr::kStages;
   extern __shared__ uint8_t dyn_smem[];
   __shared__ __align__(8) uint64_t full_bar[NST];
@@ -882,6 +888,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           tmem_ld_wait16(r);
 #pragma unroll
           for (int i = 0; i < 16; ++i) ra[i] = r[i];
+          if (j == 1) early_release(acc);             // columns 0-63 read
           if (j + 1 < nch_h) tmem_ld16(tbase + 32 * (j + 1), r);
           const int f0 = ti.n0 + 32 * j;
           const int c0 = (f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
@@ -1395,10 +1402,11 @@ cudaError_t launch_wgrad_pair(const GemmArgs& args, int grid, cudaStream_t s) {
 
 template <int MODE, int ACT, int OP>
 cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
-  constexpr size_t smem =
-      OP == kOpNv ? SMEM_BYTES_NV
-                  : (OP == kOpMx ? SMEM_BYTES_MX
-                                 : (Traits<MODE, OP>::kHAsync ? SMEM_BYTES_HA : SMEM_BYTES));
+  constexpr size_t smem = OP == kOpNv    ? SMEM_BYTES_NV
+                         : OP == kOpMxH ? SMEM_BYTES_MXH
+                         : OP == kOpMx  ? SMEM_BYTES_MX
+                         : Traits<MODE, OP>::kHAsync ? SMEM_BYTES_HA
+                                                     : SMEM_BYTES;
   static_assert(smem <= 232448, "shared memory per CTA");
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<MODE, ACT, OP>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1442,7 +1450,9 @@ cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cud
   switch (mode) {
     case kFc1Glu: return launch_act<kFc1Glu, kOpMx>(args, grid, s);
     case kFc2: return launch_mode<kFc2, 0, kOpMx>(args, grid, s);
-    case kDgradDglu: return launch_act<kDgradDglu, kOpMx>(args, grid, s);
+    case kDgradDglu:
+      return args.K <= kHAsyncMaxKMx ? launch_act<kDgradDglu, kOpMxH>(args, grid, s)
+                                     : launch_act<kDgradDglu, kOpMx>(args, grid, s);
     case kDgradFc1: return launch_mode<kDgradFc1, 0, kOpMx>(args, grid, s);
     case kWgrad: return launch_mode<kWgrad, 0, kOpMx>(args, grid, s);
     case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpMx>(args, grid, s);
