@@ -18,9 +18,11 @@
 // Engine", "Claims and evidence": one grouped GEMM call over ragged groups.
 //
 // Design of the grouped GEMM (one CTA per SM, 10 warps):
-//   warp 0   TMA producer: 128B-swizzled operand tiles into a 4-stage ring.
+//   warp 0   TMA producer: 128B-swizzled operand tiles into a ring of 4
+//            stages (3 for NVFP4 and for the async-H dGLU variants).
 //   warp 1   TMEM owner and single-thread MMA issuer (M=128, N=256; K=16
-//            per bf16 MMA, K=32 per block-scaled MXFP8 MMA).
+//            per bf16 MMA, K=32 per block-scaled MXFP8 MMA, K=64 per NVFP4
+//            MMA).
 //   warps 2-9 epilogue, two warps per TMEM lane quarter, each taking 16 of
 //            every 32 accumulator columns: tcgen05.ld, fused math, bf16
 //            (and MXFP8) outputs.  Two 256-column accumulators in TMEM let
@@ -1150,7 +1152,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
 // the rows of group e of P^T Q, with P [rows, m_ext] and Q [rows, n_ext] both
 // read MN-major.  A pair owns a 256 x 256 output tile: CTA r stages rows
 // m0+128r.. of P and columns n0+128r.. of Q (16 KB + 16 KB per 64-row K step,
-// 6 stages) and keeps output rows m0+128r.. in its TMEM.  The lead CTA issues
+// 5 stages) and keeps output rows m0+128r.. in its TMEM.  The lead CTA issues
 // the MMAs (M=256, N=256) and its commits arrive on both CTAs' barriers;
 // both CTAs' TMA loads complete on the lead CTA's "full" barriers.  Per SM
 // this halves the operand bytes per MMA relative to the single-CTA tile.
