@@ -46,14 +46,14 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch from one ncu capture of the default
 # workload (profiles/grouped_gemm_bf16_t4096_e64.md), with the hash of the
 # GEMM sources the counters were taken on; a changed kernel reports null.
-_NCU_SRC = "d7e31ef6a207c43d"
+_NCU_SRC = "1314f5f30a03dd35"
 NCU_TRAFFIC = {
-    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 788.546560e6 + 216.858112e6, "src": _NCU_SRC},
-    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.573632e6 + 101.975808e6, "src": _NCU_SRC},
-    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 595.847168e6 + 135.504640e6, "src": _NCU_SRC},
-    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 842.212864e6 + 104.080896e6, "src": _NCU_SRC},
-    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.303296e6 + 313.145856e6, "src": _NCU_SRC},
-    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 257.506304e6 + 682.261248e6, "src": _NCU_SRC},
+    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 788.908288e6 + 217.554688e6, "src": _NCU_SRC},
+    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.593856e6 + 102.047744e6, "src": _NCU_SRC},
+    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 599.201792e6 + 135.541248e6, "src": _NCU_SRC},
+    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 840.325376e6 + 104.433920e6, "src": _NCU_SRC},
+    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.397504e6 + 313.203456e6, "src": _NCU_SRC},
+    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 257.616896e6 + 682.265856e6, "src": _NCU_SRC},
 }
 
 
