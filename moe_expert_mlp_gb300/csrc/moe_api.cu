@@ -294,24 +294,21 @@ moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   const int T = desc->T, E = desc->E, k = desc->k;
-  const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
   int32_t* chunk = static_cast<int32_t*>(ws);
   cudaError_t e = cudaMemsetAsync(row_src, 0xFF, sizeof(int32_t) * desc->capacity, stream);
   if (e == cudaSuccess && T > 0)
     e = launch_topk(logits, bias, T, E, k, topk_idx, topk_w, chunk, di->status, stream);
   if (e == cudaSuccess) {
-    if (T > 0)
-      e = launch_scan(chunk, nchunks, E, desc->capacity, counts, offsets, padded_offsets,
-                      tile_prefix, di->status, stream);
-    else
+    if (T > 0) {
+      e = launch_scan_assign(topk_idx, T, E, k, chunk, desc->capacity, counts, offsets,
+                             padded_offsets, tile_prefix, row_src, row_of, di->status, stream);
+    } else {
       e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
-    if (e == cudaSuccess && T == 0)
-      e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
-                                     tile_prefix, di->status, stream);
+      if (e == cudaSuccess)
+        e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
+                                       tile_prefix, di->status, stream);
+    }
   }
-  if (e == cudaSuccess && T > 0)
-    e = launch_assign(topk_idx, T, E, k, chunk, padded_offsets, row_src, row_of, di->status,
-                      stream);
   if (e == cudaSuccess)
     e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
                            di->sms, stream);
@@ -364,18 +361,16 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
     if (e == cudaSuccess) e = launch_grouped_gemm(kRouter, g, grid_for(di, desc), stream);
   }
   if (e == cudaSuccess) {
-    if (T > 0)
-      e = launch_scan(chunk, nchunks, E, desc->capacity, counts, offsets, padded_offsets,
-                      tile_prefix, di->status, stream);
-    else
+    if (T > 0) {
+      e = launch_scan_assign(topk_idx, T, E, k, chunk, desc->capacity, counts, offsets,
+                             padded_offsets, tile_prefix, row_src, row_of, di->status, stream);
+    } else {
       e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
-    if (e == cudaSuccess && T == 0)
-      e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
-                                     tile_prefix, di->status, stream);
+      if (e == cudaSuccess)
+        e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
+                                       tile_prefix, di->status, stream);
+    }
   }
-  if (e == cudaSuccess && T > 0)
-    e = launch_assign(topk_idx, T, E, k, chunk, padded_offsets, row_src, row_of, di->status,
-                      stream);
   if (e == cudaSuccess)
     e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
                            di->sms, stream);

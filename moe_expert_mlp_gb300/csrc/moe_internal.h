@@ -22,15 +22,15 @@ inline int fc1_pad(int F) { return (F + kGluHalf - 1) / kGluHalf * kGluHalf; }
 cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, int k,
                         int32_t* topk_idx, float* topk_w, int32_t* chunk_counts, int* status,
                         cudaStream_t s);
-cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int capacity,
-                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
-                        int32_t* tile_prefix, int* status, cudaStream_t s);
 cudaError_t launch_offsets_from_counts(const int32_t* counts, int E, int capacity,
                                        int32_t* offsets, int32_t* padded_offsets,
                                        int32_t* tile_prefix, int* status, cudaStream_t s);
-cudaError_t launch_assign(const int32_t* topk_idx, int T, int E, int k,
-                          const int32_t* chunk_base, const int32_t* padded_offsets,
-                          int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s);
+// Group offsets from the per-chunk histogram and the stable assignment of
+// (token, slot) pairs to rows, in one launch (one block per chunk).
+cudaError_t launch_scan_assign(const int32_t* topk_idx, int T, int E, int k,
+                               const int32_t* chunk_counts, int capacity, int32_t* counts,
+                               int32_t* offsets, int32_t* padded_offsets, int32_t* tile_prefix,
+                               int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s);
 cudaError_t launch_gather_rows(const void* x, const int32_t* row_src,
                                const int32_t* padded_offsets, int E, int d, int T, int capacity,
                                void* x_perm, int num_sms, cudaStream_t s);

@@ -125,28 +125,6 @@ __device__ void scan_experts(const int32_t* cnt, int E, int capacity, int32_t* o
   if (p > capacity) set_status(status, MOE_DEV_BAD_OFFSETS);
 }
 
-// chunk_counts [nchunks][E] -> exclusive per-expert bases over chunks (in
-// place), counts and the three expert prefixes.
-__global__ void k_scan(int32_t* __restrict__ chunk_counts, int nchunks, int E, int capacity,
-                       int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
-                       int32_t* __restrict__ padded_offsets, int32_t* __restrict__ tile_prefix,
-                       int* status) {
-  __shared__ int32_t s_tot[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = chunk_counts[static_cast<size_t>(c) * E + e];
-      chunk_counts[static_cast<size_t>(c) * E + e] = run;
-      run += v;
-    }
-    s_tot[e] = run;
-    counts[e] = run;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0)
-    scan_experts(s_tot, E, capacity, offsets, padded_offsets, tile_prefix, status);
-}
-
 __global__ void k_offsets_from_counts(const int32_t* __restrict__ counts, int E, int capacity,
                                       int32_t* offsets, int32_t* padded_offsets,
                                       int32_t* tile_prefix, int* status) {
@@ -156,16 +134,48 @@ __global__ void k_offsets_from_counts(const int32_t* __restrict__ counts, int E,
   if (threadIdx.x == 0) scan_experts(s_c, E, capacity, offsets, padded_offsets, tile_prefix, status);
 }
 
-// ----------------------------------------------------- stable assignment
-// One thread per token, one block per chunk.  The row of (token t, expert e)
-// is padded_offsets[e] + (tokens of earlier chunks choosing e) + (earlier
-// tokens of this chunk choosing e), so rows inside a group ascend by token.
-// Ranks inside a warp come from ballots, across warps from a shared prefix.
-__global__ void __launch_bounds__(kTokensPerChunk) k_assign(
+// ------------------------------------------- group offsets + stable assignment
+// One thread per token, one block per chunk.  Every block first reduces the
+// per-chunk expert histogram [nchunks][E] itself: the expert totals give the
+// padded group offsets, the chunks before its own give its base; block 0
+// also writes counts, offsets, padded offsets and the tile prefix for the
+// later kernels.  The row of (token t, expert e) is padded_offsets[e] +
+// (tokens of earlier chunks choosing e) + (earlier tokens of this chunk
+// choosing e), so rows inside a group ascend by token.  Ranks inside a warp
+// come from ballots, across warps from a shared prefix.
+__global__ void __launch_bounds__(kTokensPerChunk) k_scan_assign(
     const int32_t* __restrict__ topk_idx, int T, int E, int k,
-    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ padded_offsets,
+    const int32_t* __restrict__ chunk_counts, int nchunks, int capacity,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ padded_offsets, int32_t* __restrict__ tile_prefix,
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_of, int* status) {
   __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
+  __shared__ int32_t s_base[kMaxExperts];
+  __shared__ int32_t s_tot[kMaxExperts];
+  __shared__ int32_t s_pad[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int before = 0, total = 0;
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[static_cast<size_t>(c) * E + e];
+      before += c < static_cast<int>(blockIdx.x) ? v : 0;
+      total += v;
+    }
+    s_base[e] = before;
+    s_tot[e] = total;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int p = 0;
+    for (int e = 0; e < E; ++e) {
+      s_pad[e] = p;
+      p += (s_tot[e] + kAlign - 1) / kAlign * kAlign;
+    }
+    if (blockIdx.x == 0) {
+      for (int e = 0; e < E; ++e) counts[e] = s_tot[e];
+      scan_experts(s_tot, E, capacity, offsets, padded_offsets, tile_prefix, status);
+    }
+  }
+  __syncthreads();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int t = blockIdx.x * kTokensPerChunk + threadIdx.x;
   const bool live = t < T;
@@ -202,7 +212,7 @@ __global__ void __launch_bounds__(kTokensPerChunk) k_assign(
     const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
     if (has) {
       const int rank = s_wcnt[warp][e] + __popc(b & lt_mask);
-      const int row = padded_offsets[e] + chunk_base[static_cast<size_t>(blockIdx.x) * E + e] + rank;
+      const int row = s_pad[e] + s_base[e] + rank;
       row_src[row] = t;
       for (int s = 0; s < k; ++s)
         if (topk_idx[static_cast<size_t>(t) * k + s] == e) row_of[static_cast<size_t>(t) * k + s] = row;
@@ -402,14 +412,6 @@ cudaError_t launch_topk(const float* logits, const float* bias, int T, int E, in
   return cudaGetLastError();
 }
 
-cudaError_t launch_scan(int32_t* chunk_counts, int nchunks, int E, int capacity,
-                        int32_t* counts, int32_t* offsets, int32_t* padded_offsets,
-                        int32_t* tile_prefix, int* status, cudaStream_t s) {
-  k_scan<<<1, 256, 0, s>>>(chunk_counts, nchunks, E, capacity, counts, offsets, padded_offsets,
-                           tile_prefix, status);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_offsets_from_counts(const int32_t* counts, int E, int capacity,
                                        int32_t* offsets, int32_t* padded_offsets,
                                        int32_t* tile_prefix, int* status, cudaStream_t s) {
@@ -418,13 +420,15 @@ cudaError_t launch_offsets_from_counts(const int32_t* counts, int E, int capacit
   return cudaGetLastError();
 }
 
-cudaError_t launch_assign(const int32_t* topk_idx, int T, int E, int k,
-                          const int32_t* chunk_base, const int32_t* padded_offsets,
-                          int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s) {
+cudaError_t launch_scan_assign(const int32_t* topk_idx, int T, int E, int k,
+                               const int32_t* chunk_counts, int capacity, int32_t* counts,
+                               int32_t* offsets, int32_t* padded_offsets, int32_t* tile_prefix,
+                               int32_t* row_src, int32_t* row_of, int* status, cudaStream_t s) {
   const int nchunks = (T + kTokensPerChunk - 1) / kTokensPerChunk;
   if (nchunks == 0) return cudaSuccess;
-  k_assign<<<nchunks, kTokensPerChunk, 0, s>>>(topk_idx, T, E, k, chunk_base, padded_offsets,
-                                               row_src, row_of, status);
+  k_scan_assign<<<nchunks, kTokensPerChunk, 0, s>>>(topk_idx, T, E, k, chunk_counts, nchunks,
+                                                    capacity, counts, offsets, padded_offsets,
+                                                    tile_prefix, row_src, row_of, status);
   return cudaGetLastError();
 }
 

@@ -371,7 +371,8 @@ class MoEExpertMLP:
         grouped_step(): six grouped GEMMs, one column-sum per bias, the two
         activation quantizations of the MXFP8 layer (NVFP4: four quantizations
         and two amax passes), and for
-        the routed layer top-k, scan, assign, gather, combine, pad-row zeroing,
-        combine backward, permute backward and router backward."""
+        the routed layer top-k, group offsets + assignment (one launch),
+        gather, combine, pad-row zeroing, combine backward, permute backward
+        and router backward."""
         n = 6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0) + (6 if self.nv else 0)
-        return n + (9 if routed else 0)
+        return n + (8 if routed else 0)

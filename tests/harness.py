@@ -272,3 +272,28 @@ def run_both_direct_nv(wl, inp):
     layer.mlp_backward()
     torch.cuda.synchronize()
     return layer, ref
+
+
+def run_oracle_routed_nv(wl, inp):
+    """The routed layer with the NVFP4 expert MLP: routing, permute, combine
+    and their backward as in the bf16 oracle; dY rounded to bf16 (the stored
+    tensor the quantizer reads) before the NVFP4 backward."""
+    p = glu_params(wl)
+    W1, b1, W2, b2 = oracle_weights(inp)
+    x = bf16_bits_to_f64(inp["x"])
+    topk_idx, topk_w, counts = oracle.route(inp["logits"], inp["bias"], wl.k)
+    offsets, padded, tiles = oracle.group_offsets(counts, 128)
+    row_src, row_of = oracle.permute_index(topk_idx, wl.E, padded)
+    xp = oracle.gather_rows(x, row_src)
+    H, A, Y = oracle.grouped_forward_nv(xp, padded, counts, W1, b1, W2, b2, p)
+    out = oracle.combine(Y, row_of, topk_w)
+    dY, dw = oracle.combine_backward(bf16_bits_to_f64(inp["dout"]), Y, row_of, topk_w,
+                                     xp.shape[0])
+    dY16 = oracle.bf16_round(dY)
+    dX, dH, dW1, db1, dW2, db2 = oracle.grouped_backward_nv(xp, H, A, dY16, padded, counts,
+                                                           W1, W2, p)
+    dx = oracle.permute_backward(dX, row_of)
+    dlogits = oracle.route_backward(dw, topk_w, topk_idx, wl.E)
+    return dict(topk_idx=topk_idx, counts=counts, padded_offsets=padded, x_perm=xp, H=H, A=A,
+                Y=Y, out=out, dY=dY16, dw=dw, dX_perm=dX, dH=dH, dW1=dW1, db1=db1, dW2=dW2,
+                db2=db2, dx=dx, dlogits=dlogits)

@@ -214,3 +214,48 @@ def test_mlp_vs_nvfp4_oracle(name):
             H.assert_close(f"{name}/{k}", g_, r, rel=H.TOL_NV, abs_=0.0)
             fro = np.linalg.norm(g_ - r) / max(np.linalg.norm(r), 1e-30)
             assert fro <= H.TOL_NV_FRO, (name, k, fro)
+
+
+ROUTED = {
+    "gptoss_routed": scaled(WORKLOADS["gptoss_t16384_e32"], T=256, E=8, k=4, d=192, F=128,
+                            w_std=0.05),
+    "max_e256_k32": scaled(WORKLOADS["bf16_t4096_e64"], T=48, E=256, k=32, d=128, F=64,
+                           w_std=0.05),
+}
+
+
+def _nv_close(name, got, ref):
+    H.assert_close(name, got, ref, rel=H.TOL_NV, abs_=0.0)
+    fro = np.linalg.norm(np.asarray(got) - ref) / max(np.linalg.norm(ref), 1e-30)
+    assert fro <= H.TOL_NV_FRO, (name, fro)
+
+
+@pytest.mark.parametrize("name", list(ROUTED))
+def test_routed_layer_nvfp4(name):
+    """The whole routed step (routing, permute, NVFP4 expert MLP, combine and
+    every backward) against the oracle with the NVFP4 expert MLP."""
+    wl = ROUTED[name]
+    inp = make_inputs(wl)
+    ref = H.run_oracle_routed_nv(wl, inp)
+    layer = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="nvfp4"))
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    T = wl.T
+    R_pad = int(ref["padded_offsets"][-1])
+    assert np.array_equal(H.to_np(layer.topk_idx)[:T], ref["topk_idx"])
+    assert np.array_equal(H.to_np(layer.padded_offsets), ref["padded_offsets"])
+    H.assert_close("H", H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)[0], ref["H"])
+    H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
+    _nv_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
+    _nv_close("out", H.to_np(layer.out)[:T], ref["out"])
+    _nv_close("dH", H.packed_to_logical_cols(H.to_np(layer.dh)[:R_pad], wl.F)[0], ref["dH"])
+    _nv_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
+    _nv_close("dW2", H.to_np(layer.dw2), ref["dW2"])
+    _nv_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    if wl.has_b1:
+        db1 = H.to_np(layer.unpack_fc1(layer.db1p.reshape(wl.E, -1, 1).contiguous(), 1))[..., 0]
+        _nv_close("db1", db1, ref["db1"])
+    if wl.has_b2:
+        H.assert_close("db2", H.to_np(layer.db2), ref["db2"])
+    _nv_close("dx", H.to_np(layer.dx)[:T], ref["dx"])
+    _nv_close("dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"])
