@@ -46,14 +46,14 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes (read + write) per launch from one ncu capture of the default
 # workload (profiles/grouped_gemm_bf16_t4096_e64.md), with the hash of the
 # GEMM sources the counters were taken on; a changed kernel reports null.
-_NCU_SRC = "1314f5f30a03dd35"
+_NCU_SRC = "b9e4ee2528075627"
 NCU_TRAFFIC = {
-    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 788.908288e6 + 217.554688e6, "src": _NCU_SRC},
-    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.593856e6 + 102.047744e6, "src": _NCU_SRC},
-    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 599.201792e6 + 135.541248e6, "src": _NCU_SRC},
-    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 840.325376e6 + 104.433920e6, "src": _NCU_SRC},
-    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.397504e6 + 313.203456e6, "src": _NCU_SRC},
-    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 257.616896e6 + 682.265856e6, "src": _NCU_SRC},
+    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 787.954432e6 + 217.387776e6, "src": _NCU_SRC},
+    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.630464e6 + 101.933568e6, "src": _NCU_SRC},
+    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 600.718848e6 + 135.138816e6, "src": _NCU_SRC},
+    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 836.186368e6 + 103.286528e6, "src": _NCU_SRC},
+    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.078272e6 + 313.084672e6, "src": _NCU_SRC},
+    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 258.155264e6 + 682.243072e6, "src": _NCU_SRC},
 }
 
 
