@@ -379,22 +379,38 @@ __global__ void k_unpack_fc1(const uint16_t* __restrict__ w1p, uint16_t* __restr
   for (int c = threadIdx.x; c < width; c += blockDim.x) dst[c] = s[c];
 }
 
-// db[e, c] = sum over the group's rows of g[r, c]: one thread per column
-// pair, rows summed in order in fp32.
+// db[e, c] = sum over the group's rows of g[r, c], in fp32 with a fixed
+// order: a block owns 32 column pairs of one expert; warp w sums rows
+// w, w+8, w+16, ... in order (a warp reads 128 contiguous bytes per row),
+// then the eight partial sums are added in warp order.
 __global__ void __launch_bounds__(256) k_group_colsum(
     const uint32_t* __restrict__ g, const int32_t* __restrict__ counts,
     const int32_t* __restrict__ padded_offsets, int pairs_per_row, uint32_t* __restrict__ out) {
+  __shared__ float s_part[8][32][2];
   const int e = blockIdx.y;
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= pairs_per_row) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * 32 + lane;
   const int r0 = padded_offsets[e], m = counts[e];
   float a0 = 0.0f, a1 = 0.0f;
-  for (int r = 0; r < m; ++r) {
-    const uint32_t v = __ldg(g + static_cast<size_t>(r0 + r) * pairs_per_row + c);
-    a0 += bf16_lo(v);
-    a1 += bf16_hi(v);
+  if (c < pairs_per_row) {
+    for (int r = warp; r < m; r += 8) {
+      const uint32_t v = __ldg(g + static_cast<size_t>(r0 + r) * pairs_per_row + c);
+      a0 += bf16_lo(v);
+      a1 += bf16_hi(v);
+    }
   }
-  out[static_cast<size_t>(e) * pairs_per_row + c] = pack_bf16x2(a0, a1);
+  s_part[warp][lane][0] = a0;
+  s_part[warp][lane][1] = a1;
+  __syncthreads();
+  if (warp == 0 && c < pairs_per_row) {
+    float b0 = 0.0f, b1 = 0.0f;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+      b0 += s_part[w][lane][0];
+      b1 += s_part[w][lane][1];
+    }
+    out[static_cast<size_t>(e) * pairs_per_row + c] = pack_bf16x2(b0, b1);
+  }
 }
 
 }  // namespace
@@ -501,7 +517,7 @@ cudaError_t launch_group_colsum(const void* g, const int32_t* counts,
                                 const int32_t* padded_offsets, int E, int width, void* out,
                                 cudaStream_t s) {
   const int pairs = width / 2;
-  dim3 grid((pairs + 255) / 256, E);
+  dim3 grid((pairs + 31) / 32, E);
   k_group_colsum<<<grid, 256, 0, s>>>(static_cast<const uint32_t*>(g), counts, padded_offsets,
                                       pairs, static_cast<uint32_t*>(out));
   return cudaGetLastError();
