@@ -207,3 +207,30 @@ def test_activation_recompute_matches_stored_h():
         assert torch.equal(a, b), name
     fwd, bwd = H.run_oracle_routed(wl, inp)
     H.assert_close("dW1", H.to_np(rec.unpack_fc1(rec.dw1p, wl.d)), bwd["dW1"])
+
+
+def test_zero_tokens_and_all_groups_empty():
+    """Degenerate sizes: a routed step with T = 0 and a grouped step with
+    every group empty run without error, route nothing, and give zero weight
+    and bias gradients (the buffers are filled with ones first)."""
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    base = scaled(WORKLOADS["gptoss_t16384_e32"], E=4, k=2, d=128, F=64)
+    dummy = make_inputs(scaled(base, T=1))              # one-row buffers for the pointers
+    for routed in (True, False):
+        wl = scaled(base, T=0)
+        layer = H.make_layer(wl)
+        H.load_layer_weights(layer, dummy)
+        for t in (layer.dw1p, layer.dw2, layer.db1p, layer.db2):
+            t.fill_(1.0)
+        if routed:
+            x = H.bits_to_dev(dummy["x"])
+            logits = torch.from_numpy(dummy["logits"]).cuda()
+            layer.step(x, logits, None, H.bits_to_dev(dummy["dout"]))
+        else:
+            layer.set_groups(torch.zeros(wl.E, dtype=torch.int32, device="cuda"))
+            layer.grouped_step()
+        torch.cuda.synchronize()
+        assert moe_read_device_status() == 0
+        assert int(layer.counts.sum()) == 0 and int(layer.padded_offsets[-1]) == 0
+        for name in ("dw1p", "dw2", "db1p", "db2"):
+            assert torch.count_nonzero(getattr(layer, name)) == 0, (routed, name)
