@@ -567,6 +567,30 @@ moe_status_t moe_fc1_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
                               const moe_mx_out_t* x_nv, const int32_t* counts,
                               const int32_t* padded_offsets, void* dw1p, cudaStream_t stream);
 
+/* NVFP4 forward (desc->dtype = MOE_DTYPE_NVFP4) in one call:
+ *   x_perm bf16 [capacity, d] -> x_nv (amax computed, rowwise + rotated
+ *   transposed copies) -> FC1 + GLU (h, a bf16; a_nv->amax) -> a_nv (rowwise
+ *   + rotated transposed copies) -> FC2 (y).
+ * x_nv / a_nv: NVFP4 buffers (q, scale, qt, scale_t, amax[2]) as described
+ * above, widths d and F. */
+moe_status_t moe_mlp_fwd_nv(const moe_mlp_desc_t* desc, const void* x_perm,
+                            const moe_mx_out_t* x_nv, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_nv_weights_t* w,
+                            const void* b1p, const void* b2, void* h, void* a,
+                            const moe_mx_out_t* a_nv, void* y, cudaStream_t stream);
+
+/* NVFP4 backward in one call: dY bf16 [capacity, d] -> dy_nv -> FC2 dgrad +
+ * dGLU (dh bf16, dh_nv->amax) -> dh_nv -> FC2 wgrad (dw2, from dy_nv and
+ * a_nv's transposed copies), FC1 dgrad (dx_perm), FC1 wgrad (dw1p, from
+ * dh_nv and x_nv's transposed copies), bias gradients (db1p / db2, NULL to
+ * skip).  x_nv and a_nv are the forward's buffers. */
+moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
+                            const moe_mx_out_t* dy_nv, const moe_mx_out_t* x_nv, const void* h,
+                            const moe_mx_out_t* a_nv, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_nv_weights_t* w, void* dh,
+                            const moe_mx_out_t* dh_nv, void* dx_perm, void* dw1p, void* db1p,
+                            void* dw2, void* db2, cudaStream_t stream);
+
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed
  * pool, or a runtime that allows no allocation after start-up).  The pages

@@ -38,7 +38,7 @@ EXPORTS = (
     "moe_fc1_wgrad_mx", "moe_route_permute_fused", "moe_nvfp4_scale_bytes", "moe_amax_nvfp4",
     "moe_quantize_nvfp4_bf16", "moe_quantize_act_nvfp4", "moe_quantize_weights_nvfp4",
     "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
-    "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv",
+    "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
 )
 
 
@@ -180,6 +180,8 @@ def lib():
             "moe_fc2_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_dgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
+            "moe_mlp_fwd_nv": (ctypes.c_int, [D] + [P] * 12),
+            "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -491,3 +493,18 @@ def moe_fc1_dgrad_nv(desc, dh_nv, counts, padded_offsets, w_nv, dx_perm, stream=
 def moe_fc1_wgrad_nv(desc, dh_nv, x_nv, counts, padded_offsets, dw1p, stream=None):
     _check(lib().moe_fc1_wgrad_nv(ctypes.byref(desc), _mx(dh_nv), _mx(x_nv), _p(counts),
                                   _p(padded_offsets), _p(dw1p), _stream(stream)))
+
+
+def moe_mlp_fwd_nv(desc, x_perm, x_nv, counts, padded_offsets, w_nv, b1p, b2, h, a, a_nv, y,
+                   stream=None):
+    _check(lib().moe_mlp_fwd_nv(ctypes.byref(desc), _p(x_perm), _mx(x_nv), _p(counts),
+                                _p(padded_offsets), _nvw(w_nv), _p(b1p), _p(b2), _p(h), _p(a),
+                                _mx(a_nv), _p(y), _stream(stream)))
+
+
+def moe_mlp_bwd_nv(desc, dy, dy_nv, x_nv, h, a_nv, counts, padded_offsets, w_nv, dh, dh_nv,
+                   dx_perm, dw1p, db1p, dw2, db2, stream=None):
+    _check(lib().moe_mlp_bwd_nv(ctypes.byref(desc), _p(dy), _mx(dy_nv), _mx(x_nv), _p(h),
+                                _mx(a_nv), _p(counts), _p(padded_offsets), _nvw(w_nv), _p(dh),
+                                _mx(dh_nv), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2),
+                                _stream(stream)))

@@ -1461,4 +1461,45 @@ moe_status_t moe_fc1_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
   return cuda_status(launch_grouped_gemm_nv(kWgrad, g, grid_for(di, desc), stream));
 }
 
+moe_status_t moe_mlp_fwd_nv(const moe_mlp_desc_t* desc, const void* x_perm,
+                            const moe_mx_out_t* x_nv, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_nv_weights_t* w,
+                            const void* b1p, const void* b2, void* h, void* a,
+                            const moe_mx_out_t* a_nv, void* y, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !a || !y || !a_nv) return MOE_ERR_NULL;
+  if ((st = moe_quantize_act_nvfp4(desc, x_perm, desc->d, padded_offsets, x_nv, 1, stream)) !=
+          MOE_OK ||
+      (st = moe_fc1_glu_fwd_nv(desc, x_nv, counts, padded_offsets, w, b1p, h, a, a_nv->amax,
+                               stream)) != MOE_OK ||
+      (st = moe_quantize_act_nvfp4(desc, a, desc->F, padded_offsets, a_nv, 0, stream)) != MOE_OK)
+    return st;
+  return moe_fc2_fwd_nv(desc, a_nv, counts, padded_offsets, w, b2, y, stream);
+}
+
+moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
+                            const moe_mx_out_t* dy_nv, const moe_mx_out_t* x_nv, const void* h,
+                            const moe_mx_out_t* a_nv, const int32_t* counts,
+                            const int32_t* padded_offsets, const moe_nv_weights_t* w, void* dh,
+                            const moe_mx_out_t* dh_nv, void* dx_perm, void* dw1p, void* db1p,
+                            void* dw2, void* db2, cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dy || !dh || !dh_nv || !dx_perm || !dw1p || !dw2) return MOE_ERR_NULL;
+  const int32_t W1 = fc1_width(desc->act, desc->F);
+  if ((st = moe_quantize_act_nvfp4(desc, dy, desc->d, padded_offsets, dy_nv, 1, stream)) !=
+          MOE_OK ||
+      (st = moe_fc2_dgrad_dglu_nv(desc, dy_nv, h, counts, padded_offsets, w, dh, dh_nv->amax,
+                                  stream)) != MOE_OK ||
+      (st = moe_quantize_act_nvfp4(desc, dh, W1, padded_offsets, dh_nv, 0, stream)) != MOE_OK ||
+      (st = moe_fc2_wgrad_nv(desc, dy_nv, a_nv, counts, padded_offsets, dw2, stream)) != MOE_OK ||
+      (st = moe_fc1_dgrad_nv(desc, dh_nv, counts, padded_offsets, w, dx_perm, stream)) !=
+          MOE_OK ||
+      (st = moe_fc1_wgrad_nv(desc, dh_nv, x_nv, counts, padded_offsets, dw1p, stream)) != MOE_OK)
+    return st;
+  if (db1p || db2) return moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream);
+  return MOE_OK;
+}
+
 }  // extern "C"

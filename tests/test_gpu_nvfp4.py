@@ -259,3 +259,35 @@ def test_routed_layer_nvfp4(name):
         H.assert_close("db2", H.to_np(layer.db2), ref["db2"])
     _nv_close("dx", H.to_np(layer.dx)[:T], ref["dx"])
     _nv_close("dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"])
+
+
+def _direct_nv_layer(wl, inp):
+    sizes = inp["group_sizes"]
+    _, padded, _ = oracle.group_offsets(sizes, align=128)
+    layer = H.make_layer(wl, capacity=max(128, int(padded[-1])), dtype="nvfp4")
+    H.load_layer_weights(layer, inp)
+    layer.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
+    R_pad = int(padded[-1])
+    layer.x_perm[:R_pad].copy_(H.bits_to_dev(H.padded_rows(inp["x"], sizes, padded, wl.d)))
+    layer.dy[:R_pad].copy_(H.bits_to_dev(H.padded_rows(inp["dout"], sizes, padded, wl.d)))
+    return layer
+
+
+def test_composite_calls_match_per_call_path():
+    """moe_mlp_fwd_nv / moe_mlp_bwd_nv give, bit for bit, what the layer's
+    sequence of single NVFP4 calls gives."""
+    wl = CASES["gptoss_like"]
+    inp = make_inputs(wl)
+    one = _direct_nv_layer(wl, inp)
+    one.mlp_forward()
+    one.mlp_backward()
+    two = _direct_nv_layer(wl, inp)
+    L.moe_mlp_fwd_nv(two.desc, two.x_perm, two.x_nv, two.counts, two.padded_offsets, two.w_nv,
+                     two.b1p, two.b2, two.h, two.a, two.a_nv, two.y)
+    L.moe_mlp_bwd_nv(two.desc, two.dy, two.dy_nv, two.x_nv, two.h, two.a_nv, two.counts,
+                     two.padded_offsets, two.w_nv, two.dh, two.dh_nv, two.dx_perm, two.dw1p,
+                     two.db1p, two.dw2, two.db2)
+    torch.cuda.synchronize()
+    for name in ("h", "a", "y", "dh", "dx_perm", "dw1p", "db1p", "dw2", "db2"):
+        t1, t2 = getattr(one, name), getattr(two, name)
+        assert torch.equal(t1.view(torch.int16), t2.view(torch.int16)), name
