@@ -11,7 +11,7 @@ import torch
 
 import oracle
 from tests import harness as H
-from workloads import WORKLOADS, make_inputs, scaled
+from workloads import WORKLOADS, f32_to_bf16_bits, make_inputs, scaled
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
@@ -234,3 +234,34 @@ def test_zero_tokens_and_all_groups_empty():
         assert int(layer.counts.sum()) == 0 and int(layer.padded_offsets[-1]) == 0
         for name in ("dw1p", "dw2", "db1p", "db2"):
             assert torch.count_nonzero(getattr(layer, name)) == 0, (routed, name)
+
+
+def test_tiny_fp32_inputs_within_bf16_tolerance():
+    """The fp32 configuration (tiny layer): the oracle runs on the fp32
+    inputs themselves, the GPU on their bf16 roundings (the path computes in
+    bf16 with fp32 accumulation; there is no TF32 path); routing, decided on
+    the identical fp32 logits, is bit-exact, and every float output is
+    within the bf16 tolerance of the fp32-input oracle."""
+    from workloads import make_inputs_fp32
+    wl = WORKLOADS["tiny_t256_e8"]
+    f = make_inputs_fp32(wl)
+    p = H.glu_params(wl)
+    W1, W2 = f["w1"].astype(np.float64), f["w2"].astype(np.float64)
+    fwd = oracle.moe_forward(f["x"].astype(np.float64), f["logits"], f["bias"], W1, None, W2,
+                             None, wl.k, p, align=128)
+    bwd = oracle.moe_backward(fwd, f["dout"].astype(np.float64), W1, W2, p)
+    layer = H.make_layer(wl)
+    dev = lambda a: H.bits_to_dev(f32_to_bf16_bits(a))
+    layer.load_weights(dev(f["w1"]), None, dev(f["w2"]), None)
+    layer.step(dev(f["x"]), torch.from_numpy(f["logits"]).cuda(), None, dev(f["dout"]))
+    torch.cuda.synchronize()
+    assert np.array_equal(H.to_np(layer.topk_idx)[:wl.T], fwd["topk_idx"])
+    assert np.array_equal(H.to_np(layer.padded_offsets), fwd["padded_offsets"])
+    # this layer's outputs are small (x ~ N(0,1)/16, W ~ N(0,0.02)), so the
+    # bound is taken without the absolute term: max|gpu-ref| <= 1e-2 max|ref|
+    for name, got, ref in [("out", H.to_np(layer.out)[:wl.T], fwd["out"]),
+                           ("dx", H.to_np(layer.dx)[:wl.T], bwd["dx"]),
+                           ("dlogits", H.to_np(layer.dlogits)[:wl.T], bwd["dlogits"]),
+                           ("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), bwd["dW1"]),
+                           ("dW2", H.to_np(layer.dw2), bwd["dW2"])]:
+        H.assert_close(name, got, ref, abs_=0.0)

@@ -11,6 +11,7 @@ from .synth import (  # noqa: F401
     bf16_bits_to_f64,
     f32_to_bf16_bits,
     make_inputs,
+    make_inputs_fp32,
     scaled,
     zipf_group_sizes,
 )

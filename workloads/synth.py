@@ -202,3 +202,28 @@ def make_inputs(wl: Workload, seed: Optional[int] = None,
     rows = wl.R if wl.router == "direct" else wl.T
     out["dout"] = _normal_bf16(rng, (rows, wl.d), 1.0)
     return out
+
+
+def make_inputs_fp32(wl: Workload, seed: Optional[int] = None) -> dict:
+    """fp32 inputs of a routed layer (x, logits, dout, w1, w2, optional
+    biases; no bf16 rounding), drawn from the workload's distributions with
+    their own seeded stream: for the fp32 configuration, whose values reach
+    a bf16 path only after rounding."""
+    rng = np.random.Generator(np.random.PCG64(wl.seed if seed is None else seed))
+    n1 = 2 * wl.F if wl.gated else wl.F
+    f32 = np.float32
+    x = rng.standard_normal((wl.T, wl.d), dtype=f32) * f32(wl.x_std)
+    if wl.router == "xw":
+        wr = rng.standard_normal((wl.d, wl.E)) / math.sqrt(wl.d)
+        logits = (x.astype(np.float64) @ wr).astype(f32)
+    else:
+        logits = rng.standard_normal((wl.T, wl.E), dtype=f32)
+    bias = rng.standard_normal(wl.E, dtype=f32) if wl.router_bias else None
+    return {
+        "x": x, "logits": logits, "bias": bias,
+        "dout": rng.standard_normal((wl.T, wl.d), dtype=f32),
+        "w1": rng.standard_normal((wl.E, n1, wl.d), dtype=f32) * f32(wl.w_std),
+        "w2": rng.standard_normal((wl.E, wl.d, wl.F), dtype=f32) * f32(wl.w_std),
+        "b1": rng.standard_normal((wl.E, n1), dtype=f32) * f32(wl.b_std) if wl.has_b1 else None,
+        "b2": rng.standard_normal((wl.E, wl.d), dtype=f32) * f32(wl.b_std) if wl.has_b2 else None,
+    }
