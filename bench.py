@@ -14,7 +14,17 @@ a barrier + synchronize on both sides.  value = algorithmic TFLOPS
 (18*d*F per routed row, padding not counted) of the whole job.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME]
+                  [--workload NAME] [--dtype bf16|mxfp8|nvfp4]
+
+The JSON line also carries: `roofline` (the GEMM with the largest time
+against the measured peak of its operand type, with the DRAM traffic of an
+ncu capture of the same kernel source), `attainable` (the whole step against
+max(FLOP / peak, algorithmic bytes / measured HBM bandwidth)), `e2e` (the
+same steps through the public API with host-resident inputs and results,
+copies overlapped by HostStepPipeline, and in line), `cpu_baseline` (the
+oracle on a bounded sample on the host cores), `clocks` (sampled during the
+timed region), per-call times in `kernels`, and the fused-vs-unfused,
+overlap and router measurements unless switched off.
 
 --impl reference times the CPU fp64 oracle (the method written out plainly)
 on a bounded sample of the same workload on the host cores.
