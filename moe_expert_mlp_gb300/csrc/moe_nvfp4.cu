@@ -47,22 +47,16 @@ __device__ __forceinline__ void fwht16(float (&v)[16]) {
       }
 }
 
-// One block of 16 values v * PRE with encode scale g (PRE = 1, or 1/4 for
-// the unscaled Hadamard outputs: an exact power-of-two factor, applied to
-// the block maximum and folded into the per-block multiplier, which rounds
-// exactly as scaling every value first would): returns the UE4M3 scale code
+// One block of 16 values with encode scale g: returns the UE4M3 scale code
 // and the 16 E2M1 codes packed two per byte (element 2i in the low nibble).
-template <bool kQuarter>
 __device__ __forceinline__ uint8_t nv_quant16(const float (&v)[16], float g, uint2& codes) {
   float m = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
-  if (kQuarter) m *= 0.25f;
   const float target = __fmul_rn(__fdiv_rn(m, 6.0f), g);
   const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(target, __NV_SATFINITE, __NV_E4M3);
   const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
-  float inv = s > 0.0f ? __fdiv_rn(g, s) : 0.0f;
-  if (kQuarter) inv *= 0.25f;
+  const float inv = s > 0.0f ? __fdiv_rn(g, s) : 0.0f;
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -78,32 +72,30 @@ __device__ __forceinline__ uint8_t nv_quant16(const float (&v)[16], float g, uin
 // Per-tensor amax of bf16 [batch, rows, cols] (rows % 16 == 0, cols % 8 ==
 // 0) over rows below *row_limit: amax[0] = max |x|, amax[1] = max |H16 x / 4|
 // over 16-row segments (each column rotated along the rows).  One thread
-// per (segment, 4 columns): sixteen 8-byte row loads (a warp reads 256
-// contiguous bytes per row), few enough registers for four CTAs per SM;
-// both outputs must be zero on entry.
-__global__ void __launch_bounds__(256, 4) k_amax_nv(const __nv_bfloat16* __restrict__ in,
-                                                    long long batch, long long rows,
-                                                    long long cols, const int32_t* row_limit,
-                                                    float* amax) {
+// per (segment, 8 columns): sixteen 16-byte row loads; both outputs must be
+// zero on entry.
+__global__ void __launch_bounds__(256) k_amax_nv(const __nv_bfloat16* __restrict__ in,
+                                                 long long batch, long long rows, long long cols,
+                                                 const int32_t* row_limit, float* amax) {
   const long long rlim = row_limit ? __ldg(row_limit) : rows;
   const long long segs = (rlim < rows ? rlim : rows) / 16;
-  const long long c4_n = cols / 4;
-  const long long n = batch * segs * c4_n;
+  const long long c8_n = cols / 8;
+  const long long n = batch * segs * c8_n;
   float m0 = 0.0f, m1 = 0.0f;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long c4 = i % c4_n, rest = i / c4_n;
+    const long long c8 = i % c8_n, rest = i / c8_n;
     const long long sg = rest % segs, b = rest / segs;
-    const uint2* p = reinterpret_cast<const uint2*>(in + (b * rows + sg * 16) * cols) + c4;
-    uint2 w[16];
+    const uint4* p = reinterpret_cast<const uint4*>(in + (b * rows + sg * 16) * cols) + c8;
+    uint4 w[16];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) w[r] = __ldg(p + r * c4_n);
+    for (int r = 0; r < 16; ++r) w[r] = __ldg(p + r * c8_n);
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
+    for (int c = 0; c < 8; ++c) {
       float v[16];
 #pragma unroll
       for (int r = 0; r < 16; ++r) {
-        const uint32_t word = (c < 2) ? w[r].x : w[r].y;
+        const uint32_t word = (c < 2) ? w[r].x : (c < 4) ? w[r].y : (c < 6) ? w[r].z : w[r].w;
         v[r] = __uint_as_float((c & 1) ? (word & 0xFFFF0000u) : (word << 16));
         m0 = fmaxf(m0, fabsf(v[r]));
       }
@@ -213,7 +205,7 @@ __global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __rest
           }
         }
         uint2 c;
-        const uint8_t sc = nv_quant16<false>(v, g_row, c);
+        const uint8_t sc = nv_quant16(v, g_row, c);
         *reinterpret_cast<uint2*>(code_r + r * 64 + blk * 8) = c;
         atom_r[(blk >> 2) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (blk & 3)] = sc;
       }
@@ -231,14 +223,13 @@ __global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __rest
               *reinterpret_cast<const uint16_t*>(tile + (rb * 16 + i) * kTilePitch + c * 2);
           v[i] = __uint_as_float(static_cast<uint32_t>(h) << 16);
         }
-        uint2 cw;
-        uint8_t sc;
         if (rotate) {
-          fwht16(v);                                  // H16 v; the 1/4 is applied in the block
-          sc = nv_quant16<true>(v, g_col, cw);
-        } else {
-          sc = nv_quant16<false>(v, g_col, cw);
+          fwht16(v);
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
         }
+        uint2 cw;
+        const uint8_t sc = nv_quant16(v, g_col, cw);
         *reinterpret_cast<uint2*>(code_c + c * 64 + ((rb ^ (c & 7)) * 8)) = cw;
         atom_c[(rb >> 2) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4 + (rb & 3)] = sc;
       }
@@ -283,7 +274,7 @@ cudaError_t launch_amax_nv(const void* in, long long batch, long long rows, long
                            cudaStream_t stream) {
   cudaError_t err = cudaMemsetAsync(amax, 0, 2 * sizeof(float), stream);
   if (err != cudaSuccess) return err;
-  const long long n = batch * (rows / 16) * (cols / 4);
+  const long long n = batch * (rows / 16) * (cols / 8);
   if (n == 0) return cudaSuccess;
   long long grid = (n + 255) / 256;
   if (grid > static_cast<long long>(num_sms) * 8) grid = static_cast<long long>(num_sms) * 8;
