@@ -58,3 +58,28 @@ def test_host_side_errors_without_gpu(libmoe):
     assert libmoe.moe_workspace_size(ctypes.byref(bad), ctypes.byref(n)) == 3  # unsupported
     assert m.moe_fc1_padded_width(2880) == 2944 and m.moe_fc1_padded_width(1408) == 1408
     assert libmoe.moe_status_string(2) == b"sizes out of the supported range"
+
+
+def test_block_scaled_calls_reject_bad_arguments_without_gpu(libmoe):
+    """The MXFP8 / NVFP4 calls validate the descriptor and pointers on the
+    host and enqueue nothing: wrong operand type, shapes the block-scaled
+    MMA cannot take, missing buffers."""
+    import ctypes
+    import moe_expert_mlp_gb300 as m
+    from moe_expert_mlp_gb300 import _lib as L
+    ok_nv = m.make_desc(T=0, E=4, k=1, d=128, F=64, dtype="nvfp4")
+    bf16 = m.make_desc(T=0, E=4, k=1, d=128, F=64)
+    bad_f = m.make_desc(T=0, E=4, k=1, d=128, F=96, dtype="nvfp4")     # F % 64 != 0
+    null = ctypes.c_void_p(None)
+    # operand type must match the call
+    assert libmoe.moe_fc1_glu_fwd_nv(ctypes.byref(bf16), *([null] * 9)) == 3
+    assert libmoe.moe_fc2_wgrad_mx(ctypes.byref(ok_nv), *([null] * 6)) == 3
+    # NVFP4 needs F % 64 == 0
+    assert libmoe.moe_fc2_fwd_nv(ctypes.byref(bad_f), *([null] * 7)) == 2
+    # valid descriptor, missing buffers
+    assert libmoe.moe_fc2_fwd_nv(ctypes.byref(ok_nv), *([null] * 7)) == 1
+    assert libmoe.moe_mlp_bwd_nv(ctypes.byref(ok_nv), *([null] * 16)) == 1
+    assert libmoe.moe_quantize_nvfp4_bf16(null, 1, 32, 32, null, 0, null) == 1
+    assert L.moe_nvfp4_scale_bytes(256, 256) == 4 * 2 * 512
+    assert L.moe_nvfp4_scale_bytes(0, 64) == 0
+    assert L.moe_mx_scale_bytes(256, 256) == 2 * 2 * 512
