@@ -487,9 +487,9 @@ moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
  *           the low nibble), 16-byte aligned; scale: UE4M3 codes in the MMA
  *           layout of MXFP8 with 16-element blocks (moe_nvfp4_scale_bytes).
  *   qt      the transposed copy [cols, rows/2], scale_t its scales.
- *   amax    float[2]: [0] the amax that encodes q, [1] the one that encodes
- *           qt (for activations the rotated tensor's amax; for weights
- *           both are the tensor's amax).
+ *   amax    float[2]: [0] the amax that encodes q (the tensor's), [1] the
+ *           one that encodes qt (the rotated tensor's).  Weights use
+ *           moe_nv_weights_t below instead.
  * The GEMMs divide the encode scales out of the accumulator (factor
  * 1 / (g_a g_b)) before bias, activation and output. */
 
