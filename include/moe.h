@@ -79,7 +79,7 @@ typedef enum {
  * *_mx calls, with E4M3 operands and one E8M0 scale per 32 elements along
  * each GEMM's contraction dimension ([FK] "Reducing exposed memory overhead
  * by fusing MXFP8 and NVFP4 quantization"); requires d and F multiples of 32
- * and recompute_h = 0.  Routing, combine and their backward are bf16 in
+ * (recompute_h: see moe_fc1_recompute_h_mx).  Routing, combine and their backward are bf16 in
  * both. */
 typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2, MOE_DTYPE_NVFP4 = 3 } moe_dtype_t;
 /* NVFP4 (the *_nv calls): E2M1 operands, one UE4M3 scale per 16 elements
@@ -453,6 +453,17 @@ moe_status_t moe_fc1_dgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
 moe_status_t moe_fc1_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_mx,
                               const moe_mx_out_t* x_mx, const int32_t* counts,
                               const int32_t* padded_offsets, void* dw1p, cudaStream_t stream);
+
+/* Activation recompute on the MXFP8 path (desc->recompute_h = 1): the
+ * forward may pass h = NULL to moe_fc1_glu_fwd_mx / moe_mlp_fwd_mx; before
+ * the backward, this call regenerates H [capacity, W1] bf16 into a buffer
+ * of the caller's from the forward's x_mx (rowwise) and w->w1 with the same
+ * MMAs in the same order (bitwise the H the forward would have stored), to
+ * be passed as h to moe_fc2_dgrad_dglu_mx / moe_mlp_bwd_mx. */
+moe_status_t moe_fc1_recompute_h_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                    const int32_t* counts, const int32_t* padded_offsets,
+                                    const moe_mx_weights_t* w, const void* b1p, void* h,
+                                    cudaStream_t stream);
 
 /* MXFP8 backward:
  *   dy     dY bf16 [capacity, d] (bias gradient)   dy_mx  its rowwise and

@@ -39,6 +39,7 @@ EXPORTS = (
     "moe_quantize_nvfp4_bf16", "moe_quantize_act_nvfp4", "moe_quantize_weights_nvfp4",
     "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
     "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
+    "moe_fc1_recompute_h_mx",
 )
 
 
@@ -181,6 +182,7 @@ def lib():
             "moe_fc1_dgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_fc1_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_mlp_fwd_nv": (ctypes.c_int, [D] + [P] * 12),
+            "moe_fc1_recompute_h_mx": (ctypes.c_int, [D] + [P] * 7),
             "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
         }
         for name, (res, args) in sig.items():
@@ -508,3 +510,9 @@ def moe_mlp_bwd_nv(desc, dy, dy_nv, x_nv, h, a_nv, counts, padded_offsets, w_nv,
                                 _mx(a_nv), _p(counts), _p(padded_offsets), _nvw(w_nv), _p(dh),
                                 _mx(dh_nv), _p(dx_perm), _p(dw1p), _p(db1p), _p(dw2), _p(db2),
                                 _stream(stream)))
+
+
+def moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, stream=None):
+    _check(lib().moe_fc1_recompute_h_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
+                                        _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h),
+                                        _stream(stream)))

@@ -862,7 +862,7 @@ void set_scales(GemmArgs& g, const uint8_t* sfa, long long a_rows, const uint8_t
 moe_status_t check_mx_desc(const moe_mlp_desc_t* d) {
   moe_status_t st = check_desc(d, false);
   if (st != MOE_OK) return st;
-  if (d->dtype != MOE_DTYPE_MXFP8 || d->recompute_h) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype != MOE_DTYPE_MXFP8) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
 
@@ -942,7 +942,8 @@ moe_status_t moe_fc1_glu_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
                                 const moe_mx_out_t* a_mx, cudaStream_t stream) {
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
-  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h) return MOE_ERR_NULL;
+  if (!counts || !padded_offsets || !mx_weights_ok(w)) return MOE_ERR_NULL;
+  if (!h && !desc->recompute_h) return MOE_ERR_NULL;   // H kept unless recomputed
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   if (!mx_ok(x_mx, true, false) || !mx_ok(a_mx, true, a_mx && a_mx->qt)) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -955,7 +956,7 @@ moe_status_t moe_fc1_glu_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
       !encode_u8(&g.tma_b, w->w1, d, W1, E, 256) ||
-      !encode_out(&g.tma_out0, h, W1, cap, 1) ||
+      (h && !encode_out(&g.tma_out0, h, W1, cap, 1)) ||
       (a && !encode_out(&g.tma_out1, a, F, cap, 1)))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
@@ -1116,6 +1117,37 @@ moe_status_t moe_fc1_wgrad_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
   g.ld0 = d;
   set_scales(g, dh_mx->scale_t, W1, x_mx->scale_t, d, 0);
   return cuda_status(launch_grouped_gemm_mx(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_recompute_h_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                    const int32_t* counts, const int32_t* padded_offsets,
+                                    const moe_mx_weights_t* w, const void* b1p, void* h,
+                                    cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!mx_ok(x_mx, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // the FC2-shaped plain kernel with W1p as B, on the forward's operands:
+  // the same MMAs in the same order as FC1, so H comes out bitwise the same
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w1, d, W1, E, 256) || !encode_out(&g.tma_out0, h, W1, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(W1);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = W1;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  set_scales(g, x_mx->scale, cap, w->w1_s, W1, sf_bytes(W1, d));
+  return cuda_status(launch_grouped_gemm_mx(kFc2, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,

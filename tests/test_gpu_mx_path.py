@@ -168,3 +168,27 @@ def test_combined_mx_calls_match_per_gemm_calls():
     torch.cuda.synchronize()
     for n, t in ref.items():
         assert torch.equal(getattr(layer, n), t), n
+
+
+def test_mxfp8_activation_recompute_matches_stored_h():
+    """MXFP8 forward without keeping H, backward regenerating it from the
+    forward's MXFP8 operands: bitwise the stored H, hence bitwise the same
+    gradients (FC1 bias, clamp and offset)."""
+    from moe_expert_mlp_gb300 import _lib as L
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    wl = ROUTED["gptoss_small"]
+    inp = make_inputs(wl)
+    ref = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8"))
+    rec = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8", recompute_h=True))
+    assert rec.h is None
+    assert moe_read_device_status() == 0
+    h2 = torch.full_like(ref.h, 7.0)
+    L.moe_fc1_recompute_h_mx(rec.desc, rec.x_mx, rec.counts, rec.padded_offsets, rec.w_mx,
+                             rec.b1p, h2)
+    torch.cuda.synchronize()
+    R_pad = int(H.to_np(ref.padded_offsets)[-1])
+    assert torch.equal(h2[:R_pad].view(torch.int16), ref.h[:R_pad].view(torch.int16))
+    for name in ("out", "dx", "dw1p", "db1p", "dw2", "db2", "dlogits", "dh"):
+        a, b = getattr(ref, name), getattr(rec, name)
+        assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                           b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
