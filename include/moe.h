@@ -84,7 +84,8 @@ typedef enum {
 typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2, MOE_DTYPE_NVFP4 = 3 } moe_dtype_t;
 /* NVFP4 (the *_nv calls): E2M1 operands, one UE4M3 scale per 16 elements
  * along each GEMM's contraction dimension and one fp32 encode scale per
- * tensor from its amax; requires d and F multiples of 64 and recompute_h = 0. */
+ * tensor from its amax; requires d and F multiples of 64 (recompute_h: see
+ * moe_fc1_recompute_h_nv). */
 
 /* GLU activations ([FK] "Overcoming training bottlenecks": SwiGLU, GeGLU,
  * sReLU with optional clamp and scaling).  With g the gate half, l the
@@ -577,6 +578,16 @@ moe_status_t moe_fc1_dgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh
 moe_status_t moe_fc1_wgrad_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* dh_nv,
                               const moe_mx_out_t* x_nv, const int32_t* counts,
                               const int32_t* padded_offsets, void* dw1p, cudaStream_t stream);
+
+/* Activation recompute on the NVFP4 path (desc->recompute_h = 1): the
+ * forward may pass h = NULL; this call regenerates H [capacity, W1] bf16
+ * into a caller buffer from the forward's x_nv (rowwise) and w->q.w1 with
+ * the same MMAs and encode factors (bitwise the H the forward would have
+ * stored), to be passed as h to the dGLU call. */
+moe_status_t moe_fc1_recompute_h_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_nv,
+                                    const int32_t* counts, const int32_t* padded_offsets,
+                                    const moe_nv_weights_t* w, const void* b1p, void* h,
+                                    cudaStream_t stream);
 
 /* NVFP4 forward (desc->dtype = MOE_DTYPE_NVFP4) in one call:
  *   x_perm bf16 [capacity, d] -> x_nv (amax computed, rowwise + rotated

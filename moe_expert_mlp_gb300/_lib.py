@@ -39,7 +39,7 @@ EXPORTS = (
     "moe_quantize_nvfp4_bf16", "moe_quantize_act_nvfp4", "moe_quantize_weights_nvfp4",
     "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
     "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
-    "moe_fc1_recompute_h_mx",
+    "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv",
 )
 
 
@@ -183,6 +183,7 @@ def lib():
             "moe_fc1_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_mlp_fwd_nv": (ctypes.c_int, [D] + [P] * 12),
             "moe_fc1_recompute_h_mx": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc1_recompute_h_nv": (ctypes.c_int, [D] + [P] * 7),
             "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
         }
         for name, (res, args) in sig.items():
@@ -515,4 +516,10 @@ def moe_mlp_bwd_nv(desc, dy, dy_nv, x_nv, h, a_nv, counts, padded_offsets, w_nv,
 def moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, stream=None):
     _check(lib().moe_fc1_recompute_h_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
                                         _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h),
+                                        _stream(stream)))
+
+
+def moe_fc1_recompute_h_nv(desc, x_nv, counts, padded_offsets, w_nv, b1p, h, stream=None):
+    _check(lib().moe_fc1_recompute_h_nv(ctypes.byref(desc), _mx(x_nv), _p(counts),
+                                        _p(padded_offsets), _nvw(w_nv), _p(b1p), _p(h),
                                         _stream(stream)))

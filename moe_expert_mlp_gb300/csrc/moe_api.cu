@@ -1196,7 +1196,7 @@ namespace {
 moe_status_t check_nv_desc(const moe_mlp_desc_t* d) {
   moe_status_t st = check_desc(d, false);
   if (st != MOE_OK) return st;
-  if (d->dtype != MOE_DTYPE_NVFP4 || d->recompute_h) return MOE_ERR_UNSUPPORTED;
+  if (d->dtype != MOE_DTYPE_NVFP4) return MOE_ERR_UNSUPPORTED;
   if (d->F % 64 != 0) return MOE_ERR_SHAPE;
   return MOE_OK;
 }
@@ -1319,7 +1319,8 @@ moe_status_t moe_fc1_glu_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
                                 float* a_amax, cudaStream_t stream) {
   moe_status_t st = check_nv_desc(desc);
   if (st != MOE_OK) return st;
-  if (!counts || !padded_offsets || !nv_weights_ok(w) || !h || !a || !a_amax) return MOE_ERR_NULL;
+  if (!counts || !padded_offsets || !nv_weights_ok(w) || !a || !a_amax) return MOE_ERR_NULL;
+  if (!h && !desc->recompute_h) return MOE_ERR_NULL;   // H kept unless recomputed
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   if (!nv_ok(x_nv, true, false)) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -1331,7 +1332,7 @@ moe_status_t moe_fc1_glu_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, x_nv->q, d / 2, cap, 1, 128) ||
       !encode_u8(&g.tma_b, w->q.w1, d / 2, W1, E, 256) ||
-      !encode_out(&g.tma_out0, h, W1, cap, 1) || !encode_out(&g.tma_out1, a, F, cap, 1))
+      (h && !encode_out(&g.tma_out0, h, W1, cap, 1)) || !encode_out(&g.tma_out1, a, F, cap, 1))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = static_cast<int>(W1);
@@ -1346,6 +1347,37 @@ moe_status_t moe_fc1_glu_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* 
   if ((st = set_amax_out(g, a_amax, desc->F, stream)) != MOE_OK) return st;
   return cuda_status(launch_grouped_gemm_nv(desc->act == MOE_ACT_SRELU ? kFc1Act : kFc1Glu, g,
                                             grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_recompute_h_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_nv,
+                                    const int32_t* counts, const int32_t* padded_offsets,
+                                    const moe_nv_weights_t* w, const void* b1p, void* h,
+                                    cudaStream_t stream) {
+  moe_status_t st = check_nv_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!counts || !padded_offsets || !nv_weights_ok(w) || !h) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!nv_ok(x_nv, true, false)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // the FC2-shaped plain kernel with W1p as B on the forward's NVFP4 operands
+  // (same MMAs, same 1/(g_a g_b) and bias): bitwise the H FC1 would store
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, x_nv->q, d / 2, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->q.w1, d / 2, W1, E, 256) || !encode_out(&g.tma_out0, h, W1, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(W1);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = W1;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  set_nv_scales(g, x_nv->scale, cap, w->q.w1_s, W1, nv_sf_bytes(W1, d), x_nv->amax, w->amax);
+  return cuda_status(launch_grouped_gemm_nv(kFc2, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc2_fwd_nv(const moe_mlp_desc_t* desc, const moe_mx_out_t* a_nv,
@@ -1500,7 +1532,7 @@ moe_status_t moe_mlp_fwd_nv(const moe_mlp_desc_t* desc, const void* x_perm,
                             const moe_mx_out_t* a_nv, void* y, cudaStream_t stream) {
   moe_status_t st = check_nv_desc(desc);
   if (st != MOE_OK) return st;
-  if (!x_perm || !a || !y || !a_nv) return MOE_ERR_NULL;
+  if (!x_perm || !a || !y || !a_nv) return MOE_ERR_NULL;   // h may be NULL with recompute_h
   if ((st = moe_quantize_act_nvfp4(desc, x_perm, desc->d, padded_offsets, x_nv, 1, stream)) !=
           MOE_OK ||
       (st = moe_fc1_glu_fwd_nv(desc, x_nv, counts, padded_offsets, w, b1p, h, a, a_nv->amax,

@@ -252,8 +252,15 @@ class MoEExpertMLP:
         if self.nv:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_nvfp4(self.desc, self.dy, self.d, po, self.dy_nv, True, stream)
+            h = self.h
+            if self.recompute_h:                  # regenerate H into a transient buffer
+                h = torch.empty((self.capacity, self.W1), dtype=torch.bfloat16,
+                                device=self.w2.device)
+                with self._t(timer, "fc1_recompute_h"):
+                    L.moe_fc1_recompute_h_nv(self.desc, self.x_nv, c, po, self.w_nv, self.b1p,
+                                             h, stream)
             with self._t(timer, "fc2_dgrad_dglu"):
-                L.moe_fc2_dgrad_dglu_nv(self.desc, self.dy_nv, self.h, c, po, self.w_nv, self.dh,
+                L.moe_fc2_dgrad_dglu_nv(self.desc, self.dy_nv, h, c, po, self.w_nv, self.dh,
                                         self.dh_nv["amax"], stream)
             with self._t(timer, "quant_dh"):
                 L.moe_quantize_act_nvfp4(self.desc, self.dh, self.W1, po, self.dh_nv, False,

@@ -291,3 +291,34 @@ def test_composite_calls_match_per_call_path():
     for name in ("h", "a", "y", "dh", "dx_perm", "dw1p", "db1p", "dw2", "db2"):
         t1, t2 = getattr(one, name), getattr(two, name)
         assert torch.equal(t1.view(torch.int16), t2.view(torch.int16)), name
+
+
+def test_nvfp4_activation_recompute_matches_stored_h():
+    """NVFP4 forward without keeping H, backward regenerating it from the
+    forward's NVFP4 operands: bitwise the stored H and the same gradients."""
+    wl = CASES["gptoss_like"]                       # FC1 bias, clamp, offset
+    inp = make_inputs(wl)
+    ref = _direct_nv_layer(wl, inp)
+    ref.mlp_forward()
+    ref.mlp_backward()
+    sizes = inp["group_sizes"]
+    _, padded, _ = oracle.group_offsets(sizes, align=128)
+    rec = H.make_layer(wl, capacity=ref.capacity, dtype="nvfp4", recompute_h=True)
+    H.load_layer_weights(rec, inp)
+    rec.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
+    rec.x_perm.copy_(ref.x_perm)
+    rec.dy.copy_(ref.dy)
+    rec.mlp_forward()
+    rec.mlp_backward()
+    assert rec.h is None
+    h2 = torch.full_like(ref.h, 7.0)
+    L.moe_fc1_recompute_h_nv(rec.desc, rec.x_nv, rec.counts, rec.padded_offsets, rec.w_nv,
+                             rec.b1p, h2)
+    torch.cuda.synchronize()
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    R_pad = int(padded[-1])
+    assert torch.equal(h2[:R_pad].view(torch.int16), ref.h[:R_pad].view(torch.int16))
+    for name in ("a", "y", "dh", "dx_perm", "dw1p", "db1p", "dw2", "db2"):
+        assert torch.equal(getattr(ref, name).view(torch.int16),
+                           getattr(rec, name).view(torch.int16)), name
