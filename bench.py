@@ -5,8 +5,12 @@ A step is one whole pass of the hot path over one batch of synthetic input:
 routing + permute -> FC1 grouped GEMM with the GLU epilogue -> FC2 grouped
 GEMM -> weighted combine -> combine backward -> FC2 dgrad with the dGLU
 epilogue -> FC2 wgrad -> FC1 dgrad -> FC1 wgrad -> permute backward ->
-router backward.  Default workload: T=4096 tokens, E=64 experts, top-6,
-d=2048, F=1408 (SwiGLU, bf16), logits ~N(0,1) plus a per-expert bias.
+router backward.  For layers whose groups are given directly (no router) the
+step is the expert MLP alone: the activation quantizations and the six
+grouped GEMMs.  Default workload: the DeepSeek-V3-shaped local experts,
+16384 routed rows over 32 experts with Zipf(1.2) group sizes (4 empty),
+d=7168, F=2048, SwiGLU, MXFP8 GEMM operands (E4M3 with an E8M0 scale per 32
+elements).
 
 The K timed steps are captured in one CUDA graph (no host synchronisation
 inside) with timing events around every library call, replayed once between
@@ -50,12 +54,14 @@ import numpy as np  # noqa: E402
 from workloads import WORKLOADS, bf16_bits_to_f64, make_inputs  # noqa: E402
 
 METRIC = "MoE expert-MLP fwd+bwd TFLOPS & tokens/s on 1 GB300; % of tensor-core peak"
-DEFAULT_WORKLOAD = "bf16_t4096_e64"
+DEFAULT_WORKLOAD = "dsv3_r16384_e32"
+DEFAULT_DTYPE = "mxfp8"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
-# DRAM bytes (read + write) per launch from one ncu capture of the default
-# workload (profiles/grouped_gemm_bf16_t4096_e64.md), with the hash of the
-# GEMM sources the counters were taken on; a changed kernel reports null.
+# DRAM bytes (read + write) per launch of each grouped GEMM, from one ncu
+# capture per workload and operand type (summaries under profiles/), with the
+# hash of the GEMM sources the counters were taken on; a changed kernel
+# reports null.
 _NCU_SRC = "b9e4ee2528075627"
 NCU_TRAFFIC = {
     ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 787.954432e6 + 217.387776e6, "src": _NCU_SRC},
@@ -557,8 +563,11 @@ def run_ours(args, wl):
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
     e2e = None
-    if not args.no_e2e and routed:
-        e2e = run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist)
+    if not args.no_e2e:
+        if routed:
+            e2e = run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist)
+        else:
+            e2e = run_e2e_grouped(torch, layer, dev, K, W, flops_step, world, dist)
 
     if rank != 0:
         if world > 1:
@@ -839,6 +848,63 @@ def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
                        "api": "MoEExpertMLP.step with in-line copies"}}
 
 
+def run_e2e_grouped(torch, layer, dev, K, W, flops_step, world, dist):
+    """End to end for groups given directly (no router): every step copies
+    in, from pinned host memory, the expert-ordered rows x_perm and their
+    upstream gradient dY in the library's padded row layout plus the group
+    sizes, recomputes the group offsets on the device, runs the expert MLP
+    forward and backward, and copies the per-row results Y and dX_perm back
+    to pinned host memory.  The weight gradients stay on the device for the
+    optimizer.  Headline: GroupedHostStepPipeline (copies overlapped with
+    the neighbouring steps' kernels); also reported: the same copies issued
+    in line on one stream."""
+    from moe_expert_mlp_gb300.pipeline import GroupedHostStepPipeline
+    host_in = dict(x_perm=layer.x_perm.cpu().pin_memory(), dy=layer.dy.cpu().pin_memory(),
+                   counts=layer.counts.cpu().pin_memory())
+    outs = [dict(y=torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory(),
+                 dx_perm=torch.empty(layer.dx_perm.shape, dtype=layer.dx_perm.dtype).pin_memory())
+            for _ in range(2)]
+    pipe = GroupedHostStepPipeline(layer, dev)
+    cnt_dev = torch.zeros_like(layer.counts)
+
+    def serial():
+        layer.x_perm.copy_(host_in["x_perm"], non_blocking=True)
+        layer.dy.copy_(host_in["dy"], non_blocking=True)
+        cnt_dev.copy_(host_in["counts"], non_blocking=True)
+        layer.grouped_step(counts=cnt_dev)
+        outs[0]["y"].copy_(layer.y, non_blocking=True)
+        outs[0]["dx_perm"].copy_(layer.dx_perm, non_blocking=True)
+
+    def timed(fn):
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b)
+        return max_over_ranks(ms, dist, dev) if world > 1 else ms
+
+    pipe.run([host_in] * W, [outs[i % 2] for i in range(W)])
+    ms = timed(lambda: pipe.run([host_in] * K, [outs[i % 2] for i in range(K)]))
+    for _ in range(W):
+        serial()
+    ms_serial = timed(lambda: [serial() for _ in range(K)])
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in outs[0].values())
+    return {"value": round(job_rate(flops_step, K, world, ms) / 1e12, 2), "unit": "TFLOPS",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / K, 5),
+            "api": "GroupedHostStepPipeline (copies overlapped); inputs x_perm, dY, group sizes; "
+                   "results Y, dX_perm; weight gradients stay on the device",
+            "serial": {"value": round(job_rate(flops_step, K, world, ms_serial) / 1e12, 2),
+                       "ms_per_step": round(ms_serial / K, 5),
+                       "api": "MoEExpertMLP.grouped_step with in-line copies"}}
+
+
 class _Null:
     def __enter__(self):
         return self
@@ -867,11 +933,14 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WORKLOADS))
-    ap.add_argument("--cpu-sample-tokens", type=int, default=1024,
-                    help="tokens (or rows) of the oracle sample in the cpu_baseline leg")
-    ap.add_argument("--ref-sample-tokens", type=int, default=256,
-                    help="tokens (or rows) per step of --impl reference")
-    ap.add_argument("--dtype", choices=["bf16", "mxfp8", "nvfp4"], default="bf16",
+    ap.add_argument("--cpu-sample-tokens", type=int, default=None,
+                    help="tokens (routed layers; default 1024) or rows (direct groups: the "
+                         "smallest experts up to this many rows; default one expert) of the "
+                         "oracle sample in the cpu_baseline leg")
+    ap.add_argument("--ref-sample-tokens", type=int, default=None,
+                    help="the same for each step of --impl reference (default 256 tokens, or "
+                         "the smallest expert)")
+    ap.add_argument("--dtype", choices=["bf16", "mxfp8", "nvfp4"], default=DEFAULT_DTYPE,
                     help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales; nvfp4: E2M1 + "
                          "UE4M3 scales per 16 + per-tensor scales)")
     ap.add_argument("--act", choices=["swiglu", "geglu", "sreglu", "srelu"], default=None,
@@ -889,6 +958,15 @@ def main():
                     help="skip the fused-vs-unfused expert MLP comparison")
     args = ap.parse_args()
     wl = WORKLOADS[args.workload]
+    # oracle samples: the oracle quantizes each sampled expert's weights
+    # (tens of millions of elements, seconds each at the DeepSeek-shaped
+    # size), so on layers with directly given groups the sample is the
+    # smallest non-empty expert and all of its rows
+    direct = wl.router == "direct"
+    if args.cpu_sample_tokens is None:
+        args.cpu_sample_tokens = 1 if direct else 1024
+    if args.ref_sample_tokens is None:
+        args.ref_sample_tokens = 1 if direct else 256
     if args.act is not None:
         wl = dataclasses.replace(wl, act=args.act)
     if args.impl == "reference":

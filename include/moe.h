@@ -623,7 +623,10 @@ moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
  * exits).  Requires ceil(T/256)*E*4 <= 262144 bytes, else returns
  * MOE_ERR_WORKSPACE and enqueues nothing.  It allocates nothing.  The first
  * call on a device looks up the array's device address (with that device
- * current) and should happen before any stream capture.  All calls share
+ * current) and should happen before any stream capture; the address is kept
+ * until the process exits, so a device reset (cudaDeviceReset) after that
+ * first call is not supported (the same holds for every call of this
+ * library, which keeps the address of its status word).  All calls share
  * the array: calls whose GPU work may overlap (unordered streams) race;
  * calls ordered on one stream are safe because each call zeroes the
  * histogram before use. */

@@ -19,7 +19,9 @@
 //     every call, so nothing left by the previous call is read);
 //   * the first call on each device looks up the array's device address
 //     (cudaGetSymbolAddress) with that device current; make that first call
-//     before any stream capture.
+//     before any stream capture.  The address is kept for the life of the
+//     process, so resetting the device (cudaDeviceReset) after the first
+//     call is not supported.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -62,10 +64,10 @@ extern "C" moe_status_t moe_route_permute_noalloc(
     int32_t* topk_idx, float* topk_w, int32_t* counts, int32_t* offsets,
     int32_t* padded_offsets, int32_t* tile_prefix, int32_t* row_src, int32_t* row_of,
     void* x_perm, cudaStream_t stream) {
-  size_t need = 0;
-  moe_status_t st = moe_workspace_size(desc, &need);
-  if (st != MOE_OK) return st;
-  if (desc->T < 0) return MOE_ERR_SHAPE;
+  // the rest of the descriptor is checked by moe_route_permute below
+  if (!desc) return MOE_ERR_NULL;
+  if (desc->T < 0 || desc->E < 1) return MOE_ERR_SHAPE;
+  moe_status_t st;
   const size_t chunks =
       (static_cast<size_t>(desc->T) + moe::kTokensPerChunk - 1) / moe::kTokensPerChunk;
   if (chunks * static_cast<size_t>(desc->E) * sizeof(int32_t) > moe::kStaticScratchBytes)

@@ -374,9 +374,25 @@ class MoEExpertMLP:
         self.forward(x, logits, bias, stream, timer)
         self.backward(dout, stream, timer)
 
-    def grouped_step(self, stream=None, timer=None):
+    def grouped_step(self, stream=None, timer=None, counts=None, x_perm=None, dy=None, y=None,
+                     dx_perm=None):
         """Forward + backward of the expert MLP alone, for groups given
-        directly (x_perm and dy already in place)."""
+        directly (x_perm and dy already in place).  counts: new group sizes
+        (int32 [E] on the device; the group offsets are recomputed on the
+        device first).  x_perm, dy, y, dx_perm: [capacity, d] bf16 device
+        tensors the layer reads its inputs from and writes its per-row
+        results to from now on (no copy is made)."""
+        if x_perm is not None:
+            self.x_perm = x_perm
+        if dy is not None:
+            self.dy = dy
+        if y is not None:
+            self.y = y
+        if dx_perm is not None:
+            self.dx_perm = dx_perm
+        if counts is not None:
+            with self._t(timer, "group_offsets"):
+                self.set_groups(counts, stream)
         self.mlp_forward(stream, timer)
         self.mlp_backward(stream, timer)
 

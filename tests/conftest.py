@@ -28,3 +28,25 @@ def read_golden(path):
                 continue
             rows.append([c.strip() for c in line.split(";")])
     return rows
+
+
+def pytest_terminal_summary(terminalreporter):
+    """Print the achieved error ratios of the MXFP8 parity checks (max
+    |gpu - ref| / max |ref| against the oracle with the same quantization,
+    relative Frobenius error against the unquantized oracle) when any were
+    recorded."""
+    try:
+        from tests import harness
+    except ImportError:
+        return
+    if not harness.MX_RATIOS:
+        return
+    tr = terminalreporter
+    tr.write_line("MXFP8 parity: max|gpu-ref|/max|ref| against the oracle with the same "
+                  "quantization (bound 1e-2) / relative Frobenius error against the "
+                  "unquantized oracle (bound 1e-1):")
+    worst_m = max(r[1] for r in harness.MX_RATIOS)
+    worst_u = max((r[2] for r in harness.MX_RATIOS if r[2] is not None), default=None)
+    for name, r_m, r_u in harness.MX_RATIOS:
+        tr.write_line(f"  {name}: {r_m:.2e}" + (f" / {r_u:.2e}" if r_u is not None else ""))
+    tr.write_line(f"  worst: {worst_m:.2e}" + (f" / {worst_u:.2e}" if worst_u is not None else ""))

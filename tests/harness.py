@@ -142,7 +142,42 @@ def packed_to_logical_cols(t_np, F):
 # --------------------------------------------------------------------------
 # MXFP8 path
 # --------------------------------------------------------------------------
-TOL_MX = 6e-2       # max|gpu - ref| <= 6e-2 * max|ref| (MXFP8 path)
+TOL_MX = 6e-2       # the MXFP8 path's tolerance (met here with the bf16 bound, below)
+# Against the unquantized fp64 oracle the MXFP8 format's own error (E4M3
+# payloads with 3 mantissa bits, chained through H -> A -> Y and dY -> dA ->
+# dH) is 6-8 % in relative Frobenius norm on these layers and reaches 15 %
+# of max|ref| in single elements (a block maximum saturated at 448 by the
+# OCP floor scale).  That comparison is a format sanity bound, which a
+# wiring error (a dropped K block, a wrong scale atom) exceeds by far; the
+# kernel check is the quantization-matched one.
+TOL_MX_FRO = 1e-1
+
+# Achieved error ratios of the MXFP8 checks, printed at the end of the run
+# (tests/conftest.py): (name, max err / max|ref| against the oracle with the
+# same MXFP8 quantization, relative Frobenius error against the unquantized
+# oracle).
+MX_RATIOS = []
+
+
+def assert_mx(name, got, ref_mx, ref_plain=None):
+    """An output of the MXFP8 path.  Against the oracle that quantizes the
+    same operands the same way, the only differences are fp32 accumulation
+    order, the bf16 rounding of stored tensors, and rare single-code flips
+    where an intermediate the GPU re-quantizes (A, dH) lands one bf16 ulp
+    away from the oracle's on the other side of an E4M3 rounding point: the
+    bf16 bound applies.  Against the unquantized fp64 oracle the format's
+    own error is bounded in relative Frobenius norm by TOL_MX_FRO."""
+    err, _ = assert_close(name, got, ref_mx)
+    scale = float(np.max(np.abs(ref_mx))) if np.size(ref_mx) else 0.0
+    r_u = None
+    if ref_plain is not None:
+        g = np.asarray(got, dtype=np.float64)
+        r = np.asarray(ref_plain, dtype=np.float64)
+        assert g.shape == r.shape, (name, g.shape, r.shape)
+        nr = float(np.linalg.norm(r))
+        r_u = float(np.linalg.norm(g - r)) / nr if nr > 0 else 0.0
+        assert r_u <= TOL_MX_FRO, f"{name} vs unquantized: relative Frobenius {r_u:.3e}"
+    MX_RATIOS.append((name, err / scale if scale > 0 else 0.0, r_u))
 
 
 def mma_scales_to_rowmajor(buf, rows, cols):

@@ -3,9 +3,11 @@ fp64 MXFP8 oracle on the same seeded inputs.
 
 Bit-exact: routing, the quantizer in the MMA scale layout, and the fused
 MXFP8 outputs of the epilogues (given the GPU's own bf16 values, as for the
-bf16 path's fused outputs).  H and A come from identical quantized operands,
-so they meet the bf16 tolerance; everything downstream of a quantized
-intermediate meets max|gpu-ref| <= 6e-2 * max|ref|.
+bf16 path's fused outputs).  Every float output meets the bf16 bound
+max|gpu-ref| <= 1e-2 * max|ref| + 1e-3 against the oracle that quantizes the
+same operands the same way (the MXFP8 path's 6e-2 tolerance, met with six
+times less), and ||gpu-ref||_F <= 1e-1 ||ref||_F against the unquantized
+fp64 oracle (the format's own error is 6-8 %, see tests/harness.py).
 """
 import numpy as np
 import pytest
@@ -29,8 +31,10 @@ ROUTED = {
 }
 
 
-def _mx_close(name, got, ref):
-    return H.assert_close(name, got, ref, rel=H.TOL_MX, abs_=0.0)
+def _mx_close(name, got, ref, plain=None):
+    """Quantization-matched oracle at the bf16 bound; the unquantized oracle
+    (when given) at the format bound in relative Frobenius norm."""
+    return H.assert_mx(name, got, ref, plain)
 
 
 def test_quantizer_mma_layout_bit_exact():
@@ -87,6 +91,7 @@ def test_routed_layer_mxfp8(name):
     wl = ROUTED[name]
     inp = make_inputs(wl)
     ref = H.run_oracle_routed_mx(wl, inp)
+    fwd, bwd = H.run_oracle_routed(wl, inp)          # unquantized fp64 oracle
     layer = H.run_gpu_routed(wl, inp, layer=H.make_layer(wl, dtype="mxfp8"))
     from moe_expert_mlp_gb300 import moe_read_device_status
     assert moe_read_device_status() == 0
@@ -98,21 +103,22 @@ def test_routed_layer_mxfp8(name):
     assert np.all(h_pad == 0)
     H.assert_close("H", h_log, ref["H"])
     H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
-    _mx_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
-    _mx_close("out", H.to_np(layer.out)[:T], ref["out"])
+    tag = name + "/"
+    _mx_close(tag + "Y", H.to_np(layer.y)[:R_pad], ref["Y"], fwd["Y"])
+    _mx_close(tag + "out", H.to_np(layer.out)[:T], ref["out"], fwd["out"])
     dh_log, dh_pad = H.packed_to_logical_cols(H.to_np(layer.dh)[:R_pad], wl.F)
     assert np.all(dh_pad == 0)
-    _mx_close("dH", dh_log, ref["dH"])
-    _mx_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
-    _mx_close("dW2", H.to_np(layer.dw2), ref["dW2"])
-    _mx_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    _mx_close(tag + "dH", dh_log, ref["dH"], bwd["dH"])
+    _mx_close(tag + "dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"], bwd["dX_perm"])
+    _mx_close(tag + "dW2", H.to_np(layer.dw2), ref["dW2"], bwd["dW2"])
+    _mx_close(tag + "dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"], bwd["dW1"])
     if wl.has_b1:
         db1 = H.to_np(layer.unpack_fc1(layer.db1p.reshape(wl.E, -1, 1).contiguous(), 1))[..., 0]
-        _mx_close("db1", db1, ref["db1"])
+        _mx_close(tag + "db1", db1, ref["db1"], bwd["db1"])
     if wl.has_b2:
-        _mx_close("db2", H.to_np(layer.db2), ref["db2"])
-    _mx_close("dx", H.to_np(layer.dx)[:T], ref["dx"])
-    _mx_close("dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"])
+        _mx_close(tag + "db2", H.to_np(layer.db2), ref["db2"], bwd["db2"])
+    _mx_close(tag + "dx", H.to_np(layer.dx)[:T], ref["dx"], bwd["dx"])
+    _mx_close(tag + "dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"], bwd["dlogits"])
     _check_fused_mx(layer, "A", layer.a, layer.a_mx, wl.F)
     _check_fused_mx(layer, "dH", layer.dh, layer.dh_mx, layer.W1)
 
@@ -125,14 +131,16 @@ def test_direct_groups_mxfp8_with_empty_experts():
     inp["group_sizes"][np.argmax(inp["group_sizes"])] -= 1
     inp["group_sizes"][int(np.flatnonzero(inp["group_sizes"] == 0)[0])] = 1
     layer, ref = H.run_both_direct_mx(wl, inp)
+    _, plain = H.run_both_direct(wl, inp)             # unquantized oracle (and a bf16 layer)
     R_pad = int(ref["padded_offsets"][-1])
     h_log, _ = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
     H.assert_close("H", h_log, ref["H"])
     H.assert_close("A", H.to_np(layer.a)[:R_pad], ref["A"])
-    _mx_close("Y", H.to_np(layer.y)[:R_pad], ref["Y"])
-    _mx_close("dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"])
-    _mx_close("dW2", H.to_np(layer.dw2), ref["dW2"])
-    _mx_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"])
+    _mx_close("direct/Y", H.to_np(layer.y)[:R_pad], ref["Y"], plain["Y"])
+    _mx_close("direct/dX_perm", H.to_np(layer.dx_perm)[:R_pad], ref["dX_perm"], plain["dX_perm"])
+    _mx_close("direct/dW2", H.to_np(layer.dw2), ref["dW2"], plain["dW2"])
+    _mx_close("direct/dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), ref["dW1"],
+              plain["dW1"])
     for e in np.flatnonzero(ref["counts"] == 0):
         assert torch.count_nonzero(layer.dw2[e]) == 0
         assert torch.count_nonzero(layer.dw1p[e]) == 0

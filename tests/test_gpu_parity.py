@@ -265,3 +265,33 @@ def test_tiny_fp32_inputs_within_bf16_tolerance():
                            ("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), bwd["dW1"]),
                            ("dW2", H.to_np(layer.dw2), bwd["dW2"])]:
         H.assert_close(name, got, ref, abs_=0.0)
+
+
+@pytest.mark.parametrize("name", ["gptoss_small", "srelu_nongated"])
+def test_composite_bf16_calls_match_per_gemm_calls(name):
+    """moe_mlp_fwd / moe_mlp_bwd (one call each: FC1 + GLU, FC2; FC2 dgrad +
+    dGLU, both weight gradients, FC1 dgrad, bias gradients) == the per-GEMM
+    calls the layer makes, bit for bit, with biases, clamp and offset (and
+    the non-gated activation)."""
+    from moe_expert_mlp_gb300 import _lib as L
+    wl = CASES[name]
+    inp = make_inputs(wl)
+    layer = H.run_gpu_routed(wl, inp)
+    names = ["h", "a", "y", "dh", "dx_perm", "dw1p", "dw2"]
+    names += [n for n in ("db1p", "db2") if getattr(layer, n) is not None]
+    ref = {n: getattr(layer, n).clone() for n in names}
+    for n in names:
+        getattr(layer, n).fill_(3.0)
+    c, po = layer.counts, layer.padded_offsets
+    L.moe_mlp_fwd(layer.desc, layer.x_perm, c, po, layer.w1p, layer.b1p, layer.w2, layer.b2,
+                  layer.h, layer.a, layer.y, layer.ws)
+    L.moe_mlp_bwd(layer.desc, layer.dy, layer.x_perm, layer.h, layer.a, c, po, layer.w1p,
+                  layer.w2, layer.dh, layer.dx_perm, layer.dw1p, layer.db1p, layer.dw2,
+                  layer.db2, layer.ws, b1p=layer.b1p)
+    torch.cuda.synchronize()
+    R_pad = int(H.to_np(layer.padded_offsets)[-1])       # rows past it are never written
+    for n, t in ref.items():
+        got = getattr(layer, n)
+        if n in ("h", "a", "y", "dh", "dx_perm"):
+            got, t = got[:R_pad], t[:R_pad]
+        assert torch.equal(got.view(torch.int16), t.view(torch.int16)), n

@@ -83,3 +83,19 @@ def test_block_scaled_calls_reject_bad_arguments_without_gpu(libmoe):
     assert L.moe_nvfp4_scale_bytes(256, 256) == 4 * 2 * 512
     assert L.moe_nvfp4_scale_bytes(0, 64) == 0
     assert L.moe_mx_scale_bytes(256, 256) == 2 * 2 * 512
+
+
+def test_noalloc_size_limit_boundary(libmoe):
+    """moe_route_permute_noalloc accepts a histogram of exactly 256 KiB
+    (ceil(T/256) * E = 65536 entries: T = 65536, E = 256) and rejects one
+    chunk more with MOE_ERR_WORKSPACE before anything else.  The accepted
+    case is given NULL buffers, so it stops at the next check (MOE_ERR_NULL
+    with a GPU, MOE_ERR_CUDA without one) and launches nothing."""
+    import ctypes
+    import moe_expert_mlp_gb300 as m
+    null = ctypes.c_void_p(None)
+    at = m.make_desc(T=65536, E=256, k=1, d=64, F=32)
+    over = m.make_desc(T=65536 + 1, E=256, k=1, d=64, F=32)
+    assert libmoe.moe_route_permute_noalloc(ctypes.byref(over), *([null] * 13)) == 4
+    assert libmoe.moe_route_permute_noalloc(ctypes.byref(at), *([null] * 13)) in (1, 6)
+    assert libmoe.moe_route_permute_noalloc(None, *([null] * 13)) == 1

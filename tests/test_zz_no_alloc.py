@@ -45,33 +45,65 @@ def _compare(got, ref):
     H.assert_close("topk_w", H.to_np(got["topk_w"]), H.to_np(ref["topk_w"]), rel=1e-5, abs_=1e-6)
 
 
-def test_noalloc_route_permute_matches_allocating_call_twice():
+def _routing_case(T, E, k, d):
     import moe_expert_mlp_gb300 as m
     from moe_expert_mlp_gb300 import _lib as L
 
-    wl = scaled(WORKLOADS["bf16_t4096_e64"], T=1500, E=24, k=5, d=192, F=64)
+    wl = scaled(WORKLOADS["bf16_t4096_e64"], T=max(T, 1), E=E, k=k, d=d, F=64)
     inp = make_inputs(wl, with_weights=False)
     dev = torch.device("cuda")
-    desc = m.make_desc(wl.T, wl.E, wl.k, wl.d, wl.F)
+    desc = m.make_desc(T, E, k, d, 64)
     x = H.bits_to_dev(inp["x"])
     logits = torch.from_numpy(inp["logits"]).to(dev)
     bias = torch.from_numpy(inp["bias"]).to(dev)
-
-    ref = _outputs(desc, wl.T, wl.E, wl.k, wl.d, dev)
-    ws = torch.zeros(m.moe_workspace_size(desc), dtype=torch.uint8, device=dev)
+    ref = _outputs(desc, max(T, 1), E, k, d, dev)
+    ws = torch.zeros(max(m.moe_workspace_size(desc), 256), dtype=torch.uint8, device=dev)
     L.moe_route_permute(desc, logits, bias, x, ref["topk_idx"], ref["topk_w"], ref["counts"],
                         ref["offsets"], ref["padded_offsets"], ref["tile_prefix"], ref["row_src"],
                         ref["row_of"], ref["x_perm"], ws)
     torch.cuda.synchronize()
+    return m, L, desc, logits, bias, x, ref
 
+
+def _noalloc(L, desc, logits, bias, x, got, stream=None):
+    L.moe_route_permute_noalloc(desc, logits, bias, x, got["topk_idx"], got["topk_w"],
+                                got["counts"], got["offsets"], got["padded_offsets"],
+                                got["tile_prefix"], got["row_src"], got["row_of"], got["x_perm"],
+                                stream)
+
+
+def test_noalloc_route_permute_matches_allocating_call_twice():
+    T, E, k, d = 1500, 24, 5, 192
+    m, L, desc, logits, bias, x, ref = _routing_case(T, E, k, d)
     for _ in range(2):
-        got = _outputs(desc, wl.T, wl.E, wl.k, wl.d, dev)
-        L.moe_route_permute_noalloc(desc, logits, bias, x, got["topk_idx"], got["topk_w"],
-                                    got["counts"], got["offsets"], got["padded_offsets"],
-                                    got["tile_prefix"], got["row_src"], got["row_of"],
-                                    got["x_perm"])
+        got = _outputs(desc, T, E, k, d, torch.device("cuda"))
+        _noalloc(L, desc, logits, bias, x, got)
         torch.cuda.synchronize()
         _compare(got, ref)
+    assert m.moe_read_device_status() == 0
+
+
+def test_noalloc_on_a_side_stream_and_with_no_tokens():
+    """The same comparison on a non-default stream, and for a batch with no
+    tokens (every count zero, offsets all zero) right after a full one, so
+    that nothing the previous call left in the shared array leaks in."""
+    T, E, k, d = 700, 16, 3, 128
+    m, L, desc, logits, bias, x, ref = _routing_case(T, E, k, d)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    got = _outputs(desc, T, E, k, d, torch.device("cuda"))
+    with torch.cuda.stream(side):
+        _noalloc(L, desc, logits, bias, x, got, side)
+    side.synchronize()
+    _compare(got, ref)
+
+    m, L, desc0, logits, bias, x, ref0 = _routing_case(0, E, k, d)
+    got0 = _outputs(desc0, 1, E, k, d, torch.device("cuda"))
+    _noalloc(L, desc0, logits, bias, x, got0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(got0["counts"]) == 0
+    for name in ("counts", "offsets", "padded_offsets", "tile_prefix"):
+        assert torch.equal(got0[name], ref0[name]), name
     assert m.moe_read_device_status() == 0
 
 
