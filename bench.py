@@ -567,7 +567,7 @@ def run_ours(args, wl):
         if routed:
             e2e = run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist)
         else:
-            e2e = run_e2e_grouped(torch, layer, dev, K, W, flops_step, world, dist)
+            e2e = run_e2e_grouped(torch, layer, inp, dev, K, W, flops_step, world, dist)
 
     if rank != 0:
         if world > 1:
@@ -848,32 +848,36 @@ def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
                        "api": "MoEExpertMLP.step with in-line copies"}}
 
 
-def run_e2e_grouped(torch, layer, dev, K, W, flops_step, world, dist):
+def run_e2e_grouped(torch, layer, inp, dev, K, W, flops_step, world, dist):
     """End to end for groups given directly (no router): every step copies
-    in, from pinned host memory, the expert-ordered rows x_perm and their
-    upstream gradient dY in the library's padded row layout plus the group
-    sizes, recomputes the group offsets on the device, runs the expert MLP
-    forward and backward, and copies the per-row results Y and dX_perm back
-    to pinned host memory.  The weight gradients stay on the device for the
-    optimizer.  Headline: GroupedHostStepPipeline (copies overlapped with
-    the neighbouring steps' kernels); also reported: the same copies issued
-    in line on one stream."""
+    in, from pinned host memory, the R expert-ordered rows x and their
+    upstream gradient dY and the group sizes, recomputes the group offsets
+    on the device, runs the expert MLP forward and backward, and copies the
+    R rows of Y and dX back to pinned host memory (group by group, between
+    the host's dense row order and the library's padded layout).  The
+    weight gradients stay on the device for the optimizer.  Headline:
+    GroupedHostStepPipeline (copies overlapped with the neighbouring steps'
+    kernels); also reported: the same copies issued in line on one stream."""
     from moe_expert_mlp_gb300.pipeline import GroupedHostStepPipeline
-    host_in = dict(x_perm=layer.x_perm.cpu().pin_memory(), dy=layer.dy.cpu().pin_memory(),
-                   counts=layer.counts.cpu().pin_memory())
-    outs = [dict(y=torch.empty(layer.y.shape, dtype=layer.y.dtype).pin_memory(),
-                 dx_perm=torch.empty(layer.dx_perm.shape, dtype=layer.dx_perm.dtype).pin_memory())
-            for _ in range(2)]
+    R, d = int(inp["group_sizes"].sum()), layer.d
+    host_in = dict(x=torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+                   dy=torch.from_numpy(inp["dout"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+                   counts=torch.from_numpy(inp["group_sizes"].astype(np.int32)).pin_memory())
+    outs = [dict(y=torch.empty((R, d), dtype=torch.bfloat16).pin_memory(),
+                 dx=torch.empty((R, d), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
     pipe = GroupedHostStepPipeline(layer, dev)
+    segs = pipe._segments(inp["group_sizes"])
     cnt_dev = torch.zeros_like(layer.counts)
 
     def serial():
-        layer.x_perm.copy_(host_in["x_perm"], non_blocking=True)
-        layer.dy.copy_(host_in["dy"], non_blocking=True)
+        for src, dst, m in segs:
+            layer.x_perm[dst:dst + m].copy_(host_in["x"][src:src + m], non_blocking=True)
+            layer.dy[dst:dst + m].copy_(host_in["dy"][src:src + m], non_blocking=True)
         cnt_dev.copy_(host_in["counts"], non_blocking=True)
         layer.grouped_step(counts=cnt_dev)
-        outs[0]["y"].copy_(layer.y, non_blocking=True)
-        outs[0]["dx_perm"].copy_(layer.dx_perm, non_blocking=True)
+        for src, dst, m in segs:
+            outs[0]["y"][src:src + m].copy_(layer.y[dst:dst + m], non_blocking=True)
+            outs[0]["dx"][src:src + m].copy_(layer.dx_perm[dst:dst + m], non_blocking=True)
 
     def timed(fn):
         torch.cuda.synchronize()
@@ -898,8 +902,8 @@ def run_e2e_grouped(torch, layer, dev, K, W, flops_step, world, dist):
     return {"value": round(job_rate(flops_step, K, world, ms) / 1e12, 2), "unit": "TFLOPS",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / K, 5),
-            "api": "GroupedHostStepPipeline (copies overlapped); inputs x_perm, dY, group sizes; "
-                   "results Y, dX_perm; weight gradients stay on the device",
+            "api": "GroupedHostStepPipeline (copies overlapped); inputs x, dY (real rows) and "
+                   "group sizes; results Y, dX (real rows); weight gradients stay on the device",
             "serial": {"value": round(job_rate(flops_step, K, world, ms_serial) / 1e12, 2),
                        "ms_per_step": round(ms_serial / K, 5),
                        "api": "MoEExpertMLP.grouped_step with in-line copies"}}

@@ -91,18 +91,22 @@ class HostStepPipeline:
 
 class GroupedHostStepPipeline:
     """Expert-MLP steps (groups given directly, no router) on host-resident
-    batches: each step copies in its expert-ordered rows x_perm and their
-    upstream gradient dY (both [capacity, d] in the library's padded row
-    layout, padding rows zero) and the group sizes, runs the forward and
-    backward of the expert MLP, and copies its per-row results Y and dX_perm
+    batches: each step copies in its expert-ordered rows x and their
+    upstream gradient dY (both [R, d] bf16, the R real rows only, group after
+    group) and the group sizes, runs the forward and backward of the expert
+    MLP, and copies its per-row results Y and dX (again the R real rows)
     back out.  The weight gradients stay in device memory, where the
     optimizer that consumes them runs.
 
-    The layer alternates between two sets of per-row device buffers (inputs
-    and results), so no device-side staging copy is needed: the inputs of
-    step i+1 are copied into the other set while step i computes, and the
-    results of step i go to the host while step i+1 computes; step i+2 waits
-    for both before it reuses the set.
+    Rows move group by group between the host's dense row order and the
+    library's padded device layout (each group starting at a multiple of 128
+    rows), so no padding row crosses the host link; padding rows of the
+    device buffers are kept zero (they are cleared whenever the group sizes,
+    and with them the layout, change).  The layer alternates between two
+    sets of per-row device buffers, so no device-side staging copy is
+    needed: the inputs of step i+1 are copied into the other set while step
+    i computes, and the results of step i go to the host while step i+1
+    computes; step i+2 waits for both before it reuses the set.
     """
 
     def __init__(self, layer, device=None):
@@ -113,17 +117,29 @@ class GroupedHostStepPipeline:
         self.sets = [dict(x_perm=layer.x_perm, dy=layer.dy, y=layer.y, dx_perm=layer.dx_perm)]
         self.sets.append({k: torch.zeros((cap, d), dtype=bf, device=dev)
                           for k in ("x_perm", "dy", "y", "dx_perm")})
+        self.layout = [None, None]               # group sizes each set was last laid out for
         self.counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(2)]
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
 
+    @staticmethod
+    def _segments(counts):
+        """(host row, device row, rows) of every non-empty group."""
+        segs, src, dst = [], 0, 0
+        for m in (int(c) for c in counts):
+            if m > 0:
+                segs.append((src, dst, m))
+            src += m
+            dst += (m + 127) // 128 * 128
+        return segs
+
     def run(self, host_inputs, host_outputs):
-        """host_inputs: list of dicts {x_perm, dy, counts} (pinned host
-        tensors: [capacity, d] bf16, [capacity, d] bf16, [E] int32), one per
-        step; host_outputs: list of dicts {y, dx_perm} (pinned host tensors
-        [capacity, d] bf16), one per step (entries may repeat).  Enqueues
-        every step on the current stream and returns; the caller
-        synchronises."""
+        """host_inputs: list of dicts {x, dy, counts} (x, dy: pinned host
+        tensors [R, d] bf16 in group order; counts: host int32 tensor [E]
+        with sum R), one per step; host_outputs: list of dicts {y, dx}
+        (pinned host tensors [R, d] bf16), one per step (entries may
+        repeat).  Enqueues every step on the current stream and returns; the
+        caller synchronises."""
         layer = self.layer
         comp = torch.cuda.current_stream()
         n = len(host_inputs)
@@ -134,16 +150,26 @@ class GroupedHostStepPipeline:
         out_copied = [torch.cuda.Event() for _ in range(2)]
         started = torch.cuda.Event()
         started.record(comp)
+        segs = [None] * n
 
         def copy_in(i):
             b = i % 2
+            hin = host_inputs[i]
+            key = tuple(int(c) for c in hin["counts"])
+            segs[i] = self._segments(key)
+            dev = self.sets[b]
             with torch.cuda.stream(self.h2d):
                 self.h2d.wait_event(started)
                 if i >= 2:                       # step i-2 was the set's last reader
                     self.h2d.wait_event(step_done[b])
-                self.sets[b]["x_perm"].copy_(host_inputs[i]["x_perm"], non_blocking=True)
-                self.sets[b]["dy"].copy_(host_inputs[i]["dy"], non_blocking=True)
-                self.counts[b].copy_(host_inputs[i]["counts"], non_blocking=True)
+                if self.layout[b] != key:        # new layout: padding rows back to zero
+                    dev["x_perm"].zero_()
+                    dev["dy"].zero_()
+                    self.layout[b] = key
+                for src, dst, m in segs[i]:
+                    dev["x_perm"][dst:dst + m].copy_(hin["x"][src:src + m], non_blocking=True)
+                    dev["dy"][dst:dst + m].copy_(hin["dy"][src:src + m], non_blocking=True)
+                self.counts[b].copy_(hin["counts"], non_blocking=True)
                 in_ready[b].record(self.h2d)
 
         copy_in(0)
@@ -160,8 +186,10 @@ class GroupedHostStepPipeline:
             step_done[b].record(comp)
             with torch.cuda.stream(self.d2h):
                 self.d2h.wait_event(step_done[b])
-                host_outputs[i]["y"].copy_(s["y"], non_blocking=True)
-                host_outputs[i]["dx_perm"].copy_(s["dx_perm"], non_blocking=True)
+                hout = host_outputs[i]
+                for src, dst, m in segs[i]:
+                    hout["y"][src:src + m].copy_(s["y"][dst:dst + m], non_blocking=True)
+                    hout["dx"][src:src + m].copy_(s["dx_perm"][dst:dst + m], non_blocking=True)
                 out_copied[b].record(self.d2h)
         comp.wait_event(out_copied[(n - 1) % 2])
         if n >= 2:
