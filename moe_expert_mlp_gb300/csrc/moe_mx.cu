@@ -52,16 +52,21 @@ __global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in
   }
 }
 
-// bf16 [batch][rows][cols] -> MXFP8 (rows, cols multiples of 32).  One CTA
-// (8 warps) per 128 x 128 tile: the tile is loaded coalesced into four
-// shared boxes of 128 rows x 32 columns (64-byte rows, 64-byte swizzle);
-// each warp quantizes 32 x 32 blocks rowwise (lane = row) or columnwise
-// (lane = column) into shared code tiles; the codes then leave as whole
-// 128-byte lines and, in the MMA scale layout, each tile's scales as one
-// 512-byte atom per direction.  Rowwise codes [batch][rows][cols];
-// columnwise codes transposed [batch][cols][rows].
+// bf16 [batch][rows][cols] -> MXFP8 (rows, cols multiples of 32).  A CTA
+// (8 warps) walks 128 x 128 tiles; each tile is loaded coalesced into four
+// shared boxes of 128 rows x 32 columns (64-byte rows, 64-byte swizzle) with
+// cp.async, double-buffered so that the next tile streams in while the
+// current one is quantized and stored; each warp quantizes 32 x 32 blocks
+// rowwise (lane = row) or columnwise (lane = column) into shared code
+// tiles; the codes then leave as whole 128-byte lines and, in the MMA scale
+// layout, each tile's scales as one 512-byte atom per direction.  Rowwise
+// codes [batch][rows][cols]; columnwise codes transposed [batch][cols][rows].
+// Rows at or past *row_limit (when given; in every batch entry) are not
+// visited.
 constexpr int kQT = 128;                       // tile edge
-constexpr int kQuantSmem = 4 * 8192 + 2 * kQT * kQT + 2 * 512;
+constexpr int kQThreads = 256;                 // 8 warps, two CTAs per SM
+constexpr int kQIn = 4 * 8192;                 // one bf16 input tile (four boxes)
+constexpr int kQuantSmem = 2 * kQIn + 2 * kQT * kQT + 2 * 512;
 
 __device__ __forceinline__ void quant_block_to_smem(const float (&v)[32], uint8_t* code_row,
                                                     int line, int c32, uint8_t& scale) {
@@ -77,46 +82,78 @@ __device__ __forceinline__ void quant_block_to_smem(const float (&v)[32], uint8_
   }
 }
 
-__global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restrict__ in,
+struct QuantTile {
+  long long b, r0, c0;
+  int nr, nc;
+};
+
+__device__ __forceinline__ QuantTile quant_tile(long long t, long long rtn, long long ctn,
+                                                long long rows, long long cols) {
+  QuantTile q;
+  q.b = t / (rtn * ctn);
+  const long long rem = t - q.b * rtn * ctn;
+  q.r0 = (rem / ctn) * kQT;
+  q.c0 = (rem % ctn) * kQT;
+  q.nr = static_cast<int>(min(static_cast<long long>(kQT), rows - q.r0));   // multiples of 32
+  q.nc = static_cast<int>(min(static_cast<long long>(kQT), cols - q.c0));
+  return q;
+}
+
+// Asynchronous load of one tile into `boxes` (thread -> 16-byte chunks; the
+// chunks outside the tensor are zero-filled).
+__device__ __forceinline__ void quant_load_async(const __nv_bfloat16* __restrict__ in,
+                                                 const QuantTile& q, long long rows,
+                                                 long long cols, uint8_t* boxes, int tid) {
+  const uint32_t base = static_cast<uint32_t>(__cvta_generic_to_shared(boxes));
+  for (int i = tid; i < kQT * 16; i += kQThreads) {
+    const int r = i >> 4, ch = i & 15;
+    const bool ok = r < q.nr && ch * 8 < q.nc;
+    const __nv_bfloat16* src = ok ? in + (q.b * rows + q.r0 + r) * cols + q.c0 + ch * 8 : in;
+    cp_async16_zfill(base + (ch >> 2) * 8192 + r * 64 + (((ch & 3) ^ ((r >> 1) & 3)) << 4),
+                     src, ok);
+  }
+}
+
+__global__ void __launch_bounds__(kQThreads, 2) k_quant_bf16(const __nv_bfloat16* __restrict__ in,
                                                     long long batch, long long rows,
                                                     long long cols, uint8_t* q, uint8_t* s,
                                                     uint8_t* qt, uint8_t* st, int mma_layout,
                                                     const int32_t* row_limit) {
   extern __shared__ __align__(1024) uint8_t qsm[];
-  uint8_t* boxes = qsm;                              // 4 x [128][64 B]
-  uint8_t* code_r = qsm + 4 * 8192;                  // [128 rows][128 B]
+  uint8_t* in_buf = qsm;                             // 2 x (4 x [128][64 B])
+  uint8_t* code_r = qsm + 2 * kQIn;                  // [128 rows][128 B]
   uint8_t* code_c = code_r + kQT * kQT;              // [128 cols][128 B]
   uint8_t* atom_r = code_c + kQT * kQT;              // scale atoms (MMA layout)
   uint8_t* atom_c = atom_r + 512;
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  const long long rtn = (rows + kQT - 1) / kQT, ctn = (cols + kQT - 1) / kQT;
+  const long long rlim = row_limit ? min(rows, static_cast<long long>(__ldg(row_limit))) : rows;
+  const long long rtn = (rlim + kQT - 1) / kQT, ctn = (cols + kQT - 1) / kQT;
   const long long ntiles = batch * rtn * ctn;
   const long long s_bytes = mma_layout ? (cols + 127) / 128 * sf_row_atoms(rows) * 512
                                        : rows * cols / 32;
   const long long st_bytes = mma_layout ? (rows + 127) / 128 * sf_row_atoms(cols) * 512
                                         : rows * cols / 32;
-  const long long rlim = row_limit ? __ldg(row_limit) : rows;   // rows past it are skipped
-  for (long long t = blockIdx.x; t < ntiles; t += gridDim.x) {
-    const long long b = t / (rtn * ctn);
-    const long long rem = t - b * rtn * ctn;
-    const long long r0 = (rem / ctn) * kQT, c0 = (rem % ctn) * kQT;
-    if (r0 >= rlim) continue;                        // uniform across the CTA
-    const int nr = static_cast<int>(min(static_cast<long long>(kQT), rows - r0));   // multiples of 32
-    const int nc = static_cast<int>(min(static_cast<long long>(kQT), cols - c0));
-    __syncthreads();                                 // previous tile fully stored
-    // load: thread -> 16-byte chunk (row i / 16, chunk i % 16 of 256 bytes)
-    for (int i = tid; i < kQT * 16; i += 256) {
-      const int r = i >> 4, ch = i & 15;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < nr && ch * 8 < nc)
-        v = __ldg(reinterpret_cast<const uint4*>(in + (b * rows + r0 + r) * cols + c0) + ch);
-      *reinterpret_cast<uint4*>(boxes + (ch >> 2) * 8192 + r * 64 +
-                                (((ch & 3) ^ ((r >> 1) & 3)) << 4)) = v;
-    }
-    for (int i = tid; i < 1024; i += 256) atom_r[i] = 0;   // both atoms
-    __syncthreads();
+  for (int i = tid; i < 1024; i += kQThreads) atom_r[i] = 0;     // both atoms
+  long long t = blockIdx.x;
+  if (t < ntiles) quant_load_async(in, quant_tile(t, rtn, ctn, rows, cols), rows, cols, in_buf, tid);
+  cp_async_commit();
+  for (int it = 0; t < ntiles; t += gridDim.x, ++it) {
+    const QuantTile qt_ = quant_tile(t, rtn, ctn, rows, cols);
+    const long long b = qt_.b, r0 = qt_.r0, c0 = qt_.c0;
+    const int nr = qt_.nr, nc = qt_.nc;
+    // the next tile streams into the other buffer (its last reader, the
+    // previous iteration's quantization, finished before that iteration's
+    // second barrier)
+    const long long tn = t + gridDim.x;
+    if (tn < ntiles)
+      quant_load_async(in, quant_tile(tn, rtn, ctn, rows, cols), rows, cols,
+                       in_buf + ((it + 1) & 1) * kQIn, tid);
+    cp_async_commit();
+    cp_async_wait<1>();                              // this thread's chunks of tile t landed
+    __syncthreads();                                 // all of tile t; previous tile stored
+    const uint8_t* boxes = in_buf + (it & 1) * kQIn;
     // quantize: 16 blocks x {rowwise, columnwise}; warp w takes items w + 8k
-    for (int item = wid; item < 32; item += 8) {
+    for (int item = wid; item < 32; item += kQThreads / 32) {
       const int colwise = item >> 4, blk = item & 15;
       const int bi = blk >> 2, bj = blk & 3;         // block row / column in the tile
       if (bi * 32 >= nr || bj * 32 >= nc) continue;  // warp-uniform
@@ -161,7 +198,7 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restr
     }
     __syncthreads();
     // store codes as whole lines: thread -> 16-byte chunk (line i / 8)
-    for (int i = tid; i < kQT * 8; i += 256) {
+    for (int i = tid; i < kQT * 8; i += kQThreads) {
       const int line = i >> 3, ch = i & 7;
       const int sch = ch ^ (line & 7);
       if (q && line < nr && ch * 16 < nc)
@@ -180,7 +217,10 @@ __global__ void __launch_bounds__(256) k_quant_bf16(const __nv_bfloat16* __restr
         reinterpret_cast<uint4*>(st + b * st_bytes + sf_mma_offset(c0, r0 / 32, sf_row_atoms(cols)))[k] =
             reinterpret_cast<const uint4*>(atom_c)[k];
     }
+    __syncthreads();                                 // code tiles and atoms free again
+    for (int i = tid; i < 1024; i += kQThreads) atom_r[i] = 0;   // both atoms, for the next tile
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace
@@ -195,8 +235,8 @@ cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows
                                          kQuantSmem);
   if (err != cudaSuccess) return err;
   long long grid = ntiles;
-  if (grid > static_cast<long long>(num_sms) * 3) grid = static_cast<long long>(num_sms) * 3;
-  k_quant_bf16<<<static_cast<int>(grid), 256, kQuantSmem, stream>>>(
+  if (grid > static_cast<long long>(num_sms) * 2) grid = static_cast<long long>(num_sms) * 2;
+  k_quant_bf16<<<static_cast<int>(grid), kQThreads, kQuantSmem, stream>>>(
       static_cast<const __nv_bfloat16*>(in), batch, rows, cols, q, s, qt, st, mma_layout,
       row_limit);
   return cudaGetLastError();
