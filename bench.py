@@ -552,7 +552,7 @@ def run_ours(args, wl):
 
     # fused vs unfused expert MLP (same kernels, activation as its own pass)
     fusion = None
-    if not args.no_fusion and not mx:
+    if not args.no_fusion and args.dtype != "nvfp4" and wl.gated:
         fusion = measure_fusion(torch, layer, K)
     overlap = None
     if args.overlap and not mx:
@@ -647,10 +647,15 @@ def run_ours(args, wl):
 
 
 def measure_fusion(torch, layer, K):
-    """Forward and backward of the expert MLP, fused epilogues vs the unfused
-    path (plain GEMMs + separate GLU / dGLU passes), CUDA events, K reps each
+    """Forward and backward of the expert MLP, fused epilogues against the
+    unfused arrangement the pages measure their kernels against: the group
+    sizes read back to the host each pass (a device-to-host copy and a
+    synchronisation), plain grouped GEMMs, and the activation (GLU / dGLU)
+    and, on the MXFP8 path, the quantization of its output (rowwise and
+    transposed) as separate memory-bound passes.  CUDA events, K reps each
     after 3 warm-ups.  The pages report up to 1.3x forward and 2.1x backward
-    for their fused kernels against an unfused path."""
+    for their fused kernels.  Also the backward with activation recompute (H
+    regenerated from the forward's operands instead of read back)."""
     def timed(fn):
         for _ in range(3):
             fn()
@@ -667,23 +672,33 @@ def measure_fusion(torch, layer, K):
     f_unf = timed(layer.mlp_forward_unfused)
     b_fused = timed(layer.mlp_backward)
     b_unf = timed(layer.mlp_backward_unfused)
-    # activation recompute: the backward regenerates H in its workspace
     from moe_expert_mlp_gb300 import _lib as L
-    desc_r = type(layer.desc).from_buffer_copy(layer.desc)
-    desc_r.recompute_h = 1
-    ws_r = torch.zeros(L.moe_workspace_size(desc_r), dtype=torch.uint8, device=layer.ws.device)
-    b_rec = timed(lambda: L.moe_mlp_bwd(
-        desc_r, layer.dy, layer.x_perm, None, layer.a, layer.counts, layer.padded_offsets,
-        layer.w1p, layer.w2, layer.dh, layer.dx_perm, layer.dw1p, layer.db1p, layer.dw2,
-        layer.db2, ws_r, b1p=layer.b1p))
-    del ws_r
+    if layer.mx:
+        # the MXFP8 backward regenerating H (moe_fc1_recompute_h_mx) first
+        layer.recompute_h = True
+        b_rec = timed(layer.mlp_backward)
+        layer.recompute_h = False
+    else:
+        # the bf16 backward regenerating H in its workspace
+        desc_r = type(layer.desc).from_buffer_copy(layer.desc)
+        desc_r.recompute_h = 1
+        ws_r = torch.zeros(L.moe_workspace_size(desc_r), dtype=torch.uint8,
+                           device=layer.ws.device)
+        b_rec = timed(lambda: L.moe_mlp_bwd(
+            desc_r, layer.dy, layer.x_perm, None, layer.a, layer.counts, layer.padded_offsets,
+            layer.w1p, layer.w2, layer.dh, layer.dx_perm, layer.dw1p, layer.db1p, layer.dw2,
+            layer.db2, ws_r, b1p=layer.b1p))
+        del ws_r
     layer.mlp_forward()                      # leave the fused results in place
     layer.mlp_backward()
+    what = ("host-synchronised group sizes, plain grouped GEMMs, GLU / dGLU as separate "
+            "passes" + (", MXFP8 quantize + transpose of A / dH as separate passes"
+                        if layer.mx else ""))
     return {"fwd_fused_ms": round(f_fused, 4), "fwd_unfused_ms": round(f_unf, 4),
             "fwd_speedup": round(f_unf / f_fused, 3), "bwd_fused_ms": round(b_fused, 4),
             "bwd_unfused_ms": round(b_unf, 4), "bwd_speedup": round(b_unf / b_fused, 3),
-            "bwd_recompute_h_ms": round(b_rec, 4),
-            "unfused": "same grouped GEMMs with plain epilogues; GLU / dGLU as separate passes"}
+            "bwd_recompute_h_ms": round(b_rec, 4), "unfused": what,
+            "pages_reported": "up to 1.3x forward, 2.1x backward (their fused vs unfused)"}
 
 
 def measure_router(torch, layer, x, logits, bias, reps=20):

@@ -613,6 +613,36 @@ moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
                             const moe_mx_out_t* dh_nv, void* dx_perm, void* dw1p, void* db1p,
                             void* dw2, void* db2, cudaStream_t stream);
 
+/* The unfused MXFP8 arrangement the fused epilogues replace ([FK]
+ * "Overcoming training bottlenecks in the MoE block": activation and
+ * quantization as separate memory-bound kernels; "From kernel-level gains
+ * to end-to-end pretraining speedups" measures the fused kernels against
+ * it).  Each call runs three kernels one after another:
+ *   moe_fc1_glu_fwd_mx_unfused:    H = X W1p^T (+b1) as a plain grouped GEMM
+ *                                  on the MXFP8 operands (h, bf16 [capacity,
+ *                                  2F_pad], packed), then A = GLU(H) from the
+ *                                  stored bf16 H (a, bf16 [capacity, F]),
+ *                                  then MXFP8 quantization of A rowwise and
+ *                                  transposed into a_mx (MMA scale layout).
+ *   moe_fc2_dgrad_dglu_mx_unfused: dA = dY W2 as a plain grouped GEMM on the
+ *                                  MXFP8 operands (da, bf16 [capacity, F],
+ *                                  caller scratch), then dH = dGLU(dA, H)
+ *                                  (dh, bf16, packed), then MXFP8 quantization
+ *                                  of dH rowwise and transposed into dh_mx.
+ * GLU activations only (MOE_ERR_UNSUPPORTED for MOE_ACT_SRELU).  A is
+ * computed from the bf16-rounded H here (the fused epilogue uses the fp32
+ * accumulator), so results agree with the fused calls to bf16 rounding, not
+ * bit for bit. */
+moe_status_t moe_fc1_glu_fwd_mx_unfused(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                        const int32_t* counts, const int32_t* padded_offsets,
+                                        const moe_mx_weights_t* w, const void* b1p, void* h,
+                                        void* a, const moe_mx_out_t* a_mx, cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu_mx_unfused(const moe_mlp_desc_t* desc,
+                                           const moe_mx_out_t* dy_mx, const void* h,
+                                           const int32_t* counts, const int32_t* padded_offsets,
+                                           const moe_mx_weights_t* w, void* da, void* dh,
+                                           const moe_mx_out_t* dh_mx, cudaStream_t stream);
+
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed
  * pool, or a runtime that allows no allocation after start-up).  The pages

@@ -39,7 +39,8 @@ EXPORTS = (
     "moe_quantize_nvfp4_bf16", "moe_quantize_act_nvfp4", "moe_quantize_weights_nvfp4",
     "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
     "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
-    "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv",
+    "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv", "moe_fc1_glu_fwd_mx_unfused",
+    "moe_fc2_dgrad_dglu_mx_unfused",
 )
 
 
@@ -183,6 +184,8 @@ def lib():
             "moe_fc1_wgrad_nv": (ctypes.c_int, [D] + [P] * 6),
             "moe_mlp_fwd_nv": (ctypes.c_int, [D] + [P] * 12),
             "moe_fc1_recompute_h_mx": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc1_glu_fwd_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_dgrad_dglu_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc1_recompute_h_nv": (ctypes.c_int, [D] + [P] * 7),
             "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
         }
@@ -517,6 +520,22 @@ def moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, str
     _check(lib().moe_fc1_recompute_h_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
                                         _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h),
                                         _stream(stream)))
+
+
+def moe_fc1_glu_fwd_mx_unfused(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, a, a_mx,
+                               stream=None):
+    """FC1 plain GEMM, GLU pass, MXFP8 quantize pass (see include/moe.h)."""
+    _check(lib().moe_fc1_glu_fwd_mx_unfused(ctypes.byref(desc), _mx(x_mx), _p(counts),
+                                            _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h), _p(a),
+                                            _mx(a_mx), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_mx_unfused(desc, dy_mx, h, counts, padded_offsets, w_mx, da, dh, dh_mx,
+                                  stream=None):
+    """FC2 dgrad plain GEMM, dGLU pass, MXFP8 quantize pass (see include/moe.h)."""
+    _check(lib().moe_fc2_dgrad_dglu_mx_unfused(ctypes.byref(desc), _mx(dy_mx), _p(h), _p(counts),
+                                               _p(padded_offsets), _mxw(w_mx), _p(da), _p(dh),
+                                               _mx(dh_mx), _stream(stream)))
 
 
 def moe_fc1_recompute_h_nv(desc, x_nv, counts, padded_offsets, w_nv, b1p, h, stream=None):

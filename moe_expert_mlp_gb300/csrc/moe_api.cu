@@ -1150,6 +1150,74 @@ moe_status_t moe_fc1_recompute_h_mx(const moe_mlp_desc_t* desc, const moe_mx_out
   return cuda_status(launch_grouped_gemm_mx(kFc2, g, grid_for(di, desc), stream));
 }
 
+moe_status_t moe_fc1_glu_fwd_mx_unfused(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
+                                        const int32_t* counts, const int32_t* padded_offsets,
+                                        const moe_mx_weights_t* w, const void* b1p, void* h,
+                                        void* a, const moe_mx_out_t* a_mx, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !h || !a) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!mx_ok(x_mx, true, false) || !mx_ok(a_mx, true, true)) return MOE_ERR_NULL;
+  // 1. plain grouped GEMM H = X W1p^T (+b1) on the MXFP8 operands
+  if ((st = moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w, b1p, h, stream)) !=
+      MOE_OK)
+    return st;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  // 2. the GLU as its own pass over the stored bf16 H
+  cudaError_t e = launch_glu_rows(h, counts, padded_offsets, desc->E, desc->F,
+                                  fc1_pad(desc->F), a, desc->act, desc->alpha, desc->limit,
+                                  desc->linear_offset, desc->out_scale, di->sms, stream);
+  // 3. MXFP8 quantization of A, rowwise and transposed, as its own pass
+  if (e == cudaSuccess)
+    e = launch_quant_bf16_mx(a, 1, desc->capacity, desc->F, a_mx->q, a_mx->scale, a_mx->qt,
+                             a_mx->scale_t, 1, padded_offsets + desc->E, di->sms, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_fc2_dgrad_dglu_mx_unfused(const moe_mlp_desc_t* desc,
+                                           const moe_mx_out_t* dy_mx, const void* h,
+                                           const int32_t* counts, const int32_t* padded_offsets,
+                                           const moe_mx_weights_t* w, void* da, void* dh,
+                                           const moe_mx_out_t* dh_mx, cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
+  if (!h || !counts || !padded_offsets || !mx_weights_ok(w) || !da || !dh) return MOE_ERR_NULL;
+  if (!mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true)) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // 1. plain grouped GEMM dA = dY W2 on the MXFP8 operands (dY codes [cap, d]
+  //    x W2^T codes [E, F, d]): the plain-output kernel, dA [cap, F] bf16
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) || !encode_out(&g.tma_out0, da, F, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = da;
+  g.ld0 = F;
+  set_scales(g, dy_mx->scale, cap, w->w2t_s, F, sf_bytes(F, d));
+  cudaError_t e = launch_grouped_gemm_mx(kFc2, g, grid_for(di, desc), stream);
+  // 2. the dGLU as its own pass over dA and the stored bf16 H
+  if (e == cudaSuccess)
+    e = launch_dglu_rows(da, h, counts, padded_offsets, desc->E, desc->F, fc1_pad(desc->F), dh,
+                         desc->act, desc->alpha, desc->limit, desc->linear_offset,
+                         desc->out_scale, di->sms, stream);
+  // 3. MXFP8 quantization of dH, rowwise and transposed, as its own pass
+  if (e == cudaSuccess)
+    e = launch_quant_bf16_mx(dh, 1, desc->capacity, static_cast<long long>(W1), dh_mx->q,
+                             dh_mx->scale, dh_mx->qt, dh_mx->scale_t, 1,
+                             padded_offsets + desc->E, di->sms, stream);
+  return cuda_status(e);
+}
+
 moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,
                             const int32_t* counts, const int32_t* padded_offsets,
                             const moe_mx_weights_t* w, const void* b1p, const void* b2, void* h,

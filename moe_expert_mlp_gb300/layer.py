@@ -321,10 +321,29 @@ class MoEExpertMLP:
                 L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2, stream)
 
     # ---------------------------------------------------- unfused comparison
+    # The arrangement the fused kernels replace: the group sizes read back to
+    # the host each pass (one device-to-host copy and a synchronisation, as a
+    # host-driven grouped GEMM needs them to size its launches), plain
+    # grouped GEMMs, and the activation -- and on the MXFP8 path the
+    # quantization of its output -- as separate memory-bound passes.
+    def _host_sync_counts(self):
+        self.host_counts = self.counts.cpu()
+
     def mlp_forward_unfused(self, stream=None, timer=None):
-        """FC1 plain GEMM + separate GLU pass, then FC2 (the unfused path the
-        fused epilogue replaces)."""
+        """FC1 plain GEMM + separate GLU pass (+ separate MXFP8 quantization
+        of A), then FC2."""
         c, po = self.counts, self.padded_offsets
+        with self._t(timer, "host_sync"):
+            self._host_sync_counts()
+        if self.mx:
+            with self._t(timer, "quant_x"):
+                L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
+            with self._t(timer, "fc1_glu_fwd"):
+                L.moe_fc1_glu_fwd_mx_unfused(self.desc, self.x_mx, c, po, self.w_mx, self.b1p,
+                                             self.h, self.a, self.a_mx, stream)
+            with self._t(timer, "fc2_fwd"):
+                L.moe_fc2_fwd_mx(self.desc, self.a_mx, c, po, self.w_mx, self.b2, self.y, stream)
+            return
         with self._t(timer, "fc1_glu_fwd"):
             L.moe_fc1_glu_fwd_unfused(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h,
                                       self.a, stream)
@@ -332,20 +351,36 @@ class MoEExpertMLP:
             L.moe_fc2_fwd(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream)
 
     def mlp_backward_unfused(self, stream=None, timer=None):
-        """FC2 dgrad plain GEMM + separate dGLU pass, then the rest as fused."""
+        """FC2 dgrad plain GEMM + separate dGLU pass (+ separate MXFP8
+        quantization of dH), then the weight gradients and FC1 dgrad."""
         if getattr(self, "da", None) is None:
             self.da = torch.zeros((self.capacity, self.F), dtype=torch.bfloat16,
                                   device=self.w2.device)
         c, po = self.counts, self.padded_offsets
-        with self._t(timer, "fc2_dgrad_dglu"):
-            L.moe_fc2_dgrad_dglu_unfused(self.desc, self.dy, self.h, c, po, self.w2, self.da,
-                                         self.dh, stream)
-        with self._t(timer, "fc2_wgrad"):
-            L.moe_fc2_wgrad(self.desc, self.dy, self.a, c, po, self.dw2, stream)
-        with self._t(timer, "fc1_dgrad"):
-            L.moe_fc1_dgrad(self.desc, self.dh, c, po, self.w1p, self.dx_perm, stream)
-        with self._t(timer, "fc1_wgrad"):
-            L.moe_fc1_wgrad(self.desc, self.dh, self.x_perm, c, po, self.dw1p, stream)
+        with self._t(timer, "host_sync"):
+            self._host_sync_counts()
+        if self.mx:
+            with self._t(timer, "quant_dy"):
+                L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
+            with self._t(timer, "fc2_dgrad_dglu"):
+                L.moe_fc2_dgrad_dglu_mx_unfused(self.desc, self.dy_mx, self.h, c, po, self.w_mx,
+                                                self.da, self.dh, self.dh_mx, stream)
+            with self._t(timer, "fc2_wgrad"):
+                L.moe_fc2_wgrad_mx(self.desc, self.dy_mx, self.a_mx, c, po, self.dw2, stream)
+            with self._t(timer, "fc1_dgrad"):
+                L.moe_fc1_dgrad_mx(self.desc, self.dh_mx, c, po, self.w_mx, self.dx_perm, stream)
+            with self._t(timer, "fc1_wgrad"):
+                L.moe_fc1_wgrad_mx(self.desc, self.dh_mx, self.x_mx, c, po, self.dw1p, stream)
+        else:
+            with self._t(timer, "fc2_dgrad_dglu"):
+                L.moe_fc2_dgrad_dglu_unfused(self.desc, self.dy, self.h, c, po, self.w2, self.da,
+                                             self.dh, stream)
+            with self._t(timer, "fc2_wgrad"):
+                L.moe_fc2_wgrad(self.desc, self.dy, self.a, c, po, self.dw2, stream)
+            with self._t(timer, "fc1_dgrad"):
+                L.moe_fc1_dgrad(self.desc, self.dh, c, po, self.w1p, self.dx_perm, stream)
+            with self._t(timer, "fc1_wgrad"):
+                L.moe_fc1_wgrad(self.desc, self.dh, self.x_perm, c, po, self.dw1p, stream)
         if self.has_b1 or self.has_b2:
             with self._t(timer, "bias_grads"):
                 L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2, stream)

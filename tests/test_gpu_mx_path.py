@@ -200,3 +200,39 @@ def test_mxfp8_activation_recompute_matches_stored_h():
         a, b = getattr(ref, name), getattr(rec, name)
         assert torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
                            b.view(torch.int16) if b.dtype == torch.bfloat16 else b), name
+
+
+def test_unfused_mxfp8_arrangement_matches_oracle():
+    """The unfused MXFP8 arrangement (host-read group sizes, plain GEMMs, GLU /
+    dGLU and MXFP8 quantization as separate passes) against the MXFP8 oracle.
+    H and A meet the bf16 bound; A is computed from the stored bf16 H here
+    (the oracle and the fused epilogue use the unrounded accumulator), so
+    more of the re-quantized A / dH codes differ from the oracle's and the
+    outputs downstream are held to the MXFP8 path's 6e-2 tolerance (measured
+    about 3.5e-2), plus the format bound against the unquantized oracle."""
+    wl = scaled(WORKLOADS["dsv3_r16384_e32"], R=700, E=9, d=256, F=192, zipf_empty=3)
+    inp = make_inputs(wl)
+    layer, ref = H.run_both_direct_mx(wl, inp)
+    _, plain = H.run_both_direct(wl, inp)
+    fused = {n: getattr(layer, n).clone() for n in ("y", "dx_perm", "dw1p", "dw2")}
+    layer.mlp_forward_unfused()
+    layer.mlp_backward_unfused()
+    torch.cuda.synchronize()
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    assert torch.equal(layer.host_counts, layer.counts.cpu())
+    R_pad = int(ref["padded_offsets"][-1])
+    h_log, _ = H.packed_to_logical_cols(H.to_np(layer.h)[:R_pad], wl.F)
+    H.assert_close("unfused/H", h_log, ref["H"])
+    H.assert_close("unfused/A", H.to_np(layer.a)[:R_pad], ref["A"])
+    outs = [("Y", H.to_np(layer.y)[:R_pad], "Y", fused["y"][:R_pad]),
+            ("dX_perm", H.to_np(layer.dx_perm)[:R_pad], "dX_perm", fused["dx_perm"][:R_pad]),
+            ("dW2", H.to_np(layer.dw2), "dW2", fused["dw2"]),
+            ("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), "dW1",
+             layer.unpack_fc1(fused["dw1p"], wl.d))]
+    for name, got, key, fz in outs:
+        H.assert_close("unfused/" + name, got, ref[key], rel=H.TOL_MX, abs_=0.0)
+        fro = np.linalg.norm(got - plain[key]) / np.linalg.norm(plain[key])
+        assert fro <= H.TOL_MX_FRO, (name, fro)
+        # and close to the fused path's own results
+        H.assert_close("unfused vs fused " + name, got, H.to_np(fz), rel=H.TOL_MX, abs_=0.0)
