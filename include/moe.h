@@ -123,9 +123,10 @@ typedef struct {
                            kernel-level gains...": configurable margin) */
   int32_t capacity;     /* rows allocated in every per-row buffer */
   int32_t recompute_h;  /* 1: the forward may skip storing H (h = NULL) and
-                           moe_mlp_bwd regenerates it in the workspace ([FK]
-                           "Next steps": activation recompute); the workspace
-                           then includes capacity*2*F_pad bf16 */
+                           moe_mlp_bwd recomputes it ([FK] "Next steps":
+                           activation recompute): inside the dGLU kernel for
+                           the GLU activations, into the workspace (which
+                           then includes capacity*F bf16) for MOE_ACT_SRELU */
 } moe_mlp_desc_t;
 
 /* Optional MXFP8 and NVFP4-preparation outputs of a GEMM epilogue ([FK]
@@ -345,9 +346,11 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
  * dw1p [E,2F_pad,d] = dh^T x_perm (packed); db1p [E,2F_pad] and db2 [E,d]
  * (NULL when the bias is absent).  Experts with no rows get zero gradients.
  * dh_mx (NULL = none): MXFP8 / amax outputs of dH (width 2*F_pad, packed).
- * h = NULL: H is recomputed from x_perm, w1p and b1p (plain FC1 grouped GEMM
- * + bias; b1p is used only then) into the workspace first; needs desc->recompute_h = 1 and a
- * workspace of moe_workspace_size() bytes. */
+ * h = NULL (needs desc->recompute_h = 1): H is recomputed from x_perm, w1p
+ * and b1p (b1p is used only then) -- for the GLU activations inside the
+ * dGLU kernel (moe_fc2_dgrad_dglu_recompute: H never reaches HBM), for
+ * MOE_ACT_SRELU by a plain FC1 grouped GEMM into the workspace first (a
+ * workspace of moe_workspace_size() bytes). */
 moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
                          const void* h, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w1p, const void* b1p,
@@ -612,6 +615,34 @@ moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
                             const int32_t* padded_offsets, const moe_nv_weights_t* w, void* dh,
                             const moe_mx_out_t* dh_nv, void* dx_perm, void* dw1p, void* db1p,
                             void* dw2, void* db2, cudaStream_t stream);
+
+/* FC2 dgrad + dGLU with activation recompute inside the kernel ([FK] "Next
+ * steps" names activation recompute as future work): for each tile of 128
+ * rows x 128 GLU features the kernel computes H = X W1p^T (+b1) for the
+ * tile's packed block (128 gate + 128 linear columns) and dA = dY W2, both
+ * over K = d, into tensor memory, rounds H to bf16 (as the stored H is) and
+ * applies the dGLU from there: H never reaches HBM, and the forward need not
+ * keep it (moe_fc1_glu_fwd with h = NULL when desc->recompute_h).  dh as in
+ * moe_fc2_dgrad_dglu (bf16, packed), plus the optional MXFP8 / amax outputs
+ * of dh_mx.  H's MMAs are the forward's, so dH equals the stored-H path's.
+ * GLU activations only (MOE_ERR_UNSUPPORTED for MOE_ACT_SRELU).
+ *   moe_fc2_dgrad_dglu_recompute:    bf16 operands x_perm, dy, w1p, w2.
+ *   moe_fc2_dgrad_dglu_recompute_mx: the forward's MXFP8 x_mx (rowwise),
+ *                                    dY's dy_mx (rowwise), the weights' w1
+ *                                    and w2t copies; dh_mx receives dH's
+ *                                    MXFP8 rowwise and transposed copies. */
+moe_status_t moe_fc2_dgrad_dglu_recompute(const moe_mlp_desc_t* desc, const void* x_perm,
+                                          const void* dy, const int32_t* counts,
+                                          const int32_t* padded_offsets, const void* w1p,
+                                          const void* b1p, const void* w2, void* dh,
+                                          const moe_mx_out_t* dh_mx, cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu_recompute_mx(const moe_mlp_desc_t* desc,
+                                             const moe_mx_out_t* x_mx,
+                                             const moe_mx_out_t* dy_mx, const int32_t* counts,
+                                             const int32_t* padded_offsets,
+                                             const moe_mx_weights_t* w, const void* b1p,
+                                             void* dh, const moe_mx_out_t* dh_mx,
+                                             cudaStream_t stream);
 
 /* The unfused MXFP8 arrangement the fused epilogues replace ([FK]
  * "Overcoming training bottlenecks in the MoE block": activation and

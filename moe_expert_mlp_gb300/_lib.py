@@ -40,7 +40,8 @@ EXPORTS = (
     "moe_fc1_glu_fwd_nv", "moe_fc2_fwd_nv", "moe_fc2_dgrad_dglu_nv", "moe_fc2_wgrad_nv",
     "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
     "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv", "moe_fc1_glu_fwd_mx_unfused",
-    "moe_fc2_dgrad_dglu_mx_unfused",
+    "moe_fc2_dgrad_dglu_mx_unfused", "moe_fc2_dgrad_dglu_recompute",
+    "moe_fc2_dgrad_dglu_recompute_mx",
 )
 
 
@@ -185,6 +186,8 @@ def lib():
             "moe_mlp_fwd_nv": (ctypes.c_int, [D] + [P] * 12),
             "moe_fc1_recompute_h_mx": (ctypes.c_int, [D] + [P] * 7),
             "moe_fc1_glu_fwd_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_dgrad_dglu_recompute": (ctypes.c_int, [D] + [P] * 10),
+            "moe_fc2_dgrad_dglu_recompute_mx": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc2_dgrad_dglu_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc1_recompute_h_nv": (ctypes.c_int, [D] + [P] * 7),
             "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
@@ -520,6 +523,22 @@ def moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, str
     _check(lib().moe_fc1_recompute_h_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
                                         _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h),
                                         _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_recompute(desc, x_perm, dy, counts, padded_offsets, w1p, b1p, w2, dh,
+                                 stream=None, mx=None):
+    """FC2 dgrad + dGLU with H recomputed inside the kernel (see include/moe.h)."""
+    _check(lib().moe_fc2_dgrad_dglu_recompute(ctypes.byref(desc), _p(x_perm), _p(dy), _p(counts),
+                                              _p(padded_offsets), _p(w1p), _p(b1p), _p(w2),
+                                              _p(dh), _mx(mx), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_recompute_mx(desc, x_mx, dy_mx, counts, padded_offsets, w_mx, b1p, dh,
+                                    dh_mx, stream=None):
+    """The same on the MXFP8 operands (see include/moe.h)."""
+    _check(lib().moe_fc2_dgrad_dglu_recompute_mx(ctypes.byref(desc), _mx(x_mx), _mx(dy_mx),
+                                                 _p(counts), _p(padded_offsets), _mxw(w_mx),
+                                                 _p(b1p), _p(dh), _mx(dh_mx), _stream(stream)))
 
 
 def moe_fc1_glu_fwd_mx_unfused(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, a, a_mx,

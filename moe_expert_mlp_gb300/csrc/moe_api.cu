@@ -238,7 +238,7 @@ moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes) {
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   *bytes = route_ws_bytes(desc) + 256;
-  if (desc->recompute_h)
+  if (desc->recompute_h && desc->act == MOE_ACT_SRELU)   // H regenerated into the workspace
     *bytes += static_cast<size_t>(desc->capacity) * fc1_width(desc->act, desc->F) * 2 + 256;
   return MOE_OK;
 }
@@ -529,6 +529,43 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
                                          grid_for(di, desc), stream));
 }
 
+moe_status_t moe_fc2_dgrad_dglu_recompute(const moe_mlp_desc_t* desc, const void* x_perm,
+                                          const void* dy, const int32_t* counts,
+                                          const int32_t* padded_offsets, const void* w1p,
+                                          const void* b1p, const void* w2, void* dh,
+                                          const moe_mx_out_t* dh_mx, cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, false);
+  if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU activations
+  if (!x_perm || !dy || !counts || !padded_offsets || !w1p || !w2 || !dh) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // H = X W1p^T (+b1) for the tile's packed block and dA = dY W2 (W2 read
+  // MN-major, two 64-feature atoms per stage), both K = d; dH from them
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_map(&g.tma_a, x_perm, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_map(&g.tma_b, w1p, d, W1, E, d * 2, W1 * d * 2, 64, 256) ||
+      !encode_map(&g.tma_a2, dy, d, cap, 1, d * 2, cap * d * 2, 64, 128) ||
+      !encode_out(&g.tma_out0, dh, W1, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.b2_atoms4d = encode_mn_atoms(&g.tma_b2, w2, F, d, E, F * 2, d * F * 2, 2);
+  if (!g.b2_atoms4d && !encode_map(&g.tma_b2, w2, F, d, E, F * 2, d * F * 2, 64, 64))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = fc1_pad(desc->F);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = W1;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  if ((st = set_mx(g, dh_mx, W1, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm(kDgradDgluRc, g, grid_for(di, desc), stream));
+}
+
 moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
                            const int32_t* counts, const int32_t* padded_offsets, void* dw2,
                            cudaStream_t stream) {
@@ -647,22 +684,29 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
       !dx_perm || !dw1p || !dw2)
     return MOE_ERR_NULL;
   if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
-  if (!h) {
-    // activation recompute: regenerate H in the workspace
-    size_t need = 0;
-    if (!desc->recompute_h) return MOE_ERR_NULL;
-    if ((st = moe_workspace_size(desc, &need)) != MOE_OK) return st;
-    if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
-    const size_t off = (route_ws_bytes(desc) + 256 + 255) / 256 * 256;
-    void* h_ws = static_cast<uint8_t*>(ws) + off;
-    if ((st = moe_fc1_recompute_h(desc, x_perm, counts, padded_offsets, w1p, b1p, h_ws,
-                                  stream)) != MOE_OK)
+  if (!h && !desc->recompute_h) return MOE_ERR_NULL;
+  if (!h && desc->act != MOE_ACT_SRELU) {
+    // activation recompute inside the dGLU kernel: H never reaches HBM
+    if ((st = moe_fc2_dgrad_dglu_recompute(desc, x_perm, dy, counts, padded_offsets, w1p, b1p,
+                                           w2, dh, dh_mx, stream)) != MOE_OK)
       return st;
-    h = h_ws;
+  } else {
+    if (!h) {
+      // non-gated activation: regenerate H in the workspace first
+      size_t need = 0;
+      if ((st = moe_workspace_size(desc, &need)) != MOE_OK) return st;
+      if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
+      const size_t off = (route_ws_bytes(desc) + 256 + 255) / 256 * 256;
+      void* h_ws = static_cast<uint8_t*>(ws) + off;
+      if ((st = moe_fc1_recompute_h(desc, x_perm, counts, padded_offsets, w1p, b1p, h_ws,
+                                    stream)) != MOE_OK)
+        return st;
+      h = h_ws;
+    }
+    if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, dh_mx, stream)) !=
+        MOE_OK)
+      return st;
   }
-  if ((st = moe_fc2_dgrad_dglu(desc, dy, h, counts, padded_offsets, w2, dh, dh_mx, stream)) !=
-      MOE_OK)
-    return st;
   if ((st = moe_fc2_wgrad(desc, dy, a, counts, padded_offsets, dw2, stream)) != MOE_OK) return st;
   if ((st = moe_fc1_dgrad(desc, dh, counts, padded_offsets, w1p, dx_perm, stream)) != MOE_OK)
     return st;
@@ -1148,6 +1192,51 @@ moe_status_t moe_fc1_recompute_h_mx(const moe_mlp_desc_t* desc, const moe_mx_out
   g.bias_ld = W1;
   set_scales(g, x_mx->scale, cap, w->w1_s, W1, sf_bytes(W1, d));
   return cuda_status(launch_grouped_gemm_mx(kFc2, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_dgrad_dglu_recompute_mx(const moe_mlp_desc_t* desc,
+                                             const moe_mx_out_t* x_mx,
+                                             const moe_mx_out_t* dy_mx, const int32_t* counts,
+                                             const int32_t* padded_offsets,
+                                             const moe_mx_weights_t* w, const void* b1p,
+                                             void* dh, const moe_mx_out_t* dh_mx,
+                                             cudaStream_t stream) {
+  moe_status_t st = check_mx_desc(desc);
+  if (st != MOE_OK) return st;
+  if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU activations
+  if (!counts || !padded_offsets || !mx_weights_ok(w) || !dh) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!mx_ok(x_mx, true, false) || !mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true))
+    return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // H = X W1p^T (+b1) on the forward's MXFP8 operands (the same MMAs as the
+  // forward), dA = dY W2 on dY's codes and W2's transposed copy [E, F, d]
+  // (128-row boxes: the tile's 128 features); dH and its MXFP8 copies
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b, w->w1, d, W1, E, 256) ||
+      !encode_u8(&g.tma_a2, dy_mx->q, d, cap, 1, 128) ||
+      !encode_u8(&g.tma_b2, w->w2t, d, F, E, 128) || !encode_out(&g.tma_out0, dh, W1, cap, 1))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = fc1_pad(desc->F);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = W1;
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  set_scales(g, x_mx->scale, cap, w->w1_s, W1, sf_bytes(W1, d));
+  g.sfa2 = dy_mx->scale;
+  g.sfa2_atoms = sf_row_atoms(cap);
+  g.sfb2 = w->w2t_s;
+  g.sfb2_atoms = sf_row_atoms(F);
+  g.sfb2_expert_bytes = sf_bytes(F, d);
+  if ((st = set_mx(g, dh_mx, W1, stream)) != MOE_OK) return st;
+  return cuda_status(launch_grouped_gemm_mx(kDgradDgluRc, g, grid_for(di, desc), stream));
 }
 
 moe_status_t moe_fc1_glu_fwd_mx_unfused(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx,

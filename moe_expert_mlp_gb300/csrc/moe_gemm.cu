@@ -97,6 +97,12 @@ constexpr int kOpBf16 = 0, kOpMx = 1, kOpNv = 2, kOpBf16H = 3, kOpMxH = 4;
 constexpr int kHAsyncMaxK = 2048, kHAsyncMaxKMx = 4096;
 __host__ __device__ constexpr bool op_mx(int op) { return op == kOpMx || op == kOpMxH; }
 constexpr int kHDepth = 3;
+// dGLU with H recomputed in the kernel: 128 GLU features per tile; TMEM holds
+// H for the tile's packed block (128 gate + 128 linear columns) at 0..255,
+// dA at 256..383, and the MXFP8 scale slots at 384 (A) and 416 (B), so the
+// next tile's scales never wait for an epilogue
+constexpr int RC_N = 128;
+constexpr uint32_t kRcDa = 256, kRcSfa = 384, kRcSfb = 416;
 constexpr int H_BUF_BYTES = kHDepth * 4 * kGemmEpiThreads * 16;
 constexpr size_t SMEM_BYTES_HA = 1024 + static_cast<size_t>(STAGES - 1) * STAGE_BYTES +
                                  kRing * BOX_BYTES + H_BUF_BYTES;
@@ -380,7 +386,7 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
     }
     ti.e = lo;
     ti.m0 = row;
-    ti.n0 = nb * BN;
+    ti.n0 = nb * (MODE == kDgradDgluRc ? RC_N : BN);
     ti.k_row0 = 0;
     ti.num_kb = 0;  // filled by caller from K
   }
@@ -442,7 +448,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   }
   __syncthreads();
 
-  const int n_tiles = (args.n_ext + BN - 1) / BN;
+  constexpr bool RC = MODE == kDgradDgluRc;
+  constexpr int TN = RC ? RC_N : BN;
+  const int n_tiles = (args.n_ext + TN - 1) / TN;
   const int m_tiles = Tr::kRaggedK ? (args.m_ext + BM - 1) / BM : 0;
   if (threadIdx.x == 0) {
     // validate the offsets read from device memory; skip all work if bad
@@ -473,7 +481,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
   const int total = s_total;
-  const int kb_fixed = Tr::kRaggedK ? 0 : (args.K + Tr::kBK - 1) / Tr::kBK;
+  const int kb_half = (args.K + Tr::kBK - 1) / Tr::kBK;   // K blocks of one GEMM
+  const int kb_fixed = Tr::kRaggedK ? 0 : (RC ? 2 * kb_half : kb_half);
   volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
@@ -501,6 +510,61 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           uint8_t* sa = smem + stage * STAGE_BYTES;
           uint8_t* sb = sa + A_BYTES;
           uint64_t* fb = &full_bar[stage];
+          if constexpr (RC) {
+            // K blocks 0 .. kb_half-1: X and the tile's packed W1p block (256
+            // rows) for H; then dY and W2's 128 rows of the tile's features
+            // for dA.  K = d in both.
+            const bool p1 = kb < kb_half;
+            const int kq = p1 ? kb : kb - kb_half;
+            if constexpr (MX) {
+              const int kx = kq * BK_MX;
+              const long long kt = kx / BK_MX;
+              uint8_t* ssf = smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES;
+              if (p1) {
+                mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES + SF_STAGE_BYTES);
+                tma_load_3d(sa, &args.tma_a, fb, kx, ti.m0, 0);
+                tma_load_3d(sb, &args.tma_b, fb, kx, 2 * ti.n0, ti.e);
+                bulk_load(ssf, args.sfa + (kt * args.sfa_atoms + (ti.m0 >> 7)) * 512, 512, fb);
+                bulk_load(ssf + 512,
+                          args.sfb + ti.e * args.sfb_expert_bytes +
+                              (kt * args.sfb_atoms + ((2 * ti.n0) >> 7)) * 512,
+                          1024, fb);
+              } else {
+                mbar_arrive_expect_tx(fb, A_BYTES + RC_N * BK_MX + 1024);
+                tma_load_3d(sa, &args.tma_a2, fb, kx, ti.m0, 0);
+                tma_load_3d(sb, &args.tma_b2, fb, kx, ti.n0, ti.e);
+                bulk_load(ssf, args.sfa2 + (kt * args.sfa2_atoms + (ti.m0 >> 7)) * 512, 512, fb);
+                bulk_load(ssf + 512,
+                          args.sfb2 + ti.e * args.sfb2_expert_bytes +
+                              (kt * args.sfb2_atoms + (ti.n0 >> 7)) * 512,
+                          512, fb);
+              }
+            } else {
+              const int kk = kq * BK;
+              if (p1) {
+                mbar_arrive_expect_tx(fb, A_BYTES + B_BYTES);
+                tma_load_3d(sa, &args.tma_a, fb, kk, ti.m0, 0);
+                tma_load_3d(sb, &args.tma_b, fb, kk, 2 * ti.n0, ti.e);
+              } else {
+                // W2 read MN-major: two 64-feature atoms (4-D box), or one
+                // box per atom that holds an in-range feature
+                const int nb2 = args.b2_atoms4d ? 2 : min(2, (args.b_ext - ti.n0 + 63) / 64);
+                mbar_arrive_expect_tx(fb, A_BYTES + nb2 * MN_BOX_BYTES);
+                tma_load_3d(sa, &args.tma_a2, fb, kk, ti.m0, 0);
+                if (args.b2_atoms4d)
+                  tma_load_4d(sb, &args.tma_b2, fb, 0, kk, ti.n0 / 64, ti.e);
+                else
+                  for (int i = 0; i < nb2; ++i)
+                    tma_load_3d(sb + i * MN_BOX_BYTES, &args.tma_b2, fb, ti.n0 + 64 * i, kk,
+                                ti.e);
+              }
+            }
+            if (++stage == NST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if constexpr (NV) {
             // packed E2M1 tiles (K-major, 256 K per 128-byte row; the TMA
             // coordinate is in bytes) and the scale atoms of each K = 64
@@ -584,8 +648,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       for (int t = blockIdx.x; t < total && ok; t += gridDim.x, ++it) {
         Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
         const int num_kb = Tr::kRaggedK ? ti.num_kb : kb_fixed;
-        const int acc = it & 1;
-        const uint32_t acc_par = (it >> 1) & 1;
+        // the recompute mode holds one tile in TMEM (H, dA, scales): one
+        // accumulator set, its phase flips every tile
+        const int acc = RC ? 0 : (it & 1);
+        const uint32_t acc_par = RC ? (it & 1) : ((it >> 1) & 1);
         if (!mbar_wait(&tempty_bar[acc], acc_par ^ 1u, args.status, abort_flag)) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
@@ -595,7 +661,7 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         // MX: this tile's scales go to the first columns of the other
         // accumulator, which the previous tile's epilogue must have read.
         const uint32_t sf_tmem = tmem_base + (acc ^ 1) * BN;
-        if constexpr (MX || NV) {
+        if constexpr ((MX || NV) && !RC) {
           if (it > 0) {
             if (!mbar_wait(&tearly_bar[acc ^ 1], ((it - 1) >> 1) & 1, args.status, abort_flag))
               break;
@@ -610,6 +676,43 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           tc_fence_after();
           const uint32_t a_base = smem_u32(smem + stage * STAGE_BYTES);
           const uint32_t b_base = a_base + A_BYTES;
+          if constexpr (RC) {
+            // H (N = 256, K-major B) into columns 0..255, then dA (N = 128)
+            // into kRcDa..; each GEMM starts its own accumulation
+            const bool p1 = kb < kb_half;
+            const bool first = (p1 ? kb : kb - kb_half) == 0;
+            const uint32_t dst = tmem_base + (p1 ? 0u : kRcDa);
+            if constexpr (MX) {
+              const uint32_t sf = smem_u32(smem + NST * STAGE_BYTES + stage * SF_STAGE_BYTES);
+              tmem_cp_32x128_x4(tmem_base + kRcSfa, sdesc_noswz(sf, 128, 128));
+              tmem_cp_32x128_x4(tmem_base + kRcSfb, sdesc_noswz(sf + 512, 128, 128));
+              if (p1)
+                tmem_cp_32x128_x4(tmem_base + kRcSfb + 4, sdesc_noswz(sf + 1024, 128, 128));
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_mx(dst, sdesc_sw128(a_base + k * 32, 16, 1024),
+                        sdesc_sw128(b_base + k * 32, 16, 1024),
+                        idesc_mx(BM, p1 ? BN : RC_N, k, k), tmem_base + kRcSfa,
+                        tmem_base + kRcSfb, (!first || k > 0) ? 1u : 0u);
+            } else {
+#pragma unroll
+              for (int k = 0; k < BK / 16; ++k) {
+                const uint64_t ad = sdesc_sw128(a_base + k * 32, 16, 1024);
+                const uint64_t bd = p1 ? sdesc_sw128(b_base + k * 32, 16, 1024)
+                                       : sdesc_sw128(b_base + k * 2048, MN_BOX_BYTES, 1024);
+                umma_bf16(dst, ad, bd,
+                          p1 ? idesc_bf16(BM, BN, false, false)
+                             : idesc_bf16(BM, RC_N, false, true),
+                          (!first || k > 0) ? 1u : 0u);
+              }
+            }
+            umma_commit(&empty_bar[stage]);
+            if (++stage == NST) {
+              stage = 0;
+              phase ^= 1u;
+            }
+            continue;
+          }
           if constexpr (NV) {
             // per K = 64 step (32 bytes along the swizzled rows): its scale
             // atoms to TMEM -- one 32-bit cell per row holding the four
@@ -710,8 +813,8 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
     int it = 0;
     for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
       Tile ti = decode_tile<MODE, Tr::kBK>(t, n_tiles, m_tiles, s_off, s_cnt, s_order, E);
-      const int acc = it & 1;
-      const uint32_t acc_par = (it >> 1) & 1;
+      const int acc = RC ? 0 : (it & 1);
+      const uint32_t acc_par = RC ? (it & 1) : ((it >> 1) & 1);
       const long long gr = ti.m0 + row_local;
       const bool valid = !Tr::kRaggedK && (gr - s_off[ti.e]) < s_cnt[ti.e];
       const int y0 = ti.m0;                     // first output row of the tile's boxes
@@ -991,6 +1094,78 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             for (int i = 0; i < 16; ++i) {
               dg[i] = live1 ? bf16_round(dg[i]) : 0.0f;
               dl[i] = live1 ? bf16_round(dl[i]) : 0.0f;
+            }
+            mx_amax_regs16(dg, lane, am_m, am_h);
+            mx_amax_regs16(dl, lane, am_m, am_h);
+          }
+        }
+      } else if (MODE == kDgradDgluRc) {
+        // tile columns are GLU features n0 .. n0+127: dA from TMEM columns
+        // kRcDa.., the recomputed gate and linear halves of H from columns
+        // 0.. and 128.. (bias added, then rounded to bf16 as the stored H
+        // is); dH in packed layout (the tile's block starts at column 2*n0)
+        const __nv_bfloat16* b1 =
+            args.bias ? static_cast<const __nv_bfloat16*>(args.bias) + ti.e * args.bias_ld +
+                            2 * ti.n0 + hc
+                      : nullptr;
+        uint32_t rda[16], rg[16], rl[16];
+        tmem_ld16(tbase + kRcDa, rda);
+        tmem_ld16(tbase, rg);
+        tmem_ld16(tbase + kGluHalf, rl);
+#pragma unroll 1
+        for (int j = 0; j < RC_N / 32; ++j) {
+          tmem_ld_wait16(rda);
+          reg_fence16(rg);
+          reg_fence16(rl);
+          float da[16], g[16], l[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            da[i] = __uint_as_float(rda[i]);
+            g[i] = __uint_as_float(rg[i]);
+            l[i] = __uint_as_float(rl[i]);
+          }
+          if (j + 1 < RC_N / 32) {              // next chunk in flight
+            tmem_ld16(tbase + kRcDa + 32 * (j + 1), rda);
+            tmem_ld16(tbase + 32 * (j + 1), rg);
+            tmem_ld16(tbase + kGluHalf + 32 * (j + 1), rl);
+          }
+          if (b1) {
+            float bg[16], bl[16];
+            load_bf16x16(b1 + 32 * j, bg);
+            load_bf16x16(b1 + kGluHalf + 32 * j, bl);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              g[i] += bg[i];
+              l[i] += bl[i];
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            g[i] = bf16_round(g[i]);
+            l[i] = bf16_round(l[i]);
+          }
+          const int f0 = ti.n0 + 32 * j;
+          const int c0 = 2 * ti.n0 + 32 * j;
+          const bool live = valid && f0 < args.f_real;
+          float dg[16], dl[16];
+          if (live) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) glu_bwd<ACT>(da[i], g[i], l[i], ap, dg[i], dl[i]);
+          }
+          const uint8_t* box_g = ring_next_box(ring);
+          ring_store_half<Tr::kNR>(ring, dg, live, &args.tma_out0, c0, y0, 0, row_local, half,
+                                   issuer);
+          if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
+          const uint8_t* box_l = ring_next_box(ring);
+          ring_store_half<Tr::kNR>(ring, dl, live, &args.tma_out0, c0 + kGluHalf, y0, 0,
+                                   row_local, half, issuer);
+          if (want_mx)
+            mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
+          if (want_mx && mx.amax) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              dg[i] = live ? bf16_round(dg[i]) : 0.0f;
+              dl[i] = live ? bf16_round(dl[i]) : 0.0f;
             }
             mx_amax_regs16(dg, lane, am_m, am_h);
             mx_amax_regs16(dl, lane, am_m, am_h);
@@ -1444,6 +1619,7 @@ cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaSt
     case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpBf16>(args, grid, s);
     case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, kOpBf16>(args, grid, s);
     case kRouter: return launch_mode<kRouter, 0, kOpBf16>(args, grid, s);
+    case kDgradDgluRc: return launch_act<kDgradDgluRc, kOpBf16>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1459,6 +1635,7 @@ cudaError_t launch_grouped_gemm_mx(int mode, const GemmArgs& args, int grid, cud
     case kWgrad: return launch_mode<kWgrad, 0, kOpMx>(args, grid, s);
     case kFc1Act: return launch_mode<kFc1Act, MOE_ACT_SRELU, kOpMx>(args, grid, s);
     case kDgradAct: return launch_mode<kDgradAct, MOE_ACT_SRELU, kOpMx>(args, grid, s);
+    case kDgradDgluRc: return launch_act<kDgradDgluRc, kOpMx>(args, grid, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -72,7 +72,9 @@ enum GemmMode : int {
   kWgradPair = 5,  // same on CTA pairs (2-SM MMA, 256x256 tiles)
   kFc1Act = 6,     // non-gated: H = X W1^T (+b1), A = act(H)   ragged M
   kDgradAct = 7,   // non-gated: dA = dY W2, dH = act'(H) dA     ragged M
-  kRouter = 8      // logits = x W_r^T, top-k in the epilogue    one dense group
+  kRouter = 8,     // logits = x W_r^T, top-k in the epilogue    one dense group
+  kDgradDgluRc = 9 // dA = dY W2 and H = X W1p^T (+b1) recomputed ragged M
+                   // for the same tile, dH = dGLU(dA, H): H never in HBM
 };
 
 // FC1 output width: 2*F_pad (gate and linear halves, packed) for the GLU
@@ -143,6 +145,18 @@ struct GemmArgs {
   // 1 / (g_a g_b), g = 2688 / amax (1 for amax 0)
   const float* nv_amax_a;
   const float* nv_amax_b;
+  // kDgradDgluRc: the second GEMM's operands (tma_a / tma_b and sfa / sfb
+  // hold the H GEMM's X and W1p): dY (K-major) and W2 (bf16: MN-major
+  // [E][d][F], as 2-atom 4-D boxes when b2_atoms4d, else 64 x 64 boxes;
+  // MXFP8: the transposed copy [E][F][d], 128-row boxes), with their scales
+  CUtensorMap tma_a2;
+  CUtensorMap tma_b2;
+  const uint8_t* sfa2;
+  const uint8_t* sfb2;
+  long long sfa2_atoms;
+  long long sfb2_atoms;
+  long long sfb2_expert_bytes;
+  int b2_atoms4d;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);

@@ -279,17 +279,23 @@ class MoEExpertMLP:
         if self.mx:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
-            h = self.h
-            if self.recompute_h:                  # regenerate H into a transient buffer
-                h = torch.empty((self.capacity, self.W1), dtype=torch.bfloat16,
-                                device=self.w2.device)
-                with self._t(timer, "fc1_recompute_h"):
-                    L.moe_fc1_recompute_h_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p,
-                                             h, stream)
-            with self._t(timer, "fc2_dgrad_dglu"):
-                dh_out = self.dh_mx if self.amax_dh is None else dict(self.dh_mx, amax=self.amax_dh)
-                L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, h, c, po, self.w_mx,
-                                        self.dh, dh_out, stream)
+            dh_out = self.dh_mx if self.amax_dh is None else dict(self.dh_mx, amax=self.amax_dh)
+            if self.recompute_h and self.gated:   # H recomputed inside the dGLU kernel
+                with self._t(timer, "fc2_dgrad_dglu"):
+                    L.moe_fc2_dgrad_dglu_recompute_mx(self.desc, self.x_mx, self.dy_mx, c, po,
+                                                      self.w_mx, self.b1p, self.dh, dh_out,
+                                                      stream)
+            else:
+                h = self.h
+                if self.recompute_h:              # regenerate H into a transient buffer
+                    h = torch.empty((self.capacity, self.W1), dtype=torch.bfloat16,
+                                    device=self.w2.device)
+                    with self._t(timer, "fc1_recompute_h"):
+                        L.moe_fc1_recompute_h_mx(self.desc, self.x_mx, c, po, self.w_mx,
+                                                 self.b1p, h, stream)
+                with self._t(timer, "fc2_dgrad_dglu"):
+                    L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, h, c, po, self.w_mx,
+                                            self.dh, dh_out, stream)
             with self._t(timer, "fc2_wgrad"):
                 L.moe_fc2_wgrad_mx(self.desc, self.dy_mx, self.a_mx, c, po, self.dw2, stream)
             with self._t(timer, "fc1_dgrad"):

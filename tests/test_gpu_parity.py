@@ -185,8 +185,9 @@ def test_unfused_path_matches_oracle(name):
 
 
 def test_activation_recompute_matches_stored_h():
-    """Forward without keeping H, backward regenerating it in the workspace:
-    the same MMAs in the same order give bitwise the same gradients."""
+    """Forward without keeping H, backward recomputing it inside the dGLU
+    kernel (H never reaches HBM): the same MMAs in the same order give
+    bitwise the same gradients."""
     wl = CASES["gptoss_small"]                       # FC1 bias, clamp, offset
     inp = make_inputs(wl)
     from moe_expert_mlp_gb300 import _lib as L
@@ -295,3 +296,30 @@ def test_composite_bf16_calls_match_per_gemm_calls(name):
         if n in ("h", "a", "y", "dh", "dx_perm"):
             got, t = got[:R_pad], t[:R_pad]
         assert torch.equal(got.view(torch.int16), t.view(torch.int16)), n
+
+
+@pytest.mark.parametrize("name", ["e16_k6_bias_raggedF", "geglu", "sreglu_scaled", "one_expert"])
+def test_dglu_with_in_kernel_recompute_matches_stored_h_kernel(name):
+    """moe_fc2_dgrad_dglu_recompute (H recomputed per tile in the dGLU
+    kernel) == moe_fc2_dgrad_dglu reading the stored H, bit for bit, on
+    several feature tiles with a ragged F, every GLU activation, FC1 bias and
+    out_scale, including the optional MXFP8 outputs of dH."""
+    from moe_expert_mlp_gb300 import _lib as L
+    wl = CASES[name]
+    inp = make_inputs(wl)
+    layer = H.run_gpu_routed(wl, inp)
+    c, po = layer.counts, layer.padded_offsets
+    mx_ref, mx_rec = layer.mx_buffers(layer.W1), layer.mx_buffers(layer.W1)
+    dh_ref = torch.full_like(layer.dh, 5.0)
+    dh_rec = torch.full_like(layer.dh, 6.0)
+    L.moe_fc2_dgrad_dglu(layer.desc, layer.dy, layer.h, c, po, layer.w2, dh_ref, mx=mx_ref)
+    L.moe_fc2_dgrad_dglu_recompute(layer.desc, layer.x_perm, layer.dy, c, po, layer.w1p,
+                                   layer.b1p, layer.w2, dh_rec, mx=mx_rec)
+    torch.cuda.synchronize()
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    R_pad = int(H.to_np(po)[-1])
+    assert torch.equal(dh_rec[:R_pad].view(torch.int16), dh_ref[:R_pad].view(torch.int16))
+    assert torch.equal(dh_rec[:R_pad].view(torch.int16), layer.dh[:R_pad].view(torch.int16))
+    for k in ("q", "scale", "qt", "scale_t", "amax"):
+        assert torch.equal(mx_rec[k], mx_ref[k]), k
