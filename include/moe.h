@@ -433,6 +433,9 @@ moe_status_t moe_mlp_fwd_mx(const moe_mlp_desc_t* desc, const moe_mx_out_t* x_mx
  *   moe_fc1_glu_fwd_mx    h, a, a_mx <- x_mx (rowwise), w1
  *   moe_fc2_fwd_mx        y          <- a_mx (rowwise), w2
  *   moe_fc2_dgrad_dglu_mx dh, dh_mx  <- dy_mx (rowwise), w2t, h
+ *                         (dh, the bf16 dH, may be NULL: only the MXFP8
+ *                         copies the later GEMMs read are then written; the
+ *                         FC1 bias gradient needs dh)
  *   moe_fc2_wgrad_mx      dw2        <- dy_mx, a_mx (transposed copies)
  *   moe_fc1_dgrad_mx      dx_perm    <- dh_mx (rowwise), w1t
  *   moe_fc1_wgrad_mx      dw1p       <- dh_mx, x_mx (transposed copies) */

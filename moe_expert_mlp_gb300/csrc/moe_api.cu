@@ -1054,19 +1054,20 @@ moe_status_t moe_fc2_dgrad_dglu_mx(const moe_mlp_desc_t* desc, const moe_mx_out_
                                    void* dh, const moe_mx_out_t* dh_mx, cudaStream_t stream) {
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
-  if (!h || !counts || !padded_offsets || !mx_weights_ok(w) || !dh) return MOE_ERR_NULL;
+  if (!h || !counts || !padded_offsets || !mx_weights_ok(w)) return MOE_ERR_NULL;
   if (!mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true)) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   const uint64_t E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
                  W1 = fc1_width(desc->act, desc->F);
   const uint64_t cap = desc->capacity;
-  // dY (codes [cap, d]) x W2^T (codes [E, F, d]); dGLU epilogue reads H
+  // dY (codes [cap, d]) x W2^T (codes [E, F, d]); dGLU epilogue reads H;
+  // the bf16 dH is stored only when dh is given
   GemmArgs g;
   fill_common(g, desc, di, counts, padded_offsets);
   if (!encode_u8(&g.tma_a, dy_mx->q, d, cap, 1, 128) ||
       !encode_u8(&g.tma_b, w->w2t, d, F, E, 256) ||
-      !encode_out(&g.tma_out0, dh, W1, cap, 1))
+      (dh && !encode_out(&g.tma_out0, dh, W1, cap, 1)))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = desc->act == MOE_ACT_SRELU ? desc->F : static_cast<int>(Fp);
@@ -1204,7 +1205,7 @@ moe_status_t moe_fc2_dgrad_dglu_recompute_mx(const moe_mlp_desc_t* desc,
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
   if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU activations
-  if (!counts || !padded_offsets || !mx_weights_ok(w) || !dh) return MOE_ERR_NULL;
+  if (!counts || !padded_offsets || !mx_weights_ok(w)) return MOE_ERR_NULL;
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
   if (!mx_ok(x_mx, true, false) || !mx_ok(dy_mx, true, false) || !mx_ok(dh_mx, true, true))
     return MOE_ERR_NULL;
@@ -1220,7 +1221,8 @@ moe_status_t moe_fc2_dgrad_dglu_recompute_mx(const moe_mlp_desc_t* desc,
   if (!encode_u8(&g.tma_a, x_mx->q, d, cap, 1, 128) ||
       !encode_u8(&g.tma_b, w->w1, d, W1, E, 256) ||
       !encode_u8(&g.tma_a2, dy_mx->q, d, cap, 1, 128) ||
-      !encode_u8(&g.tma_b2, w->w2t, d, F, E, 128) || !encode_out(&g.tma_out0, dh, W1, cap, 1))
+      !encode_u8(&g.tma_b2, w->w2t, d, F, E, 128) ||
+      (dh && !encode_out(&g.tma_out0, dh, W1, cap, 1)))
     return MOE_ERR_SHAPE;
   g.K = desc->d;
   g.n_ext = fc1_pad(desc->F);
@@ -1327,6 +1329,7 @@ moe_status_t moe_mlp_bwd_mx(const moe_mlp_desc_t* desc, const void* dy,
   moe_status_t st = check_mx_desc(desc);
   if (st != MOE_OK) return st;
   if (!dy || !dx_perm || !dw1p || !dw2) return MOE_ERR_NULL;
+  if (db1p && !dh) return MOE_ERR_NULL;            // the FC1 bias gradient sums dH
   if (!mx_ok(dy_mx, true, true) || !mx_ok(x_mx, false, true) || !mx_ok(a_mx, false, true) ||
       !mx_ok(dh_mx, true, true))
     return MOE_ERR_NULL;

@@ -804,6 +804,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       }
     };
     const bool want_mx = mx.q != nullptr || mx.qt != nullptr || mx.amax != nullptr;
+    // dGLU: the bf16 dH store is optional (the MXFP8 path may need only the
+    // quantized copies, which are made from the staged boxes)
+    const CUtensorMap* const dh_map = args.out0 != nullptr ? &args.tma_out0 : nullptr;
     // NVFP4: undo the two operands' encode scales on the accumulator
     float nv_alpha = 1.0f;
     if constexpr (NV)
@@ -1001,11 +1004,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           float dg[16], dl[16];
           if (live) dglu_compute16<ACT>(ra, hgv, hlv, ap, dg, dl);
           const uint8_t* box_g = ring_next_box(ring);
-          ring_store_half<Tr::kNR>(ring, dg, live, &args.tma_out0, c0, y0, 0, row_local, half,
+          ring_store_half<Tr::kNR>(ring, dg, live, dh_map, c0, y0, 0, row_local, half,
                                    issuer);
           if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
           const uint8_t* box_l = ring_next_box(ring);
-          ring_store_half<Tr::kNR>(ring, dl, live, &args.tma_out0, c0 + kGluHalf, y0, 0,
+          ring_store_half<Tr::kNR>(ring, dl, live, dh_map, c0 + kGluHalf, y0, 0,
                                    row_local, half, issuer);
           if (want_mx)
             mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
@@ -1047,11 +1050,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           if (live0) dglu_compute16<ACT>(ra, hg[0], hl[0], ap, dg, dl);
           {
             const uint8_t* box_g = ring_next_box(ring);
-            ring_store_half<Tr::kNR>(ring, dg, live0, &args.tma_out0, c0, y0, 0, row_local, half,
+            ring_store_half<Tr::kNR>(ring, dg, live0, dh_map, c0, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
             const uint8_t* box_l = ring_next_box(ring);
-            ring_store_half<Tr::kNR>(ring, dl, live0, &args.tma_out0, c0 + kGluHalf, y0, 0,
+            ring_store_half<Tr::kNR>(ring, dl, live0, dh_map, c0 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);
@@ -1080,11 +1083,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           if (live1) dglu_compute16<ACT>(ra, hg[1], hl[1], ap, dg, dl);
           {
             const uint8_t* box_g = ring_next_box(ring);
-            ring_store_half<Tr::kNR>(ring, dg, live1, &args.tma_out0, c1, y0, 0, row_local, half,
+            ring_store_half<Tr::kNR>(ring, dg, live1, dh_map, c1, y0, 0, row_local, half,
                                      issuer);
             if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c1, lane, half);
             const uint8_t* box_l = ring_next_box(ring);
-            ring_store_half<Tr::kNR>(ring, dl, live1, &args.tma_out0, c1 + kGluHalf, y0, 0,
+            ring_store_half<Tr::kNR>(ring, dl, live1, dh_map, c1 + kGluHalf, y0, 0,
                                      row_local, half, issuer);
             if (want_mx)
               mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c1 + kGluHalf, lane, half);
@@ -1153,11 +1156,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             for (int i = 0; i < 16; ++i) glu_bwd<ACT>(da[i], g[i], l[i], ap, dg[i], dl[i]);
           }
           const uint8_t* box_g = ring_next_box(ring);
-          ring_store_half<Tr::kNR>(ring, dg, live, &args.tma_out0, c0, y0, 0, row_local, half,
+          ring_store_half<Tr::kNR>(ring, dg, live, dh_map, c0, y0, 0, row_local, half,
                                    issuer);
           if (want_mx) mx_block_half(mx, box_g, quarter * 32, y0 + quarter * 32, c0, lane, half);
           const uint8_t* box_l = ring_next_box(ring);
-          ring_store_half<Tr::kNR>(ring, dl, live, &args.tma_out0, c0 + kGluHalf, y0, 0,
+          ring_store_half<Tr::kNR>(ring, dl, live, dh_map, c0 + kGluHalf, y0, 0,
                                    row_local, half, issuer);
           if (want_mx)
             mx_block_half(mx, box_l, quarter * 32, y0 + quarter * 32, c0 + kGluHalf, lane, half);

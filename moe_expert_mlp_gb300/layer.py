@@ -19,7 +19,8 @@ from . import _lib as L
 class MoEExpertMLP:
     def __init__(self, E, d, F, T=0, k=1, act="swiglu", alpha=1.0, limit=math.inf,
                  linear_offset=0.0, out_scale=1.0, has_b1=False, has_b2=False, sm_margin=0,
-                 capacity=None, device="cuda", recompute_h=False, dtype="bf16"):
+                 capacity=None, device="cuda", recompute_h=False, dtype="bf16",
+                 keep_bf16_copies=None):
         self.desc = L.make_desc(T, E, k, d, F, act=act, alpha=alpha, limit=limit,
                                 linear_offset=linear_offset, out_scale=out_scale,
                                 has_b1=has_b1, has_b2=has_b2, sm_margin=sm_margin,
@@ -37,6 +38,11 @@ class MoEExpertMLP:
         # recompute_h: the forward keeps no H; the backward regenerates it in
         # the library workspace (activation recompute)
         self.recompute_h = recompute_h
+        # the bf16 A and dH: on the MXFP8 path the later GEMMs read only
+        # their MXFP8 copies, so by default they are not written there (dH
+        # still is when the FC1 bias gradient needs it); the bf16 and NVFP4
+        # paths always write them
+        self.keep_bf16 = (dtype != "mxfp8") if keep_bf16_copies is None else bool(keep_bf16_copies)
         self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
         self.Fp = L.moe_fc1_padded_width(F)
         # FC1 output width: packed gate|linear halves (2*F_pad) for the GLU
@@ -235,7 +241,7 @@ class MoEExpertMLP:
             with self._t(timer, "fc1_glu_fwd"):
                 a_out = self.a_mx if self.amax_a is None else dict(self.a_mx, amax=self.amax_a)
                 L.moe_fc1_glu_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.h,
-                                     self.a, a_out, stream)
+                                     self.a if self.keep_bf16 else None, a_out, stream)
             with self._t(timer, "fc2_fwd"):
                 L.moe_fc2_fwd_mx(self.desc, self.a_mx, c, po, self.w_mx, self.b2, self.y, stream)
             return
@@ -280,11 +286,11 @@ class MoEExpertMLP:
             with self._t(timer, "quant_dy"):
                 L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
             dh_out = self.dh_mx if self.amax_dh is None else dict(self.dh_mx, amax=self.amax_dh)
+            dh = self.dh if (self.keep_bf16 or self.has_b1) else None
             if self.recompute_h and self.gated:   # H recomputed inside the dGLU kernel
                 with self._t(timer, "fc2_dgrad_dglu"):
                     L.moe_fc2_dgrad_dglu_recompute_mx(self.desc, self.x_mx, self.dy_mx, c, po,
-                                                      self.w_mx, self.b1p, self.dh, dh_out,
-                                                      stream)
+                                                      self.w_mx, self.b1p, dh, dh_out, stream)
             else:
                 h = self.h
                 if self.recompute_h:              # regenerate H into a transient buffer
@@ -294,8 +300,8 @@ class MoEExpertMLP:
                         L.moe_fc1_recompute_h_mx(self.desc, self.x_mx, c, po, self.w_mx,
                                                  self.b1p, h, stream)
                 with self._t(timer, "fc2_dgrad_dglu"):
-                    L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, h, c, po, self.w_mx,
-                                            self.dh, dh_out, stream)
+                    L.moe_fc2_dgrad_dglu_mx(self.desc, self.dy_mx, h, c, po, self.w_mx, dh,
+                                            dh_out, stream)
             with self._t(timer, "fc2_wgrad"):
                 L.moe_fc2_wgrad_mx(self.desc, self.dy_mx, self.a_mx, c, po, self.dw2, stream)
             with self._t(timer, "fc1_dgrad"):

@@ -59,7 +59,10 @@ def run_oracle_routed(wl, inp):
 
 
 def make_layer(wl, **kw):
+    """A layer for the workload; the parity tests compare the bf16 A and dH
+    too, so they are kept on every path unless the caller says otherwise."""
     from moe_expert_mlp_gb300 import MoEExpertMLP
+    kw.setdefault("keep_bf16_copies", True)
     return MoEExpertMLP(wl.E, wl.d, wl.F, T=wl.T, k=wl.k, act=wl.act, alpha=wl.alpha,
                         limit=wl.limit, linear_offset=wl.linear_offset, out_scale=wl.out_scale,
                         has_b1=wl.has_b1, has_b2=wl.has_b2, **kw)
