@@ -62,14 +62,11 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # capture per workload and operand type (summaries under profiles/), with the
 # hash of the GEMM sources the counters were taken on; a changed kernel
 # reports null.
-_NCU_SRC = "b9e4ee2528075627"
+_NCU_SRC = "fa346d2198d39246"
 NCU_TRAFFIC = {
-    ("fc1_glu_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 787.954432e6 + 217.387776e6, "src": _NCU_SRC},
-    ("fc2_fwd", "bf16_t4096_e64", "bf16"): {"bytes": 409.630464e6 + 101.933568e6, "src": _NCU_SRC},
-    ("fc2_dgrad_dglu", "bf16_t4096_e64", "bf16"): {"bytes": 600.718848e6 + 135.138816e6, "src": _NCU_SRC},
-    ("fc1_dgrad", "bf16_t4096_e64", "bf16"): {"bytes": 836.186368e6 + 103.286528e6, "src": _NCU_SRC},
-    ("fc2_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 185.078272e6 + 313.084672e6, "src": _NCU_SRC},
-    ("fc1_wgrad", "bf16_t4096_e64", "bf16"): {"bytes": 258.155264e6 + 682.243072e6, "src": _NCU_SRC},
+    # FC1 weight gradient of the default layer: full-layer one-pass capture
+    ("fc1_wgrad", "dsv3_r16384_e32", "mxfp8"): {"bytes": 259026176.0 + 1822821120.0,
+                                                 "src": _NCU_SRC},
 }
 
 
