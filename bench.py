@@ -123,6 +123,14 @@ def call_work(wl, name, R, dtype="bf16"):
         "quant_x": R * d * (2 + 2 + 2 / 32),
         "quant_dy": R * d * (2 + 2 + 2 / 32),
     }
+    if dtype == "mxfp8" and wl.router != "direct":
+        # routed MXFP8 layers: the permutation and the combine backward also
+        # write the rowwise copies of x_perm / dY; the passes only the
+        # transposed copies
+        q = 1 + 1 / 32
+        mem.update(route_permute=mem["route_permute"] + R * d * q,
+                   combine_bwd=mem["combine_bwd"] + R * d * q,
+                   quant_x=R * d * (2 + q), quant_dy=R * d * (2 + q))
     if dtype == "nvfp4":
         # bf16 rows in; rowwise and rotated transposed E2M1 codes (half a
         # byte each) + one scale per 16 out; x and dY also read once for amax

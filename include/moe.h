@@ -339,6 +339,32 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
                                        const int32_t* padded_offsets, void* dy, float* dw,
                                        cudaStream_t stream);
 
+/* The permutation and the combine backward with the rowwise MXFP8 copy of
+ * the rows they write fused in ([FK] "Reducing exposed memory overhead by
+ * fusing MXFP8 and NVFP4 quantization": the quantization happens in the
+ * kernel that produces the tensor): moe_route_permute_mx also writes x_mx
+ * (q [capacity,d] E4M3 codes, scale in the MMA layout) of x_perm, and
+ * moe_unpermute_combine_bwd_mx the same of dy, quantized from its stored
+ * bf16 values; padding rows get zero codes and scales.  Codes and scales are
+ * bit for bit those of moe_quantize_act_mx (same rule, same conversions).
+ * Rowwise only (x_mx / dy_mx: q and scale given, qt NULL, no amax, MMA
+ * layout): the transposed copies need 32-row column blocks and stay with
+ * moe_quantize_act_mx given only qt / scale_t.  Other arguments, results and
+ * errors as moe_route_permute / moe_unpermute_combine_bwd. */
+moe_status_t moe_route_permute_mx(const moe_mlp_desc_t* desc, const float* logits,
+                                  const float* bias, const void* x, int32_t* topk_idx,
+                                  float* topk_w, int32_t* counts, int32_t* offsets,
+                                  int32_t* padded_offsets, int32_t* tile_prefix,
+                                  int32_t* row_src, int32_t* row_of, void* x_perm,
+                                  const moe_mx_out_t* x_mx, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream);
+moe_status_t moe_unpermute_combine_bwd_mx(const moe_mlp_desc_t* desc, const void* dout,
+                                          const void* y, const int32_t* row_of,
+                                          const float* topk_w, const int32_t* row_src,
+                                          const int32_t* padded_offsets, void* dy,
+                                          const moe_mx_out_t* dy_mx, float* dw,
+                                          cudaStream_t stream);
+
 /* Expert MLP backward: FC2 dgrad with the dGLU epilogue ([FK] GLU section:
  * the epilogue reads the GEMM output and computes dSwiGLU) -> dh
  * [capacity,2F_pad] packed; FC2 wgrad dw2 [E,d,F] = sum over the group's

@@ -41,7 +41,7 @@ EXPORTS = (
     "moe_fc1_dgrad_nv", "moe_fc1_wgrad_nv", "moe_mlp_fwd_nv", "moe_mlp_bwd_nv",
     "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv", "moe_fc1_glu_fwd_mx_unfused",
     "moe_fc2_dgrad_dglu_mx_unfused", "moe_fc2_dgrad_dglu_recompute",
-    "moe_fc2_dgrad_dglu_recompute_mx",
+    "moe_fc2_dgrad_dglu_recompute_mx", "moe_route_permute_mx", "moe_unpermute_combine_bwd_mx",
 )
 
 
@@ -187,6 +187,8 @@ def lib():
             "moe_fc1_recompute_h_mx": (ctypes.c_int, [D] + [P] * 7),
             "moe_fc1_glu_fwd_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc2_dgrad_dglu_recompute": (ctypes.c_int, [D] + [P] * 10),
+            "moe_route_permute_mx": (ctypes.c_int, [D] + [P] * 14 + [ctypes.c_size_t, P]),
+            "moe_unpermute_combine_bwd_mx": (ctypes.c_int, [D] + [P] * 9 + [P]),
             "moe_fc2_dgrad_dglu_recompute_mx": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc2_dgrad_dglu_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc1_recompute_h_nv": (ctypes.c_int, [D] + [P] * 7),
@@ -523,6 +525,24 @@ def moe_fc1_recompute_h_mx(desc, x_mx, counts, padded_offsets, w_mx, b1p, h, str
     _check(lib().moe_fc1_recompute_h_mx(ctypes.byref(desc), _mx(x_mx), _p(counts),
                                         _p(padded_offsets), _mxw(w_mx), _p(b1p), _p(h),
                                         _stream(stream)))
+
+
+def moe_route_permute_mx(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,
+                         padded_offsets, tile_prefix, row_src, row_of, x_perm, x_mx, ws,
+                         stream=None):
+    """moe_route_permute that also writes x_perm's rowwise MXFP8 copy."""
+    _check(lib().moe_route_permute_mx(
+        ctypes.byref(desc), _p(logits), _p(bias), _p(x), _p(topk_idx), _p(topk_w), _p(counts),
+        _p(offsets), _p(padded_offsets), _p(tile_prefix), _p(row_src), _p(row_of), _p(x_perm),
+        _mx(x_mx), _p(ws), ws.numel() * ws.element_size(), _stream(stream)))
+
+
+def moe_unpermute_combine_bwd_mx(desc, dout, y, row_of, topk_w, row_src, padded_offsets, dy,
+                                 dy_mx, dw, stream=None):
+    """moe_unpermute_combine_bwd that also writes dy's rowwise MXFP8 copy."""
+    _check(lib().moe_unpermute_combine_bwd_mx(
+        ctypes.byref(desc), _p(dout), _p(y), _p(row_of), _p(topk_w), _p(row_src),
+        _p(padded_offsets), _p(dy), _mx(dy_mx), _p(dw), _stream(stream)))
 
 
 def moe_fc2_dgrad_dglu_recompute(desc, x_perm, dy, counts, padded_offsets, w1p, b1p, w2, dh,

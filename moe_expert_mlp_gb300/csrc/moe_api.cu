@@ -278,12 +278,13 @@ moe_status_t moe_unpack_fc1(const moe_mlp_desc_t* desc, const void* w1p, void* w
   return cuda_status(launch_unpack_fc1(w1p, w1, desc->E, desc->F, rows_width, stream));
 }
 
-moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
+static moe_status_t route_permute_impl(const moe_mlp_desc_t* desc, const float* logits,
                                const float* bias, const void* x, int32_t* topk_idx,
                                float* topk_w, int32_t* counts, int32_t* offsets,
                                int32_t* padded_offsets, int32_t* tile_prefix,
                                int32_t* row_src, int32_t* row_of, void* x_perm, void* ws,
-                               size_t ws_bytes, cudaStream_t stream) {
+                               size_t ws_bytes, cudaStream_t stream, uint8_t* xq,
+                               uint8_t* xs) {
   moe_status_t st = check_desc(desc, true);
   if (st != MOE_OK) return st;
   if (!logits || !x || !topk_idx || !topk_w || !counts || !offsets || !padded_offsets ||
@@ -310,9 +311,37 @@ moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
     }
   }
   if (e == cudaSuccess)
-    e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
-                           di->sms, stream);
+    e = xq ? launch_gather_rows_mx(x, row_src, padded_offsets, E, desc->d, T, desc->capacity,
+                                   x_perm, xq, xs, di->sms, stream)
+           : launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity,
+                                x_perm, di->sms, stream);
   return cuda_status(e);
+}
+
+moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
+                               const float* bias, const void* x, int32_t* topk_idx,
+                               float* topk_w, int32_t* counts, int32_t* offsets,
+                               int32_t* padded_offsets, int32_t* tile_prefix,
+                               int32_t* row_src, int32_t* row_of, void* x_perm, void* ws,
+                               size_t ws_bytes, cudaStream_t stream) {
+  return route_permute_impl(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,
+                            padded_offsets, tile_prefix, row_src, row_of, x_perm, ws, ws_bytes,
+                            stream, nullptr, nullptr);
+}
+
+moe_status_t moe_route_permute_mx(const moe_mlp_desc_t* desc, const float* logits,
+                                  const float* bias, const void* x, int32_t* topk_idx,
+                                  float* topk_w, int32_t* counts, int32_t* offsets,
+                                  int32_t* padded_offsets, int32_t* tile_prefix,
+                                  int32_t* row_src, int32_t* row_of, void* x_perm,
+                                  const moe_mx_out_t* x_mx, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream) {
+  if (!x_mx || !x_mx->q || !x_mx->scale) return MOE_ERR_NULL;
+  if (x_mx->layout != MOE_MX_SCALES_MMA || x_mx->qt || x_mx->amax) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(x_mx->q) & 15) return MOE_ERR_SHAPE;
+  return route_permute_impl(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,
+                            padded_offsets, tile_prefix, row_src, row_of, x_perm, ws, ws_bytes,
+                            stream, x_mx->q, x_mx->scale);
 }
 
 moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
@@ -493,6 +522,30 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
                                        desc->capacity, dy, di->sms, stream);
   if (e == cudaSuccess)
     e = launch_combine_bwd(dout, y, row_of, topk_w, desc->T, desc->k, desc->d, dy, dw, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_unpermute_combine_bwd_mx(const moe_mlp_desc_t* desc, const void* dout,
+                                          const void* y, const int32_t* row_of,
+                                          const float* topk_w, const int32_t* row_src,
+                                          const int32_t* padded_offsets, void* dy,
+                                          const moe_mx_out_t* dy_mx, float* dw,
+                                          cudaStream_t stream) {
+  moe_status_t st = check_desc(desc, true);
+  if (st != MOE_OK) return st;
+  if (!dout || !y || !row_of || !topk_w || !row_src || !padded_offsets || !dy || !dw)
+    return MOE_ERR_NULL;
+  if (!dy_mx || !dy_mx->q || !dy_mx->scale) return MOE_ERR_NULL;
+  if (dy_mx->layout != MOE_MX_SCALES_MMA || dy_mx->qt || dy_mx->amax) return MOE_ERR_UNSUPPORTED;
+  if (reinterpret_cast<uintptr_t>(dy_mx->q) & 15) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  cudaError_t e = launch_zero_pad_rows(row_src, padded_offsets, desc->E, desc->d,
+                                       desc->capacity, dy, di->sms, stream, dy_mx->q,
+                                       dy_mx->scale);
+  if (e == cudaSuccess)
+    e = launch_combine_bwd_mx(dout, y, row_of, topk_w, desc->T, desc->k, desc->d,
+                              desc->capacity, dy, dw, dy_mx->q, dy_mx->scale, stream);
   return cuda_status(e);
 }
 

@@ -39,9 +39,20 @@ cudaError_t launch_combine(const void* y, const int32_t* row_of, const float* w,
 cudaError_t launch_combine_bwd(const void* dout, const void* y, const int32_t* row_of,
                                const float* w, int T, int k, int d, void* dy, float* dw,
                                cudaStream_t s);
+// Zero the padding rows (row_src < 0) of a per-row tensor, and when q / sf
+// are given the rows' MXFP8 rowwise codes and scales (MMA layout).
 cudaError_t launch_zero_pad_rows(const int32_t* row_src, const int32_t* padded_offsets, int E,
                                  int width, int capacity, void* rows, int num_sms,
-                                 cudaStream_t s);
+                                 cudaStream_t s, uint8_t* q = nullptr, uint8_t* sf = nullptr);
+// The gather / combine backward that also write the rowwise MXFP8 copy of
+// the rows they write (codes [capacity, d], scales in the MMA layout).
+cudaError_t launch_gather_rows_mx(const void* x, const int32_t* row_src,
+                                  const int32_t* padded_offsets, int E, int d, int T,
+                                  int capacity, void* x_perm, uint8_t* q, uint8_t* sf,
+                                  int num_sms, cudaStream_t s);
+cudaError_t launch_combine_bwd_mx(const void* dout, const void* y, const int32_t* row_of,
+                                  const float* w, int T, int k, int d, int capacity, void* dy,
+                                  float* dw, uint8_t* q, uint8_t* sf, cudaStream_t s);
 cudaError_t launch_permute_bwd(const void* dx_perm, const int32_t* row_of, int T, int k, int d,
                                void* dx, cudaStream_t s);
 cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* idx, int T, int E,

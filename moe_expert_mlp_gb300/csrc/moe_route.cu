@@ -18,6 +18,7 @@
 #include <math.h>
 
 #include "moe_internal.h"
+#include "moe_mx.cuh"
 #include "moe_ptx.cuh"
 
 namespace moe {
@@ -242,18 +243,6 @@ __global__ void __launch_bounds__(256) k_gather_rows(
   }
 }
 
-__global__ void __launch_bounds__(256) k_zero_pad_rows(
-    const int32_t* __restrict__ row_src, const int32_t* __restrict__ padded_offsets, int E,
-    int vec_per_row, int capacity, uint4* __restrict__ rows_out) {
-  const int rows = min(padded_offsets[E], capacity);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
-    if (row_src[j] >= 0) continue;
-    uint4* dst = rows_out + static_cast<size_t>(j) * vec_per_row;
-    for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-  }
-}
-
 __device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {
   v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
   v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
@@ -268,6 +257,75 @@ __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   w.z = pack_bf16x2(v[4], v[5]);
   w.w = pack_bf16x2(v[6], v[7]);
   return w;
+}
+
+// MXFP8 (rowwise) of the eight bf16 values a lane holds: groups of four
+// lanes hold one 32-element block (16-byte chunks 4b .. 4b+3 of a row), whose
+// abs-max the group shares with two shuffles; the codes and the scale are
+// those of the standalone quantizer (same scale rule, same conversions).
+// The whole warp calls (inactive lanes pass zeros and store nothing).
+__device__ __forceinline__ void mx_row_chunk(const float (&v)[8], bool active, int lane,
+                                             uint8_t* q_row, uint8_t* sf, long long row,
+                                             int chunk, long long row_atoms) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+  m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+  if (!active) return;
+  const int s = mx_scale_exponent(m);
+  const float inv = mx_inv_scale(s);
+  const uint32_t w0 = e4m3x2(v[0] * inv, v[1] * inv) | (e4m3x2(v[2] * inv, v[3] * inv) << 16);
+  const uint32_t w1 = e4m3x2(v[4] * inv, v[5] * inv) | (e4m3x2(v[6] * inv, v[7] * inv) << 16);
+  *reinterpret_cast<uint2*>(q_row + chunk * 8) = make_uint2(w0, w1);
+  if ((lane & 3) == 0) sf[sf_mma_offset(row, chunk >> 2, row_atoms)] = static_cast<uint8_t>(s + 127);
+}
+
+// The gather with the rowwise MXFP8 copy of every row it writes (codes
+// [capacity, d], scales in the MMA layout); padding rows get zero codes and
+// scales.
+__global__ void __launch_bounds__(256) k_gather_rows_mx(
+    const uint4* __restrict__ x, const int32_t* __restrict__ row_src,
+    const int32_t* __restrict__ padded_offsets, int E, int vec_per_row, int T, int capacity,
+    uint4* __restrict__ x_perm, uint8_t* __restrict__ q, uint8_t* __restrict__ sf,
+    long long row_atoms) {
+  const int rows = min(padded_offsets[E], capacity);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
+    const int t = row_src[j];
+    const bool real = t >= 0 && t < T;
+    uint4* dst = x_perm + static_cast<size_t>(j) * vec_per_row;
+    const uint4* src = x + static_cast<size_t>(real ? t : 0) * vec_per_row;
+    uint8_t* q_row = q + static_cast<size_t>(j) * vec_per_row * 8;
+    for (int c0 = 0; c0 < vec_per_row; c0 += 32) {
+      const int c = c0 + lane;
+      const bool active = c < vec_per_row;
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (active && real) w = __ldg(src + c);
+      if (active) dst[c] = w;
+      float v[8];
+      unpack8(w, v);
+      mx_row_chunk(v, active, lane, q_row, sf, j, c, row_atoms);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256) k_zero_pad_rows(
+    const int32_t* __restrict__ row_src, const int32_t* __restrict__ padded_offsets, int E,
+    int vec_per_row, int capacity, uint4* __restrict__ rows_out, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sf, long long row_atoms) {
+  const int rows = min(padded_offsets[E], capacity);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
+    if (row_src[j] >= 0) continue;
+    uint4* dst = rows_out + static_cast<size_t>(j) * vec_per_row;
+    for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
+    if (q) {                      // the row's MXFP8 codes (8 per chunk) and scales
+      uint2* qr = reinterpret_cast<uint2*>(q + static_cast<size_t>(j) * vec_per_row * 8);
+      for (int c = lane; c < vec_per_row; c += 32) qr[c] = make_uint2(0, 0);
+      for (int b = lane; b < vec_per_row / 4; b += 32) sf[sf_mma_offset(j, b, row_atoms)] = 0;
+    }
+  }
 }
 
 // ------------------------------------------------------------- combine
@@ -314,6 +372,52 @@ __global__ void __launch_bounds__(128) k_combine_bwd(
         o[i] = ws * g[i];
       }
       dy[static_cast<size_t>(r) * vec_per_row + c] = pack8(o);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) s_part[warp] = dot;
+    __syncthreads();
+    if (threadIdx.x == 0)
+      dw[static_cast<size_t>(t) * k + s] = (s_part[0] + s_part[1]) + (s_part[2] + s_part[3]);
+    __syncthreads();
+  }
+}
+
+// The combine backward with the rowwise MXFP8 copy of each dY row it writes,
+// quantized from the stored (bf16-rounded) values.
+__global__ void __launch_bounds__(128) k_combine_bwd_mx(
+    const uint4* __restrict__ dout, const uint4* __restrict__ y,
+    const int32_t* __restrict__ row_of, const float* __restrict__ w, int k, int vec_per_row,
+    uint4* __restrict__ dy, float* __restrict__ dw, uint8_t* __restrict__ q,
+    uint8_t* __restrict__ sf, long long row_atoms) {
+  __shared__ float s_part[4];
+  const int t = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int s = 0; s < k; ++s) {
+    const int r = row_of[static_cast<size_t>(t) * k + s];
+    const float ws = w[static_cast<size_t>(t) * k + s];
+    uint8_t* q_row = q + static_cast<size_t>(r) * vec_per_row * 8;
+    float dot = 0.0f;
+    for (int c0 = 0; c0 < vec_per_row; c0 += blockDim.x) {
+      const int c = c0 + threadIdx.x;
+      const bool active = c < vec_per_row;
+      float g[8], v[8], o[8];
+      if (active) {
+        unpack8(__ldg(dout + static_cast<size_t>(t) * vec_per_row + c), g);
+        unpack8(__ldg(y + static_cast<size_t>(r) * vec_per_row + c), v);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) g[i] = v[i] = 0.0f;
+      }
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        dot = fmaf(g[i], v[i], dot);
+        o[i] = ws * g[i];
+      }
+      const uint4 packed = pack8(o);
+      if (active) dy[static_cast<size_t>(r) * vec_per_row + c] = packed;
+      float ob[8];
+      unpack8(packed, ob);                       // the stored bf16 values
+      mx_row_chunk(ob, active, lane, q_row, sf, r, c, row_atoms);
     }
     dot = warp_sum(dot);
     if (lane == 0) s_part[warp] = dot;
@@ -458,9 +562,31 @@ cudaError_t launch_gather_rows(const void* x, const int32_t* row_src,
 
 cudaError_t launch_zero_pad_rows(const int32_t* row_src, const int32_t* padded_offsets, int E,
                                  int width, int capacity, void* rows, int num_sms,
-                                 cudaStream_t s) {
+                                 cudaStream_t s, uint8_t* q, uint8_t* sf) {
   k_zero_pad_rows<<<num_sms * 4, 256, 0, s>>>(row_src, padded_offsets, E, width / 8, capacity,
-                                              static_cast<uint4*>(rows));
+                                              static_cast<uint4*>(rows), q, sf,
+                                              sf_row_atoms(capacity));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_rows_mx(const void* x, const int32_t* row_src,
+                                  const int32_t* padded_offsets, int E, int d, int T,
+                                  int capacity, void* x_perm, uint8_t* q, uint8_t* sf,
+                                  int num_sms, cudaStream_t s) {
+  k_gather_rows_mx<<<num_sms * 8, 256, 0, s>>>(static_cast<const uint4*>(x), row_src,
+                                               padded_offsets, E, d / 8, T, capacity,
+                                               static_cast<uint4*>(x_perm), q, sf,
+                                               sf_row_atoms(capacity));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd_mx(const void* dout, const void* y, const int32_t* row_of,
+                                  const float* w, int T, int k, int d, int capacity, void* dy,
+                                  float* dw, uint8_t* q, uint8_t* sf, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  k_combine_bwd_mx<<<T, 128, 0, s>>>(static_cast<const uint4*>(dout),
+                                     static_cast<const uint4*>(y), row_of, w, k, d / 8,
+                                     static_cast<uint4*>(dy), dw, q, sf, sf_row_atoms(capacity));
   return cudaGetLastError();
 }
 

@@ -43,6 +43,11 @@ class MoEExpertMLP:
         # still is when the FC1 bias gradient needs it); the bf16 and NVFP4
         # paths always write them
         self.keep_bf16 = (dtype != "mxfp8") if keep_bf16_copies is None else bool(keep_bf16_copies)
+        # MXFP8: whether the rowwise copies of x_perm / dY were written by the
+        # permutation / the combine backward (then the quantize passes make
+        # only the transposed copies)
+        self._x_row_fused = False
+        self._dy_row_fused = False
         self.T, self.E, self.k, self.d, self.F = T, E, k, d, F
         self.Fp = L.moe_fc1_padded_width(F)
         # FC1 output width: packed gate|linear halves (2*F_pad) for the GLU
@@ -189,14 +194,31 @@ class MoEExpertMLP:
 
     def route(self, x, logits, bias=None, stream=None, timer=None):
         with self._t(timer, "route_permute"):
-            L.moe_route_permute(self.desc, logits, bias, x, self.topk_idx, self.topk_w,
-                                self.counts, self.offsets, self.padded_offsets, self.tile_prefix,
-                                self.row_src, self.row_of, self.x_perm, self.ws, stream)
+            if self.mx:          # x_perm's rowwise MXFP8 copy written by the gather
+                L.moe_route_permute_mx(self.desc, logits, bias, x, self.topk_idx, self.topk_w,
+                                       self.counts, self.offsets, self.padded_offsets,
+                                       self.tile_prefix, self.row_src, self.row_of, self.x_perm,
+                                       self._rowwise(self.x_mx), self.ws, stream)
+                self._x_row_fused = True
+            else:
+                L.moe_route_permute(self.desc, logits, bias, x, self.topk_idx, self.topk_w,
+                                    self.counts, self.offsets, self.padded_offsets,
+                                    self.tile_prefix, self.row_src, self.row_of, self.x_perm,
+                                    self.ws, stream)
+
+    @staticmethod
+    def _rowwise(mx):
+        return dict(q=mx["q"], scale=mx["scale"], layout="mma")
+
+    @staticmethod
+    def _colwise(mx):
+        return dict(qt=mx["qt"], scale_t=mx["scale_t"], layout="mma")
 
     def route_fused(self, x, w_router, bias=None, logits_out=None, stream=None, timer=None):
         """Routing from the tokens themselves: router GEMM (x W_r^T) with the
         top-k in its epilogue, then the same permutation as route();
         w_router bf16 [E,d]; logits_out fp32 [T,E] or None."""
+        self._x_row_fused = False
         with self._t(timer, "route_fused"):
             L.moe_route_permute_fused(self.desc, x, w_router, bias, logits_out, self.topk_idx,
                                       self.topk_w, self.counts, self.offsets,
@@ -237,7 +259,9 @@ class MoEExpertMLP:
             return
         if self.mx:
             with self._t(timer, "quant_x"):
-                L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po, self.x_mx, stream)
+                L.moe_quantize_act_mx(self.desc, self.x_perm, self.d, po,
+                                      self._colwise(self.x_mx) if self._x_row_fused else self.x_mx,
+                                      stream)
             with self._t(timer, "fc1_glu_fwd"):
                 a_out = self.a_mx if self.amax_a is None else dict(self.a_mx, amax=self.amax_a)
                 L.moe_fc1_glu_fwd_mx(self.desc, self.x_mx, c, po, self.w_mx, self.b1p, self.h,
@@ -284,7 +308,9 @@ class MoEExpertMLP:
             return
         if self.mx:
             with self._t(timer, "quant_dy"):
-                L.moe_quantize_act_mx(self.desc, self.dy, self.d, po, self.dy_mx, stream)
+                L.moe_quantize_act_mx(self.desc, self.dy, self.d, po,
+                                      self._colwise(self.dy_mx) if self._dy_row_fused
+                                      else self.dy_mx, stream)
             dh_out = self.dh_mx if self.amax_dh is None else dict(self.dh_mx, amax=self.amax_dh)
             dh = self.dh if (self.keep_bf16 or self.has_b1) else None
             if self.recompute_h and self.gated:   # H recomputed inside the dGLU kernel
@@ -406,9 +432,15 @@ class MoEExpertMLP:
 
     def backward(self, dout, stream=None, timer=None):
         with self._t(timer, "combine_bwd"):
-            L.moe_unpermute_combine_bwd(self.desc, dout, self.y, self.row_of, self.topk_w,
-                                        self.row_src, self.padded_offsets, self.dy, self.dw,
-                                        stream)
+            if self.mx:          # dY's rowwise MXFP8 copy written by the combine backward
+                L.moe_unpermute_combine_bwd_mx(self.desc, dout, self.y, self.row_of, self.topk_w,
+                                               self.row_src, self.padded_offsets, self.dy,
+                                               self._rowwise(self.dy_mx), self.dw, stream)
+                self._dy_row_fused = True
+            else:
+                L.moe_unpermute_combine_bwd(self.desc, dout, self.y, self.row_of, self.topk_w,
+                                            self.row_src, self.padded_offsets, self.dy, self.dw,
+                                            stream)
         self.mlp_backward(stream, timer)
         with self._t(timer, "permute_bwd"):
             L.moe_permute_bwd(self.desc, self.dx_perm, self.row_of, self.dx, stream)
@@ -429,6 +461,7 @@ class MoEExpertMLP:
         device first).  x_perm, dy, y, dx_perm: [capacity, d] bf16 device
         tensors the layer reads its inputs from and writes its per-row
         results to from now on (no copy is made)."""
+        self._x_row_fused = self._dy_row_fused = False   # x_perm, dy given directly
         if x_perm is not None:
             self.x_perm = x_perm
         if dy is not None:

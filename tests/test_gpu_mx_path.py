@@ -121,6 +121,11 @@ def test_routed_layer_mxfp8(name):
     _mx_close(tag + "dlogits", H.to_np(layer.dlogits)[:T], ref["dlogits"], bwd["dlogits"])
     _check_fused_mx(layer, "A", layer.a, layer.a_mx, wl.F)
     _check_fused_mx(layer, "dH", layer.dh, layer.dh_mx, layer.W1)
+    # x_perm's and dY's rowwise copies come from the permutation and the
+    # combine backward, their transposed copies from the quantize pass
+    assert layer._x_row_fused and layer._dy_row_fused
+    _check_fused_mx(layer, "x_perm", layer.x_perm, layer.x_mx, wl.d)
+    _check_fused_mx(layer, "dY", layer.dy, layer.dy_mx, wl.d)
 
 
 def test_direct_groups_mxfp8_with_empty_experts():
