@@ -34,7 +34,8 @@
  * b1p and every FC1-shaped output (h, dh, dw1p, db1p) use the same packed
  * column order.
  *
- * All tensors are row-major, bf16 unless stated.  All pointers are DEVICE
+ * All tensors are row-major, bf16 unless stated (fp32 throughout with
+ * MOE_DTYPE_FP32, see the fp32 / TF32 section).  All pointers are DEVICE
  * pointers (the caller allocates and owns every buffer; the library never
  * allocates, frees or synchronises, and reads no device data on the host),
  * so every call can be captured in a CUDA graph.  Calls are asynchronous on
@@ -80,8 +81,16 @@ typedef enum {
  * each GEMM's contraction dimension ([FK] "Reducing exposed memory overhead
  * by fusing MXFP8 and NVFP4 quantization"); requires d and F multiples of 32
  * (recompute_h: see moe_fc1_recompute_h_mx).  Routing, combine and their backward are bf16 in
- * both. */
-typedef enum { MOE_DTYPE_BF16 = 1, MOE_DTYPE_MXFP8 = 2, MOE_DTYPE_NVFP4 = 3 } moe_dtype_t;
+ * both.  FP32: every activation, weight and gradient tensor is fp32
+ * (routing, permutation, combine and their backward included), and the
+ * grouped GEMMs run on the TF32 tensor cores (the *_tf32 calls, or
+ * moe_mlp_fwd / moe_mlp_bwd with this dtype); fp32 accumulation. */
+typedef enum {
+  MOE_DTYPE_BF16 = 1,
+  MOE_DTYPE_MXFP8 = 2,
+  MOE_DTYPE_NVFP4 = 3,
+  MOE_DTYPE_FP32 = 4
+} moe_dtype_t;
 /* NVFP4 (the *_nv calls): E2M1 operands, one UE4M3 scale per 16 elements
  * along each GEMM's contraction dimension and one fp32 encode scale per
  * tensor from its amax; requires d and F multiples of 64 (recompute_h: see
@@ -702,6 +711,66 @@ moe_status_t moe_fc2_dgrad_dglu_mx_unfused(const moe_mlp_desc_t* desc,
                                            const int32_t* counts, const int32_t* padded_offsets,
                                            const moe_mx_weights_t* w, void* da, void* dh,
                                            const moe_mx_out_t* dh_mx, cudaStream_t stream);
+
+/* ------------------------------------------------------- fp32 / TF32 path
+ * desc->dtype == MOE_DTYPE_FP32: the tensors of every call are fp32 (same
+ * shapes, layouts, padding and packing as the bf16 path).  The routing,
+ * permutation, combine and bias-gradient calls (moe_route_permute,
+ * moe_route_permute_noalloc, moe_unpermute_combine[_bwd], moe_permute_bwd,
+ * moe_bias_grads, moe_repack_fc1, moe_unpack_fc1) follow the descriptor's
+ * dtype; their sums are fp32.  The grouped GEMMs run on the TF32 tensor cores
+ * (tcgen05 kind::tf32: operands rounded to TF32's 10-bit mantissa by the
+ * tensor core, fp32 accumulation) with the same fused epilogues as the bf16
+ * calls, and store fp32 results.  Every operand is read K-major, so the
+ * backward reads transposed copies:
+ *   moe_transpose_weights_tf32  w1t [E, d, W1] = w1p^T, w2t [E, F, d] = w2^T
+ *                               (once per weight update)
+ *   moe_transpose_rows_f32      out [width, capacity] = in^T for the rows
+ *                               below padded_offsets[E] (x_perm, dY, A)
+ *   moe_fc1_glu_fwd_tf32        h, a (+ a_t = A^T [F, capacity], optional)
+ *                               <- x_perm, w1p, b1p
+ *   moe_fc2_fwd_tf32            y <- a, w2, b2
+ *   moe_fc2_dgrad_dglu_tf32     dh and/or dh_t = dH^T [W1, capacity]
+ *                               <- dy, h, w2t
+ *   moe_fc2_wgrad_tf32          dw2 [E, d, F] <- dy_t [d, capacity],
+ *                               a_t [F, capacity]   (K = group rows)
+ *   moe_fc1_dgrad_tf32          dx_perm <- dh, w1t
+ *   moe_fc1_wgrad_tf32          dw1p [E, W1, d] <- dh_t [W1, capacity],
+ *                               x_t [d, capacity]   (K = group rows)
+ * W1 = 2*F_pad for the GLU activations, F for MOE_ACT_SRELU.  The transposed
+ * copies hold zeros in the padding rows' columns (the row tensors are zero
+ * there).  moe_mlp_fwd with MOE_DTYPE_FP32 runs the two forward GEMMs (a_mx,
+ * y_mx must be NULL); moe_mlp_bwd makes the transposed weights and
+ * activations in its workspace (moe_workspace_size includes them), then runs
+ * the four backward GEMMs and the bias gradients (dh_mx NULL).
+ * recompute_h is not supported with fp32 tensors.  Output pointers (h, a,
+ * a_t, y, dh, dh_t, dw1p, dw2, dx_perm) must be 16-byte aligned (else
+ * MOE_ERR_SHAPE); other errors as for the bf16 calls. */
+moe_status_t moe_transpose_weights_tf32(const moe_mlp_desc_t* desc, const void* w1p,
+                                        const void* w2, void* w1t, void* w2t,
+                                        cudaStream_t stream);
+moe_status_t moe_transpose_rows_f32(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                    const int32_t* padded_offsets, void* out,
+                                    cudaStream_t stream);
+moe_status_t moe_fc1_glu_fwd_tf32(const moe_mlp_desc_t* desc, const void* x_perm,
+                                  const int32_t* counts, const int32_t* padded_offsets,
+                                  const void* w1p, const void* b1p, void* h, void* a, void* a_t,
+                                  cudaStream_t stream);
+moe_status_t moe_fc2_fwd_tf32(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
+                              const int32_t* padded_offsets, const void* w2, const void* b2,
+                              void* y, cudaStream_t stream);
+moe_status_t moe_fc2_dgrad_dglu_tf32(const moe_mlp_desc_t* desc, const void* dy, const void* h,
+                                     const int32_t* counts, const int32_t* padded_offsets,
+                                     const void* w2t, void* dh, void* dh_t, cudaStream_t stream);
+moe_status_t moe_fc2_wgrad_tf32(const moe_mlp_desc_t* desc, const void* dy_t, const void* a_t,
+                                const int32_t* counts, const int32_t* padded_offsets, void* dw2,
+                                cudaStream_t stream);
+moe_status_t moe_fc1_dgrad_tf32(const moe_mlp_desc_t* desc, const void* dh,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const void* w1t, void* dx_perm, cudaStream_t stream);
+moe_status_t moe_fc1_wgrad_tf32(const moe_mlp_desc_t* desc, const void* dh_t, const void* x_t,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                void* dw1p, cudaStream_t stream);
 
 /* moe_route_permute for callers that cannot allocate device memory (for
  * example a host program whose device memory is all handed to its own fixed

@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libmoe.so")
 MOE_DTYPE_BF16 = 1
 MOE_DTYPE_MXFP8 = 2
 MOE_DTYPE_NVFP4 = 3
+MOE_DTYPE_FP32 = 4
 MOE_MX_SCALES_ROWMAJOR = 0
 MOE_MX_SCALES_MMA = 1
 ACTS = {"swiglu": 0, "geglu": 1, "srelu": 2, "sreglu": 3}
@@ -42,6 +43,9 @@ EXPORTS = (
     "moe_fc1_recompute_h_mx", "moe_fc1_recompute_h_nv", "moe_fc1_glu_fwd_mx_unfused",
     "moe_fc2_dgrad_dglu_mx_unfused", "moe_fc2_dgrad_dglu_recompute",
     "moe_fc2_dgrad_dglu_recompute_mx", "moe_route_permute_mx", "moe_unpermute_combine_bwd_mx",
+    "moe_transpose_weights_tf32", "moe_transpose_rows_f32", "moe_fc1_glu_fwd_tf32",
+    "moe_fc2_fwd_tf32", "moe_fc2_dgrad_dglu_tf32", "moe_fc2_wgrad_tf32", "moe_fc1_dgrad_tf32",
+    "moe_fc1_wgrad_tf32",
 )
 
 
@@ -108,7 +112,8 @@ def make_desc(T, E, k, d, F, act="swiglu", alpha=1.0, limit=math.inf, linear_off
     if capacity is None:
         capacity = T * k + E * 127
         capacity = (capacity + 127) // 128 * 128
-    dt = {"bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8, "nvfp4": MOE_DTYPE_NVFP4}[dtype]
+    dt = {"bf16": MOE_DTYPE_BF16, "mxfp8": MOE_DTYPE_MXFP8, "nvfp4": MOE_DTYPE_NVFP4,
+          "fp32": MOE_DTYPE_FP32}[dtype]
     return moe_mlp_desc_t(T, E, k, d, F, dt, ACTS[act], alpha, limit, linear_offset,
                           out_scale, int(has_b1), int(has_b2), 128, sm_margin, capacity,
                           int(recompute_h))
@@ -193,6 +198,14 @@ def lib():
             "moe_fc2_dgrad_dglu_mx_unfused": (ctypes.c_int, [D] + [P] * 9),
             "moe_fc1_recompute_h_nv": (ctypes.c_int, [D] + [P] * 7),
             "moe_mlp_bwd_nv": (ctypes.c_int, [D] + [P] * 16),
+            "moe_transpose_weights_tf32": (ctypes.c_int, [D] + [P] * 5),
+            "moe_transpose_rows_f32": (ctypes.c_int, [D, P, ctypes.c_int32, P, P, P]),
+            "moe_fc1_glu_fwd_tf32": (ctypes.c_int, [D] + [P] * 9),
+            "moe_fc2_fwd_tf32": (ctypes.c_int, [D] + [P] * 7),
+            "moe_fc2_dgrad_dglu_tf32": (ctypes.c_int, [D] + [P] * 8),
+            "moe_fc2_wgrad_tf32": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_dgrad_tf32": (ctypes.c_int, [D] + [P] * 6),
+            "moe_fc1_wgrad_tf32": (ctypes.c_int, [D] + [P] * 6),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -581,3 +594,48 @@ def moe_fc1_recompute_h_nv(desc, x_nv, counts, padded_offsets, w_nv, b1p, h, str
     _check(lib().moe_fc1_recompute_h_nv(ctypes.byref(desc), _mx(x_nv), _p(counts),
                                         _p(padded_offsets), _nvw(w_nv), _p(b1p), _p(h),
                                         _stream(stream)))
+
+
+# ------------------------------------------------------- fp32 / TF32 path
+def moe_transpose_weights_tf32(desc, w1p, w2, w1t, w2t, stream=None):
+    _check(lib().moe_transpose_weights_tf32(ctypes.byref(desc), _p(w1p), _p(w2), _p(w1t),
+                                            _p(w2t), _stream(stream)))
+
+
+def moe_transpose_rows_f32(desc, x, width, padded_offsets, out, stream=None):
+    _check(lib().moe_transpose_rows_f32(ctypes.byref(desc), _p(x), width, _p(padded_offsets),
+                                        _p(out), _stream(stream)))
+
+
+def moe_fc1_glu_fwd_tf32(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, a_t=None,
+                         stream=None):
+    _check(lib().moe_fc1_glu_fwd_tf32(ctypes.byref(desc), _p(x_perm), _p(counts),
+                                      _p(padded_offsets), _p(w1p), _p(b1p), _p(h), _p(a),
+                                      _p(a_t), _stream(stream)))
+
+
+def moe_fc2_fwd_tf32(desc, a, counts, padded_offsets, w2, b2, y, stream=None):
+    _check(lib().moe_fc2_fwd_tf32(ctypes.byref(desc), _p(a), _p(counts), _p(padded_offsets),
+                                  _p(w2), _p(b2), _p(y), _stream(stream)))
+
+
+def moe_fc2_dgrad_dglu_tf32(desc, dy, h, counts, padded_offsets, w2t, dh, dh_t=None,
+                            stream=None):
+    _check(lib().moe_fc2_dgrad_dglu_tf32(ctypes.byref(desc), _p(dy), _p(h), _p(counts),
+                                         _p(padded_offsets), _p(w2t), _p(dh), _p(dh_t),
+                                         _stream(stream)))
+
+
+def moe_fc2_wgrad_tf32(desc, dy_t, a_t, counts, padded_offsets, dw2, stream=None):
+    _check(lib().moe_fc2_wgrad_tf32(ctypes.byref(desc), _p(dy_t), _p(a_t), _p(counts),
+                                    _p(padded_offsets), _p(dw2), _stream(stream)))
+
+
+def moe_fc1_dgrad_tf32(desc, dh, counts, padded_offsets, w1t, dx_perm, stream=None):
+    _check(lib().moe_fc1_dgrad_tf32(ctypes.byref(desc), _p(dh), _p(counts), _p(padded_offsets),
+                                    _p(w1t), _p(dx_perm), _stream(stream)))
+
+
+def moe_fc1_wgrad_tf32(desc, dh_t, x_t, counts, padded_offsets, dw1p, stream=None):
+    _check(lib().moe_fc1_wgrad_tf32(ctypes.byref(desc), _p(dh_t), _p(x_t), _p(counts),
+                                    _p(padded_offsets), _p(dw1p), _stream(stream)))

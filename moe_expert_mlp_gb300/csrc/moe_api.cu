@@ -107,7 +107,8 @@ moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
   if (d->d < 64 || d->d % 64 != 0) return MOE_ERR_SHAPE;
   if (d->F < 32 || d->F % 32 != 0) return MOE_ERR_SHAPE;
   if (d->align != kAlign) return MOE_ERR_UNSUPPORTED;
-  if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8 && d->dtype != MOE_DTYPE_NVFP4)
+  if (d->dtype != MOE_DTYPE_BF16 && d->dtype != MOE_DTYPE_MXFP8 && d->dtype != MOE_DTYPE_NVFP4 &&
+      d->dtype != MOE_DTYPE_FP32)
     return MOE_ERR_UNSUPPORTED;
   if (d->act != MOE_ACT_SWIGLU && d->act != MOE_ACT_GEGLU && d->act != MOE_ACT_SREGLU &&
       d->act != MOE_ACT_SRELU)
@@ -122,6 +123,40 @@ moe_status_t check_desc(const moe_mlp_desc_t* d, bool need_tokens) {
   }
   return MOE_OK;
 }
+
+// Calls whose tensors are bf16 (every GEMM call without a type suffix, and
+// the quantizers of bf16 tensors): not for a descriptor of fp32 tensors.
+moe_status_t check_bf16_desc(const moe_mlp_desc_t* d, bool need_tokens = false) {
+  moe_status_t st = check_desc(d, need_tokens);
+  if (st != MOE_OK) return st;
+  return d->dtype == MOE_DTYPE_FP32 ? MOE_ERR_UNSUPPORTED : MOE_OK;
+}
+
+// Bytes per element of the activation, weight and gradient tensors.
+size_t act_bytes(const moe_mlp_desc_t* d) { return d->dtype == MOE_DTYPE_FP32 ? 4 : 2; }
+
+// Workspace of the fp32 backward (moe_mlp_bwd with MOE_DTYPE_FP32): the
+// transposed weights W1p^T [E][d][W1] and W2^T [E][F][d], and the transposed
+// activations x_perm^T, dY^T [d][cap], A^T [F][cap], dH^T [W1][cap], each
+// rounded up to 256 bytes.
+size_t tf32_bwd_ws_bytes(const moe_mlp_desc_t* d) {
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t E = d->E, dm = d->d, F = d->F, W1 = fc1_width(d->act, d->F), cap = d->capacity;
+  return r(E * dm * W1 * 4) + r(E * F * dm * 4) + 2 * r(dm * cap * 4) + r(F * cap * 4) +
+         r(W1 * cap * 4);
+}
+
+moe_status_t mlp_fwd_tf32(const moe_mlp_desc_t* desc, const void* x_perm, const int32_t* counts,
+                          const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                          const void* w2, const void* b2, void* h, void* a, void* y,
+                          const moe_mx_out_t* a_mx, const moe_mx_out_t* y_mx,
+                          cudaStream_t stream);
+moe_status_t mlp_bwd_tf32(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
+                          const void* h, const void* a, const int32_t* counts,
+                          const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                          const void* w2, void* dh, void* dx_perm, void* dw1p, void* db1p,
+                          void* dw2, void* db2, const moe_mx_out_t* dh_mx, void* ws,
+                          size_t ws_bytes, cudaStream_t stream);
 
 int grid_for(const DeviceInfo* di, const moe_mlp_desc_t* d) {
   int g = di->sms - d->sm_margin;
@@ -240,6 +275,8 @@ moe_status_t moe_workspace_size(const moe_mlp_desc_t* desc, size_t* bytes) {
   *bytes = route_ws_bytes(desc) + 256;
   if (desc->recompute_h && desc->act == MOE_ACT_SRELU)   // H regenerated into the workspace
     *bytes += static_cast<size_t>(desc->capacity) * fc1_width(desc->act, desc->F) * 2 + 256;
+  if (desc->dtype == MOE_DTYPE_FP32)   // transposed operands of the fp32 backward
+    *bytes = (*bytes + 255) / 256 * 256 + tf32_bwd_ws_bytes(desc);
   return MOE_OK;
 }
 
@@ -252,14 +289,16 @@ moe_status_t moe_repack_fc1(const moe_mlp_desc_t* desc, const void* w1, const vo
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   cudaError_t e;
+  const size_t eb = act_bytes(desc);   // rows move as 2-byte units
   if (desc->act == MOE_ACT_SRELU) {   // no halves to interleave: a plain copy
     const size_t n = static_cast<size_t>(desc->E) * desc->F;
-    e = cudaMemcpyAsync(w1p, w1, n * desc->d * 2, cudaMemcpyDeviceToDevice, stream);
-    if (e == cudaSuccess && b1) e = cudaMemcpyAsync(b1p, b1, n * 2, cudaMemcpyDeviceToDevice, stream);
+    e = cudaMemcpyAsync(w1p, w1, n * desc->d * eb, cudaMemcpyDeviceToDevice, stream);
+    if (e == cudaSuccess && b1) e = cudaMemcpyAsync(b1p, b1, n * eb, cudaMemcpyDeviceToDevice, stream);
     return cuda_status(e);
   }
-  e = launch_repack_fc1(w1, w1p, desc->E, desc->F, desc->d, stream);
-  if (e == cudaSuccess && b1) e = launch_repack_fc1(b1, b1p, desc->E, desc->F, 1, stream);
+  const int units = static_cast<int>(eb / 2);
+  e = launch_repack_fc1(w1, w1p, desc->E, desc->F, desc->d * units, stream);
+  if (e == cudaSuccess && b1) e = launch_repack_fc1(b1, b1p, desc->E, desc->F, units, stream);
   return cuda_status(e);
 }
 
@@ -271,11 +310,13 @@ moe_status_t moe_unpack_fc1(const moe_mlp_desc_t* desc, const void* w1p, void* w
   if (rows_width < 1) return MOE_ERR_SHAPE;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
+  const size_t eb = act_bytes(desc);
   if (desc->act == MOE_ACT_SRELU)
     return cuda_status(cudaMemcpyAsync(w1, w1p,
-                                       static_cast<size_t>(desc->E) * desc->F * rows_width * 2,
+                                       static_cast<size_t>(desc->E) * desc->F * rows_width * eb,
                                        cudaMemcpyDeviceToDevice, stream));
-  return cuda_status(launch_unpack_fc1(w1p, w1, desc->E, desc->F, rows_width, stream));
+  return cuda_status(launch_unpack_fc1(w1p, w1, desc->E, desc->F,
+                                       rows_width * static_cast<int>(eb / 2), stream));
 }
 
 static moe_status_t route_permute_impl(const moe_mlp_desc_t* desc, const float* logits,
@@ -313,8 +354,9 @@ static moe_status_t route_permute_impl(const moe_mlp_desc_t* desc, const float* 
   if (e == cudaSuccess)
     e = xq ? launch_gather_rows_mx(x, row_src, padded_offsets, E, desc->d, T, desc->capacity,
                                    x_perm, xq, xs, di->sms, stream)
-           : launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity,
-                                x_perm, di->sms, stream);
+           : launch_gather_rows(x, row_src, padded_offsets, E,
+                                desc->d * static_cast<int>(act_bytes(desc) / 2), T,
+                                desc->capacity, x_perm, di->sms, stream);
   return cuda_status(e);
 }
 
@@ -338,6 +380,7 @@ moe_status_t moe_route_permute_mx(const moe_mlp_desc_t* desc, const float* logit
                                   cudaStream_t stream) {
   if (!x_mx || !x_mx->q || !x_mx->scale) return MOE_ERR_NULL;
   if (x_mx->layout != MOE_MX_SCALES_MMA || x_mx->qt || x_mx->amax) return MOE_ERR_UNSUPPORTED;
+  if (desc && desc->dtype == MOE_DTYPE_FP32) return MOE_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(x_mx->q) & 15) return MOE_ERR_SHAPE;
   return route_permute_impl(desc, logits, bias, x, topk_idx, topk_w, counts, offsets,
                             padded_offsets, tile_prefix, row_src, row_of, x_perm, ws, ws_bytes,
@@ -351,7 +394,7 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
                                      int32_t* tile_prefix, int32_t* row_src, int32_t* row_of,
                                      void* x_perm, void* ws, size_t ws_bytes,
                                      cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, true);
+  moe_status_t st = check_bf16_desc(desc, true);
   if (st != MOE_OK) return st;
   if (!x || !w_router || !topk_idx || !topk_w || !counts || !offsets || !padded_offsets ||
       !tile_prefix || !row_src || !row_of || !x_perm)
@@ -422,7 +465,7 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                              const int32_t* counts, const int32_t* padded_offsets,
                              const void* w1p, const void* b1p, void* h, void* a,
                              const moe_mx_out_t* a_mx, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!x_perm || !counts || !padded_offsets || !w1p || !a) return MOE_ERR_NULL;
   if (!h && !desc->recompute_h) return MOE_ERR_NULL;
@@ -456,7 +499,7 @@ moe_status_t moe_fc1_glu_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
 moe_status_t moe_fc2_fwd(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
                          const int32_t* padded_offsets, const void* w2, const void* b2, void* y,
                          const moe_mx_out_t* y_mx, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!a || !counts || !padded_offsets || !w2 || !y) return MOE_ERR_NULL;
   if (desc->has_b2 && !b2) return MOE_ERR_NULL;
@@ -489,6 +532,9 @@ moe_status_t moe_mlp_fwd(const moe_mlp_desc_t* desc, const void* x_perm,
                          cudaStream_t stream) {
   (void)ws;
   (void)ws_bytes;
+  if (desc && desc->dtype == MOE_DTYPE_FP32)
+    return mlp_fwd_tf32(desc, x_perm, counts, padded_offsets, w1p, b1p, w2, b2, h, a, y, a_mx,
+                        y_mx, stream);
   if (!w2 || !y || (desc && desc->has_b2 && !b2)) return MOE_ERR_NULL;
   moe_status_t st =
       moe_fc1_glu_fwd(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a, a_mx, stream);
@@ -504,6 +550,9 @@ moe_status_t moe_unpermute_combine(const moe_mlp_desc_t* desc, const void* y,
   if (!y || !row_of || !topk_w || !out) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
+  if (desc->dtype == MOE_DTYPE_FP32)
+    return cuda_status(
+        launch_combine_f32(y, row_of, topk_w, desc->T, desc->k, desc->d, out, stream));
   return cuda_status(launch_combine(y, row_of, topk_w, desc->T, desc->k, desc->d, out, stream));
 }
 
@@ -518,10 +567,15 @@ moe_status_t moe_unpermute_combine_bwd(const moe_mlp_desc_t* desc, const void* d
     return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
-  cudaError_t e = launch_zero_pad_rows(row_src, padded_offsets, desc->E, desc->d,
-                                       desc->capacity, dy, di->sms, stream);
+  const bool f32 = desc->dtype == MOE_DTYPE_FP32;
+  cudaError_t e = launch_zero_pad_rows(row_src, padded_offsets, desc->E,
+                                       f32 ? 2 * desc->d : desc->d, desc->capacity, dy, di->sms,
+                                       stream);
   if (e == cudaSuccess)
-    e = launch_combine_bwd(dout, y, row_of, topk_w, desc->T, desc->k, desc->d, dy, dw, stream);
+    e = f32 ? launch_combine_bwd_f32(dout, y, row_of, topk_w, desc->T, desc->k, desc->d, dy, dw,
+                                     stream)
+            : launch_combine_bwd(dout, y, row_of, topk_w, desc->T, desc->k, desc->d, dy, dw,
+                                 stream);
   return cuda_status(e);
 }
 
@@ -537,6 +591,7 @@ moe_status_t moe_unpermute_combine_bwd_mx(const moe_mlp_desc_t* desc, const void
     return MOE_ERR_NULL;
   if (!dy_mx || !dy_mx->q || !dy_mx->scale) return MOE_ERR_NULL;
   if (dy_mx->layout != MOE_MX_SCALES_MMA || dy_mx->qt || dy_mx->amax) return MOE_ERR_UNSUPPORTED;
+  if (desc->dtype == MOE_DTYPE_FP32) return MOE_ERR_UNSUPPORTED;
   if (reinterpret_cast<uintptr_t>(dy_mx->q) & 15) return MOE_ERR_SHAPE;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
@@ -553,7 +608,7 @@ moe_status_t moe_fc2_dgrad_dglu(const moe_mlp_desc_t* desc, const void* dy, cons
                                 const int32_t* counts, const int32_t* padded_offsets,
                                 const void* w2, void* dh, const moe_mx_out_t* dh_mx,
                                 cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!dy || !h || !counts || !padded_offsets || !w2 || !dh) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -587,7 +642,7 @@ moe_status_t moe_fc2_dgrad_dglu_recompute(const moe_mlp_desc_t* desc, const void
                                           const int32_t* padded_offsets, const void* w1p,
                                           const void* b1p, const void* w2, void* dh,
                                           const moe_mx_out_t* dh_mx, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU activations
   if (!x_perm || !dy || !counts || !padded_offsets || !w1p || !w2 || !dh) return MOE_ERR_NULL;
@@ -622,7 +677,7 @@ moe_status_t moe_fc2_dgrad_dglu_recompute(const moe_mlp_desc_t* desc, const void
 moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const void* a,
                            const int32_t* counts, const int32_t* padded_offsets, void* dw2,
                            cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!dy || !a || !counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -651,7 +706,7 @@ moe_status_t moe_fc2_wgrad(const moe_mlp_desc_t* desc, const void* dy, const voi
 moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int32_t* counts,
                            const int32_t* padded_offsets, const void* w1p, void* dx_perm,
                            cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!dh || !counts || !padded_offsets || !w1p || !dx_perm) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -680,7 +735,7 @@ moe_status_t moe_fc1_dgrad(const moe_mlp_desc_t* desc, const void* dh, const int
 moe_status_t moe_fc1_wgrad(const moe_mlp_desc_t* desc, const void* dh, const void* x_perm,
                            const int32_t* counts, const int32_t* padded_offsets, void* dw1p,
                            cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!dh || !x_perm || !counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -718,10 +773,10 @@ moe_status_t moe_bias_grads(const moe_mlp_desc_t* desc, const void* dy, const vo
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   cudaError_t e = cudaSuccess;
-  if (db2) e = launch_group_colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream);
+  const auto colsum = desc->dtype == MOE_DTYPE_FP32 ? launch_group_colsum_f32 : launch_group_colsum;
+  if (db2) e = colsum(dy, counts, padded_offsets, desc->E, desc->d, db2, stream);
   if (e == cudaSuccess && db1p)
-    e = launch_group_colsum(dh, counts, padded_offsets, desc->E, fc1_width(desc->act, desc->F), db1p,
-                            stream);
+    e = colsum(dh, counts, padded_offsets, desc->E, fc1_width(desc->act, desc->F), db1p, stream);
   return cuda_status(e);
 }
 
@@ -731,6 +786,9 @@ moe_status_t moe_mlp_bwd(const moe_mlp_desc_t* desc, const void* dy, const void*
                          const void* w2, void* dh, void* dx_perm, void* dw1p, void* db1p,
                          void* dw2, void* db2, const moe_mx_out_t* dh_mx, void* ws,
                          size_t ws_bytes, cudaStream_t stream) {
+  if (desc && desc->dtype == MOE_DTYPE_FP32)
+    return mlp_bwd_tf32(desc, dy, x_perm, h, a, counts, padded_offsets, w1p, b1p, w2, dh,
+                        dx_perm, dw1p, db1p, dw2, db2, dh_mx, ws, ws_bytes, stream);
   moe_status_t st = check_desc(desc, false);
   if (st != MOE_OK) return st;
   if (!dy || !x_perm || !a || !counts || !padded_offsets || !w1p || !w2 || !dh ||
@@ -775,7 +833,7 @@ moe_status_t moe_fc1_glu_fwd_unfused(const moe_mlp_desc_t* desc, const void* x_p
                                      const int32_t* counts, const int32_t* padded_offsets,
                                      const void* w1p, const void* b1p, void* h, void* a,
                                      cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
   if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
@@ -810,7 +868,7 @@ moe_status_t moe_fc1_glu_fwd_unfused(const moe_mlp_desc_t* desc, const void* x_p
 moe_status_t moe_fc1_recompute_h(const moe_mlp_desc_t* desc, const void* x_perm,
                                  const int32_t* counts, const int32_t* padded_offsets,
                                  const void* w1p, const void* b1p, void* h, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!x_perm || !counts || !padded_offsets || !w1p || !h) return MOE_ERR_NULL;
   if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
@@ -839,7 +897,7 @@ moe_status_t moe_fc2_dgrad_dglu_unfused(const moe_mlp_desc_t* desc, const void* 
                                         const void* h, const int32_t* counts,
                                         const int32_t* padded_offsets, const void* w2, void* da,
                                         void* dh, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (desc->act == MOE_ACT_SRELU) return MOE_ERR_UNSUPPORTED;   // GLU passes only
   if (!dy || !h || !counts || !padded_offsets || !w2 || !da || !dh) return MOE_ERR_NULL;
@@ -877,6 +935,9 @@ moe_status_t moe_permute_bwd(const moe_mlp_desc_t* desc, const void* dx_perm,
   if (!dx_perm || !row_of || !dx) return MOE_ERR_NULL;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
+  if (desc->dtype == MOE_DTYPE_FP32)
+    return cuda_status(
+        launch_combine_f32(dx_perm, row_of, nullptr, desc->T, desc->k, desc->d, dx, stream));
   return cuda_status(launch_permute_bwd(dx_perm, row_of, desc->T, desc->k, desc->d, dx, stream));
 }
 
@@ -997,7 +1058,7 @@ moe_status_t moe_quantize_mx_bf16(const void* in, int64_t batch, int64_t rows, i
 moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int32_t width,
                                  const int32_t* padded_offsets, const moe_mx_out_t* out,
                                  cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!in || !padded_offsets || !out) return MOE_ERR_NULL;
   if ((out->q && !out->scale) || (out->qt && !out->scale_t) || (!out->q && !out->qt))
@@ -1018,7 +1079,7 @@ moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int
 moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p,
                                      const void* w2, const moe_mx_weights_t* out,
                                      cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!w1p || !w2 || !mx_weights_ok(out)) return MOE_ERR_NULL;
   DeviceInfo* di;
@@ -1482,7 +1543,7 @@ moe_status_t moe_quantize_nvfp4_bf16(const void* in, int64_t batch, int64_t rows
 moe_status_t moe_quantize_act_nvfp4(const moe_mlp_desc_t* desc, const void* in, int32_t width,
                                     const int32_t* padded_offsets, const moe_mx_out_t* out,
                                     int32_t compute_amax, cudaStream_t stream) {
-  moe_status_t st = check_desc(desc, false);
+  moe_status_t st = check_bf16_desc(desc);
   if (st != MOE_OK) return st;
   if (!in || !padded_offsets || !out) return MOE_ERR_NULL;
   if (!nv_ok(out, out->q != nullptr, out->qt != nullptr) || (!out->q && !out->qt))
@@ -1780,3 +1841,279 @@ moe_status_t moe_mlp_bwd_nv(const moe_mlp_desc_t* desc, const void* dy,
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// fp32 tensors (MOE_DTYPE_FP32): the grouped GEMMs on TF32 tensor cores
+// (tcgen05 kind::tf32) with the same fused epilogues; every operand K-major,
+// the backward's transposed operands from transposed copies.
+namespace moe {
+namespace {
+
+// fp32 operand [E][rows][K] (K contiguous), boxes of 32 K x box_rows rows.
+bool encode_f32(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint64_t E,
+                uint32_t box_rows) {
+  return encode_map(map, base, K, rows, E, K * 4, rows * K * 4, 32, box_rows,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_DATA_TYPE_FLOAT32);
+}
+
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status_t check_f32_desc(const moe_mlp_desc_t* d) {
+  moe_status_t st = check_desc(d, false);
+  if (st != MOE_OK) return st;
+  if (d->dtype != MOE_DTYPE_FP32 || d->recompute_h) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" {
+
+moe_status_t moe_transpose_weights_tf32(const moe_mlp_desc_t* desc, const void* w1p,
+                                        const void* w2, void* w1t, void* w2t,
+                                        cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!w1p || !w2 || !w1t || !w2t) return MOE_ERR_NULL;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const long long E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  cudaError_t e = launch_transpose_f32(w1p, E, W1, d, w1t, nullptr, stream);
+  if (e == cudaSuccess) e = launch_transpose_f32(w2, E, d, F, w2t, nullptr, stream);
+  return cuda_status(e);
+}
+
+moe_status_t moe_transpose_rows_f32(const moe_mlp_desc_t* desc, const void* in, int32_t width,
+                                    const int32_t* padded_offsets, void* out,
+                                    cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!in || !padded_offsets || !out) return MOE_ERR_NULL;
+  if (width < 1) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  return cuda_status(launch_transpose_f32(in, 1, desc->capacity, width, out,
+                                          padded_offsets + desc->E, stream));
+}
+
+moe_status_t moe_fc1_glu_fwd_tf32(const moe_mlp_desc_t* desc, const void* x_perm,
+                                  const int32_t* counts, const int32_t* padded_offsets,
+                                  const void* w1p, const void* b1p, void* h, void* a, void* a_t,
+                                  cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!x_perm || !counts || !padded_offsets || !w1p || !h || !a) return MOE_ERR_NULL;
+  if (desc->has_b1 && !b1p) return MOE_ERR_NULL;
+  if (!al16(h) || !al16(a) || !al16(a_t)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // x_perm [cap, d] x W1p [E, W1, d]^T; GLU epilogue (A^T optional)
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, x_perm, d, cap, 1, 128) || !encode_f32(&g.tma_b, w1p, d, W1, E, 256))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = static_cast<int>(W1);
+  g.b_ext = g.n_ext;
+  g.out0 = h;
+  g.ld0 = W1;
+  g.out1 = a;
+  g.ld1 = desc->F;
+  g.out1_t = static_cast<float*>(a_t);
+  g.bias = desc->has_b1 ? b1p : nullptr;
+  g.bias_ld = W1;
+  return cuda_status(launch_grouped_gemm_tf32(desc->act == MOE_ACT_SRELU ? kFc1Act : kFc1Glu, g,
+                                              grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_fwd_tf32(const moe_mlp_desc_t* desc, const void* a, const int32_t* counts,
+                              const int32_t* padded_offsets, const void* w2, const void* b2,
+                              void* y, cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!a || !counts || !padded_offsets || !w2 || !y) return MOE_ERR_NULL;
+  if (desc->has_b2 && !b2) return MOE_ERR_NULL;
+  if (!al16(y)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, cap = desc->capacity;
+  // A [cap, F] x W2 [E, d, F]^T
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, a, F, cap, 1, 128) || !encode_f32(&g.tma_b, w2, F, d, E, 256))
+    return MOE_ERR_SHAPE;
+  g.K = desc->F;
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = y;
+  g.ld0 = d;
+  g.bias = desc->has_b2 ? b2 : nullptr;
+  g.bias_ld = d;
+  return cuda_status(launch_grouped_gemm_tf32(kFc2, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_dgrad_dglu_tf32(const moe_mlp_desc_t* desc, const void* dy, const void* h,
+                                     const int32_t* counts, const int32_t* padded_offsets,
+                                     const void* w2t, void* dh, void* dh_t, cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dy || !h || !counts || !padded_offsets || !w2t || (!dh && !dh_t)) return MOE_ERR_NULL;
+  if (!al16(h) || !al16(dh) || !al16(dh_t)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // dY [cap, d] x W2^T [E, F, d]^T; the dGLU epilogue reads H
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, dy, d, cap, 1, 128) || !encode_f32(&g.tma_b, w2t, d, F, E, 256))
+    return MOE_ERR_SHAPE;
+  g.K = desc->d;
+  g.n_ext = desc->act == MOE_ACT_SRELU ? desc->F : fc1_pad(desc->F);
+  g.b_ext = desc->F;
+  g.out0 = dh;
+  g.ld0 = W1;
+  g.out0_t = static_cast<float*>(dh_t);
+  g.aux = h;
+  g.ld_aux = W1;
+  return cuda_status(launch_grouped_gemm_tf32(desc->act == MOE_ACT_SRELU ? kDgradAct : kDgradDglu,
+                                              g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc2_wgrad_tf32(const moe_mlp_desc_t* desc, const void* dy_t, const void* a_t,
+                                const int32_t* counts, const int32_t* padded_offsets, void* dw2,
+                                cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dy_t || !a_t || !counts || !padded_offsets || !dw2) return MOE_ERR_NULL;
+  if (!al16(dw2)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t d = desc->d, F = desc->F, cap = desc->capacity;
+  // dW2[e] = dY^T A over the group's rows: [d, cap] and [F, cap]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, dy_t, cap, d, 1, 128) || !encode_f32(&g.tma_b, a_t, cap, F, 1, 256))
+    return MOE_ERR_SHAPE;
+  g.m_ext = desc->d;
+  g.n_ext = desc->F;
+  g.b_ext = desc->F;
+  g.out0 = dw2;
+  g.ld0 = F;
+  return cuda_status(launch_grouped_gemm_tf32(kWgrad, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_dgrad_tf32(const moe_mlp_desc_t* desc, const void* dh,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                const void* w1t, void* dx_perm, cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dh || !counts || !padded_offsets || !w1t || !dx_perm) return MOE_ERR_NULL;
+  if (!al16(dx_perm)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t E = desc->E, d = desc->d, W1 = fc1_width(desc->act, desc->F);
+  const uint64_t cap = desc->capacity;
+  // dH [cap, W1] x W1p^T [E, d, W1]^T
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, dh, W1, cap, 1, 128) || !encode_f32(&g.tma_b, w1t, W1, d, E, 256))
+    return MOE_ERR_SHAPE;
+  g.K = static_cast<int>(W1);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dx_perm;
+  g.ld0 = d;
+  return cuda_status(launch_grouped_gemm_tf32(kDgradFc1, g, grid_for(di, desc), stream));
+}
+
+moe_status_t moe_fc1_wgrad_tf32(const moe_mlp_desc_t* desc, const void* dh_t, const void* x_t,
+                                const int32_t* counts, const int32_t* padded_offsets,
+                                void* dw1p, cudaStream_t stream) {
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (!dh_t || !x_t || !counts || !padded_offsets || !dw1p) return MOE_ERR_NULL;
+  if (!al16(dw1p)) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  if ((st = device_info(&di)) != MOE_OK) return st;
+  const uint64_t d = desc->d, W1 = fc1_width(desc->act, desc->F), cap = desc->capacity;
+  // dW1p[e] = dH^T X over the group's rows: [W1, cap] and [d, cap]
+  GemmArgs g;
+  fill_common(g, desc, di, counts, padded_offsets);
+  if (!encode_f32(&g.tma_a, dh_t, cap, W1, 1, 128) || !encode_f32(&g.tma_b, x_t, cap, d, 1, 256))
+    return MOE_ERR_SHAPE;
+  g.m_ext = static_cast<int>(W1);
+  g.n_ext = desc->d;
+  g.b_ext = desc->d;
+  g.out0 = dw1p;
+  g.ld0 = d;
+  return cuda_status(launch_grouped_gemm_tf32(kWgrad, g, grid_for(di, desc), stream));
+}
+
+}  // extern "C"
+
+namespace moe {
+namespace {
+
+moe_status_t mlp_fwd_tf32(const moe_mlp_desc_t* desc, const void* x_perm, const int32_t* counts,
+                          const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                          const void* w2, const void* b2, void* h, void* a, void* y,
+                          const moe_mx_out_t* a_mx, const moe_mx_out_t* y_mx,
+                          cudaStream_t stream) {
+  if (a_mx || y_mx) return MOE_ERR_UNSUPPORTED;
+  moe_status_t st = moe_fc1_glu_fwd_tf32(desc, x_perm, counts, padded_offsets, w1p, b1p, h, a,
+                                         nullptr, stream);
+  if (st != MOE_OK) return st;
+  return moe_fc2_fwd_tf32(desc, a, counts, padded_offsets, w2, b2, y, stream);
+}
+
+moe_status_t mlp_bwd_tf32(const moe_mlp_desc_t* desc, const void* dy, const void* x_perm,
+                          const void* h, const void* a, const int32_t* counts,
+                          const int32_t* padded_offsets, const void* w1p, const void* b1p,
+                          const void* w2, void* dh, void* dx_perm, void* dw1p, void* db1p,
+                          void* dw2, void* db2, const moe_mx_out_t* dh_mx, void* ws,
+                          size_t ws_bytes, cudaStream_t stream) {
+  (void)b1p;
+  moe_status_t st = check_f32_desc(desc);
+  if (st != MOE_OK) return st;
+  if (dh_mx) return MOE_ERR_UNSUPPORTED;
+  if (!dy || !x_perm || !h || !a || !counts || !padded_offsets || !w1p || !w2 || !dh ||
+      !dx_perm || !dw1p || !dw2)
+    return MOE_ERR_NULL;
+  if ((desc->has_b1 && !db1p) || (desc->has_b2 && !db2)) return MOE_ERR_NULL;
+  size_t need = 0;
+  if ((st = moe_workspace_size(desc, &need)) != MOE_OK) return st;
+  if (!ws || ws_bytes < need || !al16(ws)) return MOE_ERR_WORKSPACE;
+  auto r = [](size_t b) { return (b + 255) / 256 * 256; };
+  const size_t E = desc->E, d = desc->d, F = desc->F, W1 = fc1_width(desc->act, desc->F),
+               cap = desc->capacity;
+  uint8_t* p = static_cast<uint8_t*>(ws) + r(route_ws_bytes(desc) + 256);
+  void* w1t = p;  p += r(E * d * W1 * 4);
+  void* w2t = p;  p += r(E * F * d * 4);
+  void* x_t = p;  p += r(d * cap * 4);
+  void* dy_t = p; p += r(d * cap * 4);
+  void* a_t = p;  p += r(F * cap * 4);
+  void* dh_t = p;
+  const int32_t dd = desc->d, ff = desc->F;
+  if ((st = moe_transpose_weights_tf32(desc, w1p, w2, w1t, w2t, stream)) != MOE_OK ||
+      (st = moe_transpose_rows_f32(desc, x_perm, dd, padded_offsets, x_t, stream)) != MOE_OK ||
+      (st = moe_transpose_rows_f32(desc, dy, dd, padded_offsets, dy_t, stream)) != MOE_OK ||
+      (st = moe_transpose_rows_f32(desc, a, ff, padded_offsets, a_t, stream)) != MOE_OK ||
+      (st = moe_fc2_dgrad_dglu_tf32(desc, dy, h, counts, padded_offsets, w2t, dh, dh_t,
+                                    stream)) != MOE_OK ||
+      (st = moe_fc2_wgrad_tf32(desc, dy_t, a_t, counts, padded_offsets, dw2, stream)) != MOE_OK ||
+      (st = moe_fc1_dgrad_tf32(desc, dh, counts, padded_offsets, w1t, dx_perm, stream)) !=
+          MOE_OK ||
+      (st = moe_fc1_wgrad_tf32(desc, dh_t, x_t, counts, padded_offsets, dw1p, stream)) != MOE_OK)
+    return st;
+  if (desc->has_b1 || desc->has_b2)
+    st = moe_bias_grads(desc, dy, dh, counts, padded_offsets, desc->has_b1 ? db1p : nullptr,
+                        desc->has_b2 ? db2 : nullptr, stream);
+  return st;
+}
+
+}  // namespace
+}  // namespace moe

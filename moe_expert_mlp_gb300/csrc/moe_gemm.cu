@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "moe_act.cuh"
 #include "moe_internal.h"
 #include "moe_mx.cuh"
 #include "moe_ptx.cuh"
@@ -117,68 +118,6 @@ struct Tile {
   int k_row0;   // ragged K: first routed row of the group
   int num_kb;   // K blocks (64 bf16 or 128 E4M3 per block)
 };
-
-struct ActP {
-  int act;
-  float alpha, limit, lin_off, out_scale;
-};
-
-// sigmoid(x) = 1 / (1 + e^-x); the approximate reciprocal is within a few
-// ulp and returns 0 when e^-x overflows to +inf.
-__device__ __forceinline__ float sigmoid_f(float x) { return __fdividef(1.0f, 1.0f + __expf(-x)); }
-
-template <int ACT>
-__device__ __forceinline__ float glu_fwd(float g, float l, const ActP& p) {
-  const float gc = fminf(g, p.limit);
-  const float lc = fminf(fmaxf(l, -p.limit), p.limit);
-  float phi;
-  if (ACT == MOE_ACT_SWIGLU) {
-    phi = gc * sigmoid_f(p.alpha * gc);
-  } else if (ACT == MOE_ACT_GEGLU) {
-    phi = 0.5f * gc * (1.0f + erff(gc * 0.70710678118654752f));
-  } else {
-    const float r = fmaxf(gc, 0.0f);
-    phi = r * r;
-  }
-  return p.out_scale * phi * (lc + p.lin_off);
-}
-
-// Non-gated squared ReLU: A = s * max(min(h, limit), 0)^2 and its gradient
-// (the clamp passes the gradient where h <= limit).
-__device__ __forceinline__ float srelu_fwd(float h, const ActP& p) {
-  const float r = fmaxf(fminf(h, p.limit), 0.0f);
-  return p.out_scale * r * r;
-}
-
-__device__ __forceinline__ float srelu_bwd(float da, float h, const ActP& p) {
-  const float r = fmaxf(fminf(h, p.limit), 0.0f);
-  return h <= p.limit ? p.out_scale * da * 2.0f * r : 0.0f;
-}
-
-template <int ACT>
-__device__ __forceinline__ void glu_bwd(float da, float g, float l, const ActP& p, float& dg,
-                                        float& dl) {
-  const float gc = fminf(g, p.limit);
-  const float lc = fminf(fmaxf(l, -p.limit), p.limit);
-  float phi, dphi;
-  if (ACT == MOE_ACT_SWIGLU) {
-    const float s = sigmoid_f(p.alpha * gc);
-    phi = gc * s;
-    dphi = s + p.alpha * gc * s * (1.0f - s);
-  } else if (ACT == MOE_ACT_GEGLU) {
-    const float cdf = 0.5f * (1.0f + erff(gc * 0.70710678118654752f));
-    const float pdf = 0.39894228040143268f * __expf(-0.5f * gc * gc);
-    phi = gc * cdf;
-    dphi = cdf + gc * pdf;
-  } else {
-    const float r = fmaxf(gc, 0.0f);
-    phi = r * r;
-    dphi = 2.0f * r;
-  }
-  const float das = p.out_scale * da;
-  dg = (g <= p.limit) ? das * (lc + p.lin_off) * dphi : 0.0f;
-  dl = (l >= -p.limit && l <= p.limit) ? das * phi : 0.0f;
-}
 
 // The 16-column share of one chunk (see the grouped GEMM's epilogue).
 template <int ACT>

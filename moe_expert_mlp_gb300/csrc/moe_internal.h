@@ -168,6 +168,10 @@ struct GemmArgs {
   long long sfb2_atoms;
   long long sfb2_expert_bytes;
   int b2_atoms4d;
+  // TF32 path (launch_grouped_gemm_tf32): optional transposed fp32 copies
+  // [width][capacity] of out0 / out1, written by the epilogue
+  float* out0_t;
+  float* out1_t;
 };
 
 cudaError_t launch_grouped_gemm(int mode, const GemmArgs& args, int grid, cudaStream_t s);
@@ -193,5 +197,22 @@ cudaError_t launch_quant_nv(const void* in, long long batch, long long rows, lon
                             const float* amax_row, const float* amax_col, int rotate,
                             const int32_t* row_limit, int num_sms, cudaStream_t stream);
 size_t grouped_gemm_smem_bytes();
+
+// ------------------------------------------------ fp32 tensors (moe_tf32.cu)
+// The ragged-M modes (kFc1Glu, kFc1Act, kFc2, kDgradDglu, kDgradAct,
+// kDgradFc1) and kWgrad on TF32 tensor cores: fp32 operands, all K-major
+// (tma_a / tma_b: 32-value boxes, 128-byte swizzle), fp32 outputs.
+cudaError_t launch_grouped_gemm_tf32(int mode, const GemmArgs& args, int grid, cudaStream_t s);
+cudaError_t launch_combine_f32(const void* y, const int32_t* row_of, const float* w, int T, int k,
+                               int d, void* out, cudaStream_t s);
+cudaError_t launch_combine_bwd_f32(const void* dout, const void* y, const int32_t* row_of,
+                                   const float* w, int T, int k, int d, void* dy, float* dw,
+                                   cudaStream_t s);
+cudaError_t launch_group_colsum_f32(const void* g, const int32_t* counts,
+                                    const int32_t* padded_offsets, int E, int width, void* out,
+                                    cudaStream_t s);
+// out[b][c][r] = in[b][r][c] for r < rows (and r < *row_limit when given).
+cudaError_t launch_transpose_f32(const void* in, long long batch, long long rows, long long cols,
+                                 void* out, const int32_t* row_limit, cudaStream_t s);
 
 }  // namespace moe

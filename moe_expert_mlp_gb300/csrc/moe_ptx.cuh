@@ -241,6 +241,29 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       : "memory");
 }
 
+// Instruction descriptor for kind::tf32: fp32 operands in shared memory,
+// both K-major, of which the tensor core uses the TF32 part (sign, 8-bit
+// exponent, 10-bit mantissa); fp32 accumulate.  A/B format code 2 = TF32.
+__host__ __device__ constexpr uint32_t idesc_tf32(int M, int N) {
+  return (1u << 4)                          // D format: f32
+         | (2u << 7)                        // A format: tf32
+         | (2u << 10)                       // B format: tf32
+         | (static_cast<uint32_t>(N >> 3) << 17)
+         | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, one K=8 step (32 bytes of each row, as
+// one K=16 bf16 step), issued by one thread.
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // ------------------------------------------ MXFP8 block-scaled MMA
 // Shared-memory descriptor of an unswizzled K-major matrix (layout code 0):
 // 8-row core matrices of 16-byte rows; lbo / sbo are the strides between

@@ -31,6 +31,13 @@ class MoEExpertMLP:
         # dtype "nvfp4": packed E2M1 operands with UE4M3 scales per 16
         # elements and per-tensor encode scales from their amax
         self.nv = dtype == "nvfp4"
+        # dtype "fp32": fp32 tensors throughout, GEMMs on the TF32 tensor
+        # cores; the backward reads transposed copies (weights transposed
+        # once per load, A and dH^T by their epilogues, x_perm and dY by a
+        # transpose pass)
+        self.f32 = dtype == "fp32"
+        if self.f32 and recompute_h:
+            raise ValueError("recompute_h is not supported with fp32 tensors")
         # optional fused NVFP4-preparation outputs (per-tensor amax of A and
         # of dH, plain and Hadamard-rotated): float[2] device tensors or None
         self.amax_a = None
@@ -59,6 +66,9 @@ class MoEExpertMLP:
         self.capacity = cap
         dev = torch.device(device)
         bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+        if self.f32:
+            bf = f32          # every activation, weight and gradient tensor
+        self.act_dtype = bf
 
         def z(*shape, dtype=bf):
             return torch.zeros(shape, dtype=dtype, device=dev)
@@ -95,6 +105,13 @@ class MoEExpertMLP:
         self.dx = z(max(T, 1), d)
         self.dlogits = z(max(T, 1), E, dtype=f32)
         self.ws = torch.zeros(max(L.moe_workspace_size(self.desc), 256), dtype=torch.uint8, device=dev)
+        if self.f32:
+            self.w1t = z(E, d, self.W1)
+            self.w2t = z(E, F, d)
+            self.x_t = z(d, cap)
+            self.a_t = z(F, cap)
+            self.dy_t = z(d, cap)
+            self.dh_t = z(self.W1, cap)
         if self.mx:
             # activations: rowwise for the GEMM that contracts over features,
             # transposed for the weight gradient that contracts over rows
@@ -167,6 +184,8 @@ class MoEExpertMLP:
             self.b2.copy_(b2)
         if self.mx or self.nv:
             self.quantize_weights(stream)
+        if self.f32:
+            L.moe_transpose_weights_tf32(self.desc, self.w1p, self.w2, self.w1t, self.w2t, stream)
 
     def quantize_weights(self, stream=None):
         """MXFP8 / NVFP4 weight copies (rowwise and transposed) from the bf16
@@ -180,7 +199,7 @@ class MoEExpertMLP:
         """Packed [E,2F_pad,width] -> logical [E,2F,width] (e.g. dW1p, db1p);
         [E,F,width] unchanged for the non-gated activation."""
         n1 = 2 * self.F if self.gated else self.F
-        out = torch.empty((self.E, n1, width), dtype=torch.bfloat16, device=packed.device)
+        out = torch.empty((self.E, n1, width), dtype=self.act_dtype, device=packed.device)
         L.moe_unpack_fc1(self.desc, packed, out, width, stream)
         return out
 
@@ -243,6 +262,15 @@ class MoEExpertMLP:
 
     def mlp_forward(self, stream=None, timer=None, a_mx=None, y_mx=None):
         c, po = self.counts, self.padded_offsets
+        if self.f32:
+            with self._t(timer, "transpose_x"):
+                L.moe_transpose_rows_f32(self.desc, self.x_perm, self.d, po, self.x_t, stream)
+            with self._t(timer, "fc1_glu_fwd"):
+                L.moe_fc1_glu_fwd_tf32(self.desc, self.x_perm, c, po, self.w1p, self.b1p, self.h,
+                                       self.a, self.a_t, stream)
+            with self._t(timer, "fc2_fwd"):
+                L.moe_fc2_fwd_tf32(self.desc, self.a, c, po, self.w2, self.b2, self.y, stream)
+            return
         if a_mx is None and self.amax_a is not None and not self.mx:
             a_mx = dict(amax=self.amax_a)
         if self.nv:
@@ -277,6 +305,23 @@ class MoEExpertMLP:
 
     def mlp_backward(self, stream=None, timer=None, dh_mx=None):
         c, po = self.counts, self.padded_offsets
+        if self.f32:
+            with self._t(timer, "transpose_dy"):
+                L.moe_transpose_rows_f32(self.desc, self.dy, self.d, po, self.dy_t, stream)
+            with self._t(timer, "fc2_dgrad_dglu"):
+                L.moe_fc2_dgrad_dglu_tf32(self.desc, self.dy, self.h, c, po, self.w2t, self.dh,
+                                          self.dh_t, stream)
+            with self._t(timer, "fc2_wgrad"):
+                L.moe_fc2_wgrad_tf32(self.desc, self.dy_t, self.a_t, c, po, self.dw2, stream)
+            with self._t(timer, "fc1_dgrad"):
+                L.moe_fc1_dgrad_tf32(self.desc, self.dh, c, po, self.w1t, self.dx_perm, stream)
+            with self._t(timer, "fc1_wgrad"):
+                L.moe_fc1_wgrad_tf32(self.desc, self.dh_t, self.x_t, c, po, self.dw1p, stream)
+            if self.has_b1 or self.has_b2:
+                with self._t(timer, "bias_grads"):
+                    L.moe_bias_grads(self.desc, self.dy, self.dh, c, po, self.db1p, self.db2,
+                                     stream)
+            return
         if dh_mx is None and self.amax_dh is not None and not self.mx:
             dh_mx = dict(amax=self.amax_dh)
         if self.nv:
@@ -480,9 +525,10 @@ class MoEExpertMLP:
         """Kernels of this library launched by one step() (routed) or
         grouped_step(): six grouped GEMMs, one column-sum per bias, the two
         activation quantizations of the MXFP8 layer (NVFP4: four quantizations
-        and two amax passes), and for
+        and two amax passes; fp32: the transposes of x_perm and dY), and for
         the routed layer top-k, group offsets + assignment (one launch),
         gather, combine, pad-row zeroing, combine backward, permute backward
         and router backward."""
-        n = 6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0) + (6 if self.nv else 0)
+        n = (6 + int(self.has_b1) + int(self.has_b2) + (2 if self.mx else 0) + (6 if self.nv else 0)
+             + (2 if self.f32 else 0))
         return n + (8 if routed else 0)

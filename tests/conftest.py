@@ -31,7 +31,8 @@ def read_golden(path):
 
 
 def pytest_terminal_summary(terminalreporter):
-    """Print the achieved error ratios of the MXFP8 parity checks (max
+    """Print the achieved error ratios of the fp32 / TF32 checks and of the
+    MXFP8 parity checks (max
     |gpu - ref| / max |ref| against the oracle with the same quantization,
     relative Frobenius error against the unquantized oracle) when any were
     recorded."""
@@ -39,9 +40,15 @@ def pytest_terminal_summary(terminalreporter):
         from tests import harness
     except ImportError:
         return
+    tr = terminalreporter
+    if harness.TF32_RATIOS:
+        tr.write_line("fp32 path on TF32 tensor cores: max|gpu-ref|/max|ref| against the fp64 "
+                      "oracle (bound 1e-2 + 1e-3/max|ref|):")
+        for name, r in harness.TF32_RATIOS:
+            tr.write_line(f"  {name}: {r:.2e}")
+        tr.write_line(f"  worst: {max(r for _, r in harness.TF32_RATIOS):.2e}")
     if not harness.MX_RATIOS:
         return
-    tr = terminalreporter
     tr.write_line("MXFP8 parity: max|gpu-ref|/max|ref| against the oracle with the same "
                   "quantization (bound 1e-2) / relative Frobenius error against the "
                   "unquantized oracle (bound 1e-1):")

@@ -99,3 +99,39 @@ def test_noalloc_size_limit_boundary(libmoe):
     assert libmoe.moe_route_permute_noalloc(ctypes.byref(over), *([null] * 13)) == 4
     assert libmoe.moe_route_permute_noalloc(ctypes.byref(at), *([null] * 13)) in (1, 6)
     assert libmoe.moe_route_permute_noalloc(None, *([null] * 13)) == 1
+
+
+def test_fp32_calls_reject_bad_arguments_without_gpu(libmoe):
+    """The fp32 / TF32 calls check the descriptor and pointers on the host:
+    the bf16 GEMM calls refuse an fp32 descriptor and the *_tf32 calls a
+    bf16 one (MOE_ERR_UNSUPPORTED), recompute_h is refused with fp32,
+    missing buffers give MOE_ERR_NULL and a misaligned output
+    MOE_ERR_SHAPE.  The fp32 workspace adds the backward's transposed
+    operands: W1p^T, W2^T, x_perm^T, dY^T, A^T and dH^T in fp32."""
+    import ctypes
+    import moe_expert_mlp_gb300 as m
+    null = ctypes.c_void_p(None)
+    E, d, F, cap = 4, 128, 96, 1024
+    f32 = m.make_desc(T=0, E=E, k=1, d=d, F=F, dtype="fp32", capacity=cap)
+    bf16 = m.make_desc(T=0, E=E, k=1, d=d, F=F, capacity=cap)
+    assert libmoe.moe_fc1_glu_fwd(ctypes.byref(f32), *([null] * 9)) == 3
+    assert libmoe.moe_fc2_wgrad(ctypes.byref(f32), *([null] * 6)) == 3
+    assert libmoe.moe_quantize_act_mx(ctypes.byref(f32), null, 128, null, null, null) == 3
+    assert libmoe.moe_fc1_glu_fwd_tf32(ctypes.byref(bf16), *([null] * 9)) == 3
+    rc = m.make_desc(T=0, E=E, k=1, d=d, F=F, dtype="fp32", capacity=cap, recompute_h=True)
+    assert libmoe.moe_fc2_fwd_tf32(ctypes.byref(rc), *([null] * 7)) == 3
+    assert libmoe.moe_fc2_fwd_tf32(ctypes.byref(f32), *([null] * 7)) == 1
+    assert libmoe.moe_fc1_wgrad_tf32(ctypes.byref(f32), *([null] * 6)) == 1
+    assert libmoe.moe_transpose_weights_tf32(ctypes.byref(f32), *([null] * 5)) == 1
+    assert libmoe.moe_transpose_rows_f32(ctypes.byref(f32), null, 128, null, null, null) == 1
+    p = ctypes.c_void_p(4096)                      # never dereferenced on the host
+    odd = ctypes.c_void_p(4100)                    # not 16-byte aligned
+    assert libmoe.moe_fc2_fwd_tf32(ctypes.byref(f32), p, p, p, p, null, odd, null) == 2
+    n_f32, n_bf16 = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    assert libmoe.moe_workspace_size(ctypes.byref(f32), ctypes.byref(n_f32)) == 0
+    assert libmoe.moe_workspace_size(ctypes.byref(bf16), ctypes.byref(n_bf16)) == 0
+    W1 = 2 * 128                                   # 2 * F_pad
+    r = lambda b: (b + 255) // 256 * 256
+    extra = (r(E * d * W1 * 4) + r(E * F * d * 4) + 2 * r(d * cap * 4) + r(F * cap * 4)
+             + r(W1 * cap * 4))
+    assert n_f32.value == r(n_bf16.value) + extra
