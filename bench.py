@@ -18,10 +18,12 @@ a barrier + synchronize on both sides.  value = algorithmic TFLOPS
 (18*d*F per routed row, padding not counted) of the whole job.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload NAME] [--dtype bf16|mxfp8|nvfp4]
+                  [--workload NAME] [--dtype bf16|mxfp8|nvfp4|fp32]
 
-The JSON line also carries: `roofline` (the GEMM with the largest time
-against the measured peak of its operand type, with the DRAM traffic of an
+The JSON line also carries: `roofline` (the GEMM with the largest time,
+against the roof that bounds it: its FLOPs over the measured tensor peak of
+its operand type or its algorithmic bytes over the measured HBM bandwidth,
+whichever takes longer, with both fractions given and the DRAM traffic of an
 ncu capture of the same kernel source), `attainable` (the whole step against
 max(FLOP / peak, algorithmic bytes / measured HBM bandwidth)), `e2e` (the
 same steps through the public API with host-resident inputs and results,
@@ -82,7 +84,7 @@ def load_peaks():
 
 def gemm_source_hash():
     h = hashlib.sha256()
-    for fn in ("moe_gemm.cu", "moe_ptx.cuh", "moe_internal.h", "moe_mx.cuh"):
+    for fn in ("moe_gemm.cu", "moe_ptx.cuh", "moe_internal.h", "moe_mx.cuh", "moe_act.cuh"):
         with open(os.path.join(ROOT, "moe_expert_mlp_gb300", "csrc", fn), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -99,7 +101,8 @@ def host_cores():
 def call_work(wl, name, R, dtype="bf16"):
     """Algorithmic FLOPs or bytes of one library call over R real routed rows.
     GEMMs: 2*M*N*K with M = routed rows.  Memory-bound calls: bytes of the
-    tensors they must read and write once (bf16 rows, index arrays ignored)."""
+    tensors they must read and write once (bf16 rows, fp32 on the fp32 path;
+    index arrays ignored)."""
     d, F, T, k = wl.d, wl.F, wl.T, wl.k
     n1 = 2 * F if wl.gated else F          # FC1 outputs (gate + linear halves when gated)
     gemm = {
@@ -131,12 +134,46 @@ def call_work(wl, name, R, dtype="bf16"):
         mem.update(route_permute=mem["route_permute"] + R * d * q,
                    combine_bwd=mem["combine_bwd"] + R * d * q,
                    quant_x=R * d * (2 + q), quant_dy=R * d * (2 + q))
+    if dtype == "fp32":
+        # fp32 rows (twice the bytes); the transposes of x_perm and dY read
+        # and write them once
+        mem = {key: 2.0 * v for key, v in mem.items() if key not in ("quant_x", "quant_dy")}
+        mem.update(route_permute=T * wl.E * 4 + T * d * 4 + R * d * 4, route_bwd=T * k * 12 + T * wl.E * 4,
+                   transpose_x=R * d * 8, transpose_dy=R * d * 8)
     if dtype == "nvfp4":
         # bf16 rows in; rowwise and rotated transposed E2M1 codes (half a
         # byte each) + one scale per 16 out; x and dY also read once for amax
         mem.update(quant_x=R * d * (2 + 2 + 1 + 2 / 16), quant_dy=R * d * (2 + 2 + 1 + 2 / 16),
                    quant_a=R * F * (2 + 1 + 2 / 16), quant_dh=R * n1 * (2 + 1 + 2 / 16))
     return "byte", float(mem.get(name, 0.0))
+
+
+def gemm_bytes(wl, name, R, dtype="bf16", keep_bf16=False):
+    """Algorithmic HBM bytes of one grouped GEMM call: its operands read once
+    and its outputs written once (R real rows; padding ignored).  Operands
+    are bf16 (2 bytes), fp32 (4) or MXFP8 codes with a scale per 32
+    (1 + 1/32); the transposed copies the backward reads are the same size.
+    Outputs: H, Y, dX and dW in bf16 (fp32 on the fp32 path); A and dH as
+    their two MXFP8 copies on the MXFP8 path (plus the bf16 tensor when
+    keep_bf16), in bf16 otherwise, with the fp32 path's transposed A and dH
+    counted too."""
+    d, F, E = wl.d, wl.F, wl.E
+    n1 = 2 * F if wl.gated else F
+    q = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16, "fp32": 4.0}[dtype]
+    o = 4.0 if dtype == "fp32" else 2.0                    # stored bf16 / fp32 element
+    if dtype in ("mxfp8", "nvfp4"):
+        act_out = 2 * q + (2.0 if keep_bf16 else 0.0)      # rowwise + transposed copies
+    else:
+        act_out = 2 * o if dtype == "fp32" else o          # fp32: plus the transposed copy
+    b = {
+        "fc1_glu_fwd": R * d * q + E * n1 * d * q + R * n1 * o + R * F * act_out,
+        "fc2_fwd": R * F * q + E * d * F * q + R * d * o,
+        "fc2_dgrad_dglu": R * d * q + E * d * F * q + R * n1 * o + R * n1 * act_out,
+        "fc2_wgrad": R * d * q + R * F * q + E * d * F * o,
+        "fc1_dgrad": R * n1 * q + E * n1 * d * q + R * d * o,
+        "fc1_wgrad": R * n1 * q + R * d * q + E * n1 * d * o,
+    }
+    return float(b[name])
 
 
 def step_bytes(wl, dtype="bf16"):
@@ -155,10 +192,21 @@ def step_bytes(wl, dtype="bf16"):
     n1 = 2 * F if wl.gated else F
     R = wl.routed_rows
     w_el = E * (n1 * d + d * F)
-    q = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16}[dtype]
+    q = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16, "fp32": 4.0}[dtype]
     b = 2.0 * w_el * (2.0 if dtype == "bf16" else q)      # two GEMMs per weight
-    b += 2.0 * w_el                                       # dW in bf16
-    if dtype == "bf16":
+    b += (4.0 if dtype == "fp32" else 2.0) * w_el         # dW in bf16 (fp32)
+    if dtype == "fp32":
+        # every weight-gradient GEMM reads transposed copies: x_perm and dY
+        # transposed by a pass (read + write), A^T and dH^T written by their
+        # epilogues; the transposed weights are made outside the step
+        per_row = 4 * (5 * d        # x_perm: written, FC1, transpose; x^T written, FC1 wgrad
+                       + 2 * n1     # H: FC1 writes, dGLU reads
+                       + 4 * F      # A and A^T: written, read by FC2 / FC2 wgrad
+                       + 2 * d      # Y
+                       + 5 * d      # dY: written, FC2 dgrad, transpose; dY^T written, wgrad
+                       + 4 * n1     # dH and dH^T: written, read by FC1 dgrad / FC1 wgrad
+                       + 2 * d)     # dX_perm
+    elif dtype == "bf16":
         per_row = 2 * (3 * d        # x_perm: written (permute or input), FC1, FC1 wgrad
                        + 2 * n1     # H: FC1 writes, dGLU reads
                        + 3 * F      # A: FC1 writes, FC2 and FC2 wgrad read
@@ -177,7 +225,7 @@ def step_bytes(wl, dtype="bf16"):
                    + 2 * 2 * d)                                    # dX_perm
     b += R * per_row
     if wl.router != "direct":
-        b += wl.T * 4 * d * 2 + wl.T * wl.E * 4 * 2               # x, out, dOut, dx; logits
+        b += wl.T * 4 * d * (4 if dtype == "fp32" else 2) + wl.T * wl.E * 4 * 2   # x, out, dOut, dx; logits
     return float(b)
 
 
@@ -419,7 +467,8 @@ def run_ours(args, wl):
     from moe_expert_mlp_gb300 import MoEExpertMLP, moe_read_device_status
 
     def bits_to_dev(bits, device):
-        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+        return t.float() if args.dtype == "fp32" else t    # fp32 layer: the same values in fp32
 
     inp = make_inputs(wl)
     routed = wl.router != "direct"
@@ -557,13 +606,13 @@ def run_ours(args, wl):
 
     # fused vs unfused expert MLP (same kernels, activation as its own pass)
     fusion = None
-    if not args.no_fusion and args.dtype != "nvfp4" and wl.gated:
+    if not args.no_fusion and args.dtype not in ("nvfp4", "fp32") and wl.gated:
         fusion = measure_fusion(torch, layer, K)
     overlap = None
-    if args.overlap and not mx:
+    if args.overlap and not mx and args.dtype != "fp32":
         overlap = measure_overlap(torch, layer)
     router = None
-    if routed and not args.no_router:
+    if routed and not args.no_router and args.dtype != "fp32":
         router = measure_router(torch, layer, x, logits, bias)
 
     # end-to-end: host buffers in pinned memory, copies inside the timed region
@@ -598,6 +647,7 @@ def run_ours(args, wl):
     kind, work = call_work(wl, dominant, R, args.dtype)
     dom_avg = sum(per[dominant]) / len(per[dominant])
     achieved = work / (dom_avg * 1e-3) / 1e12
+    dom_bytes = gemm_bytes(wl, dominant, R, args.dtype, keep_bf16=getattr(layer, "keep_bf16", False))
     peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
     peak_note = f"{peak_src} bf16 burst (cuBLAS)"
     if args.dtype == "mxfp8":   # no measured FP8 figure: bf16 measured x nominal FP8/BF16 (2)
@@ -606,10 +656,13 @@ def run_ours(args, wl):
     elif args.dtype == "nvfp4":  # bf16 measured x the nominal FP4/BF16 dense ratio (13.5/2.25)
         peak *= 6.0
         peak_note = f"{peak_src} bf16 burst (cuBLAS) x 6, the nominal FP4/BF16 dense ratio"
+    elif args.dtype == "fp32":   # TF32 MMA: bf16 measured x the nominal TF32/BF16 ratio (1.1/2.25)
+        peak *= 1100.0 / 2250.0
+        peak_note = f"{peak_src} bf16 burst (cuBLAS) x 1.1/2.25, the nominal TF32/BF16 dense ratio"
     # attainable-roofline view of the whole step: max(FLOP / tensor peak,
     # algorithmic bytes / measured HBM bandwidth), and the nominal peak
     hbm = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
-    nominal = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 13500.0}[args.dtype]
+    nominal = {"bf16": 2250.0, "mxfp8": 4500.0, "nvfp4": 13500.0, "fp32": 1100.0}[args.dtype]
     sb = step_bytes(wl, args.dtype)
     t_tc, t_hbm = flops_step / (peak * 1e12) * 1e3, sb / (hbm * 1e9) * 1e3
     attainable = {"bytes_per_step": round(sb), "t_tensor_ms": round(t_tc, 4),
@@ -619,6 +672,21 @@ def run_ours(args, wl):
                   "nominal_peak_tflops": nominal, "hbm_gbs": hbm}
     tr = NCU_TRAFFIC.get((dominant, wl.name, args.dtype))
     traffic = tr["bytes"] if tr and tr.get("src") == gemm_source_hash() else None
+    # the dominant GEMM against both roofs; the one that takes longer bounds it
+    gbs = dom_bytes / (dom_avg * 1e-3) / 1e9
+    t_tc_dom, t_hbm_dom = work / (peak * 1e12), dom_bytes / (hbm * 1e9)
+    tensor_roof = {"achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                   "frac": round(achieved / peak, 4), "peak_source": peak_note}
+    hbm_roof = {"achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(gbs / hbm, 4), "bytes": round(dom_bytes),
+                "peak_source": f"{peak_src} copy bandwidth"}
+    if t_hbm_dom > t_tc_dom:
+        roofline = dict(bound="hbm", kernel=dominant, **{k: v for k, v in hbm_roof.items()
+                                                         if k != "bytes"})
+    else:
+        roofline = dict(bound="tensor", kernel=dominant, **tensor_roof)
+    roofline.update(traffic=traffic, algorithmic_bytes=round(dom_bytes), tensor=tensor_roof,
+                    hbm=hbm_roof)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOPS", "n_gpus": world,
         "steps": K, "warmup": W, "ms_per_step": round(ms_step, 5), "higher_is_better": True,
@@ -629,9 +697,7 @@ def run_ours(args, wl):
         "tokens_per_s": round(job_rate(wl.T if routed else R, K, world, ms_max), 1),
         "pct_of_tc_peak": round(100.0 * value / world / peak, 2),
         "attainable": attainable,
-        "roofline": {"bound": "tensor", "kernel": dominant, "achieved": round(achieved, 2),
-                     "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-                     "traffic": traffic, "peak_source": peak_note},
+        "roofline": roofline,
         "kernels": kernels,
         "gpu_launches": layer.kernels_per_step(routed) * K,
         "weight_prep_ms": round(weight_prep_ms, 4),
@@ -820,9 +886,10 @@ def run_e2e(torch, layer, inp, dev, K, W, flops_step, world, dist):
     neighbouring steps' kernels); also reported: the same copies issued in
     line, one step after another, on one stream."""
     from moe_expert_mlp_gb300.pipeline import HostStepPipeline
-    xh = torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    host = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(layer.act_dtype)
+    xh = host(inp["x"]).pin_memory()
     lh = torch.from_numpy(inp["logits"]).pin_memory()
-    dh = torch.from_numpy(inp["dout"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    dh = host(inp["dout"]).pin_memory()
     bias = torch.from_numpy(inp["bias"]).to(dev) if inp["bias"] is not None else None
     xd, ld, dd = (torch.empty_like(t, device=dev) for t in (xh, lh, dh))
     outs = [dict(out=torch.empty(layer.out.shape, dtype=layer.out.dtype).pin_memory(),
@@ -880,11 +947,11 @@ def run_e2e_grouped(torch, layer, inp, dev, K, W, flops_step, world, dist):
     kernels); also reported: the same copies issued in line on one stream."""
     from moe_expert_mlp_gb300.pipeline import GroupedHostStepPipeline
     R, d = int(inp["group_sizes"].sum()), layer.d
-    host_in = dict(x=torch.from_numpy(inp["x"].view(np.int16)).view(torch.bfloat16).pin_memory(),
-                   dy=torch.from_numpy(inp["dout"].view(np.int16)).view(torch.bfloat16).pin_memory(),
+    host = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).to(layer.act_dtype)
+    host_in = dict(x=host(inp["x"]).pin_memory(), dy=host(inp["dout"]).pin_memory(),
                    counts=torch.from_numpy(inp["group_sizes"].astype(np.int32)).pin_memory())
-    outs = [dict(y=torch.empty((R, d), dtype=torch.bfloat16).pin_memory(),
-                 dx=torch.empty((R, d), dtype=torch.bfloat16).pin_memory()) for _ in range(2)]
+    outs = [dict(y=torch.empty((R, d), dtype=layer.act_dtype).pin_memory(),
+                 dx=torch.empty((R, d), dtype=layer.act_dtype).pin_memory()) for _ in range(2)]
     pipe = GroupedHostStepPipeline(layer, dev)
     segs = pipe._segments(inp["group_sizes"])
     cnt_dev = torch.zeros_like(layer.counts)
@@ -964,9 +1031,10 @@ def main():
     ap.add_argument("--ref-sample-tokens", type=int, default=None,
                     help="the same for each step of --impl reference (default 256 tokens, or "
                          "the smallest expert)")
-    ap.add_argument("--dtype", choices=["bf16", "mxfp8", "nvfp4"], default=DEFAULT_DTYPE,
+    ap.add_argument("--dtype", choices=["bf16", "mxfp8", "nvfp4", "fp32"], default=DEFAULT_DTYPE,
                     help="GEMM operand type (mxfp8: E4M3 + E8M0 block scales; nvfp4: E2M1 + "
-                         "UE4M3 scales per 16 + per-tensor scales)")
+                         "UE4M3 scales per 16 + per-tensor scales; fp32: fp32 tensors, TF32 "
+                         "tensor-core GEMMs)")
     ap.add_argument("--act", choices=["swiglu", "geglu", "sreglu", "srelu"], default=None,
                     help="override the workload's activation (the dense sweep)")
     ap.add_argument("--amax", action="store_true",

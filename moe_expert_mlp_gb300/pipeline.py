@@ -27,7 +27,7 @@ class HostStepPipeline:
         self.layer = layer
         dev = torch.device(device) if device is not None else layer.w2.device
         T, E, d = max(layer.T, 1), layer.E, layer.d
-        bf, f32 = torch.bfloat16, torch.float32
+        bf, f32 = layer.act_dtype, torch.float32
         self.inp = [dict(x=torch.empty((T, d), dtype=bf, device=dev),
                          logits=torch.empty((T, E), dtype=f32, device=dev),
                          dout=torch.empty((T, d), dtype=bf, device=dev)) for _ in range(2)]
@@ -113,7 +113,7 @@ class GroupedHostStepPipeline:
         self.layer = layer
         dev = torch.device(device) if device is not None else layer.w2.device
         cap, d, E = layer.capacity, layer.d, layer.E
-        bf = torch.bfloat16
+        bf = layer.act_dtype
         self.sets = [dict(x_perm=layer.x_perm, dy=layer.dy, y=layer.y, dx_perm=layer.dx_perm)]
         self.sets.append({k: torch.zeros((cap, d), dtype=bf, device=dev)
                           for k in ("x_perm", "dy", "y", "dx_perm")})

@@ -238,11 +238,12 @@ def test_zero_tokens_and_all_groups_empty():
 
 
 def test_tiny_fp32_inputs_within_bf16_tolerance():
-    """The fp32 configuration (tiny layer): the oracle runs on the fp32
-    inputs themselves, the GPU on their bf16 roundings (the path computes in
-    bf16 with fp32 accumulation; there is no TF32 path); routing, decided on
-    the identical fp32 logits, is bit-exact, and every float output is
-    within the bf16 tolerance of the fp32-input oracle."""
+    """The fp32 configuration (tiny layer) through the bf16 layer: the
+    oracle runs on the fp32 inputs themselves, the GPU on their bf16
+    roundings (bf16 storage, fp32 accumulation); routing, decided on the
+    identical fp32 logits, is bit-exact, and every float output is within
+    the bf16 tolerance of the fp32-input oracle.  (The fp32 layer on the
+    TF32 tensor cores is tested in test_gpu_tf32.py.)"""
     from workloads import make_inputs_fp32
     wl = WORKLOADS["tiny_t256_e8"]
     f = make_inputs_fp32(wl)
