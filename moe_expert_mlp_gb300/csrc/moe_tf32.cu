@@ -15,7 +15,7 @@
 // "Accelerating dropless MoE training with JAX and NVIDIA Transformer
 // Engine", "Claims and evidence": one grouped GEMM over ragged groups.
 //
-// Design (one CTA per SM, 6 warps, tiles of 128 rows x 256 columns):
+// Design (one CTA per SM, 10 warps, tiles of 128 rows x 256 columns):
 //   warp 0    TMA producer: K-major fp32 operand tiles, 32 values (one
 //             128-byte swizzled row) per operand row and stage, into a ring
 //             of 4 stages (48 KB each).
@@ -23,11 +23,12 @@
 //             tcgen05.mma kind::tf32 (the same 32 bytes per row per step as
 //             a bf16 K=16 step); two 256-column fp32 accumulators, so the
 //             epilogue of one tile overlaps the MMAs of the next.
-//   warps 2-5 epilogue, one per TMEM lane quarter: tcgen05.ld of 32 columns
-//             at a time, the fused math, fp32 stores.  A thread owns one
-//             output row and writes its 32 values as 128 contiguous bytes;
-//             the optional transposed copies are written one column per
-//             store, 32 consecutive rows = 128 contiguous bytes per warp.
+//   warps 2-9 epilogue, two per TMEM lane quarter, each taking 16 of every
+//             32 accumulator columns (tcgen05.ld of 16 columns), the fused
+//             math, fp32 stores.  A thread owns one output row and writes
+//             its 16 values of a chunk as 64 contiguous bytes; the optional
+//             transposed copies are written one column per store, 32
+//             consecutive rows = 128 contiguous bytes per warp.
 // Every operand is K-major: the backward reads transposed weight copies and
 // transposed activations (A and dH transposed by the epilogues that produce
 // them, x_perm and dY by k_transpose_f32).  Tiles whose 128 rows are all
@@ -52,8 +53,8 @@ constexpr int T_STAGES = 4;
 constexpr int TA_BYTES = TM * TK * 4;           // 16 KB
 constexpr int TB_BYTES = TN * TK * 4;           // 32 KB
 constexpr int T_STAGE_BYTES = TA_BYTES + TB_BYTES;
-constexpr int T_THREADS = 192;                  // producer, MMA, 4 epilogue warps
-constexpr int T_EPI_WARPS = 4;
+constexpr int T_THREADS = 320;                  // producer, MMA, 8 epilogue warps
+constexpr int T_EPI_WARPS = 8;
 constexpr int T_TMEM_COLS = 2 * TN;
 constexpr size_t T_SMEM_BYTES = 1024 + static_cast<size_t>(T_STAGES) * T_STAGE_BYTES;
 
@@ -97,17 +98,17 @@ __device__ __forceinline__ TTile tf32_tile(int t, int n_tiles, int m_tiles, cons
   return ti;
 }
 
-__device__ __forceinline__ void store_f32x32(float* dst, const float (&v)[32]) {
+__device__ __forceinline__ void store_f32x16(float* dst, const float (&v)[16]) {
   float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
+  for (int i = 0; i < 4; ++i)
     d4[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
 }
 
-__device__ __forceinline__ void load_f32x32(const float* src, float (&v)[32]) {
+__device__ __forceinline__ void load_f32x16(const float* src, float (&v)[16]) {
   const float4* s4 = reinterpret_cast<const float4*>(src);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
+  for (int i = 0; i < 4; ++i) {
     const float4 w = __ldg(s4 + i);
     v[4 * i] = w.x;
     v[4 * i + 1] = w.y;
@@ -116,27 +117,27 @@ __device__ __forceinline__ void load_f32x32(const float* src, float (&v)[32]) {
   }
 }
 
-// Column c0 + i of this thread's row r, for the 32 values, into the
-// transposed copy [width][ld]: lane i of the warp holds row r = r0 + i, so
-// each store instruction writes 32 consecutive floats.
-__device__ __forceinline__ void store_t_f32x32(float* dst_t, long long ld, int c0, int r,
-                                               const float (&v)[32]) {
+// Column c0 + i of this thread's row r, for the 16 values, into the
+// transposed copy [width][ld]: lane j of the warp holds row r0 + j, so each
+// store instruction writes 32 consecutive floats.
+__device__ __forceinline__ void store_t_f32x16(float* dst_t, long long ld, int c0, int r,
+                                               const float (&v)[16]) {
 #pragma unroll
-  for (int i = 0; i < 32; ++i) dst_t[static_cast<long long>(c0 + i) * ld + r] = v[i];
+  for (int i = 0; i < 16; ++i) dst_t[static_cast<long long>(c0 + i) * ld + r] = v[i];
 }
 
-// The 32 accumulator columns [col, col + 32) of this warp's lane quarter as
+// The 16 accumulator columns [col, col + 16) of this warp's lane quarter as
 // floats (zeros when the tile had no MMA).  Whole warp calls.
-__device__ __forceinline__ void acc_load(uint32_t taddr, bool have, float (&v)[32]) {
-  uint32_t r[32];
+__device__ __forceinline__ void acc_load(uint32_t taddr, bool have, float (&v)[16]) {
+  uint32_t r[16];
   if (have) {
-    tmem_ld32(taddr, r);
-    tmem_ld_wait(r);
+    tmem_ld16(taddr, r);
+    tmem_ld_wait16(r);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
   } else {
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+    for (int i = 0; i < 16; ++i) v[i] = 0.0f;
   }
 }
 
@@ -275,6 +276,7 @@ __global__ void __launch_bounds__(T_THREADS, 1)
   } else {
     // ============================== epilogue ==============================
     const int quarter = warp & 3;               // TMEM lanes 32*quarter .. +31
+    const int hc = 16 * ((warp - 2) >> 2);      // this warp's 16 of every 32 columns
     const ActP ap{args.act, args.alpha, args.limit, args.lin_off, args.out_scale};
     const long long cap = args.capacity;
     float* out0 = static_cast<float*>(args.out0);
@@ -288,7 +290,7 @@ __global__ void __launch_bounds__(T_THREADS, 1)
       if (!mbar_wait(&tfull_bar[acc], use & 1u, args.status, abort_flag)) break;
       tc_fence_after();
       const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN;
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + acc * TN + hc;
       const bool have = ti.nkb > 0;             // warp-uniform
       const int r = ti.m0 + quarter * 32 + lane;
       const float* bias = static_cast<const float*>(args.bias);
@@ -298,64 +300,64 @@ __global__ void __launch_bounds__(T_THREADS, 1)
         // dW[e] rows m0.., columns n0..; rows past m_ext are not stored
         float* dst = out0 + (static_cast<long long>(ti.e) * args.m_ext + r) * args.ld0;
         for (int c = 0; c < TN / 32 && ti.n0 + 32 * c < args.n_ext; ++c) {
-          float v[32];
+          float v[16];
           acc_load(tbase + 32 * c, have, v);
-          if (r < args.m_ext) store_f32x32(dst + ti.n0 + 32 * c, v);
+          if (r < args.m_ext) store_f32x16(dst + ti.n0 + 32 * c + hc, v);
         }
       } else {
         const bool live = have && (r - s_off[ti.e]) < cnt[ti.e];   // a real row of the group
         if (MODE == kFc1Glu) {
           // columns 0..127 gate, 128..255 linear halves of 128 GLU features
           for (int c = 0; c < 4; ++c) {
-            float g[32], l[32], a[32];
+            float g[16], l[16], a[16];
             acc_load(tbase + 32 * c, have, g);
             acc_load(tbase + 128 + 32 * c, have, l);
-            const int cg = ti.n0 + 32 * c, cl = cg + 128;
+            const int cg = ti.n0 + 32 * c + hc, cl = cg + 128;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               g[i] = live ? g[i] + (bias ? bias[cg + i] : 0.0f) : 0.0f;
               l[i] = live ? l[i] + (bias ? bias[cl + i] : 0.0f) : 0.0f;
               a[i] = live ? glu_fwd<ACT>(g[i], l[i], ap) : 0.0f;
             }
             if (out0) {
-              store_f32x32(out0 + r * args.ld0 + cg, g);
-              store_f32x32(out0 + r * args.ld0 + cl, l);
+              store_f32x16(out0 + r * args.ld0 + cg, g);
+              store_f32x16(out0 + r * args.ld0 + cl, l);
             }
-            const int f0 = ti.n0 / 2 + 32 * c;  // GLU feature of column cg
+            const int f0 = ti.n0 / 2 + 32 * c + hc;   // GLU feature of column cg
             if (f0 < args.f_real) {
-              if (out1) store_f32x32(out1 + r * args.ld1 + f0, a);
-              if (args.out1_t) store_t_f32x32(args.out1_t, cap, f0, r, a);
+              if (out1) store_f32x16(out1 + r * args.ld1 + f0, a);
+              if (args.out1_t) store_t_f32x16(args.out1_t, cap, f0, r, a);
             }
           }
         } else if (MODE == kFc1Act || MODE == kFc2 || MODE == kDgradFc1) {
           for (int c = 0; c < TN / 32 && ti.n0 + 32 * c < args.n_ext; ++c) {
-            float h[32], a[32];
+            float h[16], a[16];
             acc_load(tbase + 32 * c, have, h);
-            const int col = ti.n0 + 32 * c;
+            const int col = ti.n0 + 32 * c + hc;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               h[i] = live ? h[i] + (bias ? bias[col + i] : 0.0f) : 0.0f;
               if (MODE == kFc1Act) a[i] = live ? srelu_fwd(h[i], ap) : 0.0f;
             }
-            if (out0) store_f32x32(out0 + r * args.ld0 + col, h);
+            if (out0) store_f32x16(out0 + r * args.ld0 + col, h);
             if (MODE == kFc1Act) {
-              if (out1) store_f32x32(out1 + r * args.ld1 + col, a);
-              if (args.out1_t) store_t_f32x32(args.out1_t, cap, col, r, a);
+              if (out1) store_f32x16(out1 + r * args.ld1 + col, a);
+              if (args.out1_t) store_t_f32x16(args.out1_t, cap, col, r, a);
             }
           }
         } else if (MODE == kDgradDglu) {
           // dA for GLU features n0.. ; dG / dL go to the packed columns of H
           for (int c = 0; c < TN / 32 && ti.n0 + 32 * c < args.n_ext; ++c) {
-            float da[32], g[32], l[32], dg[32], dl[32];
+            float da[16], g[16], l[16], dg[16], dl[16];
             acc_load(tbase + 32 * c, have, da);
-            const int f0 = ti.n0 + 32 * c;
+            const int f0 = ti.n0 + 32 * c + hc;
             const int cg = (f0 / kGluHalf) * 2 * kGluHalf + f0 % kGluHalf, cl = cg + kGluHalf;
             if (live) {
-              load_f32x32(aux + r * args.ld_aux + cg, g);
-              load_f32x32(aux + r * args.ld_aux + cl, l);
+              load_f32x16(aux + r * args.ld_aux + cg, g);
+              load_f32x16(aux + r * args.ld_aux + cl, l);
             }
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < 16; ++i) {
               if (live) {
                 glu_bwd<ACT>(da[i], g[i], l[i], ap, dg[i], dl[i]);
               } else {
@@ -364,24 +366,24 @@ __global__ void __launch_bounds__(T_THREADS, 1)
               }
             }
             if (out0) {
-              store_f32x32(out0 + r * args.ld0 + cg, dg);
-              store_f32x32(out0 + r * args.ld0 + cl, dl);
+              store_f32x16(out0 + r * args.ld0 + cg, dg);
+              store_f32x16(out0 + r * args.ld0 + cl, dl);
             }
             if (args.out0_t) {
-              store_t_f32x32(args.out0_t, cap, cg, r, dg);
-              store_t_f32x32(args.out0_t, cap, cl, r, dl);
+              store_t_f32x16(args.out0_t, cap, cg, r, dg);
+              store_t_f32x16(args.out0_t, cap, cl, r, dl);
             }
           }
         } else if (MODE == kDgradAct) {
           for (int c = 0; c < TN / 32 && ti.n0 + 32 * c < args.n_ext; ++c) {
-            float da[32], h[32], dh[32];
+            float da[16], h[16], dh[16];
             acc_load(tbase + 32 * c, have, da);
-            const int col = ti.n0 + 32 * c;
-            if (live) load_f32x32(aux + r * args.ld_aux + col, h);
+            const int col = ti.n0 + 32 * c + hc;
+            if (live) load_f32x16(aux + r * args.ld_aux + col, h);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) dh[i] = live ? srelu_bwd(da[i], h[i], ap) : 0.0f;
-            if (out0) store_f32x32(out0 + r * args.ld0 + col, dh);
-            if (args.out0_t) store_t_f32x32(args.out0_t, cap, col, r, dh);
+            for (int i = 0; i < 16; ++i) dh[i] = live ? srelu_bwd(da[i], h[i], ap) : 0.0f;
+            if (out0) store_f32x16(out0 + r * args.ld0 + col, dh);
+            if (args.out0_t) store_t_f32x16(args.out0_t, cap, col, r, dh);
           }
         }
       }
