@@ -775,9 +775,9 @@ def measure_fusion(torch, layer, K):
 def measure_router(torch, layer, x, logits, bias, reps=20):
     """Routing from given logits (the step's moe_route_permute) against the
     fused router, which computes the logits itself (router GEMM x W_r^T,
-    W_r seeded bf16 [E,d]) and takes the top-k in the GEMM epilogue, both
-    followed by the same permutation; each captured in a CUDA graph, CUDA
-    events around the replays, medians."""
+    W_r seeded bf16 [E,d]), takes the top-k in the GEMM epilogue and runs
+    the same permutation in the same launch; each captured in a CUDA graph,
+    CUDA events around the replays, medians."""
     g = torch.Generator(device="cpu").manual_seed(5)
     w_r = (torch.randn((layer.E, layer.d), generator=g) / layer.d ** 0.5).to(torch.bfloat16)
     w_r = w_r.to(x.device)
@@ -806,8 +806,8 @@ def measure_router(torch, layer, x, logits, bias, reps=20):
     layer.route(x, logits, bias)          # leave the step's routing in place
     torch.cuda.synchronize()
     return {"route_permute_ms": round(given, 4), "route_fused_ms": round(fused, 4),
-            "fused": "router GEMM x W_r^T + top-k/softmax/histogram epilogue, then the "
-                     "same scan/assign/gather"}
+            "fused": "one cooperative launch: router GEMM x W_r^T + top-k/softmax/histogram "
+                     "epilogue, then (after grid-wide barriers) the same scan/assign/gather"}
 
 
 def measure_overlap(torch, layer, reps=10):

@@ -241,8 +241,12 @@ moe_status_t moe_route_permute(const moe_mlp_desc_t* desc, const float* logits,
  * the GEMM epilogue, per token, the top-k of logit + bias (fp32, ties to the
  * lower expert, descending), the softmax of the selected raw logits and the
  * expert histogram -- the logits never go through HBM unless `logits`
- * (fp32 [T,E]) is given; then the scan, counting-sort assignment and gather
- * of moe_route_permute.  Outputs and workspace as in moe_route_permute.  The
+ * (fp32 [T,E]) is given; then, in the same launch, the scan, counting-sort
+ * assignment and gather of moe_route_permute (a cooperative launch: after
+ * the GEMM every CTA meets at grid-wide barriers whose waits end after a
+ * time limit with MOE_DEV_TIMEOUT; MOE_ERR_CUDA if the grid cannot be
+ * resident at once).  Outputs as in moe_route_permute; ws:
+ * moe_workspace_size() bytes (the histogram and the barrier counter).  The
  * selection is decided on the kernel's fp32 logits. */
 moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
                                      const void* w_router, const float* bias, float* logits,

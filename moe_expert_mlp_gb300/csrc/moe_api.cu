@@ -400,7 +400,9 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
       !tile_prefix || !row_src || !row_of || !x_perm)
     return MOE_ERR_NULL;
   if (desc->T > 0 && !ws) return MOE_ERR_NULL;
-  if (ws_bytes < route_ws_bytes(desc)) return MOE_ERR_WORKSPACE;
+  // the chunk histogram, then the grid-barrier counter of the routing tail
+  const size_t ctr_off = route_ws_bytes(desc);
+  if (ws_bytes < ctr_off + 256) return MOE_ERR_WORKSPACE;
   DeviceInfo* di;
   if ((st = device_info(&di)) != MOE_OK) return st;
   const int T = desc->T, E = desc->E, k = desc->k;
@@ -409,8 +411,12 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
   int32_t* chunk = static_cast<int32_t*>(ws);
   cudaError_t e = cudaMemsetAsync(row_src, 0xFF, sizeof(int32_t) * desc->capacity, stream);
   if (e == cudaSuccess && T > 0) {
+    unsigned int* grid_ctr = reinterpret_cast<unsigned int*>(static_cast<uint8_t*>(ws) + ctr_off);
     e = cudaMemsetAsync(chunk, 0, sizeof(int32_t) * nchunks * E, stream);
-    // logits = x W_r^T on the tensor cores, top-k + softmax + histogram in the epilogue
+    if (e == cudaSuccess) e = cudaMemsetAsync(grid_ctr, 0, sizeof(unsigned int), stream);
+    // one cooperative launch: logits = x W_r^T on the tensor cores, top-k +
+    // softmax + histogram in the epilogue, then (after grid-wide barriers)
+    // the group tables, the row assignment and the gather of x_perm
     GemmArgs g;
     memset(&g, 0, sizeof(g));
     g.status = di->status;
@@ -430,19 +436,27 @@ moe_status_t moe_route_permute_fused(const moe_mlp_desc_t* desc, const void* x,
     g.r_w = topk_w;
     g.r_hist = chunk;
     g.r_logits = logits;
+    g.r_grid = grid_ctr;
+    g.r_counts = counts;
+    g.r_offsets = offsets;
+    g.r_padded = padded_offsets;
+    g.r_tiles = tile_prefix;
+    g.r_row_src = row_src;
+    g.r_row_of = row_of;
+    g.r_x = x;
+    g.r_x_perm = x_perm;
+    g.r_tokens = T;
+    g.r_vec_per_row = desc->d / 8;
+    g.r_capacity = desc->capacity;
+    g.r_nchunks = nchunks;
     if (e == cudaSuccess) e = launch_grouped_gemm(kRouter, g, grid_for(di, desc), stream);
+    return cuda_status(e);
   }
-  if (e == cudaSuccess) {
-    if (T > 0) {
-      e = launch_scan_assign(topk_idx, T, E, k, chunk, desc->capacity, counts, offsets,
-                             padded_offsets, tile_prefix, row_src, row_of, di->status, stream);
-    } else {
-      e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
-      if (e == cudaSuccess)
-        e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
-                                       tile_prefix, di->status, stream);
-    }
-  }
+  // no tokens: every group is empty
+  if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, sizeof(int32_t) * E, stream);
+  if (e == cudaSuccess)
+    e = launch_offsets_from_counts(counts, E, desc->capacity, offsets, padded_offsets,
+                                   tile_prefix, di->status, stream);
   if (e == cudaSuccess)
     e = launch_gather_rows(x, row_src, padded_offsets, E, desc->d, T, desc->capacity, x_perm,
                            di->sms, stream);

@@ -40,6 +40,7 @@
 #include "moe_internal.h"
 #include "moe_mx.cuh"
 #include "moe_ptx.cuh"
+#include "moe_route.cuh"
 
 namespace moe {
 
@@ -330,6 +331,38 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
     ti.num_kb = 0;  // filled by caller from K
   }
   return ti;
+}
+
+// The fused router's permutation, in the same launch as its logits GEMM
+// (a cooperative launch, every CTA resident): once all CTAs have written
+// their tokens' top-k choices and the per-chunk expert histogram (grid
+// barrier 1), each CTA assigns the rows of chunks blockIdx.x,
+// blockIdx.x + gridDim.x, ... with the first kTokensPerChunk threads (the
+// standalone scan_assign's arithmetic, its scratch in the now idle operand
+// stages); once every row source is known (grid barrier 2), all warps of
+// the grid gather x_perm row by row.
+__device__ __noinline__ void router_permute_tail(const GemmArgs& args, uint8_t* smem) {
+  __shared__ int s_gfail;
+  if (threadIdx.x == 0) s_gfail = 0;
+  if (!grid_sync(args.r_grid, gridDim.x, args.status, &s_gfail)) return;
+  AssignSmem& sm = *reinterpret_cast<AssignSmem*>(smem);
+  const int E = args.n_ext;
+  for (int c = blockIdx.x; c < args.r_nchunks; c += gridDim.x) {
+    if (threadIdx.x < kTokensPerChunk)
+      scan_assign_chunk(c, static_cast<int>(threadIdx.x), args.r_idx, args.r_tokens, E,
+                        args.topk, args.r_hist, args.r_nchunks, args.r_capacity, args.r_counts,
+                        args.r_offsets, args.r_padded, args.r_tiles, args.r_row_src,
+                        args.r_row_of, args.status, sm,
+                        [] { named_bar_sync(2, kTokensPerChunk); });
+    __syncthreads();                            // the scratch is reused by the next chunk
+  }
+  if (!grid_sync(args.r_grid, 2 * gridDim.x, args.status, &s_gfail)) return;
+  const int rows = min(__ldcg(args.r_padded + E), args.r_capacity);
+  const int warps = GEMM_THREADS / 32;
+  const int lane = threadIdx.x & 31;
+  for (int j = blockIdx.x * warps + (threadIdx.x >> 5); j < rows; j += gridDim.x * warps)
+    gather_row_warp(static_cast<const uint4*>(args.r_x), args.r_row_src, j, args.r_vec_per_row,
+                    args.r_tokens, static_cast<uint4*>(args.r_x_perm), lane);
 }
 
 template <int MODE, int ACT, int OP>
@@ -1262,6 +1295,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
     tc_fence_after();
     tmem_dealloc(tmem_base, TMEM_COLS);
   }
+  if constexpr (MODE == kRouter) {
+    if (args.r_grid != nullptr) router_permute_tail(args, smem);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1531,6 +1567,29 @@ cudaError_t launch_mode(const GemmArgs& args, int grid, cudaStream_t s) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
   if (err != cudaSuccess) return err;
+  if (MODE == kRouter && args.r_grid != nullptr) {
+    // the routing tail waits on every CTA: all of them must be resident
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_grouped_gemm<MODE, ACT, OP>,
+                                                        GEMM_THREADS, smem);
+    if (err != cudaSuccess) return err;
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess ||
+        (err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return err;
+    if (grid > per_sm * sms) return cudaErrorCooperativeLaunchTooLarge;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(GEMM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, k_grouped_gemm<MODE, ACT, OP>, args);
+  }
   k_grouped_gemm<MODE, ACT, OP><<<grid, GEMM_THREADS, smem, s>>>(args);
   return cudaGetLastError();
 }

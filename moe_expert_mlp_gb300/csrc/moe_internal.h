@@ -151,6 +151,24 @@ struct GemmArgs {
   float* r_w;
   int32_t* r_hist;
   float* r_logits;
+  // kRouter with the permutation in the same launch (a cooperative launch:
+  // after the logits GEMM every CTA meets at grid-wide barriers on r_grid, a
+  // counter zeroed before the launch; nullptr: top-k only): the group
+  // tables, the row maps and the gathered rows x_perm of the r_tokens bf16
+  // token rows r_x (r_vec_per_row 16-byte vectors each)
+  unsigned int* r_grid;
+  int32_t* r_counts;
+  int32_t* r_offsets;
+  int32_t* r_padded;
+  int32_t* r_tiles;
+  int32_t* r_row_src;
+  int32_t* r_row_of;
+  const void* r_x;
+  void* r_x_perm;
+  int r_tokens;
+  int r_vec_per_row;
+  int r_capacity;
+  int r_nchunks;
   // NVFP4 operands (launch_grouped_gemm_nv): per-tensor amax of the
   // quantized A and B operands; the epilogue scales the accumulator by
   // 1 / (g_a g_b), g = 2688 / amax (1 for amax 0)

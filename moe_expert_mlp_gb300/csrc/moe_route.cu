@@ -20,12 +20,11 @@
 #include "moe_internal.h"
 #include "moe_mx.cuh"
 #include "moe_ptx.cuh"
+#include "moe_route.cuh"
 
 namespace moe {
 
 namespace {
-
-constexpr int kWarps = kTokensPerChunk / 32;   // 8 warps per routing block
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -105,27 +104,6 @@ __global__ void __launch_bounds__(256) k_topk(
 }
 
 // ------------------------------------------------------------- scans
-// Serial scans of at most 256 experts by one thread: offsets, padded
-// offsets (groups start at multiples of kAlign) and the tile prefix.
-__device__ void scan_experts(const int32_t* cnt, int E, int capacity, int32_t* offsets,
-                             int32_t* padded_offsets, int32_t* tile_prefix, int* status) {
-  int o = 0, p = 0, tp = 0;
-  for (int e = 0; e < E; ++e) {
-    offsets[e] = o;
-    padded_offsets[e] = p;
-    tile_prefix[e] = tp;
-    const int c = cnt[e];
-    if (c < 0) set_status(status, MOE_DEV_BAD_OFFSETS);
-    o += c;
-    p += (c + kAlign - 1) / kAlign * kAlign;
-    tp += (c + kAlign - 1) / kAlign;
-  }
-  offsets[E] = o;
-  padded_offsets[E] = p;
-  tile_prefix[E] = tp;
-  if (p > capacity) set_status(status, MOE_DEV_BAD_OFFSETS);
-}
-
 __global__ void k_offsets_from_counts(const int32_t* __restrict__ counts, int E, int capacity,
                                       int32_t* offsets, int32_t* padded_offsets,
                                       int32_t* tile_prefix, int* status) {
@@ -136,89 +114,17 @@ __global__ void k_offsets_from_counts(const int32_t* __restrict__ counts, int E,
 }
 
 // ------------------------------------------- group offsets + stable assignment
-// One thread per token, one block per chunk.  Every block first reduces the
-// per-chunk expert histogram [nchunks][E] itself: the expert totals give the
-// padded group offsets, the chunks before its own give its base; block 0
-// also writes counts, offsets, padded offsets and the tile prefix for the
-// later kernels.  The row of (token t, expert e) is padded_offsets[e] +
-// (tokens of earlier chunks choosing e) + (earlier tokens of this chunk
-// choosing e), so rows inside a group ascend by token.  Ranks inside a warp
-// come from ballots, across warps from a shared prefix.
+// One thread per token, one block per chunk (scan_assign_chunk).
 __global__ void __launch_bounds__(kTokensPerChunk) k_scan_assign(
     const int32_t* __restrict__ topk_idx, int T, int E, int k,
     const int32_t* __restrict__ chunk_counts, int nchunks, int capacity,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
     int32_t* __restrict__ padded_offsets, int32_t* __restrict__ tile_prefix,
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_of, int* status) {
-  __shared__ int32_t s_wcnt[kWarps][kMaxExperts];
-  __shared__ int32_t s_base[kMaxExperts];
-  __shared__ int32_t s_tot[kMaxExperts];
-  __shared__ int32_t s_pad[kMaxExperts];
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int before = 0, total = 0;
-    for (int c = 0; c < nchunks; ++c) {
-      const int v = chunk_counts[static_cast<size_t>(c) * E + e];
-      before += c < static_cast<int>(blockIdx.x) ? v : 0;
-      total += v;
-    }
-    s_base[e] = before;
-    s_tot[e] = total;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int p = 0;
-    for (int e = 0; e < E; ++e) {
-      s_pad[e] = p;
-      p += (s_tot[e] + kAlign - 1) / kAlign * kAlign;
-    }
-    if (blockIdx.x == 0) {
-      for (int e = 0; e < E; ++e) counts[e] = s_tot[e];
-      scan_experts(s_tot, E, capacity, offsets, padded_offsets, tile_prefix, status);
-    }
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kTokensPerChunk + threadIdx.x;
-  const bool live = t < T;
-  uint64_t sel[kMaxExperts / 64] = {0, 0, 0, 0};
-  if (live) {
-    for (int s = 0; s < k; ++s) {
-      const int e = topk_idx[static_cast<size_t>(t) * k + s];
-      if (e < 0 || e >= E) {
-        set_status(status, MOE_DEV_BAD_EXPERT);
-        continue;
-      }
-      sel[e >> 6] |= 1ull << (e & 63);
-    }
-  }
-  const uint32_t lt_mask = (1u << lane) - 1u;
-  for (int e = 0; e < E; ++e) {
-    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
-    const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-    if (lane == 0) s_wcnt[warp][e] = __popc(b);
-  }
-  __syncthreads();
-  // exclusive prefix over warps, per expert
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = 0;
-    for (int w = 0; w < kWarps; ++w) {
-      const int v = s_wcnt[w][e];
-      s_wcnt[w][e] = run;
-      run += v;
-    }
-  }
-  __syncthreads();
-  for (int e = 0; e < E; ++e) {
-    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
-    const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-    if (has) {
-      const int rank = s_wcnt[warp][e] + __popc(b & lt_mask);
-      const int row = s_pad[e] + s_base[e] + rank;
-      row_src[row] = t;
-      for (int s = 0; s < k; ++s)
-        if (topk_idx[static_cast<size_t>(t) * k + s] == e) row_of[static_cast<size_t>(t) * k + s] = row;
-    }
-  }
+  __shared__ AssignSmem sm;
+  scan_assign_chunk(static_cast<int>(blockIdx.x), static_cast<int>(threadIdx.x), topk_idx, T, E,
+                    k, chunk_counts, nchunks, capacity, counts, offsets, padded_offsets,
+                    tile_prefix, row_src, row_of, status, sm, [] { __syncthreads(); });
 }
 
 // ---------------------------------------------------------- row gather
@@ -231,16 +137,8 @@ __global__ void __launch_bounds__(256) k_gather_rows(
     uint4* __restrict__ x_perm) {
   const int rows = min(padded_offsets[E], capacity);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8) {
-    const int t = row_src[j];
-    uint4* dst = x_perm + static_cast<size_t>(j) * vec_per_row;
-    if (t >= 0 && t < T) {
-      const uint4* src = x + static_cast<size_t>(t) * vec_per_row;
-      for (int c = lane; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
-    } else {
-      for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
-    }
-  }
+  for (int j = blockIdx.x * 8 + warp; j < rows; j += gridDim.x * 8)
+    gather_row_warp(x, row_src, j, vec_per_row, T, x_perm, lane);
 }
 
 __device__ __forceinline__ void unpack8(const uint4& w, float (&v)[8]) {

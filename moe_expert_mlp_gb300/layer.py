@@ -234,9 +234,9 @@ class MoEExpertMLP:
         return dict(qt=mx["qt"], scale_t=mx["scale_t"], layout="mma")
 
     def route_fused(self, x, w_router, bias=None, logits_out=None, stream=None, timer=None):
-        """Routing from the tokens themselves: router GEMM (x W_r^T) with the
-        top-k in its epilogue, then the same permutation as route();
-        w_router bf16 [E,d]; logits_out fp32 [T,E] or None."""
+        """Routing from the tokens themselves, in one launch: router GEMM
+        (x W_r^T) with the top-k in its epilogue, then the same permutation
+        as route(); w_router bf16 [E,d]; logits_out fp32 [T,E] or None."""
         self._x_row_fused = False
         with self._t(timer, "route_fused"):
             L.moe_route_permute_fused(self.desc, x, w_router, bias, logits_out, self.topk_idx,

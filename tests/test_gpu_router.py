@@ -1,5 +1,5 @@
-"""Fused router (router GEMM with the top-k in its epilogue) against the
-oracle.  The logits come from the tensor cores in fp32; they are checked
+"""Fused router (router GEMM with the top-k in its epilogue and the
+permutation in the same cooperative launch) against the oracle.  The logits come from the tensor cores in fp32; they are checked
 against the oracle's fp64 x W_r^T within the fp32 accumulation error, and
 the selection -- an integer decision taken in floating point -- is checked
 bit for bit against the oracle's routing applied to the kernel's own fp32
@@ -22,6 +22,9 @@ CASES = {
     "e64_k6_bias": (scaled(BASE, T=1000, d=512, F=128), True),
     "e40_k3_ragged": (scaled(BASE, T=777, E=40, k=3, d=320, F=64), True),
     "e200_k8": (scaled(BASE, T=300, E=200, k=8, d=256, F=64), False),
+    # more 256-token chunks (157) than CTAs: the in-launch assignment loops
+    "many_chunks": (scaled(BASE, T=40000, E=16, k=2, d=128, F=64), True),
+    "one_token": (scaled(BASE, T=1, E=8, k=2, d=128, F=64), False),
 }
 
 
@@ -80,3 +83,38 @@ def test_fused_router_equals_route_permute_on_its_logits():
         assert torch.equal(getattr(fused, n), getattr(plain, n)), n
     assert torch.equal(fused.x_perm.view(torch.int16), plain.x_perm.view(torch.int16))
     assert torch.allclose(fused.topk_w, plain.topk_w, rtol=1e-6, atol=1e-7)
+
+
+def test_fused_router_replays_in_a_cuda_graph():
+    """The cooperative launch is captured in a CUDA graph; replays give the
+    eager call's results bit for bit (the grid-barrier counter is zeroed by
+    a memset node of the same graph before every launch)."""
+    wl, _ = CASES["e40_k3_ragged"]
+    inp = make_inputs(wl, with_weights=False)
+    rng = np.random.default_rng(9)
+    wr = H.bits_to_dev(f32_to_bf16_bits(
+        (rng.standard_normal((wl.E, wl.d)) / np.sqrt(wl.d)).astype(np.float32)))
+    bias = torch.from_numpy(rng.standard_normal(wl.E).astype(np.float32)).cuda()
+    x = H.bits_to_dev(inp["x"])
+    eager = H.make_layer(wl)
+    eager.route_fused(x, wr, bias)
+    torch.cuda.synchronize()
+    layer = H.make_layer(wl)
+    layer.route_fused(x, wr, bias)              # warm-up outside the capture
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            layer.route_fused(x, wr, bias, stream=s)
+    for n in ("topk_idx", "counts", "padded_offsets", "row_src", "row_of", "x_perm"):
+        getattr(layer, n).zero_()
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    for n in ("topk_idx", "counts", "offsets", "padded_offsets", "tile_prefix", "row_src",
+              "row_of"):
+        assert torch.equal(getattr(layer, n), getattr(eager, n)), n
+    assert torch.equal(layer.x_perm.view(torch.int16), eager.x_perm.view(torch.int16))
