@@ -102,23 +102,30 @@ class GroupedHostStepPipeline:
     library's padded device layout (each group starting at a multiple of 128
     rows), so no padding row crosses the host link; padding rows of the
     device buffers are kept zero (they are cleared whenever the group sizes,
-    and with them the layout, change).  The layer alternates between two
-    sets of per-row device buffers, so no device-side staging copy is
-    needed: the inputs of step i+1 are copied into the other set while step
-    i computes, and the results of step i go to the host while step i+1
-    computes; step i+2 waits for both before it reuses the set.
+    and with them the layout, change).  The layer cycles through `depth`
+    sets of per-row device buffers (default two), so no device-side staging
+    copy is needed: the inputs of the next depth-1 steps stream in while a
+    step computes, and each step's results go to the host while the
+    following steps compute; step i+depth waits for both before it reuses
+    step i's set.  (Where the host link, not the kernels, sets the pace, a
+    third set does not shorten the step: both directions are already busy
+    all the time.)
     """
 
-    def __init__(self, layer, device=None):
+    def __init__(self, layer, device=None, depth=2):
+        if depth < 2:
+            raise ValueError("depth must be at least 2")
         self.layer = layer
         dev = torch.device(device) if device is not None else layer.w2.device
         cap, d, E = layer.capacity, layer.d, layer.E
         bf = layer.act_dtype
+        self.depth = depth
         self.sets = [dict(x_perm=layer.x_perm, dy=layer.dy, y=layer.y, dx_perm=layer.dx_perm)]
-        self.sets.append({k: torch.zeros((cap, d), dtype=bf, device=dev)
-                          for k in ("x_perm", "dy", "y", "dx_perm")})
-        self.layout = [None, None]               # group sizes each set was last laid out for
-        self.counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(2)]
+        for _ in range(depth - 1):
+            self.sets.append({k: torch.zeros((cap, d), dtype=bf, device=dev)
+                              for k in ("x_perm", "dy", "y", "dx_perm")})
+        self.layout = [None] * depth             # group sizes each set was last laid out for
+        self.counts = [torch.zeros(E, dtype=torch.int32, device=dev) for _ in range(depth)]
         self.h2d = torch.cuda.Stream(device=dev)
         self.d2h = torch.cuda.Stream(device=dev)
 
@@ -145,22 +152,23 @@ class GroupedHostStepPipeline:
         n = len(host_inputs)
         if n == 0:
             return
-        in_ready = [torch.cuda.Event() for _ in range(2)]
-        step_done = [torch.cuda.Event() for _ in range(2)]
-        out_copied = [torch.cuda.Event() for _ in range(2)]
+        D = self.depth
+        in_ready = [torch.cuda.Event() for _ in range(D)]
+        step_done = [torch.cuda.Event() for _ in range(D)]
+        out_copied = [torch.cuda.Event() for _ in range(D)]
         started = torch.cuda.Event()
         started.record(comp)
         segs = [None] * n
 
         def copy_in(i):
-            b = i % 2
+            b = i % D
             hin = host_inputs[i]
             key = tuple(int(c) for c in hin["counts"])
             segs[i] = self._segments(key)
             dev = self.sets[b]
             with torch.cuda.stream(self.h2d):
                 self.h2d.wait_event(started)
-                if i >= 2:                       # step i-2 was the set's last reader
+                if i >= D:                       # step i-D was the set's last reader
                     self.h2d.wait_event(step_done[b])
                 if self.layout[b] != key:        # new layout: padding rows back to zero
                     dev["x_perm"].zero_()
@@ -172,13 +180,14 @@ class GroupedHostStepPipeline:
                 self.counts[b].copy_(hin["counts"], non_blocking=True)
                 in_ready[b].record(self.h2d)
 
-        copy_in(0)
+        for i in range(min(D - 1, n)):
+            copy_in(i)
         for i in range(n):
-            b = i % 2
-            if i + 1 < n:
-                copy_in(i + 1)
+            b = i % D
+            if i + D - 1 < n:
+                copy_in(i + D - 1)
             comp.wait_event(in_ready[b])
-            if i >= 2:                           # results of step i-2 are on the host
+            if i >= D:                           # results of step i-D are on the host
                 comp.wait_event(out_copied[b])
             s = self.sets[b]
             layer.grouped_step(counts=self.counts[b], x_perm=s["x_perm"], dy=s["dy"], y=s["y"],
@@ -191,9 +200,8 @@ class GroupedHostStepPipeline:
                     hout["y"][src:src + m].copy_(s["y"][dst:dst + m], non_blocking=True)
                     hout["dx"][src:src + m].copy_(s["dx_perm"][dst:dst + m], non_blocking=True)
                 out_copied[b].record(self.d2h)
-        comp.wait_event(out_copied[(n - 1) % 2])
-        if n >= 2:
-            comp.wait_event(out_copied[(n - 2) % 2])
+        for i in range(max(0, n - D), n):
+            comp.wait_event(out_copied[i % D])
         # leave the layer on its own buffers
         s0 = self.sets[0]
         layer.x_perm, layer.dy, layer.y, layer.dx_perm = (s0["x_perm"], s0["dy"], s0["y"],

@@ -324,3 +324,24 @@ def test_dglu_with_in_kernel_recompute_matches_stored_h_kernel(name):
     assert torch.equal(dh_rec[:R_pad].view(torch.int16), layer.dh[:R_pad].view(torch.int16))
     for k in ("q", "scale", "qt", "scale_t", "amax"):
         assert torch.equal(mx_rec[k], mx_ref[k]), k
+
+
+def test_largest_routing_sizes():
+    """The largest routing problem the library is sized for in one call:
+    65536 tokens over 256 experts, top-8 (DeepSeek-V3's expert count and
+    top-k), 256 token chunks of the histogram; routing, offsets and the
+    permutation bit-exact, the layer's outputs and gradients within the bf16
+    bound."""
+    wl = scaled(BASE, T=65536, E=256, k=8, d=64, F=32)
+    inp = make_inputs(wl)
+    fwd, bwd = H.run_oracle_routed(wl, inp)
+    layer = H.run_gpu_routed(wl, inp)
+    from moe_expert_mlp_gb300 import moe_read_device_status
+    assert moe_read_device_status() == 0
+    _check_routing(layer, fwd, wl)
+    T = wl.T
+    H.assert_close("out", H.to_np(layer.out)[:T], fwd["out"])
+    H.assert_close("dx", H.to_np(layer.dx)[:T], bwd["dx"])
+    H.assert_close("dlogits", H.to_np(layer.dlogits)[:T], bwd["dlogits"])
+    H.assert_close("dW2", H.to_np(layer.dw2), bwd["dW2"])
+    H.assert_close("dW1", H.to_np(layer.unpack_fc1(layer.dw1p, wl.d)), bwd["dW1"])

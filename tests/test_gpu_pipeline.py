@@ -58,10 +58,10 @@ def _grouped_serial(layer, x, dy, counts):
     return y, dx
 
 
-@pytest.mark.parametrize("dtype", ["bf16", "mxfp8"])
-def test_grouped_pipeline_matches_serial_steps(dtype):
+@pytest.mark.parametrize("dtype,depth", [("bf16", 2), ("mxfp8", 2), ("bf16", 3)])
+def test_grouped_pipeline_matches_serial_steps(dtype, depth):
     """GroupedHostStepPipeline (real rows only, moved group by group into the
-    padded layout, two alternating buffer sets) == serial grouped steps, bit
+    padded layout, two or three buffer sets in turn) == serial grouped steps, bit
     for bit, over four batches whose group sizes change after the second
     (the padded layout changes, old rows must not leak into padding)."""
     from moe_expert_mlp_gb300.pipeline import GroupedHostStepPipeline
@@ -82,7 +82,7 @@ def test_grouped_pipeline_matches_serial_steps(dtype):
                           counts=torch.from_numpy(sizes).pin_memory()))
     outs = [dict(y=torch.empty((R, d), dtype=torch.bfloat16).pin_memory(),
                  dx=torch.empty((R, d), dtype=torch.bfloat16).pin_memory()) for _ in steps]
-    GroupedHostStepPipeline(layer).run(steps, outs)
+    GroupedHostStepPipeline(layer, depth=depth).run(steps, outs)
     torch.cuda.synchronize()
     for st, o in zip(steps, outs):
         y, dx = _grouped_serial(layer, st["x"], st["dy"], st["counts"])
