@@ -807,6 +807,12 @@ moe_status_t moe_route_permute_noalloc(const moe_mlp_desc_t* desc, const float* 
  * the context usable. */
 moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream);
 
+/* The same for the grid-wide barrier of the fused router's cooperative
+ * launch: one CTA arrives at a barrier that expects a second arrival nobody
+ * makes; after limit_us microseconds (1..5e6) the wait gives up, sets
+ * MOE_DEV_TIMEOUT and the kernel returns. */
+moe_status_t moe_selftest_grid_wait_timeout(uint32_t limit_us, cudaStream_t stream);
+
 /* Read (and optionally clear) the sticky device status word of the current
  * device.  Synchronises the device; call outside stream capture. */
 moe_status_t moe_read_device_status(int32_t* host_status, int32_t clear);

@@ -45,7 +45,7 @@ EXPORTS = (
     "moe_fc2_dgrad_dglu_recompute_mx", "moe_route_permute_mx", "moe_unpermute_combine_bwd_mx",
     "moe_transpose_weights_tf32", "moe_transpose_rows_f32", "moe_fc1_glu_fwd_tf32",
     "moe_fc2_fwd_tf32", "moe_fc2_dgrad_dglu_tf32", "moe_fc2_wgrad_tf32", "moe_fc1_dgrad_tf32",
-    "moe_fc1_wgrad_tf32",
+    "moe_fc1_wgrad_tf32", "moe_selftest_grid_wait_timeout",
 )
 
 
@@ -155,6 +155,7 @@ def lib():
             "moe_bias_grads": (ctypes.c_int, [D] + [P] * 7),
             "moe_route_permute_noalloc": (ctypes.c_int, [D] + [P] * 12 + [P]),
             "moe_selftest_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
+            "moe_selftest_grid_wait_timeout": (ctypes.c_int, [ctypes.c_uint32, P]),
             "moe_fc1_glu_fwd_unfused": (ctypes.c_int, [D] + [P] * 8),
             "moe_fc1_recompute_h": (ctypes.c_int, [D] + [P] * 7),
             "moe_fc2_dgrad_dglu_unfused": (ctypes.c_int, [D] + [P] * 8),
@@ -358,6 +359,10 @@ def moe_bias_grads(desc, dy, dh, counts, padded_offsets, db1p, db2, stream=None)
 
 def moe_selftest_wait_timeout(limit_us, stream=None):
     _check(lib().moe_selftest_wait_timeout(int(limit_us), _stream(stream)))
+
+
+def moe_selftest_grid_wait_timeout(limit_us, stream=None):
+    _check(lib().moe_selftest_grid_wait_timeout(int(limit_us), _stream(stream)))
 
 
 def moe_quantize_mx(x, colwise, q, scales, stream=None):

@@ -39,6 +39,20 @@ __global__ void k_wait_selftest(int* status, unsigned long long limit_ns) {
   if (threadIdx.x == 0) mbar_wait(&bar, 0, status, &abort_flag, limit_ns);
 }
 
+// One CTA arrives at a grid barrier that expects a second arrival nobody
+// makes (the fused router's barrier); the wait gives up after limit_ns and
+// records a timeout.
+__device__ unsigned int g_selftest_grid_ctr;
+
+__global__ void k_grid_wait_selftest(int* status, unsigned long long limit_ns) {
+  __shared__ int fail;
+  if (threadIdx.x == 0) {
+    fail = 0;
+    g_selftest_grid_ctr = 0;
+  }
+  grid_sync(&g_selftest_grid_ctr, 2u, status, &fail, limit_ns);
+}
+
 constexpr int kMaxDevices = 64;
 
 struct DeviceInfo {
@@ -972,6 +986,15 @@ moe_status_t moe_selftest_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
   moe_status_t st = device_info(&di);
   if (st != MOE_OK) return st;
   k_wait_selftest<<<1, 32, 0, stream>>>(di->status, 1000ull * limit_us);
+  return cuda_status(cudaGetLastError());
+}
+
+moe_status_t moe_selftest_grid_wait_timeout(uint32_t limit_us, cudaStream_t stream) {
+  if (limit_us == 0 || limit_us > 5000000) return MOE_ERR_SHAPE;
+  DeviceInfo* di;
+  moe_status_t st = device_info(&di);
+  if (st != MOE_OK) return st;
+  k_grid_wait_selftest<<<1, 64, 0, stream>>>(di->status, 1000ull * limit_us);
   return cuda_status(cudaGetLastError());
 }
 

@@ -86,11 +86,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
 
 // Grid-wide barrier of a cooperative launch (all CTAs resident): each CTA
 // arrives once on a zeroed counter and waits until `target` arrivals are
-// seen; the wait gives up after kWaitLimitNs, sets MOE_DEV_TIMEOUT and
+// seen; the wait gives up after limit_ns, sets MOE_DEV_TIMEOUT and
 // *s_fail (shared), and then the CTA skips later barriers.  Whole CTA
 // calls; returns false once this CTA has given up.
 __device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target, int* status,
-                                          volatile int* s_fail) {
+                                          volatile int* s_fail,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
   __syncthreads();
   if (threadIdx.x == 0 && *s_fail == 0) {
     __threadfence();
@@ -100,7 +101,7 @@ __device__ __forceinline__ bool grid_sync(unsigned int* ctr, unsigned int target
       unsigned int v;
       asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
       if (v >= target) break;
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit_ns) {
         set_status(status, MOE_DEV_TIMEOUT);
         *s_fail = 1;
         break;

@@ -27,6 +27,25 @@ def test_wait_timeout_sets_status_and_context_survives():
     assert torch.isfinite(layer.out.float()).all()
 
 
+def test_grid_barrier_timeout_sets_status_and_context_survives():
+    """The fused router's grid-wide barrier: a CTA waiting for an arrival
+    that never comes gives up after its limit, sets the timeout bit and
+    returns; the fused router then still runs correctly."""
+    import moe_expert_mlp_gb300 as m
+    assert m.moe_read_device_status(clear=True) == 0
+    m._lib.moe_selftest_grid_wait_timeout(50000)       # 50 ms, the second arrival never comes
+    assert m.moe_read_device_status(clear=True) & MOE_DEV_TIMEOUT
+    assert m.moe_read_device_status(clear=False) == 0
+    wl = scaled(WORKLOADS["bf16_t4096_e64"], T=300, E=8, k=2, d=128, F=64)
+    inp = make_inputs(wl, with_weights=False)
+    layer = H.make_layer(wl)
+    wr = torch.randn((wl.E, wl.d), device="cuda").to(torch.bfloat16)
+    layer.route_fused(H.bits_to_dev(inp["x"]), wr)
+    torch.cuda.synchronize()
+    assert m.moe_read_device_status() == 0
+    assert int(layer.counts.sum()) == wl.T * wl.k
+
+
 def test_inconsistent_offsets_are_detected_and_skipped():
     import moe_expert_mlp_gb300 as m
     wl = scaled(WORKLOADS["dsv3_r16384_e32"], R=300, E=4, d=128, F=64, zipf_empty=0)
