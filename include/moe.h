@@ -717,6 +717,11 @@ moe_status_t moe_fc2_dgrad_dglu_mx_unfused(const moe_mlp_desc_t* desc,
                                            const moe_mx_out_t* dh_mx, cudaStream_t stream);
 
 /* ------------------------------------------------------- fp32 / TF32 path
+ * The same routed-expert MLP ([FK] "Overcoming training bottlenecks in the
+ * MoE block": grouped GEMM + activation and + dActivation; "Optimizing GLU
+ * activations with fused GEMM epilogues", Figure 2: the repacked FC1 tile
+ * and its GLU epilogue; [DL] "Claims and evidence": ragged groups) on fp32
+ * tensors.
  * desc->dtype == MOE_DTYPE_FP32: the tensors of every call are fp32 (same
  * shapes, layouts, padding and packing as the bf16 path).  The routing,
  * permutation, combine and bias-gradient calls (moe_route_permute,
