@@ -135,3 +135,19 @@ def test_fp32_calls_reject_bad_arguments_without_gpu(libmoe):
     extra = (r(E * d * W1 * 4) + r(E * F * d * 4) + 2 * r(d * cap * 4) + r(F * cap * 4)
              + r(W1 * cap * 4))
     assert n_f32.value == r(n_bf16.value) + extra
+
+
+def test_header_and_c_caller_compile_as_c(libmoe, tmp_path):
+    """include/moe.h is plain C: the C caller of tests/c_abi (a whole layer
+    step on caller-owned device buffers) compiles as C99 with every warning
+    an error and links against libmoe.so and the CUDA runtime."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None or not os.path.isdir("/usr/local/cuda/include"):
+        pytest.skip("needs gcc and the CUDA headers")
+    from tests.test_gpu_c_abi import build_layer_step
+    exe = build_layer_step(str(tmp_path))
+    assert os.path.exists(exe)
+    r = subprocess.run(["nm", "-D", "--undefined-only", exe], capture_output=True, text=True)
+    for name in ("moe_route_permute", "moe_mlp_fwd", "moe_mlp_bwd", "moe_unpermute_combine"):
+        assert name in r.stdout, name
