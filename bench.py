@@ -155,14 +155,16 @@ def gemm_bytes(wl, name, R, dtype="bf16", keep_bf16=False):
     (1 + 1/32); the transposed copies the backward reads are the same size.
     Outputs: H, Y, dX and dW in bf16 (fp32 on the fp32 path); A and dH as
     their two MXFP8 copies on the MXFP8 path (plus the bf16 tensor when
-    keep_bf16), in bf16 otherwise, with the fp32 path's transposed A and dH
-    counted too."""
+    keep_bf16), in bf16 otherwise (NVFP4: bf16, quantized by later passes),
+    with the fp32 path's transposed A and dH counted too."""
     d, F, E = wl.d, wl.F, wl.E
     n1 = 2 * F if wl.gated else F
     q = {"bf16": 2.0, "mxfp8": 1.0 + 1.0 / 32, "nvfp4": 0.5 + 1.0 / 16, "fp32": 4.0}[dtype]
     o = 4.0 if dtype == "fp32" else 2.0                    # stored bf16 / fp32 element
-    if dtype in ("mxfp8", "nvfp4"):
+    if dtype == "mxfp8":
         act_out = 2 * q + (2.0 if keep_bf16 else 0.0)      # rowwise + transposed copies
+    elif dtype == "nvfp4":
+        act_out = 2.0            # bf16 (its NVFP4 copies come from separate passes)
     else:
         act_out = 2 * o if dtype == "fp32" else o          # fp32: plus the transposed copy
     b = {
