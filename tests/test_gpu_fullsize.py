@@ -7,7 +7,8 @@ reduction over its expert's rows.  Tolerances as in the small parity tests:
 max|gpu-ref| <= 1e-2 max|ref| + 1e-3 over the sampled values against the
 oracle with the same operand format (bf16, or MXFP8 quantized the same way);
 on the MXFP8 path also a relative Frobenius error <= 1e-1 against the
-unquantized oracle (the format's own error is 6-8 %).
+unquantized oracle (the format's own error is 6-8 %).  The fp32 layer (TF32
+GEMMs) is held to the bf16 bound against the plain oracle.
 """
 import numpy as np
 import pytest
@@ -21,7 +22,10 @@ pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
 
 CASES = [("bf16_t4096_e64", "bf16"), ("dsv3_r16384_e32", "bf16"), ("dsv3_r16384_e32", "mxfp8"),
-         ("gptoss_t16384_e32", "mxfp8"), ("dense_m16384", "bf16")]
+         ("gptoss_t16384_e32", "mxfp8"), ("dense_m16384", "bf16"),
+         # the fp32 layer (TF32 GEMMs) at the DeepSeek-shaped size, on the same
+         # (bf16-valued) inputs held in fp32
+         ("dsv3_r16384_e32", "fp32")]
 
 
 def _run_gpu(wl, inp, dtype):
@@ -34,10 +38,16 @@ def _run_gpu(wl, inp, dtype):
     sizes = inp["group_sizes"]
     cap = max(128, int(sum((int(m) + 127) // 128 * 128 for m in sizes)))
     layer = H.make_layer(wl, capacity=cap, dtype=dtype)
-    H.load_layer_weights(layer, inp)
+    f32 = dtype == "fp32"
+    dev = (lambda b: H.bits_to_dev(b).float()) if f32 else H.bits_to_dev
+    if f32:
+        opt = lambda b: dev(b) if b is not None else None
+        layer.load_weights(dev(inp["w1"]), opt(inp["b1"]), dev(inp["w2"]), opt(inp["b2"]))
+    else:
+        H.load_layer_weights(layer, inp)
     layer.set_groups(torch.from_numpy(sizes.astype(np.int32)).cuda())
     po = H.to_np(layer.padded_offsets)
-    xs, dys = H.bits_to_dev(inp["x"]), H.bits_to_dev(inp["dout"])
+    xs, dys = dev(inp["x"]), dev(inp["dout"])
     src = 0
     for e, m in enumerate(sizes):
         m = int(m)
