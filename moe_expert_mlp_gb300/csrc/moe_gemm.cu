@@ -899,7 +899,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         for (int j = 0; j < kGluHalf / 32; ++j) {
           tmem_ld_wait16(rg);
           reg_fence16(rl);
-          if (j == 1) early_release(acc);             // columns 0-63 read
           float g[16], l[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
@@ -913,6 +912,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           if (j + 1 < kGluHalf / 32) {        // next chunk's accumulator in flight
             tmem_ld16(tbase + 32 * (j + 1), rg);
             tmem_ld16(tbase + kGluHalf + 32 * (j + 1), rl);
+          }
+          if (j == 0) {                       // columns 0-63 read: the next tile may stage
+            tmem_ld_wait16(rg);               // its scales there before this chunk's work
+            reg_fence16(rl);
+            early_release(acc);
           }
           if (b1) {
             float bg[16], bl[16];
@@ -968,8 +972,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           tmem_ld_wait16(r);
 #pragma unroll
           for (int i = 0; i < 16; ++i) ra[i] = r[i];
-          if (j == 1) early_release(acc);             // columns 0-63 read
           if (j + 1 < nch_h) tmem_ld16(tbase + 32 * (j + 1), r);
+          if (j == 0) {                       // columns 0-63 read (chunk 1 waited for early)
+            tmem_ld_wait16(r);
+            early_release(acc);
+          }
           const int f0 = ti.n0 + 32 * j;
           const int c0 = (f0 / kGluHalf) * 2 * kGluHalf + (f0 % kGluHalf);
           const bool live = valid && f0 < args.f_real;
@@ -1018,6 +1025,10 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           for (int i = 0; i < 16; ++i)
             ra[i] = NV ? __float_as_uint(__uint_as_float(r[i]) * nv_alpha) : r[i];
           tmem_ld16(tbase + 32 * (j + 1), r);
+          if (j == 0) {                       // columns 0-63 read (chunk 1 waited for early)
+            tmem_ld_wait16(r);
+            early_release(acc);
+          }
           const bool live0 = valid && f0 < args.f_real;
           if (live0) dglu_compute16<ACT>(ra, hg[0], hl[0], ap, dg, dl);
           {
@@ -1046,7 +1057,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
             load_raw32(Hrow + c2 + hc + kGluHalf, hl[0]);
           }
           tmem_ld_wait16(r);
-          if (j == 0) early_release(acc);             // columns 0-63 read
 #pragma unroll
           for (int i = 0; i < 16; ++i)
             ra[i] = NV ? __float_as_uint(__uint_as_float(r[i]) * nv_alpha) : r[i];
