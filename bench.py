@@ -452,6 +452,40 @@ def workload_config(wl, dtype="bf16"):
 
 
 # --------------------------------------------------------------- GPU bench
+def run_quantize_only(args, wl):
+    """The MXFP8 activation quantizer alone (rowwise + transposed, scales in
+    the MMA layout) on a [routed rows, d] bf16 tensor of the workload: a
+    small-memory command for kernel profiles.  Prints one JSON line with the
+    kernel's CUDA-event time and its algorithmic bytes over that time."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from moe_expert_mlp_gb300 import _lib as L
+    rows, cols = wl.routed_rows, wl.d
+    torch.manual_seed(0)
+    x = torch.randn(rows, cols, device="cuda").to(torch.bfloat16)
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    out = dict(q=torch.empty((rows, cols), **u8),
+               scale=torch.empty(L.moe_mx_scale_bytes(rows, cols), **u8),
+               qt=torch.empty((cols, rows), **u8),
+               scale_t=torch.empty(L.moe_mx_scale_bytes(cols, rows), **u8), layout="mma")
+    for _ in range(args.warmup):
+        L.moe_quantize_mx_bf16(x, 1, rows, cols, out)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        L.moe_quantize_mx_bf16(x, 1, rows, cols, out)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(args.steps, 1)
+    nbytes = rows * cols * 2 + 2 * rows * cols * (1 + 1 / 32)   # bf16 in; codes + scales twice
+    print(json.dumps({"kernel": "mx_quantize", "rows": rows, "cols": cols, "ms": round(ms, 5),
+                      "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1), "steps": args.steps,
+                      "warmup": args.warmup, "l2": "no flush: input and outputs far above L2"}))
+    return 0
+
+
 def run_ours(args, wl):
     import torch
     import torch.distributed as dist
@@ -1048,6 +1082,9 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quantize-only", action="store_true",
+                    help="time only the MXFP8 activation quantizer on a [routed rows, d] "
+                         "tensor of the workload (a small-memory command for kernel profiles)")
     ap.add_argument("--no-fusion", action="store_true",
                     help="skip the fused-vs-unfused expert MLP comparison")
     args = ap.parse_args()
@@ -1065,6 +1102,8 @@ def main():
         wl = dataclasses.replace(wl, act=args.act)
     if args.impl == "reference":
         return run_reference(args, wl)
+    if args.quantize_only:
+        return run_quantize_only(args, wl)
     return run_ours(args, wl)
 
 

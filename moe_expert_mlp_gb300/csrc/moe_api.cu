@@ -262,6 +262,15 @@ void fill_common(GemmArgs& a, const moe_mlp_desc_t* d, const DeviceInfo* di,
 }  // namespace
 }  // namespace moe
 
+namespace moe {
+bool encode_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1,
+                   CUtensorMapSwizzle swizzle, CUtensorMapDataType dtype) {
+  return g_encode != nullptr &&
+         encode_map(map, base, d0, d1, d2, row_bytes, plane_bytes, box0, box1, swizzle, dtype);
+}
+}  // namespace moe
+
 using namespace moe;
 
 extern "C" {
@@ -1089,7 +1098,7 @@ moe_status_t moe_quantize_mx_bf16(const void* in, int64_t batch, int64_t rows, i
   if (st != MOE_OK) return st;
   return cuda_status(launch_quant_bf16_mx(in, batch, rows, cols, out->q, out->scale, out->qt,
                                           out->scale_t, out->layout == MOE_MX_SCALES_MMA,
-                                          nullptr, di->sms, stream));
+                                          nullptr, di->sms, di->status, stream));
 }
 
 moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int32_t width,
@@ -1110,7 +1119,7 @@ moe_status_t moe_quantize_act_mx(const moe_mlp_desc_t* desc, const void* in, int
   if ((st = device_info(&di)) != MOE_OK) return st;
   return cuda_status(launch_quant_bf16_mx(in, 1, desc->capacity, width, out->q, out->scale,
                                           out->qt, out->scale_t, 1, padded_offsets + desc->E,
-                                          di->sms, stream));
+                                          di->sms, di->status, stream));
 }
 
 moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p,
@@ -1124,10 +1133,10 @@ moe_status_t moe_quantize_weights_mx(const moe_mlp_desc_t* desc, const void* w1p
   const long long E = desc->E, d = desc->d, F = desc->F, Fp = fc1_pad(desc->F),
                  W1 = fc1_width(desc->act, desc->F);
   cudaError_t e = launch_quant_bf16_mx(w1p, E, W1, d, out->w1, out->w1_s, out->w1t,
-                                       out->w1t_s, 1, nullptr, di->sms, stream);
+                                       out->w1t_s, 1, nullptr, di->sms, di->status, stream);
   if (e == cudaSuccess)
     e = launch_quant_bf16_mx(w2, E, d, F, out->w2, out->w2_s, out->w2t, out->w2t_s, 1, nullptr,
-                             di->sms, stream);
+                             di->sms, di->status, stream);
   return cuda_status(e);
 }
 
@@ -1415,7 +1424,8 @@ moe_status_t moe_fc1_glu_fwd_mx_unfused(const moe_mlp_desc_t* desc, const moe_mx
   // 3. MXFP8 quantization of A, rowwise and transposed, as its own pass
   if (e == cudaSuccess)
     e = launch_quant_bf16_mx(a, 1, desc->capacity, desc->F, a_mx->q, a_mx->scale, a_mx->qt,
-                             a_mx->scale_t, 1, padded_offsets + desc->E, di->sms, stream);
+                             a_mx->scale_t, 1, padded_offsets + desc->E, di->sms, di->status,
+                             stream);
   return cuda_status(e);
 }
 
@@ -1456,7 +1466,7 @@ moe_status_t moe_fc2_dgrad_dglu_mx_unfused(const moe_mlp_desc_t* desc,
   if (e == cudaSuccess)
     e = launch_quant_bf16_mx(dh, 1, desc->capacity, static_cast<long long>(W1), dh_mx->q,
                              dh_mx->scale, dh_mx->qt, dh_mx->scale_t, 1,
-                             padded_offsets + desc->E, di->sms, stream);
+                             padded_offsets + desc->E, di->sms, di->status, stream);
   return cuda_status(e);
 }
 

@@ -202,7 +202,13 @@ cudaError_t launch_grouped_gemm_nv(int mode, const GemmArgs& args, int grid, cud
 cudaError_t launch_quant_bf16_mx(const void* in, long long batch, long long rows, long long cols,
                                  uint8_t* q, uint8_t* s, uint8_t* qt, uint8_t* st,
                                  int mma_layout, const int32_t* row_limit, int num_sms,
-                                 cudaStream_t stream);
+                                 int* status, cudaStream_t stream);
+// 3-D tensor map (moe_api.cu): dims innermost first, the innermost
+// contiguous, row_bytes / plane_bytes the strides of dims 1 and 2; false when
+// the driver rejects it (alignment, extents) or the encoder is not loaded yet.
+bool encode_map_3d(CUtensorMap* map, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                   uint64_t row_bytes, uint64_t plane_bytes, uint32_t box0, uint32_t box1,
+                   CUtensorMapSwizzle swizzle, CUtensorMapDataType dtype);
 // NVFP4 quantization (moe_nvfp4.cu): scale-buffer bytes of a [rows, cols]
 // operand; per-tensor plain and 16-row-Hadamard amax (zeroed first); the
 // rowwise / (rotated) transposed quantizer with encode amax pointers.

@@ -67,6 +67,39 @@ __device__ __forceinline__ uint8_t mx_quant32_words(const float (&v)[32], uint32
   return static_cast<uint8_t>(s + 127);
 }
 
+// max(|a|, |b|) per bf16 half (the sign bit of the result is not used)
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Block of 32 bf16 (value 2i in the low half of word i, 2i+1 in the high
+// half) -> eight words of E4M3 codes; returns the E8M0 scale code.  The
+// scale and the codes follow mx_quant32_words exactly: the block maximum is
+// taken on the bf16 magnitudes, which order like the values.
+__device__ __forceinline__ uint8_t mx_quant32_packed(const uint32_t (&w)[16], uint32_t (&c)[8]) {
+  uint32_t m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) m[i] = bf16x2_absmax(w[2 * i], w[2 * i + 1]);
+#pragma unroll
+  for (int k = 4; k >= 1; k >>= 1)
+#pragma unroll
+    for (int i = 0; i < k; ++i) m[i] = bf16x2_absmax(m[i], m[i + k]);
+  const uint32_t lo = m[0] & 0x7FFFu, hi = (m[0] >> 16) & 0x7FFFu;
+  const float amax = __uint_as_float((lo > hi ? lo : hi) << 16);
+  const int s = mx_scale_exponent(amax);
+  const float inv = mx_inv_scale(s);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const uint32_t a = w[2 * j], b = w[2 * j + 1];
+    const uint32_t c0 = e4m3x2(__uint_as_float(a << 16) * inv, __uint_as_float(a & 0xFFFF0000u) * inv);
+    const uint32_t c1 = e4m3x2(__uint_as_float(b << 16) * inv, __uint_as_float(b & 0xFFFF0000u) * inv);
+    c[j] = c0 | (c1 << 16);
+  }
+  return static_cast<uint8_t>(s + 127);
+}
+
 // Quantize one block of 32 values: writes 32 codes (16-byte aligned
 // destination) and returns the E8M0 scale code.
 __device__ __forceinline__ uint8_t mx_quant32(const float (&v)[32], uint8_t* q) {
@@ -124,21 +157,22 @@ __device__ __forceinline__ void mx_block_from_box(const MxOut& mx, const uint8_t
   if (mx.q) {
     // the lane's own row: four 16-byte chunks (the swizzle spreads the 8
     // rows of a quarter warp over distinct banks)
-    float v[32];
+    uint32_t w[16], c[8];
     const int r = row0 + lane;
     const uint4* rowp = reinterpret_cast<const uint4*>(box + r * 64);
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const uint4 c4 = rowp[q ^ ((r >> 1) & 3)];
-      const uint32_t w[4] = {c4.x, c4.y, c4.z, c4.w};
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        v[8 * q + 2 * k] = __uint_as_float(w[k] << 16);
-        v[8 * q + 2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-      }
+      w[4 * q] = c4.x;
+      w[4 * q + 1] = c4.y;
+      w[4 * q + 2] = c4.z;
+      w[4 * q + 3] = c4.w;
     }
     const long long row = r0 + lane;
-    const uint8_t sc = mx_quant32(v, mx.q + row * mx.width + col0);
+    const uint8_t sc = mx_quant32_packed(w, c);
+    uint4* dq = reinterpret_cast<uint4*>(mx.q + row * mx.width + col0);
+    dq[0] = make_uint4(c[0], c[1], c[2], c[3]);
+    dq[1] = make_uint4(c[4], c[5], c[6], c[7]);
     mx.s[mx.mma_layout ? sf_mma_offset(row, col0 / 32, sf_row_atoms(mx.cap))
                        : row * (mx.width / 32) + col0 / 32] = sc;
   }

@@ -70,6 +70,40 @@ def test_quantizer_mma_layout_bit_exact():
         assert np.count_nonzero(sbuf) <= n_used and np.count_nonzero(stbuf) <= n_used
 
 
+@pytest.mark.parametrize("direction", ["rows", "cols"])
+def test_quantizer_rowmajor_one_direction(direction):
+    """moe_quantize_mx_bf16 with row-major scales and only one of the two
+    outputs: rows x cols of 96 x 416 (a partial last tile in both
+    directions), a batch of two, values spanning 2^-40 .. 2^40 per row."""
+    from moe_expert_mlp_gb300 import _lib as L
+    rng = np.random.default_rng(17)
+    batch, rows, cols = 2, 96, 416
+    v = (rng.standard_normal((batch, rows, cols)) *
+         np.exp2(rng.integers(-40, 40, (batch, rows, 1)))).astype(np.float32)
+    bits = torch.from_numpy(v).to(torch.bfloat16)
+    vals = bits.float().numpy()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    if direction == "rows":
+        out = dict(q=torch.zeros((batch, rows, cols), **u8),
+                   scale=torch.zeros(batch * rows * cols // 32, **u8))
+    else:
+        out = dict(qt=torch.zeros((batch, cols, rows), **u8),
+                   scale_t=torch.zeros(batch * rows * cols // 32, **u8))
+    L.moe_quantize_mx_bf16(bits.cuda(), batch, rows, cols, out)
+    torch.cuda.synchronize()
+    for b in range(batch):
+        if direction == "rows":
+            q_ref, s_ref = oracle.mx_quantize_rows(vals[b])
+            assert np.array_equal(out["q"][b].cpu().numpy(), q_ref)
+            assert np.array_equal(out["scale"].cpu().numpy().reshape(batch, rows, cols // 32)[b],
+                                  s_ref)
+        else:
+            qt_ref, st_ref = oracle.mx_quantize_cols(vals[b])
+            assert np.array_equal(out["qt"][b].cpu().numpy(), qt_ref)
+            assert np.array_equal(
+                out["scale_t"].cpu().numpy().reshape(batch, cols, rows // 32)[b], st_ref)
+
+
 def _check_fused_mx(layer, name, x_bf16, mx, width):
     """Fused epilogue MXFP8 outputs (MMA layout) == oracle quantizer applied
     to the GPU's stored bf16 tensor."""
