@@ -195,15 +195,24 @@ __global__ void __launch_bounds__(256) k_gather_rows_mx(
     uint4* dst = x_perm + static_cast<size_t>(j) * vec_per_row;
     const uint4* src = x + static_cast<size_t>(real ? t : 0) * vec_per_row;
     uint8_t* q_row = q + static_cast<size_t>(j) * vec_per_row * 8;
-    for (int c0 = 0; c0 < vec_per_row; c0 += 32) {
-      const int c = c0 + lane;
-      const bool active = c < vec_per_row;
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (active && real) w = __ldg(src + c);
-      if (active) dst[c] = w;
-      float v[8];
-      unpack8(w, v);
-      mx_row_chunk(v, active, lane, q_row, sf, j, c, row_atoms);
+    // four 16-byte loads per lane in flight before the first is used
+    for (int c0 = 0; c0 < vec_per_row; c0 += 128) {
+      uint4 w[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int c = c0 + 32 * u + lane;
+        w[u] = c < vec_per_row && real ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (c0 + 32 * u >= vec_per_row) break;     // warp-uniform
+        const int c = c0 + 32 * u + lane;
+        const bool active = c < vec_per_row;
+        if (active) dst[c] = w[u];
+        float v[8];
+        unpack8(w[u], v);
+        mx_row_chunk(v, active, lane, q_row, sf, j, c, row_atoms);
+      }
     }
   }
 }

@@ -152,7 +152,16 @@ __device__ inline void gather_row_warp(const uint4* __restrict__ x,
   uint4* dst = x_perm + static_cast<size_t>(j) * vec_per_row;
   if (t >= 0 && t < T) {
     const uint4* src = x + static_cast<size_t>(t) * vec_per_row;
-    for (int c = lane; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
+    int c = lane;
+    for (; c + 96 < vec_per_row; c += 128) {       // four loads in flight per lane
+      const uint4 a = __ldg(src + c), b = __ldg(src + c + 32), d = __ldg(src + c + 64),
+                  e = __ldg(src + c + 96);
+      dst[c] = a;
+      dst[c + 32] = b;
+      dst[c + 64] = d;
+      dst[c + 96] = e;
+    }
+    for (; c < vec_per_row; c += 32) dst[c] = __ldg(src + c);
   } else {
     for (int c = lane; c < vec_per_row; c += 32) dst[c] = make_uint4(0, 0, 0, 0);
   }
