@@ -104,6 +104,70 @@ def test_quantizer_rowmajor_one_direction(direction):
                 out["scale_t"].cpu().numpy().reshape(batch, cols, rows // 32)[b], st_ref)
 
 
+def _edge_value_tensor(rows, cols, rng):
+    """bf16 values that exercise every decision of the block quantizer: all-
+    zero blocks, signed zeros, a block maximum exactly at a power of two and
+    just below one, values that saturate at 448 after scaling (the floor
+    scale leaves up to 2x headroom), E4M3 subnormals and the round-to-even
+    ties of the three-bit mantissa, the extremes of the bf16 range and
+    blocks of bf16 subnormals."""
+    v = rng.standard_normal((rows, cols)).astype(np.float32)
+    blocks = v.reshape(rows, cols // 32, 32)
+    kinds = rng.integers(0, 8, size=blocks.shape[:2])
+    for r in range(rows):
+        for b in range(cols // 32):
+            k, blk = kinds[r, b], blocks[r, b]
+            if k == 0:
+                blk[:] = 0.0
+                blk[::3] = -0.0
+            elif k == 1:                       # max exactly 2^e
+                blk *= 0.25
+                blk[rng.integers(32)] = np.float32(2.0 ** rng.integers(-30, 30))
+            elif k == 2:                       # max just below 2^(e+1): saturation
+                e = rng.integers(-30, 30)
+                blk[:] = np.float32(2.0 ** e) * np.float32(1.99) * np.sign(blk)
+            elif k == 3:                       # E4M3 subnormals after scaling
+                blk[:] = np.float32(2.0 ** -9) * rng.integers(-7, 8, size=32)
+                blk[0] = 256.0
+            elif k == 4:                       # ties: odd multiples of half a code step
+                blk[:] = np.float32(1.0 + (2 * rng.integers(0, 4, size=32) + 1) / 16.0)
+                blk[0] = 2.0
+            elif k == 5:                       # bf16 extremes
+                blk[:] = np.float32(3.0e38) * np.sign(blk)
+                blk[1] = np.float32(1e-38)
+            elif k == 6:                       # one huge value, the rest underflow
+                blk[:] = np.float32(1e-30) * blk
+                blk[5] = np.float32(1e10)
+            else:                              # bf16 subnormals only
+                blk[:] = np.float32(1e-39) * blk
+    return v
+
+
+def test_quantizer_edge_values_bit_exact():
+    """moe_quantize_mx_bf16 == the oracle quantizer on blocks built to hit
+    the scale rule's edges and the conversion's rounding and saturation
+    (rowwise and transposed, MMA scale layout, 256 x 384)."""
+    from moe_expert_mlp_gb300 import _lib as L
+    rng = np.random.default_rng(23)
+    rows, cols = 256, 384
+    bits = torch.from_numpy(_edge_value_tensor(rows, cols, rng)).to(torch.bfloat16)
+    vals = bits.float().numpy()
+    u8 = dict(dtype=torch.uint8, device="cuda")
+    sb, stb = L.moe_mx_scale_bytes(rows, cols), L.moe_mx_scale_bytes(cols, rows)
+    out = dict(q=torch.zeros((rows, cols), **u8), scale=torch.zeros(sb, **u8),
+               qt=torch.zeros((cols, rows), **u8), scale_t=torch.zeros(stb, **u8),
+               layout="mma")
+    L.moe_quantize_mx_bf16(bits.cuda(), 1, rows, cols, out)
+    torch.cuda.synchronize()
+    q_ref, s_ref = oracle.mx_quantize_rows(vals)
+    qt_ref, st_ref = oracle.mx_quantize_cols(vals)
+    assert np.array_equal(out["q"].cpu().numpy(), q_ref)
+    assert np.array_equal(out["qt"].cpu().numpy(), qt_ref)
+    assert np.array_equal(H.mma_scales_to_rowmajor(out["scale"].cpu().numpy(), rows, cols), s_ref)
+    assert np.array_equal(H.mma_scales_to_rowmajor(out["scale_t"].cpu().numpy(), cols, rows),
+                          st_ref)
+
+
 def _check_fused_mx(layer, name, x_bf16, mx, width):
     """Fused epilogue MXFP8 outputs (MMA layout) == oracle quantizer applied
     to the GPU's stored bf16 tensor."""
