@@ -341,6 +341,94 @@ __device__ __forceinline__ Tile decode_tile(int t, int n_tiles, int m_tiles, con
 // standalone scan_assign's arithmetic, its scratch in the now idle operand
 // stages); once every row source is known (grid barrier 2), all warps of
 // the grid gather x_perm row by row.
+// Fused router epilogue for one token (this lane's accumulator row at trow):
+// the top-k experts of logit + bias, ties to the lower expert, in descending
+// score, and the softmax of their raw logits.  The best LIST scores are kept
+// sorted in registers (static indices only): experts arrive in ascending
+// order and a candidate moves ahead of an entry only with a strictly larger
+// score, so equal scores keep the lower expert first; candidates not above
+// the current k-th score are skipped.  LIST >= args.topk.
+template <int LIST>
+__device__ __forceinline__ void router_topk_row(const GemmArgs& args, uint32_t trow, long long gr,
+                                                bool valid) {
+  const int Ec = args.n_ext, kk = args.topk;
+  float sv[LIST], lv[LIST];
+  int iv[LIST];
+#pragma unroll
+  for (int s = 0; s < LIST; ++s) {
+    sv[s] = -INFINITY;
+    lv[s] = 0.0f;
+    iv[s] = kMaxExperts + s;
+  }
+  float kth = -INFINITY;                      // score of slot kk-1
+#pragma unroll 1
+  for (int c0 = 0; c0 < Ec; c0 += 32) {
+    uint32_t r[32];
+    tmem_ld32(trow + c0, r);
+    tmem_ld_wait(r);
+    // the chunk fully unrolled: the accumulator registers keep static
+    // indices (a runtime index would put them in local memory)
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = c0 + i;
+      const float l = __uint_as_float(r[i]);
+      if (e < Ec && valid && args.r_logits) args.r_logits[gr * Ec + e] = l;
+      float cs = l + (args.r_bias && e < Ec ? __ldg(args.r_bias + e) : 0.0f);
+      if (!(e < Ec && cs > kth)) continue;     // also drops NaN and -inf
+      float cl = l;
+      int ci = e;
+#pragma unroll
+      for (int s = 0; s < LIST; ++s) {
+        if (cs > sv[s]) {
+          const float ts = sv[s], tl = lv[s];
+          const int ti = iv[s];
+          sv[s] = cs;
+          lv[s] = cl;
+          iv[s] = ci;
+          cs = ts;
+          cl = tl;
+          ci = ti;
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < LIST; ++s)
+        if (s == kk - 1) kth = sv[s];
+    }
+  }
+  if (!valid) return;
+  // slots [0, kk); unfilled ones (non-finite scores) keep their sentinel
+  float mx_l = -INFINITY;
+  bool short_list = false;
+#pragma unroll
+  for (int s = 0; s < LIST; ++s)
+    if (s < kk) {
+      if (iv[s] < Ec) mx_l = fmaxf(mx_l, lv[s]);
+      else short_list = true;
+    }
+  if (short_list) set_status(args.status, MOE_DEV_BAD_EXPERT);
+  float sum = 0.0f;
+#pragma unroll
+  for (int s = 0; s < LIST; ++s)
+    if (s < kk && iv[s] < Ec) sum += expf(lv[s] - mx_l);
+#pragma unroll
+  for (int s = 0; s < LIST; ++s) {
+    if (s < kk) {
+      const bool got = iv[s] < Ec;
+      const int e = got ? iv[s] : s;
+      args.r_idx[gr * kk + s] = e;
+      args.r_w[gr * kk + s] = got ? expf(lv[s] - mx_l) / sum : 0.0f;
+      atomicAdd(&args.r_hist[(gr / kTokensPerChunk) * Ec + e], 1);
+    }
+  }
+}
+
+// top-k beyond 8: the long list in a call of its own, so that its
+// registers do not weigh on the kernel's common path
+__device__ __noinline__ void router_topk_row_long(const GemmArgs& args, uint32_t trow,
+                                                  long long gr, bool valid) {
+  router_topk_row<kMaxTopK>(args, trow, gr, valid);
+}
+
 __device__ __noinline__ void router_permute_tail(const GemmArgs& args, uint8_t* smem) {
   __shared__ int s_gfail;
   if (threadIdx.x == 0) s_gfail = 0;
@@ -844,49 +932,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
         // over the E accumulator columns, ties to the lower expert, read 32
         // columns at a time; softmax of the selected raw logits
         if (half == 0) {
-          const int Ec = args.n_ext, kk = args.topk;
-          float sv[kMaxTopK], lv[kMaxTopK];
-          int iv[kMaxTopK];
-          int cnt = 0;
           const uint32_t trow = tbase - hc;
-#pragma unroll 1
-          for (int c0 = 0; c0 < Ec; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(trow + c0, r);
-            tmem_ld_wait(r);
-#pragma unroll 1
-            for (int i = 0; i < 32 && c0 + i < Ec; ++i) {
-              const int e = c0 + i;
-              const float l = __uint_as_float(r[i]);
-              if (valid && args.r_logits) args.r_logits[gr * Ec + e] = l;
-              const float sc = l + (args.r_bias ? args.r_bias[e] : 0.0f);
-              if (cnt == kk && !(sc > sv[kk - 1])) continue;
-              int pos = cnt < kk ? cnt : kk - 1;
-              while (pos > 0 && sc > sv[pos - 1]) {
-                sv[pos] = sv[pos - 1];
-                lv[pos] = lv[pos - 1];
-                iv[pos] = iv[pos - 1];
-                --pos;
-              }
-              sv[pos] = sc;
-              lv[pos] = l;
-              iv[pos] = e;
-              if (cnt < kk) ++cnt;
-            }
-          }
-          if (valid) {
-            if (cnt < kk) set_status(args.status, MOE_DEV_BAD_EXPERT);   // non-finite scores
-            float mx_l = -INFINITY;
-            for (int s_ = 0; s_ < cnt; ++s_) mx_l = fmaxf(mx_l, lv[s_]);
-            float sum = 0.0f;
-            for (int s_ = 0; s_ < cnt; ++s_) sum += expf(lv[s_] - mx_l);
-            for (int s_ = 0; s_ < kk; ++s_) {
-              const int e = s_ < cnt ? iv[s_] : s_;
-              args.r_idx[gr * kk + s_] = e;
-              args.r_w[gr * kk + s_] = s_ < cnt ? expf(lv[s_] - mx_l) / sum : 0.0f;
-              atomicAdd(&args.r_hist[(gr / kTokensPerChunk) * Ec + e], 1);
-            }
-          }
+          if (args.topk <= 8)
+            router_topk_row<8>(args, trow, gr, valid);
+          else
+            router_topk_row_long(args, trow, gr, valid);
         }
       } else if (MODE == kFc1Glu) {
         const __nv_bfloat16* b1 =

@@ -99,7 +99,10 @@ __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __re
   const int warp = tid >> 5, lane = tid & 31;
   const int t = chunk * NT + tid;
   const bool live = t < T;
-  uint64_t sel[kMaxExperts / 64] = {0, 0, 0, 0};
+  // the token's experts as a 256-bit mask in four scalars (a runtime index
+  // into an array would keep it in local memory)
+  static_assert(kMaxExperts == 256, "four 64-bit mask words");
+  uint64_t sel0 = 0, sel1 = 0, sel2 = 0, sel3 = 0;
   if (live) {
     for (int s = 0; s < k; ++s) {
       const int e = __ldcg(topk_idx + static_cast<size_t>(t) * k + s);
@@ -107,12 +110,22 @@ __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __re
         set_status(status, MOE_DEV_BAD_EXPERT);
         continue;
       }
-      sel[e >> 6] |= 1ull << (e & 63);
+      const uint64_t bit = 1ull << (e & 63);
+      const int w = e >> 6;
+      sel0 |= w == 0 ? bit : 0ull;
+      sel1 |= w == 1 ? bit : 0ull;
+      sel2 |= w == 2 ? bit : 0ull;
+      sel3 |= w == 3 ? bit : 0ull;
     }
   }
+  auto has_expert = [&](int e) {
+    const int w = e >> 6;
+    const uint64_t word = w == 0 ? sel0 : (w == 1 ? sel1 : (w == 2 ? sel2 : sel3));
+    return ((word >> (e & 63)) & 1ull) != 0;
+  };
   const uint32_t lt_mask = (1u << lane) - 1u;
   for (int e = 0; e < E; ++e) {
-    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
+    const bool has = has_expert(e);
     const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
     if (lane == 0) sm.wcnt[warp][e] = __popc(b);
   }
@@ -128,7 +141,7 @@ __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __re
   }
   sync();
   for (int e = 0; e < E; ++e) {
-    const bool has = (sel[e >> 6] >> (e & 63)) & 1ull;
+    const bool has = has_expert(e);
     const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
     if (has) {
       const int rank = sm.wcnt[warp][e] + __popc(b & lt_mask);
