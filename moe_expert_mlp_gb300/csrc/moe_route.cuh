@@ -44,6 +44,7 @@ __device__ inline void scan_experts(const int32_t* cnt, int E, int capacity, int
 
 // Shared scratch of one chunk's assignment (kTokensPerChunk / 32 warps).
 struct AssignSmem {
+  uint32_t bal[kTokensPerChunk / 32][kMaxExperts];   // per warp: lanes choosing e
   int32_t wcnt[kTokensPerChunk / 32][kMaxExperts];
   int32_t base[kMaxExperts];
   int32_t tot[kMaxExperts];
@@ -58,8 +59,10 @@ struct AssignSmem {
 // counts, offsets, padded offsets and the tile prefix.  The row of (token
 // t, expert e) is padded_offsets[e] + (tokens of earlier chunks choosing e)
 // + (earlier tokens of this chunk choosing e), so rows inside a group ascend
-// by token.  Ranks inside a warp come from ballots, across warps from a
-// shared prefix.
+// by token.  One pass over the experts records, per warp, the ballot of its
+// lanes choosing each expert; ranks inside a warp are popcounts of those
+// ballots below the lane, across warps a shared prefix, and each token then
+// places only its own k choices.
 template <typename Sync>
 __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __restrict__ topk_idx,
                                          int T, int E, int k,
@@ -127,7 +130,10 @@ __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __re
   for (int e = 0; e < E; ++e) {
     const bool has = has_expert(e);
     const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-    if (lane == 0) sm.wcnt[warp][e] = __popc(b);
+    if (lane == 0) {
+      sm.bal[warp][e] = b;
+      sm.wcnt[warp][e] = __popc(b);
+    }
   }
   sync();
   // exclusive prefix over warps, per expert
@@ -140,18 +146,16 @@ __device__ inline void scan_assign_chunk(int chunk, int tid, const int32_t* __re
     }
   }
   sync();
-  for (int e = 0; e < E; ++e) {
-    const bool has = has_expert(e);
-    const uint32_t b = __ballot_sync(0xFFFFFFFFu, has);
-    if (has) {
-      const int rank = sm.wcnt[warp][e] + __popc(b & lt_mask);
-      const int row = sm.pad[e] + sm.base[e] + rank;
-      row_src[row] = t;
-      // re-reads of this token's choices: the first read above went to L2,
-      // so these plain loads find the current values (and then L1)
-      for (int s = 0; s < k; ++s)
-        if (topk_idx[static_cast<size_t>(t) * k + s] == e) row_of[static_cast<size_t>(t) * k + s] = row;
-    }
+  if (!live) return;
+  // re-reads of this token's choices: the first read above went to L2, so
+  // these plain loads find the current values
+  for (int s = 0; s < k; ++s) {
+    const int e = topk_idx[static_cast<size_t>(t) * k + s];
+    if (e < 0 || e >= E) continue;                // recorded above
+    const int rank = sm.wcnt[warp][e] + __popc(sm.bal[warp][e] & lt_mask);
+    const int row = sm.pad[e] + sm.base[e] + rank;
+    row_src[row] = t;
+    row_of[static_cast<size_t>(t) * k + s] = row;
   }
 }
 
