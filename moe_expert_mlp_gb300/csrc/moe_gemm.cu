@@ -466,7 +466,6 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   __shared__ __align__(8) uint64_t tearly_bar[2];   // MX: first chunk of an accumulator read
   __shared__ uint32_t s_tmem_base;
   __shared__ int s_abort;
-  __shared__ int s_total;
   __shared__ int s_off[kMaxExperts + 1];
   __shared__ int s_order[kMaxExperts];
 
@@ -512,21 +511,14 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
   constexpr int TN = RC ? RC_N : BN;
   const int n_tiles = (args.n_ext + TN - 1) / TN;
   const int m_tiles = Tr::kRaggedK ? (args.m_ext + BM - 1) / BM : 0;
-  if (threadIdx.x == 0) {
-    // validate the offsets read from device memory; skip all work if bad
-    bool ok = s_off[0] == 0 && s_off[E] <= args.capacity;
-    for (int e = 0; e < E && ok; ++e) {
-      const int span = s_off[e + 1] - s_off[e];
-      ok = span >= 0 && (span % BM) == 0 && s_cnt[e] >= 0 && s_cnt[e] <= span;
-    }
-    if (!ok) {
-      set_status(args.status, MOE_DEV_BAD_OFFSETS);
-      s_total = 0;
-    } else if (Tr::kRaggedK) {
-      s_total = E * m_tiles * n_tiles;
-    } else {
-      s_total = (s_off[E] / BM) * n_tiles;
-    }
+  // validate the offsets and sizes read from device memory (one group per
+  // thread: a serial loop would chain one memory round trip per group);
+  // skip all work if any is bad
+  bool ok_e = true;
+  for (int e = threadIdx.x; e < E; e += GEMM_THREADS) {
+    const int span = s_off[e + 1] - s_off[e];
+    const int c = s_cnt[e];
+    ok_e = ok_e && span >= 0 && (span % BM) == 0 && c >= 0 && c <= span;
   }
   if (Tr::kRaggedK) {
     // largest group first; equal sizes keep expert order
@@ -537,10 +529,11 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
       s_order[rank] = e;
     }
   }
-  __syncthreads();
+  const bool ok = __syncthreads_and(ok_e) != 0 && s_off[0] == 0 && s_off[E] <= args.capacity;
+  if (!ok && threadIdx.x == 0) set_status(args.status, MOE_DEV_BAD_OFFSETS);
   tc_fence_after();
   const uint32_t tmem_base = s_tmem_base;
-  const int total = s_total;
+  const int total = !ok ? 0 : (Tr::kRaggedK ? E * m_tiles * n_tiles : (s_off[E] / BM) * n_tiles);
   const int kb_half = (args.K + Tr::kBK - 1) / Tr::kBK;   // K blocks of one GEMM
   const int kb_fixed = Tr::kRaggedK ? 0 : (RC ? 2 * kb_half : kb_half);
   volatile int* abort_flag = &s_abort;
