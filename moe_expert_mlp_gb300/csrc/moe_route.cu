@@ -241,16 +241,36 @@ __global__ void __launch_bounds__(256) k_zero_pad_rows(
 __global__ void __launch_bounds__(128) k_combine(
     const uint4* __restrict__ y, const int32_t* __restrict__ row_of,
     const float* __restrict__ w, int k, int vec_per_row, uint4* __restrict__ out) {
+  __shared__ int s_r[kMaxTopK];
+  __shared__ float s_w[kMaxTopK];
   const int t = blockIdx.x;
+  if (threadIdx.x < k) {
+    s_r[threadIdx.x] = row_of[static_cast<size_t>(t) * k + threadIdx.x];
+    s_w[threadIdx.x] = w ? w[static_cast<size_t>(t) * k + threadIdx.x] : 1.0f;
+  }
+  __syncthreads();
   for (int c = threadIdx.x; c < vec_per_row; c += blockDim.x) {
     float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-    for (int s = 0; s < k; ++s) {
-      const int r = row_of[static_cast<size_t>(t) * k + s];
-      const float ws = w ? w[static_cast<size_t>(t) * k + s] : 1.0f;
-      float v[8];
-      unpack8(__ldg(y + static_cast<size_t>(r) * vec_per_row + c), v);
+    // four slots' rows in flight at a time; accumulated in slot order
+    int s = 0;
+    for (; s + 4 <= k; s += 4) {
+      uint4 v4[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = fmaf(ws, v[i], acc[i]);
+      for (int u = 0; u < 4; ++u)
+        v4[u] = __ldg(y + static_cast<size_t>(s_r[s + u]) * vec_per_row + c);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        float v[8];
+        unpack8(v4[u], v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_w[s + u], v[i], acc[i]);
+      }
+    }
+    for (; s < k; ++s) {
+      float v[8];
+      unpack8(__ldg(y + static_cast<size_t>(s_r[s]) * vec_per_row + c), v);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(s_w[s], v[i], acc[i]);
     }
     out[static_cast<size_t>(t) * vec_per_row + c] = pack8(acc);
   }
@@ -262,7 +282,7 @@ __global__ void __launch_bounds__(128) k_combine_bwd(
     const uint4* __restrict__ dout, const uint4* __restrict__ y,
     const int32_t* __restrict__ row_of, const float* __restrict__ w, int k, int vec_per_row,
     uint4* __restrict__ dy, float* __restrict__ dw) {
-  __shared__ float s_part[4];
+  __shared__ float s_part[4][kMaxTopK];
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int s = 0; s < k; ++s) {
@@ -281,12 +301,13 @@ __global__ void __launch_bounds__(128) k_combine_bwd(
       dy[static_cast<size_t>(r) * vec_per_row + c] = pack8(o);
     }
     dot = warp_sum(dot);
-    if (lane == 0) s_part[warp] = dot;
-    __syncthreads();
-    if (threadIdx.x == 0)
-      dw[static_cast<size_t>(t) * k + s] = (s_part[0] + s_part[1]) + (s_part[2] + s_part[3]);
-    __syncthreads();
+    if (lane == 0) s_part[warp][s] = dot;            // each warp its own entries
   }
+  __syncthreads();                                  // one barrier per token
+  if (threadIdx.x < k)
+    dw[static_cast<size_t>(t) * k + threadIdx.x] =
+        (s_part[0][threadIdx.x] + s_part[1][threadIdx.x]) +
+        (s_part[2][threadIdx.x] + s_part[3][threadIdx.x]);
 }
 
 // The combine backward with the rowwise MXFP8 copy of each dY row it writes,
@@ -296,7 +317,7 @@ __global__ void __launch_bounds__(128) k_combine_bwd_mx(
     const int32_t* __restrict__ row_of, const float* __restrict__ w, int k, int vec_per_row,
     uint4* __restrict__ dy, float* __restrict__ dw, uint8_t* __restrict__ q,
     uint8_t* __restrict__ sf, long long row_atoms) {
-  __shared__ float s_part[4];
+  __shared__ float s_part[4][kMaxTopK];
   const int t = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   for (int s = 0; s < k; ++s) {
@@ -327,12 +348,13 @@ __global__ void __launch_bounds__(128) k_combine_bwd_mx(
       mx_row_chunk(ob, active, lane, q_row, sf, r, c, row_atoms);
     }
     dot = warp_sum(dot);
-    if (lane == 0) s_part[warp] = dot;
-    __syncthreads();
-    if (threadIdx.x == 0)
-      dw[static_cast<size_t>(t) * k + s] = (s_part[0] + s_part[1]) + (s_part[2] + s_part[3]);
-    __syncthreads();
+    if (lane == 0) s_part[warp][s] = dot;            // each warp its own entries
   }
+  __syncthreads();                                  // one barrier per token
+  if (threadIdx.x < k)
+    dw[static_cast<size_t>(t) * k + threadIdx.x] =
+        (s_part[0][threadIdx.x] + s_part[1][threadIdx.x]) +
+        (s_part[2][threadIdx.x] + s_part[3][threadIdx.x]);
 }
 
 // dlogits[t, idx[t,s]] = w_s * (dw_s - sum_s' w_s' dw_s'), zero elsewhere.
