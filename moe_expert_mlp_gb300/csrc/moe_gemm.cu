@@ -181,6 +181,28 @@ __device__ __forceinline__ void ring_store_half(StoreRing& ring, const float (&v
   ring.slot = ring.slot == NR - 1 ? 0 : ring.slot + 1;
 }
 
+// A whole output tile of zeros (a weight-gradient tile of an empty group):
+// one box is zeroed once and stored `nch` times along the tile's columns in
+// one bulk group, instead of staging and meeting once per box.
+template <int NR>
+__device__ __forceinline__ void ring_store_zero_tile(StoreRing& ring, const CUtensorMap* map,
+                                                     int x0, int nch, int y, int z, int row,
+                                                     int half, bool issuer) {
+  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;
+  const uint32_t raddr = buf + row * 64;
+  const uint4 zero = make_uint4(0, 0, 0, 0);
+  st_shared_v4(raddr + (2 * half) * 16, zero);
+  st_shared_v4(raddr + (2 * half + 1) * 16, zero);
+  fence_proxy_async_smem();
+  named_bar_sync(kEpiBar, kGemmEpiThreads);
+  if (issuer) {
+    for (int j = 0; j < nch; ++j) tma_store_3d(map, buf, x0 + 32 * j, y, z);
+    bulk_commit();
+    bulk_wait_read<NR - 2>();
+  }
+  ring.slot = ring.slot == NR - 1 ? 0 : ring.slot + 1;
+}
+
 // MXFP8 of a staged 32 x 32 block shared by the two warps of a lane quarter:
 // half 0 quantizes its rows, half 1 its columns.
 __device__ __forceinline__ void mx_block_half(const MxOut& mx, const uint8_t* box, int row0,
@@ -1216,9 +1238,12 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1) k_grouped_gemm(const __grid_c
           if (nch > 1) tmem_ld16(tbase + 32, rb);
         } else {
           early_release(acc);
+          if (write && MODE == kWgrad)
+            ring_store_zero_tile<Tr::kNR>(ring, &args.tma_out0, ti.n0, nch, y0, ti.e, row_local,
+                                          half, issuer);
         }
 #pragma unroll 1
-        for (int j = 0; j < nch; j += 2) {
+        for (int j = 0; j < nch && (has_acc || MODE != kWgrad); j += 2) {
           const bool two = j + 1 < nch;
           const int c0 = ti.n0 + 32 * j;
           float v0[16], v1[16];

@@ -249,6 +249,29 @@ def test_direct_groups_mxfp8_with_empty_experts():
         assert torch.count_nonzero(layer.dw1p[e]) == 0
 
 
+def test_empty_group_weight_gradients_are_written():
+    """The weight-gradient tiles of empty groups store zeros (one zeroed box
+    stored along the tile): buffers holding other values beforehand come
+    back zero for those experts and unchanged for the rest."""
+    wl = scaled(WORKLOADS["dsv3_r16384_e32"], R=700, E=9, d=256, F=192, zipf_empty=3)
+    inp = make_inputs(wl)
+    layer, ref = H.run_both_direct_mx(wl, inp)
+    dw1, dw2 = layer.dw1p.clone(), layer.dw2.clone()
+    layer.dw1p.fill_(3.0)
+    layer.dw2.fill_(-2.0)
+    layer.mlp_backward()
+    torch.cuda.synchronize()
+    empty = np.flatnonzero(ref["counts"] == 0)
+    assert empty.size > 0
+    for e in range(wl.E):
+        if e in empty:
+            assert torch.count_nonzero(layer.dw2[e]) == 0
+            assert torch.count_nonzero(layer.dw1p[e]) == 0
+        else:
+            assert torch.equal(layer.dw2[e], dw2[e])
+            assert torch.equal(layer.dw1p[e], dw1[e])
+
+
 def test_mxfp8_deterministic_bitwise():
     wl = ROUTED["gptoss_small"]
     inp = make_inputs(wl)
