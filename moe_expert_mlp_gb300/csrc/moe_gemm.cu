@@ -296,6 +296,25 @@ __device__ __forceinline__ void ring_store_pair(StoreRing& ring, const float (&v
   ring.slot = ring.slot == 2 * (NPAIRS - 1) ? 0 : ring.slot + 2;
 }
 
+// The pair kernel's zero tile (an empty group): one staged pair of zero
+// boxes stored along the tile's columns in one bulk group.
+__device__ __forceinline__ void ring_store_pair_zero_tile(StoreRing& ring, const CUtensorMap* map2,
+                                                          int n0, int nch, int y, int z, int row,
+                                                          int half, bool issuer) {
+  const float zero[16] = {0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0};
+  const uint32_t buf = ring.base + ring.slot * BOX_BYTES;
+  stage_box_half(buf, zero, false, row, half);
+  stage_box_half(buf + BOX_BYTES, zero, false, row, half);
+  fence_proxy_async_smem();
+  named_bar_sync(kEpiBar, kGemmEpiThreads);
+  if (issuer) {
+    for (int j = 0; j < nch; j += 2) tma_store_4d(map2, buf, 0, y, (n0 + 32 * j) / 32, z);
+    bulk_commit();
+    bulk_wait_read<1>();
+  }
+  ring.slot = ring.slot == 2 * (3 - 1) ? 0 : ring.slot + 2;
+}
+
 // bf16: the backward reads transposed operands MN-major from the forward's
 // buffers.  MXFP8 / NVFP4: every operand is K-major (the transposed copies
 // are quantized along the contraction dimension).
@@ -1585,9 +1604,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(GEMM_THREADS, 1)
       if (has_acc) {
         tmem_ld16(tbase, ra);
         if (nch > 1) tmem_ld16(tbase + 32, rb);
+      } else if (write) {
+        ring_store_pair_zero_tile(ring, &args.tma_out2, n0, nch, y0, e, row_local, half, issuer);
       }
 #pragma unroll 1
-      for (int j = 0; j < nch; j += 2) {
+      for (int j = 0; j < nch && has_acc; j += 2) {
         const bool two = j + 1 < nch;
         float v0[16], v1[16];
         if (has_acc) {

@@ -123,6 +123,20 @@ def test_direct_groups_with_empty_experts():
     for e in np.flatnonzero(ref["counts"] == 0):
         assert torch.count_nonzero(layer.dw2[e]) == 0
         assert torch.count_nonzero(layer.dw1p[e]) == 0
+    # ... written by the kernel (a zeroed box stored along each tile), not
+    # left from the buffers' initial zeros; the other experts unchanged
+    dw1, dw2 = layer.dw1p.clone(), layer.dw2.clone()
+    layer.dw1p.fill_(3.0)
+    layer.dw2.fill_(-2.0)
+    layer.mlp_backward()
+    torch.cuda.synchronize()
+    for e in range(wl.E):
+        if ref["counts"][e] == 0:
+            assert torch.count_nonzero(layer.dw2[e]) == 0
+            assert torch.count_nonzero(layer.dw1p[e]) == 0
+        else:
+            assert torch.equal(layer.dw2[e], dw2[e])
+            assert torch.equal(layer.dw1p[e], dw1[e])
 
 
 def test_dense_single_group():
