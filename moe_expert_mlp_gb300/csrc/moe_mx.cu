@@ -63,8 +63,8 @@ __global__ void __launch_bounds__(256) k_quant_cols(const float* __restrict__ in
 // memory into the code boxes; with the scales in the MMA layout each tile's
 // scales leave as one 512-byte atom per direction.  Rowwise codes
 // [batch][rows][cols]; columnwise codes transposed [batch][cols][rows].
-// Rows at or past *row_limit (when given; in every batch entry) are not
-// visited.
+// Tiles that start at or past *row_limit (when given; in every batch entry)
+// are not visited.
 constexpr int kQT = 128;                       // tile edge
 constexpr int kQThreads = 256;                 // 8 warps, two CTAs per SM
 constexpr int kQIn = 4 * 8192;                 // one bf16 input tile (four boxes)
