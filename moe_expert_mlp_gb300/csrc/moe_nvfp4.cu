@@ -47,16 +47,28 @@ __device__ __forceinline__ void fwht16(float (&v)[16]) {
       }
 }
 
-// One block of 16 values with encode scale g: returns the UE4M3 scale code
-// and the 16 E2M1 codes packed two per byte (element 2i in the low nibble).
-__device__ __forceinline__ uint8_t nv_quant16(const float (&v)[16], float g, uint2& codes) {
+// g / s for every non-negative UE4M3 scale code (s = the code's value; 0 for
+// s = 0), correctly rounded as the per-block division would be: the block
+// quantizer looks the factor up instead of dividing.  128 threads fill it.
+__device__ __forceinline__ void nv_inv_table(float* table, float g, int tid) {
+  if (tid < 128) {
+    const float s = __half2float(
+        __half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(tid), __NV_E4M3)));
+    table[tid] = s > 0.0f ? __fdiv_rn(g, s) : 0.0f;
+  }
+}
+
+// One block of 16 values with encode scale g (inv_of = its nv_inv_table):
+// returns the UE4M3 scale code and the 16 E2M1 codes packed two per byte
+// (element 2i in the low nibble).
+__device__ __forceinline__ uint8_t nv_quant16(const float (&v)[16], float g, const float* inv_of,
+                                              uint2& codes) {
   float m = 0.0f;
 #pragma unroll
   for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
   const float target = __fmul_rn(__fdiv_rn(m, 6.0f), g);
   const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(target, __NV_SATFINITE, __NV_E4M3);
-  const float s = __half2float(__half(__nv_cvt_fp8_to_halfraw(sc, __NV_E4M3)));
-  const float inv = s > 0.0f ? __fdiv_rn(g, s) : 0.0f;
+  const float inv = inv_of[sc & 0x7F];      // target >= 0: a non-negative, finite code
   uint32_t w[2] = {0u, 0u};
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
@@ -147,6 +159,9 @@ __global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __rest
   const long long rlim = row_limit ? __ldg(row_limit) : rows;
   const float g_row = q ? nv_encode_scale_q(amax_row) : 1.0f;
   const float g_col = qt ? nv_encode_scale_q(amax_col) : 1.0f;
+  __shared__ float inv_row[128], inv_col[128];
+  nv_inv_table(inv_row, g_row, tid);
+  nv_inv_table(inv_col, g_col, tid);           // visible after the tile loop's first barrier
   // the tile's 2048 16-byte chunks, eight per thread, are loaded one tile
   // ahead into registers so that the loads overlap the previous tile's work
   auto load_tile = [&](long long t, uint4 (&v)[8]) {
@@ -205,7 +220,7 @@ __global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __rest
           }
         }
         uint2 c;
-        const uint8_t sc = nv_quant16(v, g_row, c);
+        const uint8_t sc = nv_quant16(v, g_row, inv_row, c);
         *reinterpret_cast<uint2*>(code_r + r * 64 + blk * 8) = c;
         atom_r[(blk >> 2) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (blk & 3)] = sc;
       }
@@ -229,7 +244,7 @@ __global__ void __launch_bounds__(256, 3) k_quant_nv(const __nv_bfloat16* __rest
           for (int i = 0; i < 16; ++i) v[i] *= 0.25f;
         }
         uint2 cw;
-        const uint8_t sc = nv_quant16(v, g_col, cw);
+        const uint8_t sc = nv_quant16(v, g_col, inv_col, cw);
         *reinterpret_cast<uint2*>(code_c + c * 64 + ((rb ^ (c & 7)) * 8)) = cw;
         atom_c[(rb >> 2) * 512 + (c & 31) * 16 + ((c >> 5) & 3) * 4 + (rb & 3)] = sc;
       }
